@@ -1,0 +1,151 @@
+"""fp64 CPU oracle for the Memory Caching forward over linear memory.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline / reference leg may import this package.  The
+product library never loads it, and it shares no code with the CUDA path: the
+arithmetic lives in ``mc_oracle.c`` (plain C, double precision, one token at a
+time), compiled here with gcc and called through ctypes.
+
+Functions
+---------
+forward(q, k, v, u, seg_len, mode, topk=0, ...)
+    State form, literal: cached segment states, online state after the token's
+    update, key mean-pool gates, Residual / GRM / Soup / SSC aggregation.
+bruteforce(q, k, v, u, seg_len, mode, topk=0)
+    Token-level twin that never forms a memory matrix (tiny inputs only).
+
+Inputs are arrays of shape [B, H, L, d] in any real dtype; they are widened
+exactly to float64 (bf16 and fp32 values are exactly representable).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+RESIDUAL, GRM, SOUP, SSC = 0, 1, 2, 3
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mc_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile mc_oracle.c into oracle/_build/liboracle.so (IEEE semantics, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            u8 = ctypes.POINTER(ctypes.c_uint8)
+            i = ctypes.c_int
+            lib.mc_oracle_forward.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i,
+                                              u8, ip, dp, dp, ip, dp, i]
+            lib.mc_oracle_forward.restype = i
+            lib.mc_oracle_bruteforce.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, dp, i]
+            lib.mc_oracle_bruteforce.restype = i
+            _lib = lib
+    return _lib
+
+
+def _as_f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor: widen through float32 (exact for bf16)
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype)) if a is not None else None
+
+
+def num_segments(L: int, seg_len: int) -> int:
+    return (L + seg_len - 1) // seg_len
+
+
+def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
+            seg_mask=None, given_sel=None, nthreads: int = 0) -> dict:
+    """Run the state-form oracle.
+
+    Returns a dict with ``y`` [B,H,L,d] and ``states`` [B,H,N,d,d] (float64); for
+    SSC also ``sel`` [B,H,L,topk] int32 (rank order, -1 padded) and ``gap``
+    [B,H,L] (fp64 distance between the last selected and the best unselected
+    score; inf where nothing was left out).  ``seg_mask`` (length N, bool)
+    restricts which segments' outputs are computed; ``given_sel`` replaces the
+    router's choice for SSC.
+    """
+    lib = _load()
+    q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
+    if u.size == 0 and mode == RESIDUAL:
+        u = np.zeros_like(q)
+    B, H, L, d = q.shape
+    for a in (k, v, u):
+        if a.shape != q.shape:
+            raise ValueError("q, k, v, u must share the shape [B, H, L, d]")
+    N = num_segments(L, seg_len)
+    y = np.zeros((B, H, L, d), np.float64)
+    states = np.zeros((B, H, N, d, d), np.float64)
+    sel = gap = None
+    kk = max(topk, 0)
+    if mode == SSC:
+        sel = np.full((B, H, L, max(kk, 1)), -1, np.int32)
+        gap = np.full((B, H, L), np.inf, np.float64)
+    gs = None
+    if given_sel is not None:
+        gs = np.ascontiguousarray(np.asarray(given_sel, dtype=np.int32))
+        if gs.shape != (B, H, L, kk):
+            raise ValueError("given_sel must be [B,H,L,topk]")
+    sm = None
+    if seg_mask is not None:
+        sm = np.ascontiguousarray(np.asarray(seg_mask, dtype=np.uint8))
+        if sm.shape != (N,):
+            raise ValueError("seg_mask must have one entry per segment")
+    st = lib.mc_oracle_forward(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                               _ptr(v, ctypes.c_double), _ptr(u, ctypes.c_double),
+                               B * H, L, d, seg_len, mode, kk,
+                               _ptr(sm, ctypes.c_uint8), _ptr(gs, ctypes.c_int32),
+                               _ptr(y, ctypes.c_double), _ptr(states, ctypes.c_double),
+                               _ptr(sel, ctypes.c_int32) if sel is not None else None,
+                               _ptr(gap, ctypes.c_double) if gap is not None else None,
+                               nthreads)
+    if st != 0:
+        raise RuntimeError(f"mc_oracle_forward failed with status {st}")
+    out = {"y": y, "states": states}
+    if mode == SSC:
+        out["sel"] = sel[..., :kk]
+        out["gap"] = gap
+    return out
+
+
+def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0) -> np.ndarray:
+    """Token-level twin: y [B,H,L,d] without forming any memory matrix (O(L^2 d))."""
+    lib = _load()
+    q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
+    B, H, L, d = q.shape
+    y = np.zeros((B, H, L, d), np.float64)
+    st = lib.mc_oracle_bruteforce(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                  _ptr(v, ctypes.c_double), _ptr(u, ctypes.c_double),
+                                  B * H, L, d, seg_len, mode, max(topk, 0),
+                                  _ptr(y, ctypes.c_double), nthreads)
+    if st != 0:
+        raise RuntimeError(f"mc_oracle_bruteforce failed with status {st}")
+    return y

@@ -1,0 +1,345 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- a hand-worked example, a closed form, a special case that reduces to
+a textbook routine (causal linear attention, gated token-level attention, a
+plain matrix product), an invariant of the mathematics, or brute force.
+
+Pages cited:
+  [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
+  [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
+           (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
+"""
+import os
+import re
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+from mc_inputs import GRM, RESIDUAL, SOUP, SSC, make_inputs
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _inputs(B, H, L, d, seed, dtype="f32"):
+    return [t.double().numpy() for t in make_inputs(B, H, L, d, seed, dtype)]
+
+
+def causal_la(q, k, v):
+    """Plain causal linear attention, y_t = sum_{j<=t} v_j (k_j . q_t) -- [MC-ja §2 eq. 2], phi = id, no 1/Z."""
+    L = q.shape[-2]
+    scores = np.einsum("...td,...jd->...tj", q, k)
+    scores = scores * np.tril(np.ones((L, L)))
+    return np.einsum("...tj,...jd->...td", scores, v)
+
+
+def blockwise_la(q, k, v, C):
+    """Causal linear attention restricted to each segment (block-diagonal causal mask)."""
+    L = q.shape[-2]
+    t = np.arange(L)
+    mask = (t[:, None] >= t[None, :]) & (t[:, None] // C == t[None, :] // C)
+    scores = np.einsum("...td,...jd->...tj", q, k) * mask
+    return np.einsum("...tj,...jd->...td", scores, v)
+
+
+def seg_number(L, C):
+    return (np.arange(L) // C + 1).astype(np.float64)
+
+
+# ---------------------------------------------------------------- worked example
+
+def _load_golden(name):
+    vals = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(":", 1)
+            vals[key.strip()] = np.array([float(x) for x in rest.split()], np.float64)
+    return vals
+
+
+def test_hand_worked_example():
+    """Hand-derived d=2 example (tests/golden/hand_example_d2.txt): Residual [MC-ja §3.1 eq. 7],
+    GRM [MC-ja §3.1 eq. 9-10], SSC [MC-sum §3.4], the cached states [MC-ja §3 eq. 4b]."""
+    g = _load_golden("hand_example_d2.txt")
+    q, k, v, u = (g[n].reshape(1, 1, 3, 2) for n in "qkvu")
+    res = oracle.forward(q, k, v, u, 2, RESIDUAL)
+    np.testing.assert_allclose(res["y"].reshape(-1), g["residual"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(res["states"][0, 0, 0].reshape(-1), g["state0"], atol=1e-12)
+    np.testing.assert_allclose(res["states"][0, 0, 1].reshape(-1), g["state1"], atol=1e-12)
+    for mode in (GRM, SOUP):
+        y = oracle.forward(q, k, v, u, 2, mode)["y"]
+        np.testing.assert_allclose(y.reshape(-1), g["grm"], rtol=0, atol=1e-12)
+    y0 = oracle.forward(q, k, v, u, 2, SSC, topk=0)["y"]
+    np.testing.assert_allclose(y0.reshape(-1), g["ssc_top0"], atol=1e-12)
+    y1 = oracle.forward(q, k, v, u, 2, SSC, topk=1)["y"]
+    np.testing.assert_allclose(y1.reshape(-1), g["ssc_top1"], atol=1e-12)
+
+
+# ---------------------------------------------------------------- states
+
+@pytest.mark.parametrize("L,C", [(96, 32), (100, 32), (64, 64), (50, 7)])
+def test_states_are_segment_gemms(L, C):
+    """Cached state of segment n is V_n^T K_n (a plain matrix product) [MC-ja §3 eq. 4b]."""
+    q, k, v, u = _inputs(2, 2, L, 8, 11)
+    st = oracle.forward(q, k, v, u, C, GRM)["states"]
+    N = (L + C - 1) // C
+    assert st.shape == (2, 2, N, 8, 8)
+    for n in range(N):
+        sl = slice(n * C, min(L, n * C + C))
+        ref = np.einsum("bhta,bhtc->bhac", v[:, :, sl], k[:, :, sl])
+        np.testing.assert_allclose(st[:, :, n], ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- collapse invariants
+
+@pytest.mark.parametrize("C", [128, 32, 8, 2, 37, 1])
+def test_residual_equals_causal_la_for_any_segmentation(C):
+    """Residual MC over a linear memory collapses to plain linear attention
+    ([MC-ja §3.1, GRM paragraph]; [MC-sum §3.1])."""
+    q, k, v, u = _inputs(1, 2, 128, 16, 1)
+    y = oracle.forward(q, k, v, u, C, RESIDUAL)["y"]
+    np.testing.assert_allclose(y, causal_la(q, k, v), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (SOUP, 0), (SSC, 3), (SSC, 0), (RESIDUAL, 0)])
+def test_single_segment_is_plain_recurrent_model(mode, topk):
+    """N = 1: nothing is cached, MC is the plain recurrent model [MC-sum §2.2]."""
+    q, k, v, u = _inputs(1, 2, 64, 16, 2)
+    for C in (64, 100):
+        y = oracle.forward(q, k, v, u, C, mode, topk)["y"]
+        np.testing.assert_allclose(y, causal_la(q, k, v), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("C", [16, 5])
+def test_grm_with_constant_gates(C):
+    """u = 0 gives equal gates 1/s over the s memories: y_t = LA_t / s_t
+    ([MC-ja §3.1]: constant gates make GRM the Residual variant, up to the softmax scale)."""
+    q, k, v, u = _inputs(1, 1, 80, 8, 3)
+    u = np.zeros_like(u)
+    y = oracle.forward(q, k, v, u, C, GRM)["y"]
+    ref = causal_la(q, k, v) / seg_number(80, C)[:, None]
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_one_token_segments_are_gated_attention():
+    """N = L: every token is its own segment, the pool of a one-token segment is its
+    key, and GRM becomes y_t = sum_{i<=t} softmax_i(u_t . k_i) v_i (k_i . q_t)
+    ([MC-sum §2.2 and §4.1]); written here as a dense masked softmax."""
+    q, k, v, u = _inputs(1, 2, 40, 8, 4)
+    y = oracle.forward(q, k, v, u, 1, GRM)["y"]
+    L = 40
+    logits = np.einsum("...td,...id->...ti", u, k)
+    logits = np.where(np.tril(np.ones((L, L), bool)), logits, -np.inf)
+    w = np.exp(logits - logits.max(-1, keepdims=True))
+    w /= w.sum(-1, keepdims=True)
+    kq = np.einsum("...td,...id->...ti", q, k)
+    ref = np.einsum("...ti,...id->...td", w * kq, v)
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("C", [16, 7])
+def test_soup_equals_grm_for_linear_memory(C):
+    """Memory Soup and GRM coincide for a linear memory ([MC-ja §3.1, SWLA paragraph];
+    [MC-sum §3.3]).  The oracle forms the soup matrix literally, so this is a real cross-check."""
+    q, k, v, u = _inputs(2, 1, 96, 8, 5)
+    a = oracle.forward(q, k, v, u, C, GRM)["y"]
+    b = oracle.forward(q, k, v, u, C, SOUP)["y"]
+    np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_ssc_limits():
+    """SSC with topk >= N-1 selects every cached memory (= GRM); topk = 0 keeps only the
+    online memory, i.e. linear attention inside each segment ([MC-sum §3.4])."""
+    q, k, v, u = _inputs(1, 2, 96, 8, 6)
+    C = 12
+    N = 8
+    grm = oracle.forward(q, k, v, u, C, GRM)["y"]
+    for kk in (N - 1, N + 5):
+        np.testing.assert_allclose(oracle.forward(q, k, v, u, C, SSC, kk)["y"], grm, rtol=1e-11, atol=1e-12)
+    y0 = oracle.forward(q, k, v, u, C, SSC, 0)["y"]
+    np.testing.assert_allclose(y0, blockwise_la(q, k, v, C), rtol=1e-10, atol=1e-12)
+
+
+def test_ssc_selection_matches_a_sort():
+    """The router's top-k ([MC-sum §3.4]) equals a stable sort of the fp32 scores, descending,
+    lower index first on ties; the pooled keys are plain means of each segment's keys."""
+    q, k, v, u = _inputs(1, 2, 120, 8, 7)
+    C, topk = 10, 3
+    out = oracle.forward(q, k, v, u, C, SSC, topk)
+    sel = out["sel"]
+    kbar = k.reshape(1, 2, 12, 10, 8).mean(axis=3)
+    for h in range(2):
+        for t in range(120):
+            s = t // C
+            r = (u[0, h, t] @ kbar[0, h, :s].T).astype(np.float32)
+            order = sorted(range(s), key=lambda i: (-r[i], i))[:topk]
+            got = [int(x) for x in sel[0, h, t] if x >= 0]
+            assert got == order, (h, t)
+
+
+def test_ssc_ties_go_to_lower_index():
+    """Equal router scores: the lower segment index wins (deterministic tie rule)."""
+    q, k, v, u = _inputs(1, 1, 40, 4, 8)
+    C = 10
+    k[0, 0, 10:20] = k[0, 0, 0:10]  # segments 0 and 1 have equal pooled keys
+    k[0, 0, 20:30] = -k[0, 0, 0:10]
+    out = oracle.forward(q, k, v, u, C, SSC, 1)
+    sel = out["sel"][0, 0, 30:40, 0]
+    kb0 = k[0, 0, 0:10].mean(0)
+    for j, t in enumerate(range(30, 40)):
+        r0 = np.float32(u[0, 0, t] @ kb0)
+        r2 = np.float32(u[0, 0, t] @ (-kb0))
+        assert sel[j] == (0 if r0 >= r2 else 2)
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+def test_causality(mode, topk):
+    """y_t depends on tokens j <= t only: changing later tokens leaves it unchanged.
+    (This pins the online pool to keys seen so far and the online memory to the
+    update before the read.)"""
+    q, k, v, u = _inputs(1, 1, 60, 8, 9)
+    C, t = 8, 27
+    a = oracle.forward(q, k, v, u, C, mode, topk)["y"]
+    q2, k2, v2, u2 = (x.copy() for x in (q, k, v, u))
+    rng = np.random.default_rng(0)
+    for x in (q2, k2, v2, u2):
+        x[..., t + 1:, :] = rng.standard_normal(x[..., t + 1:, :].shape)
+    b = oracle.forward(q2, k2, v2, u2, C, mode, topk)["y"]
+    np.testing.assert_array_equal(a[..., : t + 1, :], b[..., : t + 1, :])
+    assert not np.allclose(a[..., t + 1:, :], b[..., t + 1:, :])
+
+
+def test_linear_in_values():
+    """The gates do not depend on v, so y is linear in v."""
+    q, k, v, u = _inputs(1, 1, 48, 8, 10)
+    v2 = _inputs(1, 1, 48, 8, 12)[2]
+    C = 8
+    for mode, topk in ((GRM, 0), (SSC, 2)):
+        a = oracle.forward(q, k, v, u, C, mode, topk)["y"]
+        b = oracle.forward(q, k, v2, u, C, mode, topk)["y"]
+        c = oracle.forward(q, k, 2.0 * v - 3.0 * v2, u, C, mode, topk)["y"]
+        np.testing.assert_allclose(c, 2.0 * a - 3.0 * b, rtol=1e-10, atol=1e-10)
+
+
+def test_completed_segment_permutation():
+    """A cached segment enters only through its final state and its key mean, both
+    invariant to the order of its tokens; later outputs cannot see the order."""
+    q, k, v, u = _inputs(1, 1, 64, 8, 13)
+    C = 16
+    perm = np.random.default_rng(1).permutation(16)
+    q2, k2, v2, u2 = (x.copy() for x in (q, k, v, u))
+    for x in (q2, k2, v2, u2):
+        x[..., 0:16, :] = x[..., perm, :]
+    for mode in (GRM, SSC):
+        a = oracle.forward(q, k, v, u, C, mode, 1)["y"]
+        b = oracle.forward(q2, k2, v2, u2, C, mode, 1)["y"]
+        np.testing.assert_allclose(a[..., 16:, :], b[..., 16:, :], rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (SSC, 0)])
+@pytest.mark.parametrize("C", [16, 9, 1])
+def test_state_form_matches_token_level_twin(mode, topk, C):
+    """The state form equals the same sum regrouped by token (the twin never forms a memory)."""
+    q, k, v, u = _inputs(1, 2, 48, 8, 14)
+    a = oracle.forward(q, k, v, u, C, mode, topk)["y"]
+    b = oracle.bruteforce(q, k, v, u, C, mode, topk)
+    np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+def test_seg_mask_and_given_selection():
+    """Partial evaluation and an externally given SSC selection reproduce the full run."""
+    q, k, v, u = _inputs(1, 2, 64, 8, 15)
+    C = 8
+    full = oracle.forward(q, k, v, u, C, SSC, 2)
+    mask = np.zeros(8, bool)
+    mask[[2, 5]] = True
+    part = oracle.forward(q, k, v, u, C, SSC, 2, seg_mask=mask)
+    for n in (2, 5):
+        np.testing.assert_array_equal(part["y"][..., n * C:(n + 1) * C, :], full["y"][..., n * C:(n + 1) * C, :])
+    again = oracle.forward(q, k, v, u, C, SSC, 2, given_sel=full["sel"])
+    np.testing.assert_array_equal(again["y"], full["y"])
+
+
+# ---------------------------------------------------------------- the pins have teeth
+
+_MUTATIONS = [
+    # (description, regex pattern, replacement)
+    ("state transposed", r"M\[\(size_t\)a \* d \+ b\] \+= vt\[a\] \* kt\[b\];",
+     "M[(size_t)a * d + b] += vt[b] * kt[a];"),
+    ("online memory transposed", r"Mon\[\(size_t\)a \* d \+ b\] \+= vt\[a\] \* kt\[b\];",
+     "Mon[(size_t)a * d + b] += vt[b] * kt[a];"),
+    ("pool not averaged", r"kbar\[\(size_t\)n \* d \+ b\] /= \(double\)\(t1 - t0\);", ";"),
+    ("online pool over a wrong count", r"r\[s\] = dot\(ut, ksum, d\) / cnt;",
+     "r[s] = dot(ut, ksum, d) / (cnt + 1.0);"),
+    ("softmax sign", r"r\[i\] = exp\(r\[i\] - m\);", "r[i] = exp(m - r[i]);"),
+    ("online gate index", r"add_matvec\(yt, g\[s\], Mon, qt, d\);", "add_matvec(yt, g[0], Mon, qt, d);"),
+    ("dropped last cached term",
+     r"for \(int i = 0; i < s; \+\+i\) add_matvec\(yt, g\[i\]",
+     "for (int i = 0; i + 1 < s; ++i) add_matvec(yt, g[i]"),
+    ("residual drops cached", r"for \(int i = 0; i < s; \+\+i\) add_matvec\(yt, 1\.0,",
+     "for (int i = 1; i < s; ++i) add_matvec(yt, 1.0,"),
+    ("ssc ties to higher index", r"if \(best < 0 \|\| fi > bv\) \{ /\* strict",
+     "if (best < 0 || fi >= bv) { /* strict"),
+    ("soup uses online twice", r"Mstar\[e\] \+= g\[i\] \* Mi\[e\];", "Mstar[e] += g[s] * Mi[e];"),
+]
+
+
+def _run_pins_against(libpath):
+    """Re-run a representative subset of the pins against a mutated oracle build."""
+    import ctypes
+    saved = oracle._lib
+    try:
+        lib = ctypes.CDLL(libpath)
+        lib.mc_oracle_forward.argtypes = saved.mc_oracle_forward.argtypes
+        lib.mc_oracle_forward.restype = ctypes.c_int
+        lib.mc_oracle_bruteforce.argtypes = saved.mc_oracle_bruteforce.argtypes
+        lib.mc_oracle_bruteforce.restype = ctypes.c_int
+        oracle._lib = lib
+        pins = [
+            test_hand_worked_example,
+            lambda: test_states_are_segment_gemms(96, 32),
+            lambda: test_residual_equals_causal_la_for_any_segmentation(8),
+            lambda: test_one_token_segments_are_gated_attention(),
+            lambda: test_soup_equals_grm_for_linear_memory(7),
+            lambda: test_ssc_limits(),
+            lambda: test_ssc_ties_go_to_lower_index(),
+            lambda: test_causality(GRM, 0),
+            lambda: test_single_segment_is_plain_recurrent_model(GRM, 0),
+        ]
+        failed = 0
+        for p in pins:
+            try:
+                p()
+            except AssertionError:
+                failed += 1
+        return failed
+    finally:
+        oracle._lib = saved
+
+
+@pytest.mark.parametrize("desc,pat,rep", _MUTATIONS, ids=[m[0] for m in _MUTATIONS])
+def test_pins_catch_planted_mistake(desc, pat, rep):
+    """Plant one plausible mistake in a copy of the oracle (on the CPU) and check that at
+    least one pin fails."""
+    oracle._load()
+    src = open(oracle._SRC).read()
+    mutated, n = re.subn(pat, rep, src)
+    assert n >= 1, f"mutation pattern not found: {desc}"
+    tmpd = tempfile.mkdtemp(prefix="mc_oracle_mut_")
+    try:
+        csrc = os.path.join(tmpd, "m.c")
+        so = os.path.join(tmpd, "m.so")
+        with open(csrc, "w") as f:
+            f.write(mutated)
+        subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", csrc, "-o", so, "-lm"],
+                       check=True)
+        assert _run_pins_against(so) >= 1, f"no pin caught: {desc}"
+    finally:
+        shutil.rmtree(tmpd, ignore_errors=True)
