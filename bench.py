@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the Memory Caching forward on GB300.
+
+One step = one full forward (segment states, online reads, gates, cached
+readout, y) over one batch of synthetic input already resident in HBM.
+Default workload: long-context MC-GRM, B=1 H=16 L=65536 d=128 seg_len=1024
+(N=64), bf16 inputs, fp32 states.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) shard nothing: each
+rank runs its own copy of the workload (independent (batch, head) problems,
+no collective on the data path) and the value is all ranks' tokens over the
+slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import mc_inputs  # noqa: E402
+from mc_inputs import GRM, RESIDUAL, SSC  # noqa: E402
+
+METRIC = "tokens/sec MC-GRM forward (L=64K,d=128,N=64) on 1 GB300; % bf16 TC peak"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+SMS = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_GHZ = 2.07
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def segment_counts(w):
+    """Per-token (s_t = 1-based segment number, n_t = cached segments read)."""
+    C, L = w.seg_len, w.L
+    s = [t // C + 1 for t in range(L)]
+    if w.mode == RESIDUAL:
+        n = [0] * L  # linear memory: the cached sum collapses into one fixed memory
+    elif w.mode == SSC:
+        n = [min(w.topk, st - 1) for st in s]
+    else:
+        n = [st - 1 for st in s]
+    return s, n
+
+
+def algorithmic_flops(w):
+    """Per step, all heads: online write + read (4 d^2 per token), cached reads
+    (2 d^2 per token and cached segment read), gate scores (2 d per token and score)."""
+    s, n = segment_counts(w)
+    d = w.d
+    per_head_online = w.L * 4 * d * d
+    per_head_cached = 2 * d * d * sum(n)
+    per_head_gate = 0 if w.mode == RESIDUAL else 2 * d * sum(s)
+    bh = w.B * w.H
+    return {"total": bh * (per_head_online + per_head_cached + per_head_gate),
+            "online": bh * per_head_online,
+            "readout": bh * (per_head_cached + per_head_gate)}
+
+
+def algorithmic_bytes(w):
+    elt = 2 if w.dtype == "bf16" else 4
+    bh = w.B * w.H
+    n_in = 4 if w.mode != RESIDUAL else 3
+    return bh * (w.L * w.d * elt * (n_in + 1) + w.N * w.d * w.d * 4)
+
+
+# ----------------------------------------------------------------------------- peaks and clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return self
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return self
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, dist=None) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / (max_ms / 1e3)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, budget_s: float, steps_hint: int = 1):
+    """Time the fp64 oracle, as it stands, on a bounded sample of workload w:
+    heads 0..P-1 (P = host cores, capped at B*H), and S segments spread evenly
+    over the sequence (S chosen to fit the time budget), full d and L.  Returns
+    (tokens/s, cores, description)."""
+    import numpy as np
+    import oracle
+    cores = os.cpu_count() or 1
+    bh = min(cores, w.B * w.H)
+    q, k, v, u = mc_inputs.make_inputs(1, bh, w.L, w.d, w.seed, w.dtype)
+    q, k, v, u = (t.float().numpy() for t in (q, k, v, u))
+    picks = [w.N // 2] if w.N < 4 else [int((i + 0.5) * w.N / 4) for i in range(4)]
+    # probe with one segment, then size the sample to the budget
+    mask = np.zeros(w.N, bool)
+    mask[picks[0]] = True
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores)
+    t_one = time.perf_counter() - t0
+    nseg = max(1, min(len(picks), int(budget_s / max(t_one, 1e-3))))
+    chosen = picks[:nseg] if nseg < len(picks) else picks
+    mask = np.zeros(w.N, bool)
+    mask[chosen] = True
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores)
+    dt = time.perf_counter() - t0
+    ntok = sum(min(w.L, (n + 1) * w.seg_len) - n * w.seg_len for n in chosen)
+    # tokens/s in the metric's unit: a token is one sequence position across all H heads
+    rate = ntok * bh / dt / w.H
+    desc = (f"fp64 oracle, heads 0..{bh - 1} of B*H={w.B * w.H}, segments {chosen} of N={w.N} "
+            f"({ntok} positions x {bh} heads, all segment states computed), {dt:.1f} s wall; "
+            f"tokens/s = positions*heads/time/H")
+    return rate, cores, desc, dt
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import memory_caching_linear_gb300 as mcl
+    from memory_caching_linear_gb300 import build as mcbuild
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mcbuild.build()
+    mcl.load_library()
+
+    q, k, v, u = mc_inputs.workload_inputs(w, device=dev)
+    torch.cuda.synchronize()
+    y = torch.empty_like(q)
+    states = torch.empty((w.B, w.H, w.N, w.d, w.d), dtype=torch.float32, device=dev)
+    fwd = mcl.mc_forward if w.dtype == "bf16" else mcl.mc_forward_f32
+
+    def step():
+        fwd(q, k, v, u, w.seg_len, w.mode, w.topk, y=y, states=states)
+
+    # warm-up (at least W steps and ~1 s so the clocks settle under load)
+    sampler = ClockSampler(dev.index).start()
+    time.sleep(0.4)
+    t_w = time.perf_counter()
+    nwarm = 0
+    while nwarm < args.warmup or time.perf_counter() - t_w < 1.0:
+        step()
+        torch.cuda.synchronize()
+        nwarm += 1
+        if nwarm > 10000:
+            break
+
+    prof = mcl.KernelProfile(capacity=args.steps * 8 + 8)
+    stream = torch.cuda.current_stream()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with prof:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    max_ms = reduce_max(ms, dist if world > 1 else None)
+    value = aggregate(w.tokens, args.steps, max_ms, world)
+
+    per_kernel = prof.per_kernel_ms()
+    launches = prof.kernel_count()
+    peaks = measured_peaks()
+    flops = algorithmic_flops(w)
+
+    # dominant kernel and its roofline
+    dom = max(per_kernel.items(), key=lambda kv: sum(kv[1])) if per_kernel else (None, [])
+    dom_name, dom_ms = dom
+    roof = None
+    kernels_ms = {n: round(sum(t) / len(t), 4) for n, t in per_kernel.items()}
+    dtype_path = "f32"
+    if dom_name:
+        avg_ms = sum(dom_ms) / len(dom_ms)
+        tensor = "tc" in dom_name
+        dtype_path = "bf16" if tensor else "f32"
+        work = flops["readout"] if "readout" in dom_name else flops["online"]
+        achieved = work / (avg_ms / 1e3) / 1e12
+        if tensor:
+            sustained = max_ms > 1000.0
+            peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+            psrc = f"bf16 {'sustained' if sustained else 'burst'} ({peaks['source']})"
+            bound = "tensor"
+        else:
+            peak = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3
+            psrc = "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"
+            bound = "alu"
+        roof = {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom_name,
+                "launch_ms": round(avg_ms, 4), "algorithmic_tflop_per_launch": round(work / 1e12, 4),
+                "peak_source": psrc}
+
+    clocks = sampler.summary()
+    step_s = max_ms / 1e3 / args.steps
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": nwarm, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_path,
+        "data": "synthetic (seeded numpy normals: q,k unit rows, v ~ N(0,1), u ~ N(0,1)/sqrt(d))",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
+                   "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype,
+                   "l2": f"inputs {4 * w.B * w.H * w.L * w.d * (2 if w.dtype == 'bf16' else 4) / 2**30:.2f} GiB "
+                         f"> L2 129 MB, not flushed",
+                   "parallelism": f"replicas x{world} (independent (batch, head) problems)"},
+        "tc_fraction_of_bf16_peak": round(flops["total"] / step_s / 1e12 / peaks["bf16_tflops"], 4),
+        "algorithmic_tflop_per_step": round(flops["total"] / 1e12, 4),
+        "hbm_fraction": round(algorithmic_bytes(w) / step_s / 1e9 / peaks["hbm_gbs"], 4),
+        "roofline": roof,
+        "kernels_ms": kernels_ms,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    # end to end through the host-buffer entry point
+    if not args.no_e2e:
+        qh, kh, vh, uh = (t.cpu().pin_memory() for t in (q, k, v, u))
+        yh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        mcl.mc_forward_host(qh, kh, vh, uh, w.seg_len, w.mode, w.topk, y=yh)
+        ksteps = max(1, min(args.steps, 10))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(ksteps):
+            mcl.mc_forward_host(qh, kh, vh, uh, w.seg_len, w.mode, w.topk, y=yh)
+        e2e_ms = (time.perf_counter() - t0) * 1e3
+        e2e_max = reduce_max(e2e_ms, dist if world > 1 else None)
+        elt = 2 if w.dtype == "bf16" else 4
+        nin = 4 if w.mode != RESIDUAL else 3
+        res["e2e"] = {"value": round(aggregate(w.tokens, ksteps, e2e_max, world), 1), "unit": UNIT,
+                      "h2d_bytes_per_step": nin * q.numel() * elt, "d2h_bytes_per_step": y.numel() * elt,
+                      "steps": ksteps, "api": "mc_forward_host (pinned host buffers)"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc, _ = oracle_sample(w, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = {"value": round(rate, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc}
+    if world > 1:
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, budget_s=budget)
+    t0 = time.perf_counter()
+    rates = []
+    desc = ""
+    cores = os.cpu_count() or 1
+    for _ in range(args.steps):
+        rate, cores, desc, _ = oracle_sample(w, budget_s=budget)
+        rates.append(rate)
+    wall = time.perf_counter() - t0
+    value = statistics.median(rates)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same generator as the GPU arm)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
+                       "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+WORKLOADS = {"long-grm": mc_inputs.LONG_GRM, "grm-d64": mc_inputs.GRM_D64, "ssc": mc_inputs.SSC_D128,
+             "tiny": mc_inputs.TINY, **{f"sweep-c{w.seg_len}": w for w in mc_inputs.SWEEP}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long-grm")
+    ap.add_argument("--mode", choices=["residual", "grm", "soup", "ssc"], default=None,
+                    help="override the workload's aggregation")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.mode:
+        w = w.with_(mode={"residual": RESIDUAL, "grm": GRM, "soup": 2, "ssc": SSC}[args.mode])
+    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * mc.h -- C ABI of the Memory Caching (MC) forward pass over a linear
+ * matrix-valued memory, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (pages cited by title, section and equation):
+ *   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (Memory Caching:
+ *            RNNs with growing memory; news.neo-ai.one/ja/article/2519)
+ *   [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
+ *            (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
+ *
+ * Per (batch b, head h) the length-L sequence is cut into N = ceil(L/seg_len)
+ * segments of seg_len tokens (the last one may be shorter).  Each segment is
+ * compressed from a zero memory with M <- M + v_t k_t^T ([MC-ja §3 eq. 4b]) and
+ * its final d x d state is cached.  Token t of segment s reads the online memory
+ * M_t^(s) (after its own update) and every cached memory at q_t, and combines
+ * them with one of four aggregations:
+ *   MC_RESIDUAL  y_t = M_t^(s) q_t + sum_{i<s} M^(i) q_t                [MC-ja §3.1 eq. 7]
+ *   MC_GRM       y_t = g_{t,s} M_t^(s) q_t + sum_{i<s} g_{t,i} M^(i) q_t,
+ *                g_t = softmax_i <u_t, mean of segment i's keys>, the current
+ *                segment pooled over its keys up to t                  [MC-ja §3.1 eq. 9-10]
+ *   MC_SOUP      y_t = (g_{t,s} M_t^(s) + sum_{i<s} g_{t,i} M^(i)) q_t  [MC-sum §3.3]
+ *                (equal to GRM for a linear memory, and computed as GRM)
+ *   MC_SSC       R_t = the topk largest <u_t, pool_i>, i<s (fp32 scores, equal
+ *                scores to the lower i); softmax over R_t and the online score;
+ *                y_t = g_{t,s} M_t^(s) q_t + sum_{i in R_t} g_{t,i} M^(i) q_t   [MC-sum §3.4]
+ * There is no 1/Z normaliser and no softmax temperature.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense and row-major: q, k, v, u, y are [B][H][L][d];
+ *     states are [B][H][N][d][d] with states[..][n][a][c] = sum v[a] k[c]
+ *     over segment n (row = value dimension, column = key dimension).
+ *   - Pointers are DEVICE pointers (except mc_forward_host), allocated and owned
+ *     by the caller; the library keeps no reference after the call returns.
+ *     Every pointer must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (any stream, NULL = the legacy default
+ *     stream) and the call returns without synchronising.  Scratch is taken from
+ *     the stream-ordered allocator (cudaMallocAsync) and released on the same
+ *     stream.  Calls on different streams are independent.
+ *   - d must be 16, 32, 64 or 128.  B, H, L, seg_len >= 1.
+ *   - Return value: MC_OK (0) or a negative MC_ERR_* code.  On an argument
+ *     error nothing is enqueued.  On MC_ERR_CUDA the contents of y and states
+ *     are undefined; work already enqueued finishes on the stream.
+ */
+#ifndef MC_H_
+#define MC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared here so C callers need no CUDA headers. */
+typedef struct CUstream_st *mc_stream_t;
+
+typedef enum {
+    MC_RESIDUAL = 0,
+    MC_GRM = 1,
+    MC_SOUP = 2,
+    MC_SSC = 3
+} mc_agg_mode;
+
+enum {
+    MC_OK = 0,
+    MC_ERR_NULL = -1,           /* a required pointer is NULL */
+    MC_ERR_SHAPE = -2,          /* B,H,L,seg_len < 1, d not in {16,32,64,128}, or sizes overflow */
+    MC_ERR_MODE = -3,           /* agg_mode not one of mc_agg_mode */
+    MC_ERR_TOPK = -4,           /* SSC with topk < 0, or 64 < topk < N-1 */
+    MC_ERR_ALLOC = -5,          /* stream-ordered scratch allocation failed */
+    MC_ERR_CUDA = -6,           /* a CUDA runtime call or kernel launch failed */
+    MC_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait gave up */
+    MC_ERR_ALIGN = -8,          /* a pointer is not 16-byte aligned */
+    MC_ERR_DEVICE = -9          /* the current device is not a compute-capability 10.3 GPU */
+};
+
+/*
+ * mc_forward -- MC forward, bf16 inputs and output, fp32 state and accumulation.
+ *   q, k, v, u : bf16 [B][H][L][d], read only.  u may be NULL for MC_RESIDUAL.
+ *   seg_len    : constant segment length C; N = ceil(L / C).
+ *   agg_mode   : an mc_agg_mode value.
+ *   topk       : cached segments each token selects (MC_SSC only; ignored otherwise).
+ *                0 keeps only the online memory; topk >= N-1 selects every cached one.
+ *   y          : bf16 [B][H][L][d], written.
+ *   states     : fp32 [B][H][N][d][d], written with every segment's final state
+ *                (the cache, [MC-ja §3 after eq. 4b]); may be NULL, then the
+ *                states live in scratch only.
+ *   stream     : CUDA stream to enqueue on.
+ */
+int mc_forward(const void *q, const void *k, const void *v, const void *u,
+               int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+               void *y, float *states, mc_stream_t stream);
+
+/* mc_forward_f32 -- identical contract with fp32 q, k, v, u and y (fp32 arithmetic throughout). */
+int mc_forward_f32(const float *q, const float *k, const float *v, const float *u,
+                   int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                   float *y, float *states, mc_stream_t stream);
+
+/*
+ * mc_ssc_select -- the SSC router alone ([MC-sum §3.4]), for inspection and tests.
+ *   k, u     : [B][H][L][d], bf16 if is_bf16 != 0 else fp32, device.
+ *   idx      : int32 [B][H][L][topk], written: for token t of segment s, the
+ *              selected cached segments (indices < s) in rank order -- highest
+ *              fp32 score first, equal scores lower index first -- padded with -1
+ *              when s < topk.  The selection is the one mc_forward /
+ *              mc_forward_f32 use for MC_SSC on the same inputs.
+ *   topk     : 1..64.
+ */
+int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int seg_len,
+                  int topk, int32_t *idx, int is_bf16, mc_stream_t stream);
+
+/*
+ * mc_forward_host -- mc_forward / mc_forward_f32 on HOST buffers (end-to-end use).
+ *   Same arguments, but q, k, v, u, y and states (optional) are host pointers
+ *   (pinned memory gives asynchronous copies).  The call copies the inputs to
+ *   device memory it allocates on `stream`, runs the forward, copies y (and the
+ *   states when non-NULL) back, frees the device memory and synchronises
+ *   `stream` before returning.  is_bf16 selects the element type of q,k,v,u,y.
+ */
+int mc_forward_host(const void *q, const void *k, const void *v, const void *u,
+                    int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                    void *y, float *states, int is_bf16, mc_stream_t stream);
+
+/*
+ * Kernel-boundary timing, for benchmarks and profilers.
+ *   mc_profile_begin(events, capacity): `events` is a caller-owned array of
+ *     `capacity` cudaEvent_t handles (created by the caller).  From now on every
+ *     forward call records, on its own stream, one event before its first
+ *     kernel and one after each kernel it launches, filling the array in order;
+ *     recording stops silently when the array is full.
+ *   mc_profile_end(): stops recording and returns how many events were recorded.
+ *   mc_profile_stage(j): name of the kernel that ran between recorded event j
+ *     and event j+1 (NULL where j+1 opened a new call, or j is out of range).
+ * Process-wide state, not thread-safe; forward calls without an active
+ * profile record nothing.  Returns MC_OK / MC_ERR_NULL.
+ */
+int mc_profile_begin(void *const *events, int capacity);
+int mc_profile_end(void);
+const char *mc_profile_stage(int j);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char *mc_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MC_H_ */

@@ -1,0 +1,226 @@
+"""Memory Caching (MC) forward over a linear matrix-valued memory, for one GB300.
+
+Thin ctypes binding over the C ABI in ``include/mc.h`` (``libmc.so``, built
+in-tree by :mod:`memory_caching_linear_gb300.build`).  The functions below only
+check and marshal arguments; every step of the forward runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is not built, or the
+device is not an sm_103a GPU, calls raise.
+
+    y, states = mc_forward(q, k, v, u, seg_len, MC_GRM)
+
+q, k, v, u are CUDA tensors [B, H, L, d] (bf16 -> ``mc_forward``; fp32 ->
+``mc_forward_f32``).  Aggregations: MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC = 0, 1, 2, 3
+MC_OK = 0
+MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
+MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
+
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_ssc_select", "mc_forward_host", "mc_profile_begin",
+            "mc_profile_end", "mc_profile_stage", "mc_status_string")
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmc.so")
+_lib = None
+
+
+class MCError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {mc_status_string(status)} (status {status})")
+        self.status = status
+
+
+def load_library():
+    """Load libmc.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m memory_caching_linear_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.mc_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
+    lib.mc_forward.restype = i
+    lib.mc_forward_f32.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
+    lib.mc_forward_f32.restype = i
+    lib.mc_ssc_select.argtypes = [vp, vp, i, i, i, i, i, i, vp, i, vp]
+    lib.mc_ssc_select.restype = i
+    lib.mc_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, i, vp]
+    lib.mc_forward_host.restype = i
+    lib.mc_profile_begin.argtypes = [vp, i]
+    lib.mc_profile_begin.restype = i
+    lib.mc_profile_end.argtypes = []
+    lib.mc_profile_end.restype = i
+    lib.mc_profile_stage.argtypes = [i]
+    lib.mc_profile_stage.restype = ctypes.c_char_p
+    lib.mc_status_string.argtypes = [i]
+    lib.mc_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def mc_status_string(status: int) -> str:
+    return load_library().mc_status_string(int(status)).decode()
+
+
+def num_segments(L: int, seg_len: int) -> int:
+    return (L + seg_len - 1) // seg_len
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t, name, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+def _forward(fn_name, q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream):
+    lib = load_library()
+    dtype = q.dtype
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors (use mc_forward_host for host buffers)")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, dtype, (B, H, L, d), dev)
+    if u is not None:
+        _check(u, "u", dtype, (B, H, L, d), dev)
+    N = num_segments(L, seg_len)
+    if y is None:
+        y = torch.empty((B, H, L, d), dtype=dtype, device=dev)
+    _check(y, "y", dtype, (B, H, L, d), dev)
+    if states is None and want_states:
+        states = torch.empty((B, H, N, d, d), dtype=torch.float32, device=dev)
+    if states is not None:
+        _check(states, "states", torch.float32, (B, H, N, d, d), dev)
+    st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None,
+                               B, H, L, d, int(seg_len), int(agg_mode), int(topk), y.data_ptr(),
+                               states.data_ptr() if states is not None else None, _stream_handle(stream, dev))
+    if st != MC_OK:
+        raise MCError(st, fn_name)
+    return y, states
+
+
+def mc_forward(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None, states=None,
+               want_states: bool = True, stream=None):
+    """bf16 MC forward (``mc_forward`` in mc.h).  Returns (y, states); states is None
+    when ``want_states`` is False and none was given."""
+    return _forward("mc_forward", q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream)
+
+
+def mc_forward_f32(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None, states=None,
+                   want_states: bool = True, stream=None):
+    """fp32 MC forward (``mc_forward_f32`` in mc.h)."""
+    return _forward("mc_forward_f32", q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream)
+
+
+def forward(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, **kw):
+    """Dispatch on the input dtype: bf16 -> mc_forward, fp32 -> mc_forward_f32."""
+    if q.dtype == torch.bfloat16:
+        return mc_forward(q, k, v, u, seg_len, agg_mode, topk, **kw)
+    if q.dtype == torch.float32:
+        return mc_forward_f32(q, k, v, u, seg_len, agg_mode, topk, **kw)
+    raise TypeError("inputs must be bf16 or fp32")
+
+
+def mc_ssc_select(k, u, seg_len: int, topk: int, *, idx=None, stream=None):
+    """SSC router alone (``mc_ssc_select``): int32 [B,H,L,topk], rank order, -1 padded."""
+    lib = load_library()
+    B, H, L, d = k.shape
+    dev = k.device
+    _check(k, "k", k.dtype, (B, H, L, d), dev)
+    _check(u, "u", k.dtype, (B, H, L, d), dev)
+    if idx is None:
+        idx = torch.empty((B, H, L, topk), dtype=torch.int32, device=dev)
+    _check(idx, "idx", torch.int32, (B, H, L, topk), dev)
+    st = lib.mc_ssc_select(k.data_ptr(), u.data_ptr(), B, H, L, d, int(seg_len), int(topk), idx.data_ptr(),
+                           1 if k.dtype == torch.bfloat16 else 0, _stream_handle(stream, dev))
+    if st != MC_OK:
+        raise MCError(st, "mc_ssc_select")
+    return idx
+
+
+class KernelProfile:
+    """Record CUDA events at every kernel boundary of the forward calls made inside
+    the ``with`` block (``mc_profile_begin`` / ``mc_profile_end``).  After the block
+    and a device synchronise, :meth:`per_kernel_ms` gives {kernel: [ms, ...]}."""
+
+    def __init__(self, capacity: int = 1024):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        self._handles = None
+        self.count = 0
+        self.stages = []
+
+    def __enter__(self):
+        for e in self.events:
+            e.record()  # materialise the lazily created events
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        st = load_library().mc_profile_begin(self._handles, len(self.events))
+        if st != MC_OK:
+            raise MCError(st, "mc_profile_begin")
+        return self
+
+    def __exit__(self, *exc):
+        lib = load_library()
+        self.count = lib.mc_profile_end()
+        self.stages = [lib.mc_profile_stage(j) for j in range(max(self.count - 1, 0))]
+        self.stages = [s.decode() if s else None for s in self.stages]
+        return False
+
+    def per_kernel_ms(self) -> dict:
+        out = {}
+        for j, name in enumerate(self.stages):
+            if name is None:
+                continue
+            out.setdefault(name, []).append(self.events[j].elapsed_time(self.events[j + 1]))
+        return out
+
+    def kernel_count(self) -> int:
+        return sum(1 for s in self.stages if s is not None)
+
+
+def mc_forward_host(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None, states=None,
+                    stream=None):
+    """End-to-end forward on HOST tensors (``mc_forward_host``): the library copies the
+    inputs to the device, runs, copies y (and states, if given) back and synchronises."""
+    lib = load_library()
+    B, H, L, d = q.shape
+    dtype = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, dtype, (B, H, L, d), torch.device("cpu"))
+    if u is not None:
+        _check(u, "u", dtype, (B, H, L, d), torch.device("cpu"))
+    if y is None:
+        y = torch.empty((B, H, L, d), dtype=dtype)
+    _check(y, "y", dtype, (B, H, L, d), torch.device("cpu"))
+    if states is not None:
+        _check(states, "states", torch.float32, (B, H, num_segments(L, seg_len), d, d), torch.device("cpu"))
+    st = lib.mc_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None,
+                             B, H, L, d, int(seg_len), int(agg_mode), int(topk), y.data_ptr(),
+                             states.data_ptr() if states is not None else None,
+                             1 if dtype == torch.bfloat16 else 0, _stream_handle(stream, torch.device("cuda")))
+    if st != MC_OK:
+        raise MCError(st, "mc_forward_host")
+    return y, states

@@ -1,0 +1,298 @@
+// mc_api.cu -- the C ABI declared in include/mc.h: argument checks, stream-ordered
+// scratch, and the choice of kernels for a shape.
+#include <cstdint>
+#include <cstring>
+
+#include "mc_internal.cuh"
+
+namespace mc {
+
+namespace {
+struct ProfileState {
+    void *const *events = nullptr;
+    int capacity = 0;
+    int count = 0;
+    const char *stage[4096];  // stage[j]: kernel between event j and j+1
+};
+ProfileState g_prof;
+}  // namespace
+
+void profile_call_start(cudaStream_t s)
+{
+    if (!g_prof.events || g_prof.count >= g_prof.capacity) return;
+    if (g_prof.count > 0 && g_prof.count - 1 < 4096) g_prof.stage[g_prof.count - 1] = nullptr;
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[g_prof.count]), s);
+    ++g_prof.count;
+}
+
+void profile_after_kernel(cudaStream_t s, const char *name)
+{
+    if (!g_prof.events || g_prof.count >= g_prof.capacity) return;
+    if (g_prof.count - 1 < 4096) g_prof.stage[g_prof.count - 1] = name;
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[g_prof.count]), s);
+    ++g_prof.count;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_device()
+{
+    // The library is built for sm_103a only; refuse anything else up front.
+    static int cached[64];  // 0 unknown, 1 ok, 2 not ok
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MC_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1 ? MC_OK : MC_ERR_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MC_ERR_CUDA;
+    const bool ok = major == 10 && minor == 3;
+    if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+    return ok ? MC_OK : MC_ERR_DEVICE;
+}
+
+int check_shape(int B, int H, int L, int d, int seg_len)
+{
+    if (B < 1 || H < 1 || L < 1 || seg_len < 1) return MC_ERR_SHAPE;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return MC_ERR_SHAPE;
+    const long long BH = (long long)B * H;
+    const long long N = ((long long)L + seg_len - 1) / seg_len;
+    if (BH > (1ll << 24)) return MC_ERR_SHAPE;
+    // every element count used for indexing fits in 62 bits and the grids fit in 2^31 blocks
+    if (BH * L * d > (1ll << 40) || BH * N * d * d > (1ll << 40)) return MC_ERR_SHAPE;
+    if (BH * N * ((seg_len + 63) / 64) >= (1ll << 31)) return MC_ERR_SHAPE;
+    return MC_OK;
+}
+
+size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct ScratchPlan {
+    size_t off_states, off_O, off_r, off_kbar, total;
+};
+
+ScratchPlan plan_scratch(const Problem &p, bool need_states)
+{
+    ScratchPlan s{};
+    size_t off = 0;
+    s.off_states = off;
+    if (need_states) off += round_up(sizeof(float) * (size_t)p.BH * p.N * p.d * p.d);
+    s.off_O = off;
+    off += round_up(sizeof(float) * (size_t)p.BH * p.L * p.d);
+    s.off_r = off;
+    off += round_up(sizeof(float) * (size_t)p.BH * p.L);
+    s.off_kbar = off;
+    off += round_up(sizeof(float) * (size_t)p.BH * p.N * p.d);
+    s.total = off;
+    return s;
+}
+
+int forward_common(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
+                   int seg_len, int agg_mode, int topk, void *y, float *states, bool bf16, cudaStream_t stream)
+{
+    if (!q || !k || !v || !y) return MC_ERR_NULL;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    int st = check_shape(B, H, L, d, seg_len);
+    if (st != MC_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y) || (u && !aligned16(u)) ||
+        (states && !aligned16(states)))
+        return MC_ERR_ALIGN;
+    Problem p{};
+    p.B = B; p.H = H; p.L = L; p.d = d; p.C = seg_len;
+    p.N = (L + seg_len - 1) / seg_len;
+    p.BH = B * H;
+    p.bf16 = bf16;
+    p.mode = agg_mode;
+    p.topk = agg_mode == MC_SSC ? topk : 0;
+    if (agg_mode == MC_SSC) {
+        if (topk < 0) return MC_ERR_TOPK;
+        // topk >= N-1 selects every cached segment for every token: that is GRM exactly.
+        if (topk >= p.N - 1) p.mode = MC_GRM;
+        else if (topk > kMaxTopk) return MC_ERR_TOPK;
+    }
+    st = check_device();
+    if (st != MC_OK) return st;
+
+    const ScratchPlan plan = plan_scratch(p, states == nullptr);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, plan.total, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    char *base = static_cast<char *>(scratch);
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.u = p.mode == MC_RESIDUAL ? nullptr : u;
+    a.y = y;
+    a.states = states ? states : reinterpret_cast<float *>(base + plan.off_states);
+    a.O_on = reinterpret_cast<float *>(base + plan.off_O);
+    a.r_on = reinterpret_cast<float *>(base + plan.off_r);
+    a.kbar = reinterpret_cast<float *>(base + plan.off_kbar);
+    a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
+
+    profile_call_start(stream);
+    cudaError_t e = launch_seg_scan_simt(p, a, stream);
+    profile_after_kernel(stream, "seg_scan_simt");
+    if (e == cudaSuccess) {
+        e = launch_readout_simt(p, a, stream);
+        profile_after_kernel(stream, "readout_simt");
+    }
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
+}  // namespace
+}  // namespace mc
+
+extern "C" {
+
+int mc_forward(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d, int seg_len,
+               int agg_mode, int topk, void *y, float *states, mc_stream_t stream)
+{
+    return mc::forward_common(q, k, v, u, B, H, L, d, seg_len, agg_mode, topk, y, states, true,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mc_forward_f32(const float *q, const float *k, const float *v, const float *u, int B, int H, int L, int d,
+                   int seg_len, int agg_mode, int topk, float *y, float *states, mc_stream_t stream)
+{
+    return mc::forward_common(q, k, v, u, B, H, L, d, seg_len, agg_mode, topk, y, states, false,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int seg_len, int topk, int32_t *idx,
+                  int is_bf16, mc_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!k || !u || !idx) return MC_ERR_NULL;
+    int st = mc::check_shape(B, H, L, d, seg_len);
+    if (st != MC_OK) return st;
+    if (topk < 1 || topk > mc::kMaxTopk) return MC_ERR_TOPK;
+    if (!mc::aligned16(k) || !mc::aligned16(u) || !mc::aligned16(idx)) return MC_ERR_ALIGN;
+    st = mc::check_device();
+    if (st != MC_OK) return st;
+    mc::Problem p{};
+    p.B = B; p.H = H; p.L = L; p.d = d; p.C = seg_len;
+    p.N = (L + seg_len - 1) / seg_len;
+    p.BH = B * H;
+    p.bf16 = is_bf16 != 0;
+    p.mode = MC_SSC;
+    p.topk = topk;
+    float *kbar = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&kbar), sizeof(float) * (size_t)p.BH * p.N * d, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    mc::FwdArgs a{};
+    a.k = k; a.u = u; a.kbar = kbar; a.sel_out = idx;
+    a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = MC_SSC; a.topk = topk;
+    cudaError_t e = mc::launch_kbar_simt(p, a, stream);
+    if (e == cudaSuccess) e = mc::launch_ssc_select_simt(p, a, stream);
+    cudaError_t ef = cudaFreeAsync(kbar, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
+int mc_forward_host(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
+                    int seg_len, int agg_mode, int topk, void *y, float *states, int is_bf16, mc_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!q || !k || !v || !y) return MC_ERR_NULL;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    int st = mc::check_shape(B, H, L, d, seg_len);
+    if (st != MC_OK) return st;
+    st = mc::check_device();
+    if (st != MC_OK) return st;
+    const size_t elt = is_bf16 ? 2 : 4;
+    const size_t n_in = (size_t)B * H * L * d;
+    const size_t N = ((size_t)L + seg_len - 1) / seg_len;
+    const size_t bytes_in = mc::round_up(n_in * elt);
+    const size_t bytes_states = states ? mc::round_up(sizeof(float) * (size_t)B * H * N * d * d) : 0;
+    const int nin = u && agg_mode != MC_RESIDUAL ? 4 : 3;
+    void *dmem = nullptr;
+    if (cudaMallocAsync(&dmem, bytes_in * (nin + 1) + bytes_states, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    char *p = static_cast<char *>(dmem);
+    void *dq = p, *dk = p + bytes_in, *dv = p + 2 * bytes_in;
+    void *du = nin == 4 ? p + 3 * bytes_in : nullptr;
+    void *dy = p + nin * bytes_in;
+    float *ds = states ? reinterpret_cast<float *>(p + (nin + 1) * bytes_in) : nullptr;
+    cudaError_t e = cudaMemcpyAsync(dq, q, n_in * elt, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, n_in * elt, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, n_in * elt, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && du) e = cudaMemcpyAsync(du, u, n_in * elt, cudaMemcpyHostToDevice, stream);
+    int rc = MC_OK;
+    if (e == cudaSuccess) {
+        rc = is_bf16 ? mc_forward(dq, dk, dv, du, B, H, L, d, seg_len, agg_mode, topk, dy, ds, stream_)
+                     : mc_forward_f32(static_cast<const float *>(dq), static_cast<const float *>(dk),
+                                      static_cast<const float *>(dv), static_cast<const float *>(du), B, H, L, d,
+                                      seg_len, agg_mode, topk, static_cast<float *>(dy), ds, stream_);
+    }
+    if (e == cudaSuccess && rc == MC_OK) e = cudaMemcpyAsync(y, dy, n_in * elt, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess && rc == MC_OK && states)
+        e = cudaMemcpyAsync(states, ds, sizeof(float) * (size_t)B * H * N * d * d, cudaMemcpyDeviceToHost, stream);
+    cudaError_t ef = cudaFreeAsync(dmem, stream);
+    cudaError_t es = cudaStreamSynchronize(stream);
+    if (rc != MC_OK) return rc;
+    if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
+int mc_profile_begin(void *const *events, int capacity)
+{
+    if (!events || capacity < 1) return MC_ERR_NULL;
+    mc::g_prof.events = events;
+    mc::g_prof.capacity = capacity;
+    mc::g_prof.count = 0;
+    for (int j = 0; j < 4096; ++j) mc::g_prof.stage[j] = nullptr;
+    return MC_OK;
+}
+
+int mc_profile_end(void)
+{
+    const int n = mc::g_prof.count;
+    mc::g_prof.events = nullptr;
+    mc::g_prof.capacity = 0;
+    return n;
+}
+
+const char *mc_profile_stage(int j)
+{
+    if (j < 0 || j >= 4096) return nullptr;
+    return mc::g_prof.stage[j];
+}
+
+const char *mc_status_string(int status)
+{
+    switch (status) {
+    case MC_OK: return "ok";
+    case MC_ERR_NULL: return "a required pointer is NULL";
+    case MC_ERR_SHAPE: return "unsupported shape (B,H,L,seg_len >= 1; d in {16,32,64,128}; sizes within limits)";
+    case MC_ERR_MODE: return "agg_mode must be MC_RESIDUAL, MC_GRM, MC_SOUP or MC_SSC";
+    case MC_ERR_TOPK: return "SSC topk out of range (0..64, or >= N-1 for all segments)";
+    case MC_ERR_ALLOC: return "stream-ordered scratch allocation failed";
+    case MC_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case MC_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    case MC_ERR_ALIGN: return "every pointer must be 16-byte aligned";
+    case MC_ERR_DEVICE: return "the current device is not a compute capability 10.3 (sm_103a) GPU";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

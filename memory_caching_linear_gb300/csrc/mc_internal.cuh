@@ -1,0 +1,88 @@
+// mc_internal.cuh -- shared declarations of the CUDA path of the Memory Caching
+// forward (device helpers, launch argument blocks, kernel launchers).
+//
+// Data flow of one forward (per batch*head "bh", segment n, token t):
+//   seg_scan   : per (bh, segment) -- the segment's final state M^(n) (fp32,
+//                the `states` output), its key mean kbar_n, the online read
+//                O_on[t] = M_t^(n) q_t, and the online gate score
+//                r_on[t] = <u_t, mean of the segment's keys up to t>.
+//   readout    : per (bh, segment, token tile) -- gates over the cached
+//                segments and the online memory, and
+//                y_t = g_{t,n} O_on[t] + sum_{i<n} g_{t,i} M^(i) q_t.
+//   ssc_select : the SSC router alone (the same score and ranking code).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mc.h"
+
+namespace mc {
+
+constexpr int kMaxTopk = 64;  // SSC selections kept per token on the device
+
+struct Problem {
+    int B, H, L, d, C, N, mode, topk;
+    int BH;
+    bool bf16;
+};
+
+// Everything one forward needs on the device.  Pointers are device pointers.
+struct FwdArgs {
+    const void *q, *k, *v, *u;  // [BH][L][d], element type per Problem::bf16
+    void *y;                    // [BH][L][d]
+    float *states;              // [BH][N][d][d]
+    float *O_on;                // [BH][L][d]   scratch
+    float *r_on;                // [BH][L]      scratch
+    float *kbar;                // [BH][N][d]   scratch
+    int32_t *sel_out;           // [BH][L][topk] (ssc_select only)
+    int BH, L, C, N, mode, topk;
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Gate score <u_t, kbar_i> in fp32, summed in key order.  Every kernel that
+// needs a router score calls this one function, so the SSC ranking seen by
+// mc_ssc_select is bit-identical to the one the forward uses.
+__device__ __forceinline__ float gate_score(const float *__restrict__ u_row, const float *__restrict__ kb, int d)
+{
+    float acc = 0.f;
+    for (int c = 0; c < d; ++c) acc = fmaf(u_row[c], __ldg(kb + c), acc);
+    return acc;
+}
+
+// Insert (val, idx) into a top-k list kept sorted by value descending, index
+// ascending.  Candidates arrive in increasing idx, so an equal value goes after
+// the ones already there (equal scores -> lower segment index first).
+__device__ __forceinline__ void topk_insert(float *vals, int *idxs, int &count, int k, float val, int idx)
+{
+    int p = count;
+    while (p > 0 && vals[p - 1] < val) --p;
+    if (p >= k) return;
+    int last = count < k ? count : k - 1;
+    for (int j = last; j > p; --j) {
+        vals[j] = vals[j - 1];
+        idxs[j] = idxs[j - 1];
+    }
+    vals[p] = val;
+    idxs[p] = idx;
+    if (count < k) ++count;
+}
+
+// Kernel-boundary profiling (mc_profile_begin): call_start() before the first
+// kernel of a forward, after_kernel(name) after each launch.
+void profile_call_start(cudaStream_t s);
+void profile_after_kernel(cudaStream_t s, const char *name);
+
+// SIMT kernels (any d in {16,32,64,128}, fp32 or bf16 inputs).
+cudaError_t launch_seg_scan_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_readout_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_kbar_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_ssc_select_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
+
+}  // namespace mc

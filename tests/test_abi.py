@@ -1,0 +1,101 @@
+"""The C-ABI library: it builds, loads, exports every entry point mc.h declares,
+and rejects bad arguments before touching a device (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import memory_caching_linear_gb300 as mcl
+from memory_caching_linear_gb300 import build as mcbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mc.h")
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mcbuild.build()
+    return mcl.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mc_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(mcl.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", mcl.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_header_compiles_as_c():
+    res = subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-x", "c", "-I", os.path.dirname(HEADER), "-"],
+                         input='#include "mc.h"\nint main(void){return mc_forward==0;}\n', text=True,
+                         capture_output=True)
+    assert res.returncode == 0, res.stderr
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        s = mcl.mc_status_string(code)
+        assert s and s != "unknown status", code
+    assert mcl.mc_status_string(-100) == "unknown status"
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, B=1, H=1, L=64, d=16, seg=16, mode=1, topk=0, y=FAKE,
+             states=None)
+    a.update(kw)
+    return lib.mc_forward(a["q"], a["k"], a["v"], a["u"], a["B"], a["H"], a["L"], a["d"], a["seg"], a["mode"],
+                          a["topk"], a["y"], a["states"], None)
+
+
+def test_argument_errors_never_reach_the_device(lib):
+    assert _fwd(lib, q=None) == mcl.MC_ERR_NULL
+    assert _fwd(lib, y=None) == mcl.MC_ERR_NULL
+    assert _fwd(lib, u=None, mode=mcl.MC_GRM) == mcl.MC_ERR_NULL
+    assert _fwd(lib, mode=7) == mcl.MC_ERR_MODE
+    assert _fwd(lib, mode=-1) == mcl.MC_ERR_MODE
+    for bad in (dict(d=17), dict(d=256), dict(L=0), dict(B=0), dict(H=-1), dict(seg=0)):
+        assert _fwd(lib, **bad) == mcl.MC_ERR_SHAPE, bad
+    assert _fwd(lib, mode=mcl.MC_SSC, topk=-1) == mcl.MC_ERR_TOPK
+    assert _fwd(lib, mode=mcl.MC_SSC, topk=65, L=4096, seg=16) == mcl.MC_ERR_TOPK
+    assert _fwd(lib, q=FAKE + 8) == mcl.MC_ERR_ALIGN
+    assert _fwd(lib, states=FAKE + 4) == mcl.MC_ERR_ALIGN
+    st = lib.mc_ssc_select(FAKE, FAKE, 1, 1, 64, 16, 16, 0, FAKE, 1, None)
+    assert st == mcl.MC_ERR_TOPK
+    st = lib.mc_ssc_select(FAKE, FAKE, 1, 1, 64, 16, 16, 65, FAKE, 1, None)
+    assert st == mcl.MC_ERR_TOPK
+    st = lib.mc_forward_host(None, FAKE, FAKE, FAKE, 1, 1, 64, 16, 16, 1, 0, FAKE, None, 1, None)
+    assert st == mcl.MC_ERR_NULL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_valid_call_without_a_device_fails_cleanly(lib):
+    st = _fwd(lib)
+    assert st in (mcl.MC_ERR_CUDA, mcl.MC_ERR_DEVICE)
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    x = torch.zeros(1, 1, 8, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mcl.mc_forward(x, x, x, x, 4, mcl.MC_GRM)
+
+
+def test_build_flags_target_sm103a():
+    flags = " ".join(mcbuild.compile_flags())
+    assert "arch=compute_103a,code=sm_103a" in flags

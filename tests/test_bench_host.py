@@ -1,0 +1,66 @@
+"""Host-side logic of bench.py: algorithmic work counts and the multi-rank
+timing reduction (run as two gloo ranks on the CPU)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import mc_inputs
+
+
+def test_algorithmic_flops_long_grm():
+    w = mc_inputs.LONG_GRM
+    f = bench.algorithmic_flops(w)
+    # GRM: sum_t (s_t - 1) = C * N (N - 1) / 2 with C = L / N
+    per_head = w.L * 4 * w.d ** 2 + 2 * w.d ** 2 * (w.seg_len * w.N * (w.N - 1) // 2) \
+        + 2 * w.d * (w.seg_len * w.N * (w.N + 1) // 2)
+    assert f["total"] == w.B * w.H * per_head
+    assert abs(f["total"] / 1e12 - 1.16) < 0.01  # ~ L d^2 (N + 3) per head
+
+
+def test_algorithmic_flops_modes():
+    w = mc_inputs.SSC_D128
+    f = bench.algorithmic_flops(w)
+    s, n = bench.segment_counts(w)
+    assert max(n) == w.topk and n[0] == 0
+    r = bench.algorithmic_flops(w.with_(mode=mc_inputs.RESIDUAL))
+    assert r["readout"] == 0 and r["total"] == r["online"]
+    assert f["total"] > r["total"]
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = 10.0 + 5.0 * rank
+    mx = bench.reduce_max(ms, dist)
+    val = bench.aggregate(1000, 4, mx, world)
+    out[rank] = (mx, val)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_reduce_max_two_gloo_ranks():
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1]
+    mx, val = out[0]
+    assert mx == 15.0
+    assert val == pytest.approx(1000 * 4 * 2 / 0.015)
+
+
+def test_single_rank_reduce_is_identity():
+    assert bench.reduce_max(3.5, None) == 3.5

@@ -1,0 +1,212 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances (the accuracy the method is specified to): max|y - y_ref| <= 1e-4 *
+max|y_ref| for fp32 inputs, <= 1e-2 * max|y_ref| for bf16 inputs with fp32
+accumulation; the cached states to the same relative bound; SSC selections
+identical except where the oracle's fp64 gap between the last selected and the
+best unselected score is below 1e-5 (there the GPU's set must still be a valid
+top-k within that gap, and y is re-checked with the oracle run on the GPU's set).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import memory_caching_linear_gb300 as mcl
+import oracle
+from mc_inputs import GRM, GRM_D64, LONG_GRM, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, TINY, make_inputs, \
+    workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from memory_caching_linear_gb300 import build
+    build.build()
+    mcl.load_library()
+
+
+def rel_err(got, ref):
+    ref = np.asarray(ref, np.float64)
+    got = np.asarray(got, np.float64)
+    scale = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (scale if scale > 0 else 1.0))
+
+
+def run_gpu(q, k, v, u, C, mode, topk=0):
+    dev = torch.device("cuda")
+    y, st = mcl.forward(q.to(dev), k.to(dev), v.to(dev), u.to(dev) if u is not None else None, C, mode, topk)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy(), st.cpu().numpy()
+
+
+def check_ssc_selection(q, k, v, u, C, topk, ref, tol):
+    """Compare the GPU router with the oracle's; return the oracle y on the GPU's selection."""
+    dev = torch.device("cuda")
+    sel = mcl.mc_ssc_select(k.to(dev), u.to(dev), C, topk).cpu().numpy()
+    osel, gap = ref["sel"], ref["gap"]
+    differ = np.any(np.sort(sel, -1) != np.sort(osel, -1), axis=-1)
+    assert np.all(gap[differ] < GAP), f"{int(differ.sum())} selections differ outside near-ties"
+    if differ.any():
+        # the GPU's set must be a valid top-k: its worst score within GAP of the oracle's k-th best
+        kf = k.double().numpy()
+        uf = u.double().numpy()
+        B, H, L, d = kf.shape
+        N = (L + C - 1) // C
+        kbar = np.stack([kf[:, :, n * C:min(L, n * C + C)].mean(2) for n in range(N)], 2)
+        for b, h, t in zip(*np.nonzero(differ)):
+            r = kbar[b, h] @ uf[b, h, t]
+            mine = [i for i in sel[b, h, t] if i >= 0]
+            theirs = [i for i in osel[b, h, t] if i >= 0]
+            assert len(mine) == len(theirs)
+            assert min(r[mine]) >= min(r[theirs]) - GAP
+        ref = oracle.forward(q, k, v, u, C, SSC, topk, given_sel=sel)
+    return ref["y"]
+
+
+CASES = [
+    # (name, B, H, L, d, C, dtype)
+    ("tiny", 1, 1, 256, 16, 64, "f32"),
+    ("tiny-N1", 1, 1, 256, 16, 256, "f32"),
+    ("ragged-f32", 1, 2, 200, 32, 64, "f32"),
+    ("C1-f32", 1, 1, 48, 16, 1, "f32"),
+    ("C37-f32", 2, 1, 150, 64, 37, "f32"),
+    ("d128-f32", 1, 2, 300, 128, 128, "f32"),
+    ("d64-bf16", 2, 2, 512, 64, 128, "bf16"),
+    ("d128-bf16", 1, 2, 1024, 128, 256, "bf16"),
+    ("d128-ragged-bf16", 1, 1, 777, 128, 256, "bf16"),
+    ("d32-bf16", 1, 3, 260, 32, 64, "bf16"),
+    ("d16-C1000-bf16", 1, 1, 600, 16, 1000, "bf16"),
+]
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 0), (SSC, 2), (SSC, 100)])
+@pytest.mark.parametrize("name,B,H,L,d,C,dtype", CASES, ids=[c[0] for c in CASES])
+def test_parity_small(name, B, H, L, d, C, dtype, mode, topk):
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype=dtype)
+    ref = oracle.forward(q, k, v, u, C, mode, topk)
+    y, st = run_gpu(q, k, v, u, C, mode, topk)
+    yref = ref["y"]
+    N = (L + C - 1) // C
+    if mode == SSC and 0 < topk < N - 1:
+        yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL[dtype])
+    assert rel_err(y, yref) <= TOL[dtype], (name, mode, topk, rel_err(y, yref))
+    assert rel_err(st, ref["states"]) <= TOL[dtype]
+    assert np.isfinite(y).all()
+
+
+def test_tiny_workload_invariants_on_gpu():
+    """The tiny workload's collapse invariants hold for the GPU results too."""
+    q, k, v, u = workload_inputs(TINY)
+    L = TINY.L
+    y_res, _ = run_gpu(q, k, v, u, TINY.seg_len, RESIDUAL)
+    y_n1, _ = run_gpu(q, k, v, u, L, GRM)
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    la = np.einsum("...tj,...jd->...td", np.einsum("...td,...jd->...tj", qd, kd) * np.tril(np.ones((L, L))), vd)
+    assert rel_err(y_res, la) <= TOL["f32"]
+    assert rel_err(y_n1, la) <= TOL["f32"]
+    y_grm, _ = run_gpu(q, k, v, u, TINY.seg_len, GRM)
+    y_soup, _ = run_gpu(q, k, v, u, TINY.seg_len, SOUP)
+    np.testing.assert_array_equal(y_grm, y_soup)
+
+
+def test_states_null_and_determinism():
+    q, k, v, u = (t.cuda() for t in make_inputs(1, 2, 640, 64, 5, "bf16"))
+    y1, _ = mcl.mc_forward(q, k, v, u, 128, GRM, want_states=False)
+    y2, st = mcl.mc_forward(q, k, v, u, 128, GRM)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert st.shape == (1, 2, 5, 64, 64)
+
+
+def test_host_entry_point_matches_device_call():
+    q, k, v, u = make_inputs(1, 2, 512, 64, 6, "bf16")
+    qp, kp, vp, up = (t.pin_memory() for t in (q, k, v, u))
+    y_host, st_host = mcl.mc_forward_host(qp, kp, vp, up, 128, GRM,
+                                          states=torch.empty(1, 2, 4, 64, 64).pin_memory())
+    y_dev, st_dev = mcl.mc_forward(qp.cuda(), kp.cuda(), vp.cuda(), up.cuda(), 128, GRM)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
+    assert torch.equal(st_host, st_dev.cpu())
+
+
+def test_bad_arguments_raise():
+    x = torch.zeros(1, 1, 8, 24, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mcl.MCError) as e:
+        mcl.mc_forward(x, x, x, x, 4, GRM)
+    assert e.value.status == mcl.MC_ERR_SHAPE
+    x = torch.zeros(1, 1, 8, 16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mcl.MCError) as e:
+        mcl.mc_forward(x, x, x, x, 4, 9)
+    assert e.value.status == mcl.MC_ERR_MODE
+    empty = torch.zeros(1, 1, 0, 16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mcl.MCError) as e:
+        mcl.mc_forward(empty, empty, empty, empty, 4, GRM)
+    assert e.value.status == mcl.MC_ERR_SHAPE
+
+
+def test_ssc_selection_small():
+    q, k, v, u = make_inputs(2, 2, 640, 64, 7, "bf16")
+    C, topk = 32, 4
+    ref = oracle.forward(q, k, v, u, C, SSC, topk)
+    sel = mcl.mc_ssc_select(k.cuda(), u.cuda(), C, topk).cpu().numpy()
+    same = np.all(sel == ref["sel"], axis=-1)
+    assert np.all(same | (ref["gap"] < GAP))
+    assert same.mean() > 0.99
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+
+def _sampled_check(w, heads, segs, mode=None, topk=None):
+    mode = w.mode if mode is None else mode
+    topk = w.topk if topk is None else topk
+    q, k, v, u = workload_inputs(w)
+    y, st = run_gpu(q, k, v, u, w.seg_len, mode, topk)
+    mask = np.zeros(w.N, bool)
+    mask[list(segs)] = True
+    for (b, h) in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        qs, ks, vs, us = (t[sl].contiguous() for t in (q, k, v, u))
+        ref = oracle.forward(qs, ks, vs, us, w.seg_len, mode, topk, seg_mask=mask)
+        assert rel_err(st[sl], ref["states"]) <= TOL[w.dtype]
+        yref = ref["y"]
+        if mode == SSC and 0 < topk < w.N - 1:
+            gpu_sel = mcl.mc_ssc_select(ks.cuda(), us.cuda(), w.seg_len, topk).cpu().numpy()
+            osel, gap = ref["sel"], ref["gap"]
+            for n in segs:
+                ts = slice(n * w.seg_len, min(w.L, (n + 1) * w.seg_len))
+                differ = np.any(np.sort(gpu_sel[..., ts, :], -1) != np.sort(osel[..., ts, :], -1), -1)
+                assert np.all(gap[..., ts][differ] < GAP)
+            yref = oracle.forward(qs, ks, vs, us, w.seg_len, mode, topk, seg_mask=mask, given_sel=gpu_sel)["y"]
+        for n in segs:
+            ts = slice(n * w.seg_len, min(w.L, (n + 1) * w.seg_len))
+            err = rel_err(y[sl][..., ts, :], yref[..., ts, :])
+            assert err <= TOL[w.dtype], (w.name, b, h, n, err)
+
+
+@pytest.mark.slow
+def test_full_size_grm_d64():
+    _sampled_check(GRM_D64, heads=[(0, 0), (3, 7)], segs=[0, 7, 15])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", SWEEP, ids=[w.name for w in SWEEP])
+def test_full_size_sweep(w):
+    segs = sorted({0, w.N // 2, w.N - 1})
+    _sampled_check(w, heads=[(7, 15)], segs=segs)
+    _sampled_check(w, heads=[(0, 3)], segs=segs, mode=RESIDUAL, topk=0)
+
+
+@pytest.mark.slow
+def test_full_size_ssc():
+    _sampled_check(SSC_D128, heads=[(0, 0), (1, 9)], segs=[1, 5, 63])
+
+
+@pytest.mark.slow
+def test_full_size_long_grm():
+    _sampled_check(LONG_GRM, heads=[(0, 0), (0, 15)], segs=[0, 1, 40, 63])
