@@ -37,7 +37,8 @@
  *     the stream-ordered allocator (cudaMallocAsync) and released on the same
  *     stream.  Calls on different streams are independent.
  *   - d must be 16, 32, 64 or 128.  B, H, L, seg_len >= 1.
- *   - Return value: MC_OK (0) or a negative MC_ERR_* code.  On an argument
+ *   - Return value: MC_OK (0) or a negative MC_ERR_* code (shape is checked
+ *     first, then the mode, then pointers).  On an argument
  *     error nothing is enqueued.  On MC_ERR_CUDA the contents of y and states
  *     are undefined; work already enqueued finishes on the stream.
  */

@@ -91,11 +91,11 @@ ScratchPlan plan_scratch(const Problem &p, bool need_states)
 int forward_common(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
                    int seg_len, int agg_mode, int topk, void *y, float *states, bool bf16, cudaStream_t stream)
 {
-    if (!q || !k || !v || !y) return MC_ERR_NULL;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
     int st = check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (!q || !k || !v || !y) return MC_ERR_NULL;
+    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y) || (u && !aligned16(u)) ||
         (states && !aligned16(states)))
         return MC_ERR_ALIGN;
@@ -170,9 +170,9 @@ int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int 
                   int is_bf16, mc_stream_t stream_)
 {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (!k || !u || !idx) return MC_ERR_NULL;
     int st = mc::check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
+    if (!k || !u || !idx) return MC_ERR_NULL;
     if (topk < 1 || topk > mc::kMaxTopk) return MC_ERR_TOPK;
     if (!mc::aligned16(k) || !mc::aligned16(u) || !mc::aligned16(idx)) return MC_ERR_ALIGN;
     st = mc::check_device();
@@ -207,11 +207,11 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
                     int seg_len, int agg_mode, int topk, void *y, float *states, int is_bf16, mc_stream_t stream_)
 {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (!q || !k || !v || !y) return MC_ERR_NULL;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
     int st = mc::check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (!q || !k || !v || !y) return MC_ERR_NULL;
+    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
     st = mc::check_device();
     if (st != MC_OK) return st;
     const size_t elt = is_bf16 ? 2 : 4;
