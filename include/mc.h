@@ -71,7 +71,8 @@ enum {
     MC_ERR_CUDA = -6,           /* a CUDA runtime call or kernel launch failed */
     MC_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait gave up */
     MC_ERR_ALIGN = -8,          /* a pointer is not 16-byte aligned */
-    MC_ERR_DEVICE = -9          /* the current device is not a compute-capability 10.3 GPU */
+    MC_ERR_DEVICE = -9,         /* the current device is not a compute-capability 10.3 GPU */
+    MC_ERR_SCRATCH = -10        /* mc_forward_noalloc: the problem needs more than its 64 MiB static scratch */
 };
 
 /*
@@ -120,6 +121,32 @@ int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int 
 int mc_forward_host(const void *q, const void *k, const void *v, const void *u,
                     int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
                     void *y, float *states, int is_bf16, mc_stream_t stream);
+
+/*
+ * mc_forward_noalloc -- mc_forward without any device allocation.  (The paper
+ * has no counterpart: this is a deployment variant of the same forward.)
+ *   For callers that cannot allocate device memory while they run -- e.g. an
+ *   engine plugin whose host framework owns all device memory and forbids
+ *   allocation inside its execute call, or a serving loop that must not risk an
+ *   allocator call or an out-of-memory error mid-request.  Same arguments,
+ *   layouts and results as mc_forward (it runs the CUDA-core kernels); the
+ *   caller still provides q, k, v, u, y and, optionally, states.
+ *   Scratch comes from one static device array of 64 MiB inside the library,
+ *   held by every GPU that loads the library until the process exits.  It must
+ *   hold O_on (B*H*L*d fp32), the online scores (B*H*L fp32), the key means
+ *   (B*H*N*d fp32) and, when states is NULL, the states (B*H*N*d*d fp32), each
+ *   rounded up to 256 bytes; larger problems return MC_ERR_SCRATCH and enqueue
+ *   nothing.  The call allocates and frees nothing.
+ *   The first call on each device looks up the array's device address (once,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls whose work overlaps on the GPU (other
+ *   streams, other host threads) race on it and must be serialised by the
+ *   caller.  Every scratch element is rewritten before it is read, so nothing
+ *   left by an earlier call needs clearing.
+ */
+int mc_forward_noalloc(const void *q, const void *k, const void *v, const void *u,
+                       int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                       void *y, float *states, mc_stream_t stream);
 
 /*
  * Kernel-boundary timing, for benchmarks and profilers.

@@ -22,9 +22,10 @@ MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC = 0, 1, 2, 3
 MC_OK = 0
 MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
+MC_ERR_SCRATCH = -10
 
-EXPORTED = ("mc_forward", "mc_forward_f32", "mc_ssc_select", "mc_forward_host", "mc_profile_begin",
-            "mc_profile_end", "mc_profile_stage", "mc_status_string")
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
+            "mc_profile_begin", "mc_profile_end", "mc_profile_stage", "mc_status_string")
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmc.so")
@@ -54,6 +55,8 @@ def load_library():
     lib.mc_ssc_select.restype = i
     lib.mc_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, i, vp]
     lib.mc_forward_host.restype = i
+    lib.mc_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
+    lib.mc_forward_noalloc.restype = i
     lib.mc_profile_begin.argtypes = [vp, i]
     lib.mc_profile_begin.restype = i
     lib.mc_profile_end.argtypes = []

@@ -291,6 +291,7 @@ const char *mc_status_string(int status)
     case MC_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case MC_ERR_ALIGN: return "every pointer must be 16-byte aligned";
     case MC_ERR_DEVICE: return "the current device is not a compute capability 10.3 (sm_103a) GPU";
+    case MC_ERR_SCRATCH: return "problem too large for mc_forward_noalloc's 64 MiB static scratch (use mc_forward)";
     default: return "unknown status";
     }
 }

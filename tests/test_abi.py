@@ -50,7 +50,7 @@ def test_header_compiles_as_c():
 
 
 def test_status_strings(lib):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = mcl.mc_status_string(code)
         assert s and s != "unknown status", code
     assert mcl.mc_status_string(-100) == "unknown status"
