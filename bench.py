@@ -237,7 +237,7 @@ def run_ours(args, w):
     time.sleep(0.4)
     t_w = time.perf_counter()
     nwarm = 0
-    while nwarm < args.warmup or time.perf_counter() - t_w < 1.0:
+    while nwarm < args.warmup or time.perf_counter() - t_w < args.warmup_seconds:
         step()
         torch.cuda.synchronize()
         nwarm += 1
@@ -386,6 +386,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long-grm")
     ap.add_argument("--mode", choices=["residual", "grm", "soup", "ssc"], default=None,
                     help="override the workload's aggregation")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0,
+                    help="keep warming up at least this long (clocks settle under load)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

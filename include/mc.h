@@ -149,6 +149,17 @@ int mc_forward_noalloc(const void *q, const void *k, const void *v, const void *
                        void *y, float *states, mc_stream_t stream);
 
 /*
+ * mc_check_device -- synchronise `stream`, then report whether any tensor-core
+ *   kernel of this library gave up on a bounded device-side wait since the last
+ *   check (and clear that record).  Every wait inside the kernels is bounded; a
+ *   kernel that gives up abandons its tile and exits cleanly, so the context
+ *   stays usable but the outputs of that call are undefined.
+ *   Returns MC_OK, MC_ERR_DEVICE_TIMEOUT, or MC_ERR_CUDA if the stream reports
+ *   an error.
+ */
+int mc_check_device(mc_stream_t stream);
+
+/*
  * Kernel-boundary timing, for benchmarks and profilers.
  *   mc_profile_begin(events, capacity): `events` is a caller-owned array of
  *     `capacity` cudaEvent_t handles (created by the caller).  From now on every

@@ -115,6 +115,28 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     st = check_device();
     if (st != MC_OK) return st;
 
+    if (tc_supported(p)) {
+        const size_t b_states = states ? 0 : round_up(sizeof(float) * (size_t)p.BH * p.N * d * d);
+        void *scratch = nullptr;
+        if (cudaMallocAsync(&scratch, b_states + tc_scratch_bytes(p), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_ALLOC;
+        }
+        FwdArgs a{};
+        a.q = q; a.k = k; a.v = v;
+        a.u = p.mode == MC_RESIDUAL ? nullptr : u;
+        a.y = y;
+        a.states = states ? states : static_cast<float *>(scratch);
+        a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = 0;
+        cudaError_t e = launch_forward_tc(p, a, static_cast<char *>(scratch) + b_states, stream);
+        cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e != cudaSuccess || ef != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_CUDA;
+        }
+        return MC_OK;
+    }
+
     const ScratchPlan plan = plan_scratch(p, states == nullptr);
     void *scratch = nullptr;
     if (cudaMallocAsync(&scratch, plan.total, stream) != cudaSuccess) {
@@ -252,6 +274,20 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
         return MC_ERR_CUDA;
     }
     return MC_OK;
+}
+
+int mc_check_device(mc_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    int was = 0;
+    if (mc::take_device_abort(&was) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return was ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
 }
 
 int mc_profile_begin(void *const *events, int capacity)

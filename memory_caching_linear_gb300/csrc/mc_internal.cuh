@@ -79,6 +79,14 @@ __device__ __forceinline__ void topk_insert(float *vals, int *idxs, int &count, 
 void profile_call_start(cudaStream_t s);
 void profile_after_kernel(cudaStream_t s, const char *name);
 
+// Tensor-core path (k_tc.cu): bf16, d = 128, seg_len % 128 == 0, L % seg_len == 0,
+// N <= 64, Residual / GRM / Soup.
+bool tc_supported(const Problem &p);
+size_t tc_scratch_bytes(const Problem &p);
+cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+// Reads and clears the device-side record of an abandoned bounded wait.
+cudaError_t take_device_abort(int *was_set);
+
 // SIMT kernels (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_seg_scan_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_readout_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);

@@ -41,7 +41,7 @@ def rel_err(got, ref):
 def run_gpu(q, k, v, u, C, mode, topk=0):
     dev = torch.device("cuda")
     y, st = mcl.forward(q.to(dev), k.to(dev), v.to(dev), u.to(dev) if u is not None else None, C, mode, topk)
-    torch.cuda.synchronize()
+    assert mcl.mc_check_device() == mcl.MC_OK  # no kernel gave up on a bounded wait
     return y.float().cpu().numpy(), st.cpu().numpy()
 
 
@@ -97,6 +97,34 @@ def test_parity_small(name, B, H, L, d, C, dtype, mode, topk):
         yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL[dtype])
     assert rel_err(y, yref) <= TOL[dtype], (name, mode, topk, rel_err(y, yref))
     assert rel_err(st, ref["states"]) <= TOL[dtype]
+    assert np.isfinite(y).all()
+
+
+# Shapes the tensor-core path takes (bf16, d = 128, seg_len % 128 == 0, N <= 64):
+# one chunk per segment, many chunks per segment, the largest N, a single
+# segment, and more (batch, head) pairs than SMs.
+TC_CASES = [
+    ("tc-C128-N64", 1, 2, 8192, 128, 128),
+    ("tc-C512-N8", 1, 2, 4096, 128, 512),
+    ("tc-C2048-N1", 2, 1, 2048, 128, 2048),
+    ("tc-C256-N4-BH160", 10, 16, 1024, 128, 256),
+]
+
+
+@pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP])
+@pytest.mark.parametrize("name,B,H,L,d,C", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_parity_tensor_core_shapes(name, B, H, L, d, C, mode):
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype="bf16")
+    if B * H > 8:  # oracle on a subset of heads keeps the CPU time small
+        heads = [(0, 0), (B - 1, H - 1), (B // 2, 3)]
+    else:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    y, st = run_gpu(q, k, v, u, C, mode)
+    for (b, h) in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.forward(*(t[sl].contiguous() for t in (q, k, v, u)), C, mode)
+        assert rel_err(y[sl], ref["y"]) <= TOL["bf16"], (name, mode, b, h, rel_err(y[sl], ref["y"]))
+        assert rel_err(st[sl], ref["states"]) <= TOL["bf16"]
     assert np.isfinite(y).all()
 
 
