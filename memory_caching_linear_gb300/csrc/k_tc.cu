@@ -65,6 +65,7 @@ struct TcArgs {
     uint8_t *kbar_img;    // [BH] x 32 KB: hi rows (16 KB) then lo rows (16 KB), row = segment
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
+    __nv_bfloat16 *gam;   // [BH][L][64] gates: g_i at column i < n, g_n at column 63
     int BH, L, C, N, CPS;
     int num_tiles;
 };
@@ -319,12 +320,116 @@ __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
 }
 
 // ============================================================================
+// gates_tc -- the gate of every token ([MC-ja §3.1 eq. 10], normalised by a
+// softmax): one CTA per 128-token chunk.  Scores r_{t,i} = <u_t, kbar_i> come
+// from two MMAs (kbar as hi + lo bf16 rows, so the score carries ~16 bits of
+// kbar; u is exact in bf16), then
+//   g_{t,i} = exp(r_{t,i} - m) / Z (i < n),  g_{t,n} = exp(r_on[t] - m) / Z
+// written as bf16: gam[token][i] for i < n and gam[token][63] for the online memory.
+// ============================================================================
+constexpr size_t kGatesSmem = 2 * kTile + 1024;
+
+__global__ void __launch_bounds__(128) gates_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t bar_load, bar_mma;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunks = a.L / kCT;
+    const int bh = blockIdx.x / chunks;
+    const int t0 = (blockIdx.x % chunks) * kCT;
+    const int n = t0 / a.C;
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 64);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        abort_flag = 0;
+        mbar_init(&bar_load, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    if (threadIdx.x == 0) {
+        const int rr = bh * a.L + t0;
+        mbar_arrive_expect_tx(&bar_load, 2 * kTile);
+        tma_load_2d(sm, &mU, 0, rr, &bar_load);
+        tma_load_2d(sm + 16384, &mU, 64, rr, &bar_load);
+        bulk_load(sm + kTile, a.kbar_img + (size_t)bh * kTile, kTile, &bar_load);
+    }
+    bool ok = mbar_wait(&bar_load, 0, &abort_flag);
+    if (threadIdx.x == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+        const uint64_t dU = make_desc_sw128(smem_u32(sm), 0, 1024);
+        const uint64_t dKb = make_desc_sw128(smem_u32(sm + kTile), 0, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tb, dU + (kmaj_off(kk, 128) >> 4), dKb + (kmaj_off(kk, 64) >> 4), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tb, dU + (kmaj_off(kk, 128) >> 4), dKb + ((16384 + kmaj_off(kk, 64)) >> 4), idS, 1);
+        mma_commit(&bar_mma);
+    }
+    if (ok) ok = mbar_wait(&bar_mma, 0, &abort_flag);
+    tc_fence_after();
+    const uint32_t row = 32 * warp + lane;
+    float sc[64];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint32_t v[16];
+        tmem_ld16(tb + ((uint32_t)(32 * warp) << 16) + 16 * m, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sc[16 * m + i] = __uint_as_float(v[i]);
+    }
+    if (ok) {
+        const size_t tok = (size_t)bh * a.L + t0 + row;
+        const float ron = a.r_on[tok];
+        float mx = ron;
+#pragma unroll
+        for (int i = 0; i < 63; ++i)
+            if (i < n) mx = fmaxf(mx, sc[i]);
+        float z = expf(ron - mx);
+#pragma unroll
+        for (int i = 0; i < 63; ++i) {
+            if (i < n) {
+                sc[i] = expf(sc[i] - mx);
+                z += sc[i];
+            } else {
+                sc[i] = 0.f;
+            }
+        }
+        const float inv = 1.f / z;
+#pragma unroll
+        for (int i = 0; i < 63; ++i) sc[i] *= inv;
+        sc[63] = expf(ron - mx) * inv;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.gam + tok * 64);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            dst[i] = make_uint4(pack_bf16x2(sc[8 * i], sc[8 * i + 1]), pack_bf16x2(sc[8 * i + 2], sc[8 * i + 3]),
+                                pack_bf16x2(sc[8 * i + 4], sc[8 * i + 5]), pack_bf16x2(sc[8 * i + 6], sc[8 * i + 7]));
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 64);
+    }
+    if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
+}
+
+// ============================================================================
 // readout_tc
 // ============================================================================
-constexpr int kT2Threads = 320;  // 0 TMA, 1 MMA, 2-5 A producers, 6-9 aux
-constexpr int kRing = 4;
-constexpr uint32_t kOffK = 0, kOffV = kTile, kOffKbar = 2 * kTile, kOffRing = 3 * kTile;
-constexpr size_t kT2Smem = 3 * kTile + kRing * kTile + 1024;
+constexpr int kT2Threads = 352;  // 0 TMA, 1 MMA issuer 0, 2-5 A producers, 6-9 aux, 10 MMA issuer 1
+constexpr int kRing = 7;     // 32 KB operand slots: K, prefix state, cached states, V of each tile
+constexpr int kASlots = 4;   // A operands (bf16, 64 TMEM columns each) in flight
+constexpr size_t kT2Smem = kRing * kTile + 1024;
 
 struct TileInfo {
     int n, c, bh;
@@ -341,6 +446,8 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs &a, int id)
     return t;
 }
 
+// Cached operands a tile reads, in order: the chunk's prefix state (c > 0), then
+// the cached states M^(0..n-1) (GRM) or their prefix sum P_n (Residual, n > 0).
 template <bool GATED>
 __device__ __forceinline__ int tile_items(const TileInfo &t)
 {
@@ -351,20 +458,19 @@ template <bool GATED>
 __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const TileInfo &t, int k)
 {
     const size_t sb = (size_t)t.bh * a.N;
-    const uint8_t *spre = a.spre_img + ((sb + t.n) * a.CPS + t.c) * kTile;
-    if (GATED) {
-        if (t.c > 0) {
-            if (k == 0) return spre;
-            --k;
-        }
-        return a.states_img + (sb + k) * kTile;
-    } else {
-        if (t.n > 0) {
-            if (k == 0) return a.prefix_img + (sb + t.n) * kTile;
-            --k;
-        }
-        return spre;
+    if (t.c > 0) {
+        if (k == 0) return a.spre_img + ((sb + t.n) * a.CPS + t.c) * kTile;
+        --k;
     }
+    return GATED ? a.states_img + (sb + k) * kTile : a.prefix_img + (sb + t.n) * kTile;
+}
+
+// Accumulator groups of a tile: items + the P V product.  With two or more the
+// two accumulators are both written (the MMA warp alternates between them).
+template <bool GATED>
+__device__ __forceinline__ int tile_groups(const TileInfo &t)
+{
+    return tile_items<GATED>(t) + 1;
 }
 
 template <bool GATED>
@@ -374,10 +480,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t ring_full[kRing], ring_empty[kRing];
-    __shared__ uint64_t kv_full, kv_empty, kb_full, kb_empty;
-    __shared__ uint64_t a_full[2], a_empty[2];
-    __shared__ uint64_t r_free, g_full, g_done, u_full, sc_full, gam_full;
-    __shared__ uint64_t y_full[2], y_empty[2];
+    __shared__ uint64_t a_full[kASlots], a_empty[kASlots];
+    __shared__ uint64_t g_full, g_done, y_full, y_empty, p_slot, p_written;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -398,179 +502,139 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
         }
-        mbar_init(&kv_full, 1);
-        mbar_init(&kv_empty, 1);
-        mbar_init(&kb_full, 1);
-        mbar_init(&kb_empty, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kASlots; ++s) {
             mbar_init(&a_full[s], 128);
             mbar_init(&a_empty[s], 1);
-            mbar_init(&y_full[s], 1);
-            mbar_init(&y_empty[s], 128);
         }
-        mbar_init(&r_free, 128);
         mbar_init(&g_full, 1);
         mbar_init(&g_done, 128);
-        mbar_init(&u_full, 128);
-        mbar_init(&sc_full, 1);
-        mbar_init(&gam_full, 128);
+        mbar_init(&p_slot, 128);
+        mbar_init(&p_written, 128);
+        mbar_init(&y_full, 2);  // one commit from each MMA issuer
+        mbar_init(&y_empty, 128);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t tY0 = tb, tR = tb + 256, tA0 = tb + 384;
+    // tensor memory: D0 (128 cols) | D1 (128; holds G at the start of a tile) | A slots (4 x 64).
+    // A slot sequence of a tile: g_n o Q (for G and the prefix state), one slot per
+    // cached operand (A warps), then P for the P V product (aux warps).
+    const uint32_t tD0 = tb, tD1 = tb + 128, tA0 = tb + 256;
     const uint32_t s_base = smem_u32(sm);
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
+        // Ring sequence of a tile: K tile, the cached operands, V tile.  At the
+        // start of each tile it also prefetches the next tile's query rows and
+        // gate rows into L2 for the A warps.
         if (lane == 0 && my_tiles > 0) {
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
-            int kv_next = 0, kb_next = GATED ? 0 : my_tiles;  // next tile whose K/V, kbar image to load
-            int it_tile = 0, it_k = 0;                          // next ring item
             uint32_t g = 0;
-            TileInfo it_info = decode_tile(a, tile_id(0));
-            while (tile_items<GATED>(it_info) == 0) {  // skip tiles that read no cached state
-                if (++it_tile >= my_tiles) break;
-                it_info = decode_tile(a, tile_id(it_tile));
-            }
-            uint64_t t_idle = 0;
-            bool idle = false;
-            while (kv_next < my_tiles || kb_next < my_tiles || it_tile < my_tiles) {
-                bool did = false;
-                if (kv_next < my_tiles && mbar_try_wait(&kv_empty, (kv_next & 1) ^ 1)) {
-                    const TileInfo t = decode_tile(a, tile_id(kv_next));
-                    const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
-                    mbar_arrive_expect_tx(&kv_full, 2 * kTile);
-                    tma_load_2d(sm + kOffK, &mK, 0, rr, &kv_full);
-                    tma_load_2d(sm + kOffK + 16384, &mK, 64, rr, &kv_full);
-                    tma_load_2d(sm + kOffV, &mV, 0, rr, &kv_full);
-                    tma_load_2d(sm + kOffV + 16384, &mV, 64, rr, &kv_full);
-                    ++kv_next;
-                    did = true;
-                }
-                if (GATED && kb_next < my_tiles && mbar_try_wait(&kb_empty, (kb_next & 1) ^ 1)) {
-                    const TileInfo t = decode_tile(a, tile_id(kb_next));
-                    mbar_arrive_expect_tx(&kb_full, kTile);
-                    bulk_load(sm + kOffKbar, a.kbar_img + (size_t)t.bh * kTile, kTile, &kb_full);
-                    ++kb_next;
-                    did = true;
-                }
-                if (it_tile < my_tiles) {
-                    const int s = g % kRing;
-                    const uint32_t r = g / kRing;
-                    if (mbar_try_wait(&ring_empty[s], (r & 1) ^ 1)) {
-                        mbar_arrive_expect_tx(&ring_full[s], kTile);
-                        bulk_load(sm + kOffRing + s * kTile, item_image<GATED>(a, it_info, it_k), kTile, &ring_full[s]);
-                        ++g;
-                        did = true;
-                        if (++it_k >= tile_items<GATED>(it_info)) {
-                            it_k = 0;
-                            ++it_tile;
-                            while (it_tile < my_tiles) {
-                                it_info = decode_tile(a, tile_id(it_tile));
-                                if (tile_items<GATED>(it_info) > 0) break;
-                                ++it_tile;
-                            }
-                        }
-                    }
-                }
-                if (did) {
-                    idle = false;
-                } else {
-                    if (abort_flag) break;
-                    if (!idle) {
-                        idle = true;
-                        t_idle = globaltimer_ns();
-                    } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
-                        abort_flag = 1;
-                        break;
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0 && my_tiles > 0) {
-            constexpr uint32_t idG = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);
-            constexpr uint32_t idC = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
-            const uint32_t kb_base = s_base + kOffKbar;
-            auto issue_scores = [&](int jn) -> bool {
-                if (!mbar_wait(&u_full, jn & 1, &abort_flag)) return false;
-                if (!mbar_wait(&kb_full, jn & 1, &abort_flag)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tR, tR + 64 + kk * 8, make_desc_sw128(kb_base + kmaj_off(kk, 64), 0, 1024), idS, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tR, tR + 64 + kk * 8, make_desc_sw128(kb_base + 16384 + kmaj_off(kk, 64), 0, 1024), idS, 1);
-                mma_commit(&sc_full);
-                mma_commit(&kb_empty);
-                return true;
-            };
-            uint32_t g = 0, ac = 0;
             bool ok = true;
-            if (GATED) ok = issue_scores(0);
+            auto slot = [&](uint32_t bytes) -> uint8_t * {
+                const int s = g % kRing;
+                if (!mbar_wait(&ring_empty[s], ((g / kRing) & 1) ^ 1, &abort_flag)) return nullptr;
+                mbar_arrive_expect_tx(&ring_full[s], bytes);
+                return sm + s * kTile;
+            };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
-                const uint32_t tY = tY0 + (j & 1) * 128;
-                // online: G = Q K^T into R
-                if (!(ok = mbar_wait(&kv_full, j & 1, &abort_flag))) break;
-                if (!(ok = mbar_wait(&r_free, j & 1, &abort_flag))) break;
-                if (!(ok = mbar_wait(&a_full[ac & 1], (ac >> 1) & 1, &abort_flag))) break;
-                tc_fence_after();
-                {
-                    const uint32_t ta = tA0 + (ac & 1) * 64;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tR, ta + kk * 8, make_desc_sw128(s_base + kOffK + kmaj_off(kk, 128), 0, 1024), idG, kk > 0);
-                    mma_commit(&g_full);
-                    mma_commit(&a_empty[ac & 1]);
-                    ++ac;
+                const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
+                if (j + 1 < my_tiles) {
+                    const TileInfo tn = decode_tile(a, tile_id(j + 1));
+                    const size_t rn = (size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT;
+                    prefetch_l2(a.q + rn * kD, kTile);
+                    if (GATED) prefetch_l2(a.gam + rn * 64, kCT * 64 * 2);
                 }
-                // online: D_Y = P V
-                if (!(ok = mbar_wait(&y_empty[j & 1], ((j >> 1) & 1) ^ 1, &abort_flag))) break;
-                if (!(ok = mbar_wait(&a_full[ac & 1], (ac >> 1) & 1, &abort_flag))) break;
-                tc_fence_after();
-                {
-                    const uint32_t ta = tA0 + (ac & 1) * 64;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tY, ta + kk * 8, make_desc_sw128(s_base + kOffV + kk * 2048u, 16384, 1024), idPV, kk > 0);
-                    mma_commit(&a_empty[ac & 1]);
-                    mma_commit(&kv_empty);
-                    ++ac;
-                }
-                // cached states (and the chunk's prefix state)
-                bool next_scores = GATED && j + 1 < my_tiles;
+                uint8_t *dst = slot(kTile);
+                if (!(ok = dst != nullptr)) break;
+                tma_load_2d(dst, &mK, 0, rr, &ring_full[g % kRing]);
+                tma_load_2d(dst + 16384, &mK, 64, rr, &ring_full[g % kRing]);
+                ++g;
                 const int items = tile_items<GATED>(t);
                 for (int k = 0; k < items; ++k) {
-                    if (next_scores && mbar_try_wait(&u_full, (j + 1) & 1) && mbar_try_wait(&kb_full, (j + 1) & 1)) {
-                        if (!(ok = issue_scores(j + 1))) break;
-                        next_scores = false;
-                    }
+                    if (!(dst = slot(kTile))) break;
+                    bulk_load(dst, item_image<GATED>(a, t, k), kTile, &ring_full[g % kRing]);
+                    ++g;
+                }
+                if (!(ok = dst != nullptr)) break;
+                if (!(ok = (dst = slot(kTile)) != nullptr)) break;
+                tma_load_2d(dst, &mV, 0, rr, &ring_full[g % kRing]);
+                tma_load_2d(dst + 16384, &mV, 64, rr, &ring_full[g % kRing]);
+                ++g;
+            }
+        }
+    } else if (warp == 1 || warp == kT2Threads / 32 - 1) {
+        // ---------------------------------------------------------- MMA issuers
+        // Two issuing threads: a single thread cannot issue tcgen05.mma fast enough
+        // to keep the tensor pipe busy once its per-group bookkeeping is counted.
+        // Issuer 1 owns accumulator D1 (G, then the odd groups of a tile), issuer 0
+        // owns D0 (the even groups).  Group k of a tile is the k-th cached operand
+        // (prefix state first), the last group is P V.  Every ring and A slot has
+        // exactly one consumer, which commits its release.
+        if (lane == 0 && my_tiles > 0) {
+            const int me = warp == 1 ? 0 : 1;
+            constexpr uint32_t idKm = idesc_bf16(128, 128, false, false);  // B K-major
+            constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);   // B MN-major (V)
+            const uint64_t dRing0 = make_desc_sw128(s_base, 0, 1024);
+            const uint64_t dRingMN = make_desc_sw128(s_base, 16384, 1024);
+            uint32_t off128[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) off128[kk] = kmaj_off(kk, 128) >> 4;
+            const uint32_t tD = me ? tD1 : tD0;
+            uint32_t g = 0, ac = 0;  // ring / A-slot index of the tile's first slot
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                const TileInfo t = decode_tile(a, tile_id(j));
+                const int groups = tile_items<GATED>(t) + 1;
+                if (me == 1) {  // G = (g_n o Q) K^T into D1
                     const int s = g % kRing;
                     if (!(ok = mbar_wait(&ring_full[s], (g / kRing) & 1, &abort_flag))) break;
-                    if (!(ok = mbar_wait(&a_full[ac & 1], (ac >> 1) & 1, &abort_flag))) break;
+                    if (!(ok = mbar_wait(&a_full[ac % kASlots], (ac / kASlots) & 1, &abort_flag))) break;
+                    if (!(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;  // tile j-1 drained
                     tc_fence_after();
-                    const uint32_t ta = tA0 + (ac & 1) * 64;
-                    const uint32_t bb = s_base + kOffRing + s * kTile;
+                    const uint32_t ta = tA0 + (ac % kASlots) * 64;
+                    const uint64_t dB = dRing0 + ((s * kTile) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tY, ta + kk * 8, make_desc_sw128(bb + kmaj_off(kk, 128), 0, 1024), idC, 1);
+                    for (int kk = 0; kk < 8; ++kk) mma_ts(tD1, ta + kk * 8, dB + off128[kk], idKm, kk > 0);
+                    mma_commit(&g_full);
                     mma_commit(&ring_empty[s]);
-                    mma_commit(&a_empty[ac & 1]);
-                    ++g;
-                    ++ac;
+                    mma_commit(&a_empty[ac % kASlots]);
+                }
+                bool used = false;
+                for (int k = me; k < groups; k += 2) {
+                    const uint32_t rk = g + 1 + k, ak = ac + 1 + k;
+                    const int s = rk % kRing;
+                    if (!(ok = mbar_wait(&ring_full[s], (rk / kRing) & 1, &abort_flag))) break;
+                    if (!(ok = mbar_wait(&a_full[ak % kASlots], (ak / kASlots) & 1, &abort_flag))) break;
+                    if (!used) {
+                        // D0: tile j-1 drained; D1: G has been read by the aux warps
+                        if (me == 0 && !(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;
+                        if (me == 1 && !(ok = mbar_wait(&g_done, j & 1, &abort_flag))) break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ta = tA0 + (ak % kASlots) * 64;
+                    const uint32_t acc0 = used ? 1u : 0u;
+                    if (k == groups - 1) {  // P V: the V operand is MN-major, a K step is 16 rows
+                        const uint64_t dB = dRingMN + ((s * kTile) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) mma_ts(tD, ta + kk * 8, dB + kk * (2048u >> 4), idPV, acc0 | (kk > 0));
+                    } else {
+                        const uint64_t dB = dRing0 + ((s * kTile) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) mma_ts(tD, ta + kk * 8, dB + off128[kk], idKm, acc0 | (kk > 0));
+                    }
+                    mma_commit(&ring_empty[s]);
+                    mma_commit(&a_empty[ak % kASlots]);
+                    used = true;
                 }
                 if (!ok) break;
-                if (next_scores && !(ok = issue_scores(j + 1))) break;
-                mma_commit(&y_full[j & 1]);
+                mma_commit(&y_full);  // both issuers commit: the tile's sum is complete
+                g += 1 + groups;
+                ac += 1 + groups;
             }
         }
     } else if (warp < 6) {
@@ -581,9 +645,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         uint32_t ac = 0;
         bool ok = true;
         auto put_a = [&](const uint32_t (&src)[64], __nv_bfloat162 gam, bool scale) -> bool {
-            if (!mbar_wait(&a_empty[ac & 1], ((ac >> 1) & 1) ^ 1, &abort_flag)) return false;
+            if (!mbar_wait(&a_empty[ac % kASlots], ((ac / kASlots) & 1) ^ 1, &abort_flag)) return false;
             tc_fence_after();
-            const uint32_t ta = tA0 + (ac & 1) * 64 + lane_base;
+            const uint32_t ta = tA0 + (ac % kASlots) * 64 + lane_base;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 uint32_t r[16];
@@ -601,34 +665,28 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&a_full[ac & 1]);
+            mbar_arrive(&a_full[ac % kASlots]);
             ++ac;
             return true;
         };
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
-            uint32_t gm2[32];  // gates g_{t,i} as bf16 pairs (i even: low half)
-            float g_on = 1.f;
+            const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
+            uint32_t gm2[32];  // gates g_{t,i} as bf16 pairs (i even: low half); g_{t,n} at 63
             if (GATED) {
-                if (!(ok = mbar_wait(&gam_full, j & 1, &abort_flag))) break;
-                tc_fence_after();
+                const uint4 *gsrc = reinterpret_cast<const uint4 *>(a.gam + tok * 64);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t v[16];
-                    tmem_ld16(tR + lane_base + 16 * m, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) gm2[8 * m + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    if (m == 3) g_on = __uint_as_float(v[15]);
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 x = __ldg(gsrc + i);
+                    gm2[4 * i] = x.x;
+                    gm2[4 * i + 1] = x.y;
+                    gm2[4 * i + 2] = x.z;
+                    gm2[4 * i + 3] = x.w;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&r_free);
-            // the token's query row
-            uint32_t qp[64];
+            uint32_t qp[64];  // the token's query row, bf16 pairs
             {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    a.q + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row) * kD);
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + tok * kD);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint4 x = __ldg(src + i);
@@ -639,156 +697,108 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 }
             }
             const __nv_bfloat162 one2 = __float2bfloat162_rn(1.f);
-            if (!(ok = put_a(qp, one2, false))) break;  // Q for G = Q K^T
-            // P = g_on * mask(G): wait for G, write P as the next A operand
-            if (!(ok = mbar_wait(&g_full, j & 1, &abort_flag))) break;
-            tc_fence_after();
-            if (!(ok = mbar_wait(&a_empty[ac & 1], ((ac >> 1) & 1) ^ 1, &abort_flag))) break;
-            tc_fence_after();
-            {
-                const uint32_t ta = tA0 + (ac & 1) * 64 + lane_base;
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t x[16], z[16];
-                    tmem_ld16(tR + lane_base + 32 * h, x);
-                    tmem_ld16(tR + lane_base + 32 * h + 16, z);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t c0 = 32 * h + 2 * i;
-                        const float p0 = c0 <= row ? g_on * __uint_as_float(x[2 * i]) : 0.f;
-                        const float p1 = c0 + 1 <= row ? g_on * __uint_as_float(x[2 * i + 1]) : 0.f;
-                        pk[i] = pack_bf16x2(p0, p1);
-                        const uint32_t c1 = 32 * h + 16 + 2 * i;
-                        const float p2 = c1 <= row ? g_on * __uint_as_float(z[2 * i]) : 0.f;
-                        const float p3 = c1 + 1 <= row ? g_on * __uint_as_float(z[2 * i + 1]) : 0.f;
-                        pk[8 + i] = pack_bf16x2(p2, p3);
-                    }
-                    tmem_st16(ta + 16 * h, pk);
-                }
-                tc_fence_before();
-                mbar_arrive(&g_done);  // R has been read
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&a_full[ac & 1]);
-                ++ac;
-            }
-            // cached items
+            // g_n o Q: A operand of G and of the prefix state
+            __nv_bfloat162 gon2 = one2;
+            if (GATED) gon2 = __high2bfloat162(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31]));
+            if (!(ok = put_a(qp, gon2, GATED))) break;                  // for G
+            if (t.c > 0 && !(ok = put_a(qp, gon2, GATED))) break;      // for the prefix state
             if (GATED) {
-                const __nv_bfloat162 gon2 = __float2bfloat162_rn(g_on);
-                if (t.c > 0 && !(ok = put_a(qp, gon2, true))) break;
-#pragma unroll
-                for (int i = 0; i < 63; ++i) {
-                    if (i >= t.n) break;
-                    const __nv_bfloat162 pair = *reinterpret_cast<const __nv_bfloat162 *>(&gm2[i >> 1]);
-                    const __nv_bfloat162 gi2 = (i & 1) ? __high2bfloat162(pair) : __low2bfloat162(pair);
-                    if (!(ok = put_a(qp, gi2, true))) break;
+                // Rolled loop (one copy of put_a keeps the code small); the gate of
+                // segment i comes from a small per-thread array.
+                const __nv_bfloat16 *gl = reinterpret_cast<const __nv_bfloat16 *>(gm2);
+#pragma unroll 1
+                for (int i = 0; i < t.n; ++i) {
+                    if (!(ok = put_a(qp, __bfloat162bfloat162(gl[i]), true))) break;
                 }
                 if (!ok) break;
-            } else {
-                const int items = tile_items<GATED>(t);
-                for (int k = 0; k < items && ok; ++k) ok = put_a(qp, one2, false);
+            } else if (t.n > 0) {
+                if (!(ok = put_a(qp, one2, false))) break;
             }
+            // The tile's last A slot carries P.  The A warps claim it in order (so
+            // every wait on a slot stays within one phase of its barrier) and hand it
+            // to the aux warps, after the previous tile's P has been written.
+            if (j > 0 && !(ok = mbar_wait(&p_written, (j - 1) & 1, &abort_flag))) break;
+            if (!(ok = mbar_wait(&a_empty[ac % kASlots], ((ac / kASlots) & 1) ^ 1, &abort_flag))) break;
+            mbar_arrive(&p_slot);
+            ++ac;
         }
     } else {
-        // ---------------------------------------------------------- aux: next-tile gates, drain
+        // ---------------------------------------------------------- aux: P, drain
         const int q4 = warp & 3;
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         bool ok = true;
-        auto pre = [&](int jn) -> bool {
-            const TileInfo t = decode_tile(a, tile_id(jn));
-            const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.u + tok * kD);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 x = __ldg(src + 4 * m + i);
-                        r[4 * i] = x.x;
-                        r[4 * i + 1] = x.y;
-                        r[4 * i + 2] = x.z;
-                        r[4 * i + 3] = x.w;
-                    }
-                    tmem_st16(tR + 64 + lane_base + 16 * m, r);
-                }
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(&u_full);
-            const float ron = a.r_on[tok];
-            if (!mbar_wait(&sc_full, jn & 1, &abort_flag)) return false;
-            tc_fence_after();
-            float sc[64];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                uint32_t v[16];
-                tmem_ld16(tR + lane_base + 16 * m, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sc[16 * m + i] = __uint_as_float(v[i]);
-            }
-            float mx = ron;
-#pragma unroll
-            for (int i = 0; i < 63; ++i)
-                if (i < t.n) mx = fmaxf(mx, sc[i]);
-            float z = expf(ron - mx);
-#pragma unroll
-            for (int i = 0; i < 63; ++i) {
-                if (i < t.n) {
-                    sc[i] = expf(sc[i] - mx);
-                    z += sc[i];
-                }
-            }
-            const float inv = 1.f / z;
-#pragma unroll
-            for (int i = 0; i < 63; ++i) sc[i] *= inv;
-            sc[63] = expf(ron - mx) * inv;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                uint32_t r[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(sc[16 * m + i]);
-                tmem_st16(tR + lane_base + 16 * m, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&gam_full);
-            return true;
-        };
-        if (GATED && my_tiles > 0) ok = pre(0);
+        uint32_t ac = 0;  // A-slot counter, kept in step with the A warps and the MMA warp
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
-            if (GATED && j + 1 < my_tiles) {
-                if (!(ok = mbar_wait(&g_done, j & 1, &abort_flag))) break;
-                tc_fence_after();
-                if (!(ok = pre(j + 1))) break;
-            }
-            // drain D_Y of tile j into y
-            if (!(ok = mbar_wait(&y_full[j & 1], (j >> 1) & 1, &abort_flag))) break;
+            ac += 1 + (uint32_t)tile_items<GATED>(t);  // the G slot and the cached operands' slots
+            // P = mask(G): G already carries the online gate g_n through its A operand
+            if (!(ok = mbar_wait(&g_full, j & 1, &abort_flag))) break;
             tc_fence_after();
-            const uint32_t tY = tY0 + (j & 1) * 128 + lane_base;
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row) * kD);
+            uint32_t pk[64];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint32_t x[16], z[16];
-                tmem_ld16(tY + 32 * h, x);
-                tmem_ld16(tY + 32 * h + 16, z);
+                tmem_ld16(tD1 + lane_base + 32 * h, x);
+                tmem_ld16(tD1 + lane_base + 32 * h + 16, z);
                 tmem_wait_ld();
-                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-#pragma unroll
-                for (int i = 0; i < 8; ++i) pk[8 + i] = pack_bf16x2(__uint_as_float(z[2 * i]), __uint_as_float(z[2 * i + 1]));
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[4 * h + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t c0 = 32 * h + 2 * i, c1 = c0 + 16;
+                    pk[16 * h + i] = pack_bf16x2(c0 <= row ? __uint_as_float(x[2 * i]) : 0.f,
+                                                 c0 + 1 <= row ? __uint_as_float(x[2 * i + 1]) : 0.f);
+                    pk[16 * h + 8 + i] = pack_bf16x2(c1 <= row ? __uint_as_float(z[2 * i]) : 0.f,
+                                                     c1 + 1 <= row ? __uint_as_float(z[2 * i + 1]) : 0.f);
+                }
             }
             tc_fence_before();
-            mbar_arrive(&y_empty[j & 1]);
+            mbar_arrive(&g_done);
+            if (!(ok = mbar_wait(&p_slot, j & 1, &abort_flag))) break;  // claimed for us by the A warps
+            tc_fence_after();
+            {
+                const uint32_t ta = tA0 + (ac % kASlots) * 64 + lane_base;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = pk[16 * h + i];
+                    tmem_st16(ta + 16 * h, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&a_full[ac % kASlots]);
+                mbar_arrive(&p_written);
+                ++ac;
+            }
+            // drain: y = D0 (+ D1 when the tile wrote both accumulators)
+            const bool both = tile_groups<GATED>(t) >= 2;
+            if (!(ok = mbar_wait(&y_full, j & 1, &abort_flag))) break;
+            tc_fence_after();
+            uint4 *dst = reinterpret_cast<uint4 *>(a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row) * kD);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t x[16], z[16], x1[16], z1[16];
+                tmem_ld16(tD0 + lane_base + 32 * h, x);
+                tmem_ld16(tD0 + lane_base + 32 * h + 16, z);
+                if (both) {
+                    tmem_ld16(tD1 + lane_base + 32 * h, x1);
+                    tmem_ld16(tD1 + lane_base + 32 * h + 16, z1);
+                }
+                tmem_wait_ld();
+                float f[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    f[i] = __uint_as_float(x[i]) + (both ? __uint_as_float(x1[i]) : 0.f);
+                    f[16 + i] = __uint_as_float(z[i]) + (both ? __uint_as_float(z1[i]) : 0.f);
+                }
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[4 * h + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+            tc_fence_before();
+            mbar_arrive(&y_empty);
         }
     }
     tc_fence_before();
@@ -830,7 +840,10 @@ size_t tc_scratch_bytes(const Problem &p)
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
     size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) +
                pad256(sizeof(float) * BH * p.L);
-    if (p.mode == MC_RESIDUAL) b += pad256(BH * N * kTile);
+    if (p.mode == MC_RESIDUAL)
+        b += pad256(BH * N * kTile);  // prefix sums of the states
+    else
+        b += pad256(sizeof(__nv_bfloat16) * BH * p.L * 64);  // gates
     return b;
 }
 
@@ -853,6 +866,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
+    a.gam = gated ? reinterpret_cast<__nv_bfloat16 *>(base) : nullptr;
     a.BH = p.BH;
     a.L = p.L;
     a.C = p.C;
@@ -895,6 +909,12 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         prefix_images<<<grid, 256, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "prefix_images");
+    } else {
+        e = cudaFuncSetAttribute(gates_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
+        if (e != cudaSuccess) return e;
+        gates_tc<<<(unsigned)(BH * (p.L / kCT)), 128, kGatesSmem, s>>>(mU, a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        profile_after_kernel(s, "gates_tc");
     }
     {
         auto k2 = gated ? readout_tc<true> : readout_tc<false>;
