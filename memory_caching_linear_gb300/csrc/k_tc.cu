@@ -327,98 +327,147 @@ __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
 //   g_{t,i} = exp(r_{t,i} - m) / Z (i < n),  g_{t,n} = exp(r_on[t] - m) / Z
 // written as bf16: gam[token][i] for i < n and gam[token][63] for the online memory.
 // ============================================================================
-constexpr size_t kGatesSmem = 2 * kTile + 1024;
+constexpr int kGatesThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + store
+constexpr size_t kGatesSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
 
-__global__ void __launch_bounds__(128) gates_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
+// Persistent: CTA b handles the contiguous tile range [b*per, (b+1)*per) of the
+// (bh, chunk) tiles, so consecutive tiles share a head and its kbar image.
+__global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t bar_load, bar_mma;
+    uint8_t *sU = sm, *sKb = sm + 2 * kTile;
+    __shared__ uint64_t u_full[2], u_empty[2], kb_full, kb_empty, s_full[2], s_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunks = a.L / kCT;
-    const int bh = blockIdx.x / chunks;
-    const int t0 = (blockIdx.x % chunks) * kCT;
-    const int n = t0 / a.C;
+    const int total = a.BH * chunks;
+    const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int first = (int)blockIdx.x * per;
+    const int last = min(total, first + per);  // tiles [first, last)
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 64);
+        tmem_alloc(&tmem_base, 128);
         tmem_relinquish();
     }
     if (threadIdx.x == 32) {
         abort_flag = 0;
-        mbar_init(&bar_load, 1);
-        mbar_init(&bar_mma, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&u_full[i], 1);
+            mbar_init(&u_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 128);
+        }
+        mbar_init(&kb_full, 1);
+        mbar_init(&kb_empty, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    if (threadIdx.x == 0) {
-        const int rr = bh * a.L + t0;
-        mbar_arrive_expect_tx(&bar_load, 2 * kTile);
-        tma_load_2d(sm, &mU, 0, rr, &bar_load);
-        tma_load_2d(sm + 16384, &mU, 64, rr, &bar_load);
-        bulk_load(sm + kTile, a.kbar_img + (size_t)bh * kTile, kTile, &bar_load);
-    }
-    bool ok = mbar_wait(&bar_load, 0, &abort_flag);
-    if (threadIdx.x == 0 && ok) {
-        tc_fence_after();
-        constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
-        const uint64_t dU = make_desc_sw128(smem_u32(sm), 0, 1024);
-        const uint64_t dKb = make_desc_sw128(smem_u32(sm + kTile), 0, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tb, dU + (kmaj_off(kk, 128) >> 4), dKb + (kmaj_off(kk, 64) >> 4), idS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tb, dU + (kmaj_off(kk, 128) >> 4), dKb + ((16384 + kmaj_off(kk, 64)) >> 4), idS, 1);
-        mma_commit(&bar_mma);
-    }
-    if (ok) ok = mbar_wait(&bar_mma, 0, &abort_flag);
-    tc_fence_after();
-    const uint32_t row = 32 * warp + lane;
-    float sc[64];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        uint32_t v[16];
-        tmem_ld16(tb + ((uint32_t)(32 * warp) << 16) + 16 * m, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sc[16 * m + i] = __uint_as_float(v[i]);
-    }
-    if (ok) {
-        const size_t tok = (size_t)bh * a.L + t0 + row;
-        const float ron = a.r_on[tok];
-        float mx = ron;
-#pragma unroll
-        for (int i = 0; i < 63; ++i)
-            if (i < n) mx = fmaxf(mx, sc[i]);
-        float z = expf(ron - mx);
-#pragma unroll
-        for (int i = 0; i < 63; ++i) {
-            if (i < n) {
-                sc[i] = expf(sc[i] - mx);
-                z += sc[i];
-            } else {
-                sc[i] = 0.f;
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&mU);
+            int kb_round = 0, prev_bh = -1;
+            for (int it = first; it < last; ++it) {
+                const int i = it - first;
+                const int bh = it / chunks, t0 = (it % chunks) * kCT;
+                if (bh != prev_bh) {
+                    if (!mbar_wait(&kb_empty, (kb_round & 1) ^ 1, &abort_flag)) break;
+                    mbar_arrive_expect_tx(&kb_full, kTile);
+                    bulk_load(sKb, a.kbar_img + (size_t)bh * kTile, kTile, &kb_full);
+                    ++kb_round;
+                    prev_bh = bh;
+                }
+                const int b = i & 1;
+                if (!mbar_wait(&u_empty[b], ((i >> 1) & 1) ^ 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&u_full[b], kTile);
+                tma_load_2d(sU + b * kTile, &mU, 0, bh * a.L + t0, &u_full[b]);
+                tma_load_2d(sU + b * kTile + 16384, &mU, 64, bh * a.L + t0, &u_full[b]);
             }
         }
-        const float inv = 1.f / z;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+            const uint64_t dKb = make_desc_sw128(smem_u32(sKb), 0, 1024);
+            int kb_round = 0, prev_bh = -1;
+            for (int it = first; it < last; ++it) {
+                const int i = it - first, b = i & 1;
+                const int bh = it / chunks;
+                if (bh != prev_bh) {
+                    if (!mbar_wait(&kb_full, kb_round & 1, &abort_flag)) break;
+                    ++kb_round;
+                    prev_bh = bh;
+                }
+                if (!mbar_wait(&u_full[b], (i >> 1) & 1, &abort_flag)) break;
+                if (!mbar_wait(&s_empty[b], ((i >> 1) & 1) ^ 1, &abort_flag)) break;
+                tc_fence_after();
+                const uint64_t dU = make_desc_sw128(smem_u32(sU + b * kTile), 0, 1024);
+                const uint32_t td = tb + b * 64;
 #pragma unroll
-        for (int i = 0; i < 63; ++i) sc[i] *= inv;
-        sc[63] = expf(ron - mx) * inv;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.gam + tok * 64);
+                for (int kk = 0; kk < 8; ++kk) mma_ss(td, dU + (kmaj_off(kk, 128) >> 4), dKb + (kmaj_off(kk, 64) >> 4), idS, kk > 0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            dst[i] = make_uint4(pack_bf16x2(sc[8 * i], sc[8 * i + 1]), pack_bf16x2(sc[8 * i + 2], sc[8 * i + 3]),
-                                pack_bf16x2(sc[8 * i + 4], sc[8 * i + 5]), pack_bf16x2(sc[8 * i + 6], sc[8 * i + 7]));
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(td, dU + (kmaj_off(kk, 128) >> 4), dKb + ((16384 + kmaj_off(kk, 64)) >> 4), idS, 1);
+                mma_commit(&s_full[b]);
+                mma_commit(&u_empty[b]);
+                if (it + 1 == last || (it + 1) / chunks != bh) mma_commit(&kb_empty);  // last tile of this head
+            }
+        }
+    } else {
+        // Two epilogue groups (warps 2-5 and 6-9) take alternate tiles, matching the
+        // two score buffers.
+        const int grp = (warp - 2) >> 2;
+        const int q4 = warp & 3;
+        const uint32_t row = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        for (int it = first + grp; it < last; it += 2) {
+            const int i = it - first, b = i & 1;
+            const int bh = it / chunks, t0 = (it % chunks) * kCT;
+            const int n = t0 / a.C;
+            if (!mbar_wait(&s_full[b], (i >> 1) & 1, &abort_flag)) break;
+            tc_fence_after();
+            float sc[64];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint32_t v[16];
+                tmem_ld16(tb + b * 64 + lane_base + 16 * m, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) sc[16 * m + k] = __uint_as_float(v[k]);
+            }
+            tc_fence_before();
+            mbar_arrive(&s_empty[b]);
+            const size_t tok = (size_t)bh * a.L + t0 + row;
+            const float ron = a.r_on[tok];
+            float mx4[4] = {ron, ron, ron, ron};  // partial maxima / sums: shorter dependency chains
+#pragma unroll
+            for (int k = 0; k < 63; ++k)
+                if (k < n) mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 63; ++k) {
+                sc[k] = k < n ? expf(sc[k] - mx) : 0.f;
+                z4[k & 3] += sc[k];
+            }
+            sc[63] = expf(ron - mx);
+            const float inv = 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
+            uint4 *dst = reinterpret_cast<uint4 *>(a.gam + tok * 64);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                dst[k] = make_uint4(pack_bf16x2(sc[8 * k] * inv, sc[8 * k + 1] * inv),
+                                    pack_bf16x2(sc[8 * k + 2] * inv, sc[8 * k + 3] * inv),
+                                    pack_bf16x2(sc[8 * k + 4] * inv, sc[8 * k + 5] * inv),
+                                    pack_bf16x2(sc[8 * k + 6] * inv, sc[8 * k + 7] * inv));
+        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tb, 64);
+        tmem_dealloc(tb, 128);
     }
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
 }
@@ -912,7 +961,9 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     } else {
         e = cudaFuncSetAttribute(gates_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
         if (e != cudaSuccess) return e;
-        gates_tc<<<(unsigned)(BH * (p.L / kCT)), 128, kGatesSmem, s>>>(mU, a);
+        const int gtiles = (int)(BH * (p.L / kCT));
+        const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
+        gates_tc<<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "gates_tc");
     }
