@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    __shared__ uint64_t full[2], empty[2], r_full, r_free, s_ready, s_read;
+    __shared__ uint64_t full[2], empty[2], r_full[2], r_empty[2], z_full[2], z_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ float ksum_s[kD];
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     const int nch = a.CPS;
 
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 256);
+        tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
     if (threadIdx.x == 32) {
@@ -158,11 +158,11 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1 + 4);  // MMA commit + one arrive per worker warp
+            mbar_init(&r_full[s], 1);
+            mbar_init(&r_empty[s], 128);
+            mbar_init(&z_full[s], 1);
+            mbar_init(&z_empty[s], 128);
         }
-        mbar_init(&r_full, 1);
-        mbar_init(&r_free, 128);
-        mbar_init(&s_ready, 1);
-        mbar_init(&s_read, 128);
         fence_mbar_init();
     }
     if (threadIdx.x >= 64) ksum_s[threadIdx.x - 64] = 0.f;
@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t tR = tb, tS = tb + 128;
+    // tensor memory: R (U K^T) x 2 | Z (chunk state V^T K) x 2, 128 columns each
+    const uint32_t tR0 = tb, tZ0 = tb + 256;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -199,71 +200,65 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             constexpr uint32_t idR = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idS = idesc_bf16(128, 128, true, true);
             for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
+                const int s = c & 1, b = c & 1;
                 const uint32_t r = c >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sm + s * kT1Stage), vb = kb + kTile, ub = kb + 2 * kTile;
-                if (GATED) {
-                    if (!mbar_wait(&r_free, (c & 1) ^ 1, &abort_flag)) break;
+                if (GATED) {  // R = U K^T (online gate score of the chunk's tokens)
+                    if (!mbar_wait(&r_empty[b], (r & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tR, make_desc_sw128(ub + kmaj_off(kk, 128), 0, 1024),
+                        mma_ss(tR0 + b * 128, make_desc_sw128(ub + kmaj_off(kk, 128), 0, 1024),
                                make_desc_sw128(kb + kmaj_off(kk, 128), 0, 1024), idR, kk > 0);
-                    mma_commit(&r_full);
+                    mma_commit(&r_full[b]);
                 }
-                if (!mbar_wait(&s_read, c & 1, &abort_flag)) break;
+                // Z = V^T K, the chunk's own state (fresh accumulator)
+                if (!mbar_wait(&z_empty[b], (r & 1) ^ 1, &abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tS, make_desc_sw128(vb + kk * 2048u, 16384, 1024), make_desc_sw128(kb + kk * 2048u, 16384, 1024),
-                           idS, (c > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&s_ready);
+                    mma_ss(tZ0 + b * 128, make_desc_sw128(vb + kk * 2048u, 16384, 1024),
+                           make_desc_sw128(kb + kk * 2048u, 16384, 1024), idS, kk > 0);
+                mma_commit(&z_full[b]);
                 mma_commit(&empty[s]);
             }
         }
     } else {
         const int q4 = warp & 3;
-        const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (S) = key column (sums)
+        const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (Z, S) = key column (sums)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        float S[kD];  // running state row: S[row][k] = sum_{j before the chunk} v_j[row] k_j[k]
+#pragma unroll
+        for (int k = 0; k < kD; ++k) S[k] = 0.f;
         float ks = 0.f;  // running sum of key column `row` over the segment, in token order
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
-            const int s = c & 1;
+            const int s = c & 1, b = c & 1;
             const uint32_t r = c >> 1;
-            if (ok && c > 0) {  // the state before chunk c, as the chunk's prefix-state image
-                ok = mbar_wait(&s_ready, (c - 1) & 1, &abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    uint8_t *img = a.spre_img + (((size_t)bh * a.N + seg) * a.CPS + c) * kTile;
-                    tmem_row_to_image(tS + lane_base, row, img, nullptr);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&s_read);
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
             const uint8_t *st = sm + s * kT1Stage;
             if (GATED && ok) {
                 float dot = 0.f;  // <u_t, keys of the segment before this chunk>
                 for (int k = 0; k < kD; ++k) dot = fmaf(bf16_at(st + 2 * kTile, row, k, 128), ksum_s[k], dot);
-                ok = mbar_wait(&r_full, c & 1, &abort_flag);
+                ok = mbar_wait(&r_full[b], r & 1, &abort_flag);
                 if (ok) {
                     tc_fence_after();
                     float w = 0.f;  // sum_{j <= t} <u_t, k_j> within the chunk
 #pragma unroll
                     for (int j16 = 0; j16 < 8; ++j16) {
                         uint32_t v[16];
-                        tmem_ld16(tR + lane_base + 16 * j16, v);
+                        tmem_ld16(tR0 + b * 128 + lane_base + 16 * j16, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             if ((uint32_t)(16 * j16 + i) <= row) w += __uint_as_float(v[i]);
                     }
                     tc_fence_before();
-                    mbar_arrive(&r_free);
+                    mbar_arrive(&r_empty[b]);
                     const int t_in_seg = c * kCT + (int)row;
                     a.r_on[(size_t)row0 + t_in_seg] = (dot + w) / (float)(t_in_seg + 1);
                 }
@@ -278,26 +273,49 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             named_bar_sync(1, 128);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        if (ok && !abort_flag && mbar_wait(&s_ready, (nch - 1) & 1, &abort_flag)) {
-            tc_fence_after();
-            const size_t sidx = (size_t)bh * a.N + seg;
-            tmem_row_to_image(tS + lane_base, row, a.states_img + sidx * kTile, a.states + sidx * kD * kD + (size_t)row * kD);
-            if (GATED) {
-                const float kb = ks / (float)a.C;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
-                uint8_t *img = a.kbar_img + (size_t)bh * kTile;
-                *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(seg, row, 64)) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(img + 16384 + sw128_offset(seg, row, 64)) = lo;
+            // S += Z_c; then S is the prefix state of chunk c + 1
+            if (ok) ok = mbar_wait(&z_full[b], r & 1, &abort_flag);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int j16 = 0; j16 < 8; ++j16) {
+                    uint32_t v[16];
+                    tmem_ld16(tZ0 + b * 128 + lane_base + 16 * j16, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) S[16 * j16 + i] += __uint_as_float(v[i]);
+                }
+                tc_fence_before();
+                mbar_arrive(&z_empty[b]);
+                const size_t sidx = (size_t)bh * a.N + seg;
+                uint8_t *img = c + 1 < nch ? a.spre_img + (sidx * a.CPS + c + 1) * kTile : a.states_img + sidx * kTile;
+#pragma unroll
+                for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunks of 8 bf16
+                    const uint4 v = make_uint4(pack_bf16x2(S[8 * cc], S[8 * cc + 1]), pack_bf16x2(S[8 * cc + 2], S[8 * cc + 3]),
+                                               pack_bf16x2(S[8 * cc + 4], S[8 * cc + 5]), pack_bf16x2(S[8 * cc + 6], S[8 * cc + 7]));
+                    *reinterpret_cast<uint4 *>(img + sw128_offset(row, 8 * cc, 128)) = v;
+                }
+                if (c + 1 == nch) {  // the segment's cached state, fp32
+                    float4 *o = reinterpret_cast<float4 *>(a.states + sidx * kD * kD + (size_t)row * kD);
+#pragma unroll
+                    for (int i = 0; i < kD / 4; ++i) o[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+                }
             }
+        }
+        if (ok && GATED && !abort_flag) {
+            const float kb = ks / (float)a.C;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
+            uint8_t *img = a.kbar_img + (size_t)bh * kTile;
+            *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(seg, row, 64)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(img + 16384 + sw128_offset(seg, row, 64)) = lo;
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tb, 256);
+        tmem_dealloc(tb, 512);
     }
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
 }
