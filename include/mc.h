@@ -34,8 +34,9 @@
  *     Every pointer must be 16-byte aligned.
  *   - Work is enqueued on `stream` (any stream, NULL = the legacy default
  *     stream) and the call returns without synchronising.  Scratch is taken from
- *     the stream-ordered allocator (cudaMallocAsync) and released on the same
- *     stream.  Calls on different streams are independent.
+ *     a library-owned stream-ordered memory pool of the current device and freed
+ *     on the same stream; the pool keeps freed blocks for later calls until
+ *     mc_trim_scratch().  Calls on different streams are independent.
  *   - d must be 16, 32, 64 or 128.  B, H, L, seg_len >= 1.
  *   - Return value: MC_OK (0) or a negative MC_ERR_* code (shape is checked
  *     first, then the mode, then pointers).  On an argument
@@ -147,6 +148,13 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u,
 int mc_forward_noalloc(const void *q, const void *k, const void *v, const void *u,
                        int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
                        void *y, float *states, mc_stream_t stream);
+
+/*
+ * mc_trim_scratch -- return the scratch memory cached by the library's pool on
+ *   the current device to the driver (blocks still in use by enqueued work are
+ *   kept).  Returns MC_OK or MC_ERR_CUDA.
+ */
+int mc_trim_scratch(void);
 
 /*
  * mc_check_device -- synchronise `stream`, then report whether any tensor-core

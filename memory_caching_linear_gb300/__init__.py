@@ -25,7 +25,8 @@ MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = 
 MC_ERR_SCRATCH = -10
 
 EXPORTED = ("mc_forward", "mc_forward_f32", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
-            "mc_check_device", "mc_profile_begin", "mc_profile_end", "mc_profile_stage", "mc_status_string")
+            "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
+            "mc_status_string")
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmc.so")
@@ -57,6 +58,8 @@ def load_library():
     lib.mc_forward_host.restype = i
     lib.mc_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
     lib.mc_forward_noalloc.restype = i
+    lib.mc_trim_scratch.argtypes = []
+    lib.mc_trim_scratch.restype = i
     lib.mc_check_device.argtypes = [vp]
     lib.mc_check_device.restype = i
     lib.mc_profile_begin.argtypes = [vp, i]
@@ -153,6 +156,11 @@ def mc_check_device(stream=None) -> int:
     """Synchronise the stream and return MC_OK or MC_ERR_DEVICE_TIMEOUT (a kernel gave up
     on a bounded wait since the last check)."""
     return load_library().mc_check_device(_stream_handle(stream, torch.device("cuda")))
+
+
+def mc_trim_scratch() -> int:
+    """Return the library's cached scratch memory on the current device to the driver."""
+    return load_library().mc_trim_scratch()
 
 
 def mc_ssc_select(k, u, seg_len: int, topk: int, *, idx=None, stream=None):

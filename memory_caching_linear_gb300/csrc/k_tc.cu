@@ -53,6 +53,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kD = 128;            // head dimension of this path
+constexpr int kTcMaxTopk = 16;     // SSC selections per token handled by the tensor-core path
 constexpr int kCT = 128;           // tokens per chunk / tile
 constexpr uint32_t kTile = 32768;  // one 128 x 128 bf16 operand tile
 
@@ -66,6 +67,8 @@ struct TcArgs {
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
     __nv_bfloat16 *gam;   // [BH][L][64] gates: g_i at column i < n, g_n at column 63
+    int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
+    int topk;             // SSC: cached segments selected per token
     int BH, L, C, N, CPS;
     int num_tiles;
 };
@@ -320,6 +323,24 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
 }
 
+// Key means alone, as hi/lo bf16 image rows (for the stand-alone SSC router):
+// the same sequential fp32 sum over the segment's tokens as seg_state_tc, so the
+// router sees bit-identical scores.
+__global__ void __launch_bounds__(kD) kbar_images_tc(const __nv_bfloat16 *__restrict__ k, TcArgs a)
+{
+    const int seg = blockIdx.x % a.N, bh = blockIdx.x / a.N;
+    const int col = threadIdx.x;
+    const __nv_bfloat16 *src = k + ((size_t)bh * a.L + (size_t)seg * a.C) * kD + col;
+    float s = 0.f;
+    for (int t = 0; t < a.C; ++t) s += __bfloat162float(src[(size_t)t * kD]);
+    const float kb = s / (float)a.C;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
+    uint8_t *img = a.kbar_img + (size_t)bh * kTile;
+    *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(seg, col, 64)) = hi;
+    *reinterpret_cast<__nv_bfloat16 *>(img + 16384 + sw128_offset(seg, col, 64)) = lo;
+}
+
 // Residual: prefix sums of the cached states, P_n = sum_{i<n} M^(i) (fp32
 // accumulate), written as bf16 operand images (P_0 is never read).
 __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
@@ -350,6 +371,7 @@ constexpr size_t kGatesSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
 
 // Persistent: CTA b handles the contiguous tile range [b*per, (b+1)*per) of the
 // (bh, chunk) tiles, so consecutive tiles share a head and its kbar image.
+template <bool SSC>
 __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -458,20 +480,44 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             tc_fence_before();
             mbar_arrive(&s_empty[b]);
             const size_t tok = (size_t)bh * a.L + t0 + row;
-            const float ron = a.r_on[tok];
+            const float ron = a.r_on ? a.r_on[tok] : 0.f;  // no r_on: router only
+            // GRM / Soup: every cached segment takes part.  SSC ([MC-sum §3.4]): the
+            // topk largest scores, equal scores to the lower segment index.
+            uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
+            if (SSC) {
+                const int cnt = min(a.topk, n);
+                uint64_t chosen = 0;
+                int32_t *so = a.sel_out ? a.sel_out + tok * a.topk : nullptr;
+                for (int r = 0; r < cnt; ++r) {
+                    float best = 0.f;
+                    int bi = -1;
+#pragma unroll
+                    for (int k = 0; k < 63; ++k)
+                        if (k < n && !((chosen >> k) & 1ull) && (bi < 0 || sc[k] > best)) {
+                            best = sc[k];
+                            bi = k;
+                        }
+                    chosen |= 1ull << bi;
+                    if (so) so[r] = bi;
+                }
+                if (so)
+                    for (int r = cnt; r < a.topk; ++r) so[r] = -1;
+                take = chosen;
+            }
             float mx4[4] = {ron, ron, ron, ron};  // partial maxima / sums: shorter dependency chains
 #pragma unroll
             for (int k = 0; k < 63; ++k)
-                if (k < n) mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
+                if ((take >> k) & 1ull) mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 63; ++k) {
-                sc[k] = k < n ? expf(sc[k] - mx) : 0.f;
+                sc[k] = ((take >> k) & 1ull) ? expf(sc[k] - mx) : 0.f;
                 z4[k & 3] += sc[k];
             }
             sc[63] = expf(ron - mx);
             const float inv = 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
+            if (!a.gam) continue;  // router only (mc_ssc_select)
             uint4 *dst = reinterpret_cast<uint4 *>(a.gam + tok * 64);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -899,7 +945,8 @@ cudaError_t take_device_abort(int *was_set)
 bool tc_supported(const Problem &p)
 {
     return p.bf16 && p.d == kD && p.C % kCT == 0 && p.L % p.C == 0 && p.N <= 64 &&
-           (p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_RESIDUAL);
+           (p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_RESIDUAL ||
+            (p.mode == MC_SSC && p.topk >= 0 && p.topk <= kTcMaxTopk));
 }
 
 size_t tc_scratch_bytes(const Problem &p)
@@ -912,6 +959,41 @@ size_t tc_scratch_bytes(const Problem &p)
     else
         b += pad256(sizeof(__nv_bfloat16) * BH * p.L * 64);  // gates
     return b;
+}
+
+// SSC router alone (mc_ssc_select) on the tensor-core path's shapes: key-mean
+// images, then the SSC gates kernel with only the router output enabled.
+size_t tc_select_scratch_bytes(const Problem &p) { return pad256((size_t)p.BH * kTile); }
+
+cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
+{
+    TcArgs a{};
+    a.kbar_img = static_cast<uint8_t *>(scratch);
+    a.sel_out = fa.sel_out;
+    a.topk = p.topk;
+    a.BH = p.BH;
+    a.L = p.L;
+    a.C = p.C;
+    a.N = p.N;
+    a.CPS = p.C / kCT;
+    CUtensorMap mU;
+    if (!make_tmap_bf16_sw128(&mU, fa.u, (unsigned long long)p.BH * p.L, kD, 128)) return cudaErrorInvalidValue;
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 148;
+    }
+    cudaError_t e = cudaMemsetAsync(a.kbar_img, 0, (size_t)p.BH * kTile, s);
+    if (e != cudaSuccess) return e;
+    kbar_images_tc<<<(unsigned)(p.BH * p.N), kD, 0, s>>>(static_cast<const __nv_bfloat16 *>(fa.k), a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gates_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
+    if (e != cudaSuccess) return e;
+    const int gtiles = p.BH * (p.L / kCT);
+    const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
+    gates_tc<true><<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
@@ -934,6 +1016,8 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
     a.gam = gated ? reinterpret_cast<__nv_bfloat16 *>(base) : nullptr;
+    a.sel_out = fa.sel_out;
+    a.topk = p.topk;
     a.BH = p.BH;
     a.L = p.L;
     a.C = p.C;
@@ -977,11 +1061,12 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "prefix_images");
     } else {
-        e = cudaFuncSetAttribute(gates_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
+        auto kg = p.mode == MC_SSC ? gates_tc<true> : gates_tc<false>;
+        e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
         if (e != cudaSuccess) return e;
         const int gtiles = (int)(BH * (p.L / kCT));
         const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
-        gates_tc<<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
+        kg<<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "gates_tc");
     }

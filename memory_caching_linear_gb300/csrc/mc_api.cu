@@ -2,10 +2,52 @@
 // scratch, and the choice of kernels for a shape.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "mc_internal.cuh"
 
 namespace mc {
+
+namespace {
+// Scratch comes from a library-owned stream-ordered pool per device that keeps
+// freed blocks cached (release threshold = all), so repeated calls -- including
+// calls that synchronise, like mc_forward_host -- do not re-map device memory.
+// mc_trim_scratch() returns the cached memory to the driver.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[64];
+
+cudaMemPool_t scratch_pool()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pools[dev] = pool;
+    }
+    return g_pools[dev];
+}
+}  // namespace
+
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s)
+{
+    cudaMemPool_t pool = scratch_pool();
+    if (!pool) return cudaMallocAsync(p, bytes, s);
+    return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
 
 namespace {
 struct ProfileState {
@@ -118,7 +160,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     if (tc_supported(p)) {
         const size_t b_states = states ? 0 : round_up(sizeof(float) * (size_t)p.BH * p.N * d * d);
         void *scratch = nullptr;
-        if (cudaMallocAsync(&scratch, b_states + tc_scratch_bytes(p), stream) != cudaSuccess) {
+        if (scratch_alloc(&scratch, b_states + tc_scratch_bytes(p), stream) != cudaSuccess) {
             cudaGetLastError();
             return MC_ERR_ALLOC;
         }
@@ -127,7 +169,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         a.u = p.mode == MC_RESIDUAL ? nullptr : u;
         a.y = y;
         a.states = states ? states : static_cast<float *>(scratch);
-        a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = 0;
+        a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
         cudaError_t e = launch_forward_tc(p, a, static_cast<char *>(scratch) + b_states, stream);
         cudaError_t ef = cudaFreeAsync(scratch, stream);
         if (e != cudaSuccess || ef != cudaSuccess) {
@@ -139,7 +181,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
 
     const ScratchPlan plan = plan_scratch(p, states == nullptr);
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, plan.total, stream) != cudaSuccess) {
+    if (scratch_alloc(&scratch, plan.total, stream) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_ALLOC;
     }
@@ -206,8 +248,24 @@ int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int 
     p.bf16 = is_bf16 != 0;
     p.mode = MC_SSC;
     p.topk = topk;
+    if (mc::tc_supported(p)) {  // the tensor-core forward's own router, bit for bit
+        void *scratch = nullptr;
+        if (mc::scratch_alloc(&scratch, mc::tc_select_scratch_bytes(p), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_ALLOC;
+        }
+        mc::FwdArgs a{};
+        a.k = k; a.u = u; a.sel_out = idx;
+        cudaError_t e = mc::launch_ssc_select_tc(p, a, scratch, stream);
+        cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e != cudaSuccess || ef != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_CUDA;
+        }
+        return MC_OK;
+    }
     float *kbar = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&kbar), sizeof(float) * (size_t)p.BH * p.N * d, stream) !=
+    if (mc::scratch_alloc(reinterpret_cast<void **>(&kbar), sizeof(float) * (size_t)p.BH * p.N * d, stream) !=
         cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_ALLOC;
@@ -243,7 +301,7 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
     const size_t bytes_states = states ? mc::round_up(sizeof(float) * (size_t)B * H * N * d * d) : 0;
     const int nin = u && agg_mode != MC_RESIDUAL ? 4 : 3;
     void *dmem = nullptr;
-    if (cudaMallocAsync(&dmem, bytes_in * (nin + 1) + bytes_states, stream) != cudaSuccess) {
+    if (mc::scratch_alloc(&dmem, bytes_in * (nin + 1) + bytes_states, stream) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_ALLOC;
     }
@@ -270,6 +328,21 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
     cudaError_t es = cudaStreamSynchronize(stream);
     if (rc != MC_OK) return rc;
     if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
+int mc_trim_scratch(void)
+{
+    std::lock_guard<std::mutex> lock(mc::g_pool_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    if (mc::g_pools[dev] && cudaMemPoolTrimTo(mc::g_pools[dev], 0) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_CUDA;
     }

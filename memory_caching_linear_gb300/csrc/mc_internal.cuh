@@ -74,6 +74,9 @@ __device__ __forceinline__ void topk_insert(float *vals, int *idxs, int &count, 
     if (count < k) ++count;
 }
 
+// Stream-ordered scratch from the library's per-device pool (mc_api.cu).
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s);
+
 // Kernel-boundary profiling (mc_profile_begin): call_start() before the first
 // kernel of a forward, after_kernel(name) after each launch.
 void profile_call_start(cudaStream_t s);
@@ -84,6 +87,8 @@ void profile_after_kernel(cudaStream_t s, const char *name);
 bool tc_supported(const Problem &p);
 size_t tc_scratch_bytes(const Problem &p);
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+size_t tc_select_scratch_bytes(const Problem &p);
+cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 // Reads and clears the device-side record of an abandoned bounded wait.
 cudaError_t take_device_abort(int *was_set);
 

@@ -128,6 +128,18 @@ def test_parity_tensor_core_shapes(name, B, H, L, d, C, mode):
     assert np.isfinite(y).all()
 
 
+@pytest.mark.parametrize("topk", [1, 3, 16])
+@pytest.mark.parametrize("name,B,H,L,d,C", TC_CASES[:2], ids=[c[0] for c in TC_CASES[:2]])
+def test_parity_tensor_core_ssc(name, B, H, L, d, C, topk):
+    """SSC on the tensor-core path: router (mc_ssc_select, the forward's own) and y."""
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32((name + "ssc").encode()) % 1000, dtype="bf16")
+    ref = oracle.forward(q, k, v, u, C, SSC, topk)
+    y, st = run_gpu(q, k, v, u, C, SSC, topk)
+    yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL["bf16"])
+    assert rel_err(y, yref) <= TOL["bf16"], (name, topk, rel_err(y, yref))
+    assert rel_err(st, ref["states"]) <= TOL["bf16"]
+
+
 def test_tiny_workload_invariants_on_gpu():
     """The tiny workload's collapse invariants hold for the GPU results too."""
     q, k, v, u = workload_inputs(TINY)
