@@ -66,7 +66,8 @@ struct TcArgs {
     uint8_t *kbar_img;    // [BH] x 32 KB: hi rows (16 KB) then lo rows (16 KB), row = segment
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
-    __nv_bfloat16 *gam;   // [BH][L][64] gates: g_i at column i < n, g_n at column 63
+    uint32_t *gam;        // gates as bf16 pairs, per 128-token tile T: [T][pair p][row]; pair p holds
+                          // (g_{2p}, g_{2p+1}); g_i for i < n, g_n in the high half of pair 31
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
     int BH, L, C, N, CPS;
@@ -83,50 +84,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t r, uint32_t k, uint32_t rows)
-{
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(r, k, rows)));
-}
-
 // K-major SW128 descriptor start for the 16-wide K step kk of a tile with `rows` rows.
 __device__ __forceinline__ uint32_t kmaj_off(int kk, uint32_t rows) { return (kk >> 2) * rows * 128u + (kk & 3) * 32u; }
-
-// Thread owns TMEM lane `row`; read 128 fp32 columns starting at taddr and
-// write them as row `row` of a bf16 SW128 operand image in global memory
-// (optionally also as fp32 to out32[0..127]).
-__device__ __forceinline__ void tmem_row_to_image(uint32_t taddr, uint32_t row, uint8_t *img, float *out32)
-{
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {  // 32 columns at a time
-        uint32_t a[16], b[16];
-        tmem_ld16(taddr + 32 * h, a);
-        tmem_ld16(taddr + 32 * h + 16, b);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pk[8 + i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-        // columns 32h..32h+31 are four 16-byte chunks (8 bf16 each)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t k = 32 * h + 8 * cc;
-            uint4 v = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-            *reinterpret_cast<uint4 *>(img + sw128_offset(row, k, 128)) = v;
-        }
-        if (out32) {
-            float4 *o = reinterpret_cast<float4 *>(out32 + 32 * h);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]), __uint_as_float(a[4 * i + 2]),
-                                   __uint_as_float(a[4 * i + 3]));
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[4 + i] = make_float4(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
-                                       __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
-        }
-    }
-}
 
 // ============================================================================
 // seg_state_tc
@@ -145,12 +104,18 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     __shared__ uint64_t full[2], empty[2], r_full[2], r_empty[2], z_full[2], z_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float ksum_s[kD];
+    __shared__ __align__(16) float ksum_s[kD];
+    __shared__ __align__(16) float red_s[8][kD];  // column-sum partials of 16-row groups
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int seg = blockIdx.x % a.N, bh = blockIdx.x / a.N;
-    const int row0 = bh * a.L + seg * a.C;  // first token row of the segment in the [BH*L, d] view
     const int nch = a.CPS;
+    // Persistent: this CTA walks segments blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // its chunks form one stream (global chunk counter g) so loads run ahead
+    // across segment boundaries.
+    const int nseg_total = a.BH * a.N;
+    const int my_segs = (int)blockIdx.x < nseg_total ? (nseg_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int my_chunks = my_segs * nch;
+    auto seg_of = [&](int gch) { return (int)blockIdx.x + (gch / nch) * (int)gridDim.x; };
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -168,7 +133,6 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         }
         fence_mbar_init();
     }
-    if (threadIdx.x >= 64) ksum_s[threadIdx.x - 64] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -181,13 +145,14 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
             if (GATED) prefetch_tensormap(&mU);
-            for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
-                const uint32_t r = c >> 1;
+            for (int gch = 0; gch < my_chunks; ++gch) {
+                const int sid = seg_of(gch), c = gch % nch;
+                const int rr = (sid / a.N) * a.L + (sid % a.N) * a.C + c * kCT;
+                const int s = gch & 1;
+                const uint32_t r = gch >> 1;
                 if (!mbar_wait(&empty[s], (r & 1) ^ 1, &abort_flag)) break;
                 uint8_t *st = sm + s * kT1Stage;
                 mbar_arrive_expect_tx(&full[s], GATED ? 3 * kTile : 2 * kTile);
-                const int rr = row0 + c * kCT;
                 tma_load_2d(st, &mK, 0, rr, &full[s]);
                 tma_load_2d(st + 16384, &mK, 64, rr, &full[s]);
                 tma_load_2d(st + kTile, &mV, 0, rr, &full[s]);
@@ -202,9 +167,9 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         if (lane == 0) {
             constexpr uint32_t idR = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idS = idesc_bf16(128, 128, true, true);
-            for (int c = 0; c < nch; ++c) {
-                const int s = c & 1, b = c & 1;
-                const uint32_t r = c >> 1;
+            for (int gch = 0; gch < my_chunks; ++gch) {
+                const int s = gch & 1, b = gch & 1;
+                const uint32_t r = gch >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sm + s * kT1Stage), vb = kb + kTile, ub = kb + 2 * kTile;
@@ -233,20 +198,41 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (Z, S) = key column (sums)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         float S[kD];  // running state row: S[row][k] = sum_{j before the chunk} v_j[row] k_j[k]
-#pragma unroll
-        for (int k = 0; k < kD; ++k) S[k] = 0.f;
         float ks = 0.f;  // running sum of key column `row` over the segment, in token order
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
         bool ok = true;
-        for (int c = 0; c < nch; ++c) {
-            const int s = c & 1, b = c & 1;
-            const uint32_t r = c >> 1;
+        for (int gch = 0; gch < my_chunks; ++gch) {
+            const int sid = seg_of(gch), c = gch % nch;
+            const int bh = sid / a.N, seg = sid % a.N;
+            const int row0 = bh * a.L + seg * a.C;
+            const int s = gch & 1, b = gch & 1;
+            const uint32_t r = gch >> 1;
+            if (c == 0) {  // a new segment: memory restarts at zero
+#pragma unroll
+                for (int k = 0; k < kD; ++k) S[k] = 0.f;
+                ks = 0.f;
+                ksum_s[row] = 0.f;
+                named_bar_sync(1, 128);
+            }
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
             const uint8_t *st = sm + s * kT1Stage;
             if (GATED && ok) {
-                float dot = 0.f;  // <u_t, keys of the segment before this chunk>
-                for (int k = 0; k < kD; ++k) dot = fmaf(bf16_at(st + 2 * kTile, row, k, 128), ksum_s[k], dot);
+                float dot = 0.f;  // <u_t, keys of the segment before this chunk>, 8 elements per 16-byte load
+#pragma unroll
+                for (int cc = 0; cc < 16; ++cc) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(st + 2 * kTile + sw128_offset(row, 8 * cc, 128));
+                    const float4 k0 = *reinterpret_cast<const float4 *>(&ksum_s[8 * cc]);
+                    const float4 k1 = *reinterpret_cast<const float4 *>(&ksum_s[8 * cc + 4]);
+                    const float2 u01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.x));
+                    const float2 u23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
+                    const float2 u45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.z));
+                    const float2 u67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.w));
+                    dot = fmaf(u01.x, k0.x, dot); dot = fmaf(u01.y, k0.y, dot);
+                    dot = fmaf(u23.x, k0.z, dot); dot = fmaf(u23.y, k0.w, dot);
+                    dot = fmaf(u45.x, k1.x, dot); dot = fmaf(u45.y, k1.y, dot);
+                    dot = fmaf(u67.x, k1.z, dot); dot = fmaf(u67.y, k1.w, dot);
+                }
                 ok = mbar_wait(&r_full[b], r & 1, &abort_flag);
                 if (ok) {
                     tc_fence_after();
@@ -266,11 +252,31 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     a.r_on[(size_t)row0 + t_in_seg] = (dot + w) / (float)(t_in_seg + 1);
                 }
             }
-            named_bar_sync(1, 128);  // every worker has read ksum_s
+            // Key column sums of the chunk, in a fixed order: thread (rg, cc) sums
+            // columns 8cc..8cc+7 over rows 16rg..16rg+15 in row order; then column
+            // `row` adds the eight group sums in rg order to the running sum.
             if (ok) {
-                float s2 = ks;
-                for (int rr = 0; rr < kCT; ++rr) s2 += bf16_at(st, rr, row, 128);
-                ks = s2;
+                const int cc = row & 15, rg = row >> 4;
+                float p8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(st + sw128_offset(16 * rg + i, 8 * cc, 128));
+                    const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.x));
+                    const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
+                    const float2 k45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.z));
+                    const float2 k67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.w));
+                    p8[0] += k01.x; p8[1] += k01.y; p8[2] += k23.x; p8[3] += k23.y;
+                    p8[4] += k45.x; p8[5] += k45.y; p8[6] += k67.x; p8[7] += k67.y;
+                }
+                *reinterpret_cast<float4 *>(&red_s[rg][8 * cc]) = make_float4(p8[0], p8[1], p8[2], p8[3]);
+                *reinterpret_cast<float4 *>(&red_s[rg][8 * cc + 4]) = make_float4(p8[4], p8[5], p8[6], p8[7]);
+            }
+            named_bar_sync(1, 128);  // every worker has read ksum_s and written its partials
+            if (ok) {
+                float cs = 0.f;
+#pragma unroll
+                for (int g8 = 0; g8 < 8; ++g8) cs += red_s[g8][row];
+                ks += cs;
                 ksum_s[row] = ks;
             }
             named_bar_sync(1, 128);
@@ -298,20 +304,20 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                                                pack_bf16x2(S[8 * cc + 4], S[8 * cc + 5]), pack_bf16x2(S[8 * cc + 6], S[8 * cc + 7]));
                     *reinterpret_cast<uint4 *>(img + sw128_offset(row, 8 * cc, 128)) = v;
                 }
-                if (c + 1 == nch) {  // the segment's cached state, fp32
+                if (c + 1 == nch) {  // the segment's cached state (fp32) and key mean
                     float4 *o = reinterpret_cast<float4 *>(a.states + sidx * kD * kD + (size_t)row * kD);
 #pragma unroll
                     for (int i = 0; i < kD / 4; ++i) o[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+                    if (GATED) {
+                        const float kbv = ks / (float)a.C;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(kbv);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(kbv - __bfloat162float(hi));
+                        uint8_t *kimg = a.kbar_img + (size_t)bh * kTile;
+                        *reinterpret_cast<__nv_bfloat16 *>(kimg + sw128_offset(seg, row, 64)) = hi;
+                        *reinterpret_cast<__nv_bfloat16 *>(kimg + 16384 + sw128_offset(seg, row, 64)) = lo;
+                    }
                 }
             }
-        }
-        if (ok && GATED && !abort_flag) {
-            const float kb = ks / (float)a.C;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
-            uint8_t *img = a.kbar_img + (size_t)bh * kTile;
-            *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(seg, row, 64)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(img + 16384 + sw128_offset(seg, row, 64)) = lo;
         }
     }
     tc_fence_before();
@@ -332,7 +338,15 @@ __global__ void __launch_bounds__(kD) kbar_images_tc(const __nv_bfloat16 *__rest
     const int col = threadIdx.x;
     const __nv_bfloat16 *src = k + ((size_t)bh * a.L + (size_t)seg * a.C) * kD + col;
     float s = 0.f;
-    for (int t = 0; t < a.C; ++t) s += __bfloat162float(src[(size_t)t * kD]);
+    for (int c0 = 0; c0 < a.C; c0 += kCT) {  // the state kernel's order: 16-row groups, then chunks
+        float cs = 0.f;
+        for (int rg = 0; rg < 8; ++rg) {
+            float p = 0.f;
+            for (int i = 0; i < 16; ++i) p += __bfloat162float(src[(size_t)(c0 + 16 * rg + i) * kD]);
+            cs += p;
+        }
+        s += cs;
+    }
     const float kb = s / (float)a.C;
     const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
     const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
@@ -364,7 +378,8 @@ __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
 // from two MMAs (kbar as hi + lo bf16 rows, so the score carries ~16 bits of
 // kbar; u is exact in bf16), then
 //   g_{t,i} = exp(r_{t,i} - m) / Z (i < n),  g_{t,n} = exp(r_on[t] - m) / Z
-// written as bf16: gam[token][i] for i < n and gam[token][63] for the online memory.
+// written as bf16 pairs in tile-transposed order (coalesced for a thread per token
+// row): gam[tile][p][row] = (g_{2p}, g_{2p+1}), g_i for i < n, g_n as element 63.
 // ============================================================================
 constexpr int kGatesThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + store
 constexpr size_t kGatesSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
@@ -518,13 +533,9 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             sc[63] = expf(ron - mx);
             const float inv = 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
             if (!a.gam) continue;  // router only (mc_ssc_select)
-            uint4 *dst = reinterpret_cast<uint4 *>(a.gam + tok * 64);
+            uint32_t *dst = a.gam + (size_t)it * (32 * kCT) + row;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                dst[k] = make_uint4(pack_bf16x2(sc[8 * k] * inv, sc[8 * k + 1] * inv),
-                                    pack_bf16x2(sc[8 * k + 2] * inv, sc[8 * k + 3] * inv),
-                                    pack_bf16x2(sc[8 * k + 4] * inv, sc[8 * k + 5] * inv),
-                                    pack_bf16x2(sc[8 * k + 6] * inv, sc[8 * k + 7] * inv));
+            for (int k = 0; k < 32; ++k) dst[k * kCT] = pack_bf16x2(sc[2 * k] * inv, sc[2 * k + 1] * inv);
         }
     }
     tc_fence_before();
@@ -539,10 +550,13 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
 // ============================================================================
 // readout_tc
 // ============================================================================
-constexpr int kT2Threads = 352;  // 0 TMA, 1 MMA issuer 0, 2-5 A producers, 6-9 aux, 10 MMA issuer 1
-constexpr int kRing = 7;     // 32 KB operand slots: K, prefix state, cached states, V of each tile
-constexpr int kASlots = 4;   // A operands (bf16, 64 TMEM columns each) in flight
-constexpr size_t kT2Smem = kRing * kTile + 1024;
+constexpr int kT2Threads = 192;    // warp 0 TMA, warp 1 MMA issuer, warps 2-5 token-row workers
+constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
+constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
+constexpr int kRing = 6;           // operand panels in flight per CTA
+constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
+constexpr uint32_t kStage = 8192;  // y staging buffer: 128 rows x 32 columns bf16 (SWIZZLE_64B)
+constexpr size_t kT2Smem = kRing * kPanel + kStage + 1024;  // two CTAs fit in an SM's 228 KB
 
 struct TileInfo {
     int n, c, bh;
@@ -578,35 +592,40 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
     return GATED ? a.states_img + (sb + k) * kTile : a.prefix_img + (sb + t.n) * kTile;
 }
 
-// Accumulator groups of a tile: items + the P V product.  With two or more the
-// two accumulators are both written (the MMA warp alternates between them).
-template <bool GATED>
-__device__ __forceinline__ int tile_groups(const TileInfo &t)
-{
-    return tile_items<GATED>(t) + 1;
-}
 
+// One tile = 128 tokens (bh, segment n, chunk c).  Per tile, in this order, into
+// one fp32 accumulator D[t][v]:
+//   G   = Q K_c^T                      (both operands in shared memory)
+//   D   = P V_c,  P = g_n * mask(G)    (P written into tensor memory by the workers)
+//   D  += (g_i o Q) X_i^T              for X_i in {S_pre(c), M^(0..n-1)} (GRM / Soup)
+//                                      or {S_pre(c), sum_{i<n} M^(i)} (Residual, g = 1)
+// Operands stream through a ring of 16 KB panels (a K-half of a 128 x 128 tile;
+// V in key halves).  The workers take their query rows from the Q panels once G
+// is done with them (and then release those panels), read the gate rows in the
+// tile-transposed layout (coalesced), and write y through shared memory with TMA
+// stores.  Two CTAs run on each SM, so while one waits on its G -> P step or its
+// drain the other keeps the tensor pipe busy.
 template <bool GATED>
-__global__ void __launch_bounds__(kT2Threads, 1)
-    readout_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, TcArgs a)
+__global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
+    readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mY, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t ring_full[kRing], ring_empty[kRing];
-    __shared__ uint64_t a_full[kASlots], a_empty[kASlots];
-    __shared__ uint64_t g_full, g_done, y_full, y_empty, p_slot, p_written;
+    __shared__ uint64_t a_full[2], a_empty[2];
+    __shared__ uint64_t g_full, y_full, y_empty, fin, q_read, stage_full, stage_free;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles_total = a.num_tiles;
-    const int my_tiles = blockIdx.x < (unsigned)ntiles_total
-                             ? (ntiles_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
-                             : 0;
-    auto tile_id = [&](int j) { return (int)blockIdx.x + j * (int)gridDim.x; };
+    const int ntiles = a.num_tiles;
+    const int my_tiles =
+        blockIdx.x < (unsigned)ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile_id = [&](int j) { return (int)blockIdx.x + j * (int)gridDim.x; };  // heaviest tiles first
 
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 512);
+        tmem_alloc(&tmem_base, kT2Cols);
         tmem_relinquish();
     }
     if (threadIdx.x == 32) {
@@ -615,310 +634,308 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
         }
-        for (int s = 0; s < kASlots; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&a_full[s], 128);
             mbar_init(&a_empty[s], 1);
         }
         mbar_init(&g_full, 1);
-        mbar_init(&g_done, 128);
-        mbar_init(&p_slot, 128);
-        mbar_init(&p_written, 128);
-        mbar_init(&y_full, 2);  // one commit from each MMA issuer
+        mbar_init(&y_full, 1);
         mbar_init(&y_empty, 128);
+        mbar_init(&fin, 1);
+        mbar_init(&q_read, 128);
+        mbar_init(&stage_full, 128);
+        mbar_init(&stage_free, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    // tensor memory: D0 (128 cols) | D1 (128; holds G at the start of a tile) | A slots (4 x 64).
-    // A slot sequence of a tile: g_n o Q (for G and the prefix state), one slot per
-    // cached operand (A warps), then P for the P V product (aux warps).
-    const uint32_t tD0 = tb, tD1 = tb + 128, tA0 = tb + 256;
+    const uint32_t tD = tb, tA0 = tb + 128;
     const uint32_t s_base = smem_u32(sm);
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        // Ring sequence of a tile: K tile, the cached operands, V tile.  At the
-        // start of each tile it also prefetches the next tile's query rows and
-        // gate rows into L2 for the A warps.
+        // ---------------------------------------------------------- TMA producer
+        // Panel sequence of a tile: Q0 K0 Q1 K1 (G), V0 V1 (P V), then both K
+        // panels of every cached operand.  The workers release the Q panels.
         if (lane == 0 && my_tiles > 0) {
+            prefetch_tensormap(&mQ);
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
             uint32_t g = 0;
             bool ok = true;
-            auto slot = [&](uint32_t bytes) -> uint8_t * {
+            auto slot = [&]() -> uint8_t * {
                 const int s = g % kRing;
                 if (!mbar_wait(&ring_empty[s], ((g / kRing) & 1) ^ 1, &abort_flag)) return nullptr;
-                mbar_arrive_expect_tx(&ring_full[s], bytes);
-                return sm + s * kTile;
+                mbar_arrive_expect_tx(&ring_full[s], kPanel);
+                return sm + s * kPanel;
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
                 const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
-                if (j + 1 < my_tiles) {
+                if (GATED && j + 1 < my_tiles) {  // the workers read the next tile's gate rows directly
                     const TileInfo tn = decode_tile(a, tile_id(j + 1));
-                    const size_t rn = (size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT;
-                    prefetch_l2(a.q + rn * kD, kTile);
-                    if (GATED) prefetch_l2(a.gam + rn * 64, kCT * 64 * 2);
+                    const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT) / kCT;
+                    prefetch_l2(a.gam + tn_id * (32 * kCT), 32 * kCT * 4);
                 }
-                uint8_t *dst = slot(kTile);
-                if (!(ok = dst != nullptr)) break;
-                tma_load_2d(dst, &mK, 0, rr, &ring_full[g % kRing]);
-                tma_load_2d(dst + 16384, &mK, 64, rr, &ring_full[g % kRing]);
-                ++g;
-                const int items = tile_items<GATED>(t);
-                for (int k = 0; k < items; ++k) {
-                    if (!(dst = slot(kTile))) break;
-                    bulk_load(dst, item_image<GATED>(a, t, k), kTile, &ring_full[g % kRing]);
+                uint8_t *dst = nullptr;
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!(ok = (dst = slot()) != nullptr)) break;
+                    tma_load_2d(dst, &mQ, 64 * h, rr, &ring_full[g % kRing]);
+                    ++g;
+                    if (!(ok = (dst = slot()) != nullptr)) break;
+                    tma_load_2d(dst, &mK, 64 * h, rr, &ring_full[g % kRing]);
                     ++g;
                 }
-                if (!(ok = dst != nullptr)) break;
-                if (!(ok = (dst = slot(kTile)) != nullptr)) break;
-                tma_load_2d(dst, &mV, 0, rr, &ring_full[g % kRing]);
-                tma_load_2d(dst + 16384, &mV, 64, rr, &ring_full[g % kRing]);
-                ++g;
+                for (int h = 0; h < 2 && ok; ++h) {  // keys 64h .. 64h + 63, both 64-wide halves of v
+                    if (!(ok = (dst = slot()) != nullptr)) break;
+                    tma_load_2d(dst, &mV, 0, rr + 64 * h, &ring_full[g % kRing]);
+                    tma_load_2d(dst + kPanel / 2, &mV, 64, rr + 64 * h, &ring_full[g % kRing]);
+                    ++g;
+                }
+                const int items = tile_items<GATED>(t);
+                for (int k = 0; k < items && ok; ++k) {
+                    const uint8_t *src = item_image<GATED>(a, t, k);
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = (dst = slot()) != nullptr)) break;
+                        bulk_load(dst, src + h * kPanel, kPanel, &ring_full[g % kRing]);
+                        ++g;
+                    }
+                }
+            }
+            // leave no copy in flight: the last use of every slot has landed
+            int give_up = 0;
+            for (uint32_t i = 0; i < (uint32_t)kRing && i < g; ++i) {
+                const uint32_t u = g - 1 - i;
+                mbar_wait_limit(&ring_full[u % kRing], (u / kRing) & 1, &give_up, kWaitLimitNs);
             }
         }
-    } else if (warp == 1 || warp == kT2Threads / 32 - 1) {
-        // ---------------------------------------------------------- MMA issuers
-        // Two issuing threads: a single thread cannot issue tcgen05.mma fast enough
-        // to keep the tensor pipe busy once its per-group bookkeeping is counted.
-        // Issuer 1 owns accumulator D1 (G, then the odd groups of a tile), issuer 0
-        // owns D0 (the even groups).  Group k of a tile is the k-th cached operand
-        // (prefix state first), the last group is P V.  Every ring and A slot has
-        // exactly one consumer, which commits its release.
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
         if (lane == 0 && my_tiles > 0) {
-            const int me = warp == 1 ? 0 : 1;
-            constexpr uint32_t idKm = idesc_bf16(128, 128, false, false);  // B K-major
+            constexpr uint32_t idKm = idesc_bf16(128, 128, false, false);  // A and B K-major
             constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);   // B MN-major (V)
-            const uint64_t dRing0 = make_desc_sw128(s_base, 0, 1024);
-            const uint64_t dRingMN = make_desc_sw128(s_base, 16384, 1024);
-            uint32_t off128[8];
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) off128[kk] = kmaj_off(kk, 128) >> 4;
-            const uint32_t tD = me ? tD1 : tD0;
-            uint32_t g = 0, ac = 0;  // ring / A-slot index of the tile's first slot
+            uint32_t g = 0, ac = 0;
             bool ok = true;
+            auto ring_ready = [&](uint32_t u) {
+                return mbar_wait(&ring_full[u % kRing], (u / kRing) & 1, &abort_flag);
+            };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
-                const int groups = tile_items<GATED>(t) + 1;
-                if (me == 1) {  // G = (g_n o Q) K^T into D1
-                    const int s = g % kRing;
-                    if (!(ok = mbar_wait(&ring_full[s], (g / kRing) & 1, &abort_flag))) break;
-                    if (!(ok = mbar_wait(&a_full[ac % kASlots], (ac / kASlots) & 1, &abort_flag))) break;
-                    if (!(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;  // tile j-1 drained
+                if (!(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;  // D of tile j-1 drained
+                // G = Q K^T
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t sq = g % kRing, sk = (g + 1) % kRing;
+                    if (!(ok = ring_ready(g) && ring_ready(g + 1))) break;
                     tc_fence_after();
-                    const uint32_t ta = tA0 + (ac % kASlots) * 64;
-                    const uint64_t dB = dRing0 + ((s * kTile) >> 4);
+                    const uint64_t dq = make_desc_sw128(s_base + sq * kPanel, 0, 1024);
+                    const uint64_t dk = make_desc_sw128(s_base + sk * kPanel, 0, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) mma_ts(tD1, ta + kk * 8, dB + off128[kk], idKm, kk > 0);
-                    mma_commit(&g_full);
-                    mma_commit(&ring_empty[s]);
-                    mma_commit(&a_empty[ac % kASlots]);
-                }
-                bool used = false;
-                for (int k = me; k < groups; k += 2) {
-                    const uint32_t rk = g + 1 + k, ak = ac + 1 + k;
-                    const int s = rk % kRing;
-                    if (!(ok = mbar_wait(&ring_full[s], (rk / kRing) & 1, &abort_flag))) break;
-                    if (!(ok = mbar_wait(&a_full[ak % kASlots], (ak / kASlots) & 1, &abort_flag))) break;
-                    if (!used) {
-                        // D0: tile j-1 drained; D1: G has been read by the aux warps
-                        if (me == 0 && !(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;
-                        if (me == 1 && !(ok = mbar_wait(&g_done, j & 1, &abort_flag))) break;
-                    }
-                    tc_fence_after();
-                    const uint32_t ta = tA0 + (ak % kASlots) * 64;
-                    const uint32_t acc0 = used ? 1u : 0u;
-                    if (k == groups - 1) {  // P V: the V operand is MN-major, a K step is 16 rows
-                        const uint64_t dB = dRingMN + ((s * kTile) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) mma_ts(tD, ta + kk * 8, dB + kk * (2048u >> 4), idPV, acc0 | (kk > 0));
-                    } else {
-                        const uint64_t dB = dRing0 + ((s * kTile) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) mma_ts(tD, ta + kk * 8, dB + off128[kk], idKm, acc0 | (kk > 0));
-                    }
-                    mma_commit(&ring_empty[s]);
-                    mma_commit(&a_empty[ak % kASlots]);
-                    used = true;
+                    for (int kk = 0; kk < 4; ++kk) mma_ss(tD, dq + 2 * kk, dk + 2 * kk, idKm, (h | kk) != 0);
+                    mma_commit(&ring_empty[sk]);  // the Q panel is released by the workers
+                    g += 2;
                 }
                 if (!ok) break;
-                mma_commit(&y_full);  // both issuers commit: the tile's sum is complete
-                g += 1 + groups;
-                ac += 1 + groups;
-            }
-        }
-    } else if (warp < 6) {
-        // ---------------------------------------------------------- A producers
-        const int q4 = warp & 3;
-        const uint32_t row = 32 * q4 + lane;
-        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        uint32_t ac = 0;
-        bool ok = true;
-        auto put_a = [&](const uint32_t (&src)[64], __nv_bfloat162 gam, bool scale) -> bool {
-            if (!mbar_wait(&a_empty[ac % kASlots], ((ac / kASlots) & 1) ^ 1, &abort_flag)) return false;
-            tc_fence_after();
-            const uint32_t ta = tA0 + (ac % kASlots) * 64 + lane_base;
+                mma_commit(&g_full);
+                // D = P V once the workers have read G and written P
+                const uint32_t ps = ac % 2;
+                if (!(ok = mbar_wait(&a_full[ps], (ac / 2) & 1, &abort_flag))) break;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t s = g % kRing;
+                    if (!(ok = ring_ready(g))) break;
+                    tc_fence_after();
+                    const uint64_t dv = make_desc_sw128(s_base + s * kPanel, kPanel / 2, 1024);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                uint32_t r[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (scale) {
-                        __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&src[16 * m + i]);
-                        __nv_bfloat162 pr = __hmul2(x, gam);
-                        r[i] = *reinterpret_cast<uint32_t *>(&pr);
-                    } else {
-                        r[i] = src[16 * m + i];
-                    }
-                }
-                tmem_st16(ta + 16 * m, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&a_full[ac % kASlots]);
-            ++ac;
-            return true;
-        };
-        for (int j = 0; j < my_tiles && ok; ++j) {
-            const TileInfo t = decode_tile(a, tile_id(j));
-            const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
-            uint32_t gm2[32];  // gates g_{t,i} as bf16 pairs (i even: low half); g_{t,n} at 63
-            if (GATED) {
-                const uint4 *gsrc = reinterpret_cast<const uint4 *>(a.gam + tok * 64);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 x = __ldg(gsrc + i);
-                    gm2[4 * i] = x.x;
-                    gm2[4 * i + 1] = x.y;
-                    gm2[4 * i + 2] = x.z;
-                    gm2[4 * i + 3] = x.w;
-                }
-            }
-            uint32_t qp[64];  // the token's query row, bf16 pairs
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + tok * kD);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint4 x = __ldg(src + i);
-                    qp[4 * i] = x.x;
-                    qp[4 * i + 1] = x.y;
-                    qp[4 * i + 2] = x.z;
-                    qp[4 * i + 3] = x.w;
-                }
-            }
-            const __nv_bfloat162 one2 = __float2bfloat162_rn(1.f);
-            // g_n o Q: A operand of G and of the prefix state
-            __nv_bfloat162 gon2 = one2;
-            if (GATED) gon2 = __high2bfloat162(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31]));
-            if (!(ok = put_a(qp, gon2, GATED))) break;                  // for G
-            if (t.c > 0 && !(ok = put_a(qp, gon2, GATED))) break;      // for the prefix state
-            if (GATED) {
-                // Rolled loop (one copy of put_a keeps the code small); the gate of
-                // segment i comes from a small per-thread array.
-                const __nv_bfloat16 *gl = reinterpret_cast<const __nv_bfloat16 *>(gm2);
-#pragma unroll 1
-                for (int i = 0; i < t.n; ++i) {
-                    if (!(ok = put_a(qp, __bfloat162bfloat162(gl[i]), true))) break;
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tD, tA0 + ps * 64 + (4 * h + kk) * 8, dv + kk * (2048u >> 4), idPV, (h | kk) != 0);
+                    mma_commit(&ring_empty[s]);
+                    ++g;
                 }
                 if (!ok) break;
-            } else if (t.n > 0) {
-                if (!(ok = put_a(qp, one2, false))) break;
+                mma_commit(&a_empty[ps]);
+                ++ac;
+                // D += (g_i o Q) X_i^T
+                const int items = tile_items<GATED>(t);
+                for (int k = 0; k < items && ok; ++k) {
+                    const uint32_t as = ac % 2;
+                    if (!(ok = mbar_wait(&a_full[as], (ac / 2) & 1, &abort_flag))) break;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t s = g % kRing;
+                        if (!(ok = ring_ready(g))) break;
+                        tc_fence_after();
+                        const uint64_t db = make_desc_sw128(s_base + s * kPanel, 0, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) mma_ts(tD, tA0 + as * 64 + (4 * h + kk) * 8, db + 2 * kk, idKm, 1);
+                        mma_commit(&ring_empty[s]);
+                        ++g;
+                    }
+                    if (!ok) break;
+                    mma_commit(&a_empty[as]);
+                    ++ac;
+                }
+                if (!ok) break;
+                mma_commit(&y_full);
             }
-            // The tile's last A slot carries P.  The A warps claim it in order (so
-            // every wait on a slot stays within one phase of its barrier) and hand it
-            // to the aux warps, after the previous tile's P has been written.
-            if (j > 0 && !(ok = mbar_wait(&p_written, (j - 1) & 1, &abort_flag))) break;
-            if (!(ok = mbar_wait(&a_empty[ac % kASlots], ((ac / kASlots) & 1) ^ 1, &abort_flag))) break;
-            mbar_arrive(&p_slot);
-            ++ac;
+            // leave no MMA in flight
+            mma_commit(&fin);
+            int give_up = 0;
+            mbar_wait_limit(&fin, 0, &give_up, kWaitLimitNs);
         }
     } else {
-        // ---------------------------------------------------------- aux: P, drain
+        // ---------------------------------------------------------- workers (thread = token row)
         const int q4 = warp & 3;
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const bool leader = warp == 2 && lane == 0;  // releases the Q panels, issues the y stores
+        uint8_t *stage = sm + kRing * kPanel;
+        uint32_t ac = 0, g = 0;  // A-slot / ring counters, in step with the MMA issuer
         bool ok = true;
-        uint32_t ac = 0;  // A-slot counter, kept in step with the A warps and the MMA warp
+        uint32_t gm2[32];  // gate pairs of the token: (g_{2p}, g_{2p+1}); g_n is element 63
+        auto load_gates = [&](int j) {
+            if (!GATED) return;
+            const TileInfo t = decode_tile(a, tile_id(j));
+            const size_t tid = ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) / kCT;
+            const uint32_t *src = a.gam + tid * (32 * kCT) + row;
+#pragma unroll
+            for (int p = 0; p < 32; ++p) gm2[p] = __ldg(src + p * kCT);
+        };
+        auto claim = [&]() -> bool {  // the next A slot is free
+            if (!mbar_wait(&a_empty[ac % 2], ((ac / 2) & 1) ^ 1, &abort_flag)) return false;
+            tc_fence_after();
+            return true;
+        };
+        auto publish = [&]() {  // hand the A slot to the issuer
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&a_full[ac % 2]);
+            ++ac;
+        };
+        if (my_tiles > 0) load_gates(0);
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
-            ac += 1 + (uint32_t)tile_items<GATED>(t);  // the G slot and the cached operands' slots
-            // P = mask(G): G already carries the online gate g_n through its A operand
+            const int items = tile_items<GATED>(t);
+            const float gn = GATED ? __bfloat162float(__high2bfloat16(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31])))
+                                   : 1.f;
             if (!(ok = mbar_wait(&g_full, j & 1, &abort_flag))) break;
             tc_fence_after();
-            uint32_t pk[64];
+            // the token's query row from the Q panels (SWIZZLE_128B: 16-byte chunk c of
+            // row r sits at chunk c ^ (r % 8)); G has finished reading them
+            uint32_t qp[64];
+            if (!(ok = mbar_wait(&ring_full[g % kRing], (g / kRing) & 1, &abort_flag) &&
+                       mbar_wait(&ring_full[(g + 2) % kRing], ((g + 2) / kRing) & 1, &abort_flag)))
+                break;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t x[16], z[16];
-                tmem_ld16(tD1 + lane_base + 32 * h, x);
-                tmem_ld16(tD1 + lane_base + 32 * h + 16, z);
-                tmem_wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                const uint8_t *pq = sm + ((g + 2 * h) % kRing) * kPanel + row * 128;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t c0 = 32 * h + 2 * i, c1 = c0 + 16;
-                    pk[16 * h + i] = pack_bf16x2(c0 <= row ? __uint_as_float(x[2 * i]) : 0.f,
-                                                 c0 + 1 <= row ? __uint_as_float(x[2 * i + 1]) : 0.f);
-                    pk[16 * h + 8 + i] = pack_bf16x2(c1 <= row ? __uint_as_float(z[2 * i]) : 0.f,
-                                                     c1 + 1 <= row ? __uint_as_float(z[2 * i + 1]) : 0.f);
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(pq + ((c ^ (row & 7)) << 4));
+                    qp[32 * h + 4 * c] = x.x;
+                    qp[32 * h + 4 * c + 1] = x.y;
+                    qp[32 * h + 4 * c + 2] = x.z;
+                    qp[32 * h + 4 * c + 3] = x.w;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&g_done);
-            if (!(ok = mbar_wait(&p_slot, j & 1, &abort_flag))) break;  // claimed for us by the A warps
-            tc_fence_after();
+            mbar_arrive(&q_read);
+            if (leader) {
+                if (!(ok = mbar_wait(&q_read, j & 1, &abort_flag))) break;
+                mbar_arrive(&ring_empty[g % kRing]);
+                mbar_arrive(&ring_empty[(g + 2) % kRing]);
+            }
+            // P = g_n * mask(G), key column c <= token row
+            if (!(ok = claim())) break;
             {
-                const uint32_t ta = tA0 + (ac % kASlots) * 64 + lane_base;
+                const uint32_t ta = tA0 + (ac % 2) * 64 + lane_base;
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    uint32_t r[16];
+                    uint32_t x[32], o[16];
+                    tmem_ld32(tD + lane_base + 32 * h, x);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = pk[16 * h + i];
-                    tmem_st16(ta + 16 * h, r);
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t c0 = 32 * h + 2 * i;
+                        o[i] = pack_bf16x2(c0 <= row ? gn * __uint_as_float(x[2 * i]) : 0.f,
+                                           c0 + 1 <= row ? gn * __uint_as_float(x[2 * i + 1]) : 0.f);
+                    }
+                    tmem_st16(ta + 16 * h, o);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&a_full[ac % kASlots]);
-                mbar_arrive(&p_written);
-                ++ac;
             }
-            // drain: y = D0 (+ D1 when the tile wrote both accumulators)
-            const bool both = tile_groups<GATED>(t) >= 2;
+            publish();
+            // cached operands: g_i o Q
+            const __nv_bfloat16 *gl = reinterpret_cast<const __nv_bfloat16 *>(gm2);
+#pragma unroll 1
+            for (int k = 0; k < items; ++k) {
+                __nv_bfloat162 gam2 = __float2bfloat162_rn(1.f);
+                if (GATED) {
+                    const int i = t.c > 0 ? k - 1 : k;  // item 0 of a chunk c > 0 is its prefix state (gate g_n)
+                    gam2 = __bfloat162bfloat162(i < 0 ? gl[63] : gl[i]);
+                }
+                if (!(ok = claim())) break;
+                const uint32_t ta = tA0 + (ac % 2) * 64 + lane_base;
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (GATED) {
+                            __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&qp[32 * m + i]);
+                            __nv_bfloat162 pr = __hmul2(x, gam2);
+                            r[i] = *reinterpret_cast<uint32_t *>(&pr);
+                        } else {
+                            r[i] = qp[32 * m + i];
+                        }
+                    }
+                    tmem_st32(ta + 32 * m, r);
+                }
+                publish();
+            }
+            if (!ok) break;
+            g += 6 + 2 * items;
+            if (j + 1 < my_tiles) load_gates(j + 1);  // lands while this tile's MMAs finish
+            // drain: read D, release it, then write y (bf16) through the staging buffers
             if (!(ok = mbar_wait(&y_full, j & 1, &abort_flag))) break;
             tc_fence_after();
-            uint4 *dst = reinterpret_cast<uint4 *>(a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row) * kD);
+            uint32_t yb[64];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                uint32_t x[16], z[16], x1[16], z1[16];
-                tmem_ld16(tD0 + lane_base + 32 * h, x);
-                tmem_ld16(tD0 + lane_base + 32 * h + 16, z);
-                if (both) {
-                    tmem_ld16(tD1 + lane_base + 32 * h, x1);
-                    tmem_ld16(tD1 + lane_base + 32 * h + 16, z1);
-                }
+                uint32_t x[32];
+                tmem_ld32(tD + lane_base + 32 * h, x);
                 tmem_wait_ld();
-                float f[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    f[i] = __uint_as_float(x[i]) + (both ? __uint_as_float(x1[i]) : 0.f);
-                    f[16 + i] = __uint_as_float(z[i]) + (both ? __uint_as_float(z1[i]) : 0.f);
-                }
-                uint32_t o[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[4 * h + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                for (int i = 0; i < 16; ++i) yb[16 * h + i] = pack_bf16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
             }
             tc_fence_before();
             mbar_arrive(&y_empty);
+            const int r0 = t.bh * a.L + t.n * a.C + t.c * kCT;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {  // 32 columns per store
+                const uint32_t use = 4 * (uint32_t)j + cc;  // uses of the staging buffer so far
+                uint8_t *buf = stage;
+                if (!(ok = mbar_wait(&stage_free, (use & 1) ^ 1, &abort_flag))) break;
+                // SWIZZLE_64B: 16-byte chunk c of a 64-byte row r sits at chunk c ^ ((r / 2) % 4)
+                uint8_t *pr = buf + row * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(pr + ((c ^ ((row >> 1) & 3)) << 4)) =
+                        make_uint4(yb[16 * cc + 4 * c], yb[16 * cc + 4 * c + 1], yb[16 * cc + 4 * c + 2], yb[16 * cc + 4 * c + 3]);
+                fence_async_smem();
+                mbar_arrive(&stage_full);
+                if (leader) {
+                    if (!(ok = mbar_wait(&stage_full, use & 1, &abort_flag))) break;
+                    tma_store_2d(&mY, buf, 32 * cc, r0);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(&stage_free);
+                }
+            }
         }
+        if (leader) bulk_wait_group<0>();  // every y store has completed
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tb, 512);
+        tmem_dealloc(tb, kT2Cols);
     }
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
 }
@@ -1015,7 +1032,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
-    a.gam = gated ? reinterpret_cast<__nv_bfloat16 *>(base) : nullptr;
+    a.gam = gated ? reinterpret_cast<uint32_t *>(base) : nullptr;
     a.sel_out = fa.sel_out;
     a.topk = p.topk;
     a.BH = p.BH;
@@ -1025,9 +1042,11 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.CPS = (int)CPS;
     a.num_tiles = (int)(BH * N * CPS);
 
-    CUtensorMap mK, mV, mU;
+    CUtensorMap mQ, mK, mV, mV64, mY, mU;
     const unsigned long long rows = (unsigned long long)BH * p.L;
-    if (!make_tmap_bf16_sw128(&mK, fa.k, rows, kD, 128) || !make_tmap_bf16_sw128(&mV, fa.v, rows, kD, 128))
+    if (!make_tmap_bf16_sw128(&mQ, fa.q, rows, kD, 128) || !make_tmap_bf16_sw128(&mK, fa.k, rows, kD, 128) ||
+        !make_tmap_bf16_sw128(&mV, fa.v, rows, kD, 128) || !make_tmap_bf16_sw128(&mV64, fa.v, rows, kD, 64) ||
+        !make_tmap_bf16(&mY, fa.y, rows, kD, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (gated) {
         if (!make_tmap_bf16_sw128(&mU, fa.u, rows, kD, 128)) return cudaErrorInvalidValue;
@@ -1051,7 +1070,8 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         auto k1 = gated ? seg_state_tc<true> : seg_state_tc<false>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT1Smem);
         if (e != cudaSuccess) return e;
-        k1<<<(unsigned)(BH * N), kT1Threads, kT1Smem, s>>>(mK, mV, mU, a);
+        const int nseg = (int)(BH * N);
+        k1<<<nseg < g_num_sms ? nseg : g_num_sms, kT1Threads, kT1Smem, s>>>(mK, mV, mU, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "seg_state_tc");
     }
@@ -1074,8 +1094,9 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         auto k2 = gated ? readout_tc<true> : readout_tc<false>;
         e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);
         if (e != cudaSuccess) return e;
-        const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-        k2<<<grid, kT2Threads, kT2Smem, s>>>(mK, mV, a);
+        const int slots = kT2CtasPerSm * g_num_sms;
+        const int grid = a.num_tiles < slots ? a.num_tiles : slots;
+        k2<<<grid, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, mY, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "readout_tc");
     }
