@@ -555,7 +555,7 @@ constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
 constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
 constexpr int kRing = 6;           // operand panels in flight per CTA
 constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
-constexpr uint32_t kStage = 8192;  // y staging buffer: 128 rows x 32 columns bf16 (SWIZZLE_64B)
+constexpr uint32_t kStage = 8192;  // y staging: 128 rows x 32 columns bf16, 2 KB per worker warp
 constexpr size_t kT2Smem = kRing * kPanel + kStage + 1024;  // two CTAs fit in an SM's 228 KB
 
 struct TileInfo {
@@ -600,21 +600,20 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 //   D  += (g_i o Q) X_i^T              for X_i in {S_pre(c), M^(0..n-1)} (GRM / Soup)
 //                                      or {S_pre(c), sum_{i<n} M^(i)} (Residual, g = 1)
 // Operands stream through a ring of 16 KB panels (a K-half of a 128 x 128 tile;
-// V in key halves).  The workers take their query rows from the Q panels once G
-// is done with them (and then release those panels), read the gate rows in the
-// tile-transposed layout (coalesced), and write y through shared memory with TMA
-// stores.  Two CTAs run on each SM, so while one waits on its G -> P step or its
+// V in key halves).  The workers take their query rows from the Q panels (and
+// release those panels once G is done), read the gate rows in the tile-transposed
+// layout (coalesced), and write y through a small shared-memory transpose.  Two CTAs run on each SM, so while one waits on its G -> P step or its
 // drain the other keeps the tensor pipe busy.
 template <bool GATED>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mY, TcArgs a)
+               const __grid_constant__ CUtensorMap mV, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t ring_full[kRing], ring_empty[kRing];
     __shared__ uint64_t a_full[2], a_empty[2];
-    __shared__ uint64_t g_full, y_full, y_empty, fin, q_read, stage_full, stage_free;
+    __shared__ uint64_t g_full, y_full, y_empty, fin, q_read;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -643,8 +642,6 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         mbar_init(&y_empty, 128);
         mbar_init(&fin, 1);
         mbar_init(&q_read, 128);
-        mbar_init(&stage_full, 128);
-        mbar_init(&stage_free, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -786,7 +783,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         const int q4 = warp & 3;
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        const bool leader = warp == 2 && lane == 0;  // releases the Q panels, issues the y stores
+        const bool leader = warp == 2 && lane == 0;  // releases the Q panels
         uint8_t *stage = sm + kRing * kPanel;
         uint32_t ac = 0, g = 0;  // A-slot / ring counters, in step with the MMA issuer
         bool ok = true;
@@ -816,10 +813,8 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             const int items = tile_items<GATED>(t);
             const float gn = GATED ? __bfloat162float(__high2bfloat16(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31])))
                                    : 1.f;
-            if (!(ok = mbar_wait(&g_full, j & 1, &abort_flag))) break;
-            tc_fence_after();
             // the token's query row from the Q panels (SWIZZLE_128B: 16-byte chunk c of
-            // row r sits at chunk c ^ (r % 8)); G has finished reading them
+            // row r sits at chunk c ^ (r % 8)), read while G runs
             uint32_t qp[64];
             if (!(ok = mbar_wait(&ring_full[g % kRing], (g / kRing) & 1, &abort_flag) &&
                        mbar_wait(&ring_full[(g + 2) % kRing], ((g + 2) / kRing) & 1, &abort_flag)))
@@ -837,7 +832,9 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 }
             }
             mbar_arrive(&q_read);
-            if (leader) {
+            if (!(ok = mbar_wait(&g_full, j & 1, &abort_flag))) break;
+            tc_fence_after();
+            if (leader) {  // G and every worker are done with the Q panels
                 if (!(ok = mbar_wait(&q_read, j & 1, &abort_flag))) break;
                 mbar_arrive(&ring_empty[g % kRing]);
                 mbar_arrive(&ring_empty[(g + 2) % kRing]);
@@ -906,30 +903,27 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             }
             tc_fence_before();
             mbar_arrive(&y_empty);
-            const int r0 = t.bh * a.L + t.n * a.C + t.c * kCT;
+            // y rows go out through a warp-private 2 KB transpose in shared memory: the
+            // warp writes its 32 rows (64 bytes each per 32-column chunk, 16-byte chunks
+            // XOR-swizzled), then stores 8 rows x 64 contiguous bytes per instruction
+            uint8_t *wst = stage + q4 * 2048;
+            __nv_bfloat16 *yrow0 = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + 32 * q4) * kD;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {  // 32 columns per store
-                const uint32_t use = 4 * (uint32_t)j + cc;  // uses of the staging buffer so far
-                uint8_t *buf = stage;
-                if (!(ok = mbar_wait(&stage_free, (use & 1) ^ 1, &abort_flag))) break;
-                // SWIZZLE_64B: 16-byte chunk c of a 64-byte row r sits at chunk c ^ ((r / 2) % 4)
-                uint8_t *pr = buf + row * 64;
+            for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(pr + ((c ^ ((row >> 1) & 3)) << 4)) =
+                    *reinterpret_cast<uint4 *>(wst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
                         make_uint4(yb[16 * cc + 4 * c], yb[16 * cc + 4 * c + 1], yb[16 * cc + 4 * c + 2], yb[16 * cc + 4 * c + 3]);
-                fence_async_smem();
-                mbar_arrive(&stage_full);
-                if (leader) {
-                    if (!(ok = mbar_wait(&stage_full, use & 1, &abort_flag))) break;
-                    tma_store_2d(&mY, buf, 32 * cc, r0);
-                    bulk_commit_group();
-                    bulk_wait_group_read<0>();
-                    mbar_arrive(&stage_free);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 8 * i + (lane >> 2), c = lane & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(wst + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+                    *reinterpret_cast<uint4 *>(yrow0 + (size_t)r * kD + 32 * cc + 8 * c) = v;
                 }
+                __syncwarp();
             }
         }
-        if (leader) bulk_wait_group<0>();  // every y store has completed
     }
     tc_fence_before();
     __syncthreads();
@@ -1042,11 +1036,10 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.CPS = (int)CPS;
     a.num_tiles = (int)(BH * N * CPS);
 
-    CUtensorMap mQ, mK, mV, mV64, mY, mU;
+    CUtensorMap mQ, mK, mV, mV64, mU;
     const unsigned long long rows = (unsigned long long)BH * p.L;
     if (!make_tmap_bf16_sw128(&mQ, fa.q, rows, kD, 128) || !make_tmap_bf16_sw128(&mK, fa.k, rows, kD, 128) ||
-        !make_tmap_bf16_sw128(&mV, fa.v, rows, kD, 128) || !make_tmap_bf16_sw128(&mV64, fa.v, rows, kD, 64) ||
-        !make_tmap_bf16(&mY, fa.y, rows, kD, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_tmap_bf16_sw128(&mV, fa.v, rows, kD, 128) || !make_tmap_bf16_sw128(&mV64, fa.v, rows, kD, 64))
         return cudaErrorInvalidValue;
     if (gated) {
         if (!make_tmap_bf16_sw128(&mU, fa.u, rows, kD, 128)) return cudaErrorInvalidValue;
@@ -1096,7 +1089,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         if (e != cudaSuccess) return e;
         const int slots = kT2CtasPerSm * g_num_sms;
         const int grid = a.num_tiles < slots ? a.num_tiles : slots;
-        k2<<<grid, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, mY, a);
+        k2<<<grid, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "readout_tc");
     }
