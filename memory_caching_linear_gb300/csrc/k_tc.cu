@@ -92,7 +92,8 @@ __device__ __forceinline__ uint32_t kmaj_off(int kk, uint32_t rows) { return (kk
 // ============================================================================
 constexpr int kT1Threads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 workers
 constexpr uint32_t kT1Stage = 3 * kTile;      // K, V, U tiles of one chunk
-constexpr size_t kT1Smem = 2 * kT1Stage + 1024;
+constexpr uint32_t kT1Stage2 = 4096;           // per worker warp: 32 rows x 128 bytes of a store in flight
+constexpr size_t kT1Smem = 2 * kT1Stage + 4 * kT1Stage2 + 1024;
 
 template <bool GATED>
 __global__ void __launch_bounds__(kT1Threads, 1)
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (Z, S) = key column (sums)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         float S[kD];  // running state row: S[row][k] = sum_{j before the chunk} v_j[row] k_j[k]
+        uint8_t *wst = sm + 2 * kT1Stage + q4 * kT1Stage2;  // this warp's staging area for global stores
         float ks = 0.f;  // running sum of key column `row` over the segment, in token order
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
             const uint8_t *st = sm + s * kT1Stage;
             if (GATED && ok) {
-                float dot = 0.f;  // <u_t, keys of the segment before this chunk>, 8 elements per 16-byte load
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};  // <u_t, keys of the segment before this chunk>
 #pragma unroll
                 for (int cc = 0; cc < 16; ++cc) {
                     const uint4 x = *reinterpret_cast<const uint4 *>(st + 2 * kTile + sw128_offset(row, 8 * cc, 128));
@@ -228,24 +230,28 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     const float2 u23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
                     const float2 u45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.z));
                     const float2 u67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.w));
-                    dot = fmaf(u01.x, k0.x, dot); dot = fmaf(u01.y, k0.y, dot);
-                    dot = fmaf(u23.x, k0.z, dot); dot = fmaf(u23.y, k0.w, dot);
-                    dot = fmaf(u45.x, k1.x, dot); dot = fmaf(u45.y, k1.y, dot);
-                    dot = fmaf(u67.x, k1.z, dot); dot = fmaf(u67.y, k1.w, dot);
+                    float &dd = d4[cc & 3];
+                    dd = fmaf(u01.x, k0.x, dd); dd = fmaf(u01.y, k0.y, dd);
+                    dd = fmaf(u23.x, k0.z, dd); dd = fmaf(u23.y, k0.w, dd);
+                    dd = fmaf(u45.x, k1.x, dd); dd = fmaf(u45.y, k1.y, dd);
+                    dd = fmaf(u67.x, k1.z, dd); dd = fmaf(u67.y, k1.w, dd);
                 }
+                const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
                 ok = mbar_wait(&r_full[b], r & 1, &abort_flag);
                 if (ok) {
                     tc_fence_after();
-                    float w = 0.f;  // sum_{j <= t} <u_t, k_j> within the chunk
+                    float w4[4] = {0.f, 0.f, 0.f, 0.f};  // sum_{j <= t} <u_t, k_j> within the chunk
 #pragma unroll
                     for (int j16 = 0; j16 < 8; ++j16) {
+                        if (16 * j16 > 32 * q4 + 31) break;  // columns past the warp's last row are masked
                         uint32_t v[16];
                         tmem_ld16(tR0 + b * 128 + lane_base + 16 * j16, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            if ((uint32_t)(16 * j16 + i) <= row) w += __uint_as_float(v[i]);
+                            if ((uint32_t)(16 * j16 + i) <= row) w4[i & 3] += __uint_as_float(v[i]);
                     }
+                    const float w = (w4[0] + w4[1]) + (w4[2] + w4[3]);
                     tc_fence_before();
                     mbar_arrive(&r_empty[b]);
                     const int t_in_seg = c * kCT + (int)row;
@@ -298,16 +304,45 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 mbar_arrive(&z_empty[b]);
                 const size_t sidx = (size_t)bh * a.N + seg;
                 uint8_t *img = c + 1 < nch ? a.spre_img + (sidx * a.CPS + c + 1) * kTile : a.states_img + sidx * kTile;
+                // Through the warp's 4 KB staging area, one 64-column panel at a time: the
+                // warp's 32 rows of a panel are 4 KB contiguous in the image, stored 512
+                // contiguous bytes per instruction.
 #pragma unroll
-                for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunks of 8 bf16
-                    const uint4 v = make_uint4(pack_bf16x2(S[8 * cc], S[8 * cc + 1]), pack_bf16x2(S[8 * cc + 2], S[8 * cc + 3]),
-                                               pack_bf16x2(S[8 * cc + 4], S[8 * cc + 5]), pack_bf16x2(S[8 * cc + 6], S[8 * cc + 7]));
-                    *reinterpret_cast<uint4 *>(img + sw128_offset(row, 8 * cc, 128)) = v;
+                for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {  // 16-byte chunk c8 of the row's panel p
+                        const int cc = 8 * p + c8;
+                        const uint4 v = make_uint4(pack_bf16x2(S[8 * cc], S[8 * cc + 1]), pack_bf16x2(S[8 * cc + 2], S[8 * cc + 3]),
+                                                   pack_bf16x2(S[8 * cc + 4], S[8 * cc + 5]), pack_bf16x2(S[8 * cc + 6], S[8 * cc + 7]));
+                        *reinterpret_cast<uint4 *>(wst + sw128_offset(lane, 8 * c8, 32)) = v;
+                    }
+                    __syncwarp();
+                    uint4 *dst = reinterpret_cast<uint4 *>(img + p * 16384 + (32 * q4) * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dst[32 * i + lane] = reinterpret_cast<const uint4 *>(wst)[32 * i + lane];
+                    __syncwarp();
                 }
                 if (c + 1 == nch) {  // the segment's cached state (fp32) and key mean
-                    float4 *o = reinterpret_cast<float4 *>(a.states + sidx * kD * kD + (size_t)row * kD);
+                    // fp32 rows of 512 bytes, 32 columns (128 bytes) at a time through the staging
+                    // area (16-byte chunk c of row r at chunk c ^ (r % 8)), 4 rows per instruction
+                    float *o = a.states + sidx * kD * kD + (size_t)(32 * q4) * kD;
 #pragma unroll
-                    for (int i = 0; i < kD / 4; ++i) o[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+                    for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const int e = 32 * blk + 4 * c8;
+                            *reinterpret_cast<float4 *>(wst + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                                make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = 4 * i + (lane >> 3), c8 = lane & 7;
+                            const float4 v = *reinterpret_cast<const float4 *>(wst + r * 128 + ((c8 ^ (r & 7)) << 4));
+                            *reinterpret_cast<float4 *>(o + (size_t)r * kD + 32 * blk + 4 * c8) = v;
+                        }
+                        __syncwarp();
+                    }
                     if (GATED) {
                         const float kbv = ks / (float)a.C;
                         const __nv_bfloat16 hi = __float2bfloat16_rn(kbv);
@@ -483,15 +518,19 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             const int n = t0 / a.C;
             if (!mbar_wait(&s_full[b], (i >> 1) & 1, &abort_flag)) break;
             tc_fence_after();
+            // Only the first n scores take part; n is the same for the whole tile, so
+            // the loops below skip whole groups of 8 segments uniformly.
             float sc[64];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                uint32_t v[16];
-                tmem_ld16(tb + b * 64 + lane_base + 16 * m, v);
-                tmem_wait_ld();
+                if (16 * m < n) {
+                    tmem_ld16f(tb + b * 64 + lane_base + 16 * m, sc + 16 * m);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) sc[16 * m + k] = __uint_as_float(v[k]);
+                    for (int k = 0; k < 16; ++k) sc[16 * m + k] = 0.f;
+                }
             }
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&s_empty[b]);
             const size_t tok = (size_t)bh * a.L + t0 + row;
@@ -507,11 +546,17 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
                     float best = 0.f;
                     int bi = -1;
 #pragma unroll
-                    for (int k = 0; k < 63; ++k)
-                        if (k < n && !((chosen >> k) & 1ull) && (bi < 0 || sc[k] > best)) {
-                            best = sc[k];
-                            bi = k;
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        if (8 * g8 >= n) break;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int k = 8 * g8 + kk;
+                            if (k < 63 && k < n && !((chosen >> k) & 1ull) && (bi < 0 || sc[k] > best)) {
+                                best = sc[k];
+                                bi = k;
+                            }
                         }
+                    }
                     chosen |= 1ull << bi;
                     if (so) so[r] = bi;
                 }
@@ -521,16 +566,29 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             }
             float mx4[4] = {ron, ron, ron, ron};  // partial maxima / sums: shorter dependency chains
 #pragma unroll
-            for (int k = 0; k < 63; ++k)
-                if ((take >> k) & 1ull) mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
+            for (int g8 = 0; g8 < 8; ++g8) {
+                if (8 * g8 >= n) break;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int k = 8 * g8 + kk;
+                    if (k < 63 && ((take >> k) & 1ull)) mx4[kk & 3] = fmaxf(mx4[kk & 3], sc[k]);
+                }
+            }
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 63; ++k) {
-                sc[k] = ((take >> k) & 1ull) ? expf(sc[k] - mx) : 0.f;
-                z4[k & 3] += sc[k];
+            for (int g8 = 0; g8 < 8; ++g8) {
+                if (8 * g8 >= n) break;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int k = 8 * g8 + kk;
+                    if (k < 63) {
+                        sc[k] = ((take >> k) & 1ull) ? __expf(sc[k] - mx) : 0.f;
+                        z4[kk & 3] += sc[k];
+                    }
+                }
             }
-            sc[63] = expf(ron - mx);
+            sc[63] = __expf(ron - mx);
             const float inv = 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
             if (!a.gam) continue;  // router only (mc_ssc_select)
             uint32_t *dst = a.gam + (size_t)it * (32 * kCT) + row;
