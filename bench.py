@@ -16,6 +16,7 @@ slowest rank's time ("scaling": "weak").
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -76,6 +77,42 @@ def algorithmic_bytes(w):
 
 
 # ----------------------------------------------------------------------------- peaks and clocks
+
+KERNEL_SOURCES = ("memory_caching_linear_gb300/csrc/k_tc.cu", "memory_caching_linear_gb300/csrc/sm100.cuh",
+                  "memory_caching_linear_gb300/csrc/mc_internal.cuh")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the tensor-core kernel sources, in a fixed order."""
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary
+    profiles/<kernel>_<workload>.md, or None when there is none or the kernel sources
+    changed after the counters were taken (the summary records their hash)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().lstrip("-").strip()
+        if ":" in line:
+            key, _, val = line.partition(":")
+            fields[key.strip().strip("`")] = val.strip().strip("`")
+    try:
+        if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError, OSError):
+        return None
+
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -207,7 +244,7 @@ def oracle_sample(w, budget_s: float, steps_hint: int = 1):
 
 # ----------------------------------------------------------------------------- our arm
 
-def run_ours(args, w):
+def run_ours(args, w, wname="long-grm"):
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -291,7 +328,7 @@ def run_ours(args, w):
             psrc = "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"
             bound = "alu"
         roof = {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom_name,
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom_name, wname), "kernel": dom_name,
                 "launch_ms": round(avg_ms, 4), "algorithmic_tflop_per_launch": round(work / 1e12, 4),
                 "peak_source": psrc}
 
@@ -397,7 +434,7 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.mode:
         w = w.with_(mode={"residual": RESIDUAL, "grm": GRM, "soup": 2, "ssc": SSC}[args.mode])
-    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w, args.workload)
     if res is not None:
         print(json.dumps(res), flush=True)
 

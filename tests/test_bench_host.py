@@ -64,3 +64,22 @@ def test_reduce_max_two_gloo_ranks():
 
 def test_single_rank_reduce_is_identity():
     assert bench.reduce_max(3.5, None) == 3.5
+
+
+def test_roofline_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """`traffic` comes from a committed ncu summary only while the kernel sources it
+    was taken on are unchanged (the summary records their sha256)."""
+    for rel in bench.KERNEL_SOURCES:
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        dst.write_text("kernel source " + rel)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    summary = tmp_path / "profiles" / "readout_tc_long-grm.md"
+    assert bench.ncu_traffic("readout_tc", "long-grm") is None  # no summary
+    summary.write_text(f"# x\n\n- kernel_source_sha256: `{bench.kernel_source_hash()}`\n"
+                       "- traffic_bytes_per_launch: 1698533376\n")
+    assert bench.ncu_traffic("readout_tc", "long-grm") == 1698533376
+    (tmp_path / bench.KERNEL_SOURCES[0]).write_text("changed")
+    assert bench.ncu_traffic("readout_tc", "long-grm") is None
+    assert bench.ncu_traffic("gates_tc", "long-grm") is None
