@@ -306,26 +306,74 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
         return MC_ERR_ALLOC;
     }
     char *p = static_cast<char *>(dmem);
-    void *dq = p, *dk = p + bytes_in, *dv = p + 2 * bytes_in;
-    void *du = nin == 4 ? p + 3 * bytes_in : nullptr;
-    void *dy = p + nin * bytes_in;
+    char *dq = p, *dk = p + bytes_in, *dv = p + 2 * bytes_in;
+    char *du = nin == 4 ? p + 3 * bytes_in : nullptr;
+    char *dy = p + nin * bytes_in;
     float *ds = states ? reinterpret_cast<float *>(p + (nin + 1) * bytes_in) : nullptr;
-    cudaError_t e = cudaMemcpyAsync(dq, q, n_in * elt, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, n_in * elt, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, n_in * elt, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess && du) e = cudaMemcpyAsync(du, u, n_in * elt, cudaMemcpyHostToDevice, stream);
+    // The (b, h) problems are independent, so the copies are pipelined against the
+    // forward over groups of heads: inputs of group c go up on `up` while group c-1
+    // runs on `stream` and y of group c-2 comes down on `down`.
+    const size_t BH = (size_t)B * H;
+    const int groups = BH >= 8 ? 8 : (int)BH;
+    const size_t per = (BH + groups - 1) / groups;  // heads per group
+    const size_t head_in = (size_t)L * d * elt, head_st = N * (size_t)d * d;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t ev[2 * 8 + 3] = {};
+    const int nev = 2 * groups + 3;
+    cudaError_t e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking);
+    for (int i = 0; i < nev && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    cudaEvent_t ev_alloc = ev[2 * groups], ev_up = ev[2 * groups + 1], ev_down = ev[2 * groups + 2];
     int rc = MC_OK;
-    if (e == cudaSuccess) {
-        rc = is_bf16 ? mc_forward(dq, dk, dv, du, B, H, L, d, seg_len, agg_mode, topk, dy, ds, stream_)
-                     : mc_forward_f32(static_cast<const float *>(dq), static_cast<const float *>(dk),
-                                      static_cast<const float *>(dv), static_cast<const float *>(du), B, H, L, d,
-                                      seg_len, agg_mode, topk, static_cast<float *>(dy), ds, stream_);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_alloc, stream);  // the device buffers exist from here on
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(up, ev_alloc, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(down, ev_alloc, 0);
+    for (int c = 0; c < groups && e == cudaSuccess && rc == MC_OK; ++c) {
+        const size_t h0 = c * per;
+        if (h0 >= BH) break;
+        const size_t hc = BH - h0 < per ? BH - h0 : per;
+        const size_t off = h0 * head_in, bytes = hc * head_in;
+        const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
+                   *hv = static_cast<const char *>(v), *hu = static_cast<const char *>(u);
+        e = cudaMemcpyAsync(dq + off, hq + off, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dk + off, hk + off, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dv + off, hv + off, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess && du) e = cudaMemcpyAsync(du + off, hu + off, bytes, cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2 * c], up);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[2 * c], 0);
+        if (e != cudaSuccess) break;
+        float *dsc = ds ? ds + h0 * head_st : nullptr;
+        rc = is_bf16 ? mc_forward(dq + off, dk + off, dv + off, du ? du + off : nullptr, 1, (int)hc, L, d, seg_len,
+                                  agg_mode, topk, dy + off, dsc, stream_)
+                     : mc_forward_f32(reinterpret_cast<const float *>(dq + off), reinterpret_cast<const float *>(dk + off),
+                                      reinterpret_cast<const float *>(dv + off),
+                                      du ? reinterpret_cast<const float *>(du + off) : nullptr, 1, (int)hc, L, d,
+                                      seg_len, agg_mode, topk, reinterpret_cast<float *>(dy + off), dsc, stream_);
+        if (rc != MC_OK) break;
+        e = cudaEventRecord(ev[2 * c + 1], stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(down, ev[2 * c + 1], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(y) + off, dy + off, bytes, cudaMemcpyDeviceToHost, down);
+        if (e == cudaSuccess && states)
+            e = cudaMemcpyAsync(states + h0 * head_st, dsc, sizeof(float) * hc * head_st, cudaMemcpyDeviceToHost, down);
     }
-    if (e == cudaSuccess && rc == MC_OK) e = cudaMemcpyAsync(y, dy, n_in * elt, cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess && rc == MC_OK && states)
-        e = cudaMemcpyAsync(states, ds, sizeof(float) * (size_t)B * H * N * d * d, cudaMemcpyDeviceToHost, stream);
+    // everything on `up` and `down` is ordered before the free on `stream`
+    cudaError_t ew = cudaSuccess;
+    if (up && ev_up && (ew = cudaEventRecord(ev_up, up)) == cudaSuccess) ew = cudaStreamWaitEvent(stream, ev_up, 0);
+    if (down && ev_down && ew == cudaSuccess && (ew = cudaEventRecord(ev_down, down)) == cudaSuccess)
+        ew = cudaStreamWaitEvent(stream, ev_down, 0);
+    if (ew != cudaSuccess) {  // cannot order the free after the copies: wait for them here
+        if (up) cudaStreamSynchronize(up);
+        if (down) cudaStreamSynchronize(down);
+    }
     cudaError_t ef = cudaFreeAsync(dmem, stream);
     cudaError_t es = cudaStreamSynchronize(stream);
+    if (up) cudaStreamSynchronize(up);
+    if (down) cudaStreamSynchronize(down);
+    for (int i = 0; i < nev; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    if (up) cudaStreamDestroy(up);
+    if (down) cudaStreamDestroy(down);
     if (rc != MC_OK) return rc;
     if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess) {
         cudaGetLastError();

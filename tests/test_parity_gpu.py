@@ -175,6 +175,20 @@ def test_host_entry_point_matches_device_call():
     assert torch.equal(st_host, st_dev.cpu())
 
 
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (RESIDUAL, 0), (SSC, 2)])
+def test_host_entry_point_head_groups(mode, topk):
+    """B*H = 15 heads go through the host entry point's copy/compute pipeline as
+    uneven head groups; the result equals one device call bit for bit."""
+    q, k, v, u = make_inputs(3, 5, 512, 128, 11, "bf16")
+    qp, kp, vp, up = (t.pin_memory() for t in (q, k, v, u))
+    y_host, st_host = mcl.mc_forward_host(qp, kp, vp, up, 128, mode, topk,
+                                          states=torch.empty(3, 5, 4, 128, 128).pin_memory())
+    y_dev, st_dev = mcl.mc_forward(qp.cuda(), kp.cuda(), vp.cuda(), up.cuda(), 128, mode, topk)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
+    assert torch.equal(st_host, st_dev.cpu())
+
+
 def test_bad_arguments_raise():
     x = torch.zeros(1, 1, 8, 24, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mcl.MCError) as e:
