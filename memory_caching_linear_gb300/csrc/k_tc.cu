@@ -613,8 +613,7 @@ constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
 constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
 constexpr int kRing = 6;           // operand panels in flight per CTA
 constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
-constexpr uint32_t kStage = 8192;  // y staging: 128 rows x 32 columns bf16, 2 KB per worker warp
-constexpr size_t kT2Smem = kRing * kPanel + kStage + 1024;  // two CTAs fit in an SM's 228 KB
+constexpr size_t kT2Smem = kRing * kPanel + 1024;  // two CTAs fit in an SM's 228 KB
 
 struct TileInfo {
     int n, c, bh;
@@ -660,7 +659,7 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 // Operands stream through a ring of 16 KB panels (a K-half of a 128 x 128 tile;
 // V in key halves).  The workers take their query rows from the Q panels (and
 // release those panels once G is done), read the gate rows in the tile-transposed
-// layout (coalesced), and write y through a small shared-memory transpose.  Two CTAs run on each SM, so while one waits on its G -> P step or its
+// layout (coalesced), and write y from a quad-transposed register layout.  Two CTAs run on each SM, so while one waits on its G -> P step or its
 // drain the other keeps the tensor pipe busy.
 template <bool GATED>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
@@ -842,7 +841,6 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const bool leader = warp == 2 && lane == 0;  // releases the Q panels
-        uint8_t *stage = sm + kRing * kPanel;
         uint32_t ac = 0, g = 0;  // A-slot / ring counters, in step with the MMA issuer
         bool ok = true;
         uint32_t gm2[32];  // gate pairs of the token: (g_{2p}, g_{2p+1}); g_n is element 63
@@ -947,39 +945,52 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             if (!ok) break;
             g += 6 + 2 * items;
             if (j + 1 < my_tiles) load_gates(j + 1);  // lands while this tile's MMAs finish
-            // drain: read D, release it, then write y (bf16) through the staging buffers
+            // drain: read D in the 16x256b layout (a quad of threads holds 8 consecutive
+            // columns of a row), release it, then transpose within each quad by shuffles
+            // so that every thread stores 16 contiguous bytes: 8 rows x 64 bytes per store
             if (!(ok = mbar_wait(&y_full, j & 1, &abort_flag))) break;
             tc_fence_after();
-            uint32_t yb[64];
+            uint32_t yb[64];  // [lane half][column half]: 8 pairs of row A, then 8 of row B
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t x[32];
-                tmem_ld32(tD + lane_base + 32 * h, x);
-                tmem_wait_ld();
+            for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) yb[16 * h + i] = pack_bf16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-            }
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t x[32];
+                    tmem_ld_16x256b_x8(tD + ((uint32_t)(32 * q4 + 16 * hl) << 16) + 64 * ch, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        yb[16 * (2 * hl + ch) + b] = pack_bf16x2(__uint_as_float(x[4 * b]), __uint_as_float(x[4 * b + 1]));
+                        yb[16 * (2 * hl + ch) + 8 + b] = pack_bf16x2(__uint_as_float(x[4 * b + 2]), __uint_as_float(x[4 * b + 3]));
+                    }
+                }
             tc_fence_before();
             mbar_arrive(&y_empty);
-            // y rows go out through a warp-private 2 KB transpose in shared memory: the
-            // warp writes its 32 rows (64 bytes each per 32-column chunk, 16-byte chunks
-            // XOR-swizzled), then stores 8 rows x 64 contiguous bytes per instruction
-            uint8_t *wst = stage + q4 * 2048;
-            __nv_bfloat16 *yrow0 = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + 32 * q4) * kD;
+            {
+                const int c = lane & 3;
+                __nv_bfloat16 *ytile = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) * kD;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+                for (int g4 = 0; g4 < 16; ++g4) {  // (lane half, column half, row A/B, block group) groups of 4 pairs
+                    uint32_t *xv = yb + 4 * g4;
+                    // 4 x 4 transpose across the quad: thread c ends with block (4 (g4 % 2) + c)
+                    // of its row, columns in order
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(wst + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-                        make_uint4(yb[16 * cc + 4 * c], yb[16 * cc + 4 * c + 1], yb[16 * cc + 4 * c + 2], yb[16 * cc + 4 * c + 3]);
-                __syncwarp();
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const uint32_t send = (c & 2) ? xv[k2] : xv[k2 + 2];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+                        if (c & 2) xv[k2] = recv; else xv[k2 + 2] = recv;
+                    }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 8 * i + (lane >> 2), c = lane & 3;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(wst + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-                    *reinterpret_cast<uint4 *>(yrow0 + (size_t)r * kD + 32 * cc + 8 * c) = v;
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        const uint32_t send = (c & 1) ? xv[2 * b2] : xv[2 * b2 + 1];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        if (c & 1) xv[2 * b2] = recv; else xv[2 * b2 + 1] = recv;
+                    }
+                    const int hl = g4 >> 3, ch = (g4 >> 2) & 1, rb = (g4 >> 1) & 1, bg = g4 & 1;
+                    const int r = 32 * q4 + 16 * hl + 8 * rb + (lane >> 2);
+                    *reinterpret_cast<uint4 *>(ytile + (size_t)r * kD + 64 * ch + 8 * (4 * bg + c)) =
+                        make_uint4(xv[0], xv[1], xv[2], xv[3]);
                 }
-                __syncwarp();
             }
         }
     }
