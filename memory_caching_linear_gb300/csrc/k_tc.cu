@@ -1,41 +1,40 @@
 // k_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) path of the Memory Caching
-// forward for bf16 inputs, d = 128, seg_len a multiple of 128, L a multiple of
-// seg_len, N <= 64, aggregations Residual / GRM / Soup.
+// forward for bf16 inputs, d = 64 or 128 (tiles are 128 wide; a 64-wide tensor
+// is zero-padded by the TMA's out-of-bounds fill), seg_len a multiple of 128, L a
+// multiple of seg_len, N <= 64, aggregations Residual / GRM / Soup / SSC (topk <= 16).
 //
 // Pages cited:
 //   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
 //   [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
 //            (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
 //
-// Two kernels.
+// Three kernels.
 //
-// seg_state_tc -- one CTA per (bh, segment n).  Walks the segment in chunks of
-//   128 tokens with the running state S = sum v_j k_j^T in tensor memory (fp32):
+// seg_state_tc -- persistent; each CTA walks its segments in chunks of 128 tokens
+//   with the running state S = sum v_j k_j^T (fp32, one row per worker thread):
 //     S += V_c^T K_c                        (update rule, [MC-ja §3 eq. 4b])
 //   Before each chunk's update it writes S (the state before the chunk) as a bf16
 //   operand image (the "prefix state" of the chunk); at the end S is the
 //   segment's cached state M^(n) ([MC-ja §3, after eq. 4b]), written as fp32
 //   (the states output) and as a bf16 image.  It also forms the key mean
-//   kbar_n ([MC-ja §3.1 eq. 10], pooled keys) as fp32 hi + lo bf16 rows of a
+//   kbar_n ([MC-ja §3.1 eq. 10], pooled keys) as hi + lo bf16 rows of a
 //   per-head operand image, and the online gate score
 //     r_on[t] = <u_t, sum_{j=t0..t} k_j> / (t - t0 + 1)
 //   from R = U_c K_c^T (tensor core) masked to j <= t plus <u_t, keys before the chunk>.
 //
-// readout_tc -- persistent; a tile is (bh, segment n, chunk c) of 128 tokens,
-//   heaviest tiles first.  For the tile's tokens it computes
-//     y_t = g_{t,n} [ P_t (S_pre(c) q_t) + sum_{j in chunk, j<=t} v_j (k_j . q_t) ]
+// gates_tc -- per 128-token chunk, the scores <u_t, kbar_i> (two MMAs: hi and lo
+//   rows) and the gates g = softmax over {scores_i}_{i<n} and r_on[t] (GRM;
+//   Soup is the same sum for a linear memory, [MC-sum §3.3]); SSC keeps the topk
+//   largest cached scores ([MC-sum §3.4]) and gives the others gate 0.
+//
+// readout_tc -- persistent, two CTAs per SM; a tile is (bh, segment n, chunk c)
+//   of 128 tokens, heaviest tiles first.  For the tile's tokens it computes
+//     y_t = g_{t,n} [ S_pre(c) q_t + sum_{j in chunk, j<=t} v_j (k_j . q_t) ]
 //         + sum_{i<n} g_{t,i} M^(i) q_t                      ([MC-ja §3.1 eq. 9])
-//   with g = softmax over {<u_t, kbar_i>}_{i<n} and r_on[t] (GRM; Soup is the
-//   same sum for a linear memory, [MC-sum §3.3]) or g = 1 (Residual, [MC-ja
-//   §3.1 eq. 7], where the cached sum collapses to one prefix state).  Every
-//   term is an MMA into one fp32 accumulator D_Y[t][v]:
-//     online:  G = Q K_c^T;  D_Y  = (g_n * mask(G)) V_c
-//     cached:  D_Y += (g_i o Q) X_i^T  for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}
-//   The A operands (g_i o Q, the masked P) are written into tensor memory by
-//   four "A" warps (thread = token row); four "aux" warps compute the next
-//   tile's scores and softmax while the current tile streams its cached states,
-//   and drain the double-buffered accumulator.  One warp issues TMA / bulk
-//   copies, one issues the MMAs.
+//   (Residual: g = 1, [MC-ja §3.1 eq. 7], where the cached sum collapses to one
+//   prefix state) as MMAs into one fp32 accumulator D per CTA:
+//     G = Q K_c^T;  D = (g_n * mask(G)) V_c;  D += (g_i o Q) X_i^T
+//   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.
 #include <cstdint>
 
 #include "mc_internal.cuh"
@@ -52,7 +51,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 128;            // head dimension of this path
+constexpr int kD = 128;            // tile width: the head dimension (64 or 128), zero-padded to it
 constexpr int kTcMaxTopk = 16;     // SSC selections per token handled by the tensor-core path
 constexpr int kCT = 128;           // tokens per chunk / tile
 constexpr uint32_t kTile = 32768;  // one 128 x 128 bf16 operand tile
@@ -71,6 +70,7 @@ struct TcArgs {
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
     int BH, L, C, N, CPS;
+    int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
     int num_tiles;
 };
 
@@ -323,11 +323,14 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     __syncwarp();
                 }
                 if (c + 1 == nch) {  // the segment's cached state (fp32) and key mean
-                    // fp32 rows of 512 bytes, 32 columns (128 bytes) at a time through the staging
-                    // area (16-byte chunk c of row r at chunk c ^ (r % 8)), 4 rows per instruction
-                    float *o = a.states + sidx * kD * kD + (size_t)(32 * q4) * kD;
+                    // fp32 rows (d values), 32 columns (128 bytes) at a time through the staging
+                    // area (16-byte chunk c of row r at chunk c ^ (r % 8)), 4 rows per instruction;
+                    // with d < 128 the padded rows and columns are not stored
+                    const int d = a.d;
+                    float *o = a.states + sidx * d * d + (size_t)(32 * q4) * d;
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk) {
+                        if (32 * q4 >= d || 32 * blk >= d) break;  // warp-uniform
 #pragma unroll
                         for (int c8 = 0; c8 < 8; ++c8) {
                             const int e = 32 * blk + 4 * c8;
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                         for (int i = 0; i < 8; ++i) {
                             const int r = 4 * i + (lane >> 3), c8 = lane & 7;
                             const float4 v = *reinterpret_cast<const float4 *>(wst + r * 128 + ((c8 ^ (r & 7)) << 4));
-                            *reinterpret_cast<float4 *>(o + (size_t)r * kD + 32 * blk + 4 * c8) = v;
+                            *reinterpret_cast<float4 *>(o + (size_t)r * d + 32 * blk + 4 * c8) = v;
                         }
                         __syncwarp();
                     }
@@ -371,13 +374,14 @@ __global__ void __launch_bounds__(kD) kbar_images_tc(const __nv_bfloat16 *__rest
 {
     const int seg = blockIdx.x % a.N, bh = blockIdx.x / a.N;
     const int col = threadIdx.x;
-    const __nv_bfloat16 *src = k + ((size_t)bh * a.L + (size_t)seg * a.C) * kD + col;
+    if (col >= a.d) return;  // the image's padded columns stay zero
+    const __nv_bfloat16 *src = k + ((size_t)bh * a.L + (size_t)seg * a.C) * a.d + col;
     float s = 0.f;
     for (int c0 = 0; c0 < a.C; c0 += kCT) {  // the state kernel's order: 16-row groups, then chunks
         float cs = 0.f;
         for (int rg = 0; rg < 8; ++rg) {
             float p = 0.f;
-            for (int i = 0; i < 16; ++i) p += __bfloat162float(src[(size_t)(c0 + 16 * rg + i) * kD]);
+            for (int i = 0; i < 16; ++i) p += __bfloat162float(src[(size_t)(c0 + 16 * rg + i) * a.d]);
             cs += p;
         }
         s += cs;
@@ -395,13 +399,14 @@ __global__ void __launch_bounds__(kD) kbar_images_tc(const __nv_bfloat16 *__rest
 __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
 {
     const int bh = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;  // element of the d x d state
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;  // element of the 128 x 128 image
     if (e >= kD * kD) return;
-    const int v = e / kD, k = e % kD;
-    const float *st = a.states + (size_t)bh * a.N * kD * kD + e;
+    const int v = e / kD, k = e % kD, d = a.d;
+    const bool inside = v < d && k < d;  // padding (d < 128) stays zero
+    const float *st = a.states + (size_t)bh * a.N * d * d + (inside ? v * d + k : 0);
     float acc = 0.f;
     for (int n = 1; n < a.N; ++n) {
-        acc += st[(size_t)(n - 1) * kD * kD];
+        if (inside) acc += st[(size_t)(n - 1) * d * d];
         *reinterpret_cast<__nv_bfloat16 *>(a.prefix_img + ((size_t)bh * a.N + n) * kTile + sw128_offset(v, k, 128)) =
             __float2bfloat16_rn(acc);
     }
@@ -968,9 +973,10 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             mbar_arrive(&y_empty);
             {
                 const int c = lane & 3;
-                __nv_bfloat16 *ytile = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) * kD;
+                __nv_bfloat16 *ytile = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) * a.d;
 #pragma unroll
                 for (int g4 = 0; g4 < 16; ++g4) {  // (lane half, column half, row A/B, block group) groups of 4 pairs
+                    if (64 * ((g4 >> 2) & 1) >= a.d) continue;  // d = 64: the padded columns are not stored
                     uint32_t *xv = yb + 4 * g4;
                     // 4 x 4 transpose across the quad: thread c ends with block (4 (g4 % 2) + c)
                     // of its row, columns in order
@@ -988,7 +994,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     }
                     const int hl = g4 >> 3, ch = (g4 >> 2) & 1, rb = (g4 >> 1) & 1, bg = g4 & 1;
                     const int r = 32 * q4 + 16 * hl + 8 * rb + (lane >> 2);
-                    *reinterpret_cast<uint4 *>(ytile + (size_t)r * kD + 64 * ch + 8 * (4 * bg + c)) =
+                    *reinterpret_cast<uint4 *>(ytile + (size_t)r * a.d + 64 * ch + 8 * (4 * bg + c)) =
                         make_uint4(xv[0], xv[1], xv[2], xv[3]);
                 }
             }
@@ -1024,7 +1030,7 @@ cudaError_t take_device_abort(int *was_set)
 
 bool tc_supported(const Problem &p)
 {
-    return p.bf16 && p.d == kD && p.C % kCT == 0 && p.L % p.C == 0 && p.N <= 64 &&
+    return p.bf16 && (p.d == kD || p.d == 64) && p.C % kCT == 0 && p.L % p.C == 0 && p.N <= 64 &&
            (p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_RESIDUAL ||
             (p.mode == MC_SSC && p.topk >= 0 && p.topk <= kTcMaxTopk));
 }
@@ -1056,8 +1062,9 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
     a.C = p.C;
     a.N = p.N;
     a.CPS = p.C / kCT;
+    a.d = p.d;
     CUtensorMap mU;
-    if (!make_tmap_bf16_sw128(&mU, fa.u, (unsigned long long)p.BH * p.L, kD, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_sw128(&mU, fa.u, (unsigned long long)p.BH * p.L, p.d, 128)) return cudaErrorInvalidValue;
     if (g_num_sms == 0) {
         int dev = 0;
         cudaGetDevice(&dev);
@@ -1103,15 +1110,18 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.C = p.C;
     a.N = p.N;
     a.CPS = (int)CPS;
+    a.d = p.d;
     a.num_tiles = (int)(BH * N * CPS);
 
     CUtensorMap mQ, mK, mV, mV64, mU;
     const unsigned long long rows = (unsigned long long)BH * p.L;
-    if (!make_tmap_bf16_sw128(&mQ, fa.q, rows, kD, 128) || !make_tmap_bf16_sw128(&mK, fa.k, rows, kD, 128) ||
-        !make_tmap_bf16_sw128(&mV, fa.v, rows, kD, 128) || !make_tmap_bf16_sw128(&mV64, fa.v, rows, kD, 64))
+    // A tensor narrower than 128 (d = 64) reads its second 64-column panel entirely out
+    // of bounds, which the TMA fills with zeros: the 128-wide tiles are zero-padded.
+    if (!make_tmap_bf16_sw128(&mQ, fa.q, rows, p.d, 128) || !make_tmap_bf16_sw128(&mK, fa.k, rows, p.d, 128) ||
+        !make_tmap_bf16_sw128(&mV, fa.v, rows, p.d, 128) || !make_tmap_bf16_sw128(&mV64, fa.v, rows, p.d, 64))
         return cudaErrorInvalidValue;
     if (gated) {
-        if (!make_tmap_bf16_sw128(&mU, fa.u, rows, kD, 128)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16_sw128(&mU, fa.u, rows, p.d, 128)) return cudaErrorInvalidValue;
     } else {
         mU = mK;
     }

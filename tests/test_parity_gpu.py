@@ -108,7 +108,9 @@ TC_CASES = [
     ("tc-C512-N8", 1, 2, 4096, 128, 512),
     ("tc-C2048-N1", 2, 1, 2048, 128, 2048),
     ("tc-C256-N4-BH160", 10, 16, 1024, 128, 256),
+    ("tc-d64-C128-N32", 1, 2, 4096, 64, 128),  # d = 64: tiles zero-padded to 128 by the TMA
 ]
+TC_SSC_CASES = TC_CASES[:2] + TC_CASES[-1:]
 
 
 @pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP])
@@ -129,7 +131,7 @@ def test_parity_tensor_core_shapes(name, B, H, L, d, C, mode):
 
 
 @pytest.mark.parametrize("topk", [1, 3, 16])
-@pytest.mark.parametrize("name,B,H,L,d,C", TC_CASES[:2], ids=[c[0] for c in TC_CASES[:2]])
+@pytest.mark.parametrize("name,B,H,L,d,C", TC_SSC_CASES, ids=[c[0] for c in TC_SSC_CASES])
 def test_parity_tensor_core_ssc(name, B, H, L, d, C, topk):
     """SSC on the tensor-core path: router (mc_ssc_select, the forward's own) and y."""
     q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32((name + "ssc").encode()) % 1000, dtype="bf16")
