@@ -8,6 +8,10 @@ those workloads.  Draw order is q, k, v, u from one numpy PCG64 stream:
   v ~ N(0, 1);  u ~ N(0, 1) / sqrt(d).
 The values are then cast to the workload's input dtype (bf16 rounds to
 nearest-even); every consumer, the oracle included, receives the cast values.
+
+The SWLA workloads also draw per-token scalars (fp32, [B, H, L]) from a second
+PCG64 stream (seed + 1000), in the order alpha, beta, lambda, with z ~ N(0, 1):
+  alpha = 1 - 0.1 sigmoid(z)  (a decay in (0.9, 1)),  beta = sigmoid(z),  lambda = sigmoid(z).
 """
 from __future__ import annotations
 
@@ -33,6 +37,7 @@ class Workload:
     dtype: str  # "f32" or "bf16"
     topk: int = 0
     seed: int = 0
+    swla: bool = False  # sliding-window linear attention (c = 2) update instead of M += v k^T
 
     @property
     def N(self) -> int:
@@ -59,7 +64,10 @@ SSC_D128 = Workload("ssc B2 H16 L16384 d128 C256 k4 bf16", 2, 16, 16384, 128, 25
 LONG_GRM = Workload("long-grm B1 H16 L65536 d128 C1024 bf16", 1, 16, 65536, 128, 1024, GRM, "bf16",
                     seed=4)
 
-ALL = (TINY, GRM_D64) + SWEEP + (SSC_D128, LONG_GRM)
+SWLA_LONG = Workload("swla-grm B1 H16 L65536 d128 C1024 bf16", 1, 16, 65536, 128, 1024, GRM, "bf16",
+                     seed=5, swla=True)
+
+ALL = (TINY, GRM_D64) + SWEEP + (SSC_D128, LONG_GRM, SWLA_LONG)
 
 
 def _np_inputs(B: int, H: int, L: int, d: int, seed: int):
@@ -88,3 +96,19 @@ def make_inputs(B: int, H: int, L: int, d: int, seed: int, dtype: str = "bf16",
 
 def workload_inputs(w: Workload, device="cpu"):
     return make_inputs(w.B, w.H, w.L, w.d, w.seed, w.dtype, device)
+
+
+def make_swla_scalars(B: int, H: int, L: int, seed: int, device: str | torch.device = "cpu"):
+    """Return (alpha, beta, lambda) as contiguous fp32 torch tensors [B, H, L]."""
+    rng = np.random.default_rng(seed + 1000)
+    shape = (B, H, L)
+    za = rng.standard_normal(shape, dtype=np.float32)
+    zb = rng.standard_normal(shape, dtype=np.float32)
+    zl = rng.standard_normal(shape, dtype=np.float32)
+    sig = lambda z: (1.0 / (1.0 + np.exp(-z.astype(np.float64)))).astype(np.float32)
+    alpha = (np.float32(1.0) - np.float32(0.1) * sig(za)).astype(np.float32)
+    return tuple(torch.from_numpy(np.ascontiguousarray(a)).to(device) for a in (alpha, sig(zb), sig(zl)))
+
+
+def workload_swla_scalars(w: Workload, device="cpu"):
+    return make_swla_scalars(w.B, w.H, w.L, w.seed, device)

@@ -14,6 +14,10 @@ forward(q, k, v, u, seg_len, mode, topk=0, ...)
 bruteforce(q, k, v, u, seg_len, mode, topk=0)
     Token-level twin that never forms a memory matrix (tiny inputs only).
 
+Both take optional ``swla=(alpha, beta, lam)`` (arrays [B, H, L]): the sliding-
+window linear attention update with c = 2, M_t = alpha_t M_{t-1} + beta_t v_{t-1}
+k_{t-1}^T + lambda_t v_t k_t^T, under the same caching and aggregation.
+
 Inputs are arrays of shape [B, H, L, d] in any real dtype; they are widened
 exactly to float64 (bf16 and fp32 values are exactly representable).
 """
@@ -64,6 +68,11 @@ def _load():
             lib.mc_oracle_forward.restype = i
             lib.mc_oracle_bruteforce.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, dp, i]
             lib.mc_oracle_bruteforce.restype = i
+            lib.mc_oracle_forward_swla.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i,
+                                                   u8, ip, dp, dp, ip, dp, i]
+            lib.mc_oracle_forward_swla.restype = i
+            lib.mc_oracle_bruteforce_swla.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, i]
+            lib.mc_oracle_bruteforce_swla.restype = i
             _lib = lib
     return _lib
 
@@ -82,8 +91,16 @@ def num_segments(L: int, seg_len: int) -> int:
     return (L + seg_len - 1) // seg_len
 
 
+def _swla_args(swla, B, H, L):
+    alpha, beta, lam = (_as_f64(a) for a in swla)
+    for a in (alpha, beta, lam):
+        if a.shape != (B, H, L):
+            raise ValueError("alpha, beta, lam must be [B, H, L]")
+    return alpha, beta, lam
+
+
 def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
-            seg_mask=None, given_sel=None, nthreads: int = 0) -> dict:
+            seg_mask=None, given_sel=None, nthreads: int = 0, swla=None) -> dict:
     """Run the state-form oracle.
 
     Returns a dict with ``y`` [B,H,L,d] and ``states`` [B,H,N,d,d] (float64); for
@@ -119,14 +136,17 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
         sm = np.ascontiguousarray(np.asarray(seg_mask, dtype=np.uint8))
         if sm.shape != (N,):
             raise ValueError("seg_mask must have one entry per segment")
-    st = lib.mc_oracle_forward(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
-                               _ptr(v, ctypes.c_double), _ptr(u, ctypes.c_double),
-                               B * H, L, d, seg_len, mode, kk,
-                               _ptr(sm, ctypes.c_uint8), _ptr(gs, ctypes.c_int32),
-                               _ptr(y, ctypes.c_double), _ptr(states, ctypes.c_double),
-                               _ptr(sel, ctypes.c_int32) if sel is not None else None,
-                               _ptr(gap, ctypes.c_double) if gap is not None else None,
-                               nthreads)
+    common = [_ptr(sm, ctypes.c_uint8), _ptr(gs, ctypes.c_int32),
+              _ptr(y, ctypes.c_double), _ptr(states, ctypes.c_double),
+              _ptr(sel, ctypes.c_int32) if sel is not None else None,
+              _ptr(gap, ctypes.c_double) if gap is not None else None, nthreads]
+    qkvu = [_ptr(a, ctypes.c_double) for a in (q, k, v, u)]
+    if swla is None:
+        st = lib.mc_oracle_forward(*qkvu, B * H, L, d, seg_len, mode, kk, *common)
+    else:
+        abl = _swla_args(swla, B, H, L)
+        st = lib.mc_oracle_forward_swla(*qkvu, *[_ptr(a, ctypes.c_double) for a in abl],
+                                        B * H, L, d, seg_len, mode, kk, *common)
     if st != 0:
         raise RuntimeError(f"mc_oracle_forward failed with status {st}")
     out = {"y": y, "states": states}
@@ -136,16 +156,22 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
     return out
 
 
-def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0) -> np.ndarray:
+def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0,
+               swla=None) -> np.ndarray:
     """Token-level twin: y [B,H,L,d] without forming any memory matrix (O(L^2 d))."""
     lib = _load()
     q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
     B, H, L, d = q.shape
     y = np.zeros((B, H, L, d), np.float64)
-    st = lib.mc_oracle_bruteforce(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
-                                  _ptr(v, ctypes.c_double), _ptr(u, ctypes.c_double),
-                                  B * H, L, d, seg_len, mode, max(topk, 0),
-                                  _ptr(y, ctypes.c_double), nthreads)
+    qkvu = [_ptr(a, ctypes.c_double) for a in (q, k, v, u)]
+    if swla is None:
+        st = lib.mc_oracle_bruteforce(*qkvu, B * H, L, d, seg_len, mode, max(topk, 0),
+                                      _ptr(y, ctypes.c_double), nthreads)
+    else:
+        abl = _swla_args(swla, B, H, L)
+        st = lib.mc_oracle_bruteforce_swla(*qkvu, *[_ptr(a, ctypes.c_double) for a in abl],
+                                           B * H, L, d, seg_len, mode, max(topk, 0),
+                                           _ptr(y, ctypes.c_double), nthreads)
     if st != 0:
         raise RuntimeError(f"mc_oracle_bruteforce failed with status {st}")
     return y

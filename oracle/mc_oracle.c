@@ -42,8 +42,18 @@
  *   - SSC ranks on the scores rounded to fp32 (the precision the router is
  *     specified in), equal fp32 scores going to the lower segment index.
  *
+ * Sliding-window linear attention with c = 2 under memory caching (SWLA, the
+ * second memory family the pages cache) replaces the update rule by
+ *   M_t^(s) = alpha_t M_{t-1}^(s) + beta_t v_{t-1} k_{t-1}^T + lambda_t v_t k_t^T
+ *                                                                        [MC-ja §3.1, SWLA eq. 28]
+ * with per-token scalars alpha, beta, lambda; the read and the aggregation are
+ * unchanged ([MC-ja §3.1, eq. 29]; GRM and Soup coincide for this linear memory).
+ * Reading: the memory restarts at each segment, so at a segment's first token the
+ * beta term (which would reach back into the previous segment) is absent.
+ *
  * All arrays are dense, row-major, [BH][L][d] for q,k,v,u,y and [BH][N][d][d]
- * for the states, state[a][b] = sum v[a] k[b] (row = value dim, column = key dim).
+ * for the states, state[a][b] = sum v[a] k[b] (row = value dim, column = key dim);
+ * alpha, beta, lambda are [BH][L].
  */
 #include <math.h>
 #include <pthread.h>
@@ -69,7 +79,30 @@ typedef struct {
     double *states;
     int32_t *sel; /* optional [L][topk], rank order, -1 padded */
     double *gap;  /* optional [L] */
+    const double *alpha, *beta, *lam; /* SWLA scalars [L]; all NULL = plain linear memory */
 } head_job;
+
+/*
+ * One step of the segment memory at token t (segment start t0):
+ *   plain: M += v_t k_t^T                                       [MC-ja §3, eq. 4b]
+ *   SWLA:  M = alpha_t M + beta_t v_{t-1} k_{t-1}^T + lambda_t v_t k_t^T, no beta
+ *          term at t = t0                                       [MC-ja §3.1, eq. 28]
+ */
+static void memory_step(const head_job *J, double *M, int t, int t0)
+{
+    const int d = J->d;
+    const double *kt = J->k + (size_t)t * d, *vt = J->v + (size_t)t * d;
+    if (!J->alpha) {
+        for (int a = 0; a < d; ++a)
+            for (int b = 0; b < d; ++b) M[(size_t)a * d + b] += vt[a] * kt[b];
+        return;
+    }
+    const double al = J->alpha[t], be = t > t0 ? J->beta[t] : 0.0, la = J->lam[t];
+    const double *kp = t > t0 ? J->k + (size_t)(t - 1) * d : kt, *vp = t > t0 ? J->v + (size_t)(t - 1) * d : vt;
+    for (int a = 0; a < d; ++a)
+        for (int b = 0; b < d; ++b)
+            M[(size_t)a * d + b] = al * M[(size_t)a * d + b] + be * vp[a] * kp[b] + la * vt[a] * kt[b];
+}
 
 static double dot(const double *a, const double *b, int d)
 {
@@ -166,9 +199,8 @@ static int head_forward(const head_job *J)
         double *M = J->states + (size_t)n * dd;
         int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
         for (int t = t0; t < t1; ++t) {
-            const double *kt = J->k + (size_t)t * d, *vt = J->v + (size_t)t * d;
-            for (int a = 0; a < d; ++a)
-                for (int b = 0; b < d; ++b) M[(size_t)a * d + b] += vt[a] * kt[b];
+            const double *kt = J->k + (size_t)t * d;
+            memory_step(J, M, t, t0);
             for (int b = 0; b < d; ++b) kbar[(size_t)n * d + b] += kt[b];
         }
         for (int b = 0; b < d; ++b) kbar[(size_t)n * d + b] /= (double)(t1 - t0);
@@ -182,9 +214,8 @@ static int head_forward(const head_job *J)
         memset(ksum, 0, (size_t)d * sizeof(double));
         for (int t = t0; t < t1; ++t) {
             const double *qt = J->q + (size_t)t * d, *kt = J->k + (size_t)t * d;
-            const double *vt = J->v + (size_t)t * d, *ut = J->u + (size_t)t * d;
-            for (int a = 0; a < d; ++a)
-                for (int b = 0; b < d; ++b) Mon[(size_t)a * d + b] += vt[a] * kt[b];
+            const double *ut = J->u + (size_t)t * d;
+            memory_step(J, Mon, t, t0);
             for (int b = 0; b < d; ++b) ksum[b] += kt[b];
             if (!want_y) continue;
 
@@ -244,6 +275,21 @@ static int head_forward(const head_job *J)
     }
     free(kbar); free(Mon); free(Mstar); free(ksum); free(r); free(g); free(idx); free(taken);
     return OR_OK;
+}
+
+/*
+ * Weight of token j's outer product v_j k_j^T in a segment memory read at step t
+ * (j <= t, both in the same segment, which starts at t0): 1 for the plain update;
+ * for SWLA, unrolling eq. 28, lambda_j prod_{i=j+1..t} alpha_i plus (when j < t)
+ * beta_{j+1} prod_{i=j+2..t} alpha_i.
+ */
+static double token_weight(const head_job *J, int j, int t)
+{
+    if (!J->alpha) return 1.0;
+    double a_lam = J->lam[j], a_beta = j < t ? J->beta[j + 1] : 0.0;
+    for (int i = j + 1; i <= t; ++i) a_lam *= J->alpha[i];
+    for (int i = j + 2; i <= t; ++i) a_beta *= J->alpha[i];
+    return a_lam + a_beta;
 }
 
 /*
@@ -310,6 +356,9 @@ static int head_bruteforce(const head_job *J)
         for (int j = 0; j <= t; ++j) {
             double wj = w[j / C];
             if (wj == 0.0) continue;
+            /* a cached segment is read at its last token, the current one at t */
+            const int seg_end = (j / C) * C + C - 1 < L - 1 ? (j / C) * C + C - 1 : L - 1;
+            wj *= token_weight(J, j, j / C == s ? t : seg_end);
             double kq = dot(J->k + (size_t)j * d, qt, d);
             const double *vj = J->v + (size_t)j * d;
             for (int a = 0; a < d; ++a) yt[a] += wj * kq * vj[a];
@@ -343,6 +392,9 @@ static void *worker(void *arg)
         if (h >= P->BH) break;
         head_job J = P->base;
         J.q += h * Ld; J.k += h * Ld; J.v += h * Ld; J.u += h * Ld;
+        if (J.alpha) {
+            J.alpha += (size_t)h * L; J.beta += (size_t)h * L; J.lam += (size_t)h * L;
+        }
         J.y += h * Ld;
         if (J.states) J.states += h * Ndd;
         if (J.sel) J.sel += (size_t)h * L * J.topk;
@@ -408,7 +460,27 @@ int mc_oracle_forward(const double *q, const double *k, const double *v, const d
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
                         seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
-                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL};
+                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, NULL, NULL, NULL};
+    P.BH = BH;
+    P.brute = 0;
+    return run_pool(&P, nthreads);
+}
+
+/* The same forward with the SWLA (c = 2) update rule; alpha, beta, lam are [BH][L]. */
+int mc_oracle_forward_swla(const double *q, const double *k, const double *v, const double *u,
+                           const double *alpha, const double *beta, const double *lam,
+                           int BH, int L, int d, int C, int mode, int topk,
+                           const uint8_t *seg_mask, const int32_t *given_sel,
+                           double *y, double *states, int32_t *sel, double *gap, int nthreads)
+{
+    int st = check_args(BH, L, d, C, mode, topk);
+    if (st != OR_OK) return st;
+    if (!q || !k || !v || !u || !y || !states || !alpha || !beta || !lam) return OR_ERR_ARG;
+    pool_ctx P;
+    memset(&P, 0, sizeof(P));
+    P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
+                        seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
+                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, alpha, beta, lam};
     P.BH = BH;
     P.brute = 0;
     return run_pool(&P, nthreads);
@@ -424,7 +496,24 @@ int mc_oracle_bruteforce(const double *q, const double *k, const double *v, cons
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, y, NULL, NULL, NULL};
+                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL};
+    P.BH = BH;
+    P.brute = 1;
+    return run_pool(&P, nthreads);
+}
+
+/* Token-level twin of the SWLA forward (y only). */
+int mc_oracle_bruteforce_swla(const double *q, const double *k, const double *v, const double *u,
+                              const double *alpha, const double *beta, const double *lam,
+                              int BH, int L, int d, int C, int mode, int topk, double *y, int nthreads)
+{
+    int st = check_args(BH, L, d, C, mode, topk);
+    if (st != OR_OK) return st;
+    if (!q || !k || !v || !u || !y || !alpha || !beta || !lam) return OR_ERR_ARG;
+    pool_ctx P;
+    memset(&P, 0, sizeof(P));
+    P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
+                        NULL, NULL, y, NULL, NULL, NULL, alpha, beta, lam};
     P.BH = BH;
     P.brute = 1;
     return run_pool(&P, nthreads);

@@ -7,6 +7,10 @@ Pages cited:
   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
   [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
            (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
+The SWLA pins (sliding-window linear attention, c = 2, [MC-ja §3.1 eq. 28-29])
+reduce it to closed forms written here with numpy: a constant decay (a decayed
+causal linear attention), alpha = 0 (a two-token window), alpha = beta = lambda
+= 1 (each past token counted twice, once within its own segment's window).
 """
 import os
 import re
@@ -269,12 +273,96 @@ def test_seg_mask_and_given_selection():
 
 # ---------------------------------------------------------------- the pins have teeth
 
+# ---------------------------------------------------------------- SWLA (c = 2)
+
+def _swla_scalars(B, H, L, seed, lo=0.5):
+    rng = np.random.default_rng(seed)
+    return (rng.uniform(lo, 1.0, (B, H, L)), rng.uniform(0.0, 1.0, (B, H, L)), rng.uniform(0.0, 1.0, (B, H, L)))
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("C", [12, 5, 1])
+def test_swla_state_form_matches_token_level_twin(mode, topk, C):
+    """The recurrence of eq. 28 and its unrolled per-token weights agree."""
+    q, k, v, u = _inputs(1, 2, 36, 6, 41)
+    sw = _swla_scalars(1, 2, 36, 7)
+    ref = oracle.forward(q, k, v, u, C, mode, topk, swla=sw)["y"]
+    twin = oracle.bruteforce(q, k, v, u, C, mode, topk, swla=sw)
+    assert np.max(np.abs(ref - twin)) <= 1e-12 * max(1.0, np.max(np.abs(twin)))
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SSC, 1)])
+def test_swla_with_unit_decay_and_no_window_is_plain_mc(mode, topk):
+    """alpha = lambda = 1, beta = 0 is the plain update M += v k^T."""
+    q, k, v, u = _inputs(1, 2, 40, 8, 42)
+    one, zero = np.ones((1, 2, 40)), np.zeros((1, 2, 40))
+    a = oracle.forward(q, k, v, u, 10, mode, topk)
+    b = oracle.forward(q, k, v, u, 10, mode, topk, swla=(one, zero, one))
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["states"], b["states"])
+
+
+def test_swla_constant_decay_is_decayed_linear_attention():
+    """beta = 0, lambda = 1, alpha = a: y_t = sum_{j<=t} a^(t-j) v_j (k_j . q_t) (one segment)."""
+    q, k, v, u = _inputs(1, 1, 30, 5, 43)
+    L, a = 30, 0.83
+    t = np.arange(L)
+    decay = np.where(t[:, None] >= t[None, :], a ** (t[:, None] - t[None, :]).clip(min=0), 0.0)
+    want = np.einsum("tj,jd->td", np.einsum("td,jd->tj", q[0, 0], k[0, 0]) * decay, v[0, 0])
+    sw = (np.full((1, 1, L), a), np.zeros((1, 1, L)), np.ones((1, 1, L)))
+    got = oracle.forward(q, k, v, u, L, RESIDUAL, swla=sw)["y"][0, 0]
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_swla_zero_decay_is_a_two_token_window():
+    """alpha = 0: y_t = lambda_t v_t (k_t . q_t) + beta_t v_{t-1} (k_{t-1} . q_t) (one segment)."""
+    q, k, v, u = _inputs(1, 1, 25, 4, 44)
+    _, be, la = _swla_scalars(1, 1, 25, 8)
+    sw = (np.zeros((1, 1, 25)), be, la)
+    got = oracle.forward(q, k, v, u, 25, RESIDUAL, swla=sw)["y"][0, 0]
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    want = la[0, 0][:, None] * np.sum(K * Q, 1)[:, None] * V
+    want[1:] += be[0, 0, 1:][:, None] * np.sum(K[:-1] * Q[1:], 1)[:, None] * V[:-1]
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+@pytest.mark.parametrize("C", [7, 1, 30])
+def test_swla_window_does_not_cross_segments(C):
+    """alpha = beta = lambda = 1, Residual: token j counts twice for every later token of its
+    segment's window reach (j + 1 in the same segment), once otherwise."""
+    q, k, v, u = _inputs(1, 1, 30, 4, 45)
+    L = 30
+    t = np.arange(L)
+    twice = (t[:, None] > t[None, :]) & ((t[None, :] + 1) // C == t[None, :] // C)
+    w = np.where(t[:, None] >= t[None, :], 1.0, 0.0) + twice
+    want = np.einsum("tj,jd->td", np.einsum("td,jd->tj", q[0, 0], k[0, 0]) * w, v[0, 0])
+    one = np.ones((1, 1, L))
+    got = oracle.forward(q, k, v, u, C, RESIDUAL, swla=(one, one, one))["y"][0, 0]
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_swla_states_are_the_segments_last_memory():
+    """The cached state of a segment is its memory after the segment's last token: with
+    alpha = 0 that is beta_T v_{T-1} k_{T-1}^T + lambda_T v_T k_T^T."""
+    q, k, v, u = _inputs(1, 1, 24, 3, 46)
+    _, be, la = _swla_scalars(1, 1, 24, 9)
+    st = oracle.forward(q, k, v, u, 8, GRM, swla=(np.zeros((1, 1, 24)), be, la))["states"][0, 0]
+    K, V = k[0, 0], v[0, 0]
+    for n in range(3):
+        T = 8 * n + 7
+        want = be[0, 0, T] * np.outer(V[T - 1], K[T - 1]) + la[0, 0, T] * np.outer(V[T], K[T])
+        assert np.max(np.abs(st[n] - want)) <= 1e-13 * np.max(np.abs(want))
+
+
 _MUTATIONS = [
     # (description, regex pattern, replacement)
     ("state transposed", r"M\[\(size_t\)a \* d \+ b\] \+= vt\[a\] \* kt\[b\];",
      "M[(size_t)a * d + b] += vt[b] * kt[a];"),
-    ("online memory transposed", r"Mon\[\(size_t\)a \* d \+ b\] \+= vt\[a\] \* kt\[b\];",
-     "Mon[(size_t)a * d + b] += vt[b] * kt[a];"),
+    ("swla window uses the current token", r"be \* vp\[a\] \* kp\[b\]", "be * vt[a] * kt[b]"),
+    ("swla decays the new terms too", r"M\[\(size_t\)a \* d \+ b\] = al \* M\[\(size_t\)a \* d \+ b\] \+ be",
+     "M[(size_t)a * d + b] = al * (M[(size_t)a * d + b]) * 1.0 + al * be"),
+    ("swla window crosses segments", r"const double al = J->alpha\[t\], be = t > t0 \? J->beta\[t\] : 0\.0",
+     "const double al = J->alpha[t], be = t > 0 ? J->beta[t] : 0.0"),
     ("pool not averaged", r"kbar\[\(size_t\)n \* d \+ b\] /= \(double\)\(t1 - t0\);", ";"),
     ("online pool over a wrong count", r"r\[s\] = dot\(ut, ksum, d\) / cnt;",
      "r[s] = dot(ut, ksum, d) / (cnt + 1.0);"),
@@ -301,6 +389,10 @@ def _run_pins_against(libpath):
         lib.mc_oracle_forward.restype = ctypes.c_int
         lib.mc_oracle_bruteforce.argtypes = saved.mc_oracle_bruteforce.argtypes
         lib.mc_oracle_bruteforce.restype = ctypes.c_int
+        lib.mc_oracle_forward_swla.argtypes = saved.mc_oracle_forward_swla.argtypes
+        lib.mc_oracle_forward_swla.restype = ctypes.c_int
+        lib.mc_oracle_bruteforce_swla.argtypes = saved.mc_oracle_bruteforce_swla.argtypes
+        lib.mc_oracle_bruteforce_swla.restype = ctypes.c_int
         oracle._lib = lib
         pins = [
             test_hand_worked_example,
@@ -312,6 +404,9 @@ def _run_pins_against(libpath):
             lambda: test_ssc_ties_go_to_lower_index(),
             lambda: test_causality(GRM, 0),
             lambda: test_single_segment_is_plain_recurrent_model(GRM, 0),
+            test_swla_constant_decay_is_decayed_linear_attention,
+            test_swla_zero_decay_is_a_two_token_window,
+            lambda: test_swla_window_does_not_cross_segments(7),
         ]
         failed = 0
         for p in pins:
