@@ -219,19 +219,20 @@ def oracle_sample(w, budget_s: float, steps_hint: int = 1):
     bh = min(cores, w.B * w.H)
     q, k, v, u = mc_inputs.make_inputs(1, bh, w.L, w.d, w.seed, w.dtype)
     q, k, v, u = (t.float().numpy() for t in (q, k, v, u))
+    sw = tuple(t.numpy() for t in mc_inputs.make_swla_scalars(1, bh, w.L, w.seed)) if w.swla else None
     picks = [w.N // 2] if w.N < 4 else [int((i + 0.5) * w.N / 4) for i in range(4)]
     # probe with one segment, then size the sample to the budget
     mask = np.zeros(w.N, bool)
     mask[picks[0]] = True
     t0 = time.perf_counter()
-    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores)
+    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores, swla=sw)
     t_one = time.perf_counter() - t0
     nseg = max(1, min(len(picks), int(budget_s / max(t_one, 1e-3))))
     chosen = picks[:nseg] if nseg < len(picks) else picks
     mask = np.zeros(w.N, bool)
     mask[chosen] = True
     t0 = time.perf_counter()
-    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores)
+    oracle.forward(q, k, v, u, w.seg_len, w.mode, w.topk, seg_mask=mask, nthreads=cores, swla=sw)
     dt = time.perf_counter() - t0
     ntok = sum(min(w.L, (n + 1) * w.seg_len) - n * w.seg_len for n in chosen)
     # tokens/s in the metric's unit: a token is one sequence position across all H heads
@@ -265,9 +266,13 @@ def run_ours(args, w, wname="long-grm"):
     y = torch.empty_like(q)
     states = torch.empty((w.B, w.H, w.N, w.d, w.d), dtype=torch.float32, device=dev)
     fwd = mcl.mc_forward if w.dtype == "bf16" else mcl.mc_forward_f32
+    sw = mc_inputs.workload_swla_scalars(w, device=dev) if w.swla else None
 
     def step():
-        fwd(q, k, v, u, w.seg_len, w.mode, w.topk, y=y, states=states)
+        if sw is not None:
+            mcl.mc_forward_swla(q, k, v, u, *sw, w.seg_len, w.mode, w.topk, y=y, states=states)
+        else:
+            fwd(q, k, v, u, w.seg_len, w.mode, w.topk, y=y, states=states)
 
     # warm-up (at least W steps and ~1 s so the clocks settle under load)
     sampler = ClockSampler(dev.index).start()
@@ -344,7 +349,8 @@ def run_ours(args, w, wname="long-grm"):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": nwarm, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_path,
-        "data": "synthetic (seeded numpy normals: q,k unit rows, v ~ N(0,1), u ~ N(0,1)/sqrt(d))",
+        "data": "synthetic (seeded numpy normals: q,k unit rows, v ~ N(0,1), u ~ N(0,1)/sqrt(d)"
+                + ("; SWLA alpha = 1 - 0.1 sigmoid(z), beta, lambda = sigmoid(z))" if w.swla else ")"),
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
                    "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype,
                    "l2": f"inputs {4 * w.B * w.H * w.L * w.d * (2 if w.dtype == 'bf16' else 4) / 2**30:.2f} GiB "
@@ -359,8 +365,8 @@ def run_ours(args, w, wname="long-grm"):
         "clocks": clocks,
     }
 
-    # end to end through the host-buffer entry point
-    if not args.no_e2e:
+    # end to end through the host-buffer entry point (plain update only)
+    if not args.no_e2e and not w.swla:
         qh, kh, vh, uh = (t.cpu().pin_memory() for t in (q, k, v, u))
         yh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
         mcl.mc_forward_host(qh, kh, vh, uh, w.seg_len, w.mode, w.topk, y=yh)
@@ -417,6 +423,7 @@ def run_reference(args, w):
 
 
 WORKLOADS = {"long-grm": mc_inputs.LONG_GRM, "grm-d64": mc_inputs.GRM_D64, "ssc": mc_inputs.SSC_D128,
+             "swla-grm": mc_inputs.SWLA_LONG,
              "tiny": mc_inputs.TINY, **{f"sweep-c{w.seg_len}": w for w in mc_inputs.SWEEP}}
 
 

@@ -99,6 +99,26 @@ int mc_forward_f32(const float *q, const float *k, const float *v, const float *
                    float *y, float *states, mc_stream_t stream);
 
 /*
+ * mc_forward_swla -- memory caching over sliding-window linear attention with a
+ * window of c = 2 ([MC-ja §3.1 eq. 28-29]): inside a segment the memory follows
+ *     M_t = alpha_t M_{t-1} + beta_t v_{t-1} k_{t-1}^T + lambda_t v_t k_t^T
+ * from an empty memory at the segment's first token (whose beta term, which would
+ * reach into the previous segment, is absent); the cached states, gates and
+ * aggregation are those of mc_forward.  GRM and Soup coincide for this linear
+ * memory.
+ *   alpha, beta, lam : fp32 [B][H][L], device, 16-byte aligned; alpha is a decay
+ *                      in (0, 1] (values are floored at 1e-30 before their log).
+ *   Other arguments as mc_forward (bf16).
+ *   Runs on the tensor-core path only: d in {64, 128}, seg_len a multiple of 128,
+ *   L a multiple of seg_len, N <= 64, SSC with topk <= 16 (or >= N-1); other
+ *   shapes return MC_ERR_SHAPE.  A NULL scalar array returns MC_ERR_NULL.
+ */
+int mc_forward_swla(const void *q, const void *k, const void *v, const void *u,
+                    const float *alpha, const float *beta, const float *lam,
+                    int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                    void *y, float *states, mc_stream_t stream);
+
+/*
  * mc_ssc_select -- the SSC router alone ([MC-sum §3.4]), for inspection and tests.
  *   k, u     : [B][H][L][d], bf16 if is_bf16 != 0 else fp32, device.
  *   idx      : int32 [B][H][L][topk], written: for token t of segment s, the

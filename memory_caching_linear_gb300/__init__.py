@@ -24,7 +24,7 @@ MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
 MC_ERR_SCRATCH = -10
 
-EXPORTED = ("mc_forward", "mc_forward_f32", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
             "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
             "mc_status_string")
 
@@ -52,6 +52,8 @@ def load_library():
     lib.mc_forward.restype = i
     lib.mc_forward_f32.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
     lib.mc_forward_f32.restype = i
+    lib.mc_forward_swla.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
+    lib.mc_forward_swla.restype = i
     lib.mc_ssc_select.argtypes = [vp, vp, i, i, i, i, i, i, vp, i, vp]
     lib.mc_ssc_select.restype = i
     lib.mc_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, i, vp]
@@ -101,7 +103,7 @@ def _check(t, name, dtype, shape=None, device=None):
         raise ValueError(f"{name} must be on {device}")
 
 
-def _forward(fn_name, q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream):
+def _forward(fn_name, q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream, swla=None):
     lib = load_library()
     dtype = q.dtype
     if q.dim() != 4:
@@ -122,8 +124,12 @@ def _forward(fn_name, q, k, v, u, seg_len, agg_mode, topk, y, states, want_state
         states = torch.empty((B, H, N, d, d), dtype=torch.float32, device=dev)
     if states is not None:
         _check(states, "states", torch.float32, (B, H, N, d, d), dev)
-    st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None,
-                               B, H, L, d, int(seg_len), int(agg_mode), int(topk), y.data_ptr(),
+    head = [q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None]
+    if swla is not None:
+        for t, n in zip(swla, ("alpha", "beta", "lam")):
+            _check(t, n, torch.float32, (B, H, L), dev)
+        head += [t.data_ptr() for t in swla]
+    st = getattr(lib, fn_name)(*head, B, H, L, d, int(seg_len), int(agg_mode), int(topk), y.data_ptr(),
                                states.data_ptr() if states is not None else None, _stream_handle(stream, dev))
     if st != MC_OK:
         raise MCError(st, fn_name)
@@ -135,6 +141,14 @@ def mc_forward(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None
     """bf16 MC forward (``mc_forward`` in mc.h).  Returns (y, states); states is None
     when ``want_states`` is False and none was given."""
     return _forward("mc_forward", q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream)
+
+
+def mc_forward_swla(q, k, v, u, alpha, beta, lam, seg_len: int, agg_mode: int, topk: int = 0, *, y=None,
+                    states=None, want_states: bool = True, stream=None):
+    """bf16 MC forward over sliding-window linear attention, c = 2 (``mc_forward_swla`` in
+    mc.h); alpha, beta, lam are fp32 [B, H, L] on the device.  Returns (y, states)."""
+    return _forward("mc_forward_swla", q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream,
+                    swla=(alpha, beta, lam))
 
 
 def mc_forward_f32(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None, states=None,

@@ -69,6 +69,7 @@ struct TcArgs {
                           // (g_{2p}, g_{2p+1}); g_i for i < n, g_n in the high half of pair 31
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
+    const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
     int BH, L, C, N, CPS;
     int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
     int num_tiles;
@@ -84,6 +85,54 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// SWLA (sliding-window linear attention, c = 2, [MC-ja §3.1 eq. 28]) within one
+// 128-token chunk whose first token is t_c:
+//   M_t = A(t_c, t) S^_c + sum_{j = t_c..t} c_{t,j} v_j k_j^T,
+//   c_{t,j} = lambda_j A(j, t) + [j < t] beta_{j+1} A(j+1, t),  A(a, t) = prod_{i=a+1..t} alpha_i,
+//   S^_c = alpha_{t_c} M_{t_c - 1} + beta_{t_c} v_{t_c - 1} k_{t_c - 1}^T   (0 at a segment's start).
+// A(a, t) = exp(ell_t - ell_a) with ell the running sum of log alpha over the chunk
+// (ell = 0 at t_c).  Every warp holds the whole chunk, lane l tokens 4l .. 4l + 3.
+struct ChunkDecay {
+    float ell[4], lam[4], bet[4];
+};
+
+__device__ __forceinline__ ChunkDecay load_chunk_decay(const float *alpha, const float *beta, const float *lam,
+                                                        size_t tok0, int lane)
+{
+    ChunkDecay cd;
+    const float4 al = *reinterpret_cast<const float4 *>(alpha + tok0 + 4 * lane);
+    const float4 be = *reinterpret_cast<const float4 *>(beta + tok0 + 4 * lane);
+    const float4 la = *reinterpret_cast<const float4 *>(lam + tok0 + 4 * lane);
+    float x0 = lane == 0 ? 0.f : logf(fmaxf(al.x, 1e-30f));  // the chunk's first token carries no decay
+    float x1 = logf(fmaxf(al.y, 1e-30f)), x2 = logf(fmaxf(al.z, 1e-30f)), x3 = logf(fmaxf(al.w, 1e-30f));
+    x1 += x0;
+    x2 += x1;
+    x3 += x2;
+    float tot = x3;  // inclusive scan of the lanes' sums
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, tot, o);
+        if (lane >= o) tot += y;
+    }
+    const float ex = tot - x3;
+    cd.ell[0] = x0 + ex;
+    cd.ell[1] = x1 + ex;
+    cd.ell[2] = x2 + ex;
+    cd.ell[3] = x3 + ex;
+    cd.lam[0] = la.x; cd.lam[1] = la.y; cd.lam[2] = la.z; cd.lam[3] = la.w;
+    cd.bet[0] = be.x; cd.bet[1] = be.y; cd.bet[2] = be.z; cd.bet[3] = be.w;
+    return cd;
+}
+
+// Value of chunk token j (0..127) from the lane that holds it; every lane of the warp calls it.
+__device__ __forceinline__ float chunk_pick(const float (&v)[4], int j)
+{
+    const int src = j >> 2, e = j & 3;
+    const float v0 = __shfl_sync(0xffffffffu, v[0], src), v1 = __shfl_sync(0xffffffffu, v[1], src);
+    const float v2 = __shfl_sync(0xffffffffu, v[2], src), v3 = __shfl_sync(0xffffffffu, v[3], src);
+    return e == 0 ? v0 : e == 1 ? v1 : e == 2 ? v2 : v3;
+}
+
 // K-major SW128 descriptor start for the 16-wide K step kk of a tile with `rows` rows.
 __device__ __forceinline__ uint32_t kmaj_off(int kk, uint32_t rows) { return (kk >> 2) * rows * 128u + (kk & 3) * 32u; }
 
@@ -95,7 +144,7 @@ constexpr uint32_t kT1Stage = 3 * kTile;      // K, V, U tiles of one chunk
 constexpr uint32_t kT1Stage2 = 4096;           // per worker warp: 32 rows x 128 bytes of a store in flight
 constexpr size_t kT1Smem = 2 * kT1Stage + 4 * kT1Stage2 + 1024;
 
-template <bool GATED>
+template <bool GATED, bool DECAY>
 __global__ void __launch_bounds__(kT1Threads, 1)
     seg_state_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                  const __grid_constant__ CUtensorMap mU, TcArgs a)
@@ -103,6 +152,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t full[2], empty[2], r_full[2], r_empty[2], z_full[2], z_empty[2];
+    __shared__ uint64_t v_scaled;  // SWLA: the workers have weighted the chunk's value rows
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ __align__(16) float ksum_s[kD];
@@ -132,6 +182,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             mbar_init(&z_full[s], 1);
             mbar_init(&z_empty[s], 128);
         }
+        mbar_init(&v_scaled, 128);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -183,8 +234,9 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                                make_desc_sw128(kb + kmaj_off(kk, 128), 0, 1024), idR, kk > 0);
                     mma_commit(&r_full[b]);
                 }
-                // Z = V^T K, the chunk's own state (fresh accumulator)
+                // Z = V^T K, the chunk's own state (fresh accumulator); SWLA: V^T diag(w) K
                 if (!mbar_wait(&z_empty[b], (r & 1) ^ 1, &abort_flag)) break;
+                if (DECAY && !mbar_wait(&v_scaled, gch & 1, &abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
@@ -219,6 +271,44 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             }
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
             const uint8_t *st = sm + s * kT1Stage;
+            // SWLA: the chunk's state is S_{c+1} = zdecay * S^_c + V^T diag(w) K, where w_j is
+            // token j's weight at the chunk's end, carried one step on (alpha', beta' of the
+            // next token) when that token is in the same segment -- so S is S^_{c+1}.
+            float zdecay = 1.f;
+            if (DECAY) {
+                const size_t tok0 = (size_t)row0 + (size_t)c * kCT;
+                const ChunkDecay cd = load_chunk_decay(a.alpha, a.beta, a.lam, tok0, lane);
+                const int jt = (int)row, jn = jt < kCT - 1 ? jt + 1 : jt;
+                const float ell_end = __shfl_sync(0xffffffffu, cd.ell[3], 31);
+                const float ell_j = chunk_pick(cd.ell, jt), lam_j = chunk_pick(cd.lam, jt);
+                const float ell_n = chunk_pick(cd.ell, jn), bet_n = chunk_pick(cd.bet, jn);
+                float a_next = 1.f, b_next = 0.f;
+                if (c + 1 < nch) {
+                    a_next = a.alpha[tok0 + kCT];
+                    b_next = a.beta[tok0 + kCT];
+                }
+                float w = lam_j * __expf(ell_end - ell_j);
+                if (jt < kCT - 1) w += bet_n * __expf(ell_end - ell_n);
+                w = a_next * w + (jt == kCT - 1 ? b_next : 0.f);
+                zdecay = a_next * __expf(ell_end);
+                if (ok) {  // value row of token jt, in place (the tile is MN-major, 128-byte swizzled)
+                    uint8_t *vt = const_cast<uint8_t *>(st) + kTile;
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        uint4 *pv = reinterpret_cast<uint4 *>(vt + sw128_offset(jt, 8 * cc, 128));
+                        uint4 x = *pv;
+                        uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xw[e]));
+                            xw[e] = pack_bf16x2(w * f.x, w * f.y);
+                        }
+                        *pv = x;
+                    }
+                    fence_async_smem();
+                }
+                mbar_arrive(&v_scaled);
+            }
             if (GATED && ok) {
                 float d4[4] = {0.f, 0.f, 0.f, 0.f};  // <u_t, keys of the segment before this chunk>
 #pragma unroll
@@ -298,7 +388,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     tmem_ld16(tZ0 + b * 128 + lane_base + 16 * j16, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) S[16 * j16 + i] += __uint_as_float(v[i]);
+                    for (int i = 0; i < 16; ++i) S[16 * j16 + i] = fmaf(zdecay, S[16 * j16 + i], __uint_as_float(v[i]));
                 }
                 tc_fence_before();
                 mbar_arrive(&z_empty[b]);
@@ -618,7 +708,8 @@ constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
 constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
 constexpr int kRing = 6;           // operand panels in flight per CTA
 constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
-constexpr size_t kT2Smem = kRing * kPanel + 1024;  // two CTAs fit in an SM's 228 KB
+constexpr uint32_t kT2Decay = 4 * 3 * kCT * 4;   // SWLA: per worker warp, ell / lambda / beta_next of a chunk
+constexpr size_t kT2Smem = kRing * kPanel + kT2Decay + 1024;  // two CTAs fit in an SM's 228 KB
 
 struct TileInfo {
     int n, c, bh;
@@ -666,7 +757,7 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 // release those panels once G is done), read the gate rows in the tile-transposed
 // layout (coalesced), and write y from a quad-transposed register layout.  Two CTAs run on each SM, so while one waits on its G -> P step or its
 // drain the other keeps the tensor pipe busy.
-template <bool GATED>
+template <bool GATED, bool DECAY>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, TcArgs a)
@@ -869,11 +960,26 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             ++ac;
         };
         if (my_tiles > 0) load_gates(0);
+        float *dsm = reinterpret_cast<float *>(sm + kRing * kPanel) + q4 * 3 * kCT;  // SWLA: ell | lambda | beta_{j+1}
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
             const int items = tile_items<GATED>(t);
             const float gn = GATED ? __bfloat162float(__high2bfloat16(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31])))
                                    : 1.f;
+            float ellt = 0.f;  // SWLA: log of A(t_c, t) for this token row
+            if (DECAY) {
+                const size_t tok0 = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT;
+                const ChunkDecay cd = load_chunk_decay(a.alpha, a.beta, a.lam, tok0, lane);
+                const float b_up = __shfl_down_sync(0xffffffffu, cd.bet[0], 1);  // beta of token 4 (lane + 1)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    dsm[4 * lane + e] = cd.ell[e];
+                    dsm[kCT + 4 * lane + e] = cd.lam[e];
+                    dsm[2 * kCT + 4 * lane + e] = e < 3 ? cd.bet[e + 1] : (lane < 31 ? b_up : 0.f);
+                }
+                __syncwarp();
+                ellt = dsm[row];
+            }
             // the token's query row from the Q panels (SWIZZLE_128B: 16-byte chunk c of
             // row r sits at chunk c ^ (r % 8)), read while G runs
             uint32_t qp[64];
@@ -909,11 +1015,30 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     uint32_t x[32], o[16];
                     tmem_ld32(tD + lane_base + 32 * h, x);
                     tmem_wait_ld();
+                    if (!DECAY) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t c0 = 32 * h + 2 * i;
-                        o[i] = pack_bf16x2(c0 <= row ? gn * __uint_as_float(x[2 * i]) : 0.f,
-                                           c0 + 1 <= row ? gn * __uint_as_float(x[2 * i + 1]) : 0.f);
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t c0 = 32 * h + 2 * i;
+                            o[i] = pack_bf16x2(c0 <= row ? gn * __uint_as_float(x[2 * i]) : 0.f,
+                                               c0 + 1 <= row ? gn * __uint_as_float(x[2 * i + 1]) : 0.f);
+                        }
+                    } else if (32 * h > 32 * q4 + 31) {  // the whole block is above every row of the warp
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = 0u;
+                    } else {
+                        // P_tj = g_n c_{t,j} G_tj, c_{t,j} = lambda_j A(j,t) + [j<t] beta_{j+1} A(j+1,t)
+                        auto coef = [&](uint32_t cj) -> float {
+                            if (cj > row) return 0.f;
+                            float cf = dsm[kCT + cj] * __expf(ellt - dsm[cj]);
+                            if (cj < row) cf += dsm[2 * kCT + cj] * __expf(ellt - dsm[cj + 1]);
+                            return cf;
+                        };
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t c0 = 32 * h + 2 * i;
+                            o[i] = pack_bf16x2(gn * coef(c0) * __uint_as_float(x[2 * i]),
+                                               gn * coef(c0 + 1) * __uint_as_float(x[2 * i + 1]));
+                        }
                     }
                     tmem_st16(ta + 16 * h, o);
                 }
@@ -924,10 +1049,13 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
 #pragma unroll 1
             for (int k = 0; k < items; ++k) {
                 __nv_bfloat162 gam2 = __float2bfloat162_rn(1.f);
+                const bool prefix = t.c > 0 && k == 0;  // item 0 of a chunk c > 0 is its prefix state (gate g_n)
                 if (GATED) {
-                    const int i = t.c > 0 ? k - 1 : k;  // item 0 of a chunk c > 0 is its prefix state (gate g_n)
+                    const int i = t.c > 0 ? k - 1 : k;
                     gam2 = __bfloat162bfloat162(i < 0 ? gl[63] : gl[i]);
                 }
+                if (DECAY && prefix) gam2 = __float2bfloat162_rn(gn * __expf(ellt));  // A(t_c, t) S^_c q_t
+                const bool scale = GATED || (DECAY && prefix);
                 if (!(ok = claim())) break;
                 const uint32_t ta = tA0 + (ac % 2) * 64 + lane_base;
 #pragma unroll
@@ -935,7 +1063,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     uint32_t r[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        if (GATED) {
+                        if (scale) {
                             __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&qp[32 * m + i]);
                             __nv_bfloat162 pr = __hmul2(x, gam2);
                             r[i] = *reinterpret_cast<uint32_t *>(&pr);
@@ -1138,8 +1266,13 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     }
 
     profile_call_start(s);
+    const bool decay = fa.alpha != nullptr;
+    a.alpha = fa.alpha;
+    a.beta = fa.beta;
+    a.lam = fa.lam;
     {
-        auto k1 = gated ? seg_state_tc<true> : seg_state_tc<false>;
+        auto k1 = gated ? (decay ? seg_state_tc<true, true> : seg_state_tc<true, false>)
+                        : (decay ? seg_state_tc<false, true> : seg_state_tc<false, false>);
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT1Smem);
         if (e != cudaSuccess) return e;
         const int nseg = (int)(BH * N);
@@ -1163,7 +1296,8 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         profile_after_kernel(s, "gates_tc");
     }
     {
-        auto k2 = gated ? readout_tc<true> : readout_tc<false>;
+        auto k2 = gated ? (decay ? readout_tc<true, true> : readout_tc<true, false>)
+                        : (decay ? readout_tc<false, true> : readout_tc<false, false>);
         e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);
         if (e != cudaSuccess) return e;
         const int slots = kT2CtasPerSm * g_num_sms;

@@ -131,15 +131,18 @@ ScratchPlan plan_scratch(const Problem &p, bool need_states)
 }
 
 int forward_common(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
-                   int seg_len, int agg_mode, int topk, void *y, float *states, bool bf16, cudaStream_t stream)
+                   int seg_len, int agg_mode, int topk, void *y, float *states, bool bf16, cudaStream_t stream,
+                   const float *alpha = nullptr, const float *beta = nullptr, const float *lam = nullptr,
+                   bool swla = false)
 {
     int st = check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
     if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
     if (!q || !k || !v || !y) return MC_ERR_NULL;
     if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (swla && (!alpha || !beta || !lam)) return MC_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y) || (u && !aligned16(u)) ||
-        (states && !aligned16(states)))
+        (states && !aligned16(states)) || (swla && (!aligned16(alpha) || !aligned16(beta) || !aligned16(lam))))
         return MC_ERR_ALIGN;
     Problem p{};
     p.B = B; p.H = H; p.L = L; p.d = d; p.C = seg_len;
@@ -154,6 +157,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         if (topk >= p.N - 1) p.mode = MC_GRM;
         else if (topk > kMaxTopk) return MC_ERR_TOPK;
     }
+    if (swla && !tc_supported(p)) return MC_ERR_SHAPE;  // the SWLA update runs on the tensor-core path only
     st = check_device();
     if (st != MC_OK) return st;
 
@@ -169,6 +173,9 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         a.u = p.mode == MC_RESIDUAL ? nullptr : u;
         a.y = y;
         a.states = states ? states : static_cast<float *>(scratch);
+        a.alpha = swla ? alpha : nullptr;
+        a.beta = swla ? beta : nullptr;
+        a.lam = swla ? lam : nullptr;
         a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
         cudaError_t e = launch_forward_tc(p, a, static_cast<char *>(scratch) + b_states, stream);
         cudaError_t ef = cudaFreeAsync(scratch, stream);
@@ -228,6 +235,14 @@ int mc_forward_f32(const float *q, const float *k, const float *v, const float *
 {
     return mc::forward_common(q, k, v, u, B, H, L, d, seg_len, agg_mode, topk, y, states, false,
                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mc_forward_swla(const void *q, const void *k, const void *v, const void *u, const float *alpha,
+                    const float *beta, const float *lam, int B, int H, int L, int d, int seg_len, int agg_mode,
+                    int topk, void *y, float *states, mc_stream_t stream)
+{
+    return mc::forward_common(q, k, v, u, B, H, L, d, seg_len, agg_mode, topk, y, states, true,
+                              reinterpret_cast<cudaStream_t>(stream), alpha, beta, lam, true);
 }
 
 int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int seg_len, int topk, int32_t *idx,

@@ -37,6 +37,7 @@ struct FwdArgs {
     float *r_on;                // [BH][L]      scratch
     float *kbar;                // [BH][N][d]   scratch
     int32_t *sel_out;           // [BH][L][topk] (ssc_select only)
+    const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L]; all null = plain update
     int BH, L, C, N, mode, topk;
 };
 

@@ -15,7 +15,8 @@ import torch
 
 import memory_caching_linear_gb300 as mcl
 import oracle
-from mc_inputs import GRM, GRM_D64, LONG_GRM, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, TINY, make_inputs, \
+from mc_inputs import GRM, GRM_D64, LONG_GRM, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, SWLA_LONG, TINY, make_inputs, \
+    make_swla_scalars, workload_swla_scalars, \
     workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -45,7 +46,7 @@ def run_gpu(q, k, v, u, C, mode, topk=0):
     return y.float().cpu().numpy(), st.cpu().numpy()
 
 
-def check_ssc_selection(q, k, v, u, C, topk, ref, tol):
+def check_ssc_selection(q, k, v, u, C, topk, ref, tol, swla=None):
     """Compare the GPU router with the oracle's; return the oracle y on the GPU's selection."""
     dev = torch.device("cuda")
     sel = mcl.mc_ssc_select(k.to(dev), u.to(dev), C, topk).cpu().numpy()
@@ -65,7 +66,7 @@ def check_ssc_selection(q, k, v, u, C, topk, ref, tol):
             theirs = [i for i in osel[b, h, t] if i >= 0]
             assert len(mine) == len(theirs)
             assert min(r[mine]) >= min(r[theirs]) - GAP
-        ref = oracle.forward(q, k, v, u, C, SSC, topk, given_sel=sel)
+        ref = oracle.forward(q, k, v, u, C, SSC, topk, given_sel=sel, swla=swla)
     return ref["y"]
 
 
@@ -189,6 +190,88 @@ def test_host_entry_point_head_groups(mode, topk):
     torch.cuda.synchronize()
     assert torch.equal(y_host, y_dev.cpu())
     assert torch.equal(st_host, st_dev.cpu())
+
+
+# ---------------------------------------------------------------- SWLA (c = 2)
+
+SWLA_CASES = [
+    ("swla-C128-N8", 1, 2, 1024, 128, 128),
+    ("swla-C256-N4-d64", 2, 1, 1024, 64, 256),
+    ("swla-C1024-N2", 1, 1, 2048, 128, 1024),
+]
+
+
+def run_gpu_swla(q, k, v, u, sw, C, mode, topk=0):
+    dev = torch.device("cuda")
+    y, st = mcl.mc_forward_swla(q.to(dev), k.to(dev), v.to(dev), u.to(dev), *(t.to(dev) for t in sw), C, mode, topk)
+    assert mcl.mc_check_device() == mcl.MC_OK
+    return y.float().cpu().numpy(), st.cpu().numpy()
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("name,B,H,L,d,C", SWLA_CASES, ids=[c[0] for c in SWLA_CASES])
+def test_parity_swla(name, B, H, L, d, C, mode, topk):
+    """Memory caching over SWLA (c = 2) against the oracle's recurrence, element by element."""
+    seed = zlib.crc32(name.encode()) % 1000
+    q, k, v, u = make_inputs(B, H, L, d, seed, "bf16")
+    sw = make_swla_scalars(B, H, L, seed)
+    ref = oracle.forward(q, k, v, u, C, mode, topk, swla=sw)
+    y, st = run_gpu_swla(q, k, v, u, sw, C, mode, topk)
+    yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL["bf16"], swla=sw) if mode == SSC else ref["y"]
+    assert rel_err(y, yref) <= TOL["bf16"], (name, mode, rel_err(y, yref))
+    assert rel_err(st, ref["states"]) <= TOL["bf16"], (name, mode, rel_err(st, ref["states"]))
+
+
+@pytest.mark.parametrize("alpha", [0.05, 0.6])
+def test_parity_swla_strong_decay(alpha):
+    """A decay far below the workload's: the chunk's decay products span many orders of magnitude."""
+    B, H, L, d, C = 1, 2, 1024, 128, 256
+    q, k, v, u = make_inputs(B, H, L, d, 77, "bf16")
+    _, be, la = make_swla_scalars(B, H, L, 77)
+    sw = (torch.full((B, H, L), alpha), be, la)
+    ref = oracle.forward(q, k, v, u, C, GRM, swla=sw)
+    y, st = run_gpu_swla(q, k, v, u, sw, C, GRM)
+    assert rel_err(y, ref["y"]) <= TOL["bf16"]
+    assert rel_err(st, ref["states"]) <= TOL["bf16"]
+
+
+def test_swla_without_decay_or_window_matches_plain_forward():
+    """alpha = lambda = 1, beta = 0 turns the SWLA kernels into the plain ones."""
+    B, H, L, d, C = 1, 2, 1024, 128, 256
+    q, k, v, u = (t.cuda() for t in make_inputs(B, H, L, d, 78, "bf16"))
+    one, zero = torch.ones(B, H, L, device="cuda"), torch.zeros(B, H, L, device="cuda")
+    y1, s1 = mcl.mc_forward(q, k, v, u, C, GRM)
+    y2, s2 = mcl.mc_forward_swla(q, k, v, u, one, zero, one, C, GRM)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2)
+    assert rel_err(y2.float().cpu().numpy(), y1.float().cpu().numpy()) <= 1e-3
+
+
+def test_swla_rejects_unsupported_shapes():
+    x = torch.zeros(1, 1, 256, 32, dtype=torch.bfloat16, device="cuda")
+    s = torch.ones(1, 1, 256, device="cuda")
+    with pytest.raises(mcl.MCError) as e:
+        mcl.mc_forward_swla(x, x, x, x, s, s, s, 128, GRM)  # d = 32 has no tensor-core path
+    assert e.value.status == mcl.MC_ERR_SHAPE
+
+
+@pytest.mark.slow
+def test_full_size_swla():
+    w = SWLA_LONG
+    q, k, v, u = workload_inputs(w)
+    sw = workload_swla_scalars(w)
+    y, st = run_gpu_swla(q, k, v, u, sw, w.seg_len, w.mode)
+    segs = [0, 31, 63]
+    mask = np.zeros(w.N, bool)
+    mask[segs] = True
+    for (b, h) in [(0, 0), (0, 11)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.forward(*(t[sl].contiguous() for t in (q, k, v, u)), w.seg_len, w.mode, seg_mask=mask,
+                             swla=tuple(t[sl].contiguous() for t in sw))
+        assert rel_err(st[sl], ref["states"]) <= TOL["bf16"]
+        for n in segs:
+            ts = slice(n * w.seg_len, (n + 1) * w.seg_len)
+            assert rel_err(y[sl][..., ts, :], ref["y"][..., ts, :]) <= TOL["bf16"], (b, h, n)
 
 
 def test_bad_arguments_raise():
