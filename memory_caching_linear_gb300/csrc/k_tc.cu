@@ -140,9 +140,15 @@ __device__ __forceinline__ uint32_t kmaj_off(int kk, uint32_t rows) { return (kk
 // seg_state_tc
 // ============================================================================
 constexpr int kT1Threads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 workers
-constexpr uint32_t kT1Stage = 3 * kTile;      // K, V, U tiles of one chunk
 constexpr uint32_t kT1Stage2 = 4096;           // per worker warp: 32 rows x 128 bytes of a store in flight
-constexpr size_t kT1Smem = 2 * kT1Stage + 4 * kT1Stage2 + 1024;
+// A stage holds the K, V, U tiles of one chunk; with the SWLA update also alpha and
+// beta of the chunk's tokens plus the next one (132 floats each) and lambda (128).
+constexpr uint32_t kT1DecOff = 3 * kTile;
+constexpr uint32_t kT1DecBytes = 2 * 132 * 4 + 128 * 4;
+template <bool DECAY>
+__host__ __device__ constexpr uint32_t t1_stage_bytes() { return DECAY ? 3 * kTile + 2048 : 3 * kTile; }  // tiles stay 1024-aligned
+template <bool DECAY>
+__host__ __device__ constexpr size_t t1_smem_bytes() { return 2 * t1_stage_bytes<DECAY>() + 4 * kT1Stage2 + 1024; }
 
 template <bool GATED, bool DECAY>
 __global__ void __launch_bounds__(kT1Threads, 1)
@@ -203,8 +209,16 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 const int s = gch & 1;
                 const uint32_t r = gch >> 1;
                 if (!mbar_wait(&empty[s], (r & 1) ^ 1, &abort_flag)) break;
-                uint8_t *st = sm + s * kT1Stage;
-                mbar_arrive_expect_tx(&full[s], GATED ? 3 * kTile : 2 * kTile);
+                uint8_t *st = sm + s * t1_stage_bytes<DECAY>();
+                // SWLA: alpha and beta reach one token into the next chunk when it is in the same segment
+                const uint32_t dec_ab = (c + 1 < nch ? 132u : 128u) * 4u;
+                mbar_arrive_expect_tx(&full[s], (GATED ? 3 * kTile : 2 * kTile) + (DECAY ? 2 * dec_ab + 512u : 0u));
+                if (DECAY) {
+                    float *dec = reinterpret_cast<float *>(st + kT1DecOff);
+                    bulk_load(dec, a.alpha + rr, dec_ab, &full[s]);
+                    bulk_load(dec + 132, a.beta + rr, dec_ab, &full[s]);
+                    bulk_load(dec + 264, a.lam + rr, 512u, &full[s]);
+                }
                 tma_load_2d(st, &mK, 0, rr, &full[s]);
                 tma_load_2d(st + 16384, &mK, 64, rr, &full[s]);
                 tma_load_2d(st + kTile, &mV, 0, rr, &full[s]);
@@ -224,7 +238,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 const uint32_t r = gch >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
-                const uint32_t kb = smem_u32(sm + s * kT1Stage), vb = kb + kTile, ub = kb + 2 * kTile;
+                const uint32_t kb = smem_u32(sm + s * t1_stage_bytes<DECAY>()), vb = kb + kTile, ub = kb + 2 * kTile;
                 if (GATED) {  // R = U K^T (online gate score of the chunk's tokens)
                     if (!mbar_wait(&r_empty[b], (r & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (Z, S) = key column (sums)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         float S[kD];  // running state row: S[row][k] = sum_{j before the chunk} v_j[row] k_j[k]
-        uint8_t *wst = sm + 2 * kT1Stage + q4 * kT1Stage2;  // this warp's staging area for global stores
+        uint8_t *wst = sm + 2 * t1_stage_bytes<DECAY>() + q4 * kT1Stage2;  // this warp's staging area for global stores
         float ks = 0.f;  // running sum of key column `row` over the segment, in token order
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
@@ -270,22 +284,22 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 named_bar_sync(1, 128);
             }
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
-            const uint8_t *st = sm + s * kT1Stage;
+            const uint8_t *st = sm + s * t1_stage_bytes<DECAY>();
             // SWLA: the chunk's state is S_{c+1} = zdecay * S^_c + V^T diag(w) K, where w_j is
             // token j's weight at the chunk's end, carried one step on (alpha', beta' of the
             // next token) when that token is in the same segment -- so S is S^_{c+1}.
             float zdecay = 1.f;
             if (DECAY) {
-                const size_t tok0 = (size_t)row0 + (size_t)c * kCT;
-                const ChunkDecay cd = load_chunk_decay(a.alpha, a.beta, a.lam, tok0, lane);
+                const float *dec = reinterpret_cast<const float *>(st + kT1DecOff);  // alpha | beta | lambda
+                const ChunkDecay cd = load_chunk_decay(dec, dec + 132, dec + 264, 0, lane);
                 const int jt = (int)row, jn = jt < kCT - 1 ? jt + 1 : jt;
                 const float ell_end = __shfl_sync(0xffffffffu, cd.ell[3], 31);
                 const float ell_j = chunk_pick(cd.ell, jt), lam_j = chunk_pick(cd.lam, jt);
                 const float ell_n = chunk_pick(cd.ell, jn), bet_n = chunk_pick(cd.bet, jn);
                 float a_next = 1.f, b_next = 0.f;
                 if (c + 1 < nch) {
-                    a_next = a.alpha[tok0 + kCT];
-                    b_next = a.beta[tok0 + kCT];
+                    a_next = dec[kCT];
+                    b_next = dec[132 + kCT];
                 }
                 float w = lam_j * __expf(ell_end - ell_j);
                 if (jt < kCT - 1) w += bet_n * __expf(ell_end - ell_n);
@@ -708,7 +722,7 @@ constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
 constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
 constexpr int kRing = 6;           // operand panels in flight per CTA
 constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
-constexpr uint32_t kT2Decay = 4 * 3 * kCT * 4;   // SWLA: per worker warp, ell / lambda / beta_next of a chunk
+constexpr uint32_t kT2Decay = 4 * 5 * kCT * 4;   // SWLA: per worker warp, ell | lambda | beta_next | E | F of a chunk
 constexpr size_t kT2Smem = kRing * kPanel + kT2Decay + 1024;  // two CTAs fit in an SM's 228 KB
 
 struct TileInfo {
@@ -823,10 +837,15 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
                 const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
-                if (GATED && j + 1 < my_tiles) {  // the workers read the next tile's gate rows directly
+                if ((GATED || DECAY) && j + 1 < my_tiles) {  // rows the workers read directly
                     const TileInfo tn = decode_tile(a, tile_id(j + 1));
                     const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT) / kCT;
-                    prefetch_l2(a.gam + tn_id * (32 * kCT), 32 * kCT * 4);
+                    if (GATED) prefetch_l2(a.gam + tn_id * (32 * kCT), 32 * kCT * 4);
+                    if (DECAY) {
+                        prefetch_l2(a.alpha + tn_id * kCT, kCT * 4);
+                        prefetch_l2(a.beta + tn_id * kCT, kCT * 4);
+                        prefetch_l2(a.lam + tn_id * kCT, kCT * 4);
+                    }
                 }
                 uint8_t *dst = nullptr;
                 for (int h = 0; h < 2 && ok; ++h) {
@@ -960,7 +979,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             ++ac;
         };
         if (my_tiles > 0) load_gates(0);
-        float *dsm = reinterpret_cast<float *>(sm + kRing * kPanel) + q4 * 3 * kCT;  // SWLA: ell | lambda | beta_{j+1}
+        float *dsm = reinterpret_cast<float *>(sm + kRing * kPanel) + q4 * 5 * kCT;  // SWLA: ell | lambda | beta_{j+1} | E | F
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
             const int items = tile_items<GATED>(t);
@@ -976,6 +995,16 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     dsm[4 * lane + e] = cd.ell[e];
                     dsm[kCT + 4 * lane + e] = cd.lam[e];
                     dsm[2 * kCT + 4 * lane + e] = e < 3 ? cd.bet[e + 1] : (lane < 31 ? b_up : 0.f);
+                }
+                __syncwarp();
+                // Per 32-column block h with reference m_h = ell_{32h}: E_j = lambda_j exp(m_h - ell_j),
+                // F_j = beta_{j+1} exp(m_h - ell_{j+1}), so c_{t,j} = exp(ell_t - m_h) (E_j + [j<t] F_j).
+#pragma unroll
+                for (int hb = 0; hb < 4; ++hb) {
+                    const int cj = 32 * hb + lane;
+                    const float m = dsm[32 * hb];
+                    dsm[3 * kCT + cj] = dsm[kCT + cj] * __expf(m - dsm[cj]);
+                    dsm[4 * kCT + cj] = cj < kCT - 1 ? dsm[2 * kCT + cj] * __expf(m - dsm[cj + 1]) : 0.f;
                 }
                 __syncwarp();
                 ellt = dsm[row];
@@ -1026,18 +1055,37 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o[i] = 0u;
                     } else {
-                        // P_tj = g_n c_{t,j} G_tj, c_{t,j} = lambda_j A(j,t) + [j<t] beta_{j+1} A(j+1,t)
-                        auto coef = [&](uint32_t cj) -> float {
-                            if (cj > row) return 0.f;
-                            float cf = dsm[kCT + cj] * __expf(ellt - dsm[cj]);
-                            if (cj < row) cf += dsm[2 * kCT + cj] * __expf(ellt - dsm[cj + 1]);
-                            return cf;
-                        };
+                        // P_tj = g_n c_{t,j} G_tj, c_{t,j} = lambda_j A(j,t) + [j<t] beta_{j+1} A(j+1,t).
+                        // Factored through the block's reference when the block's decay range keeps
+                        // E and F finite; element by element otherwise (strong decay).
+                        const float m = dsm[32 * h];
+                        const bool factored = m - dsm[32 * h + 32 < kCT ? 32 * h + 32 : kCT - 1] <= 80.f &&
+                                              dsm[kCT - 1] - m <= 80.f;  // warp-uniform
+                        if (factored) {
+                            const float et = gn * __expf(ellt - m);
+                            auto coef = [&](uint32_t cj) -> float {
+                                if (cj > row) return 0.f;
+                                return dsm[3 * kCT + cj] + (cj < row ? dsm[4 * kCT + cj] : 0.f);
+                            };
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint32_t c0 = 32 * h + 2 * i;
-                            o[i] = pack_bf16x2(gn * coef(c0) * __uint_as_float(x[2 * i]),
-                                               gn * coef(c0 + 1) * __uint_as_float(x[2 * i + 1]));
+                            for (int i = 0; i < 16; ++i) {
+                                const uint32_t c0 = 32 * h + 2 * i;
+                                o[i] = pack_bf16x2(et * coef(c0) * __uint_as_float(x[2 * i]),
+                                                   et * coef(c0 + 1) * __uint_as_float(x[2 * i + 1]));
+                            }
+                        } else {
+                            auto coef = [&](uint32_t cj) -> float {
+                                if (cj > row) return 0.f;
+                                float cf = dsm[kCT + cj] * __expf(ellt - dsm[cj]);
+                                if (cj < row) cf += dsm[2 * kCT + cj] * __expf(ellt - dsm[cj + 1]);
+                                return cf;
+                            };
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint32_t c0 = 32 * h + 2 * i;
+                                o[i] = pack_bf16x2(gn * coef(c0) * __uint_as_float(x[2 * i]),
+                                                   gn * coef(c0 + 1) * __uint_as_float(x[2 * i + 1]));
+                            }
                         }
                     }
                     tmem_st16(ta + 16 * h, o);
@@ -1273,10 +1321,11 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     {
         auto k1 = gated ? (decay ? seg_state_tc<true, true> : seg_state_tc<true, false>)
                         : (decay ? seg_state_tc<false, true> : seg_state_tc<false, false>);
-        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT1Smem);
+        const size_t smem1 = decay ? t1_smem_bytes<true>() : t1_smem_bytes<false>();
+        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
         if (e != cudaSuccess) return e;
         const int nseg = (int)(BH * N);
-        k1<<<nseg < g_num_sms ? nseg : g_num_sms, kT1Threads, kT1Smem, s>>>(mK, mV, mU, a);
+        k1<<<nseg < g_num_sms ? nseg : g_num_sms, kT1Threads, smem1, s>>>(mK, mV, mU, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "seg_state_tc");
     }
