@@ -393,6 +393,62 @@ def run_ours(args, w, wname="long-grm"):
     return res if rank == 0 else None
 
 
+def run_decode(args):
+    """One recurrent decoding step (mc_decode_step) per sequence: B = 8, H = 16, d = 128,
+    seg_len = 1024, position 63*1024 + 512 (63 cached segments, mid-segment), GRM.  The
+    step reads every cached fp32 state once: reported against HBM."""
+    import torch
+    import memory_caching_linear_gb300 as mcl
+    from memory_caching_linear_gb300 import build as mcbuild
+    mcbuild.build()
+    mcl.load_library()
+    B, H, d, C, nmax = 8, 16, 128, 1024, 64
+    t = 63 * C + 512
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device="cpu").manual_seed(6)
+    cache = mcl.DecodeCache(B, H, d, C, nmax, device=dev)
+    cache.states.copy_(torch.randn(cache.states.shape, generator=g) / d)
+    cache.kbar.copy_(torch.nn.functional.normalize(torch.randn(cache.kbar.shape, generator=g), dim=-1))
+    cache.online.copy_(torch.randn(cache.online.shape, generator=g) / d)
+    cache.ksum.copy_(torch.randn(cache.ksum.shape, generator=g))
+    q, k, v, u = (x[:, :, 0, :].contiguous() for x in mc_inputs.make_inputs(B, H, 1, d, 6, "bf16", device=dev))
+    y = torch.empty_like(q)
+
+    def step():
+        cache.t = t
+        mcl.mc_decode_step(cache, q, k, v, u, GRM, y=y)
+
+    sampler = ClockSampler(dev.index).start()
+    for _ in range(max(args.warmup, 50)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 200)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1) / steps
+    s_cached = t // C
+    bytes_step = B * H * (s_cached * d * d * 4 + 2 * d * d * 4 + s_cached * d * 4 + 3 * d * 2)
+    peak = measured_peaks()["hbm_gbs"]
+    achieved = bytes_step / (ms / 1e3) / 1e9
+    return {
+        "metric": "tokens/sec MC-GRM decode step (d=128, 63 cached segments)", "value": round(B / (ms / 1e3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 50),
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (random fp32 caches, seeded bf16 token)",
+        "config": {"workload": f"decode-grm B{B} H{H} d{d} C{C} t={t}", "B": B, "H": H, "d": d, "seg_len": C,
+                   "cached_segments": s_cached},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "decode_gates + decode_read", "algorithmic_bytes_per_step": bytes_step},
+        "gpu_launches": 2 * steps, "clocks": sampler.summary(),
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, w):
@@ -433,7 +489,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long-grm")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["decode-grm"], default="long-grm")
     ap.add_argument("--mode", choices=["residual", "grm", "soup", "ssc"], default=None,
                     help="override the workload's aggregation")
     ap.add_argument("--warmup-seconds", type=float, default=1.0,
@@ -444,6 +500,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "decode-grm":
+        if args.impl == "ours":
+            print(json.dumps(run_decode(args)), flush=True)
+        return
     w = WORKLOADS[args.workload]
     if args.mode:
         w = w.with_(mode={"residual": RESIDUAL, "grm": GRM, "soup": 2, "ssc": SSC}[args.mode])

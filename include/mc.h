@@ -119,6 +119,34 @@ int mc_forward_swla(const void *q, const void *k, const void *v, const void *u,
                     void *y, float *states, mc_stream_t stream);
 
 /*
+ * mc_decode_step -- one recurrent decoding step: the token at position t of each
+ * of the B*H sequences (all at the same position) updates and reads the memory
+ * caches, exactly as mc_forward treats token t ([MC-ja §3 eq. 4b-5, §3.1 eq.
+ * 7-10]; Soup is read as GRM, identical for this linear memory).  Run for
+ * t = 0, 1, 2, ... from caches whose contents are ignored at t = 0, it
+ * reproduces mc_forward's y token by token and leaves every completed
+ * segment's state in `states`.
+ *   q, k, v, u : the new token, [B][H][d], bf16 if is_bf16 != 0 else fp32 (u may
+ *                be NULL for Residual).  y: [B][H][d], written, same dtype.
+ *   t          : the token's position; segment s = t / seg_len.
+ *   states     : fp32 [B][H][n_max][d][d], cached segment states M^(i), i < s,
+ *                read; at the segment's last token (t % seg_len == seg_len - 1)
+ *                M^(s) is written to slot s.
+ *   kbar       : fp32 [B][H][n_max][d], cached key means, same rule.
+ *   online     : fp32 [B][H][d][d], the current segment's memory (in/out).
+ *   ksum       : fp32 [B][H][d], the current segment's key sum (in/out).
+ *   n_max      : capacity of the caches in segments, 1..64; t / seg_len < n_max.
+ *   SSC ranks fp32 scores <u, kbar_i> (equal scores: lower index first).
+ *   Errors as mc_forward; MC_ERR_SHAPE also for t < 0 or a full cache.  The
+ *   call is asynchronous on `stream`; it allocates a few bytes of scratch
+ *   per head from the library's pool.
+ */
+int mc_decode_step(const void *q, const void *k, const void *v, const void *u,
+                   int B, int H, int d, int seg_len, int agg_mode, int topk, int t,
+                   float *states, float *kbar, float *online, float *ksum, int n_max,
+                   void *y, int is_bf16, mc_stream_t stream);
+
+/*
  * mc_ssc_select -- the SSC router alone ([MC-sum §3.4]), for inspection and tests.
  *   k, u     : [B][H][L][d], bf16 if is_bf16 != 0 else fp32, device.
  *   idx      : int32 [B][H][L][topk], written: for token t of segment s, the

@@ -24,7 +24,7 @@ MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
 MC_ERR_SCRATCH = -10
 
-EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
             "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
             "mc_status_string")
 
@@ -54,6 +54,8 @@ def load_library():
     lib.mc_forward_f32.restype = i
     lib.mc_forward_swla.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
     lib.mc_forward_swla.restype = i
+    lib.mc_decode_step.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, i, vp]
+    lib.mc_decode_step.restype = i
     lib.mc_ssc_select.argtypes = [vp, vp, i, i, i, i, i, i, vp, i, vp]
     lib.mc_ssc_select.restype = i
     lib.mc_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, i, vp]
@@ -149,6 +151,51 @@ def mc_forward_swla(q, k, v, u, alpha, beta, lam, seg_len: int, agg_mode: int, t
     mc.h); alpha, beta, lam are fp32 [B, H, L] on the device.  Returns (y, states)."""
     return _forward("mc_forward_swla", q, k, v, u, seg_len, agg_mode, topk, y, states, want_states, stream,
                     swla=(alpha, beta, lam))
+
+
+class DecodeCache:
+    """Device caches for recurrent decoding with ``mc_decode_step``: cached segment
+    states [B,H,n_max,d,d] and key means [B,H,n_max,d], the online memory
+    [B,H,d,d] and key sum [B,H,d] (fp32), plus the next position ``t``."""
+
+    def __init__(self, B: int, H: int, d: int, seg_len: int, n_max: int, device="cuda"):
+        self.seg_len, self.n_max, self.t = int(seg_len), int(n_max), 0
+        f32 = dict(dtype=torch.float32, device=device)
+        self.states = torch.zeros((B, H, n_max, d, d), **f32)
+        self.kbar = torch.zeros((B, H, n_max, d), **f32)
+        self.online = torch.zeros((B, H, d, d), **f32)
+        self.ksum = torch.zeros((B, H, d), **f32)
+
+
+def mc_decode_step(cache: DecodeCache, q, k, v, u, agg_mode: int, topk: int = 0, *, y=None, stream=None):
+    """One decoding step (``mc_decode_step`` in mc.h) for tokens q, k, v, u of shape
+    [B, H, d] at position ``cache.t``; advances ``cache.t`` and returns y [B, H, d]."""
+    lib = load_library()
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, d]")
+    B, H, d = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    for t_, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t_, n, q.dtype, (B, H, d), dev)
+    if u is not None:
+        _check(u, "u", q.dtype, (B, H, d), dev)
+    if y is None:
+        y = torch.empty((B, H, d), dtype=q.dtype, device=dev)
+    _check(y, "y", q.dtype, (B, H, d), dev)
+    for t_, n, shp in ((cache.states, "states", (B, H, cache.n_max, d, d)), (cache.kbar, "kbar", (B, H, cache.n_max, d)),
+                       (cache.online, "online", (B, H, d, d)), (cache.ksum, "ksum", (B, H, d))):
+        _check(t_, n, torch.float32, shp, dev)
+    st = lib.mc_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None,
+                            B, H, d, cache.seg_len, int(agg_mode), int(topk), cache.t,
+                            cache.states.data_ptr(), cache.kbar.data_ptr(), cache.online.data_ptr(),
+                            cache.ksum.data_ptr(), cache.n_max, y.data_ptr(), int(q.dtype == torch.bfloat16),
+                            _stream_handle(stream, dev))
+    if st != MC_OK:
+        raise MCError(st, "mc_decode_step")
+    cache.t += 1
+    return y
 
 
 def mc_forward_f32(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, *, y=None, states=None,

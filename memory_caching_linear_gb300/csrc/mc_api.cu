@@ -245,6 +245,46 @@ int mc_forward_swla(const void *q, const void *k, const void *v, const void *u, 
                               reinterpret_cast<cudaStream_t>(stream), alpha, beta, lam, true);
 }
 
+int mc_decode_step(const void *q, const void *k, const void *v, const void *u, int B, int H, int d, int seg_len,
+                   int agg_mode, int topk, int t, float *states, float *kbar, float *online, float *ksum, int n_max,
+                   void *y, int is_bf16, mc_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int st = mc::check_shape(B, H, 1, d, seg_len);
+    if (st != MC_OK) return st;
+    if (t < 0 || n_max < 1 || n_max > mc::kDecMaxN - 1 || t / seg_len >= n_max) return MC_ERR_SHAPE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode == MC_SSC && topk < 0) return MC_ERR_TOPK;
+    if (!q || !k || !v || !y || !states || !kbar || !online || !ksum) return MC_ERR_NULL;
+    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (!mc::aligned16(q) || !mc::aligned16(k) || !mc::aligned16(v) || !mc::aligned16(y) || (u && !mc::aligned16(u)) ||
+        !mc::aligned16(states) || !mc::aligned16(kbar) || !mc::aligned16(online) || !mc::aligned16(ksum))
+        return MC_ERR_ALIGN;
+    st = mc::check_device();
+    if (st != MC_OK) return st;
+    mc::DecodeArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.u = agg_mode == MC_RESIDUAL ? nullptr : u;
+    a.y = y;
+    a.states = states; a.kbar = kbar; a.online = online; a.ksum = ksum;
+    a.BH = B * H; a.d = d; a.C = seg_len; a.mode = agg_mode == MC_SOUP ? MC_GRM : agg_mode;
+    a.topk = agg_mode == MC_SSC ? topk : 0;
+    a.t = t; a.nmax = n_max; a.bf16 = is_bf16 != 0;
+    void *gates = nullptr;
+    if (mc::scratch_alloc(&gates, sizeof(float) * (size_t)a.BH * mc::kDecGateWords, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    a.gates = static_cast<float *>(gates);
+    cudaError_t e = mc::launch_decode_step(a, stream);
+    cudaError_t ef = cudaFreeAsync(gates, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
 int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int seg_len, int topk, int32_t *idx,
                   int is_bf16, mc_stream_t stream_)
 {

@@ -75,6 +75,20 @@ __device__ __forceinline__ void topk_insert(float *vals, int *idxs, int &count, 
     if (count < k) ++count;
 }
 
+// One decoding step (k_decode.cu).  Caches: states [BH][nmax][d][d], kbar
+// [BH][nmax][d], online [BH][d][d], ksum [BH][d] (fp32); the token's q, k, v, u
+// and y are [BH][d] (bf16 or fp32); gates is scratch [BH][kDecGateWords].
+constexpr int kDecMaxN = 65;        // cached segments (at most 64) plus the online memory
+constexpr int kDecGateWords = 132;  // per-head gate record of the decoding step (k_decode.cu)
+struct DecodeArgs {
+    const void *q, *k, *v, *u;
+    void *y;
+    float *states, *kbar, *online, *ksum, *gates;
+    int BH, d, C, mode, topk, t, nmax;
+    bool bf16;
+};
+cudaError_t launch_decode_step(const DecodeArgs &a, cudaStream_t s);
+
 // Stream-ordered scratch from the library's per-device pool (mc_api.cu).
 cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s);
 

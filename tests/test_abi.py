@@ -82,6 +82,17 @@ def test_argument_errors_never_reach_the_device(lib):
     assert st == mcl.MC_ERR_TOPK
     st = lib.mc_forward_host(None, FAKE, FAKE, FAKE, 1, 1, 64, 16, 16, 1, 0, FAKE, None, 1, None)
     assert st == mcl.MC_ERR_NULL
+    dec = lambda **kw: lib.mc_decode_step(*[kw.get(n, FAKE) for n in ("q", "k", "v", "u")], 1, 1, kw.get("d", 16), 16,
+                                          kw.get("mode", 1), 0, kw.get("t", 0), FAKE, FAKE, FAKE, FAKE,
+                                          kw.get("n_max", 4), FAKE, 1, None)
+    assert dec(t=-1) == mcl.MC_ERR_SHAPE
+    assert dec(t=64) == mcl.MC_ERR_SHAPE  # segment 4 needs a fifth cache slot
+    assert dec(n_max=65) == mcl.MC_ERR_SHAPE
+    assert dec(d=24) == mcl.MC_ERR_SHAPE
+    assert dec(mode=9) == mcl.MC_ERR_MODE
+    assert dec(q=None) == mcl.MC_ERR_NULL
+    assert dec(u=None) == mcl.MC_ERR_NULL
+    assert dec(q=FAKE + 4) == mcl.MC_ERR_ALIGN
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")

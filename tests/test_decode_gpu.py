@@ -1,0 +1,69 @@
+"""Recurrent decoding (mc_decode_step): run token by token from empty caches, it
+must reproduce the oracle's forward -- y for every token and the cached segment
+states -- for every aggregation.
+
+Pages cited:
+  [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
+  [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
+           (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
+"""
+import numpy as np
+import pytest
+import torch
+
+import memory_caching_linear_gb300 as mcl
+import oracle
+from mc_inputs import GRM, RESIDUAL, SOUP, SSC, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from memory_caching_linear_gb300 import build
+    build.build()
+    mcl.load_library()
+
+
+def decode_all(q, k, v, u, C, mode, topk, n_max):
+    B, H, L, d = q.shape
+    qd, kd, vd, ud = (t.cuda() for t in (q, k, v, u))
+    cache = mcl.DecodeCache(B, H, d, C, n_max)
+    ys = []
+    for t in range(L):
+        tok = [x[:, :, t, :].contiguous() for x in (qd, kd, vd, ud)]
+        ys.append(mcl.mc_decode_step(cache, *tok, mode, topk).float().cpu())
+    torch.cuda.synchronize()
+    assert mcl.mc_check_device() == mcl.MC_OK
+    return torch.stack(ys, 2).numpy(), cache
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("d,C,L,dtype", [(64, 128, 512, "bf16"), (32, 48, 200, "f32"), (128, 256, 768, "bf16")])
+def test_decode_reproduces_the_forward(mode, topk, d, C, L, dtype):
+    q, k, v, u = make_inputs(1, 2, L, d, 17 + d, dtype)
+    N = (L + C - 1) // C
+    ref = oracle.forward(q, k, v, u, C, mode, topk)
+    y, cache = decode_all(q, k, v, u, C, mode, topk, n_max=N + 1)
+    keep = np.ones(y.shape[:3], bool)
+    if mode == SSC:  # fp32 near-ties may rank either way
+        keep = ref["gap"] >= GAP
+    yref = ref["y"]
+    err = np.abs(y - yref)[keep].max() / np.abs(yref).max()
+    assert err <= TOL[dtype], err
+    done = L // C  # segments completed by the last token
+    st = cache.states[:, :, :done].cpu().numpy()
+    serr = np.abs(st - ref["states"][:, :, :done]).max() / np.abs(ref["states"]).max()
+    assert serr <= TOL["f32"], serr  # fp32 sums of the exact inputs
+
+
+def test_decode_rejects_a_full_cache():
+    q = torch.zeros(1, 1, 64, dtype=torch.bfloat16, device="cuda")
+    cache = mcl.DecodeCache(1, 1, 64, 16, n_max=2)
+    cache.t = 32  # segment 2 does not fit in two slots
+    with pytest.raises(mcl.MCError) as e:
+        mcl.mc_decode_step(cache, q, q, q, q, GRM)
+    assert e.value.status == mcl.MC_ERR_SHAPE
