@@ -8,7 +8,7 @@
 //   [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
 //            (gitcode.csdn.net/6a26b456662f9a54cb7b57bd.html)
 //
-// Three kernels.
+// Two kernels make the forward; a third serves the SSC router alone.
 //
 // seg_state_tc -- persistent; each CTA walks its segments in chunks of 128 tokens
 //   with the running state S = sum v_j k_j^T (fp32, one row per worker thread):
@@ -22,11 +22,6 @@
 //     r_on[t] = <u_t, sum_{j=t0..t} k_j> / (t - t0 + 1)
 //   from R = U_c K_c^T (tensor core) masked to j <= t plus <u_t, keys before the chunk>.
 //
-// gates_tc -- per 128-token chunk, the scores <u_t, kbar_i> (two MMAs: hi and lo
-//   rows) and the gates g = softmax over {scores_i}_{i<n} and r_on[t] (GRM;
-//   Soup is the same sum for a linear memory, [MC-sum §3.3]); SSC keeps the topk
-//   largest cached scores ([MC-sum §3.4]) and gives the others gate 0.
-//
 // readout_tc -- persistent, two CTAs per SM; a tile is (bh, segment n, chunk c)
 //   of 128 tokens, heaviest tiles first.  For the tile's tokens it computes
 //     y_t = g_{t,n} [ S_pre(c) q_t + sum_{j in chunk, j<=t} v_j (k_j . q_t) ]
@@ -34,7 +29,14 @@
 //   (Residual: g = 1, [MC-ja §3.1 eq. 7], where the cached sum collapses to one
 //   prefix state) as MMAs into one fp32 accumulator D per CTA:
 //     G = Q K_c^T;  D = (g_n * mask(G)) V_c;  D += (g_i o Q) X_i^T
-//   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.
+//   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.  The gates come from the
+//   scores <u_t, kbar_i> (two MMAs per tile: kbar as hi and lo rows) and r_on[t]:
+//   g = softmax over {scores_i}_{i<n} and r_on[t] (GRM; Soup is the same sum for
+//   a linear memory, [MC-sum §3.3]); SSC keeps the topk largest cached scores
+//   ([MC-sum §3.4]) and gives the others gate 0.
+//
+// ssc_router_tc -- the SSC router alone (the selected segments of every token),
+//   from the same scores.
 #include <cstdint>
 
 #include "mc_internal.cuh"
@@ -65,8 +67,6 @@ struct TcArgs {
     uint8_t *kbar_img;    // [BH] x 32 KB: hi rows (16 KB) then lo rows (16 KB), row = segment
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
-    uint32_t *gam;        // gates as bf16 pairs, per 128-token tile T: [T][pair p][row]; pair p holds
-                          // (g_{2p}, g_{2p+1}); g_i for i < n, g_n in the high half of pair 31
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
@@ -147,6 +147,7 @@ constexpr uint32_t kT1DecOff = 3 * kTile;
 constexpr uint32_t kT1DecBytes = 2 * 132 * 4 + 128 * 4;
 template <bool DECAY>
 __host__ __device__ constexpr uint32_t t1_stage_bytes() { return DECAY ? 3 * kTile + 2048 : 3 * kTile; }  // tiles stay 1024-aligned
+static_assert(kT1DecBytes <= 2048, "the SWLA scalars fit the stage's tail");
 template <bool DECAY>
 __host__ __device__ constexpr size_t t1_smem_bytes() { return 2 * t1_stage_bytes<DECAY>() + 4 * kT1Stage2 + 1024; }
 
@@ -516,22 +517,84 @@ __global__ void __launch_bounds__(256) prefix_images(TcArgs a)
     }
 }
 
+// The gates of one token ([MC-ja §3.1 eq. 10], normalised by a softmax) from its
+// scores sc[0..n) against the cached segments and its online score ron.  GRM / Soup:
+// every cached segment takes part; SSC ([MC-sum §3.4]): the topk largest scores,
+// equal scores to the lower segment index (their indices, in rank order and -1
+// padded, go to so when given).  On return sc[i] (i < 63) holds the unnormalised
+// weight of segment i (0 when not taken or i >= n), sc[63] the online one; the
+// result is 1 / Z.  n is the same for every thread of a warp, so the loops skip
+// whole groups of 8 segments uniformly.
+template <bool SSC>
+__device__ __forceinline__ float token_gates(float (&sc)[64], int n, float ron, int topk, int32_t *so)
+{
+    uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
+    if (SSC) {
+        const int cnt = min(topk, n);
+        uint64_t chosen = 0;
+        for (int r = 0; r < cnt; ++r) {
+            float best = 0.f;
+            int bi = -1;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+                if (8 * g8 >= n) break;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int k = 8 * g8 + kk;
+                    if (k < 63 && k < n && !((chosen >> k) & 1ull) && (bi < 0 || sc[k] > best)) {
+                        best = sc[k];
+                        bi = k;
+                    }
+                }
+            }
+            chosen |= 1ull << bi;
+            if (so) so[r] = bi;
+        }
+        if (so)
+            for (int r = cnt; r < topk; ++r) so[r] = -1;
+        take = chosen;
+    }
+    float mx4[4] = {ron, ron, ron, ron};  // partial maxima / sums: shorter dependency chains
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        if (8 * g8 >= n) break;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int k = 8 * g8 + kk;
+            if (k < 63 && ((take >> k) & 1ull)) mx4[kk & 3] = fmaxf(mx4[kk & 3], sc[k]);
+        }
+    }
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        if (8 * g8 >= n) break;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int k = 8 * g8 + kk;
+            if (k < 63) {
+                sc[k] = ((take >> k) & 1ull) ? __expf(sc[k] - mx) : 0.f;
+                z4[kk & 3] += sc[k];
+            }
+        }
+    }
+    sc[63] = __expf(ron - mx);
+    return 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
+}
+
 // ============================================================================
-// gates_tc -- the gate of every token ([MC-ja §3.1 eq. 10], normalised by a
-// softmax): one CTA per 128-token chunk.  Scores r_{t,i} = <u_t, kbar_i> come
-// from two MMAs (kbar as hi + lo bf16 rows, so the score carries ~16 bits of
-// kbar; u is exact in bf16), then
-//   g_{t,i} = exp(r_{t,i} - m) / Z (i < n),  g_{t,n} = exp(r_on[t] - m) / Z
-// written as bf16 pairs in tile-transposed order (coalesced for a thread per token
-// row): gam[tile][p][row] = (g_{2p}, g_{2p+1}), g_i for i < n, g_n as element 63.
+// ssc_router_tc -- the SSC router ([MC-sum §3.4]): for every token the topk
+// cached segments with the largest scores r_{t,i} = <u_t, kbar_i> (i < n), in rank
+// order, equal scores to the lower index, -1 padded.  One CTA per 128-token chunk;
+// the scores come from two MMAs (kbar as hi + lo bf16 rows, so the score carries
+// ~16 bits of kbar; u is exact in bf16).
 // ============================================================================
-constexpr int kGatesThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax + store
-constexpr size_t kGatesSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
+constexpr int kRouterThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 selection
+constexpr size_t kRouterSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
 
 // Persistent: CTA b handles the contiguous tile range [b*per, (b+1)*per) of the
 // (bh, chunk) tiles, so consecutive tiles share a head and its kbar image.
-template <bool SSC>
-__global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
+__global__ void __launch_bounds__(kRouterThreads, 2) ssc_router_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -627,8 +690,7 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             const int n = t0 / a.C;
             if (!mbar_wait(&s_full[b], (i >> 1) & 1, &abort_flag)) break;
             tc_fence_after();
-            // Only the first n scores take part; n is the same for the whole tile, so
-            // the loops below skip whole groups of 8 segments uniformly.
+            // Only the first n scores take part (n is the same for the whole tile).
             float sc[64];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -643,66 +705,7 @@ __global__ void __launch_bounds__(kGatesThreads, 2) gates_tc(const __grid_consta
             tc_fence_before();
             mbar_arrive(&s_empty[b]);
             const size_t tok = (size_t)bh * a.L + t0 + row;
-            const float ron = a.r_on ? a.r_on[tok] : 0.f;  // no r_on: router only
-            // GRM / Soup: every cached segment takes part.  SSC ([MC-sum §3.4]): the
-            // topk largest scores, equal scores to the lower segment index.
-            uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
-            if (SSC) {
-                const int cnt = min(a.topk, n);
-                uint64_t chosen = 0;
-                int32_t *so = a.sel_out ? a.sel_out + tok * a.topk : nullptr;
-                for (int r = 0; r < cnt; ++r) {
-                    float best = 0.f;
-                    int bi = -1;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        if (8 * g8 >= n) break;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const int k = 8 * g8 + kk;
-                            if (k < 63 && k < n && !((chosen >> k) & 1ull) && (bi < 0 || sc[k] > best)) {
-                                best = sc[k];
-                                bi = k;
-                            }
-                        }
-                    }
-                    chosen |= 1ull << bi;
-                    if (so) so[r] = bi;
-                }
-                if (so)
-                    for (int r = cnt; r < a.topk; ++r) so[r] = -1;
-                take = chosen;
-            }
-            float mx4[4] = {ron, ron, ron, ron};  // partial maxima / sums: shorter dependency chains
-#pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
-                if (8 * g8 >= n) break;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int k = 8 * g8 + kk;
-                    if (k < 63 && ((take >> k) & 1ull)) mx4[kk & 3] = fmaxf(mx4[kk & 3], sc[k]);
-                }
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            float z4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
-                if (8 * g8 >= n) break;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int k = 8 * g8 + kk;
-                    if (k < 63) {
-                        sc[k] = ((take >> k) & 1ull) ? __expf(sc[k] - mx) : 0.f;
-                        z4[kk & 3] += sc[k];
-                    }
-                }
-            }
-            sc[63] = __expf(ron - mx);
-            const float inv = 1.f / (sc[63] + (z4[0] + z4[1]) + (z4[2] + z4[3]));
-            if (!a.gam) continue;  // router only (mc_ssc_select)
-            uint32_t *dst = a.gam + (size_t)it * (32 * kCT) + row;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) dst[k * kCT] = pack_bf16x2(sc[2 * k] * inv, sc[2 * k + 1] * inv);
+            token_gates<true>(sc, n, 0.f, a.topk, a.sel_out + tok * a.topk);
         }
     }
     tc_fence_before();
@@ -771,16 +774,16 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 // release those panels once G is done), read the gate rows in the tile-transposed
 // layout (coalesced), and write y from a quad-transposed register layout.  Two CTAs run on each SM, so while one waits on its G -> P step or its
 // drain the other keeps the tensor pipe busy.
-template <bool GATED, bool DECAY>
+template <bool GATED, bool DECAY, bool SSC>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, TcArgs a)
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t ring_full[kRing], ring_empty[kRing];
     __shared__ uint64_t a_full[2], a_empty[2];
-    __shared__ uint64_t g_full, y_full, y_empty, fin, q_read;
+    __shared__ uint64_t g_full, y_full, y_empty, fin, q_read, s_full;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -805,6 +808,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             mbar_init(&a_empty[s], 1);
         }
         mbar_init(&g_full, 1);
+        mbar_init(&s_full, 1);
         mbar_init(&y_full, 1);
         mbar_init(&y_empty, 128);
         mbar_init(&fin, 1);
@@ -820,12 +824,14 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // Panel sequence of a tile: Q0 K0 Q1 K1 (G), V0 V1 (P V), then both K
-        // panels of every cached operand.  The workers release the Q panels.
+        // Panel sequence of a tile: (gated) U0 U1 KBhi KBlo (gate scores), Q0 K0 Q1 K1
+        // (G), V0 V1 (P V), then both K panels of every cached operand.  The workers
+        // release the Q panels.
         if (lane == 0 && my_tiles > 0) {
             prefetch_tensormap(&mQ);
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
+            if (GATED) prefetch_tensormap(&mU);
             uint32_t g = 0;
             bool ok = true;
             auto slot = [&]() -> uint8_t * {
@@ -840,7 +846,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 if ((GATED || DECAY) && j + 1 < my_tiles) {  // rows the workers read directly
                     const TileInfo tn = decode_tile(a, tile_id(j + 1));
                     const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT) / kCT;
-                    if (GATED) prefetch_l2(a.gam + tn_id * (32 * kCT), 32 * kCT * 4);
+                    if (GATED) prefetch_l2(a.r_on + tn_id * kCT, kCT * 4);
                     if (DECAY) {
                         prefetch_l2(a.alpha + tn_id * kCT, kCT * 4);
                         prefetch_l2(a.beta + tn_id * kCT, kCT * 4);
@@ -848,6 +854,18 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     }
                 }
                 uint8_t *dst = nullptr;
+                if (GATED) {  // U (two K panels) and the head's key-mean image (hi rows, lo rows)
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = (dst = slot()) != nullptr)) break;
+                        tma_load_2d(dst, &mU, 64 * h, rr, &ring_full[g % kRing]);
+                        ++g;
+                    }
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = (dst = slot()) != nullptr)) break;
+                        bulk_load(dst, a.kbar_img + (size_t)t.bh * kTile + h * kPanel, kPanel, &ring_full[g % kRing]);
+                        ++g;
+                    }
+                }
                 for (int h = 0; h < 2 && ok; ++h) {
                     if (!(ok = (dst = slot()) != nullptr)) break;
                     tma_load_2d(dst, &mQ, 64 * h, rr, &ring_full[g % kRing]);
@@ -891,6 +909,29 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
+                if (GATED) {
+                    // gate scores S = U (kbar_hi + kbar_lo)^T into the tile's first A slot (the
+                    // workers read S there, then write P over it); the slot's last readers were
+                    // issued before this
+                    constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+                    const uint32_t ts = tA0 + (ac % 2) * 64;
+                    if (!(ok = ring_ready(g) && ring_ready(g + 1) && ring_ready(g + 2) && ring_ready(g + 3))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb) {  // hi rows, then lo rows
+                        const uint64_t dkb = make_desc_sw128(s_base + ((g + 2 + kb) % kRing) * kPanel, 0, 1024);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t du = make_desc_sw128(s_base + ((g + h) % kRing) * kPanel, 0, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(ts, du + 2 * kk, dkb + ((8192u * h) >> 4) + 2 * kk, idS, (kb | h | kk) != 0);
+                        }
+                    }
+                    for (int i = 0; i < 4; ++i) mma_commit(&ring_empty[(g + i) % kRing]);
+                    mma_commit(&s_full);
+                    g += 4;
+                }
                 if (!(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;  // D of tile j-1 drained
                 // G = Q K^T
                 for (int h = 0; h < 2; ++h) {
@@ -959,14 +1000,6 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         uint32_t ac = 0, g = 0;  // A-slot / ring counters, in step with the MMA issuer
         bool ok = true;
         uint32_t gm2[32];  // gate pairs of the token: (g_{2p}, g_{2p+1}); g_n is element 63
-        auto load_gates = [&](int j) {
-            if (!GATED) return;
-            const TileInfo t = decode_tile(a, tile_id(j));
-            const size_t tid = ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) / kCT;
-            const uint32_t *src = a.gam + tid * (32 * kCT) + row;
-#pragma unroll
-            for (int p = 0; p < 32; ++p) gm2[p] = __ldg(src + p * kCT);
-        };
         auto claim = [&]() -> bool {  // the next A slot is free
             if (!mbar_wait(&a_empty[ac % 2], ((ac / 2) & 1) ^ 1, &abort_flag)) return false;
             tc_fence_after();
@@ -978,13 +1011,34 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             mbar_arrive(&a_full[ac % 2]);
             ++ac;
         };
-        if (my_tiles > 0) load_gates(0);
         float *dsm = reinterpret_cast<float *>(sm + kRing * kPanel) + q4 * 5 * kCT;  // SWLA: ell | lambda | beta_{j+1} | E | F
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
             const int items = tile_items<GATED>(t);
-            const float gn = GATED ? __bfloat162float(__high2bfloat16(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31])))
-                                   : 1.f;
+            float gn = 1.f;
+            if (GATED) {
+                // the token's gates from the scores S in this tile's first A slot
+                g += 4;  // the U and key-mean panels, released by the issuer
+                const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
+                const float ron = __ldg(a.r_on + tok);
+                if (!(ok = mbar_wait(&s_full, j & 1, &abort_flag))) break;
+                tc_fence_after();
+                float sc[64];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if (16 * m < t.n) {
+                        tmem_ld16f(tA0 + (ac % 2) * 64 + lane_base + 16 * m, sc + 16 * m);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) sc[16 * m + k] = 0.f;
+                    }
+                }
+                tmem_wait_ld();
+                const float inv = token_gates<SSC>(sc, t.n, ron, a.topk, nullptr);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) gm2[k] = pack_bf16x2(sc[2 * k] * inv, sc[2 * k + 1] * inv);
+                gn = __bfloat162float(__high2bfloat16(*reinterpret_cast<const __nv_bfloat162 *>(&gm2[31])));
+            }
             float ellt = 0.f;  // SWLA: log of A(t_c, t) for this token row
             if (DECAY) {
                 const size_t tok0 = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT;
@@ -1125,7 +1179,6 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             }
             if (!ok) break;
             g += 6 + 2 * items;
-            if (j + 1 < my_tiles) load_gates(j + 1);  // lands while this tile's MMAs finish
             // drain: read D in the 16x256b layout (a quad of threads holds 8 consecutive
             // columns of a row), release it, then transpose within each quad by shuffles
             // so that every thread stores 16 contiguous bytes: 8 rows x 64 bytes per store
@@ -1216,15 +1269,12 @@ size_t tc_scratch_bytes(const Problem &p)
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
     size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) +
                pad256(sizeof(float) * BH * p.L);
-    if (p.mode == MC_RESIDUAL)
-        b += pad256(BH * N * kTile);  // prefix sums of the states
-    else
-        b += pad256(sizeof(__nv_bfloat16) * BH * p.L * 64);  // gates
+    if (p.mode == MC_RESIDUAL) b += pad256(BH * N * kTile);  // prefix sums of the states
     return b;
 }
 
 // SSC router alone (mc_ssc_select) on the tensor-core path's shapes: key-mean
-// images, then the SSC gates kernel with only the router output enabled.
+// images, then the router kernel.
 size_t tc_select_scratch_bytes(const Problem &p) { return pad256((size_t)p.BH * kTile); }
 
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
@@ -1251,11 +1301,11 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
     if (e != cudaSuccess) return e;
     kbar_images_tc<<<(unsigned)(p.BH * p.N), kD, 0, s>>>(static_cast<const __nv_bfloat16 *>(fa.k), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gates_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
+    e = cudaFuncSetAttribute(ssc_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
     if (e != cudaSuccess) return e;
     const int gtiles = p.BH * (p.L / kCT);
     const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
-    gates_tc<true><<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
+    ssc_router_tc<<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
     return cudaGetLastError();
 }
 
@@ -1278,7 +1328,6 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
-    a.gam = gated ? reinterpret_cast<uint32_t *>(base) : nullptr;
     a.sel_out = fa.sel_out;
     a.topk = p.topk;
     a.BH = p.BH;
@@ -1334,24 +1383,17 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         prefix_images<<<grid, 256, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "prefix_images");
-    } else {
-        auto kg = p.mode == MC_SSC ? gates_tc<true> : gates_tc<false>;
-        e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatesSmem);
-        if (e != cudaSuccess) return e;
-        const int gtiles = (int)(BH * (p.L / kCT));
-        const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
-        kg<<<ggrid, kGatesThreads, kGatesSmem, s>>>(mU, a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        profile_after_kernel(s, "gates_tc");
     }
     {
-        auto k2 = gated ? (decay ? readout_tc<true, true> : readout_tc<true, false>)
-                        : (decay ? readout_tc<false, true> : readout_tc<false, false>);
+        const bool ssc = p.mode == MC_SSC;
+        auto k2 = !gated ? (decay ? readout_tc<false, true, false> : readout_tc<false, false, false>)
+                  : ssc  ? (decay ? readout_tc<true, true, true> : readout_tc<true, false, true>)
+                         : (decay ? readout_tc<true, true, false> : readout_tc<true, false, false>);
         e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);
         if (e != cudaSuccess) return e;
         const int slots = kT2CtasPerSm * g_num_sms;
         const int grid = a.num_tiles < slots ? a.num_tiles : slots;
-        k2<<<grid, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, a);
+        k2<<<grid, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, mU, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "readout_tc");
     }

@@ -28,8 +28,9 @@ def test_algorithmic_flops_modes():
     s, n = bench.segment_counts(w)
     assert max(n) == w.topk and n[0] == 0
     r = bench.algorithmic_flops(w.with_(mode=mc_inputs.RESIDUAL))
-    assert r["readout"] == 0 and r["total"] == r["online"]
-    assert f["total"] > r["total"]
+    online_read = w.B * w.H * w.L * 2 * w.d ** 2  # M_t q_t per token
+    assert r["readout"] == online_read and r["total"] == r["online"] == r["state"] + r["readout"]
+    assert f["total"] == f["state"] + f["readout"] > r["total"]
 
 
 def _free_port():
