@@ -13,7 +13,7 @@
  * compressed from a zero memory with M <- M + v_t k_t^T ([MC-ja §3 eq. 4b]) and
  * its final d x d state is cached.  Token t of segment s reads the online memory
  * M_t^(s) (after its own update) and every cached memory at q_t, and combines
- * them with one of four aggregations:
+ * them with one of five aggregations:
  *   MC_RESIDUAL  y_t = M_t^(s) q_t + sum_{i<s} M^(i) q_t                [MC-ja §3.1 eq. 7]
  *   MC_GRM       y_t = g_{t,s} M_t^(s) q_t + sum_{i<s} g_{t,i} M^(i) q_t,
  *                g_t = softmax_i <u_t, mean of segment i's keys>, the current
@@ -23,6 +23,11 @@
  *   MC_SSC       R_t = the topk largest <u_t, pool_i>, i<s (fp32 scores, equal
  *                scores to the lower i); softmax over R_t and the online score;
  *                y_t = g_{t,s} M_t^(s) q_t + sum_{i in R_t} g_{t,i} M^(i) q_t   [MC-sum §3.4]
+ *   MC_MEAN      y_t = (M_t^(s) q_t + sum_{i<s} M^(i) q_t) / (s + 1): memory caching
+ *                added after training, an average over the memories with no
+ *                learned weights (u is not read and may be NULL) [MC-ja, variants
+ *                appendix after eq. 35, "memory caching as post-training"]; equal to
+ *                GRM with u = 0
  * There is no 1/Z normaliser and no softmax temperature.
  *
  * Conventions for every entry point:
@@ -59,7 +64,8 @@ typedef enum {
     MC_RESIDUAL = 0,
     MC_GRM = 1,
     MC_SOUP = 2,
-    MC_SSC = 3
+    MC_SSC = 3,
+    MC_MEAN = 4
 } mc_agg_mode;
 
 enum {
@@ -78,7 +84,7 @@ enum {
 
 /*
  * mc_forward -- MC forward, bf16 inputs and output, fp32 state and accumulation.
- *   q, k, v, u : bf16 [B][H][L][d], read only.  u may be NULL for MC_RESIDUAL.
+ *   q, k, v, u : bf16 [B][H][L][d], read only.  u may be NULL for MC_RESIDUAL and MC_MEAN.
  *   seg_len    : constant segment length C; N = ceil(L / C).
  *   agg_mode   : an mc_agg_mode value.
  *   topk       : cached segments each token selects (MC_SSC only; ignored otherwise).

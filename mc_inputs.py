@@ -21,8 +21,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-RESIDUAL, GRM, SOUP, SSC = 0, 1, 2, 3
-MODE_NAMES = {RESIDUAL: "residual", GRM: "grm", SOUP: "soup", SSC: "ssc"}
+RESIDUAL, GRM, SOUP, SSC, MEAN = 0, 1, 2, 3, 4
+MODE_NAMES = {RESIDUAL: "residual", GRM: "grm", SOUP: "soup", SSC: "ssc", MEAN: "mean"}
 
 
 @dataclass(frozen=True)

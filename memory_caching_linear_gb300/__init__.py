@@ -9,7 +9,7 @@ device is not an sm_103a GPU, calls raise.
     y, states = mc_forward(q, k, v, u, seg_len, MC_GRM)
 
 q, k, v, u are CUDA tensors [B, H, L, d] (bf16 -> ``mc_forward``; fp32 ->
-``mc_forward_f32``).  Aggregations: MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC.
+``mc_forward_f32``).  Aggregations: MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC, MC_MEAN.
 """
 from __future__ import annotations
 
@@ -18,7 +18,7 @@ import os
 
 import torch
 
-MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC = 0, 1, 2, 3
+MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC, MC_MEAN = 0, 1, 2, 3, 4
 MC_OK = 0
 MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9

@@ -13,7 +13,8 @@
 //   pool:    p_t = (sum_{j=t0..t} k_j) / (t - t0 + 1)              [MC-ja §3.1, eq. 10]
 //   scores:  r_i = <u_t, kbar_i> (i < s), r_s = <u_t, p_t>         [MC-ja §3.1, eq. 10]
 //   gates:   GRM / Soup softmax over r_0..r_s; SSC the topk largest cached scores
-//            (ties to the lower index) and the online one; Residual all 1
+//            (ties to the lower index) and the online one; Residual all 1; Mean
+//            all 1 / (s + 1) (memory caching added after training, no router)
 //                                                                   [MC-ja §3.1 eq. 7-10; MC-sum §3.3-3.4]
 //   read:    y_t = g_s M_t^(s) q_t + sum_{i<s} g_i M^(i) q_t        [MC-ja §3.1, eq. 9]
 //   at t = t0 + C - 1: M^(s) = M_t^(s), kbar_s = p_t               [MC-ja §3, after eq. 4b]
@@ -64,13 +65,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_gates(DecodeArgs a)
     __syncthreads();
     float *gout = a.gates + (size_t)bh * kDecGateWords;
     int *gidx = reinterpret_cast<int *>(gout + 64);
-    if (a.mode == MC_RESIDUAL) {
+    if (a.mode == MC_RESIDUAL || a.mode == MC_MEAN) {
+        const float w = a.mode == MC_MEAN ? 1.f / (float)(s + 1) : 1.f;
         for (int i = tid; i < s; i += kDecThreads) {
-            gout[i] = 1.f;
+            gout[i] = w;
             gidx[i] = i;
         }
         if (tid == 0) {
-            gout[128] = 1.f;
+            gout[128] = w;
             gidx[65] = s;
         }
         return;

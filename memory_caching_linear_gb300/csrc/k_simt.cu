@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(D) kbar_simt(FwdArgs a)
 //   GRM / Soup: g_t = softmax over {<u_t,kbar_i>}_{i<n} and r_on[t]   [MC-ja §3.1 eq. 9-10]
 //   SSC:        the top-k cached scores plus r_on[t], softmax over those [MC-sum §3.4]
 //   Residual:   g = 1                                                 [MC-ja §3.1 eq. 7]
+//   Mean:       g = 1 / (n + 1), the post-training form (no router)
 //   y_t = g_{t,n} O_on[t] + sum_{i<n} g_{t,i} M^(i) q_t
 // Soup is computed as GRM: for a linear memory the parameter average read at q_t
 // is the gated sum of the reads ([MC-sum §3.3]).
@@ -227,7 +228,8 @@ __global__ void __launch_bounds__(kThreads) readout_simt(FwdArgs a)
     const int cnt = te - tb;
     const int n = seg;  // cached segments 0..n-1
     const int mode = a.mode;
-    const bool gated = mode != MC_RESIDUAL;
+    const bool gated = mode_uses_u(mode);
+    const float wmean = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;  // Residual / Mean weight
 
     const size_t base = (size_t)bh * a.L * D;
     const T *q = static_cast<const T *>(a.q) + base;
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) readout_simt(FwdArgs a)
     // Per-token gate normalisation.
     if (tid < kTR) {
         const int t = tid;
-        float go = 1.f;
+        float go = wmean;
         if (t < cnt && gated) {
             const float ron = a.r_on[(size_t)bh * a.L + tb + t];
             const float *ur = Us + t * P;
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) readout_simt(FwdArgs a)
             const int t = tid;
             if (t < cnt) {
                 if (!gated) {
-                    gi = 1.f;
+                    gi = wmean;
                 } else if (mode == MC_SSC) {
                     const int c = cur[t];
                     if (c < nsel[t] && seli[t * kMaxTopk + c] == i) {

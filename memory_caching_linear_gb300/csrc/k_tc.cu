@@ -1,7 +1,8 @@
 // k_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) path of the Memory Caching
 // forward for bf16 inputs, d = 64 or 128 (tiles are 128 wide; a 64-wide tensor
 // is zero-padded by the TMA's out-of-bounds fill), seg_len a multiple of 128, L a
-// multiple of seg_len, N <= 64, aggregations Residual / GRM / Soup / SSC (topk <= 16).
+// multiple of seg_len, N <= 64, aggregations Residual / GRM / Soup / SSC (topk <= 16) /
+// Mean.
 //
 // Pages cited:
 //   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
@@ -27,7 +28,7 @@
 //     y_t = g_{t,n} [ S_pre(c) q_t + sum_{j in chunk, j<=t} v_j (k_j . q_t) ]
 //         + sum_{i<n} g_{t,i} M^(i) q_t                      ([MC-ja §3.1 eq. 9])
 //   (Residual: g = 1, [MC-ja §3.1 eq. 7], where the cached sum collapses to one
-//   prefix state) as MMAs into one fp32 accumulator D per CTA:
+//   prefix state; Mean: the same with g = 1 / (n + 1)) as MMAs into one fp32 accumulator D per CTA:
 //     G = Q K_c^T;  D = (g_n * mask(G)) V_c;  D += (g_i o Q) X_i^T
 //   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.  The gates come from the
 //   scores <u_t, kbar_i> (two MMAs per tile: kbar as hi and lo rows) and r_on[t]:
@@ -69,6 +70,7 @@ struct TcArgs {
     float *r_on;          // [BH][L]
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
+    int mean;             // Mean aggregation: the Residual path with every weight 1 / (n + 1)
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
     int BH, L, C, N, CPS;
     int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
@@ -1015,7 +1017,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         for (int j = 0; j < my_tiles && ok; ++j) {
             const TileInfo t = decode_tile(a, tile_id(j));
             const int items = tile_items<GATED>(t);
-            float gn = 1.f;
+            float gn = a.mean ? 1.f / (float)(t.n + 1) : 1.f;  // Residual: 1
             if (GATED) {
                 // the token's gates from the scores S in this tile's first A slot
                 g += 4;  // the U and key-mean panels, released by the issuer
@@ -1150,14 +1152,14 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             const __nv_bfloat16 *gl = reinterpret_cast<const __nv_bfloat16 *>(gm2);
 #pragma unroll 1
             for (int k = 0; k < items; ++k) {
-                __nv_bfloat162 gam2 = __float2bfloat162_rn(1.f);
+                __nv_bfloat162 gam2 = __float2bfloat162_rn(gn);  // Residual: 1, Mean: 1 / (n + 1)
                 const bool prefix = t.c > 0 && k == 0;  // item 0 of a chunk c > 0 is its prefix state (gate g_n)
                 if (GATED) {
                     const int i = t.c > 0 ? k - 1 : k;
                     gam2 = __bfloat162bfloat162(i < 0 ? gl[63] : gl[i]);
                 }
                 if (DECAY && prefix) gam2 = __float2bfloat162_rn(gn * __expf(ellt));  // A(t_c, t) S^_c q_t
-                const bool scale = GATED || (DECAY && prefix);
+                const bool scale = GATED || (DECAY && prefix) || a.mean;
                 if (!(ok = claim())) break;
                 const uint32_t ta = tA0 + (ac % 2) * 64 + lane_base;
 #pragma unroll
@@ -1261,7 +1263,7 @@ bool tc_supported(const Problem &p)
 {
     return p.bf16 && (p.d == kD || p.d == 64) && p.C % kCT == 0 && p.L % p.C == 0 && p.N <= 64 &&
            (p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_RESIDUAL ||
-            (p.mode == MC_SSC && p.topk >= 0 && p.topk <= kTcMaxTopk));
+            p.mode == MC_MEAN || (p.mode == MC_SSC && p.topk >= 0 && p.topk <= kTcMaxTopk));
 }
 
 size_t tc_scratch_bytes(const Problem &p)
@@ -1269,7 +1271,7 @@ size_t tc_scratch_bytes(const Problem &p)
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
     size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) +
                pad256(sizeof(float) * BH * p.L);
-    if (p.mode == MC_RESIDUAL) b += pad256(BH * N * kTile);  // prefix sums of the states
+    if (!mode_uses_u(p.mode)) b += pad256(BH * N * kTile);  // prefix sums of the states
     return b;
 }
 
@@ -1311,7 +1313,7 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
 
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
 {
-    const bool gated = p.mode != MC_RESIDUAL;
+    const bool gated = mode_uses_u(p.mode);
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
     uint8_t *base = static_cast<uint8_t *>(scratch);
     TcArgs a{};
@@ -1330,6 +1332,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.prefix_img = gated ? nullptr : base;
     a.sel_out = fa.sel_out;
     a.topk = p.topk;
+    a.mean = p.mode == MC_MEAN;
     a.BH = p.BH;
     a.L = p.L;
     a.C = p.C;

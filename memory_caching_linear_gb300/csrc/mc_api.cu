@@ -137,9 +137,9 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
 {
     int st = check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
     if (!q || !k || !v || !y) return MC_ERR_NULL;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (mode_uses_u(agg_mode) && !u) return MC_ERR_NULL;
     if (swla && (!alpha || !beta || !lam)) return MC_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y) || (u && !aligned16(u)) ||
         (states && !aligned16(states)) || (swla && (!aligned16(alpha) || !aligned16(beta) || !aligned16(lam))))
@@ -170,7 +170,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         }
         FwdArgs a{};
         a.q = q; a.k = k; a.v = v;
-        a.u = p.mode == MC_RESIDUAL ? nullptr : u;
+        a.u = mode_uses_u(p.mode) ? u : nullptr;
         a.y = y;
         a.states = states ? states : static_cast<float *>(scratch);
         a.alpha = swla ? alpha : nullptr;
@@ -195,7 +195,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     char *base = static_cast<char *>(scratch);
     FwdArgs a{};
     a.q = q; a.k = k; a.v = v;
-    a.u = p.mode == MC_RESIDUAL ? nullptr : u;
+    a.u = mode_uses_u(p.mode) ? u : nullptr;
     a.y = y;
     a.states = states ? states : reinterpret_cast<float *>(base + plan.off_states);
     a.O_on = reinterpret_cast<float *>(base + plan.off_O);
@@ -253,10 +253,10 @@ int mc_decode_step(const void *q, const void *k, const void *v, const void *u, i
     int st = mc::check_shape(B, H, 1, d, seg_len);
     if (st != MC_OK) return st;
     if (t < 0 || n_max < 1 || n_max > mc::kDecMaxN - 1 || t / seg_len >= n_max) return MC_ERR_SHAPE;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
     if (agg_mode == MC_SSC && topk < 0) return MC_ERR_TOPK;
     if (!q || !k || !v || !y || !states || !kbar || !online || !ksum) return MC_ERR_NULL;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (mc::mode_uses_u(agg_mode) && !u) return MC_ERR_NULL;
     if (!mc::aligned16(q) || !mc::aligned16(k) || !mc::aligned16(v) || !mc::aligned16(y) || (u && !mc::aligned16(u)) ||
         !mc::aligned16(states) || !mc::aligned16(kbar) || !mc::aligned16(online) || !mc::aligned16(ksum))
         return MC_ERR_ALIGN;
@@ -264,7 +264,7 @@ int mc_decode_step(const void *q, const void *k, const void *v, const void *u, i
     if (st != MC_OK) return st;
     mc::DecodeArgs a{};
     a.q = q; a.k = k; a.v = v;
-    a.u = agg_mode == MC_RESIDUAL ? nullptr : u;
+    a.u = mc::mode_uses_u(agg_mode) ? u : nullptr;
     a.y = y;
     a.states = states; a.kbar = kbar; a.online = online; a.ksum = ksum;
     a.BH = B * H; a.d = d; a.C = seg_len; a.mode = agg_mode == MC_SOUP ? MC_GRM : agg_mode;
@@ -344,9 +344,9 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int st = mc::check_shape(B, H, L, d, seg_len);
     if (st != MC_OK) return st;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
     if (!q || !k || !v || !y) return MC_ERR_NULL;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (mc::mode_uses_u(agg_mode) && !u) return MC_ERR_NULL;
     st = mc::check_device();
     if (st != MC_OK) return st;
     const size_t elt = is_bf16 ? 2 : 4;
@@ -354,7 +354,7 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
     const size_t N = ((size_t)L + seg_len - 1) / seg_len;
     const size_t bytes_in = mc::round_up(n_in * elt);
     const size_t bytes_states = states ? mc::round_up(sizeof(float) * (size_t)B * H * N * d * d) : 0;
-    const int nin = u && agg_mode != MC_RESIDUAL ? 4 : 3;
+    const int nin = u && mc::mode_uses_u(agg_mode) ? 4 : 3;
     void *dmem = nullptr;
     if (mc::scratch_alloc(&dmem, bytes_in * (nin + 1) + bytes_states, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -496,7 +496,7 @@ const char *mc_status_string(int status)
     case MC_OK: return "ok";
     case MC_ERR_NULL: return "a required pointer is NULL";
     case MC_ERR_SHAPE: return "unsupported shape (B,H,L,seg_len >= 1; d in {16,32,64,128}; sizes within limits)";
-    case MC_ERR_MODE: return "agg_mode must be MC_RESIDUAL, MC_GRM, MC_SOUP or MC_SSC";
+    case MC_ERR_MODE: return "agg_mode must be MC_RESIDUAL, MC_GRM, MC_SOUP, MC_SSC or MC_MEAN";
     case MC_ERR_TOPK: return "SSC topk out of range (0..64, or >= N-1 for all segments)";
     case MC_ERR_ALLOC: return "stream-ordered scratch allocation failed";
     case MC_ERR_CUDA: return "a CUDA call or kernel launch failed";

@@ -22,6 +22,10 @@ namespace mc {
 
 constexpr int kMaxTopk = 64;  // SSC selections kept per token on the device
 
+// Aggregations whose gates come from the router <u_t, pooled keys>; Residual and
+// Mean weigh every memory the same and never read u.
+__host__ __device__ inline bool mode_uses_u(int mode) { return mode == MC_GRM || mode == MC_SOUP || mode == MC_SSC; }
+
 struct Problem {
     int B, H, L, d, C, N, mode, topk;
     int BH;

@@ -67,9 +67,9 @@ extern "C" int mc_forward_noalloc(const void *q, const void *k, const void *v, c
     if (BH > (1ll << 24) || BH * L * d > (1ll << 40) || BH * N * d * d > (1ll << 40) ||
         BH * N * ((seg_len + 63) / 64) >= (1ll << 31))
         return MC_ERR_SHAPE;
-    if (agg_mode < MC_RESIDUAL || agg_mode > MC_SSC) return MC_ERR_MODE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
     if (!q || !k || !v || !y) return MC_ERR_NULL;
-    if (agg_mode != MC_RESIDUAL && !u) return MC_ERR_NULL;
+    if (mc::mode_uses_u(agg_mode) && !u) return MC_ERR_NULL;
     if (!al16(q) || !al16(k) || !al16(v) || !al16(y) || (u && !al16(u)) || (states && !al16(states)))
         return MC_ERR_ALIGN;
 
@@ -111,7 +111,7 @@ extern "C" int mc_forward_noalloc(const void *q, const void *k, const void *v, c
     // reads it, so nothing left by an earlier call needs clearing.
     mc::FwdArgs a{};
     a.q = q; a.k = k; a.v = v;
-    a.u = p.mode == MC_RESIDUAL ? nullptr : u;
+    a.u = mc::mode_uses_u(p.mode) ? u : nullptr;
     a.y = y;
     a.states = states ? states : reinterpret_cast<float *>(base);
     a.O_on = reinterpret_cast<float *>(base + b_states);

@@ -10,7 +10,7 @@ Functions
 ---------
 forward(q, k, v, u, seg_len, mode, topk=0, ...)
     State form, literal: cached segment states, online state after the token's
-    update, key mean-pool gates, Residual / GRM / Soup / SSC aggregation.
+    update, key mean-pool gates, Residual / GRM / Soup / SSC / Mean aggregation.
 bruteforce(q, k, v, u, seg_len, mode, topk=0)
     Token-level twin that never forms a memory matrix (tiny inputs only).
 
@@ -30,7 +30,7 @@ import threading
 
 import numpy as np
 
-RESIDUAL, GRM, SOUP, SSC = 0, 1, 2, 3
+RESIDUAL, GRM, SOUP, SSC, MEAN = 0, 1, 2, 3, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mc_oracle.c")
@@ -112,7 +112,7 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
     """
     lib = _load()
     q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
-    if u.size == 0 and mode == RESIDUAL:
+    if u.size == 0 and mode in (RESIDUAL, MEAN):
         u = np.zeros_like(q)
     B, H, L, d = q.shape
     for a in (k, v, u):

@@ -35,12 +35,18 @@
  *             gamma_t = softmax over {r_{t,i} : i in R_t} and r_{t,s},
  *             y_t = gamma_{t,s} M_t^(s) q_t + sum_{i in R_t} gamma_{t,i} M^(i) q_t
  *                                                                        [MC-sum §3.4]
+ *   Mean:     memory caching added to a model after training: the memories
+ *             are averaged with no learned weights,
+ *             y_t = (M_t^(s) q_t + sum_{i<s} M^(i) q_t) / (s + 1)
+ *                          [MC-ja, variants appendix after eq. 35, post-training MC]
  * Readings where the pages are silent (each one is listed in the design notes):
  *   - phi = identity and no 1/Z normaliser (unnormalised linear attention, [MC-ja §2]);
  *   - the pooled summary pools keys (the gate needs a vector in the key space);
  *   - softmax has no temperature; the last segment may be shorter than C;
  *   - SSC ranks on the scores rounded to fp32 (the precision the router is
- *     specified in), equal fp32 scores going to the lower segment index.
+ *     specified in), equal fp32 scores going to the lower segment index;
+ *   - Mean averages the online memory together with the cached ones, each with
+ *     weight 1 / (s + 1).
  *
  * Sliding-window linear attention with c = 2 under memory caching (SWLA, the
  * second memory family the pages cache) replaces the update rule by
@@ -62,7 +68,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { OR_RESIDUAL = 0, OR_GRM = 1, OR_SOUP = 2, OR_SSC = 3 };
+enum { OR_RESIDUAL = 0, OR_GRM = 1, OR_SOUP = 2, OR_SSC = 3, OR_MEAN = 4 };
 
 enum {
     OR_OK = 0,
@@ -228,6 +234,12 @@ static int head_forward(const head_job *J)
                 for (int i = 0; i < s; ++i) add_matvec(yt, 1.0, J->states + (size_t)i * dd, qt, d);
                 continue;
             }
+            if (J->mode == OR_MEAN) { /* the average of the s + 1 memories, read at q_t */
+                const double w = 1.0 / (double)(s + 1);
+                add_matvec(yt, w, Mon, qt, d);
+                for (int i = 0; i < s; ++i) add_matvec(yt, w, J->states + (size_t)i * dd, qt, d);
+                continue;
+            }
 
             for (int i = 0; i < s; ++i) r[i] = dot(ut, kbar + (size_t)i * d, d);
             r[s] = dot(ut, ksum, d) / cnt;
@@ -326,6 +338,8 @@ static int head_bruteforce(const head_job *J)
         for (int i = 0; i <= s; ++i) w[i] = 0.0;
         if (J->mode == OR_RESIDUAL) {
             for (int i = 0; i <= s; ++i) w[i] = 1.0;
+        } else if (J->mode == OR_MEAN) {
+            for (int i = 0; i <= s; ++i) w[i] = 1.0 / (double)(s + 1);
         } else if (J->mode == OR_GRM || J->mode == OR_SOUP) {
             double m = r[0];
             for (int i = 1; i <= s; ++i) m = r[i] > m ? r[i] : m;
@@ -436,7 +450,7 @@ static int run_pool(pool_ctx *P, int nthreads)
 static int check_args(int BH, int L, int d, int C, int mode, int topk)
 {
     if (BH <= 0 || L <= 0 || d <= 0 || C <= 0) return OR_ERR_ARG;
-    if (mode < OR_RESIDUAL || mode > OR_SSC) return OR_ERR_ARG;
+    if (mode < OR_RESIDUAL || mode > OR_MEAN) return OR_ERR_ARG;
     if (mode == OR_SSC && topk < 0) return OR_ERR_ARG;
     return OR_OK;
 }

@@ -68,6 +68,8 @@ def test_argument_errors_never_reach_the_device(lib):
     assert _fwd(lib, q=None) == mcl.MC_ERR_NULL
     assert _fwd(lib, y=None) == mcl.MC_ERR_NULL
     assert _fwd(lib, u=None, mode=mcl.MC_GRM) == mcl.MC_ERR_NULL
+    for mode in (mcl.MC_RESIDUAL, mcl.MC_MEAN):  # no router input needed: the call gets past the checks
+        assert _fwd(lib, u=None, mode=mode) not in (mcl.MC_ERR_NULL, mcl.MC_ERR_MODE)
     assert _fwd(lib, mode=7) == mcl.MC_ERR_MODE
     assert _fwd(lib, mode=-1) == mcl.MC_ERR_MODE
     for bad in (dict(d=17), dict(d=256), dict(L=0), dict(B=0), dict(H=-1), dict(seg=0)):
@@ -92,6 +94,7 @@ def test_argument_errors_never_reach_the_device(lib):
     assert dec(mode=9) == mcl.MC_ERR_MODE
     assert dec(q=None) == mcl.MC_ERR_NULL
     assert dec(u=None) == mcl.MC_ERR_NULL
+    assert dec(u=None, mode=mcl.MC_MEAN) not in (mcl.MC_ERR_NULL, mcl.MC_ERR_MODE)
     assert dec(q=FAKE + 4) == mcl.MC_ERR_ALIGN
 
 

@@ -13,7 +13,7 @@ import torch
 
 import memory_caching_linear_gb300 as mcl
 import oracle
-from mc_inputs import GRM, RESIDUAL, SOUP, SSC, make_inputs
+from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -30,24 +30,25 @@ def _lib():
 
 def decode_all(q, k, v, u, C, mode, topk, n_max):
     B, H, L, d = q.shape
-    qd, kd, vd, ud = (t.cuda() for t in (q, k, v, u))
+    qd, kd, vd, ud = (x.cuda() if x is not None else None for x in (q, k, v, u))
     cache = mcl.DecodeCache(B, H, d, C, n_max)
     ys = []
     for t in range(L):
-        tok = [x[:, :, t, :].contiguous() for x in (qd, kd, vd, ud)]
+        tok = [x[:, :, t, :].contiguous() if x is not None else None for x in (qd, kd, vd, ud)]
         ys.append(mcl.mc_decode_step(cache, *tok, mode, topk).float().cpu())
     torch.cuda.synchronize()
     assert mcl.mc_check_device() == mcl.MC_OK
     return torch.stack(ys, 2).numpy(), cache
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
 @pytest.mark.parametrize("d,C,L,dtype", [(64, 128, 512, "bf16"), (32, 48, 200, "f32"), (128, 256, 768, "bf16")])
 def test_decode_reproduces_the_forward(mode, topk, d, C, L, dtype):
     q, k, v, u = make_inputs(1, 2, L, d, 17 + d, dtype)
     N = (L + C - 1) // C
     ref = oracle.forward(q, k, v, u, C, mode, topk)
-    y, cache = decode_all(q, k, v, u, C, mode, topk, n_max=N + 1)
+    # the post-training average needs no router input
+    y, cache = decode_all(q, k, v, None if mode == MEAN else u, C, mode, topk, n_max=N + 1)
     keep = np.ones(y.shape[:3], bool)
     if mode == SSC:  # fp32 near-ties may rank either way
         keep = ref["gap"] >= GAP

@@ -22,7 +22,7 @@ import numpy as np
 import pytest
 
 import oracle
-from mc_inputs import GRM, RESIDUAL, SOUP, SSC, make_inputs
+from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -128,6 +128,19 @@ def test_grm_with_constant_gates(C):
     y = oracle.forward(q, k, v, u, C, GRM)["y"]
     ref = causal_la(q, k, v) / seg_number(80, C)[:, None]
     np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("C", [16, 5, 1, 80])
+def test_mean_is_linear_attention_over_the_memory_count(C):
+    """Memory caching added after training averages the s + 1 memories with equal
+    weights ([MC-ja, variants appendix, post-training MC]); for a linear memory their
+    sum is plain causal linear attention, so y_t = LA_t / (s_t + 1) whatever u is."""
+    q, k, v, u = _inputs(1, 2, 80, 8, 4)
+    y = oracle.forward(q, k, v, u, C, MEAN)["y"]
+    ref = causal_la(q, k, v) / seg_number(80, C)[:, None]
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+    y0 = oracle.forward(q, k, v, np.zeros((0,)), C, MEAN)["y"]  # u is not read
+    np.testing.assert_array_equal(y0, y)
 
 
 def test_one_token_segments_are_gated_attention():
@@ -247,7 +260,7 @@ def test_completed_segment_permutation():
         np.testing.assert_allclose(a[..., 16:, :], b[..., 16:, :], rtol=1e-11, atol=1e-12)
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (SSC, 0)])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (SSC, 0), (MEAN, 0)])
 @pytest.mark.parametrize("C", [16, 9, 1])
 def test_state_form_matches_token_level_twin(mode, topk, C):
     """The state form equals the same sum regrouped by token (the twin never forms a memory)."""
@@ -280,7 +293,7 @@ def _swla_scalars(B, H, L, seed, lo=0.5):
     return (rng.uniform(lo, 1.0, (B, H, L)), rng.uniform(0.0, 1.0, (B, H, L)), rng.uniform(0.0, 1.0, (B, H, L)))
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
 @pytest.mark.parametrize("C", [12, 5, 1])
 def test_swla_state_form_matches_token_level_twin(mode, topk, C):
     """The recurrence of eq. 28 and its unrolled per-token weights agree."""
@@ -376,6 +389,8 @@ _MUTATIONS = [
     ("ssc ties to higher index", r"if \(best < 0 \|\| fi > bv\) \{ /\* strict",
      "if (best < 0 || fi >= bv) { /* strict"),
     ("soup uses online twice", r"Mstar\[e\] \+= g\[i\] \* Mi\[e\];", "Mstar[e] += g[s] * Mi[e];"),
+    ("mean over the cached memories only", r"const double w = 1\.0 / \(double\)\(s \+ 1\);",
+     "const double w = 1.0 / (double)(s > 0 ? s : 1);"),
 ]
 
 
@@ -404,6 +419,7 @@ def _run_pins_against(libpath):
             lambda: test_ssc_ties_go_to_lower_index(),
             lambda: test_causality(GRM, 0),
             lambda: test_single_segment_is_plain_recurrent_model(GRM, 0),
+            lambda: test_mean_is_linear_attention_over_the_memory_count(5),
             test_swla_constant_decay_is_decayed_linear_attention,
             test_swla_zero_decay_is_a_two_token_window,
             lambda: test_swla_window_does_not_cross_segments(7),

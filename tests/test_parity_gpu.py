@@ -15,7 +15,7 @@ import torch
 
 import memory_caching_linear_gb300 as mcl
 import oracle
-from mc_inputs import GRM, GRM_D64, LONG_GRM, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, SWLA_LONG, TINY, make_inputs, \
+from mc_inputs import GRM, GRM_D64, LONG_GRM, MEAN, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, SWLA_LONG, TINY, make_inputs, \
     make_swla_scalars, workload_swla_scalars, \
     workload_inputs
 
@@ -86,7 +86,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 0), (SSC, 2), (SSC, 100)])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 0), (SSC, 2), (SSC, 100), (MEAN, 0)])
 @pytest.mark.parametrize("name,B,H,L,d,C,dtype", CASES, ids=[c[0] for c in CASES])
 def test_parity_small(name, B, H, L, d, C, dtype, mode, topk):
     q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype=dtype)
@@ -114,7 +114,7 @@ TC_CASES = [
 TC_SSC_CASES = TC_CASES[:2] + TC_CASES[-1:]
 
 
-@pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP])
+@pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP, MEAN])
 @pytest.mark.parametrize("name,B,H,L,d,C", TC_CASES, ids=[c[0] for c in TC_CASES])
 def test_parity_tensor_core_shapes(name, B, H, L, d, C, mode):
     q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype="bf16")
@@ -141,6 +141,21 @@ def test_parity_tensor_core_ssc(name, B, H, L, d, C, topk):
     yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL["bf16"])
     assert rel_err(y, yref) <= TOL["bf16"], (name, topk, rel_err(y, yref))
     assert rel_err(st, ref["states"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name,B,H,L,d,C,dtype", [("mean-tc", 1, 2, 2048, 128, 256, "bf16"),
+                                                  ("mean-ffma", 1, 2, 300, 32, 64, "f32")])
+def test_mean_needs_no_u(name, B, H, L, d, C, dtype):
+    """The post-training average reads no router input: u = NULL gives the same y, and
+    it equals GRM with u = 0 (equal gates) on the GPU too."""
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype=dtype)
+    y, st = run_gpu(q, k, v, None, C, MEAN)
+    y_u, _ = run_gpu(q, k, v, u, C, MEAN)
+    np.testing.assert_array_equal(y, y_u)
+    ref = oracle.forward(q, k, v, u, C, MEAN)
+    assert rel_err(y, ref["y"]) <= TOL[dtype]
+    y_g, _ = run_gpu(q, k, v, torch.zeros_like(u), C, GRM)
+    assert rel_err(y_g, ref["y"]) <= TOL[dtype]
 
 
 def test_tiny_workload_invariants_on_gpu():
@@ -208,7 +223,7 @@ def run_gpu_swla(q, k, v, u, sw, C, mode, topk=0):
     return y.float().cpu().numpy(), st.cpu().numpy()
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
 @pytest.mark.parametrize("name,B,H,L,d,C", SWLA_CASES, ids=[c[0] for c in SWLA_CASES])
 def test_parity_swla(name, B, H, L, d, C, mode, topk):
     """Memory caching over SWLA (c = 2) against the oracle's recurrence, element by element."""
