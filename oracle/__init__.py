@@ -13,6 +13,9 @@ forward(q, k, v, u, seg_len, mode, topk=0, ...)
     update, key mean-pool gates, Residual / GRM / Soup / SSC / Mean aggregation.
 bruteforce(q, k, v, u, seg_len, mode, topk=0)
     Token-level twin that never forms a memory matrix (tiny inputs only).
+backward(q, k, v, u, dy, seg_len, mode, topk=0)
+    Gradients dq, dk, dv, du of <y, dy> (plain linear memory), by the chain rule
+    through the forward's steps.
 
 Both take optional ``swla=(alpha, beta, lam)`` (arrays [B, H, L]): the sliding-
 window linear attention update with c = 2, M_t = alpha_t M_{t-1} + beta_t v_{t-1}
@@ -73,6 +76,8 @@ def _load():
             lib.mc_oracle_forward_swla.restype = i
             lib.mc_oracle_bruteforce_swla.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, i]
             lib.mc_oracle_bruteforce_swla.restype = i
+            lib.mc_oracle_backward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
+            lib.mc_oracle_backward.restype = i
             _lib = lib
     return _lib
 
@@ -175,3 +180,24 @@ def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: 
     if st != 0:
         raise RuntimeError(f"mc_oracle_bruteforce failed with status {st}")
     return y
+
+
+def backward(q, k, v, u, dy, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0) -> dict:
+    """Gradients of the forward for the upstream gradient ``dy`` of y (plain linear
+    memory): a dict with ``dq``, ``dk``, ``dv``, ``du`` [B,H,L,d] float64 (``du`` is
+    zero for Residual and Mean, which read no u)."""
+    lib = _load()
+    q, k, v, u, dy = (_as_f64(a) for a in (q, k, v, u, dy))
+    if u.size == 0 and mode in (RESIDUAL, MEAN):
+        u = np.zeros_like(q)
+    B, H, L, d = q.shape
+    for a in (k, v, u, dy):
+        if a.shape != q.shape:
+            raise ValueError("q, k, v, u, dy must share the shape [B, H, L, d]")
+    out = {n: np.zeros((B, H, L, d), np.float64) for n in ("dq", "dk", "dv", "du")}
+    st = lib.mc_oracle_backward(*[_ptr(a, ctypes.c_double) for a in (q, k, v, u, dy)], B * H, L, d, seg_len,
+                                mode, max(topk, 0), *[_ptr(out[n], ctypes.c_double) for n in ("dq", "dk", "dv", "du")],
+                                nthreads)
+    if st != 0:
+        raise RuntimeError(f"mc_oracle_backward failed with status {st}")
+    return out

@@ -1,6 +1,6 @@
 /*
  * mc_oracle.c -- plain fp64 CPU oracle for the Memory Caching (MC) forward pass
- * over a linear matrix-valued memory.
+ * over a linear matrix-valued memory, and for its gradient (the backward pass).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this file; only the test-suite, the smoke check and the benchmark's CPU
@@ -86,6 +86,8 @@ typedef struct {
     int32_t *sel; /* optional [L][topk], rank order, -1 padded */
     double *gap;  /* optional [L] */
     const double *alpha, *beta, *lam; /* SWLA scalars [L]; all NULL = plain linear memory */
+    const double *dy;                 /* backward: upstream gradient of y [L][d] */
+    double *dq, *dk, *dv, *du;        /* backward: gradients [L][d], written */
 } head_job;
 
 /*
@@ -382,13 +384,176 @@ static int head_bruteforce(const head_job *J)
     return OR_OK;
 }
 
+/*
+ * Gradient of the forward pass (plain linear memory) for an upstream gradient dy
+ * of y: the chain rule taken through the forward's own steps, token by token.
+ * With the aggregation y_t = g_on o_on + sum_c g_c o_c over the memories that take
+ * part (o = M q_t, the online memory M_t^(s) and the selected cached M^(i)):
+ *   dg = dy_t . o                                          (gate of each memory)
+ *   softmax:  dr = g (dg - sum g dg)      (GRM / Soup / SSC over the selected set;
+ *             the selection itself is piecewise constant and passes no gradient)
+ *   scores:   r_i = <u_t, kbar_i>, r_on = <u_t, ksum_t> / cnt
+ *             -> du_t, and d kbar_i += dr_i u_t, d k_j += dr_on u_t / cnt (j = t0..t)
+ *   reads:    dq_t = sum g M^T dy_t;  a read of M = sum_j v_j k_j^T with weight g passes
+ *             d v_j += g (k_j . q_t) dy_t,  d k_j += g (v_j . dy_t) q_t
+ * Residual (g = 1) and Mean (g = 1 / (s + 1)) have constant gates.  Soup is the same
+ * function as GRM for a linear memory (the parameter average read at q_t is the
+ * gated sum of the reads), so it takes the same derivative.  A cached memory's
+ * contributions are gathered per segment, G_i = sum_t g_{t,i} dy_t q_t^T, and
+ * spread over its tokens at the end (d v_j += G_i k_j, d k_j += G_i^T v_j), with the
+ * pooled key's gradient d kbar_i / |segment i|.
+ */
+static int head_backward(const head_job *J)
+{
+    const int L = J->L, d = J->d, C = J->C;
+    const int N = (L + C - 1) / C;
+    const size_t dd = (size_t)d * d;
+    const int gated = J->mode == OR_GRM || J->mode == OR_SOUP || J->mode == OR_SSC;
+
+    double *kbar = calloc((size_t)N * d, sizeof(double));
+    double *Mon = malloc(dd * sizeof(double));
+    double *ksum = malloc((size_t)d * sizeof(double));
+    double *r = malloc((size_t)(N + 1) * sizeof(double));
+    double *g = malloc((size_t)(N + 1) * sizeof(double));
+    double *dg = malloc((size_t)(N + 1) * sizeof(double));
+    double *o = malloc((size_t)d * sizeof(double));
+    double *G = calloc((size_t)N * dd, sizeof(double));
+    double *dkbar = calloc((size_t)N * d, sizeof(double));
+    double *states = calloc((size_t)N * dd, sizeof(double));
+    int *idx = malloc((size_t)(N + 1) * sizeof(int));
+    uint8_t *taken = malloc((size_t)(N + 1));
+    if (!kbar || !Mon || !ksum || !r || !g || !dg || !o || !G || !dkbar || !states || !idx || !taken) {
+        free(kbar); free(Mon); free(ksum); free(r); free(g); free(dg); free(o); free(G); free(dkbar);
+        free(states); free(idx); free(taken);
+        return OR_ERR_NOMEM;
+    }
+    memset(J->dq, 0, (size_t)L * d * sizeof(double));
+    memset(J->dk, 0, (size_t)L * d * sizeof(double));
+    memset(J->dv, 0, (size_t)L * d * sizeof(double));
+    memset(J->du, 0, (size_t)L * d * sizeof(double));
+
+    /* the forward's cached states and pooled keys */
+    for (int n = 0; n < N; ++n) {
+        double *M = states + (size_t)n * dd;
+        int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
+        for (int t = t0; t < t1; ++t) {
+            memory_step(J, M, t, t0);
+            for (int b = 0; b < d; ++b) kbar[(size_t)n * d + b] += J->k[(size_t)t * d + b];
+        }
+        for (int b = 0; b < d; ++b) kbar[(size_t)n * d + b] /= (double)(t1 - t0);
+    }
+
+    for (int s = 0; s < N; ++s) {
+        int t0 = s * C, t1 = t0 + C < L ? t0 + C : L;
+        memset(Mon, 0, dd * sizeof(double));
+        memset(ksum, 0, (size_t)d * sizeof(double));
+        for (int t = t0; t < t1; ++t) {
+            const double *qt = J->q + (size_t)t * d, *kt = J->k + (size_t)t * d;
+            const double *ut = J->u + (size_t)t * d, *dyt = J->dy + (size_t)t * d;
+            memory_step(J, Mon, t, t0);
+            for (int b = 0; b < d; ++b) ksum[b] += kt[b];
+            const double cnt = (double)(t - t0 + 1);
+
+            /* the memories that take part (idx[0..nsel)) and their gates g[0..nsel], online last */
+            int nsel = 0;
+            if (gated) {
+                for (int i = 0; i < s; ++i) r[i] = dot(ut, kbar + (size_t)i * d, d);
+                r[s] = dot(ut, ksum, d) / cnt;
+            }
+            if (J->mode == OR_SSC) {
+                double gp;
+                nsel = ssc_rank(r, s, J->topk, idx, taken, &gp);
+            } else {
+                for (int i = 0; i < s; ++i) idx[nsel++] = i;
+            }
+            if (gated) {
+                for (int c = 0; c < nsel; ++c) g[c] = r[idx[c]];
+                g[nsel] = r[s];
+                softmax(g, nsel + 1);
+            } else {
+                const double w = J->mode == OR_MEAN ? 1.0 / (double)(s + 1) : 1.0;
+                for (int c = 0; c <= nsel; ++c) g[c] = w;
+            }
+
+            /* gate gradients dg = dy_t . (M q_t) */
+            for (int c = 0; c <= nsel; ++c) {
+                const double *M = c < nsel ? states + (size_t)idx[c] * dd : Mon;
+                memset(o, 0, (size_t)d * sizeof(double));
+                add_matvec(o, 1.0, M, qt, d);
+                dg[c] = dot(dyt, o, d);
+            }
+            if (gated) { /* softmax, then the scores */
+                double sgd = 0.0;
+                for (int c = 0; c <= nsel; ++c) sgd += g[c] * dg[c];
+                double *dut = J->du + (size_t)t * d;
+                for (int c = 0; c <= nsel; ++c) {
+                    const double dr = g[c] * (dg[c] - sgd);
+                    if (c < nsel) {
+                        const double *kb = kbar + (size_t)idx[c] * d;
+                        double *dkb = dkbar + (size_t)idx[c] * d;
+                        for (int b = 0; b < d; ++b) {
+                            dut[b] += dr * kb[b];
+                            dkb[b] += dr * ut[b];
+                        }
+                    } else {
+                        for (int b = 0; b < d; ++b) dut[b] += dr * ksum[b] / cnt;
+                        for (int j = t0; j <= t; ++j)
+                            for (int b = 0; b < d; ++b) J->dk[(size_t)j * d + b] += dr * ut[b] / cnt;
+                    }
+                }
+            }
+
+            /* the reads: dq_t, the online memory's tokens, and G of the cached memories */
+            double *dqt = J->dq + (size_t)t * d;
+            for (int c = 0; c <= nsel; ++c) {
+                const double *M = c < nsel ? states + (size_t)idx[c] * dd : Mon;
+                for (int a = 0; a < d; ++a)
+                    for (int b = 0; b < d; ++b) dqt[b] += g[c] * M[(size_t)a * d + b] * dyt[a];
+            }
+            for (int c = 0; c < nsel; ++c) {
+                double *Gi = G + (size_t)idx[c] * dd;
+                for (int a = 0; a < d; ++a)
+                    for (int b = 0; b < d; ++b) Gi[(size_t)a * d + b] += g[c] * dyt[a] * qt[b];
+            }
+            const double gon = g[nsel];
+            for (int j = t0; j <= t; ++j) {
+                const double *kj = J->k + (size_t)j * d, *vj = J->v + (size_t)j * d;
+                const double kq = dot(kj, qt, d), vdy = dot(vj, dyt, d);
+                for (int b = 0; b < d; ++b) {
+                    J->dv[(size_t)j * d + b] += gon * kq * dyt[b];
+                    J->dk[(size_t)j * d + b] += gon * vdy * qt[b];
+                }
+            }
+        }
+    }
+
+    /* spread each cached memory's gradient over its segment's tokens */
+    for (int n = 0; n < N; ++n) {
+        const double *Gn = G + (size_t)n * dd;
+        int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
+        for (int j = t0; j < t1; ++j) {
+            const double *kj = J->k + (size_t)j * d, *vj = J->v + (size_t)j * d;
+            double *dvj = J->dv + (size_t)j * d, *dkj = J->dk + (size_t)j * d;
+            for (int a = 0; a < d; ++a)
+                for (int b = 0; b < d; ++b) {
+                    dvj[a] += Gn[(size_t)a * d + b] * kj[b];
+                    dkj[b] += Gn[(size_t)a * d + b] * vj[a];
+                }
+            for (int b = 0; b < d; ++b) dkj[b] += dkbar[(size_t)n * d + b] / (double)(t1 - t0);
+        }
+    }
+    free(kbar); free(Mon); free(ksum); free(r); free(g); free(dg); free(o); free(G); free(dkbar);
+    free(states); free(idx); free(taken);
+    return OR_OK;
+}
+
 /* ---- threading over (batch, head) ---- */
 
 typedef struct {
     head_job base;
     int BH;
-    int brute;
-    int next; /* shared work counter */
+    int brute; /* 0 state form, 1 token-level twin, 2 backward */
+    int next;  /* shared work counter */
     int status;
     pthread_mutex_t mu;
 } pool_ctx;
@@ -409,12 +574,15 @@ static void *worker(void *arg)
         if (J.alpha) {
             J.alpha += (size_t)h * L; J.beta += (size_t)h * L; J.lam += (size_t)h * L;
         }
-        J.y += h * Ld;
+        if (J.y) J.y += h * Ld;
         if (J.states) J.states += h * Ndd;
         if (J.sel) J.sel += (size_t)h * L * J.topk;
         if (J.gap) J.gap += (size_t)h * L;
         if (J.given_sel) J.given_sel += (size_t)h * L * J.topk;
-        int st = P->brute ? head_bruteforce(&J) : head_forward(&J);
+        if (J.dy) {
+            J.dy += h * Ld; J.dq += h * Ld; J.dk += h * Ld; J.dv += h * Ld; J.du += h * Ld;
+        }
+        int st = P->brute == 2 ? head_backward(&J) : P->brute ? head_bruteforce(&J) : head_forward(&J);
         if (st != OR_OK) {
             pthread_mutex_lock(&P->mu);
             P->status = st;
@@ -474,7 +642,8 @@ int mc_oracle_forward(const double *q, const double *k, const double *v, const d
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
                         seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
-                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, NULL, NULL, NULL};
+                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, NULL, NULL, NULL,
+                        NULL, NULL, NULL, NULL, NULL};
     P.BH = BH;
     P.brute = 0;
     return run_pool(&P, nthreads);
@@ -494,7 +663,8 @@ int mc_oracle_forward_swla(const double *q, const double *k, const double *v, co
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
                         seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
-                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, alpha, beta, lam};
+                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, alpha, beta, lam,
+                        NULL, NULL, NULL, NULL, NULL};
     P.BH = BH;
     P.brute = 0;
     return run_pool(&P, nthreads);
@@ -510,7 +680,7 @@ int mc_oracle_bruteforce(const double *q, const double *k, const double *v, cons
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL};
+                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL};
     P.BH = BH;
     P.brute = 1;
     return run_pool(&P, nthreads);
@@ -527,8 +697,28 @@ int mc_oracle_bruteforce_swla(const double *q, const double *k, const double *v,
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, y, NULL, NULL, NULL, alpha, beta, lam};
+                        NULL, NULL, y, NULL, NULL, NULL, alpha, beta, lam, NULL, NULL, NULL, NULL, NULL};
     P.BH = BH;
     P.brute = 1;
+    return run_pool(&P, nthreads);
+}
+
+/*
+ * Gradients of the forward (plain linear memory) for the upstream gradient dy:
+ * dq, dk, dv, du [BH][L][d] are written (du is zero for Residual and Mean).
+ */
+int mc_oracle_backward(const double *q, const double *k, const double *v, const double *u, const double *dy,
+                       int BH, int L, int d, int C, int mode, int topk,
+                       double *dq, double *dk, double *dv, double *du, int nthreads)
+{
+    int st = check_args(BH, L, d, C, mode, topk);
+    if (st != OR_OK) return st;
+    if (!q || !k || !v || !u || !dy || !dq || !dk || !dv || !du) return OR_ERR_ARG;
+    pool_ctx P;
+    memset(&P, 0, sizeof(P));
+    P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
+                        NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, dy, dq, dk, dv, du};
+    P.BH = BH;
+    P.brute = 2;
     return run_pool(&P, nthreads);
 }
