@@ -125,6 +125,32 @@ int mc_forward_swla(const void *q, const void *k, const void *v, const void *u,
                     void *y, float *states, mc_stream_t stream);
 
 /*
+ * mc_backward -- gradients of the forward over the plain linear memory (the
+ * update M <- M + v k^T): for an upstream gradient dy of y, the gradients of
+ * <y, dy> with respect to q, k, v and u.  They follow the forward's steps by the
+ * chain rule: the gates' softmax ([MC-ja §3.1 eq. 9-10]), the pooled keys of the
+ * scores, the reads of the online and cached memories ([MC-ja §3 eq. 4b-5]) and,
+ * through the cached states M^(i) = sum v k^T, every token of a cached segment.
+ * The SSC selection ([MC-sum §3.4]) is piecewise constant and passes no
+ * gradient; Soup takes GRM's (the same function for a linear memory).
+ *   q, k, v, u, dy : bf16 [B][H][L][d], read only (u may be NULL for MC_RESIDUAL
+ *                    and MC_MEAN).
+ *   dq, dk, dv, du : bf16 [B][H][L][d], written (fp32 accumulation).  du may be
+ *                    NULL for MC_RESIDUAL and MC_MEAN (it is zero there); if
+ *                    given it is zeroed.
+ *   Other arguments and errors as mc_forward.  The call recomputes the forward's
+ *   segment states in scratch (about (2 N d^2 + 2 L d + 6 L) floats per (b, h)).
+ */
+int mc_backward(const void *q, const void *k, const void *v, const void *u, const void *dy,
+                int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                void *dq, void *dk, void *dv, void *du, mc_stream_t stream);
+
+/* mc_backward_f32 -- identical contract with fp32 inputs and gradients. */
+int mc_backward_f32(const float *q, const float *k, const float *v, const float *u, const float *dy,
+                    int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
+                    float *dq, float *dk, float *dv, float *du, mc_stream_t stream);
+
+/*
  * mc_decode_step -- one recurrent decoding step: the token at position t of each
  * of the B*H sequences (all at the same position) updates and reads the memory
  * caches, exactly as mc_forward treats token t ([MC-ja §3 eq. 4b-5, §3.1 eq.

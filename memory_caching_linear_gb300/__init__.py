@@ -24,7 +24,7 @@ MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
 MC_ERR_SCRATCH = -10
 
-EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_backward", "mc_backward_f32", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
             "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
             "mc_status_string")
 
@@ -54,6 +54,10 @@ def load_library():
     lib.mc_forward_f32.restype = i
     lib.mc_forward_swla.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
     lib.mc_forward_swla.restype = i
+    lib.mc_backward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
+    lib.mc_backward.restype = i
+    lib.mc_backward_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
+    lib.mc_backward_f32.restype = i
     lib.mc_decode_step.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, i, vp]
     lib.mc_decode_step.restype = i
     lib.mc_ssc_select.argtypes = [vp, vp, i, i, i, i, i, i, vp, i, vp]
@@ -211,6 +215,64 @@ def forward(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, **kw):
     if q.dtype == torch.float32:
         return mc_forward_f32(q, k, v, u, seg_len, agg_mode, topk, **kw)
     raise TypeError("inputs must be bf16 or fp32")
+
+
+def mc_backward(q, k, v, u, dy, seg_len: int, agg_mode: int, topk: int = 0, *, dq=None, dk=None, dv=None,
+                du=None, stream=None):
+    """Gradients (dq, dk, dv, du) of <y, dy> for the forward on the same inputs
+    (``mc_backward`` / ``mc_backward_f32`` in mc.h, chosen by the dtype).  du is None
+    for Residual and Mean unless a buffer is given (then it is zeroed)."""
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dev, dtype = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("inputs must be bf16 or fp32")
+    shape = (B, H, L, d)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dy, "dy")):
+        _check(t, n, dtype, shape, dev)
+    if u is not None:
+        _check(u, "u", dtype, shape, dev)
+    uses_u = agg_mode in (MC_GRM, MC_SOUP, MC_SSC)
+    out = []
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        t = torch.empty(shape, dtype=dtype, device=dev) if t is None else t
+        _check(t, n, dtype, shape, dev)
+        out.append(t)
+    if du is None and uses_u:
+        du = torch.empty(shape, dtype=dtype, device=dev)
+    if du is not None:
+        _check(du, "du", dtype, shape, dev)
+    fn = lib.mc_backward if dtype == torch.bfloat16 else lib.mc_backward_f32
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None, dy.data_ptr(),
+            B, H, L, d, int(seg_len), int(agg_mode), int(topk), *[t.data_ptr() for t in out],
+            du.data_ptr() if du is not None else None, _stream_handle(stream, dev))
+    if st != MC_OK:
+        raise MCError(st, "mc_backward")
+    return (*out, du)
+
+
+class MemoryCaching(torch.autograd.Function):
+    """Autograd wrapper: y = MemoryCaching.apply(q, k, v, u, seg_len, agg_mode, topk)
+    runs the library's forward and, on backward, ``mc_backward`` (u may be None for
+    Residual and Mean)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0):
+        y, _ = forward(q, k, v, u, seg_len, agg_mode, topk, want_states=False)
+        ctx.save_for_backward(q, k, v, u if u is not None else torch.empty(0, device=q.device))
+        ctx.cfg = (seg_len, agg_mode, topk, u is not None)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        q, k, v, u = ctx.saved_tensors
+        seg_len, agg_mode, topk, has_u = ctx.cfg
+        dq, dk, dv, du = mc_backward(q, k, v, u if has_u else None, dy.contiguous(), seg_len, agg_mode, topk)
+        return dq, dk, dv, (du if has_u else None), None, None, None
 
 
 def mc_check_device(stream=None) -> int:

@@ -218,10 +218,69 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     return MC_OK;
 }
 
+int backward_common(const void *q, const void *k, const void *v, const void *u, const void *dy, int B, int H, int L,
+                    int d, int seg_len, int agg_mode, int topk, void *dq, void *dk, void *dv, void *du, bool bf16,
+                    cudaStream_t stream)
+{
+    int st = check_shape(B, H, L, d, seg_len);
+    if (st != MC_OK) return st;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
+    const bool uses_u = mode_uses_u(agg_mode);
+    if (!q || !k || !v || !dy || !dq || !dk || !dv) return MC_ERR_NULL;
+    if (uses_u && (!u || !du)) return MC_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dy) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv) || (u && !aligned16(u)) || (du && !aligned16(du)))
+        return MC_ERR_ALIGN;
+    Problem p{};
+    p.B = B; p.H = H; p.L = L; p.d = d; p.C = seg_len;
+    p.N = (L + seg_len - 1) / seg_len;
+    p.BH = B * H;
+    p.bf16 = bf16;
+    p.mode = agg_mode == MC_SOUP ? MC_GRM : agg_mode;  // the same function for a linear memory
+    p.topk = agg_mode == MC_SSC ? topk : 0;
+    if (agg_mode == MC_SSC) {
+        if (topk < 0) return MC_ERR_TOPK;
+        if (topk >= p.N - 1) p.mode = MC_GRM;
+        else if (topk > kMaxTopk) return MC_ERR_TOPK;
+    }
+    if (p.mode != MC_SSC) p.topk = 0;
+    st = check_device();
+    if (st != MC_OK) return st;
+    void *scratch = nullptr;
+    if (scratch_alloc(&scratch, backward_scratch_bytes(p), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    cudaError_t e = cudaSuccess;
+    if (!uses_u && du) e = cudaMemsetAsync(du, 0, (size_t)p.BH * L * d * (bf16 ? 2 : 4), stream);
+    if (e == cudaSuccess) e = launch_backward_simt(p, q, k, v, uses_u ? u : nullptr, dy, dq, dk, dv, du, scratch, stream);
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
 }  // namespace
 }  // namespace mc
 
 extern "C" {
+
+int mc_backward(const void *q, const void *k, const void *v, const void *u, const void *dy, int B, int H, int L,
+                int d, int seg_len, int agg_mode, int topk, void *dq, void *dk, void *dv, void *du, mc_stream_t stream)
+{
+    return mc::backward_common(q, k, v, u, dy, B, H, L, d, seg_len, agg_mode, topk, dq, dk, dv, du, true,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mc_backward_f32(const float *q, const float *k, const float *v, const float *u, const float *dy, int B, int H,
+                    int L, int d, int seg_len, int agg_mode, int topk, float *dq, float *dk, float *dv, float *du,
+                    mc_stream_t stream)
+{
+    return mc::backward_common(q, k, v, u, dy, B, H, L, d, seg_len, agg_mode, topk, dq, dk, dv, du, false,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
 
 int mc_forward(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d, int seg_len,
                int agg_mode, int topk, void *y, float *states, mc_stream_t stream)

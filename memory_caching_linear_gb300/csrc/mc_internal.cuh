@@ -54,6 +54,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // Gate score <u_t, kbar_i> in fp32, summed in key order.  Every kernel that
 // needs a router score calls this one function, so the SSC ranking seen by
 // mc_ssc_select is bit-identical to the one the forward uses.
+// kb must be GLOBAL memory (it is read with __ldg); u_row may be shared or global.
 __device__ __forceinline__ float gate_score(const float *__restrict__ u_row, const float *__restrict__ kb, int d)
 {
     float acc = 0.f;
@@ -116,5 +117,28 @@ cudaError_t launch_seg_scan_simt(const Problem &p, const FwdArgs &a, cudaStream_
 cudaError_t launch_readout_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_kbar_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_ssc_select_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
+
+// Backward pass (k_bwd_simt.cu).  Inputs q, k, v, u, dy and outputs dq, dk, dv, du
+// are [BH][L][d] (element type per Problem::bf16); the rest is fp32 scratch.
+constexpr int kBwdTokWords = 5;  // per token: softmax max m, sum z, online gate, delta = sum g dg, pool weight w
+struct BwdArgs {
+    const void *q, *k, *v, *u, *dy;
+    void *dq, *dk, *dv, *du;
+    const float *states;  // [BH][N][d][d] cached states (recomputed forward)
+    const float *kbar;    // [BH][N][d]
+    const float *r_on;    // [BH][L]
+    const float *O_on;    // [BH][L][d]  M_t q_t (online read)
+    const float *X_on;    // [BH][L][d]  M_t^T dy_t
+    float *G;             // [BH][N][d][d]  sum_t g_{t,i} dy_t q_t^T per cached segment
+    float *dkbar;         // [BH][N][d]  gradient of the key means (accumulated)
+    float *tok;           // [BH][L][kBwdTokWords]
+    int32_t *sel_idx;     // SSC: [BH][L][topk] selected segments (segment order, -1 padded)
+    float *sel_g;         // SSC: [BH][L][topk] their gates
+    int BH, L, C, N, mode, topk;
+};
+size_t backward_scratch_bytes(const Problem &p);
+cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
+                                 const void *dy, void *dq, void *dk, void *dv, void *du, void *scratch,
+                                 cudaStream_t s);
 
 }  // namespace mc

@@ -1,0 +1,103 @@
+"""Parity of the backward pass (mc_backward / mc_backward_f32, through the C ABI)
+with the oracle's backward: the gradients dq, dk, dv, du of <y, dy>, element by
+element, at sizes that span several tiles and a ragged tail.
+
+Tolerance per gradient tensor: max|g - g_ref| <= 1e-4 * max|g_ref| for fp32
+inputs, <= 1e-2 * max|g_ref| for bf16 inputs and outputs (fp32 accumulation) --
+the forward's bounds.  SSC cases are chosen without fp32 near-ties in the router
+(the selection passes no gradient, so a flipped near-tie would change it).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import memory_caching_linear_gb300 as mcl
+import oracle
+from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+NAMES = ("dq", "dk", "dv", "du")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from memory_caching_linear_gb300 import build
+    build.build()
+    mcl.load_library()
+
+
+def rel_err(got, ref):
+    scale = np.abs(ref).max()
+    return float(np.abs(np.asarray(got, np.float64) - ref).max() / (scale if scale > 0 else 1.0))
+
+
+def _case(name, B, H, L, d, dtype):
+    seed = zlib.crc32(name.encode()) % 1000
+    q, k, v, u = make_inputs(B, H, L, d, seed=seed, dtype=dtype)
+    g = torch.Generator().manual_seed(seed + 7)
+    dy = torch.randn(B, H, L, d, generator=g).to(q.dtype)
+    return q, k, v, u, dy
+
+
+def run_backward(q, k, v, u, dy, C, mode, topk=0):
+    dev = torch.device("cuda")
+    out = mcl.mc_backward(*(t.to(dev) if t is not None else None for t in (q, k, v, u, dy)), C, mode, topk)
+    assert mcl.mc_check_device() == mcl.MC_OK
+    return {n: (t.float().cpu().numpy() if t is not None else None) for n, t in zip(NAMES, out)}
+
+
+CASES = [
+    # (name, B, H, L, d, C, dtype)
+    ("b-tiny", 1, 1, 256, 16, 64, "f32"),
+    ("b-N1", 1, 1, 200, 16, 256, "f32"),
+    ("b-ragged", 1, 2, 200, 32, 64, "f32"),
+    ("b-C1", 1, 1, 40, 16, 1, "f32"),
+    ("b-C37", 2, 1, 150, 64, 37, "f32"),
+    ("b-d128", 1, 1, 300, 128, 128, "f32"),
+    ("b-d64-bf16", 1, 2, 512, 64, 128, "bf16"),
+    ("b-d128-bf16", 1, 1, 777, 128, 256, "bf16"),
+]
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 0), (SSC, 2), (SSC, 100),
+                                       (MEAN, 0)])
+@pytest.mark.parametrize("name,B,H,L,d,C,dtype", CASES, ids=[c[0] for c in CASES])
+def test_backward_parity(name, B, H, L, d, C, dtype, mode, topk):
+    q, k, v, u, dy = _case(name, B, H, L, d, dtype)
+    if mode == SSC and 0 < topk < (L + C - 1) // C - 1:
+        gap = oracle.forward(q, k, v, u, C, SSC, topk)["gap"]
+        assert gap.min() >= 1e-5, "inputs with an fp32 near-tie in the router"
+    ref = oracle.backward(q, k, v, u, dy, C, mode, topk)
+    got = run_backward(q, k, v, u, dy, C, mode, topk)
+    for n in NAMES:
+        if got[n] is None:
+            assert mode in (RESIDUAL, MEAN)
+            continue
+        err = rel_err(got[n], ref[n])
+        assert err <= TOL[dtype], (name, mode, topk, n, err)
+        assert np.isfinite(got[n]).all()
+
+
+def test_backward_without_u_for_unrouted_modes():
+    q, k, v, u, dy = _case("b-nou", 1, 2, 300, 32, "f32")
+    for mode in (RESIDUAL, MEAN):
+        ref = oracle.backward(q, k, v, u, dy, 64, mode)
+        got = run_backward(q, k, v, None, dy, 64, mode)
+        assert got["du"] is None
+        for n in ("dq", "dk", "dv"):
+            assert rel_err(got[n], ref[n]) <= TOL["f32"], (mode, n)
+
+
+def test_autograd_wrapper_matches_the_entry_point():
+    dev = torch.device("cuda")
+    q, k, v, u, dy = (t.to(dev) for t in _case("b-autograd", 1, 2, 256, 64, "f32"))
+    leaves = [t.clone().requires_grad_(True) for t in (q, k, v, u)]
+    y = mcl.MemoryCaching.apply(*leaves, 64, GRM, 0)
+    grads = torch.autograd.grad(y, leaves, dy)
+    direct = mcl.mc_backward(q, k, v, u, dy, 64, GRM)
+    for a, b in zip(grads, direct):
+        torch.testing.assert_close(a, b, rtol=0, atol=0)
