@@ -457,6 +457,86 @@ def run_decode(args):
     }
 
 
+def backward_flops(w):
+    """Algorithmic work of the backward (all heads).  Per token and cached read: the
+    read's value M q (2 d^2, needed for the gate gradient and not kept by the
+    forward), dq (2 d^2) and the state gradient dy q^T (2 d^2); per token, twice the
+    online write + read (8 d^2); per token and score, the score gradients du and the
+    key-mean gradient (4 d).  The gate kernel's share: the cached M q and dq and the
+    score gradients."""
+    s, n = segment_counts(w)
+    bh = w.B * w.H
+    d = w.d
+    routed = w.mode not in (RESIDUAL, mc_inputs.MEAN)
+    score = 4 * d * sum(s) if routed else 0
+    total = bh * (6 * d * d * sum(n) + 8 * d * d * w.L + score)
+    gates = bh * (4 * d * d * sum(n) + score)
+    return {"total": total, "bwd_gates_simt": gates}
+
+
+def run_backward(args, w, wname):
+    """The backward pass (mc_backward) on a forward workload: gradients of <y, dy> for
+    seeded dy, inputs resident on the device; K timed steps with CUDA events."""
+    import torch
+    import memory_caching_linear_gb300 as mcl
+    from memory_caching_linear_gb300 import build as mcbuild
+    mcbuild.build()
+    mcl.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, u = mc_inputs.workload_inputs(w, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 101)
+    dy = torch.randn(q.shape, generator=g).to(device=dev, dtype=q.dtype)
+    grads = [torch.empty_like(q) for _ in range(4)]
+
+    def step():
+        mcl.mc_backward(q, k, v, u, dy, w.seg_len, w.mode, w.topk, dq=grads[0], dk=grads[1], dv=grads[2],
+                        du=grads[3])
+
+    sampler = ClockSampler(dev.index).start()
+    nwarm = max(args.warmup, 3)
+    for _ in range(nwarm):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = mcl.KernelProfile(capacity=args.steps * 8 + 8)
+    with prof:
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    per_kernel = prof.per_kernel_ms()
+    kernels_ms = {n: round(sum(t) / len(t) * (len(t) / args.steps), 4) for n, t in per_kernel.items()}
+    flops = backward_flops(w)
+    dom = "bwd_gates_simt"
+    dom_ms = kernels_ms.get(dom, 0.0)
+    peak = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3
+    achieved = flops[dom] / (dom_ms / 1e3) / 1e12 if dom_ms else 0.0
+    return {
+        "metric": f"tokens/sec MC-{mc_inputs.MODE_NAMES[w.mode].upper()} backward ({w.name})",
+        "value": round(w.tokens / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": nwarm, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (the forward workload's seeded inputs; dy ~ N(0, 1))",
+        "config": {"workload": f"bwd-{wname} {w.name}", "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len,
+                   "N": w.N, "agg": mc_inputs.MODE_NAMES[w.mode], "input_dtype": w.dtype,
+                   "l2": "inputs > L2 129 MB, not flushed"},
+        "algorithmic_tflop_per_step": round(flops["total"] / 1e12, 4),
+        "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom, "launch_ms": dom_ms,
+                     "algorithmic_tflop_per_launch": round(flops[dom] / 1e12, 4),
+                     "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"},
+        "kernels_ms": kernels_ms, "gpu_launches": prof.kernel_count() // max(args.steps, 1) * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, w):
@@ -497,7 +577,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["decode-grm"], default="long-grm")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["decode-grm"] + ["bwd-" + n for n in sorted(WORKLOADS)],
+                    default="long-grm")
     ap.add_argument("--mode", choices=["residual", "grm", "soup", "ssc"], default=None,
                     help="override the workload's aggregation")
     ap.add_argument("--warmup-seconds", type=float, default=1.0,
@@ -511,6 +592,11 @@ def main(argv=None):
     if args.workload == "decode-grm":
         if args.impl == "ours":
             print(json.dumps(run_decode(args)), flush=True)
+        return
+    if args.workload.startswith("bwd-"):
+        if args.impl == "ours":
+            name = args.workload[4:]
+            print(json.dumps(run_backward(args, WORKLOADS[name], name)), flush=True)
         return
     w = WORKLOADS[args.workload]
     if args.mode:
