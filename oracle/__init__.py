@@ -78,6 +78,10 @@ def _load():
             lib.mc_oracle_bruteforce_swla.restype = i
             lib.mc_oracle_backward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
             lib.mc_oracle_backward.restype = i
+            lib.mc_oracle_forward_segments.argtypes = [dp, dp, dp, dp, i, i, i, ip, i, i, i, ip, dp, dp, ip, dp, i]
+            lib.mc_oracle_forward_segments.restype = i
+            lib.mc_oracle_bruteforce_segments.argtypes = [dp, dp, dp, dp, i, i, i, ip, i, i, i, dp, i]
+            lib.mc_oracle_bruteforce_segments.restype = i
             _lib = lib
     return _lib
 
@@ -104,8 +108,26 @@ def _swla_args(swla, B, H, L):
     return alpha, beta, lam
 
 
+def log_segments(L: int) -> list:
+    """Logarithmic segmentation ([MC-sum §4.2]; the Log-Linear++ variant of [MC-ja]'s
+    variants appendix): L written in binary, one segment per set bit with that power of
+    two as its length, the longest first.  Returns the boundaries [0, ..., L]."""
+    off = [0]
+    for bit in reversed(range(L.bit_length())):
+        if (L >> bit) & 1:
+            off.append(off[-1] + (1 << bit))
+    return off
+
+
+def _seg_array(seg_off, L):
+    a = np.ascontiguousarray(np.asarray(seg_off, dtype=np.int32))
+    if a.ndim != 1 or len(a) < 2 or a[0] != 0 or a[-1] != L or np.any(np.diff(a) <= 0):
+        raise ValueError("seg_off must rise strictly from 0 to L")
+    return a
+
+
 def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
-            seg_mask=None, given_sel=None, nthreads: int = 0, swla=None) -> dict:
+            seg_mask=None, given_sel=None, nthreads: int = 0, swla=None, seg_off=None) -> dict:
     """Run the state-form oracle.
 
     Returns a dict with ``y`` [B,H,L,d] and ``states`` [B,H,N,d,d] (float64); for
@@ -113,7 +135,8 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
     [B,H,L] (fp64 distance between the last selected and the best unselected
     score; inf where nothing was left out).  ``seg_mask`` (length N, bool)
     restricts which segments' outputs are computed; ``given_sel`` replaces the
-    router's choice for SSC.
+    router's choice for SSC.  ``seg_off`` (boundaries [0, ..., L]) replaces the
+    constant segment length ``seg_len`` by given segments.
     """
     lib = _load()
     q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
@@ -123,7 +146,8 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
     for a in (k, v, u):
         if a.shape != q.shape:
             raise ValueError("q, k, v, u must share the shape [B, H, L, d]")
-    N = num_segments(L, seg_len)
+    so = _seg_array(seg_off, L) if seg_off is not None else None
+    N = len(so) - 1 if so is not None else num_segments(L, seg_len)
     y = np.zeros((B, H, L, d), np.float64)
     states = np.zeros((B, H, N, d, d), np.float64)
     sel = gap = None
@@ -146,7 +170,12 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
               _ptr(sel, ctypes.c_int32) if sel is not None else None,
               _ptr(gap, ctypes.c_double) if gap is not None else None, nthreads]
     qkvu = [_ptr(a, ctypes.c_double) for a in (q, k, v, u)]
-    if swla is None:
+    if so is not None:
+        if swla is not None or sm is not None:
+            raise ValueError("seg_off does not combine with swla or seg_mask")
+        st = lib.mc_oracle_forward_segments(*qkvu, B * H, L, d, _ptr(so, ctypes.c_int32), N, mode, kk,
+                                            *common[1:])
+    elif swla is None:
         st = lib.mc_oracle_forward(*qkvu, B * H, L, d, seg_len, mode, kk, *common)
     else:
         abl = _swla_args(swla, B, H, L)
@@ -162,14 +191,18 @@ def forward(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *,
 
 
 def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0,
-               swla=None) -> np.ndarray:
+               swla=None, seg_off=None) -> np.ndarray:
     """Token-level twin: y [B,H,L,d] without forming any memory matrix (O(L^2 d))."""
     lib = _load()
     q, k, v, u = (_as_f64(a) for a in (q, k, v, u))
     B, H, L, d = q.shape
     y = np.zeros((B, H, L, d), np.float64)
     qkvu = [_ptr(a, ctypes.c_double) for a in (q, k, v, u)]
-    if swla is None:
+    if seg_off is not None:
+        so = _seg_array(seg_off, L)
+        st = lib.mc_oracle_bruteforce_segments(*qkvu, B * H, L, d, _ptr(so, ctypes.c_int32), len(so) - 1, mode,
+                                               max(topk, 0), _ptr(y, ctypes.c_double), nthreads)
+    elif swla is None:
         st = lib.mc_oracle_bruteforce(*qkvu, B * H, L, d, seg_len, mode, max(topk, 0),
                                       _ptr(y, ctypes.c_double), nthreads)
     else:

@@ -88,7 +88,25 @@ typedef struct {
     const double *alpha, *beta, *lam; /* SWLA scalars [L]; all NULL = plain linear memory */
     const double *dy;                 /* backward: upstream gradient of y [L][d] */
     double *dq, *dk, *dv, *du;        /* backward: gradients [L][d], written */
+    const int32_t *seg_off;           /* optional: segment n = [seg_off[n], seg_off[n+1]), nseg of them */
+    int nseg;
 } head_job;
+
+/* Segments: constant length C (the last one may be shorter), or the given boundaries. */
+static int num_seg(const head_job *J) { return J->seg_off ? J->nseg : (J->L + J->C - 1) / J->C; }
+static int seg_lo(const head_job *J, int n) { return J->seg_off ? J->seg_off[n] : n * J->C; }
+static int seg_hi(const head_job *J, int n)
+{
+    if (J->seg_off) return J->seg_off[n + 1];
+    return (n + 1) * J->C < J->L ? (n + 1) * J->C : J->L;
+}
+static int seg_of(const head_job *J, int t)
+{
+    if (!J->seg_off) return t / J->C;
+    int n = 0;
+    while (J->seg_off[n + 1] <= t) ++n;
+    return n;
+}
 
 /*
  * One step of the segment memory at token t (segment start t0):
@@ -183,8 +201,8 @@ static int ssc_rank(const double *r, int ncached, int topk, int *idx, uint8_t *t
 /* State form, literal: eq. 4b per token, eq. 7/9/10 or the Soup / SSC formulas per token. */
 static int head_forward(const head_job *J)
 {
-    const int L = J->L, d = J->d, C = J->C;
-    const int N = (L + C - 1) / C;
+    const int d = J->d;
+    const int N = num_seg(J);
     const size_t dd = (size_t)d * d;
 
     double *kbar = calloc((size_t)N * d, sizeof(double));
@@ -205,7 +223,7 @@ static int head_forward(const head_job *J)
     memset(J->states, 0, (size_t)N * dd * sizeof(double));
     for (int n = 0; n < N; ++n) {
         double *M = J->states + (size_t)n * dd;
-        int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
+        int t0 = seg_lo(J, n), t1 = seg_hi(J, n);
         for (int t = t0; t < t1; ++t) {
             const double *kt = J->k + (size_t)t * d;
             memory_step(J, M, t, t0);
@@ -216,7 +234,7 @@ static int head_forward(const head_job *J)
 
     /* Step 2: per token, the online memory after its update, the scores, the aggregation. */
     for (int s = 0; s < N; ++s) {
-        int t0 = s * C, t1 = t0 + C < L ? t0 + C : L;
+        int t0 = seg_lo(J, s), t1 = seg_hi(J, s);
         int want_y = J->seg_mask == NULL || J->seg_mask[s] != 0;
         memset(Mon, 0, dd * sizeof(double));
         memset(ksum, 0, (size_t)d * sizeof(double));
@@ -314,8 +332,8 @@ static double token_weight(const head_job *J, int j, int t)
  */
 static int head_bruteforce(const head_job *J)
 {
-    const int L = J->L, d = J->d, C = J->C;
-    const int N = (L + C - 1) / C;
+    const int L = J->L, d = J->d;
+    const int N = num_seg(J);
     double *w = malloc((size_t)(N + 1) * sizeof(double));
     double *r = malloc((size_t)(N + 1) * sizeof(double));
     double *pool = malloc((size_t)d * sizeof(double));
@@ -325,11 +343,11 @@ static int head_bruteforce(const head_job *J)
         return OR_ERR_NOMEM;
     }
     for (int t = 0; t < L; ++t) {
-        const int s = t / C;
+        const int s = seg_of(J, t);
         const double *qt = J->q + (size_t)t * d, *ut = J->u + (size_t)t * d;
-        /* pooled keys: segments i < s over their whole span, segment s over [sC, t] */
+        /* pooled keys: segments i < s over their whole span, segment s from its start to t */
         for (int i = 0; i <= s; ++i) {
-            int a0 = i * C, a1 = (i < s) ? (a0 + C < L ? a0 + C : L) : t + 1;
+            int a0 = seg_lo(J, i), a1 = (i < s) ? seg_hi(J, i) : t + 1;
             memset(pool, 0, (size_t)d * sizeof(double));
             for (int j = a0; j < a1; ++j)
                 for (int b = 0; b < d; ++b) pool[b] += J->k[(size_t)j * d + b];
@@ -370,11 +388,12 @@ static int head_bruteforce(const head_job *J)
         double *yt = J->y + (size_t)t * d;
         memset(yt, 0, (size_t)d * sizeof(double));
         for (int j = 0; j <= t; ++j) {
-            double wj = w[j / C];
+            const int sj = seg_of(J, j);
+            double wj = w[sj];
             if (wj == 0.0) continue;
             /* a cached segment is read at its last token, the current one at t */
-            const int seg_end = (j / C) * C + C - 1 < L - 1 ? (j / C) * C + C - 1 : L - 1;
-            wj *= token_weight(J, j, j / C == s ? t : seg_end);
+            const int seg_end = seg_hi(J, sj) - 1;
+            wj *= token_weight(J, j, sj == s ? t : seg_end);
             double kq = dot(J->k + (size_t)j * d, qt, d);
             const double *vj = J->v + (size_t)j * d;
             for (int a = 0; a < d; ++a) yt[a] += wj * kq * vj[a];
@@ -405,8 +424,8 @@ static int head_bruteforce(const head_job *J)
  */
 static int head_backward(const head_job *J)
 {
-    const int L = J->L, d = J->d, C = J->C;
-    const int N = (L + C - 1) / C;
+    const int L = J->L, d = J->d;
+    const int N = num_seg(J);
     const size_t dd = (size_t)d * d;
     const int gated = J->mode == OR_GRM || J->mode == OR_SOUP || J->mode == OR_SSC;
 
@@ -435,7 +454,7 @@ static int head_backward(const head_job *J)
     /* the forward's cached states and pooled keys */
     for (int n = 0; n < N; ++n) {
         double *M = states + (size_t)n * dd;
-        int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
+        int t0 = seg_lo(J, n), t1 = seg_hi(J, n);
         for (int t = t0; t < t1; ++t) {
             memory_step(J, M, t, t0);
             for (int b = 0; b < d; ++b) kbar[(size_t)n * d + b] += J->k[(size_t)t * d + b];
@@ -444,7 +463,7 @@ static int head_backward(const head_job *J)
     }
 
     for (int s = 0; s < N; ++s) {
-        int t0 = s * C, t1 = t0 + C < L ? t0 + C : L;
+        int t0 = seg_lo(J, s), t1 = seg_hi(J, s);
         memset(Mon, 0, dd * sizeof(double));
         memset(ksum, 0, (size_t)d * sizeof(double));
         for (int t = t0; t < t1; ++t) {
@@ -530,7 +549,7 @@ static int head_backward(const head_job *J)
     /* spread each cached memory's gradient over its segment's tokens */
     for (int n = 0; n < N; ++n) {
         const double *Gn = G + (size_t)n * dd;
-        int t0 = n * C, t1 = t0 + C < L ? t0 + C : L;
+        int t0 = seg_lo(J, n), t1 = seg_hi(J, n);
         for (int j = t0; j < t1; ++j) {
             const double *kj = J->k + (size_t)j * d, *vj = J->v + (size_t)j * d;
             double *dvj = J->dv + (size_t)j * d, *dkj = J->dk + (size_t)j * d;
@@ -561,8 +580,8 @@ typedef struct {
 static void *worker(void *arg)
 {
     pool_ctx *P = (pool_ctx *)arg;
-    const int L = P->base.L, d = P->base.d, C = P->base.C;
-    const int N = (L + C - 1) / C;
+    const int L = P->base.L, d = P->base.d;
+    const int N = num_seg(&P->base);
     const size_t Ld = (size_t)L * d, Ndd = (size_t)N * d * d;
     for (;;) {
         pthread_mutex_lock(&P->mu);
@@ -643,7 +662,7 @@ int mc_oracle_forward(const double *q, const double *k, const double *v, const d
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
                         seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
                         mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, NULL, NULL, NULL,
-                        NULL, NULL, NULL, NULL, NULL};
+                        NULL, NULL, NULL, NULL, NULL, NULL, 0};
     P.BH = BH;
     P.brute = 0;
     return run_pool(&P, nthreads);
@@ -664,7 +683,7 @@ int mc_oracle_forward_swla(const double *q, const double *k, const double *v, co
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
                         seg_mask, mode == OR_SSC ? given_sel : NULL, y, states,
                         mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, alpha, beta, lam,
-                        NULL, NULL, NULL, NULL, NULL};
+                        NULL, NULL, NULL, NULL, NULL, NULL, 0};
     P.BH = BH;
     P.brute = 0;
     return run_pool(&P, nthreads);
@@ -680,7 +699,7 @@ int mc_oracle_bruteforce(const double *q, const double *k, const double *v, cons
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL};
+                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0};
     P.BH = BH;
     P.brute = 1;
     return run_pool(&P, nthreads);
@@ -697,7 +716,7 @@ int mc_oracle_bruteforce_swla(const double *q, const double *k, const double *v,
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, y, NULL, NULL, NULL, alpha, beta, lam, NULL, NULL, NULL, NULL, NULL};
+                        NULL, NULL, y, NULL, NULL, NULL, alpha, beta, lam, NULL, NULL, NULL, NULL, NULL, NULL, 0};
     P.BH = BH;
     P.brute = 1;
     return run_pool(&P, nthreads);
@@ -717,8 +736,61 @@ int mc_oracle_backward(const double *q, const double *k, const double *v, const 
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, dy, dq, dk, dv, du};
+                        NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, dy, dq, dk, dv, du, NULL, 0};
     P.BH = BH;
     P.brute = 2;
+    return run_pool(&P, nthreads);
+}
+
+static int check_segments(int L, const int32_t *seg_off, int nseg)
+{
+    if (!seg_off || nseg <= 0 || seg_off[0] != 0 || seg_off[nseg] != L) return OR_ERR_ARG;
+    for (int n = 0; n < nseg; ++n)
+        if (seg_off[n + 1] <= seg_off[n]) return OR_ERR_ARG;
+    return OR_OK;
+}
+
+/*
+ * The forward with given segment boundaries: segment n is tokens
+ * [seg_off[n], seg_off[n+1]) (seg_off[0] = 0, strictly increasing, seg_off[nseg] = L),
+ * the same for every (batch, head).  Everything else as mc_oracle_forward; states
+ * is [BH][nseg][d][d].
+ */
+int mc_oracle_forward_segments(const double *q, const double *k, const double *v, const double *u,
+                               int BH, int L, int d, const int32_t *seg_off, int nseg, int mode, int topk,
+                               const int32_t *given_sel, double *y, double *states, int32_t *sel, double *gap,
+                               int nthreads)
+{
+    int st = check_args(BH, L, d, 1, mode, topk);
+    if (st == OR_OK) st = check_segments(L, seg_off, nseg);
+    if (st != OR_OK) return st;
+    if (!q || !k || !v || !u || !y || !states) return OR_ERR_ARG;
+    pool_ctx P;
+    memset(&P, 0, sizeof(P));
+    P.base = (head_job){q, k, v, u, L, d, 1, mode, mode == OR_SSC ? topk : 0,
+                        NULL, mode == OR_SSC ? given_sel : NULL, y, states,
+                        mode == OR_SSC ? sel : NULL, mode == OR_SSC ? gap : NULL, NULL, NULL, NULL,
+                        NULL, NULL, NULL, NULL, NULL, seg_off, nseg};
+    P.BH = BH;
+    P.brute = 0;
+    return run_pool(&P, nthreads);
+}
+
+/* Token-level twin with given segment boundaries (y only). */
+int mc_oracle_bruteforce_segments(const double *q, const double *k, const double *v, const double *u,
+                                  int BH, int L, int d, const int32_t *seg_off, int nseg, int mode, int topk,
+                                  double *y, int nthreads)
+{
+    int st = check_args(BH, L, d, 1, mode, topk);
+    if (st == OR_OK) st = check_segments(L, seg_off, nseg);
+    if (st != OR_OK) return st;
+    if (!q || !k || !v || !u || !y) return OR_ERR_ARG;
+    pool_ctx P;
+    memset(&P, 0, sizeof(P));
+    P.base = (head_job){q, k, v, u, L, d, 1, mode, mode == OR_SSC ? topk : 0,
+                        NULL, NULL, y, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                        seg_off, nseg};
+    P.BH = BH;
+    P.brute = 1;
     return run_pool(&P, nthreads);
 }

@@ -143,6 +143,70 @@ def test_mean_is_linear_attention_over_the_memory_count(C):
     np.testing.assert_array_equal(y0, y)
 
 
+def test_log_segmentation_worked_example():
+    """The pages' worked example of the logarithmic segmentation (tests/golden/log_segments.txt)."""
+    vals = _load_golden("log_segments.txt")
+    for L, lens in vals.items():
+        off = oracle.log_segments(int(L))
+        assert list(np.diff(off)) == [int(x) for x in lens]
+
+
+@pytest.mark.parametrize("L", [1, 2, 37, 64, 100, 1000, 65535])
+def test_log_segmentation_properties(L):
+    """One segment per set bit of L, distinct powers of two, longest first, N <= log2 L + 1."""
+    lens = np.diff(oracle.log_segments(L))
+    assert lens.sum() == L and len(lens) == bin(L).count("1")
+    assert all(x & (x - 1) == 0 for x in lens) and list(lens) == sorted(lens, reverse=True)
+    assert len(lens) <= int(np.log2(L)) + 1
+
+
+VAR_SEGS = [[0, 40, 56, 60, 61, 64], [0, 1, 2, 3, 64], [0, 64]]
+
+
+@pytest.mark.parametrize("off", VAR_SEGS + [None])
+def test_variable_segments_residual_is_causal_la(off):
+    """Residual collapses to causal LA for ANY segmentation, constant or not."""
+    q, k, v, u = _inputs(1, 2, 64, 8, 21)
+    off = off if off is not None else oracle.log_segments(64 - 1) + []
+    L = off[-1]
+    q, k, v, u = (x[..., :L, :] for x in (q, k, v, u))
+    y = oracle.forward(q, k, v, u, None, RESIDUAL, seg_off=off)["y"]
+    np.testing.assert_allclose(y, causal_la(q, k, v), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("off", VAR_SEGS)
+def test_variable_segments_constant_gates(off):
+    """u = 0 (GRM) or Mean: equal gates over the s + 1 memories, y_t = LA_t / (s_t + 1)."""
+    q, k, v, u = _inputs(1, 1, 64, 8, 22)
+    s_of = np.searchsorted(np.asarray(off), np.arange(64), side="right")  # s_t + 1
+    ref = causal_la(q, k, v) / s_of[:, None]
+    for mode, uu in ((GRM, np.zeros_like(u)), (MEAN, u)):
+        y = oracle.forward(q, k, v, uu, None, mode, seg_off=off)["y"]
+        np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (SSC, 1), (SOUP, 0), (MEAN, 0)])
+@pytest.mark.parametrize("off", VAR_SEGS)
+def test_variable_segments_state_form_matches_twin(off, mode, topk):
+    q, k, v, u = _inputs(1, 2, 64, 8, 23)
+    a = oracle.forward(q, k, v, u, None, mode, topk, seg_off=off)
+    b = oracle.bruteforce(q, k, v, u, None, mode, topk, seg_off=off)
+    np.testing.assert_allclose(a["y"], b, rtol=1e-10, atol=1e-11)
+    for n in range(len(off) - 1):  # the cached states are the segments' V^T K
+        K, V = k[..., off[n]:off[n + 1], :], v[..., off[n]:off[n + 1], :]
+        np.testing.assert_allclose(a["states"][:, :, n], np.einsum("bhta,bhtc->bhac", V, K), rtol=1e-12,
+                                   atol=1e-12)
+
+
+def test_constant_boundaries_match_the_segment_length():
+    q, k, v, u = _inputs(1, 2, 70, 8, 24)
+    off = list(range(0, 70, 16)) + [70]
+    for mode, topk in ((GRM, 0), (SSC, 2)):
+        a = oracle.forward(q, k, v, u, 16, mode, topk)
+        b = oracle.forward(q, k, v, u, None, mode, topk, seg_off=off)
+        np.testing.assert_array_equal(a["y"], b["y"])
+
+
 def test_one_token_segments_are_gated_attention():
     """N = L: every token is its own segment, the pool of a one-token segment is its
     key, and GRM becomes y_t = sum_{i<=t} softmax_i(u_t . k_i) v_i (k_i . q_t)
@@ -389,6 +453,8 @@ _MUTATIONS = [
     ("ssc ties to higher index", r"if \(best < 0 \|\| fi > bv\) \{ /\* strict",
      "if (best < 0 || fi >= bv) { /* strict"),
     ("soup uses online twice", r"Mstar\[e\] \+= g\[i\] \* Mi\[e\];", "Mstar[e] += g[s] * Mi[e];"),
+    ("segment end one token early", r"if \(J->seg_off\) return J->seg_off\[n \+ 1\];",
+     "if (J->seg_off) return J->seg_off[n + 1] - (n + 2 < J->nseg ? 1 : 0);"),
     ("mean over the cached memories only", r"const double w = 1\.0 / \(double\)\(s \+ 1\);",
      "const double w = 1.0 / (double)(s > 0 ? s : 1);"),
 ]
@@ -408,6 +474,9 @@ def _run_pins_against(libpath):
         lib.mc_oracle_forward_swla.restype = ctypes.c_int
         lib.mc_oracle_bruteforce_swla.argtypes = saved.mc_oracle_bruteforce_swla.argtypes
         lib.mc_oracle_bruteforce_swla.restype = ctypes.c_int
+        for fn in ("mc_oracle_forward_segments", "mc_oracle_bruteforce_segments"):
+            getattr(lib, fn).argtypes = getattr(saved, fn).argtypes
+            getattr(lib, fn).restype = ctypes.c_int
         oracle._lib = lib
         pins = [
             test_hand_worked_example,
@@ -420,6 +489,8 @@ def _run_pins_against(libpath):
             lambda: test_causality(GRM, 0),
             lambda: test_single_segment_is_plain_recurrent_model(GRM, 0),
             lambda: test_mean_is_linear_attention_over_the_memory_count(5),
+            lambda: test_variable_segments_constant_gates(VAR_SEGS[0]),
+            lambda: test_variable_segments_state_form_matches_twin(VAR_SEGS[0], GRM, 0),
             test_swla_constant_decay_is_decayed_linear_attention,
             test_swla_zero_decay_is_a_two_token_window,
             lambda: test_swla_window_does_not_cross_segments(7),
