@@ -537,6 +537,74 @@ def run_backward(args, w, wname):
     }
 
 
+LOGLINEAR = mc_inputs.Workload("loglinear-grm B1 H16 L65535 d128 log-segments bf16", 1, 16, 65535, 128, 65535, GRM,
+                               "bf16", seed=7)
+
+
+def run_segments(args):
+    """Log-Linear++: GRM over the logarithmic segmentation of L = 65535 (16 segments of
+    32768, 16384, ..., 1 tokens), B1 H16 d128 bf16, through mc_forward_segments."""
+    import torch
+    import memory_caching_linear_gb300 as mcl
+    from memory_caching_linear_gb300 import build as mcbuild
+    mcbuild.build()
+    mcl.load_library()
+    w = LOGLINEAR
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, u = mc_inputs.workload_inputs(w, device=dev)
+    off = mcl.log_segments(w.L)
+    lens = [b - a for a, b in zip(off[:-1], off[1:])]
+    y = torch.empty_like(q)
+    states = torch.empty((w.B, w.H, len(lens), w.d, w.d), dtype=torch.float32, device=dev)
+
+    def step():
+        mcl.mc_forward_segments(q, k, v, u, off, w.mode, y=y, states=states)
+
+    sampler = ClockSampler(dev.index).start()
+    nwarm = max(args.warmup, 3)
+    for _ in range(nwarm):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    prof = mcl.KernelProfile(capacity=args.steps * 4 + 8)
+    with prof:
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    kernels_ms = {n: round(sum(t) / args.steps, 4) for n, t in prof.per_kernel_ms().items()}
+    # algorithmic work per head: L 4 d^2 + 2 d^2 sum_t n_t + 2 d sum_t (n_t + 1), n_t = cached segments of t
+    sum_n = sum(i * ln for i, ln in enumerate(lens))
+    bh, d = w.B * w.H, w.d
+    f_state = bh * w.L * 2 * d * d
+    f_read = bh * (w.L * 2 * d * d + 2 * d * d * sum_n + 2 * d * (sum_n + w.L))
+    dom = max(kernels_ms, key=kernels_ms.get)
+    work = f_read if dom == "readout_simt" else f_state
+    peak = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3
+    achieved = work / (kernels_ms[dom] / 1e3) / 1e12
+    return {
+        "metric": "tokens/sec Log-Linear++ (MC-GRM, logarithmic segments) forward", "value": round(w.tokens / (ms / 1e3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": nwarm, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy normals: q,k unit rows, v ~ N(0,1), u ~ N(0,1)/sqrt(d))",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "segments": lens, "agg": "grm",
+                   "input_dtype": w.dtype, "l2": "inputs 1.00 GiB > L2 129 MB, not flushed"},
+        "algorithmic_tflop_per_step": round((f_state + f_read) / 1e12, 4),
+        "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom, "launch_ms": kernels_ms[dom],
+                     "algorithmic_tflop_per_launch": round(work / 1e12, 4),
+                     "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"},
+        "kernels_ms": kernels_ms, "gpu_launches": 2 * args.steps, "clocks": sampler.summary(),
+    }
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, w):
@@ -577,7 +645,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["decode-grm"] + ["bwd-" + n for n in sorted(WORKLOADS)],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["decode-grm", "loglinear-grm"] +
+                    ["bwd-" + n for n in sorted(WORKLOADS)],
                     default="long-grm")
     ap.add_argument("--mode", choices=["residual", "grm", "soup", "ssc"], default=None,
                     help="override the workload's aggregation")
@@ -592,6 +661,10 @@ def main(argv=None):
     if args.workload == "decode-grm":
         if args.impl == "ours":
             print(json.dumps(run_decode(args)), flush=True)
+        return
+    if args.workload == "loglinear-grm":
+        if args.impl == "ours":
+            print(json.dumps(run_segments(args)), flush=True)
         return
     if args.workload.startswith("bwd-"):
         if args.impl == "ours":

@@ -125,6 +125,32 @@ int mc_forward_swla(const void *q, const void *k, const void *v, const void *u,
                     void *y, float *states, mc_stream_t stream);
 
 /*
+ * mc_forward_segments -- the forward with given segment boundaries instead of a
+ * constant segment length: segment n is tokens [seg_off[n], seg_off[n+1]), the
+ * same for every (b, h).  With the logarithmic segmentation of mc_log_segments and
+ * MC_GRM this is the Log-Linear++ variant ([MC-ja] variants appendix; [MC-sum]
+ * §4.2: segments of power-of-two lengths, N <= log2 L + 1).
+ *   seg_off : HOST int32 [nseg + 1], 0 = seg_off[0] < seg_off[1] < ... < seg_off[nseg] = L;
+ *             read during the call only.
+ *   states  : fp32 [B][H][nseg][d][d] or NULL.
+ *   is_bf16 : q, k, v, u, y are bf16 if non-zero, fp32 otherwise.
+ *   Other arguments as mc_forward.  Runs on the FFMA kernels.  MC_ERR_SHAPE for
+ *   boundaries that do not rise strictly from 0 to L.
+ */
+int mc_forward_segments(const void *q, const void *k, const void *v, const void *u,
+                        int B, int H, int L, int d, const int32_t *seg_off, int nseg,
+                        int agg_mode, int topk, void *y, float *states, int is_bf16, mc_stream_t stream);
+
+/*
+ * mc_log_segments -- the logarithmic segmentation of a length-L sequence ([MC-sum]
+ * §4.2): one segment per set bit of L, that power of two long, the longest first
+ * (37 -> 32, 4, 1).  Writes the boundaries [0, ..., L] to seg_off (host, cap
+ * entries) and returns the number of segments, or MC_ERR_SHAPE (L < 1, or cap too
+ * small) / MC_ERR_NULL.  Host only; touches no device.
+ */
+int mc_log_segments(int L, int32_t *seg_off, int cap);
+
+/*
  * mc_backward -- gradients of the forward over the plain linear memory (the
  * update M <- M + v k^T): for an upstream gradient dy of y, the gradients of
  * <y, dy> with respect to q, k, v and u.  They follow the forward's steps by the

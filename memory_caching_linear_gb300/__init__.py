@@ -24,7 +24,7 @@ MC_ERR_NULL, MC_ERR_SHAPE, MC_ERR_MODE, MC_ERR_TOPK = -1, -2, -3, -4
 MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = -5, -6, -7, -8, -9
 MC_ERR_SCRATCH = -10
 
-EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_backward", "mc_backward_f32", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
+EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_forward_segments", "mc_log_segments", "mc_backward", "mc_backward_f32", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
             "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
             "mc_status_string")
 
@@ -54,6 +54,10 @@ def load_library():
     lib.mc_forward_f32.restype = i
     lib.mc_forward_swla.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp]
     lib.mc_forward_swla.restype = i
+    lib.mc_forward_segments.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, i, i, i, vp, vp, i, vp]
+    lib.mc_forward_segments.restype = i
+    lib.mc_log_segments.argtypes = [i, vp, i]
+    lib.mc_log_segments.restype = i
     lib.mc_backward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
     lib.mc_backward.restype = i
     lib.mc_backward_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, vp]
@@ -215,6 +219,51 @@ def forward(q, k, v, u, seg_len: int, agg_mode: int, topk: int = 0, **kw):
     if q.dtype == torch.float32:
         return mc_forward_f32(q, k, v, u, seg_len, agg_mode, topk, **kw)
     raise TypeError("inputs must be bf16 or fp32")
+
+
+def log_segments(L: int) -> list:
+    """The logarithmic segmentation of length L (``mc_log_segments``): boundaries [0, ..., L]."""
+    buf = (ctypes.c_int32 * 33)()
+    n = load_library().mc_log_segments(int(L), buf, 33)
+    if n < 0:
+        raise MCError(n, "mc_log_segments")
+    return list(buf[:n + 1])
+
+
+def mc_forward_segments(q, k, v, u, seg_off, agg_mode: int, topk: int = 0, *, y=None, states=None,
+                        want_states: bool = True, stream=None):
+    """Forward over given segment boundaries (``mc_forward_segments``); bf16 or fp32 inputs.
+    ``seg_off`` is a sequence [0, ..., L]; with :func:`log_segments` and MC_GRM this is
+    the Log-Linear++ variant.  Returns (y, states)."""
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dev, dtype = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("inputs must be bf16 or fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, dtype, (B, H, L, d), dev)
+    if u is not None:
+        _check(u, "u", dtype, (B, H, L, d), dev)
+    off = (ctypes.c_int32 * len(seg_off))(*[int(x) for x in seg_off])
+    nseg = len(seg_off) - 1
+    if y is None:
+        y = torch.empty((B, H, L, d), dtype=dtype, device=dev)
+    _check(y, "y", dtype, (B, H, L, d), dev)
+    if states is None and want_states:
+        states = torch.empty((B, H, nseg, d, d), dtype=torch.float32, device=dev)
+    if states is not None:
+        _check(states, "states", torch.float32, (B, H, nseg, d, d), dev)
+    st = lib.mc_forward_segments(q.data_ptr(), k.data_ptr(), v.data_ptr(), u.data_ptr() if u is not None else None,
+                                 B, H, L, d, off, nseg, int(agg_mode), int(topk), y.data_ptr(),
+                                 states.data_ptr() if states is not None else None,
+                                 1 if dtype == torch.bfloat16 else 0, _stream_handle(stream, dev))
+    if st != MC_OK:
+        raise MCError(st, "mc_forward_segments")
+    return y, states
 
 
 def mc_backward(q, k, v, u, dy, seg_len: int, agg_mode: int, topk: int = 0, *, dq=None, dk=None, dv=None,

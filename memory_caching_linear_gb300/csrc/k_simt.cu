@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(kThreads) seg_scan_simt(FwdArgs a)
 
     const int seg = blockIdx.x % a.N;
     const int bh = blockIdx.x / a.N;
-    const int t0 = seg * a.C;
-    const int t1 = min(t0 + a.C, a.L);
+    const int t0 = seg_begin(a, seg);
+    const int t1 = seg_end(a, seg);
     const size_t base = (size_t)bh * a.L * D;
     const T *q = static_cast<const T *>(a.q) + base;
     const T *k = static_cast<const T *>(a.k) + base;
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(D) kbar_simt(FwdArgs a)
 {
     const int seg = blockIdx.x % a.N;
     const int bh = blockIdx.x / a.N;
-    const int t0 = seg * a.C, t1 = min(t0 + a.C, a.L);
+    const int t0 = seg_begin(a, seg), t1 = seg_end(a, seg);
     const T *k = static_cast<const T *>(a.k) + (size_t)bh * a.L * D;
     float s = 0.f;
     for (int t = t0; t < t1; ++t) s += to_f(k[(size_t)t * D + threadIdx.x]);
@@ -221,9 +221,9 @@ __global__ void __launch_bounds__(kThreads) readout_simt(FwdArgs a)
     const int seg = a.N - 1 - (int)(blockIdx.x / per_seg);
     const int rem = blockIdx.x % per_seg;
     const int bh = rem / tps, tile = rem % tps;
-    const int t0 = seg * a.C;
+    const int t0 = seg_begin(a, seg);
     const int tb = t0 + tile * kTR;
-    const int te = min(min(tb + kTR, t0 + a.C), a.L);
+    const int te = min(tb + kTR, seg_end(a, seg));
     if (tb >= te) return;
     const int cnt = te - tb;
     const int n = seg;  // cached segments 0..n-1
@@ -396,9 +396,9 @@ __global__ void __launch_bounds__(kTR) ssc_select_simt(FwdArgs a)
     const int bh = blockIdx.x / per_bh;
     const int rem = blockIdx.x % per_bh;
     const int seg = rem / tps, tile = rem % tps;
-    const int t0 = seg * a.C;
+    const int t0 = seg_begin(a, seg);
     const int tb = t0 + tile * kTR;
-    const int te = min(min(tb + kTR, t0 + a.C), a.L);
+    const int te = min(tb + kTR, seg_end(a, seg));
     if (tb >= te) return;
     const int cnt = te - tb;
     const size_t base = (size_t)bh * a.L * D;

@@ -218,6 +218,79 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     return MC_OK;
 }
 
+// The forward over given segment boundaries (FFMA kernels; seg_off is host memory).
+int forward_segments(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
+                     const int32_t *seg_off, int nseg, int agg_mode, int topk, void *y, float *states, bool bf16,
+                     cudaStream_t stream)
+{
+    if (!seg_off) return MC_ERR_NULL;
+    if (nseg < 1 || nseg > L || seg_off[0] != 0 || seg_off[nseg] != L) return MC_ERR_SHAPE;
+    int maxlen = 0;
+    for (int n = 0; n < nseg; ++n) {
+        if (seg_off[n + 1] <= seg_off[n]) return MC_ERR_SHAPE;
+        maxlen = seg_off[n + 1] - seg_off[n] > maxlen ? seg_off[n + 1] - seg_off[n] : maxlen;
+    }
+    int st = check_shape(B, H, L, d, maxlen);
+    if (st != MC_OK) return st;
+    if ((long long)B * H * nseg * ((maxlen + 63) / 64) >= (1ll << 31) || (long long)B * H * nseg * d * d > (1ll << 40))
+        return MC_ERR_SHAPE;
+    if (agg_mode < MC_RESIDUAL || agg_mode > MC_MEAN) return MC_ERR_MODE;
+    if (!q || !k || !v || !y) return MC_ERR_NULL;
+    if (mode_uses_u(agg_mode) && !u) return MC_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y) || (u && !aligned16(u)) ||
+        (states && !aligned16(states)))
+        return MC_ERR_ALIGN;
+    Problem p{};
+    p.B = B; p.H = H; p.L = L; p.d = d; p.C = maxlen;
+    p.N = nseg;
+    p.BH = B * H;
+    p.bf16 = bf16;
+    p.mode = agg_mode;
+    p.topk = agg_mode == MC_SSC ? topk : 0;
+    if (agg_mode == MC_SSC) {
+        if (topk < 0) return MC_ERR_TOPK;
+        if (topk >= p.N - 1) p.mode = MC_GRM;
+        else if (topk > kMaxTopk) return MC_ERR_TOPK;
+    }
+    st = check_device();
+    if (st != MC_OK) return st;
+    const ScratchPlan plan = plan_scratch(p, states == nullptr);
+    const size_t off_bytes = round_up(sizeof(int32_t) * (size_t)(nseg + 1));
+    void *scratch = nullptr;
+    if (scratch_alloc(&scratch, plan.total + off_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    char *base = static_cast<char *>(scratch);
+    int32_t *doff = reinterpret_cast<int32_t *>(base + plan.total);
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.u = mode_uses_u(p.mode) ? u : nullptr;
+    a.y = y;
+    a.states = states ? states : reinterpret_cast<float *>(base + plan.off_states);
+    a.O_on = reinterpret_cast<float *>(base + plan.off_O);
+    a.r_on = reinterpret_cast<float *>(base + plan.off_r);
+    a.kbar = reinterpret_cast<float *>(base + plan.off_kbar);
+    a.seg_off = doff;
+    a.BH = p.BH; a.L = L; a.C = maxlen; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
+    cudaError_t e = cudaMemcpyAsync(doff, seg_off, sizeof(int32_t) * (size_t)(nseg + 1), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) {
+        profile_call_start(stream);
+        e = launch_seg_scan_simt(p, a, stream);
+        profile_after_kernel(stream, "seg_scan_simt");
+    }
+    if (e == cudaSuccess) {
+        e = launch_readout_simt(p, a, stream);
+        profile_after_kernel(stream, "readout_simt");
+    }
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
 int backward_common(const void *q, const void *k, const void *v, const void *u, const void *dy, int B, int H, int L,
                     int d, int seg_len, int agg_mode, int topk, void *dq, void *dk, void *dv, void *du, bool bf16,
                     cudaStream_t stream)
@@ -266,6 +339,31 @@ int backward_common(const void *q, const void *k, const void *v, const void *u, 
 }  // namespace mc
 
 extern "C" {
+
+int mc_forward_segments(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
+                        const int32_t *seg_off, int nseg, int agg_mode, int topk, void *y, float *states, int is_bf16,
+                        mc_stream_t stream)
+{
+    return mc::forward_segments(q, k, v, u, B, H, L, d, seg_off, nseg, agg_mode, topk, y, states, is_bf16 != 0,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mc_log_segments(int L, int32_t *seg_off, int cap)
+{
+    if (L < 1) return MC_ERR_SHAPE;
+    if (!seg_off) return MC_ERR_NULL;
+    int nseg = 0;
+    for (int bit = 30; bit >= 0; --bit) nseg += (L >> bit) & 1;
+    if (cap < nseg + 1) return MC_ERR_SHAPE;
+    int n = 0;
+    seg_off[0] = 0;
+    for (int bit = 30; bit >= 0; --bit)
+        if ((L >> bit) & 1) {
+            seg_off[n + 1] = seg_off[n] + (1 << bit);
+            ++n;
+        }
+    return nseg;
+}
 
 int mc_backward(const void *q, const void *k, const void *v, const void *u, const void *dy, int B, int H, int L,
                 int d, int seg_len, int agg_mode, int topk, void *dq, void *dk, void *dv, void *du, mc_stream_t stream)

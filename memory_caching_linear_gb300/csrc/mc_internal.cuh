@@ -42,8 +42,16 @@ struct FwdArgs {
     float *kbar;                // [BH][N][d]   scratch
     int32_t *sel_out;           // [BH][L][topk] (ssc_select only)
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L]; all null = plain update
+    const int32_t *seg_off;     // optional [N+1] segment boundaries (device); then C is the longest segment
     int BH, L, C, N, mode, topk;
 };
+
+// Segment n's tokens [seg_begin, seg_end): constant length C, or the given boundaries.
+__device__ __forceinline__ int seg_begin(const FwdArgs &a, int n) { return a.seg_off ? a.seg_off[n] : n * a.C; }
+__device__ __forceinline__ int seg_end(const FwdArgs &a, int n)
+{
+    return a.seg_off ? a.seg_off[n + 1] : min((n + 1) * a.C, a.L);
+}
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -113,3 +113,19 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
 def test_build_flags_target_sm103a():
     flags = " ".join(mcbuild.compile_flags())
     assert "arch=compute_103a,code=sm_103a" in flags
+
+
+def test_log_segments_on_the_host(lib):
+    """mc_log_segments needs no device: the pages' worked example (37 -> 32, 4, 1) and the
+    oracle's own logarithmic segmentation for other lengths; errors for bad arguments."""
+    import oracle
+    assert mcl.log_segments(37) == [0, 32, 36, 37]
+    for L in (1, 2, 3, 64, 1000, 65535, 1 << 20):
+        assert mcl.log_segments(L) == oracle.log_segments(L)
+    buf = (ctypes.c_int32 * 2)()
+    assert lib.mc_log_segments(0, buf, 2) == mcl.MC_ERR_SHAPE
+    assert lib.mc_log_segments(3, buf, 2) == mcl.MC_ERR_SHAPE  # needs three boundaries
+    assert lib.mc_log_segments(3, None, 8) == mcl.MC_ERR_NULL
+    off = (ctypes.c_int32 * 3)(0, 5, 4)  # not rising
+    st = lib.mc_forward_segments(FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 16, off, 2, 1, 0, FAKE, None, 1, None)
+    assert st == mcl.MC_ERR_SHAPE

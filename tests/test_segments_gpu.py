@@ -1,0 +1,70 @@
+"""Parity of the forward over given segment boundaries (mc_forward_segments) with the
+oracle, including the logarithmic segmentation of Log-Linear++ ([MC-sum §4.2]; the
+variants appendix of "メモリキャッシング：メモリ容量が増大する RNN"): y and the cached
+states element by element, every aggregation, fp32 and bf16.  Tolerances as the
+forward: 1e-4 * max|ref| (fp32), 1e-2 * max|ref| (bf16)."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import memory_caching_linear_gb300 as mcl
+import oracle
+from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from memory_caching_linear_gb300 import build
+    build.build()
+    mcl.load_library()
+
+
+def rel_err(got, ref):
+    scale = np.abs(ref).max()
+    return float(np.abs(np.asarray(got, np.float64) - ref).max() / (scale if scale > 0 else 1.0))
+
+
+CASES = [
+    # (name, B, H, L, d, dtype, boundaries or None for the logarithmic segmentation)
+    ("log-1000-f32", 1, 2, 1000, 32, "f32", None),
+    ("log-777-bf16", 1, 1, 777, 128, "bf16", None),
+    ("log-4095-d64", 1, 1, 4095, 64, "bf16", None),
+    ("custom-f32", 2, 1, 300, 16, "f32", [0, 7, 8, 100, 260, 300]),
+    ("one-seg", 1, 1, 256, 64, "f32", [0, 256]),
+]
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (RESIDUAL, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
+@pytest.mark.parametrize("name,B,H,L,d,dtype,off", CASES, ids=[c[0] for c in CASES])
+def test_segments_parity(name, B, H, L, d, dtype, off, mode, topk):
+    # the library's and the oracle's logarithmic segmentations are computed separately
+    off_gpu = mcl.log_segments(L) if off is None else off
+    off = oracle.log_segments(L) if off is None else off
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype=dtype)
+    ref = oracle.forward(q, k, v, u, None, mode, topk, seg_off=off)
+    dev = torch.device("cuda")
+    y, st = mcl.mc_forward_segments(*(t.to(dev) for t in (q, k, v, u)), off_gpu, mode, topk)
+    assert mcl.mc_check_device() == mcl.MC_OK
+    y, st = y.float().cpu().numpy(), st.cpu().numpy()
+    yref = ref["y"]
+    if mode == SSC and 0 < topk < len(off) - 2:
+        differ = ref["gap"] < 1e-5  # fp32 near-ties may rank either way: compare elsewhere
+        keep = ~differ
+        assert rel_err(y[keep], yref[keep]) <= TOL[dtype]
+    else:
+        assert rel_err(y, yref) <= TOL[dtype], (name, mode, rel_err(y, yref))
+    assert rel_err(st, ref["states"]) <= TOL[dtype]
+
+
+def test_constant_boundaries_match_mc_forward():
+    q, k, v, u = (t.cuda() for t in make_inputs(1, 2, 640, 32, 3, "f32"))
+    y0, s0 = mcl.forward(q, k, v, u, 128, GRM)
+    y1, s1 = mcl.mc_forward_segments(q, k, v, u, list(range(0, 641, 128)), GRM)
+    torch.testing.assert_close(y1, y0, rtol=0, atol=0)
+    torch.testing.assert_close(s1, s0, rtol=0, atol=0)
