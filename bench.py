@@ -458,20 +458,26 @@ def run_decode(args):
 
 
 def backward_flops(w):
-    """Algorithmic work of the backward (all heads).  Per token and cached read: the
-    read's value M q (2 d^2, needed for the gate gradient and not kept by the
-    forward), dq (2 d^2) and the state gradient dy q^T (2 d^2); per token, twice the
+    """Algorithmic work of the backward (all heads), in total and per kernel.  Per token and
+    cached read: the read's value M q (2 d^2, needed for the gate gradient and not kept by
+    the forward), dq (2 d^2) and the state gradient dy q^T (2 d^2); per token, twice the
     online write + read (8 d^2); per token and score, the score gradients du and the
-    key-mean gradient (4 d).  The gate kernel's share: the cached M q and dq and the
-    score gradients."""
+    key-mean gradient (4 d).  Per kernel: the tensor-core cached pass does M q and dq of
+    the cached reads, the G kernels the state gradients, the gate kernel the score
+    gradients (and, without the tensor-core pass, the cached M q and dq too), the segment
+    scan the online write and read (4 d^2 per token and run), the reverse scan the online
+    gradients (6 d^2 per token)."""
     s, n = segment_counts(w)
     bh = w.B * w.H
     d = w.d
     routed = w.mode not in (RESIDUAL, mc_inputs.MEAN)
     score = 4 * d * sum(s) if routed else 0
-    total = bh * (6 * d * d * sum(n) + 8 * d * d * w.L + score)
-    gates = bh * (4 * d * d * sum(n) + score)
-    return {"total": total, "bwd_gates_simt": gates}
+    cached = 4 * d * d * sum(n)
+    return {"total": bh * (6 * d * d * sum(n) + 8 * d * d * w.L + score),
+            "bwd_cached_tc": bh * cached, "bwd_gates_simt": bh * (cached + score),
+            "bwd_route_simt": bh * score // 2, "bwd_dkbar_simt": bh * score // 2,
+            "bwd_G_tc": bh * 2 * d * d * sum(n), "bwd_G_simt": bh * 2 * d * d * sum(n),
+            "seg_scan_simt": bh * 4 * d * d * w.L, "bwd_scan_simt": bh * 6 * d * d * w.L}
 
 
 def run_backward(args, w, wname):
@@ -514,24 +520,34 @@ def run_backward(args, w, wname):
     per_kernel = prof.per_kernel_ms()
     kernels_ms = {n: round(sum(t) / len(t) * (len(t) / args.steps), 4) for n, t in per_kernel.items()}
     flops = backward_flops(w)
-    dom = "bwd_gates_simt"
-    dom_ms = kernels_ms.get(dom, 0.0)
-    peak = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3
-    achieved = flops[dom] / (dom_ms / 1e3) / 1e12 if dom_ms else 0.0
+    dom = max(kernels_ms, key=kernels_ms.get)
+    dom_ms = kernels_ms[dom]
+    key = dom
+    # the segment scan runs twice per step (states and O_on, then M_t^T dy_t): its time is the sum
+    work = flops[key] * (2 if dom == "seg_scan_simt" else 1)
+    tensor = dom.endswith("_tc")
+    if tensor:
+        peaks = measured_peaks()
+        peak, psrc, bound = peaks["bf16_tflops"], f"bf16 burst ({peaks['source']})", "tensor"
+    else:
+        peak, psrc, bound = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ / 1e3, \
+            "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz", "alu"
+    achieved = work / (dom_ms / 1e3) / 1e12 if dom_ms else 0.0
     return {
         "metric": f"tokens/sec MC-{mc_inputs.MODE_NAMES[w.mode].upper()} backward ({w.name})",
         "value": round(w.tokens / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": nwarm, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
+        "vs_baseline": None, "dtype": "bf16+f32" if "bwd_cached_tc" in kernels_ms else "f32",
         "data": "synthetic (the forward workload's seeded inputs; dy ~ N(0, 1))",
         "config": {"workload": f"bwd-{wname} {w.name}", "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len,
                    "N": w.N, "agg": mc_inputs.MODE_NAMES[w.mode], "input_dtype": w.dtype,
                    "l2": "inputs > L2 129 MB, not flushed"},
         "algorithmic_tflop_per_step": round(flops["total"] / 1e12, 4),
-        "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom, "launch_ms": dom_ms,
-                     "algorithmic_tflop_per_launch": round(flops[dom] / 1e12, 4),
-                     "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"},
+                     "algorithmic_tflop_per_launch": round(work / 1e12, 4), "peak_source": psrc},
+        "kernels_tflops": {n: round(flops.get(n, 0) * (2 if n == "seg_scan_simt" else 1) / (t / 1e3) / 1e12, 2)
+                           for n, t in kernels_ms.items() if t},
         "kernels_ms": kernels_ms, "gpu_launches": prof.kernel_count() // max(args.steps, 1) * args.steps,
         "clocks": sampler.summary(),
     }

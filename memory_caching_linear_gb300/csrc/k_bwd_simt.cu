@@ -20,13 +20,17 @@
 //   with E_j  = G_n + sum_{t >= j in segment n} g_{t,n} dy_t q_t^T for token j of segment n.
 // Residual (g = 1) and Mean (g = 1 / (n + 1)) have constant gates and du = 0.
 //
-// Three kernels after the forward's segment scan has been re-run twice (once for
-// the cached states, key means, online scores and O_on = M_t q_t; once on
-// (dy, v, k) for X_on = M_t^T dy_t):
+// After the forward's segment scan has been re-run twice (once for the cached
+// states, key means, online scores and O_on = M_t q_t; once on (dy, v, k) for
+// X_on = M_t^T dy_t), on the FFMA path:
 //   bwd_gates_simt  per (b,h, segment, 64-token tile): gates, dg against every cached
 //                   state, dq, du, dkbar (atomics) and the per-token softmax data;
 //   bwd_G_simt      per (b,h, cached segment i): G_i over every later token;
 //   bwd_scan_simt   per (b,h, segment): walks the segment backwards with E, writes dk, dv.
+// On the shapes of the tensor-core path the cached states' O(N L d^2) part runs on
+// the tensor cores (k_bwd_tc.cu: dg and the cached dq, and G), and the gate work on
+// whole shared-memory tables: bwd_route_simt (before the cached pass: the gates;
+// after it: delta, dr, du, dq) and bwd_dkbar_simt (the key-mean gradient from dr).
 #include "mc_internal.cuh"
 
 namespace mc {
@@ -34,6 +38,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTB = 64;  // tokens per gate tile
+constexpr int kTab = 64; // cached segments whose scores a gate tile keeps in shared memory
 constexpr int kTG = 32;  // tokens per step of the G accumulation
 
 template <typename F>
@@ -79,6 +84,7 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
     int *seli = reinterpret_cast<int *>(selv + kTB * kMaxTopk);
     int *cur = seli + kTB * kMaxTopk;
     int *nsel = cur + kTB;
+    float *sct = reinterpret_cast<float *>(nsel + kTB);  // kTB x kTab: <u_t, kbar_i>
 
     const int tps = (a.C + kTB - 1) / kTB;
     const int per_seg = a.BH * tps;
@@ -110,12 +116,39 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
         Us[r * P + c] = (ok && gated) ? to_f(u[gi]) : 0.f;
         Ks[r * P + c] = (ok && gated) ? to_f(k[gi]) : 0.f;
     }
-    if (gated && tid < D) {  // keys of this segment before the tile (pooled score of the online memory)
-        float s = 0.f;
-        for (int j = t0; j < tb; ++j) s += to_f(k[(size_t)j * D + tid]);
-        kpre[tid] = s;
+    // keys of this segment before the tile (the online memory's pooled key, for du): every
+    // thread sums a column over a strided share of the tokens, four loads in flight
+    const bool need_kpre = gated;
+    if (need_kpre && tid < D) kpre[tid] = 0.f;
+    __syncthreads();
+    if (need_kpre) {
+        constexpr int parts = kThreads / D;
+        const int col = tid % D, part = tid / D;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int j = t0 + part;
+        for (; j + 3 * parts < tb; j += 4 * parts) {
+            s0 += to_f(k[(size_t)j * D + col]);
+            s1 += to_f(k[(size_t)(j + parts) * D + col]);
+            s2 += to_f(k[(size_t)(j + 2 * parts) * D + col]);
+            s3 += to_f(k[(size_t)(j + 3 * parts) * D + col]);
+        }
+        for (; j < tb; j += parts) s0 += to_f(k[(size_t)j * D + col]);
+        atomicAdd(&kpre[col], (s0 + s1) + (s2 + s3));
     }
     __syncthreads();
+    // the router scores of the tile against every cached segment, all threads at once (the same
+    // arithmetic as gate_score everywhere else, so every pass ranks identically)
+    const bool use_tab = gated && n <= kTab;
+    if (use_tab) {
+        for (int e = tid; e < kTB * n; e += kThreads) {  // a warp: 32 tokens, one segment (its kbar row broadcast)
+            const int i = e / kTB, t = e % kTB;
+            sct[t * kTab + i] = t < cnt ? gate_score(Us + t * P, kbar + (size_t)i * D, D) : 0.f;
+        }
+        __syncthreads();
+    }
+    auto score = [&](int t, int i) -> float {
+        return use_tab ? sct[t * kTab + i] : gate_score(Us + t * P, kbar + (size_t)i * D, D);
+    };
 
     // Gates, as in the forward readout.
     if (tid < kTB) {
@@ -123,14 +156,13 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
         float go = const_gate(mode, n), m = 0.f, z = 1.f;
         if (t < cnt && gated) {
             const float ron = a.r_on[(size_t)bh * a.L + tb + t];
-            const float *ur = Us + t * P;
             if (mode == MC_SSC) {
                 float *vals = selv + t * kMaxTopk;
                 int *idxs = seli + t * kMaxTopk;
                 int count = 0;
                 const int kk = min(a.topk, kMaxTopk);
                 if (kk > 0)
-                    for (int i = 0; i < n; ++i) topk_insert(vals, idxs, count, kk, gate_score(ur, kbar + (size_t)i * D, D), i);
+                    for (int i = 0; i < n; ++i) topk_insert(vals, idxs, count, kk, score(t, i), i);
                 m = ron;
                 for (int c = 0; c < count; ++c) m = fmaxf(m, vals[c]);
                 z = expf(ron - m);
@@ -160,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
                 m = ron;  // streaming softmax over r_on and the cached scores
                 z = 1.f;
                 for (int i = 0; i < n; ++i) {
-                    const float r = gate_score(ur, kbar + (size_t)i * D, D);
+                    const float r = score(t, i);
                     if (r > m) {
                         z = z * expf(m - r) + 1.f;
                         m = r;
@@ -193,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
             }
             return 0.f;
         }
-        return expf(gate_score(Us + t * P, kbar + (size_t)i * D, D) - m_t[t]) / z_t[t];
+        return expf(score(t, i) - m_t[t]) / z_t[t];
     };
 
     float dq[TPT][RB], dua[TPT][RB], gk[TPT][RB];
@@ -210,67 +242,75 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
         }
         if (gated && tid < D) kb[tid] = kbar[(size_t)i * D + tid];
         if (!__syncthreads_or(gi != 0.f)) continue;  // no token of the tile reads segment i
-        const float *Mi = states + (size_t)i * D * D;
-        float z1[TPT][RB];  // (M^(i) q_t) at value dims tx + 16 r
-#pragma unroll
-        for (int p = 0; p < TPT; ++p)
-#pragma unroll
-            for (int r = 0; r < RB; ++r) z1[p][r] = 0.f;
-#pragma unroll
-        for (int kc = 0; kc < D; kc += KC) {  // unrolled: dq is indexed by the block
-            for (int e = tid; e < D * KC; e += kThreads) {
-                const int vr = e / KC, c = e % KC;
-                Ms[vr * KP + c] = __ldg(Mi + (size_t)vr * D + kc + c);
-            }
-            __syncthreads();
-#pragma unroll 4
-            for (int c = 0; c < KC; ++c) {
-                float qv[TPT];
-#pragma unroll
-                for (int p = 0; p < TPT; ++p) qv[p] = Qs[(ty + 16 * p) * P + kc + c];
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    const float mv = Ms[(tx + 16 * r) * KP + c];
-#pragma unroll
-                    for (int p = 0; p < TPT; ++p) z1[p][r] = fmaf(qv[p], mv, z1[p][r]);
-                }
-            }
-            // (M^(i)^T dy_t) at the block's key dims kc + tx + 16 r2
-            float z2[TPT][RK];
+        float dgv[TPT];  // dg_{t,i} = dy_t . (M^(i) q_t), complete in every lane of the token's group
+        {
+            const float *Mi = states + (size_t)i * D * D;
+            float z1[TPT][RB];  // (M^(i) q_t) at value dims tx + 16 r
 #pragma unroll
             for (int p = 0; p < TPT; ++p)
 #pragma unroll
-                for (int r2 = 0; r2 < RK; ++r2) z2[p][r2] = 0.f;
-#pragma unroll 4
-            for (int vr = 0; vr < D; ++vr) {
-                float yv[TPT];
+                for (int r = 0; r < RB; ++r) z1[p][r] = 0.f;
 #pragma unroll
-                for (int p = 0; p < TPT; ++p) yv[p] = Ys[(ty + 16 * p) * P + vr];
-#pragma unroll
-                for (int r2 = 0; r2 < RK; ++r2) {
-                    const float mv = Ms[vr * KP + tx + 16 * r2];
-#pragma unroll
-                    for (int p = 0; p < TPT; ++p) z2[p][r2] = fmaf(yv[p], mv, z2[p][r2]);
+            for (int kc = 0; kc < D; kc += KC) {  // unrolled: dq is indexed by the block
+                for (int e = tid; e < D * KC; e += kThreads) {
+                    const int vr = e / KC, c = e % KC;
+                    Ms[vr * KP + c] = __ldg(Mi + (size_t)vr * D + kc + c);
                 }
+                __syncthreads();
+#pragma unroll 4
+                for (int c = 0; c < KC; ++c) {
+                    float qv[TPT];
+#pragma unroll
+                    for (int p = 0; p < TPT; ++p) qv[p] = Qs[(ty + 16 * p) * P + kc + c];
+#pragma unroll
+                    for (int r = 0; r < RB; ++r) {
+                        const float mv = Ms[(tx + 16 * r) * KP + c];
+#pragma unroll
+                        for (int p = 0; p < TPT; ++p) z1[p][r] = fmaf(qv[p], mv, z1[p][r]);
+                    }
+                }
+                // (M^(i)^T dy_t) at the block's key dims kc + tx + 16 r2
+                float z2[TPT][RK];
+#pragma unroll
+                for (int p = 0; p < TPT; ++p)
+#pragma unroll
+                    for (int r2 = 0; r2 < RK; ++r2) z2[p][r2] = 0.f;
+#pragma unroll 4
+                for (int vr = 0; vr < D; ++vr) {
+                    float yv[TPT];
+#pragma unroll
+                    for (int p = 0; p < TPT; ++p) yv[p] = Ys[(ty + 16 * p) * P + vr];
+#pragma unroll
+                    for (int r2 = 0; r2 < RK; ++r2) {
+                        const float mv = Ms[vr * KP + tx + 16 * r2];
+#pragma unroll
+                        for (int p = 0; p < TPT; ++p) z2[p][r2] = fmaf(yv[p], mv, z2[p][r2]);
+                    }
+                }
+#pragma unroll
+                for (int p = 0; p < TPT; ++p) {
+                    const float g = gb[ty + 16 * p];
+#pragma unroll
+                    for (int r2 = 0; r2 < RK; ++r2) dq[p][kc / 16 + r2] = fmaf(g, z2[p][r2], dq[p][kc / 16 + r2]);
+                }
+                __syncthreads();
             }
+            // partial over this thread's dims, then the 16 lanes of the token
 #pragma unroll
             for (int p = 0; p < TPT; ++p) {
-                const float g = gb[ty + 16 * p];
+                const int t = ty + 16 * p;
+                float part = 0.f;
 #pragma unroll
-                for (int r2 = 0; r2 < RK; ++r2) dq[p][kc / 16 + r2] = fmaf(g, z2[p][r2], dq[p][kc / 16 + r2]);
+                for (int r = 0; r < RB; ++r) part = fmaf(Ys[t * P + tx + 16 * r], z1[p][r], part);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                dgv[p] = part;
             }
-            __syncthreads();
         }
-        // dg_{t,i} = dy_t . (M^(i) q_t): partial over this thread's dims, then the 16 lanes of the token
 #pragma unroll
         for (int p = 0; p < TPT; ++p) {
             const int t = ty + 16 * p;
-            float part = 0.f;
-#pragma unroll
-            for (int r = 0; r < RB; ++r) part = fmaf(Ys[t * P + tx + 16 * r], z1[p][r], part);
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            const float c = gb[t] * part;  // g dg
+            const float c = gb[t] * dgv[p];  // g dg
             if (gated) {
 #pragma unroll
                 for (int r = 0; r < RB; ++r) {
@@ -369,6 +409,242 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
             __syncthreads();
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_route_simt: the gate work of the tensor-core backward, one CTA per (bh,
+// segment n, tile of kTB tokens), on whole tables in shared memory (n <= 63):
+//   scores r_{t,i} = <u_t, kbar_i>, the gates g_{t,i} (GRM / Soup softmax with the
+//   online score; SSC over the topk largest, equal scores to the lower index;
+//   Residual 1; Mean 1 / (n + 1)); with gates_only the gates go to gam and nothing
+//   else happens.  Otherwise, with dg_{t,i} from the tensor cores:
+//   delta_t = sum_i g dg + g_on dg_on,  dr_{t,i} = g (dg - delta) -> dr,
+//   du_t = sum_i dr_{t,i} kbar_i + dr_on p_t,  dq_t = (cached part) + g_on M_t^T dy_t.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
+{
+    constexpr int P = D + 1;
+    constexpr int RB = D / 16;
+    constexpr int TPT = kTB / 16;
+    extern __shared__ float sm[];
+    float *Us = sm;              // kTB x P: u for the scores, then the running key sums of the tile
+    float *Kc = Us;
+    float *gt = Us + kTB * P;    // kTB x kTab: scores, then gates
+    float *dt = gt + kTB * kTab; // kTB x kTab: dg, then dr
+    float *kpre = dt + kTB * kTab;  // D
+    float *m_t = kpre + D, *z_t = m_t + kTB, *gon = z_t + kTB, *dl = gon + kTB, *dgo = dl + kTB;
+    uint64_t *chosen = reinterpret_cast<uint64_t *>(dgo + kTB);  // SSC: the selected cached segments of a token
+
+    const int tps = (a.C + kTB - 1) / kTB;
+    const int per_seg = a.BH * tps;
+    const int n = a.N - 1 - (int)(blockIdx.x / per_seg);
+    const int rem = blockIdx.x % per_seg;
+    const int bh = rem / tps, tile = rem % tps;
+    const int t0 = n * a.C;
+    const int tb = t0 + tile * kTB;
+    const int te = min(min(tb + kTB, t0 + a.C), a.L);
+    if (tb >= te) return;
+    const int cnt = te - tb;
+    const int mode = a.mode;
+    const bool gated = gated_mode(mode);
+    const bool finish = !a.gates_only;
+    const size_t base = (size_t)bh * a.L * D;
+    const T *k = static_cast<const T *>(a.k) + base, *dy = static_cast<const T *>(a.dy) + base;
+    const T *u = gated ? static_cast<const T *>(a.u) + base : nullptr;
+    const float *kbar = a.kbar + (size_t)bh * a.N * D;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const size_t seg_base = (size_t)bh * a.N * a.L + tb;  // [N][L] tables of this head, at the tile
+
+    for (int e = tid; e < kTB * D; e += kThreads) {
+        const int r = e / D, c = e % D;
+        Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
+    }
+    const bool need_kpre = gated && finish;
+    if (need_kpre && tid < D) kpre[tid] = 0.f;
+    __syncthreads();
+    if (need_kpre) {  // keys of the segment before the tile: a strided share per thread, four loads in flight
+        constexpr int parts = kThreads / D;
+        const int col = tid % D, part = tid / D;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int j = t0 + part;
+        for (; j + 3 * parts < tb; j += 4 * parts) {
+            s0 += to_f(k[(size_t)j * D + col]);
+            s1 += to_f(k[(size_t)(j + parts) * D + col]);
+            s2 += to_f(k[(size_t)(j + 2 * parts) * D + col]);
+            s3 += to_f(k[(size_t)(j + 3 * parts) * D + col]);
+        }
+        for (; j < tb; j += parts) s0 += to_f(k[(size_t)j * D + col]);
+        atomicAdd(&kpre[col], (s0 + s1) + (s2 + s3));
+    }
+    if (gated)  // scores: a warp takes 32 tokens of one segment (its kbar row broadcast)
+        for (int e = tid; e < kTB * n; e += kThreads) {
+            const int i = e / kTB, t = e % kTB;
+            gt[t * kTab + i] = t < cnt ? gate_score(Us + t * P, kbar + (size_t)i * D, D) : 0.f;
+        }
+    __syncthreads();
+    if (finish && gated) {  // u is spent: the buffer takes the tile's keys, then their running sums per column
+        for (int e = tid; e < kTB * D; e += kThreads) {
+            const int r = e / D, c = e % D;
+            Kc[r * P + c] = r < cnt ? to_f(k[(size_t)(tb + r) * D + c]) : 0.f;
+        }
+        __syncthreads();
+        if (tid < D) {
+            float s = 0.f;
+            for (int r = 0; r < cnt; ++r) {
+                s += Kc[r * P + tid];
+                Kc[r * P + tid] = s;
+            }
+        }
+    }
+
+    // per token: softmax max and sum (with the online score), the SSC selection, the online gate
+    if (tid < kTB) {
+        const int t = tid;
+        float go = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f, m = 0.f, z = 1.f;
+        uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
+        if (t < cnt && gated) {
+            const float ron = a.r_on[(size_t)bh * a.L + tb + t];
+            const float *sr = gt + t * kTab;
+            if (mode == MC_SSC) {
+                uint64_t pick = 0;
+                const int kk = min(a.topk, n);
+                for (int r = 0; r < kk; ++r) {  // the largest unpicked score, the lower index on ties
+                    int bi = -1;
+                    for (int i = 0; i < n; ++i)
+                        if (!((pick >> i) & 1ull) && (bi < 0 || sr[i] > sr[bi])) bi = i;
+                    pick |= 1ull << bi;
+                }
+                take = pick;
+            }
+            m = ron;
+            for (int i = 0; i < n; ++i)
+                if ((take >> i) & 1ull) m = fmaxf(m, sr[i]);
+            z = expf(ron - m);
+            for (int i = 0; i < n; ++i)
+                if ((take >> i) & 1ull) z += expf(sr[i] - m);
+            go = expf(ron - m) / z;
+        }
+        m_t[t] = m;
+        z_t[t] = z;
+        gon[t] = t < cnt ? go : 0.f;
+        chosen[t] = take;
+    }
+    __syncthreads();
+    // gates in place of the scores
+    for (int e = tid; e < kTB * n; e += kThreads) {
+        const int i = e / kTB, t = e % kTB;
+        float g = 0.f;
+        if (t < cnt) {
+            if (!gated) g = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
+            else if ((chosen[t] >> i) & 1ull) g = expf(gt[t * kTab + i] - m_t[t]) / z_t[t];
+        }
+        gt[t * kTab + i] = g;
+        if (!finish && a.gam && t < cnt) a.gam[seg_base + (size_t)i * a.L + t] = g;
+        if (finish) dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
+    }
+    if (!finish) return;
+
+    // the online memory's dg: dy_t . O_on[t] over the token's 16 lanes
+    const float *Oon = a.O_on + base, *Xon = a.X_on + base;
+#pragma unroll
+    for (int p = 0; p < TPT; ++p) {
+        const int t = ty + 16 * p;
+        float part = 0.f;
+        if (t < cnt) {
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const size_t gi = (size_t)(tb + t) * D + tx + 16 * r;
+                part = fmaf(to_f(dy[gi]), Oon[gi], part);
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (tx == 0) dgo[t] = part;
+    }
+    __syncthreads();
+    if (tid < kTB) {  // delta_t = sum_i g dg + g_on dg_on
+        const int t = tid;
+        float s = gon[t] * dgo[t];
+        for (int i = 0; i < n; ++i) s = fmaf(gt[t * kTab + i], dt[t * kTab + i], s);
+        dl[t] = s;
+    }
+    __syncthreads();
+    // dr = g (dg - delta), in place, and out for the key-mean gradient
+    for (int e = tid; e < kTB * n; e += kThreads) {
+        const int i = e / kTB, t = e % kTB;
+        const float dr = gt[t * kTab + i] * (dt[t * kTab + i] - dl[t]);
+        dt[t * kTab + i] = dr;
+        if (t < cnt && gated) a.dr[seg_base + (size_t)i * a.L + t] = dr;
+    }
+    __syncthreads();
+
+    T *dqo = static_cast<T *>(a.dq) + base;
+    T *duo = gated ? static_cast<T *>(a.du) + base : nullptr;
+    float *tok = a.tok + ((size_t)bh * a.L + tb) * kBwdTokWords;
+#pragma unroll
+    for (int p = 0; p < TPT; ++p) {
+        const int t = ty + 16 * p;
+        if (t >= cnt) continue;
+        const float dron = gon[t] * (dgo[t] - dl[t]);  // dr of the online memory
+        const float inv_cnt = 1.f / (float)(tb + t - t0 + 1);
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int c = tx + 16 * r;
+            const size_t gi = (size_t)(tb + t) * D + c;
+            dqo[gi] = from_f<T>(a.dq_in[((size_t)bh * a.L + tb + t) * D + c] + gon[t] * Xon[gi]);
+            if (gated) {
+                float du = dron * (kpre[c] + Kc[t * P + c]) * inv_cnt;
+                for (int i = 0; i < n; ++i) du = fmaf(dt[t * kTab + i], __ldg(kbar + (size_t)i * D + c), du);
+                duo[gi] = from_f<T>(du);
+            }
+        }
+        if (tx == 0) {
+            float *w = tok + (size_t)t * kBwdTokWords;
+            w[0] = m_t[t];
+            w[1] = z_t[t];
+            w[2] = gon[t];
+            w[3] = dl[t];
+            w[4] = gated ? dron * inv_cnt : 0.f;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_dkbar_simt: the key-mean gradient of a cached segment from the score
+// gradients, dkbar_i = sum_{t >= (i+1) C} dr_{t,i} u_t.  One CTA per (bh, i < N-1,
+// chunk of kDkChunk later tokens); a thread sums a dimension over a strided share
+// of the chunk (four tokens in flight), the CTA adds its sum to dkbar (zeroed first).
+// ---------------------------------------------------------------------------
+constexpr int kDkChunk = 1024;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks)
+{
+    __shared__ float part[D];
+    const int ch = (int)blockIdx.x % chunks, rest = (int)blockIdx.x / chunks;
+    const int i = rest / a.BH, bh = rest % a.BH;
+    const int t_lo = (i + 1) * a.C + ch * kDkChunk;
+    if (t_lo >= a.L) return;
+    const int t_hi = min(t_lo + kDkChunk, a.L);
+    constexpr int parts = kThreads / D;
+    const int col = threadIdx.x % D, p = threadIdx.x / D;
+    if (threadIdx.x < D) part[threadIdx.x] = 0.f;
+    __syncthreads();
+    const T *u = static_cast<const T *>(a.u) + (size_t)bh * a.L * D + col;
+    const float *dr = a.dr + ((size_t)bh * a.N + i) * a.L;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int t = t_lo + p;
+    for (; t + 3 * parts < t_hi; t += 4 * parts) {
+        s0 = fmaf(__ldg(dr + t), to_f(u[(size_t)t * D]), s0);
+        s1 = fmaf(__ldg(dr + t + parts), to_f(u[(size_t)(t + parts) * D]), s1);
+        s2 = fmaf(__ldg(dr + t + 2 * parts), to_f(u[(size_t)(t + 2 * parts) * D]), s2);
+        s3 = fmaf(__ldg(dr + t + 3 * parts), to_f(u[(size_t)(t + 3 * parts) * D]), s3);
+    }
+    for (; t < t_hi; t += parts) s0 = fmaf(__ldg(dr + t), to_f(u[(size_t)t * D]), s0);
+    atomicAdd(&part[col], (s0 + s1) + (s2 + s3));
+    __syncthreads();
+    if (threadIdx.x < D) atomicAdd(a.dkbar + ((size_t)bh * a.N + i) * D + threadIdx.x, part[threadIdx.x]);
 }
 
 // ---------------------------------------------------------------------------
@@ -617,21 +893,28 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_simt(BwdArgs a)
 }
 
 template <typename T, int D>
-cudaError_t backward_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
+cudaError_t gates_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 {
     constexpr int P = D + 1;
     constexpr int KC = D < 32 ? D : 32;
-    cudaError_t e;
-    {
-        const size_t smem = sizeof(float) * (4 * kTB * P + D * (KC + 1) + 2 * D + 6 * kTB + kTB * kMaxTopk) +
-                            sizeof(int) * (kTB * kMaxTopk + 2 * kTB);
-        auto kern = bwd_gates_simt<T, D>;
-        if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-        const long long tps = (p.C + kTB - 1) / kTB;
-        kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        profile_after_kernel(s, "bwd_gates_simt");
-    }
+    const size_t smem = sizeof(float) * (4 * kTB * P + D * (KC + 1) + 2 * D + 6 * kTB + kTB * kMaxTopk + kTB * kTab) +
+                        sizeof(int) * (kTB * kMaxTopk + 2 * kTB);
+    auto kern = bwd_gates_simt<T, D>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    const long long tps = (p.C + kTB - 1) / kTB;
+    kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_after_kernel(s, "bwd_gates_simt");
+    return cudaSuccess;
+}
+
+template <typename T, int D>
+cudaError_t backward_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
+{
+    constexpr int P = D + 1;
+    cudaError_t e = gates_impl<T, D>(p, a, s);
+    if (e != cudaSuccess) return e;
     if (p.N > 1) {
         const size_t smem = sizeof(float) * (3 * kTG * P + kTG);
         auto kern = bwd_G_simt<T, D>;
@@ -653,18 +936,63 @@ cudaError_t backward_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     return cudaSuccess;
 }
 
-#define MC_BWD_DISPATCH(p, a, s)                                                                   \
+#define MC_BWD_DISPATCH(FN, p, a, s)                                                                 \
     do {                                                                                           \
         switch ((p).d) {                                                                           \
-        case 16: return (p).bf16 ? backward_impl<__nv_bfloat16, 16>(p, a, s) : backward_impl<float, 16>(p, a, s);   \
-        case 32: return (p).bf16 ? backward_impl<__nv_bfloat16, 32>(p, a, s) : backward_impl<float, 32>(p, a, s);   \
-        case 64: return (p).bf16 ? backward_impl<__nv_bfloat16, 64>(p, a, s) : backward_impl<float, 64>(p, a, s);   \
-        case 128: return (p).bf16 ? backward_impl<__nv_bfloat16, 128>(p, a, s) : backward_impl<float, 128>(p, a, s); \
+        case 16: return (p).bf16 ? FN<__nv_bfloat16, 16>(p, a, s) : FN<float, 16>(p, a, s);   \
+        case 32: return (p).bf16 ? FN<__nv_bfloat16, 32>(p, a, s) : FN<float, 32>(p, a, s);   \
+        case 64: return (p).bf16 ? FN<__nv_bfloat16, 64>(p, a, s) : FN<float, 64>(p, a, s);   \
+        case 128: return (p).bf16 ? FN<__nv_bfloat16, 128>(p, a, s) : FN<float, 128>(p, a, s); \
         default: return cudaErrorInvalidValue;                                                     \
         }                                                                                          \
     } while (0)
 
-cudaError_t launch_bwd_kernels(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(p, a, s); }
+template <typename T, int D>
+cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
+{
+    constexpr int P = D + 1;
+    const size_t smem = sizeof(float) * (kTB * P + 2 * kTB * kTab + D + 5 * kTB) + sizeof(uint64_t) * kTB;
+    auto kern = bwd_route_simt<T, D>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    const long long tps = (p.C + kTB - 1) / kTB;
+    kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_after_kernel(s, "bwd_route_simt");
+    if (!a.gates_only && a.dr && p.N > 1) {
+        const int chunks = (p.L - p.C + kDkChunk - 1) / kDkChunk;
+        bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * (p.N - 1) * chunks), kThreads, 0, s>>>(a, chunks);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        profile_after_kernel(s, "bwd_dkbar_simt");
+    }
+    return cudaSuccess;
+}
+
+// The tensor-core path after the cached pass: the gate work, G on the tensor cores, the reverse scan.
+template <typename T, int D>
+cudaError_t backward_tc_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
+{
+    constexpr int P = D + 1;
+    constexpr int TC = D >= 128 ? 32 : 64;
+    constexpr int TP = TC + 1;
+    cudaError_t e = route_impl<T, D>(p, a, s);
+    if (e != cudaSuccess) return e;
+    if (p.N > 1) {
+        if ((e = launch_bwd_G_tc(p, a.dy, a.q, a.gam, a.G, s)) != cudaSuccess) return e;
+        profile_after_kernel(s, "bwd_G_tc");
+    }
+    const size_t smem = sizeof(float) * (5 * TC * P + D * P + 2 * TC * TP + D);
+    auto kern = bwd_scan_simt<T, D, TC>;
+    if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
+    kern<<<(unsigned)((long long)p.BH * p.N), kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_after_kernel(s, "bwd_scan_simt");
+    return cudaSuccess;
+}
+
+cudaError_t launch_bwd_kernels(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(backward_impl, p, a, s); }
+cudaError_t launch_bwd_tc_rest(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(backward_tc_impl, p, a, s); }
+cudaError_t launch_bwd_route(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(route_impl, p, a, s); }
 
 size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -677,9 +1005,10 @@ size_t backward_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
     const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
+    const size_t gam = bwd_tc_supported(p) && mode_uses_u(p.mode) ? N : 0;
     return 2 * pad256(4 * BH * N * d * d) + 2 * pad256(4 * BH * N * d) + pad256(4 * BH * L) +
            2 * pad256(4 * BH * L * d) + pad256(4 * BH * L * kBwdTokWords) + pad256(4 * BH * L * sel) +
-           pad256(4 * BH * L * sel);
+           pad256(4 * BH * L * sel) + pad256(4 * BH * L * gam) + (bwd_tc_supported(p) ? bwd_cached_scratch_bytes(p) : 0);
 }
 
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
@@ -705,6 +1034,9 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
     int32_t *sel_idx = reinterpret_cast<int32_t *>(take(4 * BH * L * sel));
     float *sel_g = reinterpret_cast<float *>(take(4 * BH * L * sel));
     const bool gated = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
+    const bool tc = bwd_tc_supported(p);
+    float *gam = tc && gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
+    void *cached_scratch = tc ? take(bwd_cached_scratch_bytes(p)) : nullptr;
 
     profile_call_start(s);
     // The forward's segment scan: cached states, key means, online scores, M_t q_t.
@@ -728,8 +1060,25 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
     a.q = q; a.k = k; a.v = v; a.u = gated ? u : nullptr; a.dy = dy;
     a.dq = dq; a.dk = dk; a.dv = dv; a.du = gated ? du : nullptr;
     a.states = states; a.kbar = kbar; a.r_on = r_on; a.O_on = O_on; a.X_on = X_on;
-    a.G = G; a.dkbar = dkbar; a.tok = tok; a.sel_idx = sel_idx; a.sel_g = sel_g;
+    a.G = G; a.dkbar = dkbar; a.tok = tok; a.sel_idx = sel_idx; a.sel_g = sel_g; a.gam = gam;
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
+    if (tc) {
+        // The cached states' part on the tensor cores: the gates first (routed modes), then
+        // dg against every cached state and the cached part of dq, then the gate work on
+        // whole tables, the key-mean gradient, G on the tensor cores and the reverse scan.
+        if (gated) {
+            BwdArgs ga = a;
+            ga.gates_only = 1;
+            if ((e = launch_bwd_route(p, ga, s)) != cudaSuccess) return e;
+        }
+        float *dg = nullptr, *dqc = nullptr;
+        if ((e = launch_bwd_cached_tc(p, dy, q, states, gam, cached_scratch, &dg, &dqc, s)) != cudaSuccess) return e;
+        profile_after_kernel(s, "bwd_cached_tc");
+        a.dg_in = dg;
+        a.dq_in = dqc;
+        a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
+        return launch_bwd_tc_rest(p, a, s);
+    }
     return launch_bwd_kernels(p, a, s);
 }
 

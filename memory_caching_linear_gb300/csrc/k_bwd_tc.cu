@@ -1,0 +1,554 @@
+// k_bwd_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) kernels of the Memory Caching
+// backward pass over a linear memory, for bf16 inputs on the shapes the forward's
+// tensor-core path takes (d = 64 or 128, seg_len a multiple of 128, L a multiple of
+// seg_len, N <= 64).
+//
+// Pages cited:
+//   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
+//
+// bwd_G_tc -- the gradient of every cached state ([MC-ja §3 after eq. 4b]: the cached
+//   M^(i) is read by every token of the later segments with its gate g_{t,i}):
+//     G_i = sum_{t in segments > i} g_{t,i} dy_t q_t^T        (d_v x d_k, fp32)
+//   One CTA per (b,h, cached segment i), the segment with the most later tokens first.
+//   Per 128-token tile: the TMA brings dy and q (two 64-column 128-byte-swizzled
+//   panels each), the four worker warps scale their token's dy row by g_{t,i} in
+//   shared memory, and one thread issues D += (g o dy)^T q as eight 128x128x16 MMAs
+//   with both operands read MN-major from shared memory.
+#include <cstdint>
+
+#include "mc_internal.cuh"
+#include "sm100.cuh"
+#include "tensormap.cuh"
+
+namespace mc {
+
+// Set by a backward tensor-core kernel that abandoned its work after a bounded wait
+// ran out; read and cleared by mc_check_device().
+__device__ int g_bwd_abort;
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kGT = 128;             // tokens per tile
+constexpr uint32_t kGTile = 32768;   // one 128 x 128 bf16 operand tile (two 16 KB panels)
+constexpr int kGStages = 3;          // (dy, q) tile pairs in flight
+constexpr int kGThreads = 192;       // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
+constexpr size_t kGSmem = kGStages * 2 * kGTile + 1024;
+
+struct GArgs {
+    const float *gam;  // [BH][N][L]: g_{t,i} of the cached segments (routed aggregations)
+    float *G;          // [BH][N][d][d]
+    int BH, L, C, N, d, mode;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    bwd_G_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, GArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t full[kGStages], scaled[kGStages], empty[kGStages], done;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;
+    const int t_begin = (i + 1) * a.C;
+    const int ntiles = (a.L - t_begin) / kGT;
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 128);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        abort_flag = 0;
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&scaled[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&done, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_base;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&mY);
+            prefetch_tensormap(&mQ);
+            int issued = 0;
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % kGStages;
+                if (!mbar_wait(&empty[s], ((j / kGStages) & 1) ^ 1, &abort_flag)) break;
+                uint8_t *st = sm + s * 2 * kGTile;
+                const int row = bh * a.L + t_begin + j * kGT;
+                mbar_arrive_expect_tx(&full[s], 2 * kGTile);
+                tma_load_2d(st, &mY, 0, row, &full[s]);
+                tma_load_2d(st + 16384, &mY, 64, row, &full[s]);
+                tma_load_2d(st + kGTile, &mQ, 0, row, &full[s]);
+                tma_load_2d(st + kGTile + 16384, &mQ, 64, row, &full[s]);
+                issued = j + 1;
+            }
+            // leave no copy in flight
+            int give_up = 0;
+            for (int j = issued > kGStages ? issued - kGStages : 0; j < issued; ++j)
+                mbar_wait_limit(&full[j % kGStages], (j / kGStages) & 1, &give_up, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idG = idesc_bf16(128, 128, true, true);  // A = (g o dy)^T, B = q: both MN-major
+            bool ok = true;
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int s = j % kGStages;
+                if (!(ok = mbar_wait(&scaled[s], (j / kGStages) & 1, &abort_flag))) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sm + s * 2 * kGTile), b0 = a0 + kGTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // 16 tokens per step: 16 rows of 128 bytes
+                    mma_ss(tD, make_desc_sw128(a0 + kk * 2048u, 16384, 1024), make_desc_sw128(b0 + kk * 2048u, 16384, 1024),
+                           idG, (j | kk) != 0);
+                mma_commit(&empty[s]);
+            }
+            // leave no MMA in flight; the drain waits for this
+            mma_commit(&done);
+        }
+    } else {
+        // ---------------------------------------------------------- workers: token row r of each tile
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
+        const float *grow = routed ? a.gam + ((size_t)bh * a.N + i) * a.L + t_begin + r : nullptr;
+        auto gate = [&](int j) -> float {  // g_{t,i} of this thread's token in tile j
+            const int t = t_begin + j * kGT + r;
+            return routed ? __ldg(grow + (size_t)j * kGT) : (a.mode == MC_MEAN ? 1.f / (float)(t / a.C + 1) : 1.f);
+        };
+        float g_next = ntiles > 0 ? gate(0) : 0.f;
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j % kGStages;
+            const float g = g_next;
+            if (j + 1 < ntiles) g_next = gate(j + 1);  // in flight while this tile is scaled
+            if (!mbar_wait(&full[s], (j / kGStages) & 1, &abort_flag)) break;
+            const __nv_bfloat162 g2 = __float2bfloat162_rn(g);
+            uint8_t *row = sm + s * 2 * kGTile + r * 128;  // the row's 128 bytes in each panel (order within is swizzled)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 *p = reinterpret_cast<uint4 *>(row + h * 16384 + c * 16);
+                    uint4 x = *p;
+                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&x);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) e[k] = __hmul2(e[k], g2);
+                    *p = x;
+                }
+            fence_async_smem();  // the tensor core reads what these threads wrote
+            mbar_arrive(&scaled[s]);
+        }
+        // drain: TMEM lane = value dim (row of G), thread = lane
+        const bool got = mbar_wait(&done, 0, &abort_flag);
+        tc_fence_after();
+        if (32 * q4 < a.d) {  // warp-uniform (d = 64 stores the first 64 rows and columns)
+            float *Go = a.G + (((size_t)bh * a.N + i) * a.d + r) * a.d;
+            for (int c0 = 0; c0 < a.d; c0 += 32) {
+                uint32_t x[32];
+                tmem_ld32(tD + ((uint32_t)(32 * q4) << 16) + c0, x);
+                tmem_wait_ld();
+                if (got) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4 *>(Go + c0 + k) =
+                            make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
+                                        __uint_as_float(x[k + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tD, 128);
+    }
+    if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
+}
+
+// ============================================================================
+// state_images_bwd -- the cached states M^(i) (fp32 [d][d]) as bf16 operand images:
+// a 128 x 128 tile, rows = value dim, two 64-column 128-byte-swizzled panels of key
+// dims (16-byte chunk c of row r at chunk c ^ (r % 8)), zero beyond d.
+// ============================================================================
+__global__ void __launch_bounds__(128) state_images_bwd(const float *__restrict__ states, uint8_t *images, int d)
+{
+    const int r = threadIdx.x;
+    const float *src = states + (size_t)blockIdx.x * d * d + (size_t)r * d;
+    uint8_t *dst = images + (size_t)blockIdx.x * kGTile + r * 128;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int col = 64 * h + 8 * c + 2 * k;
+                const float lo = r < d && col < d ? src[col] : 0.f;
+                const float hi = r < d && col + 1 < d ? src[col + 1] : 0.f;
+                w[k] = pack_bf16x2(lo, hi);
+            }
+            *reinterpret_cast<uint4 *>(dst + h * 16384 + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+}
+
+// ============================================================================
+// bwd_cached_tc -- per 128-token tile (b,h, segment n, chunk c) and cached segment
+// i < n, with W_i = dY M^(i) (d_k wide):
+//   dg_{t,i} = q_t . W_i[t]  (= dy_t . M^(i) q_t, the gate's gradient)
+//   dq_t    += (g_{t,i} dy_t) M^(i)^T summed over i  (the cached part of dq)
+// Persistent, one CTA per SM; tiles with the most cached segments first.  Warp 0
+// streams dy and q of the tile (TMA) and one 32 KB state image per segment through a
+// three-slot ring; warp 1 issues W_i = dY M^(i) (SS, image read MN-major) into one of
+// two W accumulators and D_q += (g_i o dY) M^(i)^T (TS, the same image) into D_q;
+// warps 2-5 own a token row each: they write g_i o dy into one of two A slots, read
+// W_i to form dg, and drain D_q at the end of the tile.
+// TMEM: D_q [0,128) | W0 [128,256) | W1 [256,384) | A0 [384,448) | A1 [448,512).
+// ============================================================================
+constexpr int kCRing = 3;
+constexpr int kCThreads = 192;
+constexpr size_t kCSmem = 2 * kGTile + kCRing * kGTile + 1024;
+
+struct CArgs {
+    const uint8_t *images;  // [BH][N] x 32 KB state images
+    const float *gam;       // [BH][N][L] gates of the cached segments (routed aggregations)
+    float *dg;              // [BH][N][L] out: dy_t . M^(i) q_t
+    float *dq;              // [BH][L][d] out: the cached part of dq (fp32)
+    int BH, L, C, N, CPS, d, mode, num_tiles;
+};
+
+__global__ void __launch_bounds__(kCThreads, 1)
+    bwd_cached_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, CArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *sY = sm, *sQ = sm + kGTile, *ring = sm + 2 * kGTile;
+    __shared__ uint64_t tile_full, tile_empty, ring_full[kCRing], ring_empty[kCRing];
+    __shared__ uint64_t w_full[2], w_empty[2], a_full[2], a_empty[2], dq_full, dq_empty, fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int my_tiles = blockIdx.x < (unsigned)a.num_tiles ? (a.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile = [&](int j, int &bh, int &n, int &c) {  // heaviest first: n = N-1 down to 1
+        const int id = (int)blockIdx.x + j * (int)gridDim.x;
+        const int per = a.BH * a.CPS;
+        n = a.N - 1 - id / per;
+        c = (id % per) / a.BH;
+        bh = (id % per) % a.BH;
+    };
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        abort_flag = 0;
+        mbar_init(&tile_full, 1);
+        mbar_init(&tile_empty, 1 + 128);  // the tile's last W MMAs + every worker has its rows
+        for (int s = 0; s < kCRing; ++s) {
+            mbar_init(&ring_full[s], 1);
+            mbar_init(&ring_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], 128);
+            mbar_init(&a_full[s], 128);
+            mbar_init(&a_empty[s], 1);
+        }
+        mbar_init(&dq_full, 1);
+        mbar_init(&dq_empty, 128);
+        mbar_init(&fin, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    const uint32_t tDq = tb, tW0 = tb + 128, tA0 = tb + 384;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0 && my_tiles > 0) {
+            prefetch_tensormap(&mY);
+            prefetch_tensormap(&mQ);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                int bh, n, c;
+                tile(j, bh, n, c);
+                if (!(ok = mbar_wait(&tile_empty, (j & 1) ^ 1, &abort_flag))) break;
+                const int row = bh * a.L + n * a.C + c * kGT;
+                mbar_arrive_expect_tx(&tile_full, 2 * kGTile);
+                tma_load_2d(sY, &mY, 0, row, &tile_full);
+                tma_load_2d(sY + 16384, &mY, 64, row, &tile_full);
+                tma_load_2d(sQ, &mQ, 0, row, &tile_full);
+                tma_load_2d(sQ + 16384, &mQ, 64, row, &tile_full);
+                for (int i = 0; i < n && ok; ++i, ++g) {
+                    const int s = g % kCRing;
+                    if (!(ok = mbar_wait(&ring_empty[s], ((g / kCRing) & 1) ^ 1, &abort_flag))) break;
+                    mbar_arrive_expect_tx(&ring_full[s], kGTile);
+                    bulk_load(ring + s * kGTile, a.images + ((size_t)bh * a.N + i) * kGTile, kGTile, &ring_full[s]);
+                }
+            }
+            // leave no copy in flight: the last use of every slot has landed
+            int give_up = 0;
+            for (uint32_t k = 0; k < (uint32_t)kCRing && k < g; ++k) {
+                const uint32_t u = g - 1 - k;
+                mbar_wait_limit(&ring_full[u % kCRing], (u / kCRing) & 1, &give_up, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && my_tiles > 0) {
+            constexpr uint32_t idW = idesc_bf16(128, 128, false, true);  // A = dY K-major, B = image MN-major
+            uint32_t g = 0;
+            bool ok = true;
+            const uint32_t y0 = smem_u32(sY), r0 = smem_u32(ring);
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                int bh, n, c;
+                tile(j, bh, n, c);
+                if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
+                for (int i = 0; i < n && ok; ++i, ++g) {
+                    const uint32_t s = g % kCRing, w = g % 2;
+                    if (!(ok = mbar_wait(&ring_full[s], (g / kCRing) & 1, &abort_flag) &&
+                               mbar_wait(&w_empty[w], ((g / 2) & 1) ^ 1, &abort_flag)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t img = r0 + s * kGTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tW0 + w * 128, make_desc_sw128(y0 + (kk >> 2) * 16384u + (kk & 3) * 32u, 0, 1024),
+                               make_desc_sw128(img + kk * 2048u, 16384, 1024), idW, kk > 0);
+                    mma_commit(&w_full[w]);
+                    if (i == n - 1) mma_commit(&tile_empty);  // dY is no longer read
+                    // D_q += (g_i o dY) M^(i)^T once the workers have written the A slot
+                    if (!(ok = mbar_wait(&a_full[w], (g / 2) & 1, &abort_flag))) break;
+                    if (i == 0 && !(ok = mbar_wait(&dq_empty, (j & 1) ^ 1, &abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tDq, tA0 + w * 64 + kk * 8, make_desc_sw128(img + kk * 2048u, 16384, 1024), idW,
+                               (i | kk) != 0);
+                    mma_commit(&a_empty[w]);
+                    mma_commit(&ring_empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&dq_full);
+            }
+            // leave no MMA in flight
+            mma_commit(&fin);
+            int give_up = 0;
+            mbar_wait_limit(&fin, 0, &give_up, kWaitLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------------- workers (thread = token row)
+        const int q4 = warp & 3;
+        const uint32_t row = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int j = 0; j < my_tiles && ok; ++j) {
+            int bh, n, c;
+            tile(j, bh, n, c);
+            const int t = n * a.C + c * kGT + row;  // token within the head
+            if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
+            // the token's q and dy rows (128-byte swizzle: chunk c of row r at chunk c ^ (r % 8))
+            uint32_t qp[64], yp[64];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint32_t off = h * 16384 + row * 128 + ((cc ^ (row & 7)) << 4);
+                    const uint4 xq = *reinterpret_cast<const uint4 *>(sQ + off);
+                    const uint4 xy = *reinterpret_cast<const uint4 *>(sY + off);
+                    qp[32 * h + 4 * cc] = xq.x; qp[32 * h + 4 * cc + 1] = xq.y;
+                    qp[32 * h + 4 * cc + 2] = xq.z; qp[32 * h + 4 * cc + 3] = xq.w;
+                    yp[32 * h + 4 * cc] = xy.x; yp[32 * h + 4 * cc + 1] = xy.y;
+                    yp[32 * h + 4 * cc + 2] = xy.z; yp[32 * h + 4 * cc + 3] = xy.w;
+                }
+            mbar_arrive(&tile_empty);
+            const float *grow = routed ? a.gam + (size_t)bh * a.N * a.L + t : nullptr;
+            float *dgrow = a.dg + (size_t)bh * a.N * a.L + t;
+            const float gconst = a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
+            float gnext = n > 0 ? (routed ? __ldg(grow) : gconst) : 0.f;
+            for (int i = 0; i < n && ok; ++i, ++g) {
+                const uint32_t w = g % 2;
+                const float gi = gnext;
+                if (i + 1 < n) gnext = routed ? __ldg(grow + (size_t)(i + 1) * a.L) : gconst;
+                // A slot w <- g_i o dy
+                if (!(ok = mbar_wait(&a_empty[w], ((g / 2) & 1) ^ 1, &abort_flag))) break;
+                tc_fence_after();
+                {
+                    const __nv_bfloat162 g2 = __float2bfloat162_rn(gi);
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&yp[32 * m + k]);
+                            __nv_bfloat162 pr = __hmul2(x, g2);
+                            r[k] = *reinterpret_cast<uint32_t *>(&pr);
+                        }
+                        tmem_st32(tA0 + w * 64 + lane_base + 32 * m, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&a_full[w]);
+                // dg = q . W_i
+                if (!(ok = mbar_wait(&w_full[w], (g / 2) & 1, &abort_flag))) break;
+                tc_fence_after();
+                float dg0 = 0.f, dg1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t x[32];
+                    tmem_ld32(tW0 + w * 128 + lane_base + 32 * m, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const uint32_t qq = qp[16 * m + k];
+                        dg0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), dg0);
+                        dg1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), dg1);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&w_empty[w]);
+                dgrow[(size_t)i * a.L] = dg0 + dg1;
+            }
+            if (!ok) break;
+            // drain D_q: the cached part of dq for this token
+            if (!(ok = mbar_wait(&dq_full, j & 1, &abort_flag))) break;
+            tc_fence_after();
+            float *dqrow = a.dq + ((size_t)bh * a.L + t) * a.d;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint32_t x[32];
+                tmem_ld32(tDq + lane_base + 32 * m, x);
+                tmem_wait_ld();
+                if (32 * m < a.d) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4 *>(dqrow + 32 * m + k) =
+                            make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
+                                        __uint_as_float(x[k + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&dq_empty);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+    if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const Problem &p)
+{
+    return p.bf16 && (p.d == 128 || p.d == 64) && p.C % kGT == 0 && p.L % p.C == 0 && p.N <= 64;
+}
+
+cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, float *G, cudaStream_t s)
+{
+    if (p.N < 2) return cudaSuccess;
+    CUtensorMap mY, mQ;
+    const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    // a 64-wide tensor reads its second panel out of bounds: the TMA fills zeros
+    if (!make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT))
+        return cudaErrorInvalidValue;
+    GArgs a{};
+    a.gam = gam;
+    a.G = G;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.d = p.d; a.mode = p.mode;
+    cudaError_t e = cudaFuncSetAttribute(bwd_G_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+    if (e != cudaSuccess) return e;
+    bwd_G_tc<<<(unsigned)(p.BH * (p.N - 1)), kGThreads, kGSmem, s>>>(mY, mQ, a);
+    return cudaGetLastError();
+}
+
+cudaError_t take_bwd_abort(int *was_set)
+{
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_bwd_abort, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *was_set = v;
+    if (v) {
+        v = 0;
+        e = cudaMemcpyToSymbol(g_bwd_abort, &v, sizeof(int));
+    }
+    return e;
+}
+
+}  // namespace mc
+
+namespace mc {
+
+size_t bwd_cached_scratch_bytes(const Problem &p)
+{
+    const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
+    auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    return pad(BH * N * kGTile) + pad(4 * BH * N * L) + pad(4 * BH * L * d);
+}
+
+cudaError_t launch_bwd_cached_tc(const Problem &p, const void *dy, const void *q, const float *states, const float *gam,
+                                 void *scratch, float **dg_out, float **dq_out, cudaStream_t s)
+{
+    const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
+    auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    uint8_t *images = static_cast<uint8_t *>(scratch);
+    float *dg = reinterpret_cast<float *>(images + pad(BH * N * kGTile));
+    float *dq = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(4 * BH * N * L));
+    *dg_out = dg;
+    *dq_out = dq;
+    state_images_bwd<<<(unsigned)(BH * N), 128, 0, s>>>(states, images, p.d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // tokens of segment 0 read no cached state: their cached dq part is zero
+    if ((e = cudaMemsetAsync(dq, 0, 4 * BH * L * d, s)) != cudaSuccess) return e;
+    if (p.N < 2) return cudaSuccess;
+    CUtensorMap mY, mQ;
+    const unsigned long long rows = (unsigned long long)BH * L;
+    if (!make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT))
+        return cudaErrorInvalidValue;
+    CArgs a{};
+    a.images = images;
+    a.gam = gam;
+    a.dg = dg;
+    a.dq = dq;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kGT; a.d = p.d; a.mode = p.mode;
+    a.num_tiles = p.BH * (p.N - 1) * a.CPS;
+    if ((e = cudaFuncSetAttribute(bwd_cached_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem)) != cudaSuccess)
+        return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+    bwd_cached_tc<<<grid, kCThreads, kCSmem, s>>>(mY, mQ, a);
+    return cudaGetLastError();
+}
+
+}  // namespace mc

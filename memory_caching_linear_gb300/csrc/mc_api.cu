@@ -615,12 +615,12 @@ int mc_check_device(mc_stream_t stream)
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    int was = 0;
-    if (mc::take_device_abort(&was) != cudaSuccess) {
+    int was = 0, was_bwd = 0;
+    if (mc::take_device_abort(&was) != cudaSuccess || mc::take_bwd_abort(&was_bwd) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    return was ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
+    return was || was_bwd ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
 }
 
 int mc_profile_begin(void *const *events, int capacity)

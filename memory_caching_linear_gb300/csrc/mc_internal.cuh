@@ -142,9 +142,22 @@ struct BwdArgs {
     float *tok;           // [BH][L][kBwdTokWords]
     int32_t *sel_idx;     // SSC: [BH][L][topk] selected segments (segment order, -1 padded)
     float *sel_g;         // SSC: [BH][L][topk] their gates
+    float *gam;           // [BH][N][L] gates of the cached segments, for the tensor-core G (routed modes), or null
+    const float *dg_in;   // [BH][N][L] dy_t . M^(i) q_t from the tensor cores, or null (computed here)
+    const float *dq_in;   // [BH][L][d] the cached part of dq from the tensor cores, or null
+    float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
+    int gates_only;       // 1: only the gates (gam, the SSC selection), nothing else
     int BH, L, C, N, mode, topk;
 };
 size_t backward_scratch_bytes(const Problem &p);
+// Tensor-core pieces of the backward (k_bwd_tc.cu): bf16, d in {64, 128}, seg_len % 128 == 0,
+// L % seg_len == 0, N <= 64.
+bool bwd_tc_supported(const Problem &p);
+cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, float *G, cudaStream_t s);
+size_t bwd_cached_scratch_bytes(const Problem &p);
+cudaError_t launch_bwd_cached_tc(const Problem &p, const void *dy, const void *q, const float *states, const float *gam,
+                                 void *scratch, float **dg_out, float **dq_out, cudaStream_t s);
+cudaError_t take_bwd_abort(int *was_set);
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
                                  const void *dy, void *dq, void *dk, void *dv, void *du, void *scratch,
                                  cudaStream_t s);
