@@ -543,10 +543,16 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
         if (!finish && a.gam && t < cnt) a.gam[seg_base + (size_t)i * a.L + t] = g;
         if (finish) dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
     }
-    if (!finish) return;
+    if (!finish) {  // the online gate, for the tensor-core pass
+        if (tid < cnt) a.tok[((size_t)bh * a.L + tb + tid) * kBwdTokWords + 2] = gon[tid];
+        return;
+    }
 
-    // the online memory's dg: dy_t . O_on[t] over the token's 16 lanes
-    const float *Oon = a.O_on + base, *Xon = a.X_on + base;
+    // the online memory's dg: from the tensor cores, or dy_t . O_on[t] over the token's 16 lanes
+    if (a.dgon_in) {
+        if (tid < cnt) dgo[tid] = a.dgon_in[(size_t)bh * a.L + tb + tid];
+    } else {
+    const float *Oon = a.O_on + base;
 #pragma unroll
     for (int p = 0; p < TPT; ++p) {
         const int t = ty + 16 * p;
@@ -561,6 +567,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (tx == 0) dgo[t] = part;
+    }
     }
     __syncthreads();
     if (tid < kTB) {  // delta_t = sum_i g dg + g_on dg_on
@@ -592,7 +599,8 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
         for (int r = 0; r < RB; ++r) {
             const int c = tx + 16 * r;
             const size_t gi = (size_t)(tb + t) * D + c;
-            dqo[gi] = from_f<T>(a.dq_in[((size_t)bh * a.L + tb + t) * D + c] + gon[t] * Xon[gi]);
+            const float dqv = a.dq_in[((size_t)bh * a.L + tb + t) * D + c];  // all of dq when X_on is null
+            dqo[gi] = from_f<T>(a.X_on ? dqv + gon[t] * a.X_on[base + gi] : dqv);
             if (gated) {
                 float du = dron * (kpre[c] + Kc[t * P + c]) * inv_cnt;
                 for (int i = 0; i < n; ++i) du = fmaf(dt[t * kTab + i], __ldg(kbar + (size_t)i * D + c), du);
@@ -1001,14 +1009,21 @@ size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Scratch of one backward call, in this order: states, G (N d^2 floats per head
 // each), kbar, dkbar (N d), r_on (L), O_on, X_on (L d), per-token words (L x 5),
 // SSC selection indices and gates (L x topk each).
+// Scratch of one backward call.  FFMA path, in this order: states, G (N d^2 floats
+// per head each), kbar, dkbar (N d), r_on (L), O_on, X_on (L d), per-token words
+// (L x 5), SSC selection indices and gates (L x topk each).  Tensor-core path: states,
+// G, kbar, dkbar, per-token words, the gates of the cached segments (routed: L x N),
+// the forward state kernel's images and r_on, and the cached pass's outputs.
 size_t backward_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
+    const size_t common = 2 * pad256(4 * BH * N * d * d) + 2 * pad256(4 * BH * N * d) + pad256(4 * BH * L * kBwdTokWords);
+    if (bwd_tc_supported(p)) {
+        const size_t gam = mode_uses_u(p.mode) ? N : 0;
+        return common + pad256(4 * BH * L * gam) + pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p));
+    }
     const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
-    const size_t gam = bwd_tc_supported(p) && mode_uses_u(p.mode) ? N : 0;
-    return 2 * pad256(4 * BH * N * d * d) + 2 * pad256(4 * BH * N * d) + pad256(4 * BH * L) +
-           2 * pad256(4 * BH * L * d) + pad256(4 * BH * L * kBwdTokWords) + pad256(4 * BH * L * sel) +
-           pad256(4 * BH * L * sel) + pad256(4 * BH * L * gam) + (bwd_tc_supported(p) ? bwd_cached_scratch_bytes(p) : 0);
+    return common + pad256(4 * BH * L) + 2 * pad256(4 * BH * L * d) + 2 * pad256(4 * BH * L * sel);
 }
 
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
@@ -1016,36 +1031,78 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
                                  cudaStream_t s)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
-    const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
     char *b = static_cast<char *>(scratch);
     auto take = [&](size_t bytes) {
         char *r = b;
         b += pad256(bytes);
         return r;
     };
+    const bool gated = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
+    const bool tc = bwd_tc_supported(p);
     float *states = reinterpret_cast<float *>(take(4 * BH * N * d * d));
     float *G = reinterpret_cast<float *>(take(4 * BH * N * d * d));
     float *kbar = reinterpret_cast<float *>(take(4 * BH * N * d));
     float *dkbar = reinterpret_cast<float *>(take(4 * BH * N * d));
+    float *tok = reinterpret_cast<float *>(take(4 * BH * L * kBwdTokWords));
+
+    BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.u = gated ? u : nullptr; a.dy = dy;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.du = gated ? du : nullptr;
+    a.states = states; a.kbar = kbar;
+    a.G = G; a.dkbar = dkbar; a.tok = tok;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
+    FwdArgs f{};
+    f.q = q; f.k = k; f.v = v; f.u = gated ? u : nullptr;
+    f.states = states; f.kbar = kbar;
+    f.BH = p.BH; f.L = p.L; f.C = p.C; f.N = p.N; f.mode = p.mode; f.topk = p.topk;
+    cudaError_t e;
+    profile_call_start(s);
+
+    if (tc) {
+        // Tensor-core path: the forward's state kernel (state and prefix-state images, r_on),
+        // the key means, the gates (routed), every memory's read on the tensor cores (dg, the
+        // online dg, dq), the gate work on whole tables, the key-mean gradient, G on the tensor
+        // cores and the reverse scan.
+        float *gam = gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
+        void *state_scratch = take(tc_state_scratch_bytes(p));
+        void *cached_scratch = take(bwd_cached_scratch_bytes(p));
+        TcImages img{};
+        if ((e = launch_state_tc(p, f, state_scratch, &img, s)) != cudaSuccess) return e;
+        profile_after_kernel(s, "seg_state_tc");
+        if (gated) {
+            if ((e = launch_kbar_simt(p, f, s)) != cudaSuccess) return e;
+            profile_after_kernel(s, "kbar_simt");
+        }
+        if ((e = cudaMemsetAsync(dkbar, 0, 4 * BH * N * d, s)) != cudaSuccess) return e;
+        a.r_on = img.r_on;
+        a.gam = gam;
+        if (gated) {
+            BwdArgs ga = a;
+            ga.gates_only = 1;
+            if ((e = launch_bwd_route(p, ga, s)) != cudaSuccess) return e;
+        }
+        float *dg = nullptr, *dgon = nullptr, *dqf = nullptr;
+        if ((e = launch_bwd_cached_tc(p, q, k, v, dy, img, gam, tok, cached_scratch, &dg, &dgon, &dqf, s)) != cudaSuccess)
+            return e;
+        profile_after_kernel(s, "bwd_cached_tc");
+        a.dg_in = dg;
+        a.dgon_in = dgon;
+        a.dq_in = dqf;
+        a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
+        return launch_bwd_tc_rest(p, a, s);
+    }
+
+    // FFMA path
+    const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
     float *r_on = reinterpret_cast<float *>(take(4 * BH * L));
     float *O_on = reinterpret_cast<float *>(take(4 * BH * L * d));
     float *X_on = reinterpret_cast<float *>(take(4 * BH * L * d));
-    float *tok = reinterpret_cast<float *>(take(4 * BH * L * kBwdTokWords));
     int32_t *sel_idx = reinterpret_cast<int32_t *>(take(4 * BH * L * sel));
     float *sel_g = reinterpret_cast<float *>(take(4 * BH * L * sel));
-    const bool gated = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
-    const bool tc = bwd_tc_supported(p);
-    float *gam = tc && gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
-    void *cached_scratch = tc ? take(bwd_cached_scratch_bytes(p)) : nullptr;
-
-    profile_call_start(s);
     // The forward's segment scan: cached states, key means, online scores, M_t q_t.
-    FwdArgs f{};
-    f.q = q; f.k = k; f.v = v; f.u = gated ? u : nullptr;
-    f.states = states; f.O_on = O_on; f.r_on = r_on; f.kbar = kbar;
-    f.BH = p.BH; f.L = p.L; f.C = p.C; f.N = p.N; f.mode = p.mode; f.topk = p.topk;
-    cudaError_t e = launch_seg_scan_simt(p, f, s);
-    if (e != cudaSuccess) return e;
+    f.O_on = O_on;
+    f.r_on = r_on;
+    if ((e = launch_seg_scan_simt(p, f, s)) != cudaSuccess) return e;
     profile_after_kernel(s, "seg_scan_simt");
     // The same scan on (dy, v, k) gives M_t^T dy_t = sum_{j <= t} k_j (v_j . dy_t); its state and
     // key-mean outputs land in G and dkbar, which are rewritten below.
@@ -1055,30 +1112,8 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
     if ((e = launch_seg_scan_simt(p, x, s)) != cudaSuccess) return e;
     profile_after_kernel(s, "seg_scan_simt");
     if ((e = cudaMemsetAsync(dkbar, 0, 4 * BH * N * d, s)) != cudaSuccess) return e;
-
-    BwdArgs a{};
-    a.q = q; a.k = k; a.v = v; a.u = gated ? u : nullptr; a.dy = dy;
-    a.dq = dq; a.dk = dk; a.dv = dv; a.du = gated ? du : nullptr;
-    a.states = states; a.kbar = kbar; a.r_on = r_on; a.O_on = O_on; a.X_on = X_on;
-    a.G = G; a.dkbar = dkbar; a.tok = tok; a.sel_idx = sel_idx; a.sel_g = sel_g; a.gam = gam;
-    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
-    if (tc) {
-        // The cached states' part on the tensor cores: the gates first (routed modes), then
-        // dg against every cached state and the cached part of dq, then the gate work on
-        // whole tables, the key-mean gradient, G on the tensor cores and the reverse scan.
-        if (gated) {
-            BwdArgs ga = a;
-            ga.gates_only = 1;
-            if ((e = launch_bwd_route(p, ga, s)) != cudaSuccess) return e;
-        }
-        float *dg = nullptr, *dqc = nullptr;
-        if ((e = launch_bwd_cached_tc(p, dy, q, states, gam, cached_scratch, &dg, &dqc, s)) != cudaSuccess) return e;
-        profile_after_kernel(s, "bwd_cached_tc");
-        a.dg_in = dg;
-        a.dq_in = dqc;
-        a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
-        return launch_bwd_tc_rest(p, a, s);
-    }
+    a.r_on = r_on; a.O_on = O_on; a.X_on = X_on;
+    a.sel_idx = sel_idx; a.sel_g = sel_g;
     return launch_bwd_kernels(p, a, s);
 }
 

@@ -183,62 +183,44 @@ __global__ void __launch_bounds__(kGThreads, 1)
 }
 
 // ============================================================================
-// state_images_bwd -- the cached states M^(i) (fp32 [d][d]) as bf16 operand images:
-// a 128 x 128 tile, rows = value dim, two 64-column 128-byte-swizzled panels of key
-// dims (16-byte chunk c of row r at chunk c ^ (r % 8)), zero beyond d.
+// bwd_cached_tc -- per 128-token tile (b,h, segment n, chunk c) the reads of every
+// memory the tile's tokens use, as the gradient needs them:
+//   the online memory M_t = S_pre(c) + sum_{j in chunk, j <= t} v_j k_j^T (gate g_on):
+//     dg_on_t  = dy_t . M_t q_t = q_t . (S_pre^T dy_t) + sum_{j<=t} (dy_t . v_j)(k_j . q_t)
+//     dq_t    += g_on (S_pre^T dy_t + sum_{j<=t} k_j (v_j . dy_t))
+//   every cached M^(i), i < n (gate g_{t,i}):
+//     dg_{t,i} = q_t . (M^(i)^T dy_t),   dq_t += g_{t,i} M^(i)^T dy_t
+// On the tensor cores: G1 = Q K^T and G2 = dY V^T (SS); P2 = g_on mask(G2) -> D_q = P2 K
+// (TS); then for the prefix state and each cached state X: W = dY X (SS, the image
+// read MN-major) for the dot with q, and D_q += (g o dY) X^T (TS, the same image).
+// Persistent, one CTA per SM, tiles with the most cached segments first.  Warp 0
+// streams Q, K, V, dY of the tile (TMA) and one 32 KB image per state through a
+// two-slot ring; warp 1 issues; warps 2-5 own a token row each.
+// TMEM: D_q [0,128) | W0 [128,256) | W1 [256,384) (G1 / G2 at a tile's start) |
+//       A0 [384,448) | A1 [448,512).
 // ============================================================================
-__global__ void __launch_bounds__(128) state_images_bwd(const float *__restrict__ states, uint8_t *images, int d)
-{
-    const int r = threadIdx.x;
-    const float *src = states + (size_t)blockIdx.x * d * d + (size_t)r * d;
-    uint8_t *dst = images + (size_t)blockIdx.x * kGTile + r * 128;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int col = 64 * h + 8 * c + 2 * k;
-                const float lo = r < d && col < d ? src[col] : 0.f;
-                const float hi = r < d && col + 1 < d ? src[col + 1] : 0.f;
-                w[k] = pack_bf16x2(lo, hi);
-            }
-            *reinterpret_cast<uint4 *>(dst + h * 16384 + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-}
-
-// ============================================================================
-// bwd_cached_tc -- per 128-token tile (b,h, segment n, chunk c) and cached segment
-// i < n, with W_i = dY M^(i) (d_k wide):
-//   dg_{t,i} = q_t . W_i[t]  (= dy_t . M^(i) q_t, the gate's gradient)
-//   dq_t    += (g_{t,i} dy_t) M^(i)^T summed over i  (the cached part of dq)
-// Persistent, one CTA per SM; tiles with the most cached segments first.  Warp 0
-// streams dy and q of the tile (TMA) and one 32 KB state image per segment through a
-// three-slot ring; warp 1 issues W_i = dY M^(i) (SS, image read MN-major) into one of
-// two W accumulators and D_q += (g_i o dY) M^(i)^T (TS, the same image) into D_q;
-// warps 2-5 own a token row each: they write g_i o dy into one of two A slots, read
-// W_i to form dg, and drain D_q at the end of the tile.
-// TMEM: D_q [0,128) | W0 [128,256) | W1 [256,384) | A0 [384,448) | A1 [448,512).
-// ============================================================================
-constexpr int kCRing = 3;
+constexpr int kCRing = 2;
 constexpr int kCThreads = 192;
-constexpr size_t kCSmem = 2 * kGTile + kCRing * kGTile + 1024;
+constexpr size_t kCSmem = 4 * kGTile + kCRing * kGTile + 1024;
 
 struct CArgs {
     const uint8_t *images;  // [BH][N] x 32 KB state images
+    const uint8_t *spre;    // [BH][N][CPS] x 32 KB prefix-state images (chunk c > 0)
     const float *gam;       // [BH][N][L] gates of the cached segments (routed aggregations)
+    const float *tok;       // [BH][L][kBwdTokWords]: word 2 is the online gate (routed aggregations)
     float *dg;              // [BH][N][L] out: dy_t . M^(i) q_t
-    float *dq;              // [BH][L][d] out: the cached part of dq (fp32)
+    float *dgon;            // [BH][L] out: dy_t . M_t q_t
+    float *dq;              // [BH][L][d] out: dq (fp32)
     int BH, L, C, N, CPS, d, mode, num_tiles;
 };
 
 __global__ void __launch_bounds__(kCThreads, 1)
-    bwd_cached_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, CArgs a)
+    bwd_cached_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mY, CArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sY = sm, *sQ = sm + kGTile, *ring = sm + 2 * kGTile;
+    uint8_t *sQ = sm, *sK = sm + kGTile, *sV = sm + 2 * kGTile, *sY = sm + 3 * kGTile, *ring = sm + 4 * kGTile;
     __shared__ uint64_t tile_full, tile_empty, ring_full[kCRing], ring_empty[kCRing];
     __shared__ uint64_t w_full[2], w_empty[2], a_full[2], a_empty[2], dq_full, dq_empty, fin;
     __shared__ uint32_t tmem_base;
@@ -246,7 +228,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int my_tiles = blockIdx.x < (unsigned)a.num_tiles ? (a.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    auto tile = [&](int j, int &bh, int &n, int &c) {  // heaviest first: n = N-1 down to 1
+    auto tile = [&](int j, int &bh, int &n, int &c) {  // heaviest first: n = N-1 down to 0
         const int id = (int)blockIdx.x + j * (int)gridDim.x;
         const int per = a.BH * a.CPS;
         n = a.N - 1 - id / per;
@@ -261,7 +243,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (threadIdx.x == 32) {
         abort_flag = 0;
         mbar_init(&tile_full, 1);
-        mbar_init(&tile_empty, 1 + 128);  // the tile's last W MMAs + every worker has its rows
+        mbar_init(&tile_empty, 1 + 128);  // the tile's last MMA reading Q, K, V, dY + every worker has its rows
         for (int s = 0; s < kCRing; ++s) {
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
@@ -286,67 +268,104 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0 && my_tiles > 0) {
-            prefetch_tensormap(&mY);
             prefetch_tensormap(&mQ);
-            uint32_t g = 0;
+            prefetch_tensormap(&mK);
+            prefetch_tensormap(&mV);
+            prefetch_tensormap(&mY);
+            uint32_t gr = 0;
             bool ok = true;
             for (int j = 0; j < my_tiles && ok; ++j) {
                 int bh, n, c;
                 tile(j, bh, n, c);
                 if (!(ok = mbar_wait(&tile_empty, (j & 1) ^ 1, &abort_flag))) break;
                 const int row = bh * a.L + n * a.C + c * kGT;
-                mbar_arrive_expect_tx(&tile_full, 2 * kGTile);
-                tma_load_2d(sY, &mY, 0, row, &tile_full);
-                tma_load_2d(sY + 16384, &mY, 64, row, &tile_full);
-                tma_load_2d(sQ, &mQ, 0, row, &tile_full);
-                tma_load_2d(sQ + 16384, &mQ, 64, row, &tile_full);
-                for (int i = 0; i < n && ok; ++i, ++g) {
-                    const int s = g % kCRing;
-                    if (!(ok = mbar_wait(&ring_empty[s], ((g / kCRing) & 1) ^ 1, &abort_flag))) break;
+                mbar_arrive_expect_tx(&tile_full, 4 * kGTile);
+                const CUtensorMap *maps[4] = {&mQ, &mK, &mV, &mY};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    tma_load_2d(sm + m * kGTile, maps[m], 0, row, &tile_full);
+                    tma_load_2d(sm + m * kGTile + 16384, maps[m], 64, row, &tile_full);
+                }
+                const int nimg = (c > 0 ? 1 : 0) + n;
+                for (int m = 0; m < nimg && ok; ++m, ++gr) {
+                    const int s = gr % kCRing;
+                    const uint8_t *src = (c > 0 && m == 0)
+                                             ? a.spre + (((size_t)bh * a.N + n) * a.CPS + c) * kGTile
+                                             : a.images + ((size_t)bh * a.N + (m - (c > 0 ? 1 : 0))) * kGTile;
+                    if (!(ok = mbar_wait(&ring_empty[s], ((gr / kCRing) & 1) ^ 1, &abort_flag))) break;
                     mbar_arrive_expect_tx(&ring_full[s], kGTile);
-                    bulk_load(ring + s * kGTile, a.images + ((size_t)bh * a.N + i) * kGTile, kGTile, &ring_full[s]);
+                    bulk_load(ring + s * kGTile, src, kGTile, &ring_full[s]);
                 }
             }
             // leave no copy in flight: the last use of every slot has landed
             int give_up = 0;
-            for (uint32_t k = 0; k < (uint32_t)kCRing && k < g; ++k) {
-                const uint32_t u = g - 1 - k;
+            for (uint32_t k = 0; k < (uint32_t)kCRing && k < gr; ++k) {
+                const uint32_t u = gr - 1 - k;
                 mbar_wait_limit(&ring_full[u % kCRing], (u / kCRing) & 1, &give_up, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0 && my_tiles > 0) {
-            constexpr uint32_t idW = idesc_bf16(128, 128, false, true);  // A = dY K-major, B = image MN-major
-            uint32_t g = 0;
+            constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // both K-major
+            constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);   // B MN-major
+            uint32_t gw = 0, ga = 0, gr = 0;
             bool ok = true;
-            const uint32_t y0 = smem_u32(sY), r0 = smem_u32(ring);
+            const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), y0 = smem_u32(sY);
+            const uint32_t r0 = smem_u32(ring);
+            auto kmaj = [](int kk) { return (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32); };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 int bh, n, c;
                 tile(j, bh, n, c);
+                const int nimg = (c > 0 ? 1 : 0) + n;
                 if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
-                for (int i = 0; i < n && ok; ++i, ++g) {
-                    const uint32_t s = g % kCRing, w = g % 2;
-                    if (!(ok = mbar_wait(&ring_full[s], (g / kCRing) & 1, &abort_flag) &&
-                               mbar_wait(&w_empty[w], ((g / 2) & 1) ^ 1, &abort_flag)))
+                // G1 = Q K^T, G2 = dY V^T into the two W buffers
+                const uint32_t w1 = gw % 2, w2 = (gw + 1) % 2;
+                if (!(ok = mbar_wait(&w_empty[w1], ((gw / 2) & 1) ^ 1, &abort_flag) &&
+                           mbar_wait(&w_empty[w2], (((gw + 1) / 2) & 1) ^ 1, &abort_flag)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tW0 + w1 * 128, make_desc_sw128(q0 + kmaj(kk), 0, 1024), make_desc_sw128(k0 + kmaj(kk), 0, 1024),
+                           idKK, kk > 0);
+                mma_commit(&w_full[w1]);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tW0 + w2 * 128, make_desc_sw128(y0 + kmaj(kk), 0, 1024), make_desc_sw128(v0 + kmaj(kk), 0, 1024),
+                           idKK, kk > 0);
+                mma_commit(&w_full[w2]);
+                gw += 2;
+                // D_q = P2 K once the workers have written P2
+                if (!(ok = mbar_wait(&a_full[ga % 2], (ga / 2) & 1, &abort_flag) &&
+                           mbar_wait(&dq_empty, (j & 1) ^ 1, &abort_flag)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tDq, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(k0 + kk * 2048u, 16384, 1024), idKM, kk > 0);
+                mma_commit(&a_empty[ga % 2]);
+                ++ga;
+                if (nimg == 0) mma_commit(&tile_empty);
+                for (int m = 0; m < nimg && ok; ++m, ++gw, ++ga, ++gr) {
+                    const uint32_t s = gr % kCRing, w = gw % 2;
+                    if (!(ok = mbar_wait(&ring_full[s], (gr / kCRing) & 1, &abort_flag) &&
+                               mbar_wait(&w_empty[w], ((gw / 2) & 1) ^ 1, &abort_flag)))
                         break;
                     tc_fence_after();
                     const uint32_t img = r0 + s * kGTile;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tW0 + w * 128, make_desc_sw128(y0 + (kk >> 2) * 16384u + (kk & 3) * 32u, 0, 1024),
-                               make_desc_sw128(img + kk * 2048u, 16384, 1024), idW, kk > 0);
+                        mma_ss(tW0 + w * 128, make_desc_sw128(y0 + kmaj(kk), 0, 1024),
+                               make_desc_sw128(img + kk * 2048u, 16384, 1024), idKM, kk > 0);
                     mma_commit(&w_full[w]);
-                    if (i == n - 1) mma_commit(&tile_empty);  // dY is no longer read
-                    // D_q += (g_i o dY) M^(i)^T once the workers have written the A slot
-                    if (!(ok = mbar_wait(&a_full[w], (g / 2) & 1, &abort_flag))) break;
-                    if (i == 0 && !(ok = mbar_wait(&dq_empty, (j & 1) ^ 1, &abort_flag))) break;
+                    if (m == nimg - 1) mma_commit(&tile_empty);  // Q, K, V, dY are no longer read
+                    if (!(ok = mbar_wait(&a_full[ga % 2], (ga / 2) & 1, &abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tDq, tA0 + w * 64 + kk * 8, make_desc_sw128(img + kk * 2048u, 16384, 1024), idW,
-                               (i | kk) != 0);
-                    mma_commit(&a_empty[w]);
+                        mma_ts(tDq, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(img + kk * 2048u, 16384, 1024), idKM, 1);
+                    mma_commit(&a_empty[ga % 2]);
                     mma_commit(&ring_empty[s]);
                 }
                 if (!ok) break;
@@ -363,13 +382,72 @@ __global__ void __launch_bounds__(kCThreads, 1)
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
-        uint32_t g = 0;
+        uint32_t gw = 0, ga = 0;
         bool ok = true;
+        // write g o dy into A slot ga % 2
+        auto put_a = [&](const uint32_t (&yp)[64], float g) -> bool {
+            if (!mbar_wait(&a_empty[ga % 2], ((ga / 2) & 1) ^ 1, &abort_flag)) return false;
+            tc_fence_after();
+            const __nv_bfloat162 g2 = __float2bfloat162_rn(g);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint32_t r[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&yp[16 * m + k]);
+                    __nv_bfloat162 pr = __hmul2(x, g2);
+                    r[k] = *reinterpret_cast<uint32_t *>(&pr);
+                }
+                tmem_st16(tA0 + (ga % 2) * 64 + lane_base + 16 * m, r);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&a_full[ga % 2]);
+            ++ga;
+            return true;
+        };
         for (int j = 0; j < my_tiles && ok; ++j) {
             int bh, n, c;
             tile(j, bh, n, c);
+            const int nimg = (c > 0 ? 1 : 0) + n;
             const int t = n * a.C + c * kGT + row;  // token within the head
             if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
+            const float gon = routed ? __ldg(a.tok + ((size_t)bh * a.L + t) * kBwdTokWords + 2)
+                                     : (a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f);
+            // in-chunk online part: dg_on += sum_{j<=t} G1 G2, P2 = g_on mask(G2)
+            float dgon = 0.f;
+            {
+                const uint32_t w1 = gw % 2, w2 = (gw + 1) % 2;
+                if (!(ok = mbar_wait(&w_full[w1], (gw / 2) & 1, &abort_flag) &&
+                           mbar_wait(&w_full[w2], ((gw + 1) / 2) & 1, &abort_flag) &&
+                           mbar_wait(&a_empty[ga % 2], ((ga / 2) & 1) ^ 1, &abort_flag)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {  // 16 key columns at a time
+                    uint32_t x1[16], x2[16], o[8];
+                    tmem_ld16(tW0 + w1 * 128 + lane_base + 16 * m, x1);
+                    tmem_ld16(tW0 + w2 * 128 + lane_base + 16 * m, x2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        const uint32_t col = 16 * m + k;
+                        const float a0 = col <= row ? __uint_as_float(x2[k]) : 0.f;
+                        const float a1 = col + 1 <= row ? __uint_as_float(x2[k + 1]) : 0.f;
+                        dgon = fmaf(__uint_as_float(x1[k]), a0, dgon);
+                        dgon = fmaf(__uint_as_float(x1[k + 1]), a1, dgon);
+                        o[k / 2] = pack_bf16x2(gon * a0, gon * a1);
+                    }
+                    tmem_st8(tA0 + (ga % 2) * 64 + lane_base + 8 * m, o);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&w_empty[w1]);
+                mbar_arrive(&w_empty[w2]);
+                mbar_arrive(&a_full[ga % 2]);
+                gw += 2;
+                ++ga;
+            }
             // the token's q and dy rows (128-byte swizzle: chunk c of row r at chunk c ^ (r % 8))
             uint32_t qp[64], yp[64];
 #pragma unroll
@@ -385,56 +463,40 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     yp[32 * h + 4 * cc + 2] = xy.z; yp[32 * h + 4 * cc + 3] = xy.w;
                 }
             mbar_arrive(&tile_empty);
+            // the prefix state (gate g_on) and the cached states (gate g_{t,i})
             const float *grow = routed ? a.gam + (size_t)bh * a.N * a.L + t : nullptr;
             float *dgrow = a.dg + (size_t)bh * a.N * a.L + t;
             const float gconst = a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
-            float gnext = n > 0 ? (routed ? __ldg(grow) : gconst) : 0.f;
-            for (int i = 0; i < n && ok; ++i, ++g) {
-                const uint32_t w = g % 2;
-                const float gi = gnext;
-                if (i + 1 < n) gnext = routed ? __ldg(grow + (size_t)(i + 1) * a.L) : gconst;
-                // A slot w <- g_i o dy
-                if (!(ok = mbar_wait(&a_empty[w], ((g / 2) & 1) ^ 1, &abort_flag))) break;
+            for (int m = 0; m < nimg && ok; ++m) {
+                const bool prefix = c > 0 && m == 0;
+                const int i = m - (c > 0 ? 1 : 0);
+                const float g = prefix ? gon : (routed ? __ldg(grow + (size_t)i * a.L) : gconst);
+                if (!(ok = put_a(yp, g))) break;
+                const uint32_t w = gw % 2;
+                if (!(ok = mbar_wait(&w_full[w], (gw / 2) & 1, &abort_flag))) break;
                 tc_fence_after();
-                {
-                    const __nv_bfloat162 g2 = __float2bfloat162_rn(gi);
+                float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        uint32_t r[32];
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&yp[32 * m + k]);
-                            __nv_bfloat162 pr = __hmul2(x, g2);
-                            r[k] = *reinterpret_cast<uint32_t *>(&pr);
-                        }
-                        tmem_st32(tA0 + w * 64 + lane_base + 32 * m, r);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&a_full[w]);
-                // dg = q . W_i
-                if (!(ok = mbar_wait(&w_full[w], (g / 2) & 1, &abort_flag))) break;
-                tc_fence_after();
-                float dg0 = 0.f, dg1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t x[32];
-                    tmem_ld32(tW0 + w * 128 + lane_base + 32 * m, x);
+                for (int mm = 0; mm < 8; ++mm) {
+                    uint32_t x[16];
+                    tmem_ld16(tW0 + w * 128 + lane_base + 16 * mm, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const uint32_t qq = qp[16 * m + k];
-                        dg0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), dg0);
-                        dg1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), dg1);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t qq = qp[8 * mm + k];
+                        d0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), d0);
+                        d1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), d1);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&w_empty[w]);
-                dgrow[(size_t)i * a.L] = dg0 + dg1;
+                ++gw;
+                if (prefix) dgon += d0 + d1;
+                else dgrow[(size_t)i * a.L] = d0 + d1;
             }
             if (!ok) break;
-            // drain D_q: the cached part of dq for this token
+            a.dgon[(size_t)bh * a.L + t] = dgon;
+            // drain D_q
             if (!(ok = mbar_wait(&dq_full, j & 1, &abort_flag))) break;
             tc_fence_after();
             float *dqrow = a.dq + ((size_t)bh * a.L + t) * a.d;
@@ -510,44 +572,44 @@ size_t bwd_cached_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    return pad(BH * N * kGTile) + pad(4 * BH * N * L) + pad(4 * BH * L * d);
+    return pad(4 * BH * N * L) + pad(4 * BH * L) + pad(4 * BH * L * d);
 }
 
-cudaError_t launch_bwd_cached_tc(const Problem &p, const void *dy, const void *q, const float *states, const float *gam,
-                                 void *scratch, float **dg_out, float **dq_out, cudaStream_t s)
+cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
+                                 const TcImages &img, const float *gam, const float *tok, void *scratch,
+                                 float **dg_out, float **dgon_out, float **dq_out, cudaStream_t s)
 {
-    const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
+    const size_t BH = p.BH, N = p.N, L = p.L;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    uint8_t *images = static_cast<uint8_t *>(scratch);
-    float *dg = reinterpret_cast<float *>(images + pad(BH * N * kGTile));
-    float *dq = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(4 * BH * N * L));
+    float *dg = static_cast<float *>(scratch);
+    float *dgon = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(4 * BH * N * L));
+    float *dq = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dgon) + pad(4 * BH * L));
     *dg_out = dg;
+    *dgon_out = dgon;
     *dq_out = dq;
-    state_images_bwd<<<(unsigned)(BH * N), 128, 0, s>>>(states, images, p.d);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // tokens of segment 0 read no cached state: their cached dq part is zero
-    if ((e = cudaMemsetAsync(dq, 0, 4 * BH * L * d, s)) != cudaSuccess) return e;
-    if (p.N < 2) return cudaSuccess;
-    CUtensorMap mY, mQ;
+    CUtensorMap mQ, mK, mV, mY;
     const unsigned long long rows = (unsigned long long)BH * L;
-    if (!make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT))
+    if (!make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mK, k, rows, p.d, kGT) ||
+        !make_tmap_bf16_sw128(&mV, v, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT))
         return cudaErrorInvalidValue;
     CArgs a{};
-    a.images = images;
+    a.images = img.states_img;
+    a.spre = img.spre_img;
     a.gam = gam;
+    a.tok = tok;
     a.dg = dg;
+    a.dgon = dgon;
     a.dq = dq;
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kGT; a.d = p.d; a.mode = p.mode;
-    a.num_tiles = p.BH * (p.N - 1) * a.CPS;
-    if ((e = cudaFuncSetAttribute(bwd_cached_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem)) != cudaSuccess)
-        return e;
+    a.num_tiles = p.BH * p.N * a.CPS;
+    cudaError_t e = cudaFuncSetAttribute(bwd_cached_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem);
+    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    bwd_cached_tc<<<grid, kCThreads, kCSmem, s>>>(mY, mQ, a);
+    bwd_cached_tc<<<grid, kCThreads, kCSmem, s>>>(mQ, mK, mV, mY, a);
     return cudaGetLastError();
 }
 

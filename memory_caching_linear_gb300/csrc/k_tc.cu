@@ -1311,6 +1311,62 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
     return cudaGetLastError();
 }
 
+size_t tc_state_scratch_bytes(const Problem &p)
+{
+    const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
+    return pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) + pad256(sizeof(float) * BH * p.L);
+}
+
+// The forward's segment-state kernel alone (plain update): the fp32 states, their and
+// the chunks' prefix-state bf16 images and, for the routed aggregations, the online
+// scores r_on and the key-mean images -- the operands the tensor-core backward reads.
+cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, TcImages *out, cudaStream_t s)
+{
+    const bool gated = mode_uses_u(p.mode);
+    const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    TcArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(fa.q);
+    a.u = static_cast<const __nv_bfloat16 *>(fa.u);
+    a.states = fa.states;
+    a.states_img = base;
+    base += pad256(BH * N * kTile);
+    a.spre_img = base;
+    base += pad256(BH * N * CPS * kTile);
+    a.kbar_img = base;
+    base += pad256(BH * kTile);
+    a.r_on = reinterpret_cast<float *>(base);
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = (int)CPS; a.d = p.d;
+    a.num_tiles = (int)(BH * N * CPS);
+    CUtensorMap mK, mV, mU;
+    const unsigned long long rows = (unsigned long long)BH * p.L;
+    if (!make_tmap_bf16_sw128(&mK, fa.k, rows, p.d, 128) || !make_tmap_bf16_sw128(&mV, fa.v, rows, p.d, 128))
+        return cudaErrorInvalidValue;
+    if (gated) {
+        if (!make_tmap_bf16_sw128(&mU, fa.u, rows, p.d, 128)) return cudaErrorInvalidValue;
+    } else {
+        mU = mK;
+    }
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 148;
+    }
+    cudaError_t e;
+    if (gated && (e = cudaMemsetAsync(a.kbar_img, 0, BH * kTile, s)) != cudaSuccess) return e;
+    auto k1 = gated ? seg_state_tc<true, false> : seg_state_tc<false, false>;
+    const size_t smem1 = t1_smem_bytes<false>();
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
+    const int nseg = (int)(BH * N);
+    k1<<<nseg < g_num_sms ? nseg : g_num_sms, kT1Threads, smem1, s>>>(mK, mV, mU, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    out->states_img = a.states_img;
+    out->spre_img = a.spre_img;
+    out->r_on = a.r_on;
+    return cudaSuccess;
+}
+
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
 {
     const bool gated = mode_uses_u(p.mode);

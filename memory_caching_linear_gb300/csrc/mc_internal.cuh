@@ -117,6 +117,15 @@ size_t tc_scratch_bytes(const Problem &p);
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 size_t tc_select_scratch_bytes(const Problem &p);
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+// The forward's state kernel alone, for the tensor-core backward: images of the cached
+// states [BH][N] and of the chunks' prefix states [BH][N][C/128] (32 KB each, 128x128
+// bf16, two 64-column 128-byte-swizzled panels, row = value dim), and r_on [BH][L].
+struct TcImages {
+    const uint8_t *states_img, *spre_img;
+    const float *r_on;
+};
+size_t tc_state_scratch_bytes(const Problem &p);
+cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, TcImages *out, cudaStream_t s);
 // Reads and clears the device-side record of an abandoned bounded wait.
 cudaError_t take_device_abort(int *was_set);
 
@@ -144,7 +153,8 @@ struct BwdArgs {
     float *sel_g;         // SSC: [BH][L][topk] their gates
     float *gam;           // [BH][N][L] gates of the cached segments, for the tensor-core G (routed modes), or null
     const float *dg_in;   // [BH][N][L] dy_t . M^(i) q_t from the tensor cores, or null (computed here)
-    const float *dq_in;   // [BH][L][d] the cached part of dq from the tensor cores, or null
+    const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null
+    const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
     int gates_only;       // 1: only the gates (gam, the SSC selection), nothing else
     int BH, L, C, N, mode, topk;
@@ -155,8 +165,9 @@ size_t backward_scratch_bytes(const Problem &p);
 bool bwd_tc_supported(const Problem &p);
 cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, float *G, cudaStream_t s);
 size_t bwd_cached_scratch_bytes(const Problem &p);
-cudaError_t launch_bwd_cached_tc(const Problem &p, const void *dy, const void *q, const float *states, const float *gam,
-                                 void *scratch, float **dg_out, float **dq_out, cudaStream_t s);
+cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
+                                 const TcImages &img, const float *gam, const float *tok, void *scratch,
+                                 float **dg_out, float **dgon_out, float **dq_out, cudaStream_t s);
 cudaError_t take_bwd_abort(int *was_set);
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
                                  const void *dy, void *dq, void *dk, void *dv, void *du, void *scratch,

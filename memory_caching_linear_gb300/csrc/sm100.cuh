@@ -196,6 +196,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // 16 lanes x 256 bits, repeated over 8 consecutive 8-column blocks.  Thread i of
 // the warp gets, for block b: r[4b], r[4b+1] = lane (base + i/4), columns
 // 8b + 2(i%4) + {0, 1}; r[4b+2], r[4b+3] = lane (base + 8 + i/4), same columns.
