@@ -9,11 +9,12 @@
 // bwd_G_tc -- the gradient of every cached state ([MC-ja §3 after eq. 4b]: the cached
 //   M^(i) is read by every token of the later segments with its gate g_{t,i}):
 //     G_i = sum_{t in segments > i} g_{t,i} dy_t q_t^T        (d_v x d_k, fp32)
-//   One CTA per (b,h, cached segment i), the segment with the most later tokens first.
-//   Per 128-token tile: the TMA brings dy and q (two 64-column 128-byte-swizzled
-//   panels each), the four worker warps scale their token's dy row by g_{t,i} in
-//   shared memory, and one thread issues D += (g o dy)^T q as eight 128x128x16 MMAs
-//   with both operands read MN-major from shared memory.
+//   One CTA per (b,h, pair of cached segments), the pair with the most later tokens
+//   first.  Per 128-token tile: the TMA brings dy and q (two 64-column
+//   128-byte-swizzled panels each), the four worker warps scale their token's dy row
+//   by the two gates in shared memory, and one thread issues D_i += (g_i o dy)^T q
+//   for both states, alternating eight 128x128x16 MMAs each, with both operands read
+//   MN-major from shared memory.
 #include <cstdint>
 
 #include "mc_internal.cuh"
@@ -32,14 +33,15 @@ using namespace sm100;
 
 constexpr int kGT = 128;             // tokens per tile
 constexpr uint32_t kGTile = 32768;   // one 128 x 128 bf16 operand tile (two 16 KB panels)
-constexpr int kGStages = 3;          // (dy, q) tile pairs in flight
+constexpr int kGStages = 2;          // tile stages in flight: dy (scaled in place for the first state), q, g o dy for the second
 constexpr int kGThreads = 192;       // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
-constexpr size_t kGSmem = kGStages * 2 * kGTile + 1024;
+constexpr uint32_t kGStage = 3 * kGTile;
+constexpr size_t kGSmem = kGStages * kGStage + 1024;
 
 struct GArgs {
     const float *gam;  // [BH][N][L]: g_{t,i} of the cached segments (routed aggregations)
     float *G;          // [BH][N][d][d]
-    int BH, L, C, N, d, mode;
+    int BH, L, C, N, d, mode, pairs;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
@@ -47,6 +49,9 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// One CTA per (b,h, pair of cached segments i0 = 2p, i1 = 2p + 1): every tile after
+// segment i0 is loaded once and feeds both accumulators (the tiles of segment i1
+// only the first).
 __global__ void __launch_bounds__(kGThreads, 1)
     bwd_G_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, GArgs a)
 {
@@ -57,12 +62,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;
-    const int t_begin = (i + 1) * a.C;
+    const int pr = (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;
+    const int i0 = 2 * pr, i1 = 2 * pr + 1;
+    const bool two = i1 < a.N - 1;  // segment N-1 has no later tokens
+    const int t_begin = (i0 + 1) * a.C;
     const int ntiles = (a.L - t_begin) / kGT;
+    const int split = a.C / kGT;  // tiles of segment i1: the second state starts after them
 
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 128);
+        tmem_alloc(&tmem_base, 256);
         tmem_relinquish();
     }
     if (threadIdx.x == 32) {
@@ -89,7 +97,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kGStages;
                 if (!mbar_wait(&empty[s], ((j / kGStages) & 1) ^ 1, &abort_flag)) break;
-                uint8_t *st = sm + s * 2 * kGTile;
+                uint8_t *st = sm + s * kGStage;
                 const int row = bh * a.L + t_begin + j * kGT;
                 mbar_arrive_expect_tx(&full[s], 2 * kGTile);
                 tma_load_2d(st, &mY, 0, row, &full[s]);
@@ -112,11 +120,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int s = j % kGStages;
                 if (!(ok = mbar_wait(&scaled[s], (j / kGStages) & 1, &abort_flag))) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sm + s * 2 * kGTile), b0 = a0 + kGTile;
+                const uint32_t y0 = smem_u32(sm + s * kGStage), q0 = y0 + kGTile, y1 = y0 + 2 * kGTile;
+                const bool second = two && j >= split;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // 16 tokens per step: 16 rows of 128 bytes
-                    mma_ss(tD, make_desc_sw128(a0 + kk * 2048u, 16384, 1024), make_desc_sw128(b0 + kk * 2048u, 16384, 1024),
-                           idG, (j | kk) != 0);
+                for (int kk = 0; kk < 8; ++kk) {  // 16 tokens per step: 16 rows of 128 bytes
+                    const uint64_t bq = make_desc_sw128(q0 + kk * 2048u, 16384, 1024);
+                    mma_ss(tD, make_desc_sw128(y0 + kk * 2048u, 16384, 1024), bq, idG, (j | kk) != 0);
+                    if (second)
+                        mma_ss(tD + 128, make_desc_sw128(y1 + kk * 2048u, 16384, 1024), bq, idG, (j > split) || kk != 0);
+                }
                 mma_commit(&empty[s]);
             }
             // leave no MMA in flight; the drain waits for this
@@ -127,48 +139,62 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
         const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
-        const float *grow = routed ? a.gam + ((size_t)bh * a.N + i) * a.L + t_begin + r : nullptr;
-        auto gate = [&](int j) -> float {  // g_{t,i} of this thread's token in tile j
+        const float *grow0 = routed ? a.gam + ((size_t)bh * a.N + i0) * a.L + t_begin + r : nullptr;
+        const float *grow1 = routed && two ? a.gam + ((size_t)bh * a.N + i1) * a.L + t_begin + r : nullptr;
+        auto gate = [&](const float *grow, int j) -> float {  // this thread's token in tile j
             const int t = t_begin + j * kGT + r;
             return routed ? __ldg(grow + (size_t)j * kGT) : (a.mode == MC_MEAN ? 1.f / (float)(t / a.C + 1) : 1.f);
         };
-        float g_next = ntiles > 0 ? gate(0) : 0.f;
+        float g0n = ntiles > 0 ? gate(grow0, 0) : 0.f;
+        float g1n = two && split < ntiles ? gate(grow1, split) : 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kGStages;
-            const float g = g_next;
-            if (j + 1 < ntiles) g_next = gate(j + 1);  // in flight while this tile is scaled
+            const bool second = two && j >= split;
+            const float g0 = g0n, g1 = g1n;
+            if (j + 1 < ntiles) {  // in flight while this tile is scaled
+                g0n = gate(grow0, j + 1);
+                if (two && j + 1 >= split) g1n = gate(grow1, j + 1);
+            }
             if (!mbar_wait(&full[s], (j / kGStages) & 1, &abort_flag)) break;
-            const __nv_bfloat162 g2 = __float2bfloat162_rn(g);
-            uint8_t *row = sm + s * 2 * kGTile + r * 128;  // the row's 128 bytes in each panel (order within is swizzled)
+            const __nv_bfloat162 g02 = __float2bfloat162_rn(g0), g12 = __float2bfloat162_rn(g1);
+            uint8_t *row = sm + s * kGStage + r * 128;  // the row's 128 bytes in each panel (order within is swizzled)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 *p = reinterpret_cast<uint4 *>(row + h * 16384 + c * 16);
-                    uint4 x = *p;
-                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&x);
+                    const uint4 x = *p;
+                    uint4 x0 = x, x1 = x;
+                    __nv_bfloat162 *e0 = reinterpret_cast<__nv_bfloat162 *>(&x0);
+                    __nv_bfloat162 *e1 = reinterpret_cast<__nv_bfloat162 *>(&x1);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) e[k] = __hmul2(e[k], g2);
-                    *p = x;
+                    for (int k = 0; k < 4; ++k) {
+                        e0[k] = __hmul2(e0[k], g02);
+                        e1[k] = __hmul2(e1[k], g12);
+                    }
+                    *p = x0;
+                    if (second) *reinterpret_cast<uint4 *>(row + 2 * kGTile + h * 16384 + c * 16) = x1;
                 }
             fence_async_smem();  // the tensor core reads what these threads wrote
             mbar_arrive(&scaled[s]);
         }
-        // drain: TMEM lane = value dim (row of G), thread = lane
+        // drain: TMEM lane = value dim (row of G), thread = lane; G_i0 then G_i1
         const bool got = mbar_wait(&done, 0, &abort_flag);
         tc_fence_after();
         if (32 * q4 < a.d) {  // warp-uniform (d = 64 stores the first 64 rows and columns)
-            float *Go = a.G + (((size_t)bh * a.N + i) * a.d + r) * a.d;
-            for (int c0 = 0; c0 < a.d; c0 += 32) {
-                uint32_t x[32];
-                tmem_ld32(tD + ((uint32_t)(32 * q4) << 16) + c0, x);
-                tmem_wait_ld();
-                if (got) {
+            for (int which = 0; which < (two ? 2 : 1); ++which) {
+                float *Go = a.G + (((size_t)bh * a.N + (which ? i1 : i0)) * a.d + r) * a.d;
+                for (int c0 = 0; c0 < a.d; c0 += 32) {
+                    uint32_t x[32];
+                    tmem_ld32(tD + 128 * which + ((uint32_t)(32 * q4) << 16) + c0, x);
+                    tmem_wait_ld();
+                    if (got) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4 *>(Go + c0 + k) =
-                            make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
-                                        __uint_as_float(x[k + 3]));
+                        for (int k = 0; k < 32; k += 4)
+                            *reinterpret_cast<float4 *>(Go + c0 + k) =
+                                make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
+                                            __uint_as_float(x[k + 3]));
+                    }
                 }
             }
         }
@@ -177,7 +203,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tD, 128);
+        tmem_dealloc(tD, 256);
     }
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
 }
@@ -545,9 +571,10 @@ cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, con
     a.gam = gam;
     a.G = G;
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.d = p.d; a.mode = p.mode;
+    a.pairs = p.N / 2;  // pairs of the cached segments 0 .. N-2
     cudaError_t e = cudaFuncSetAttribute(bwd_G_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
     if (e != cudaSuccess) return e;
-    bwd_G_tc<<<(unsigned)(p.BH * (p.N - 1)), kGThreads, kGSmem, s>>>(mY, mQ, a);
+    bwd_G_tc<<<(unsigned)(p.BH * a.pairs), kGThreads, kGSmem, s>>>(mY, mQ, a);
     return cudaGetLastError();
 }
 
