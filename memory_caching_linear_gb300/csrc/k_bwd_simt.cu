@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     const int mode = a.mode;
     const bool gated = gated_mode(mode);
     const bool finish = !a.gates_only;
+    const bool stored = finish && gated && a.gam;  // the gates pass ran: gam and the online gate are in memory
     const size_t base = (size_t)bh * a.L * D;
     const T *k = static_cast<const T *>(a.k) + base, *dy = static_cast<const T *>(a.dy) + base;
     const T *u = gated ? static_cast<const T *>(a.u) + base : nullptr;
@@ -456,10 +457,11 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     const size_t seg_base = (size_t)bh * a.N * a.L + tb;  // [N][L] tables of this head, at the tile
 
-    for (int e = tid; e < kTB * D; e += kThreads) {
-        const int r = e / D, c = e % D;
-        Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
-    }
+    if (!stored)
+        for (int e = tid; e < kTB * D; e += kThreads) {
+            const int r = e / D, c = e % D;
+            Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
+        }
     const bool need_kpre = gated && finish;
     if (need_kpre && tid < D) kpre[tid] = 0.f;
     __syncthreads();
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
         for (; j < tb; j += parts) s0 += to_f(k[(size_t)j * D + col]);
         atomicAdd(&kpre[col], (s0 + s1) + (s2 + s3));
     }
-    if (gated)  // scores: a warp takes 32 tokens of one segment (its kbar row broadcast)
+    if (gated && !stored)  // scores: a warp takes 32 tokens of one segment (its kbar row broadcast)
         for (int e = tid; e < kTB * n; e += kThreads) {
             const int i = e / kTB, t = e % kTB;
             gt[t * kTab + i] = t < cnt ? gate_score(Us + t * P, kbar + (size_t)i * D, D) : 0.f;
@@ -499,7 +501,14 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     }
 
     // per token: softmax max and sum (with the online score), the SSC selection, the online gate
-    if (tid < kTB) {
+    if (stored && tid < kTB) {
+        const int t = tid;
+        const float *tw = a.tok + ((size_t)bh * a.L + tb + t) * kBwdTokWords;
+        m_t[t] = t < cnt ? tw[0] : 0.f;
+        z_t[t] = t < cnt ? tw[1] : 1.f;
+        gon[t] = t < cnt ? tw[2] : 0.f;
+        chosen[t] = ~0ull;
+    } else if (tid < kTB) {
         const int t = tid;
         float go = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f, m = 0.f, z = 1.f;
         uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
@@ -537,14 +546,20 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
         float g = 0.f;
         if (t < cnt) {
             if (!gated) g = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
+            else if (stored) g = a.gam[seg_base + (size_t)i * a.L + t];
             else if ((chosen[t] >> i) & 1ull) g = expf(gt[t * kTab + i] - m_t[t]) / z_t[t];
         }
         gt[t * kTab + i] = g;
-        if (!finish && a.gam && t < cnt) a.gam[seg_base + (size_t)i * a.L + t] = g;
+        if (!finish && a.gam && t < cnt) a.gam[seg_base + (size_t)i * a.L + t] = g;  // the gates pass
         if (finish) dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
     }
-    if (!finish) {  // the online gate, for the tensor-core pass
-        if (tid < cnt) a.tok[((size_t)bh * a.L + tb + tid) * kBwdTokWords + 2] = gon[tid];
+    if (!finish) {  // the softmax data and the online gate, for the tensor-core pass and the finishing pass
+        if (tid < cnt) {
+            float *tw = a.tok + ((size_t)bh * a.L + tb + tid) * kBwdTokWords;
+            tw[0] = m_t[tid];
+            tw[1] = z_t[tid];
+            tw[2] = gon[tid];
+        }
         return;
     }
 
