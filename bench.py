@@ -465,8 +465,9 @@ def backward_flops(w):
     key-mean gradient (4 d).  Per kernel: the tensor-core cached pass does M q and dq of
     the cached reads, the G kernels the state gradients, the gate kernel the score
     gradients (and, without the tensor-core pass, the cached M q and dq too), the segment
-    scan the online write and read (4 d^2 per token and run), the reverse scan the online
-    gradients (6 d^2 per token)."""
+    scan the online write and read (4 d^2 per token and run), the reverse scan / the
+    tensor-core dk, dv kernel the online gradients (6 d^2 per token), the state kernel the
+    online write (2 d^2 per token)."""
     s, n = segment_counts(w)
     bh = w.B * w.H
     d = w.d
@@ -477,7 +478,8 @@ def backward_flops(w):
             "bwd_cached_tc": bh * cached, "bwd_gates_simt": bh * (cached + score),
             "bwd_route_simt": bh * score // 2, "bwd_dkbar_simt": bh * score // 2,
             "bwd_G_tc": bh * 2 * d * d * sum(n), "bwd_G_simt": bh * 2 * d * d * sum(n),
-            "seg_scan_simt": bh * 4 * d * d * w.L, "bwd_scan_simt": bh * 6 * d * d * w.L}
+            "seg_scan_simt": bh * 4 * d * d * w.L, "bwd_scan_simt": bh * 6 * d * d * w.L,
+            "bwd_kv_tc": bh * 6 * d * d * w.L, "seg_state_tc": bh * 2 * d * d * w.L, "kbar_simt": bh * d * w.L}
 
 
 def run_backward(args, w, wname):

@@ -991,25 +991,19 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     return cudaSuccess;
 }
 
-// The tensor-core path after the cached pass: the gate work, G on the tensor cores, the reverse scan.
+// The tensor-core path after the cached pass: the gate work, G and dk / dv on the tensor cores.
 template <typename T, int D>
 cudaError_t backward_tc_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 {
-    constexpr int P = D + 1;
-    constexpr int TC = D >= 128 ? 32 : 64;
-    constexpr int TP = TC + 1;
     cudaError_t e = route_impl<T, D>(p, a, s);
     if (e != cudaSuccess) return e;
+    uint8_t *Gimg = reinterpret_cast<uint8_t *>(a.G);
     if (p.N > 1) {
-        if ((e = launch_bwd_G_tc(p, a.dy, a.q, a.gam, a.G, s)) != cudaSuccess) return e;
+        if ((e = launch_bwd_G_tc(p, a.dy, a.q, a.gam, Gimg, s)) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_G_tc");
     }
-    const size_t smem = sizeof(float) * (5 * TC * P + D * P + 2 * TC * TP + D);
-    auto kern = bwd_scan_simt<T, D, TC>;
-    if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-    kern<<<(unsigned)((long long)p.BH * p.N), kThreads, smem, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    profile_after_kernel(s, "bwd_scan_simt");
+    if ((e = launch_bwd_kv_tc(p, a.q, a.k, a.v, a.u, a.dy, Gimg, a.tok, a.dkbar, a.dk, a.dv, s)) != cudaSuccess) return e;
+    profile_after_kernel(s, "bwd_kv_tc");
     return cudaSuccess;
 }
 
@@ -1032,7 +1026,9 @@ size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t backward_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
-    const size_t common = 2 * pad256(4 * BH * N * d * d) + 2 * pad256(4 * BH * N * d) + pad256(4 * BH * L * kBwdTokWords);
+    const size_t gbytes = bwd_tc_supported(p) ? (size_t)32768 * BH * N : 4 * BH * N * d * d;  // G: images or fp32
+    const size_t common = pad256(4 * BH * N * d * d) + pad256(gbytes) + 2 * pad256(4 * BH * N * d) +
+                          pad256(4 * BH * L * kBwdTokWords);
     if (bwd_tc_supported(p)) {
         const size_t gam = mode_uses_u(p.mode) ? N : 0;
         return common + pad256(4 * BH * L * gam) + pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p));
@@ -1055,7 +1051,7 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
     const bool gated = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
     const bool tc = bwd_tc_supported(p);
     float *states = reinterpret_cast<float *>(take(4 * BH * N * d * d));
-    float *G = reinterpret_cast<float *>(take(4 * BH * N * d * d));
+    float *G = reinterpret_cast<float *>(take(tc ? (size_t)32768 * BH * N : 4 * BH * N * d * d));
     float *kbar = reinterpret_cast<float *>(take(4 * BH * N * d));
     float *dkbar = reinterpret_cast<float *>(take(4 * BH * N * d));
     float *tok = reinterpret_cast<float *>(take(4 * BH * L * kBwdTokWords));

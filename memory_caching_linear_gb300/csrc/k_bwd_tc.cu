@@ -8,7 +8,8 @@
 //
 // bwd_G_tc -- the gradient of every cached state ([MC-ja §3 after eq. 4b]: the cached
 //   M^(i) is read by every token of the later segments with its gate g_{t,i}):
-//     G_i = sum_{t in segments > i} g_{t,i} dy_t q_t^T        (d_v x d_k, fp32)
+//     G_i = sum_{t in segments > i} g_{t,i} dy_t q_t^T        (d_v x d_k, fp32 accumulation,
+//                                                              written as a bf16 operand image)
 //   One CTA per (b,h, pair of cached segments), the pair with the most later tokens
 //   first.  Per 128-token tile: the TMA brings dy and q (two 64-column
 //   128-byte-swizzled panels each), the four worker warps scale their token's dy row
@@ -40,13 +41,18 @@ constexpr size_t kGSmem = kGStages * kGStage + 1024;
 
 struct GArgs {
     const float *gam;  // [BH][N][L]: g_{t,i} of the cached segments (routed aggregations)
-    float *G;          // [BH][N][d][d]
+    uint8_t *G;        // [BH][N] x 32 KB: G_i as a bf16 operand image (rows = value dim, as a state image)
     int BH, L, C, N, d, mode, pairs;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // One CTA per (b,h, pair of cached segments i0 = 2p, i1 = 2p + 1): every tile after
@@ -178,22 +184,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
             fence_async_smem();  // the tensor core reads what these threads wrote
             mbar_arrive(&scaled[s]);
         }
-        // drain: TMEM lane = value dim (row of G), thread = lane; G_i0 then G_i1
+        // drain: TMEM lane = value dim (row of G), thread = lane; G_i0 then G_i1 as bf16
+        // images (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8); zero beyond d)
         const bool got = mbar_wait(&done, 0, &abort_flag);
         tc_fence_after();
-        if (32 * q4 < a.d) {  // warp-uniform (d = 64 stores the first 64 rows and columns)
-            for (int which = 0; which < (two ? 2 : 1); ++which) {
-                float *Go = a.G + (((size_t)bh * a.N + (which ? i1 : i0)) * a.d + r) * a.d;
-                for (int c0 = 0; c0 < a.d; c0 += 32) {
-                    uint32_t x[32];
-                    tmem_ld32(tD + 128 * which + ((uint32_t)(32 * q4) << 16) + c0, x);
-                    tmem_wait_ld();
-                    if (got) {
+        for (int which = 0; which < (two ? 2 : 1); ++which) {
+            uint8_t *img = a.G + ((size_t)bh * a.N + (which ? i1 : i0)) * kGTile + r * 128;
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t x[32];
+                tmem_ld32(tD + 128 * which + ((uint32_t)(32 * q4) << 16) + c0, x);
+                tmem_wait_ld();
+                if (got) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4)
-                            *reinterpret_cast<float4 *>(Go + c0 + k) =
-                                make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
-                                            __uint_as_float(x[k + 3]));
+                    for (int q = 0; q < 4; ++q) {  // 8 columns = one 16-byte chunk
+                        const int c8 = c0 / 8 + q, h = c8 >> 3, cc = c8 & 7;
+                        const uint4 v = make_uint4(
+                            pack_bf16x2(__uint_as_float(x[8 * q]), __uint_as_float(x[8 * q + 1])),
+                            pack_bf16x2(__uint_as_float(x[8 * q + 2]), __uint_as_float(x[8 * q + 3])),
+                            pack_bf16x2(__uint_as_float(x[8 * q + 4]), __uint_as_float(x[8 * q + 5])),
+                            pack_bf16x2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7])));
+                        *reinterpret_cast<uint4 *>(img + h * 16384 + ((cc ^ (r & 7)) << 4)) = v;
                     }
                 }
             }
@@ -552,6 +562,283 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
 }
 
+// ============================================================================
+// bwd_kv_tc -- dk and dv of one 128-token chunk c of segment n (tokens j), from the
+// cached state's gradient G_n and the online memory's reads in the segment (tokens
+// t >= j, gate g_on(t)):
+//   dv_j = G_n k_j + sum_{t >= j in n} g_on(t) (k_j . q_t) dy_t
+//   dk_j = G_n^T v_j + sum_{t >= j in n} g_on(t) (v_j . dy_t) q_t
+//          + sum_{t >= j in n} w_t u_t + dkbar_n / |n|      (w_t = dr_on(t) / cnt_t)
+// On the tensor cores: D_v = K G^T, D_k = V G (the G image); then for every chunk c'
+// >= c of the segment X = K Q'^T, Y = V dY'^T (SS); the workers turn them into
+// P3 = g_on mask(X), P4 = g_on mask(Y), P5 = w mask (mask: t >= j inside chunk c)
+// and D_v += P3 dY', D_k += P4 Q' + P5 U' (TS, the chunk tiles read MN-major).
+// Persistent, one CTA per SM, chunks with the most later chunks first.
+// TMEM: D_v [0,128) | D_k [128,256) | X [256,384) | Y [384,512).
+// ============================================================================
+constexpr int kVThreads = 192;
+constexpr size_t kVSmem = 6 * kGTile + 1024;  // K, V, G image; Q', dY', U' of the current chunk pair
+
+struct VArgs {
+    const uint8_t *G;      // [BH][N] x 32 KB G images (segments < N-1)
+    const float *tok;      // [BH][L][kBwdTokWords]: word 2 the online gate, word 4 the pooled-key weight w
+    const float *dkbar;    // [BH][N][d]
+    void *dk, *dv;         // bf16 [BH][L][d] out
+    int BH, L, C, N, CPS, d, routed, num_tiles;
+};
+
+__global__ void __launch_bounds__(kVThreads, 1)
+    bwd_kv_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+              const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mY,
+              const __grid_constant__ CUtensorMap mU, VArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *sK = sm, *sV = sm + kGTile, *sG = sm + 2 * kGTile;
+    uint8_t *sQ = sm + 3 * kGTile, *sY = sm + 4 * kGTile, *sU = sm + 5 * kGTile;
+    __shared__ uint64_t kv_full, kv_empty, pr_full, pr_empty, xy_full, p_full, d_full, d_empty, fin;
+    __shared__ float gs[2][128], ws[2][128];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int my_tiles = blockIdx.x < (unsigned)a.num_tiles ? (a.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile = [&](int j, int &bh, int &n, int &c) {  // chunk 0 (the most later chunks) first
+        const int id = (int)blockIdx.x + j * (int)gridDim.x;
+        const int per = a.BH * a.N;
+        c = id / per;
+        n = (id % per) / a.BH;
+        bh = (id % per) % a.BH;
+    };
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        abort_flag = 0;
+        mbar_init(&kv_full, 1);
+        mbar_init(&kv_empty, 1);
+        mbar_init(&pr_full, 1);
+        mbar_init(&pr_empty, 1);
+        mbar_init(&xy_full, 1);
+        mbar_init(&p_full, 128);
+        mbar_init(&d_full, 1);
+        mbar_init(&d_empty, 128);
+        mbar_init(&fin, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    const uint32_t tDv = tb, tDk = tb + 128, tX = tb + 256, tY = tb + 384;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0 && my_tiles > 0) {
+            prefetch_tensormap(&mK);
+            prefetch_tensormap(&mV);
+            prefetch_tensormap(&mQ);
+            prefetch_tensormap(&mY);
+            if (a.routed) prefetch_tensormap(&mU);
+            uint32_t pc = 0;
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                int bh, n, c;
+                tile(j, bh, n, c);
+                const bool hasG = n < a.N - 1;
+                if (!(ok = mbar_wait(&kv_empty, (j & 1) ^ 1, &abort_flag))) break;
+                const int row = bh * a.L + n * a.C + c * kGT;
+                mbar_arrive_expect_tx(&kv_full, (hasG ? 3 : 2) * kGTile);
+                tma_load_2d(sK, &mK, 0, row, &kv_full);
+                tma_load_2d(sK + 16384, &mK, 64, row, &kv_full);
+                tma_load_2d(sV, &mV, 0, row, &kv_full);
+                tma_load_2d(sV + 16384, &mV, 64, row, &kv_full);
+                if (hasG) bulk_load(sG, a.G + ((size_t)bh * a.N + n) * kGTile, kGTile, &kv_full);
+                for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
+                    if (!(ok = mbar_wait(&pr_empty, (pc & 1) ^ 1, &abort_flag))) break;
+                    const int r2 = bh * a.L + n * a.C + c2 * kGT;
+                    mbar_arrive_expect_tx(&pr_full, (a.routed ? 3 : 2) * kGTile);
+                    tma_load_2d(sQ, &mQ, 0, r2, &pr_full);
+                    tma_load_2d(sQ + 16384, &mQ, 64, r2, &pr_full);
+                    tma_load_2d(sY, &mY, 0, r2, &pr_full);
+                    tma_load_2d(sY + 16384, &mY, 64, r2, &pr_full);
+                    if (a.routed) {
+                        tma_load_2d(sU, &mU, 0, r2, &pr_full);
+                        tma_load_2d(sU + 16384, &mU, 64, r2, &pr_full);
+                    }
+                }
+            }
+            // leave no copy in flight
+            int give_up = 0;
+            if (pc > 0) mbar_wait_limit(&pr_full, (pc - 1) & 1, &give_up, kWaitLimitNs);
+            mbar_wait_limit(&kv_full, (my_tiles - 1) & 1, &give_up, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && my_tiles > 0) {
+            constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);
+            auto kmaj = [](int kk) { return (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32); };
+            const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV), g0 = smem_u32(sG);
+            const uint32_t q0 = smem_u32(sQ), y0 = smem_u32(sY), u0 = smem_u32(sU);
+            uint32_t pc = 0;
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                int bh, n, c;
+                tile(j, bh, n, c);
+                const bool hasG = n < a.N - 1;
+                if (!(ok = mbar_wait(&kv_full, j & 1, &abort_flag) && mbar_wait(&d_empty, (j & 1) ^ 1, &abort_flag)))
+                    break;
+                tc_fence_after();
+                if (hasG) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // D_v = K G^T: B = G image K-major (rows = value dim)
+                        mma_ss(tDv, make_desc_sw128(k0 + kmaj(kk), 0, 1024), make_desc_sw128(g0 + kmaj(kk), 0, 1024),
+                               idKK, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // D_k = V G: B = G image MN-major
+                        mma_ss(tDk, make_desc_sw128(v0 + kmaj(kk), 0, 1024), make_desc_sw128(g0 + kk * 2048u, 16384, 1024),
+                               idKM, kk > 0);
+                }
+                for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
+                    if (!(ok = mbar_wait(&pr_full, pc & 1, &abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // X = K Q'^T
+                        mma_ss(tX, make_desc_sw128(k0 + kmaj(kk), 0, 1024), make_desc_sw128(q0 + kmaj(kk), 0, 1024), idKK,
+                               kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // Y = V dY'^T
+                        mma_ss(tY, make_desc_sw128(v0 + kmaj(kk), 0, 1024), make_desc_sw128(y0 + kmaj(kk), 0, 1024), idKK,
+                               kk > 0);
+                    mma_commit(&xy_full);
+                    if (!(ok = mbar_wait(&p_full, pc & 1, &abort_flag))) break;
+                    tc_fence_after();
+                    const bool first = !hasG && c2 == c;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // D_v += P3 dY'
+                        mma_ts(tDv, tX + kk * 8, make_desc_sw128(y0 + kk * 2048u, 16384, 1024), idKM, !first || kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // D_k += P4 Q'
+                        mma_ts(tDk, tY + kk * 8, make_desc_sw128(q0 + kk * 2048u, 16384, 1024), idKM, !first || kk > 0);
+                    if (a.routed) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)  // D_k += P5 U'
+                            mma_ts(tDk, tY + 64 + kk * 8, make_desc_sw128(u0 + kk * 2048u, 16384, 1024), idKM, 1);
+                    }
+                    mma_commit(&pr_empty);
+                }
+                if (!ok) break;
+                mma_commit(&kv_empty);
+                mma_commit(&d_full);
+            }
+            // leave no MMA in flight
+            mma_commit(&fin);
+            int give_up = 0;
+            mbar_wait_limit(&fin, 0, &give_up, kWaitLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------------- workers (thread = row j of chunk c)
+        const int q4 = warp & 3;
+        const uint32_t row = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        uint32_t pc = 0;
+        bool ok = true;
+        for (int j = 0; j < my_tiles && ok; ++j) {
+            int bh, n, c;
+            tile(j, bh, n, c);
+            for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
+                // the gates and pooled-key weights of chunk c2's tokens (each worker brings its own)
+                const int b = pc & 1;
+                const float *tw = a.tok + ((size_t)bh * a.L + n * a.C + c2 * kGT + row) * kBwdTokWords;
+                gs[b][row] = tw[2];
+                ws[b][row] = a.routed ? tw[4] : 0.f;
+                named_bar_sync(1, 128);
+                if (!(ok = mbar_wait(&xy_full, pc & 1, &abort_flag))) break;
+                tc_fence_after();
+                const bool diag = c2 == c;  // the same chunk: only t >= j
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {  // 16 key columns t at a time
+                    uint32_t x[16], y[16], o3[8], o4[8];
+                    tmem_ld16(tX + lane_base + 16 * m, x);
+                    tmem_ld16(tY + lane_base + 16 * m, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        const int t = 16 * m + k;
+                        const float g0 = (!diag || t >= (int)row) ? gs[b][t] : 0.f;
+                        const float g1 = (!diag || t + 1 >= (int)row) ? gs[b][t + 1] : 0.f;
+                        o3[k / 2] = pack_bf16x2(g0 * __uint_as_float(x[k]), g1 * __uint_as_float(x[k + 1]));
+                        o4[k / 2] = pack_bf16x2(g0 * __uint_as_float(y[k]), g1 * __uint_as_float(y[k + 1]));
+                    }
+                    tmem_st8(tX + lane_base + 8 * m, o3);
+                    tmem_st8(tY + lane_base + 8 * m, o4);
+                }
+                if (a.routed) {  // P5 = w mask, written after every read of Y
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        uint32_t o5[8];
+#pragma unroll
+                        for (int k = 0; k < 16; k += 2) {
+                            const int t = 16 * m + k;
+                            o5[k / 2] = pack_bf16x2((!diag || t >= (int)row) ? ws[b][t] : 0.f,
+                                                    (!diag || t + 1 >= (int)row) ? ws[b][t + 1] : 0.f);
+                        }
+                        tmem_st8(tY + 64 + lane_base + 8 * m, o5);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full);
+            }
+            if (!ok) break;
+            // drain: dv = D_v, dk = D_k + dkbar_n / |n|
+            if (!(ok = mbar_wait(&d_full, j & 1, &abort_flag))) break;
+            tc_fence_after();
+            const size_t tok = (size_t)bh * a.L + n * a.C + c * kGT + row;
+            __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(a.dv) + tok * a.d;
+            __nv_bfloat16 *dko = static_cast<__nv_bfloat16 *>(a.dk) + tok * a.d;
+            const float *rho = a.dkbar + ((size_t)bh * a.N + n) * a.d;
+            const float inv_len = 1.f / (float)a.C;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint32_t xv[32], xk[32];
+                tmem_ld32(tDv + lane_base + 32 * m, xv);
+                tmem_ld32(tDk + lane_base + 32 * m, xk);
+                tmem_wait_ld();
+                if (32 * m < a.d) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 8) {
+                        uint4 ov, ok4;
+                        uint32_t *pv = reinterpret_cast<uint32_t *>(&ov), *pk = reinterpret_cast<uint32_t *>(&ok4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = 32 * m + k + 2 * e;
+                            pv[e] = pack_bf16x2(__uint_as_float(xv[k + 2 * e]), __uint_as_float(xv[k + 2 * e + 1]));
+                            const float r0 = a.routed ? __ldg(rho + col) * inv_len : 0.f;
+                            const float r1 = a.routed ? __ldg(rho + col + 1) * inv_len : 0.f;
+                            pk[e] = pack_bf16x2(__uint_as_float(xk[k + 2 * e]) + r0, __uint_as_float(xk[k + 2 * e + 1]) + r1);
+                        }
+                        *reinterpret_cast<uint4 *>(dvo + 32 * m + k) = ov;
+                        *reinterpret_cast<uint4 *>(dko + 32 * m + k) = ok4;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&d_empty);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+    if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
+}
+
 }  // namespace
 
 bool bwd_tc_supported(const Problem &p)
@@ -559,7 +846,7 @@ bool bwd_tc_supported(const Problem &p)
     return p.bf16 && (p.d == 128 || p.d == 64) && p.C % kGT == 0 && p.L % p.C == 0 && p.N <= 64;
 }
 
-cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, float *G, cudaStream_t s)
+cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, uint8_t *G, cudaStream_t s)
 {
     if (p.N < 2) return cudaSuccess;
     CUtensorMap mY, mQ;
@@ -637,6 +924,43 @@ cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k,
     if (sms <= 0) sms = 148;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
     bwd_cached_tc<<<grid, kCThreads, kCSmem, s>>>(mQ, mK, mV, mY, a);
+    return cudaGetLastError();
+}
+
+}  // namespace mc
+
+namespace mc {
+
+cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
+                             const uint8_t *G, const float *tok, const float *dkbar, void *dk, void *dv, cudaStream_t s)
+{
+    const bool routed = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
+    CUtensorMap mK, mV, mQ, mY, mU;
+    const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    if (!make_tmap_bf16_sw128(&mK, k, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mV, v, rows, p.d, kGT) ||
+        !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT))
+        return cudaErrorInvalidValue;
+    if (routed) {
+        if (!make_tmap_bf16_sw128(&mU, u, rows, p.d, kGT)) return cudaErrorInvalidValue;
+    } else {
+        mU = mK;
+    }
+    VArgs a{};
+    a.G = G;
+    a.tok = tok;
+    a.dkbar = dkbar;
+    a.dk = dk;
+    a.dv = dv;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kGT; a.d = p.d; a.routed = routed ? 1 : 0;
+    a.num_tiles = p.BH * p.N * a.CPS;
+    cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kVSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+    bwd_kv_tc<<<grid, kVThreads, kVSmem, s>>>(mK, mV, mQ, mY, mU, a);
     return cudaGetLastError();
 }
 

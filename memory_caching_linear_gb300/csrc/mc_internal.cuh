@@ -146,7 +146,8 @@ struct BwdArgs {
     const float *r_on;    // [BH][L]
     const float *O_on;    // [BH][L][d]  M_t q_t (online read)
     const float *X_on;    // [BH][L][d]  M_t^T dy_t
-    float *G;             // [BH][N][d][d]  sum_t g_{t,i} dy_t q_t^T per cached segment
+    float *G;             // [BH][N][d][d]  sum_t g_{t,i} dy_t q_t^T per cached segment (tensor-core path:
+                          // [BH][N] x 32 KB bf16 operand images)
     float *dkbar;         // [BH][N][d]  gradient of the key means (accumulated)
     float *tok;           // [BH][L][kBwdTokWords]
     int32_t *sel_idx;     // SSC: [BH][L][topk] selected segments (segment order, -1 padded)
@@ -163,7 +164,9 @@ size_t backward_scratch_bytes(const Problem &p);
 // Tensor-core pieces of the backward (k_bwd_tc.cu): bf16, d in {64, 128}, seg_len % 128 == 0,
 // L % seg_len == 0, N <= 64.
 bool bwd_tc_supported(const Problem &p);
-cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, float *G, cudaStream_t s);
+cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, uint8_t *G, cudaStream_t s);
+cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
+                             const uint8_t *G, const float *tok, const float *dkbar, void *dk, void *dv, cudaStream_t s);
 size_t bwd_cached_scratch_bytes(const Problem &p);
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
                                  const TcImages &img, const float *gam, const float *tok, void *scratch,
