@@ -634,40 +634,50 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// bwd_dkbar_simt: the key-mean gradient of a cached segment from the score
-// gradients, dkbar_i = sum_{t >= (i+1) C} dr_{t,i} u_t.  One CTA per (bh, i < N-1,
-// chunk of kDkChunk later tokens); a thread sums a dimension over a strided share
-// of the chunk (four tokens in flight), the CTA adds its sum to dkbar (zeroed first).
+// bwd_dkbar_simt: the key-mean gradients from the score gradients,
+// dkbar_i = sum_{t : n(t) > i} dr_{t,i} u_t, on the shapes of the tensor-core path
+// (N <= 64).  One CTA per (bh, kDkChunk tokens): every token's u is read once and
+// feeds every cached segment it scored; a thread keeps one dimension's sums for all
+// segments over a strided share of the chunk, 128 tokens at a time with their dr
+// staged in shared memory, and the CTA adds them to dkbar (zeroed first).
 // ---------------------------------------------------------------------------
 constexpr int kDkChunk = 1024;
+constexpr int kDkSub = 128;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks)
 {
-    __shared__ float part[D];
-    const int ch = (int)blockIdx.x % chunks, rest = (int)blockIdx.x / chunks;
-    const int i = rest / a.BH, bh = rest % a.BH;
-    const int t_lo = (i + 1) * a.C + ch * kDkChunk;
-    if (t_lo >= a.L) return;
-    const int t_hi = min(t_lo + kDkChunk, a.L);
     constexpr int parts = kThreads / D;
-    const int col = threadIdx.x % D, p = threadIdx.x / D;
-    if (threadIdx.x < D) part[threadIdx.x] = 0.f;
-    __syncthreads();
+    __shared__ float sdr[kTab][kDkSub];
+    const int ch = (int)blockIdx.x % chunks, bh = (int)blockIdx.x / chunks;
+    const int t_lo = ch * kDkChunk, t_hi = min(t_lo + kDkChunk, a.L);
+    const int col = threadIdx.x % D, part = threadIdx.x / D;
+    const int nmax = min(a.N - 1, (t_hi - 1) / a.C);  // cached segments any token of the chunk scored
     const T *u = static_cast<const T *>(a.u) + (size_t)bh * a.L * D + col;
-    const float *dr = a.dr + ((size_t)bh * a.N + i) * a.L;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int t = t_lo + p;
-    for (; t + 3 * parts < t_hi; t += 4 * parts) {
-        s0 = fmaf(__ldg(dr + t), to_f(u[(size_t)t * D]), s0);
-        s1 = fmaf(__ldg(dr + t + parts), to_f(u[(size_t)(t + parts) * D]), s1);
-        s2 = fmaf(__ldg(dr + t + 2 * parts), to_f(u[(size_t)(t + 2 * parts) * D]), s2);
-        s3 = fmaf(__ldg(dr + t + 3 * parts), to_f(u[(size_t)(t + 3 * parts) * D]), s3);
+    const float *dr = a.dr + (size_t)bh * a.N * a.L;
+    float acc[kTab];
+#pragma unroll
+    for (int i = 0; i < kTab; ++i) acc[i] = 0.f;
+    for (int t0 = t_lo; t0 < t_hi; t0 += kDkSub) {
+        const int cnt = min(kDkSub, t_hi - t0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nmax * kDkSub; e += kThreads) {
+            const int i = e / kDkSub, t = e % kDkSub;
+            sdr[i][t] = t < cnt && i < (t0 + t) / a.C ? dr[(size_t)i * a.L + t0 + t] : 0.f;
+        }
+        __syncthreads();
+        for (int t = part; t < cnt; t += parts) {
+            const float uv = to_f(u[(size_t)(t0 + t) * D]);
+            const int n_t = min((t0 + t) / a.C, kTab);
+#pragma unroll
+            for (int i = 0; i < kTab; ++i)
+                if (i < n_t) acc[i] = fmaf(sdr[i][t], uv, acc[i]);
+        }
     }
-    for (; t < t_hi; t += parts) s0 = fmaf(__ldg(dr + t), to_f(u[(size_t)t * D]), s0);
-    atomicAdd(&part[col], (s0 + s1) + (s2 + s3));
-    __syncthreads();
-    if (threadIdx.x < D) atomicAdd(a.dkbar + ((size_t)bh * a.N + i) * D + threadIdx.x, part[threadIdx.x]);
+    float *dk = a.dkbar + (size_t)bh * a.N * D + col;
+#pragma unroll
+    for (int i = 0; i < kTab; ++i)
+        if (i < nmax && acc[i] != 0.f) atomicAdd(dk + (size_t)i * D, acc[i]);
 }
 
 // ---------------------------------------------------------------------------
@@ -983,8 +993,8 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_after_kernel(s, "bwd_route_simt");
     if (!a.gates_only && a.dr && p.N > 1) {
-        const int chunks = (p.L - p.C + kDkChunk - 1) / kDkChunk;
-        bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * (p.N - 1) * chunks), kThreads, 0, s>>>(a, chunks);
+        const int chunks = (p.L + kDkChunk - 1) / kDkChunk;
+        bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * chunks), kThreads, 0, s>>>(a, chunks);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_dkbar_simt");
     }
