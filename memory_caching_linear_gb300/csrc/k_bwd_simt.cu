@@ -462,8 +462,9 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             const int r = e / D, c = e % D;
             Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
         }
-    const bool need_kpre = gated && finish;
-    if (need_kpre && tid < D) kpre[tid] = 0.f;
+    const bool need_kpre = gated && finish && !a.kpre_tiles;
+    if (gated && finish && tid < D)
+        kpre[tid] = a.kpre_tiles ? a.kpre_tiles[(((size_t)bh * a.N + n) * tps + tile) * D + tid] : 0.f;
     __syncthreads();
     if (need_kpre) {  // keys of the segment before the tile: a strided share per thread, four loads in flight
         constexpr int parts = kThreads / D;
@@ -630,6 +631,36 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             w[3] = dl[t];
             w[4] = gated ? dron * inv_cnt : 0.f;
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_kpre_simt: for every segment, the sum of its keys before each 64-token tile
+// (the pooled key of the online memory needs it); one CTA of D threads per (bh,
+// segment), a thread per dimension walking the segment, four tokens in flight.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(D) bwd_kpre_simt(BwdArgs a)
+{
+    const int n = (int)blockIdx.x % a.N, bh = (int)blockIdx.x / a.N;
+    const int t0 = n * a.C, t1 = min(t0 + a.C, a.L);
+    const int tps = (a.C + kTB - 1) / kTB;
+    const T *k = static_cast<const T *>(a.k) + (size_t)bh * a.L * D + threadIdx.x;
+    float *out = a.kpre_tiles + ((size_t)bh * a.N + n) * tps * D + threadIdx.x;
+    float s = 0.f;
+    for (int tile = 0; tile < tps; ++tile) {
+        out[(size_t)tile * D] = s;
+        const int tb = t0 + tile * kTB, te = min(tb + kTB, t1);
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int t = tb;
+        for (; t + 3 < te; t += 4) {
+            s0 += to_f(k[(size_t)t * D]);
+            s1 += to_f(k[(size_t)(t + 1) * D]);
+            s2 += to_f(k[(size_t)(t + 2) * D]);
+            s3 += to_f(k[(size_t)(t + 3) * D]);
+        }
+        for (; t < te; ++t) s0 += to_f(k[(size_t)t * D]);
+        s += (s0 + s1) + (s2 + s3);
     }
 }
 
@@ -988,6 +1019,11 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     auto kern = bwd_route_simt<T, D>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
+    if (!a.gates_only && a.kpre_tiles) {
+        bwd_kpre_simt<T, D><<<(unsigned)((long long)p.BH * p.N), D, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        profile_after_kernel(s, "bwd_kpre_simt");
+    }
     const long long tps = (p.C + kTB - 1) / kTB;
     kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1041,7 +1077,9 @@ size_t backward_scratch_bytes(const Problem &p)
                           pad256(4 * BH * L * kBwdTokWords);
     if (bwd_tc_supported(p)) {
         const size_t gam = mode_uses_u(p.mode) ? N : 0;
-        return common + pad256(4 * BH * L * gam) + pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p));
+        const size_t kpre = mode_uses_u(p.mode) ? N * ((p.C + kTB - 1) / kTB) * d : 0;
+        return common + pad256(4 * BH * L * gam) + pad256(4 * BH * kpre) + pad256(tc_state_scratch_bytes(p)) +
+               pad256(bwd_cached_scratch_bytes(p));
     }
     const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
     return common + pad256(4 * BH * L) + 2 * pad256(4 * BH * L * d) + 2 * pad256(4 * BH * L * sel);
@@ -1085,6 +1123,7 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         // online dg, dq), the gate work on whole tables, the key-mean gradient, G on the tensor
         // cores and the reverse scan.
         float *gam = gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
+        a.kpre_tiles = gated ? reinterpret_cast<float *>(take(4 * BH * N * ((p.C + kTB - 1) / kTB) * d)) : nullptr;
         void *state_scratch = take(tc_state_scratch_bytes(p));
         void *cached_scratch = take(bwd_cached_scratch_bytes(p));
         TcImages img{};

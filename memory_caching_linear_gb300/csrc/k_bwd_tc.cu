@@ -36,7 +36,7 @@ constexpr int kGT = 128;             // tokens per tile
 constexpr uint32_t kGTile = 32768;   // one 128 x 128 bf16 operand tile (two 16 KB panels)
 constexpr int kGStages = 2;          // tile stages in flight: dy (scaled in place for the first state), q, g o dy for the second
 constexpr int kGThreads = 192;       // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
-constexpr uint32_t kGStage = 3 * kGTile;
+constexpr uint32_t kGStage = 3 * kGTile + 1024;  // + the tile's gates of both segments (2 x 128 floats)
 constexpr size_t kGSmem = kGStages * kGStage + 1024;
 
 struct GArgs {
@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int t_begin = (i0 + 1) * a.C;
     const int ntiles = (a.L - t_begin) / kGT;
     const int split = a.C / kGT;  // tiles of segment i1: the second state starts after them
+    const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -105,11 +106,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (!mbar_wait(&empty[s], ((j / kGStages) & 1) ^ 1, &abort_flag)) break;
                 uint8_t *st = sm + s * kGStage;
                 const int row = bh * a.L + t_begin + j * kGT;
-                mbar_arrive_expect_tx(&full[s], 2 * kGTile);
+                const bool g0 = routed, g1 = routed && two && j >= split;  // gates to bring along
+                mbar_arrive_expect_tx(&full[s], 2 * kGTile + (g0 ? 512 : 0) + (g1 ? 512 : 0));
                 tma_load_2d(st, &mY, 0, row, &full[s]);
                 tma_load_2d(st + 16384, &mY, 64, row, &full[s]);
                 tma_load_2d(st + kGTile, &mQ, 0, row, &full[s]);
                 tma_load_2d(st + kGTile + 16384, &mQ, 64, row, &full[s]);
+                const size_t goff = (size_t)t_begin + (size_t)j * kGT;
+                if (g0) bulk_load(st + 3 * kGTile, a.gam + ((size_t)bh * a.N + i0) * a.L + goff, 512, &full[s]);
+                if (g1) bulk_load(st + 3 * kGTile + 512, a.gam + ((size_t)bh * a.N + i1) * a.L + goff, 512, &full[s]);
                 issued = j + 1;
             }
             // leave no copy in flight
@@ -144,24 +149,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         // ---------------------------------------------------------- workers: token row r of each tile
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
-        const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
-        const float *grow0 = routed ? a.gam + ((size_t)bh * a.N + i0) * a.L + t_begin + r : nullptr;
-        const float *grow1 = routed && two ? a.gam + ((size_t)bh * a.N + i1) * a.L + t_begin + r : nullptr;
-        auto gate = [&](const float *grow, int j) -> float {  // this thread's token in tile j
-            const int t = t_begin + j * kGT + r;
-            return routed ? __ldg(grow + (size_t)j * kGT) : (a.mode == MC_MEAN ? 1.f / (float)(t / a.C + 1) : 1.f);
-        };
-        float g0n = ntiles > 0 ? gate(grow0, 0) : 0.f;
-        float g1n = two && split < ntiles ? gate(grow1, split) : 0.f;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kGStages;
             const bool second = two && j >= split;
-            const float g0 = g0n, g1 = g1n;
-            if (j + 1 < ntiles) {  // in flight while this tile is scaled
-                g0n = gate(grow0, j + 1);
-                if (two && j + 1 >= split) g1n = gate(grow1, j + 1);
-            }
             if (!mbar_wait(&full[s], (j / kGStages) & 1, &abort_flag)) break;
+            // the gates came with the tile (routed); Residual 1, Mean 1 / (n(t) + 1)
+            const float *gsm = reinterpret_cast<const float *>(sm + s * kGStage + 3 * kGTile);
+            const float gc = a.mode == MC_MEAN ? 1.f / (float)((t_begin + j * kGT) / a.C + 1) : 1.f;
+            const float g0 = routed ? gsm[r] : gc;
+            const float g1 = routed ? (second ? gsm[128 + r] : 0.f) : gc;
             const __nv_bfloat162 g02 = __float2bfloat162_rn(g0), g12 = __float2bfloat162_rn(g1);
             uint8_t *row = sm + s * kGStage + r * 128;  // the row's 128 bytes in each panel (order within is swizzled)
 #pragma unroll

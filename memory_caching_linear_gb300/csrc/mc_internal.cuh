@@ -157,6 +157,7 @@ struct BwdArgs {
     const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
+    float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
     int gates_only;       // 1: only the gates (gam, the SSC selection), nothing else
     int BH, L, C, N, mode, topk;
 };
