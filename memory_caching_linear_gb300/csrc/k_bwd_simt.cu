@@ -414,10 +414,10 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
 // ---------------------------------------------------------------------------
 // bwd_route_simt: the gate work of the tensor-core backward, one CTA per (bh,
 // segment n, tile of kTB tokens), on whole tables in shared memory (n <= 63):
-//   scores r_{t,i} = <u_t, kbar_i>, the gates g_{t,i} (GRM / Soup softmax with the
-//   online score; SSC over the topk largest, equal scores to the lower index;
-//   Residual 1; Mean 1 / (n + 1)); with gates_only the gates go to gam and nothing
-//   else happens.  Otherwise, with dg_{t,i} from the tensor cores:
+//   the gates g_{t,i} -- read from gam (routed aggregations, written by the
+//   tensor-core gates pass) or, without it, scores r_{t,i} = <u_t, kbar_i> and GRM /
+//   Soup softmax with the online score, SSC over the topk largest (equal scores to
+//   the lower index); Residual 1; Mean 1 / (n + 1).  With dg_{t,i} from the tensor cores:
 //   delta_t = sum_i g dg + g_on dg_on,  dr_{t,i} = g (dg - delta) -> dr,
 //   du_t = sum_i dr_{t,i} kbar_i + dr_on p_t,  dq_t = (cached part) + g_on M_t^T dy_t.
 // ---------------------------------------------------------------------------
@@ -448,8 +448,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     const int cnt = te - tb;
     const int mode = a.mode;
     const bool gated = gated_mode(mode);
-    const bool finish = !a.gates_only;
-    const bool stored = finish && gated && a.gam;  // the gates pass ran: gam and the online gate are in memory
+    const bool stored = gated && a.gam;  // the gates pass ran: gam and the online gate are in memory
     const size_t base = (size_t)bh * a.L * D;
     const T *k = static_cast<const T *>(a.k) + base, *dy = static_cast<const T *>(a.dy) + base;
     const T *u = gated ? static_cast<const T *>(a.u) + base : nullptr;
@@ -462,8 +461,8 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             const int r = e / D, c = e % D;
             Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
         }
-    const bool need_kpre = gated && finish && !a.kpre_tiles;
-    if (gated && finish && tid < D)
+    const bool need_kpre = gated && !a.kpre_tiles;
+    if (gated && tid < D)
         kpre[tid] = a.kpre_tiles ? a.kpre_tiles[(((size_t)bh * a.N + n) * tps + tile) * D + tid] : 0.f;
     __syncthreads();
     if (need_kpre) {  // keys of the segment before the tile: a strided share per thread, four loads in flight
@@ -486,7 +485,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             gt[t * kTab + i] = t < cnt ? gate_score(Us + t * P, kbar + (size_t)i * D, D) : 0.f;
         }
     __syncthreads();
-    if (finish && gated) {  // u is spent: the buffer takes the tile's keys, then their running sums per column
+    if (gated) {  // u is spent: the buffer takes the tile's keys, then their running sums per column
         for (int e = tid; e < kTB * D; e += kThreads) {
             const int r = e / D, c = e % D;
             Kc[r * P + c] = r < cnt ? to_f(k[(size_t)(tb + r) * D + c]) : 0.f;
@@ -505,8 +504,8 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     if (stored && tid < kTB) {
         const int t = tid;
         const float *tw = a.tok + ((size_t)bh * a.L + tb + t) * kBwdTokWords;
-        m_t[t] = t < cnt ? tw[0] : 0.f;
-        z_t[t] = t < cnt ? tw[1] : 1.f;
+        m_t[t] = 0.f;  // (the softmax data are not kept on this path)
+        z_t[t] = 1.f;
         gon[t] = t < cnt ? tw[2] : 0.f;
         chosen[t] = ~0ull;
     } else if (tid < kTB) {
@@ -551,17 +550,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             else if ((chosen[t] >> i) & 1ull) g = expf(gt[t * kTab + i] - m_t[t]) / z_t[t];
         }
         gt[t * kTab + i] = g;
-        if (!finish && a.gam && t < cnt) a.gam[seg_base + (size_t)i * a.L + t] = g;  // the gates pass
-        if (finish) dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
-    }
-    if (!finish) {  // the softmax data and the online gate, for the tensor-core pass and the finishing pass
-        if (tid < cnt) {
-            float *tw = a.tok + ((size_t)bh * a.L + tb + tid) * kBwdTokWords;
-            tw[0] = m_t[tid];
-            tw[1] = z_t[tid];
-            tw[2] = gon[tid];
-        }
-        return;
+        dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
     }
 
     // the online memory's dg: from the tensor cores, or dy_t . O_on[t] over the token's 16 lanes
@@ -1019,7 +1008,7 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     auto kern = bwd_route_simt<T, D>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    if (!a.gates_only && a.kpre_tiles) {
+    if (a.kpre_tiles) {
         bwd_kpre_simt<T, D><<<(unsigned)((long long)p.BH * p.N), D, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_kpre_simt");
@@ -1028,7 +1017,7 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_after_kernel(s, "bwd_route_simt");
-    if (!a.gates_only && a.dr && p.N > 1) {
+    if (a.dr && p.N > 1) {
         const int chunks = (p.L + kDkChunk - 1) / kDkChunk;
         bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * chunks), kThreads, 0, s>>>(a, chunks);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1055,7 +1044,6 @@ cudaError_t backward_tc_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 
 cudaError_t launch_bwd_kernels(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(backward_impl, p, a, s); }
 cudaError_t launch_bwd_tc_rest(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(backward_tc_impl, p, a, s); }
-cudaError_t launch_bwd_route(const Problem &p, const BwdArgs &a, cudaStream_t s) { MC_BWD_DISPATCH(route_impl, p, a, s); }
 
 size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -1118,10 +1106,10 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
     profile_call_start(s);
 
     if (tc) {
-        // Tensor-core path: the forward's state kernel (state and prefix-state images, r_on),
-        // the key means, the gates (routed), every memory's read on the tensor cores (dg, the
-        // online dg, dq), the gate work on whole tables, the key-mean gradient, G on the tensor
-        // cores and the reverse scan.
+        // Tensor-core path: the forward's state kernel (state, prefix-state and key-mean images,
+        // r_on), the key means, the gates (routed, tensor cores), every memory's read on the tensor
+        // cores (dg, the online dg, dq), the gate work on whole tables, the key-mean gradient, G
+        // and dk / dv on the tensor cores.
         float *gam = gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
         a.kpre_tiles = gated ? reinterpret_cast<float *>(take(4 * BH * N * ((p.C + kTB - 1) / kTB) * d)) : nullptr;
         void *state_scratch = take(tc_state_scratch_bytes(p));
@@ -1136,10 +1124,9 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         if ((e = cudaMemsetAsync(dkbar, 0, 4 * BH * N * d, s)) != cudaSuccess) return e;
         a.r_on = img.r_on;
         a.gam = gam;
-        if (gated) {
-            BwdArgs ga = a;
-            ga.gates_only = 1;
-            if ((e = launch_bwd_route(p, ga, s)) != cudaSuccess) return e;
+        if (gated) {  // the gates on the tensor cores, from the state kernel's key-mean images and r_on
+            if ((e = launch_bwd_gates_tc(p, u, img, gam, tok, s)) != cudaSuccess) return e;
+            profile_after_kernel(s, "gate_tiles_tc");
         }
         float *dg = nullptr, *dgon = nullptr, *dqf = nullptr;
         if ((e = launch_bwd_cached_tc(p, q, k, v, dy, img, gam, tok, cached_scratch, &dg, &dgon, &dqf, s)) != cudaSuccess)

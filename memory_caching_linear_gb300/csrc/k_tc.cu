@@ -36,8 +36,8 @@
 //   a linear memory, [MC-sum §3.3]); SSC keeps the topk largest cached scores
 //   ([MC-sum §3.4]) and gives the others gate 0.
 //
-// ssc_router_tc -- the SSC router alone (the selected segments of every token),
-//   from the same scores.
+// gate_tiles_tc -- the same scores per 128-token chunk, for the SSC router alone (the
+//   selected segments of every token) and for the gates of the backward pass.
 #include <cstdint>
 
 #include "mc_internal.cuh"
@@ -68,6 +68,8 @@ struct TcArgs {
     uint8_t *kbar_img;    // [BH] x 32 KB: hi rows (16 KB) then lo rows (16 KB), row = segment
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
+    float *gam_out;       // backward gates: [BH][N][L] g_{t,i}, or null
+    float *tok_out;       // backward gates: [BH][L][kBwdTokWords], word 2 = the online gate
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
     int mean;             // Mean aggregation: the Residual path with every weight 1 / (n + 1)
@@ -585,9 +587,9 @@ __device__ __forceinline__ float token_gates(float (&sc)[64], int n, float ron, 
 }
 
 // ============================================================================
-// ssc_router_tc -- the SSC router ([MC-sum §3.4]): for every token the topk
+// gate_tiles_tc -- the SSC router ([MC-sum §3.4]): for every token the topk
 // cached segments with the largest scores r_{t,i} = <u_t, kbar_i> (i < n), in rank
-// order, equal scores to the lower index, -1 padded.  One CTA per 128-token chunk;
+// order, equal scores to the lower index, -1 padded; or the backward's gates.  Per 128-token chunk;
 // the scores come from two MMAs (kbar as hi + lo bf16 rows, so the score carries
 // ~16 bits of kbar; u is exact in bf16).
 // ============================================================================
@@ -596,7 +598,11 @@ constexpr size_t kRouterSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
 
 // Persistent: CTA b handles the contiguous tile range [b*per, (b+1)*per) of the
 // (bh, chunk) tiles, so consecutive tiles share a head and its kbar image.
-__global__ void __launch_bounds__(kRouterThreads, 2) ssc_router_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
+// MODE 0: the SSC router (sel_out).  MODE 1 / 2: the gates of the backward pass --
+// GRM / Soup softmax, or SSC -- with the online score r_on, written as g_{t,i}
+// ([N][L] per head, 0 where not taken) and the online gate.
+template <int MODE>
+__global__ void __launch_bounds__(kRouterThreads, 2) gate_tiles_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -707,7 +713,14 @@ __global__ void __launch_bounds__(kRouterThreads, 2) ssc_router_tc(const __grid_
             tc_fence_before();
             mbar_arrive(&s_empty[b]);
             const size_t tok = (size_t)bh * a.L + t0 + row;
-            token_gates<true>(sc, n, 0.f, a.topk, a.sel_out + tok * a.topk);
+            if (MODE == 0) {
+                token_gates<true>(sc, n, 0.f, a.topk, a.sel_out + tok * a.topk);
+            } else {
+                const float inv = token_gates<MODE == 2>(sc, n, a.r_on[tok], a.topk, nullptr);
+                float *g = a.gam_out + (size_t)bh * a.N * a.L + t0 + row;
+                for (int k = 0; k < n; ++k) g[(size_t)k * a.L] = sc[k] * inv;
+                a.tok_out[tok * kBwdTokWords + 2] = sc[63] * inv;
+            }
         }
     }
     tc_fence_before();
@@ -1303,11 +1316,11 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
     if (e != cudaSuccess) return e;
     kbar_images_tc<<<(unsigned)(p.BH * p.N), kD, 0, s>>>(static_cast<const __nv_bfloat16 *>(fa.k), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(ssc_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
+    e = cudaFuncSetAttribute(gate_tiles_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
     if (e != cudaSuccess) return e;
     const int gtiles = p.BH * (p.L / kCT);
     const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
-    ssc_router_tc<<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
+    gate_tiles_tc<0><<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
     return cudaGetLastError();
 }
 
@@ -1363,8 +1376,30 @@ cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, 
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     out->states_img = a.states_img;
     out->spre_img = a.spre_img;
+    out->kbar_img = a.kbar_img;
     out->r_on = a.r_on;
     return cudaSuccess;
+}
+
+// The backward's gates from the state kernel's key-mean images and r_on (routed modes).
+cudaError_t launch_bwd_gates_tc(const Problem &p, const void *u, const TcImages &img, float *gam, float *tok, cudaStream_t s)
+{
+    TcArgs a{};
+    a.kbar_img = const_cast<uint8_t *>(img.kbar_img);
+    a.r_on = const_cast<float *>(img.r_on);
+    a.gam_out = gam;
+    a.tok_out = tok;
+    a.topk = p.topk;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kCT; a.d = p.d;
+    CUtensorMap mU;
+    if (!make_tmap_bf16_sw128(&mU, u, (unsigned long long)p.BH * p.L, p.d, 128)) return cudaErrorInvalidValue;
+    auto k = p.mode == MC_SSC ? gate_tiles_tc<2> : gate_tiles_tc<1>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
+    if (e != cudaSuccess) return e;
+    const int gtiles = p.BH * (p.L / kCT);
+    const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
+    k<<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)

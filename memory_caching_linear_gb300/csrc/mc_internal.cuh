@@ -121,11 +121,14 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scrat
 // states [BH][N] and of the chunks' prefix states [BH][N][C/128] (32 KB each, 128x128
 // bf16, two 64-column 128-byte-swizzled panels, row = value dim), and r_on [BH][L].
 struct TcImages {
-    const uint8_t *states_img, *spre_img;
+    const uint8_t *states_img, *spre_img, *kbar_img;
     const float *r_on;
 };
 size_t tc_state_scratch_bytes(const Problem &p);
 cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, TcImages *out, cudaStream_t s);
+// The backward's gates on the tensor cores (routed modes): g_{t,i} to gam [BH][N][L] and the
+// online gate to word 2 of tok [BH][L][kBwdTokWords].
+cudaError_t launch_bwd_gates_tc(const Problem &p, const void *u, const TcImages &img, float *gam, float *tok, cudaStream_t s);
 // Reads and clears the device-side record of an abandoned bounded wait.
 cudaError_t take_device_abort(int *was_set);
 
@@ -158,7 +161,6 @@ struct BwdArgs {
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
     float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
-    int gates_only;       // 1: only the gates (gam, the SSC selection), nothing else
     int BH, L, C, N, mode, topk;
 };
 size_t backward_scratch_bytes(const Problem &p);
