@@ -31,6 +31,8 @@
 // the tensor cores (k_bwd_tc.cu: dg and the cached dq, and G), and the gate work on
 // whole shared-memory tables: bwd_route_simt (before the cached pass: the gates;
 // after it: delta, dr, du, dq) and bwd_dkbar_simt (the key-mean gradient from dr).
+#include <type_traits>
+
 #include "mc_internal.cuh"
 
 namespace mc {
@@ -413,28 +415,63 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
 
 // ---------------------------------------------------------------------------
 // bwd_route_simt: the gate work of the tensor-core backward, one CTA per (bh,
-// segment n, tile of kTB tokens), on whole tables in shared memory (n <= 63):
-//   the gates g_{t,i} -- read from gam (routed aggregations, written by the
-//   tensor-core gates pass) or, without it, scores r_{t,i} = <u_t, kbar_i> and GRM /
-//   Soup softmax with the online score, SSC over the topk largest (equal scores to
-//   the lower index); Residual 1; Mean 1 / (n + 1).  With dg_{t,i} from the tensor cores:
+// segment n, tile of kTB tokens), heavy segments first.  It reads the gates g_{t,i}
+// (routed aggregations: the tensor-core gates pass wrote them with the online gate in
+// token word 2; Residual 1; Mean 1 / (n + 1)) and, from the tensor cores, dg_{t,i},
+// dg_on and dq, and computes per token
 //   delta_t = sum_i g dg + g_on dg_on,  dr_{t,i} = g (dg - delta) -> dr,
-//   du_t = sum_i dr_{t,i} kbar_i + dr_on p_t,  dq_t = (cached part) + g_on M_t^T dy_t.
+//   du_t = sum_i dr_{t,i} kbar_i + dr_on p_t   (p_t = mean of the segment's keys up to t),
+//   dq_t in the output type, and token words 2-4 (online gate, delta, w = dr_on / cnt_t).
+// The gate and dr tables sit in shared memory as [i][t]; for du a warp owns kTB / 8
+// tokens and a lane D / 32 dimensions (a register tile over every cached segment).
 // ---------------------------------------------------------------------------
+template <int CPL, typename T>
+__device__ __forceinline__ void load_cols(const T *p, float (&x)[CPL])
+{
+    if constexpr (std::is_same<T, float>::value && CPL == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else if constexpr (std::is_same<T, __nv_bfloat16>::value && CPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) x[c] = to_f(p[c]);
+    }
+}
+
+template <int CPL, typename T>
+__device__ __forceinline__ void store_cols(T *p, const float (&x)[CPL])
+{
+    if constexpr (std::is_same<T, float>::value && CPL == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    } else if constexpr (std::is_same<T, __nv_bfloat16>::value && CPL == 4) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 v;
+        v.x = *reinterpret_cast<const uint32_t *>(&a);
+        v.y = *reinterpret_cast<const uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = v;
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) p[c] = from_f<T>(x[c]);
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
 {
-    constexpr int P = D + 1;
-    constexpr int RB = D / 16;
-    constexpr int TPT = kTB / 16;
-    extern __shared__ float sm[];
-    float *Us = sm;              // kTB x P: u for the scores, then the running key sums of the tile
-    float *Kc = Us;
-    float *gt = Us + kTB * P;    // kTB x kTab: scores, then gates
-    float *dt = gt + kTB * kTab; // kTB x kTab: dg, then dr
-    float *kpre = dt + kTB * kTab;  // D
-    float *m_t = kpre + D, *z_t = m_t + kTB, *gon = z_t + kTB, *dl = gon + kTB, *dgo = dl + kTB;
-    uint64_t *chosen = reinterpret_cast<uint64_t *>(dgo + kTB);  // SSC: the selected cached segments of a token
+    constexpr int CPL = D >= 32 ? D / 32 : 1;  // dimensions per lane
+    constexpr int NW = kThreads / 32;
+    constexpr int TPW = kTB / NW;              // tokens per warp
+    constexpr int PARTS = kThreads / kTB;      // threads per token in the delta sum
+    static_assert(TPW == 8 && PARTS * kTB == kThreads, "tile shape");
+    __shared__ __align__(16) float gt[kTab * kTB];  // [i][t]: gates
+    __shared__ __align__(16) float dt[kTab * kTB];  // [i][t]: dg, then dr
+    __shared__ float tot[NW][D];                    // each warp's key sums over its tokens
+    __shared__ float red[PARTS][kTB];
+    __shared__ float gon[kTB], dgo[kTB], dl[kTB];
 
     const int tps = (a.C + kTB - 1) / kTB;
     const int per_seg = a.BH * tps;
@@ -446,180 +483,130 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
     const int te = min(min(tb + kTB, t0 + a.C), a.L);
     if (tb >= te) return;
     const int cnt = te - tb;
-    const int mode = a.mode;
-    const bool gated = gated_mode(mode);
-    const bool stored = gated && a.gam;  // the gates pass ran: gam and the online gate are in memory
+    const bool gated = gated_mode(a.mode);
+    const float gconst = const_gate(a.mode, n);
     const size_t base = (size_t)bh * a.L * D;
-    const T *k = static_cast<const T *>(a.k) + base, *dy = static_cast<const T *>(a.dy) + base;
-    const T *u = gated ? static_cast<const T *>(a.u) + base : nullptr;
-    const float *kbar = a.kbar + (size_t)bh * a.N * D;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     const size_t seg_base = (size_t)bh * a.N * a.L + tb;  // [N][L] tables of this head, at the tile
+    const size_t tok0 = (size_t)bh * a.L + tb;            // the tile's first token within the [BH][L] tables
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c0 = CPL * lane;
+    const bool lane_on = c0 < D;
+    const int tw = warp * TPW;  // the warp's first token of the tile
 
-    if (!stored)
-        for (int e = tid; e < kTB * D; e += kThreads) {
-            const int r = e / D, c = e % D;
-            Us[r * P + c] = (r < cnt && gated) ? to_f(u[(size_t)(tb + r) * D + c]) : 0.f;
-        }
-    const bool need_kpre = gated && !a.kpre_tiles;
-    if (gated && tid < D)
-        kpre[tid] = a.kpre_tiles ? a.kpre_tiles[(((size_t)bh * a.N + n) * tps + tile) * D + tid] : 0.f;
-    __syncthreads();
-    if (need_kpre) {  // keys of the segment before the tile: a strided share per thread, four loads in flight
-        constexpr int parts = kThreads / D;
-        const int col = tid % D, part = tid / D;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int j = t0 + part;
-        for (; j + 3 * parts < tb; j += 4 * parts) {
-            s0 += to_f(k[(size_t)j * D + col]);
-            s1 += to_f(k[(size_t)(j + parts) * D + col]);
-            s2 += to_f(k[(size_t)(j + 2 * parts) * D + col]);
-            s3 += to_f(k[(size_t)(j + 3 * parts) * D + col]);
-        }
-        for (; j < tb; j += parts) s0 += to_f(k[(size_t)j * D + col]);
-        atomicAdd(&kpre[col], (s0 + s1) + (s2 + s3));
-    }
-    if (gated && !stored)  // scores: a warp takes 32 tokens of one segment (its kbar row broadcast)
-        for (int e = tid; e < kTB * n; e += kThreads) {
-            const int i = e / kTB, t = e % kTB;
-            gt[t * kTab + i] = t < cnt ? gate_score(Us + t * P, kbar + (size_t)i * D, D) : 0.f;
-        }
-    __syncthreads();
-    if (gated) {  // u is spent: the buffer takes the tile's keys, then their running sums per column
-        for (int e = tid; e < kTB * D; e += kThreads) {
-            const int r = e / D, c = e % D;
-            Kc[r * P + c] = r < cnt ? to_f(k[(size_t)(tb + r) * D + c]) : 0.f;
-        }
-        __syncthreads();
-        if (tid < D) {
-            float s = 0.f;
-            for (int r = 0; r < cnt; ++r) {
-                s += Kc[r * P + tid];
-                Kc[r * P + tid] = s;
-            }
-        }
-    }
-
-    // per token: softmax max and sum (with the online score), the SSC selection, the online gate
-    if (stored && tid < kTB) {
-        const int t = tid;
-        const float *tw = a.tok + ((size_t)bh * a.L + tb + t) * kBwdTokWords;
-        m_t[t] = 0.f;  // (the softmax data are not kept on this path)
-        z_t[t] = 1.f;
-        gon[t] = t < cnt ? tw[2] : 0.f;
-        chosen[t] = ~0ull;
-    } else if (tid < kTB) {
-        const int t = tid;
-        float go = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f, m = 0.f, z = 1.f;
-        uint64_t take = n >= 64 ? ~0ull : ((1ull << n) - 1);
-        if (t < cnt && gated) {
-            const float ron = a.r_on[(size_t)bh * a.L + tb + t];
-            const float *sr = gt + t * kTab;
-            if (mode == MC_SSC) {
-                uint64_t pick = 0;
-                const int kk = min(a.topk, n);
-                for (int r = 0; r < kk; ++r) {  // the largest unpicked score, the lower index on ties
-                    int bi = -1;
-                    for (int i = 0; i < n; ++i)
-                        if (!((pick >> i) & 1ull) && (bi < 0 || sr[i] > sr[bi])) bi = i;
-                    pick |= 1ull << bi;
-                }
-                take = pick;
-            }
-            m = ron;
-            for (int i = 0; i < n; ++i)
-                if ((take >> i) & 1ull) m = fmaxf(m, sr[i]);
-            z = expf(ron - m);
-            for (int i = 0; i < n; ++i)
-                if ((take >> i) & 1ull) z += expf(sr[i] - m);
-            go = expf(ron - m) / z;
-        }
-        m_t[t] = m;
-        z_t[t] = z;
-        gon[t] = t < cnt ? go : 0.f;
-        chosen[t] = take;
-    }
-    __syncthreads();
-    // gates in place of the scores
     for (int e = tid; e < kTB * n; e += kThreads) {
         const int i = e / kTB, t = e % kTB;
-        float g = 0.f;
-        if (t < cnt) {
-            if (!gated) g = mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
-            else if (stored) g = a.gam[seg_base + (size_t)i * a.L + t];
-            else if ((chosen[t] >> i) & 1ull) g = expf(gt[t * kTab + i] - m_t[t]) / z_t[t];
-        }
-        gt[t * kTab + i] = g;
-        dt[t * kTab + i] = t < cnt ? a.dg_in[seg_base + (size_t)i * a.L + t] : 0.f;
+        const size_t gi = seg_base + (size_t)i * a.L + t;
+        gt[e] = t < cnt ? (gated ? a.gam[gi] : gconst) : 0.f;
+        dt[e] = t < cnt ? a.dg_in[gi] : 0.f;
     }
-
-    // the online memory's dg: from the tensor cores, or dy_t . O_on[t] over the token's 16 lanes
-    if (a.dgon_in) {
-        if (tid < cnt) dgo[tid] = a.dgon_in[(size_t)bh * a.L + tb + tid];
-    } else {
-    const float *Oon = a.O_on + base;
-#pragma unroll
-    for (int p = 0; p < TPT; ++p) {
-        const int t = ty + 16 * p;
-        float part = 0.f;
-        if (t < cnt) {
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                const size_t gi = (size_t)(tb + t) * D + tx + 16 * r;
-                part = fmaf(to_f(dy[gi]), Oon[gi], part);
-            }
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (tx == 0) dgo[t] = part;
+    if (tid < kTB) {
+        const int t = tid;
+        gon[t] = t < cnt ? (gated ? a.tok[(tok0 + t) * kBwdTokWords + 2] : gconst) : 0.f;
+        dgo[t] = t < cnt ? a.dgon_in[tok0 + t] : 0.f;
     }
+    // the keys of the warp's tokens, running sums in registers (the pooled key of the online memory)
+    float run[TPW][CPL];
+    if (gated) {
+        const T *k = static_cast<const T *>(a.k) + base;
+        float s[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) s[c] = 0.f;
+#pragma unroll
+        for (int j = 0; j < TPW; ++j) {
+            float x[CPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) x[c] = 0.f;
+            if (lane_on && tw + j < cnt) load_cols<CPL>(k + (size_t)(tb + tw + j) * D + c0, x);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) run[j][c] = (s[c] += x[c]);
+        }
+        if (lane_on)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) tot[warp][c0 + c] = s[c];
     }
     __syncthreads();
-    if (tid < kTB) {  // delta_t = sum_i g dg + g_on dg_on
+    {  // delta_t: kTB tokens x PARTS strided shares of the segments
+        const int t = tid % kTB, part = tid / kTB;
+        float s = 0.f;
+        for (int i = part; i < n; i += PARTS) s = fmaf(gt[i * kTB + t], dt[i * kTB + t], s);
+        red[part][t] = s;
+    }
+    __syncthreads();
+    if (tid < kTB) {
         const int t = tid;
         float s = gon[t] * dgo[t];
-        for (int i = 0; i < n; ++i) s = fmaf(gt[t * kTab + i], dt[t * kTab + i], s);
+#pragma unroll
+        for (int part = 0; part < PARTS; ++part) s += red[part][t];
         dl[t] = s;
     }
     __syncthreads();
     // dr = g (dg - delta), in place, and out for the key-mean gradient
     for (int e = tid; e < kTB * n; e += kThreads) {
-        const int i = e / kTB, t = e % kTB;
-        const float dr = gt[t * kTab + i] * (dt[t * kTab + i] - dl[t]);
-        dt[t * kTab + i] = dr;
-        if (t < cnt && gated) a.dr[seg_base + (size_t)i * a.L + t] = dr;
+        const int t = e % kTB;
+        const float dr = gt[e] * (dt[e] - dl[t]);
+        dt[e] = dr;
+        if (gated && t < cnt) a.dr[seg_base + (size_t)(e / kTB) * a.L + t] = dr;
     }
     __syncthreads();
 
-    T *dqo = static_cast<T *>(a.dq) + base;
-    T *duo = gated ? static_cast<T *>(a.du) + base : nullptr;
-    float *tok = a.tok + ((size_t)bh * a.L + tb) * kBwdTokWords;
+    if (lane_on) {
+        T *dqo = static_cast<T *>(a.dq) + base;
 #pragma unroll
-    for (int p = 0; p < TPT; ++p) {
-        const int t = ty + 16 * p;
-        if (t >= cnt) continue;
-        const float dron = gon[t] * (dgo[t] - dl[t]);  // dr of the online memory
-        const float inv_cnt = 1.f / (float)(tb + t - t0 + 1);
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            const int c = tx + 16 * r;
-            const size_t gi = (size_t)(tb + t) * D + c;
-            const float dqv = a.dq_in[((size_t)bh * a.L + tb + t) * D + c];  // all of dq when X_on is null
-            dqo[gi] = from_f<T>(a.X_on ? dqv + gon[t] * a.X_on[base + gi] : dqv);
-            if (gated) {
-                float du = dron * (kpre[c] + Kc[t * P + c]) * inv_cnt;
-                for (int i = 0; i < n; ++i) du = fmaf(dt[t * kTab + i], __ldg(kbar + (size_t)i * D + c), du);
-                duo[gi] = from_f<T>(du);
+        for (int j = 0; j < TPW; ++j) {
+            const int t = tw + j;
+            if (t < cnt) {
+                float x[CPL];
+                load_cols<CPL>(a.dq_in + (tok0 + t) * D + c0, x);
+                store_cols<CPL>(dqo + (size_t)(tb + t) * D + c0, x);
             }
         }
-        if (tx == 0) {
-            float *w = tok + (size_t)t * kBwdTokWords;
-            w[0] = m_t[t];
-            w[1] = z_t[t];
-            w[2] = gon[t];
-            w[3] = dl[t];
-            w[4] = gated ? dron * inv_cnt : 0.f;
+    }
+    if (gated && lane_on) {
+        float acc[TPW][CPL];
+#pragma unroll
+        for (int j = 0; j < TPW; ++j)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[j][c] = 0.f;
+        const float *kb = a.kbar + (size_t)bh * a.N * D + c0;
+        for (int i = 0; i < n; ++i) {
+            float kv[CPL];
+            load_cols<CPL>(kb + (size_t)i * D, kv);
+            const float4 r0 = *reinterpret_cast<const float4 *>(dt + i * kTB + tw);
+            const float4 r1 = *reinterpret_cast<const float4 *>(dt + i * kTB + tw + 4);
+            const float dr[TPW] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int j = 0; j < TPW; ++j)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[j][c] = fmaf(dr[j], kv[c], acc[j][c]);
         }
+        // the keys of the segment before the warp's tokens
+        float off[CPL];
+        load_cols<CPL>(a.kpre_tiles + (((size_t)bh * a.N + n) * tps + tile) * D + c0, off);
+        for (int w = 0; w < warp; ++w)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) off[c] += tot[w][c0 + c];
+        T *duo = static_cast<T *>(a.du) + base;
+#pragma unroll
+        for (int j = 0; j < TPW; ++j) {
+            const int t = tw + j;
+            if (t < cnt) {
+                const float dron = gon[t] * (dgo[t] - dl[t]);
+                const float inv_cnt = 1.f / (float)(tb + t - t0 + 1);
+                float x[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) x[c] = fmaf(dron * (off[c] + run[j][c]), inv_cnt, acc[j][c]);
+                store_cols<CPL>(duo + (size_t)(tb + t) * D + c0, x);
+            }
+        }
+    }
+    if (tid < cnt) {
+        const int t = tid;
+        float *w = a.tok + (tok0 + t) * kBwdTokWords;
+        w[0] = 0.f;  // (the softmax data are not kept on this path)
+        w[1] = 1.f;
+        w[2] = gon[t];
+        w[3] = dl[t];
+        w[4] = gated ? gon[t] * (dgo[t] - dl[t]) / (float)(tb + t - t0 + 1) : 0.f;
     }
 }
 
@@ -668,11 +655,13 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks)
 {
     constexpr int parts = kThreads / D;
-    __shared__ float sdr[kTab][kDkSub];
+    constexpr int TG = 4;  // tokens per step: one 16-byte row of dr per segment
+    __shared__ __align__(16) float sdr[kTab][kDkSub];
     const int ch = (int)blockIdx.x % chunks, bh = (int)blockIdx.x / chunks;
     const int t_lo = ch * kDkChunk, t_hi = min(t_lo + kDkChunk, a.L);
     const int col = threadIdx.x % D, part = threadIdx.x / D;
     const int nmax = min(a.N - 1, (t_hi - 1) / a.C);  // cached segments any token of the chunk scored
+    const int nstage = min(kTab, (nmax + 7) & ~7);    // rows staged: whole blocks of 8 segments
     const T *u = static_cast<const T *>(a.u) + (size_t)bh * a.L * D + col;
     const float *dr = a.dr + (size_t)bh * a.N * a.L;
     float acc[kTab];
@@ -681,17 +670,27 @@ __global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks
     for (int t0 = t_lo; t0 < t_hi; t0 += kDkSub) {
         const int cnt = min(kDkSub, t_hi - t0);
         __syncthreads();
-        for (int e = threadIdx.x; e < nmax * kDkSub; e += kThreads) {
+        for (int e = threadIdx.x; e < nstage * kDkSub; e += kThreads) {
             const int i = e / kDkSub, t = e % kDkSub;
             sdr[i][t] = t < cnt && i < (t0 + t) / a.C ? dr[(size_t)i * a.L + t0 + t] : 0.f;
         }
         __syncthreads();
-        for (int t = part; t < cnt; t += parts) {
-            const float uv = to_f(u[(size_t)(t0 + t) * D]);
-            const int n_t = min((t0 + t) / a.C, kTab);
+        for (int t = part * TG; t < cnt; t += parts * TG) {
+            float uv[TG];
 #pragma unroll
-            for (int i = 0; i < kTab; ++i)
-                if (i < n_t) acc[i] = fmaf(sdr[i][t], uv, acc[i]);
+            for (int j = 0; j < TG; ++j) uv[j] = t + j < cnt ? to_f(u[(size_t)(t0 + t + j) * D]) : 0.f;
+            // segments the group's last token scored (the others' rows are zero there)
+            const int n_t = min((t0 + min(t + TG, cnt) - 1) / a.C, kTab);
+#pragma unroll
+            for (int ib = 0; ib < kTab / 8; ++ib) {
+                if (8 * ib >= n_t) break;
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) {
+                    const int i = 8 * ib + ii;
+                    const float4 r = *reinterpret_cast<const float4 *>(&sdr[i][t]);
+                    acc[i] = fmaf(r.x, uv[0], fmaf(r.y, uv[1], fmaf(r.z, uv[2], fmaf(r.w, uv[3], acc[i]))));
+                }
+            }
         }
     }
     float *dk = a.dkbar + (size_t)bh * a.N * D + col;
@@ -1003,18 +1002,14 @@ cudaError_t backward_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 template <typename T, int D>
 cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 {
-    constexpr int P = D + 1;
-    const size_t smem = sizeof(float) * (kTB * P + 2 * kTB * kTab + D + 5 * kTB) + sizeof(uint64_t) * kTB;
-    auto kern = bwd_route_simt<T, D>;
-    cudaError_t e = set_smem(kern, smem);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     if (a.kpre_tiles) {
         bwd_kpre_simt<T, D><<<(unsigned)((long long)p.BH * p.N), D, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_kpre_simt");
     }
     const long long tps = (p.C + kTB - 1) / kTB;
-    kern<<<(unsigned)((long long)p.BH * p.N * tps), kThreads, smem, s>>>(a);
+    bwd_route_simt<T, D><<<(unsigned)((long long)p.BH * p.N * tps), kThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_after_kernel(s, "bwd_route_simt");
     if (a.dr && p.N > 1) {

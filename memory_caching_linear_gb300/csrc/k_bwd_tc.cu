@@ -34,9 +34,14 @@ using namespace sm100;
 
 constexpr int kGT = 128;             // tokens per tile
 constexpr uint32_t kGTile = 32768;   // one 128 x 128 bf16 operand tile (two 16 KB panels)
-constexpr int kGStages = 2;          // tile stages in flight: dy (scaled in place for the first state), q, g o dy for the second
-constexpr int kGThreads = 192;       // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
-constexpr uint32_t kGStage = 3 * kGTile + 1024;  // + the tile's gates of both segments (2 x 128 floats)
+// The G kernel streams 64-token tiles (two 8 KB panels per operand) so that four
+// tile stages fit in shared memory: dy (scaled in place for the first segment), q,
+// g o dy for the second segment, and both segments' gates.
+constexpr int kG2 = 64;                    // tokens per G tile
+constexpr uint32_t kG2Tile = 16384;        // one 64 x 128 bf16 operand tile (two 8 KB panels)
+constexpr int kGStages = 4;
+constexpr int kGThreads = 192;             // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
+constexpr uint32_t kGStage = 3 * kG2Tile + 1024;
 constexpr size_t kGSmem = kGStages * kGStage + 1024;
 
 struct GArgs {
@@ -72,8 +77,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int i0 = 2 * pr, i1 = 2 * pr + 1;
     const bool two = i1 < a.N - 1;  // segment N-1 has no later tokens
     const int t_begin = (i0 + 1) * a.C;
-    const int ntiles = (a.L - t_begin) / kGT;
-    const int split = a.C / kGT;  // tiles of segment i1: the second state starts after them
+    const int ntiles = (a.L - t_begin) / kG2;
+    const int split = a.C / kG2;  // tiles of segment i1: the second state starts after them
     const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
 
     if (warp == 0) {
@@ -105,16 +110,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int s = j % kGStages;
                 if (!mbar_wait(&empty[s], ((j / kGStages) & 1) ^ 1, &abort_flag)) break;
                 uint8_t *st = sm + s * kGStage;
-                const int row = bh * a.L + t_begin + j * kGT;
+                const int row = bh * a.L + t_begin + j * kG2;
                 const bool g0 = routed, g1 = routed && two && j >= split;  // gates to bring along
-                mbar_arrive_expect_tx(&full[s], 2 * kGTile + (g0 ? 512 : 0) + (g1 ? 512 : 0));
+                mbar_arrive_expect_tx(&full[s], 2 * kG2Tile + (g0 ? 256 : 0) + (g1 ? 256 : 0));
                 tma_load_2d(st, &mY, 0, row, &full[s]);
-                tma_load_2d(st + 16384, &mY, 64, row, &full[s]);
-                tma_load_2d(st + kGTile, &mQ, 0, row, &full[s]);
-                tma_load_2d(st + kGTile + 16384, &mQ, 64, row, &full[s]);
-                const size_t goff = (size_t)t_begin + (size_t)j * kGT;
-                if (g0) bulk_load(st + 3 * kGTile, a.gam + ((size_t)bh * a.N + i0) * a.L + goff, 512, &full[s]);
-                if (g1) bulk_load(st + 3 * kGTile + 512, a.gam + ((size_t)bh * a.N + i1) * a.L + goff, 512, &full[s]);
+                tma_load_2d(st + kG2Tile / 2, &mY, 64, row, &full[s]);
+                tma_load_2d(st + kG2Tile, &mQ, 0, row, &full[s]);
+                tma_load_2d(st + kG2Tile + kG2Tile / 2, &mQ, 64, row, &full[s]);
+                const size_t goff = (size_t)t_begin + (size_t)j * kG2;
+                if (g0) bulk_load(st + 3 * kG2Tile, a.gam + ((size_t)bh * a.N + i0) * a.L + goff, 256, &full[s]);
+                if (g1) bulk_load(st + 3 * kG2Tile + 512, a.gam + ((size_t)bh * a.N + i1) * a.L + goff, 256, &full[s]);
                 issued = j + 1;
             }
             // leave no copy in flight
@@ -131,14 +136,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int s = j % kGStages;
                 if (!(ok = mbar_wait(&scaled[s], (j / kGStages) & 1, &abort_flag))) break;
                 tc_fence_after();
-                const uint32_t y0 = smem_u32(sm + s * kGStage), q0 = y0 + kGTile, y1 = y0 + 2 * kGTile;
+                const uint32_t y0 = smem_u32(sm + s * kGStage), q0 = y0 + kG2Tile, y1 = y0 + 2 * kG2Tile;
                 const bool second = two && j >= split;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {  // 16 tokens per step: 16 rows of 128 bytes
-                    const uint64_t bq = make_desc_sw128(q0 + kk * 2048u, 16384, 1024);
-                    mma_ss(tD, make_desc_sw128(y0 + kk * 2048u, 16384, 1024), bq, idG, (j | kk) != 0);
+                for (int kk = 0; kk < 4; ++kk) {  // 16 tokens per step: 16 rows of 128 bytes; the 64-column halves 8 KB apart
+                    const uint64_t bq = make_desc_sw128(q0 + kk * 2048u, kG2Tile / 2, 1024);
+                    mma_ss(tD, make_desc_sw128(y0 + kk * 2048u, kG2Tile / 2, 1024), bq, idG, (j | kk) != 0);
                     if (second)
-                        mma_ss(tD + 128, make_desc_sw128(y1 + kk * 2048u, 16384, 1024), bq, idG, (j > split) || kk != 0);
+                        mma_ss(tD + 128, make_desc_sw128(y1 + kk * 2048u, kG2Tile / 2, 1024), bq, idG,
+                               (j > split) || kk != 0);
                 }
                 mma_commit(&empty[s]);
             }
@@ -146,37 +152,39 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mma_commit(&done);
         }
     } else {
-        // ---------------------------------------------------------- workers: token row r of each tile
+        // ---------------------------------------------------------- workers: a thread scales one panel row
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
+        const int trow = r & 63, h = r >> 6;  // token row of the tile, 64-column panel
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kGStages;
             const bool second = two && j >= split;
             if (!mbar_wait(&full[s], (j / kGStages) & 1, &abort_flag)) break;
             // the gates came with the tile (routed); Residual 1, Mean 1 / (n(t) + 1)
-            const float *gsm = reinterpret_cast<const float *>(sm + s * kGStage + 3 * kGTile);
-            const float gc = a.mode == MC_MEAN ? 1.f / (float)((t_begin + j * kGT) / a.C + 1) : 1.f;
-            const float g0 = routed ? gsm[r] : gc;
-            const float g1 = routed ? (second ? gsm[128 + r] : 0.f) : gc;
+            const float *gsm = reinterpret_cast<const float *>(sm + s * kGStage + 3 * kG2Tile);
+            const float gc = a.mode == MC_MEAN ? 1.f / (float)((t_begin + j * kG2) / a.C + 1) : 1.f;
+            const float g0 = routed ? gsm[trow] : gc;
+            const float g1 = routed ? (second ? gsm[128 + trow] : 0.f) : gc;
             const __nv_bfloat162 g02 = __float2bfloat162_rn(g0), g12 = __float2bfloat162_rn(g1);
-            uint8_t *row = sm + s * kGStage + r * 128;  // the row's 128 bytes in each panel (order within is swizzled)
+            uint8_t *rowp = sm + s * kGStage + h * (kG2Tile / 2) + trow * 128;  // the row's 128 bytes of one panel
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int c = 0; c < 8; ++c) {
+                // every chunk of the row takes the same gate: start each row at its own chunk so
+                // that the eight rows of a shared-memory phase hit eight different banks
+                const int pc = (c + trow) & 7;
+                uint4 *p = reinterpret_cast<uint4 *>(rowp + pc * 16);
+                const uint4 x = *p;
+                uint4 x0 = x, x1 = x;
+                __nv_bfloat162 *e0 = reinterpret_cast<__nv_bfloat162 *>(&x0);
+                __nv_bfloat162 *e1 = reinterpret_cast<__nv_bfloat162 *>(&x1);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 *p = reinterpret_cast<uint4 *>(row + h * 16384 + c * 16);
-                    const uint4 x = *p;
-                    uint4 x0 = x, x1 = x;
-                    __nv_bfloat162 *e0 = reinterpret_cast<__nv_bfloat162 *>(&x0);
-                    __nv_bfloat162 *e1 = reinterpret_cast<__nv_bfloat162 *>(&x1);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        e0[k] = __hmul2(e0[k], g02);
-                        e1[k] = __hmul2(e1[k], g12);
-                    }
-                    *p = x0;
-                    if (second) *reinterpret_cast<uint4 *>(row + 2 * kGTile + h * 16384 + c * 16) = x1;
+                for (int k = 0; k < 4; ++k) {
+                    e0[k] = __hmul2(e0[k], g02);
+                    e1[k] = __hmul2(e1[k], g12);
                 }
+                *p = x0;
+                if (second) *reinterpret_cast<uint4 *>(rowp + 2 * kG2Tile + pc * 16) = x1;
+            }
             fence_async_smem();  // the tensor core reads what these threads wrote
             mbar_arrive(&scaled[s]);
         }
@@ -193,13 +201,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (got) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {  // 8 columns = one 16-byte chunk
-                        const int c8 = c0 / 8 + q, h = c8 >> 3, cc = c8 & 7;
+                        const int c8 = c0 / 8 + q, hh = c8 >> 3, cc = c8 & 7;
                         const uint4 v = make_uint4(
                             pack_bf16x2(__uint_as_float(x[8 * q]), __uint_as_float(x[8 * q + 1])),
                             pack_bf16x2(__uint_as_float(x[8 * q + 2]), __uint_as_float(x[8 * q + 3])),
                             pack_bf16x2(__uint_as_float(x[8 * q + 4]), __uint_as_float(x[8 * q + 5])),
                             pack_bf16x2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7])));
-                        *reinterpret_cast<uint4 *>(img + h * 16384 + ((cc ^ (r & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4 *>(img + hh * 16384 + ((cc ^ (r & 7)) << 4)) = v;
                     }
                 }
             }
@@ -848,7 +856,7 @@ cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, con
     CUtensorMap mY, mQ;
     const unsigned long long rows = (unsigned long long)p.BH * p.L;
     // a 64-wide tensor reads its second panel out of bounds: the TMA fills zeros
-    if (!make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT))
+    if (!make_tmap_bf16_sw128(&mY, dy, rows, p.d, kG2) || !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kG2))
         return cudaErrorInvalidValue;
     GArgs a{};
     a.gam = gam;
