@@ -460,7 +460,7 @@ __device__ __forceinline__ void store_cols(T *p, const float (&x)[CPL])
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
+__global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
 {
     constexpr int CPL = D >= 32 ? D / 32 : 1;  // dimensions per lane
     constexpr int NW = kThreads / 32;
@@ -504,8 +504,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
         gon[t] = t < cnt ? (gated ? a.tok[(tok0 + t) * kBwdTokWords + 2] : gconst) : 0.f;
         dgo[t] = t < cnt ? a.dgon_in[tok0 + t] : 0.f;
     }
-    // the keys of the warp's tokens, running sums in registers (the pooled key of the online memory)
-    float run[TPW][CPL];
+    // the key sums of each warp's tokens (the pooled key of the online memory)
     if (gated) {
         const T *k = static_cast<const T *>(a.k) + base;
         float s[CPL];
@@ -518,7 +517,7 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
             for (int c = 0; c < CPL; ++c) x[c] = 0.f;
             if (lane_on && tw + j < cnt) load_cols<CPL>(k + (size_t)(tb + tw + j) * D + c0, x);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) run[j][c] = (s[c] += x[c]);
+            for (int c = 0; c < CPL; ++c) s[c] += x[c];
         }
         if (lane_on)
 #pragma unroll
@@ -579,22 +578,27 @@ __global__ void __launch_bounds__(kThreads) bwd_route_simt(BwdArgs a)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) acc[j][c] = fmaf(dr[j], kv[c], acc[j][c]);
         }
-        // the keys of the segment before the warp's tokens
+        // the keys of the segment before the warp's tokens, then through each token
         float off[CPL];
         load_cols<CPL>(a.kpre_tiles + (((size_t)bh * a.N + n) * tps + tile) * D + c0, off);
         for (int w = 0; w < warp; ++w)
 #pragma unroll
             for (int c = 0; c < CPL; ++c) off[c] += tot[w][c0 + c];
         T *duo = static_cast<T *>(a.du) + base;
+        const T *k = static_cast<const T *>(a.k) + base;
 #pragma unroll
         for (int j = 0; j < TPW; ++j) {
             const int t = tw + j;
             if (t < cnt) {
+                float x[CPL];
+                load_cols<CPL>(k + (size_t)(tb + t) * D + c0, x);  // the running key sum, again (cached)
                 const float dron = gon[t] * (dgo[t] - dl[t]);
                 const float inv_cnt = 1.f / (float)(tb + t - t0 + 1);
-                float x[CPL];
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) x[c] = fmaf(dron * (off[c] + run[j][c]), inv_cnt, acc[j][c]);
+                for (int c = 0; c < CPL; ++c) {
+                    off[c] += x[c];
+                    x[c] = fmaf(dron * off[c], inv_cnt, acc[j][c]);
+                }
                 store_cols<CPL>(duo + (size_t)(tb + t) * D + c0, x);
             }
         }
@@ -643,55 +647,87 @@ __global__ void __launch_bounds__(D) bwd_kpre_simt(BwdArgs a)
 // ---------------------------------------------------------------------------
 // bwd_dkbar_simt: the key-mean gradients from the score gradients,
 // dkbar_i = sum_{t : n(t) > i} dr_{t,i} u_t, on the shapes of the tensor-core path
-// (N <= 64).  One CTA per (bh, kDkChunk tokens): every token's u is read once and
+// (N <= 64, seg_len and L multiples of kDkSub, so each kDkSub-token sub-chunk lies in
+// one segment).  One CTA per (bh, kDkChunk tokens): every token's u is read once and
 // feeds every cached segment it scored; a thread keeps one dimension's sums for all
-// segments over a strided share of the chunk, 128 tokens at a time with their dr
-// staged in shared memory, and the CTA adds them to dkbar (zeroed first).
+// segments over a strided share of each sub-chunk, four tokens per step.  The
+// sub-chunks' dr rows are staged in shared memory by asynchronous copies, two
+// buffers deep; the CTA adds its sums to dkbar (zeroed first).
 // ---------------------------------------------------------------------------
 constexpr int kDkChunk = 1024;
 constexpr int kDkSub = 128;
+constexpr size_t kDkSmem = 2 * sizeof(float) * kTab * kDkSub;
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks)
 {
     constexpr int parts = kThreads / D;
     constexpr int TG = 4;  // tokens per step: one 16-byte row of dr per segment
-    __shared__ __align__(16) float sdr[kTab][kDkSub];
+    extern __shared__ __align__(16) float sdr[];  // [2][kTab][kDkSub]
     const int ch = (int)blockIdx.x % chunks, bh = (int)blockIdx.x / chunks;
     const int t_lo = ch * kDkChunk, t_hi = min(t_lo + kDkChunk, a.L);
+    const int nsub = (t_hi - t_lo) / kDkSub;
     const int col = threadIdx.x % D, part = threadIdx.x / D;
     const int nmax = min(a.N - 1, (t_hi - 1) / a.C);  // cached segments any token of the chunk scored
-    const int nstage = min(kTab, (nmax + 7) & ~7);    // rows staged: whole blocks of 8 segments
     const T *u = static_cast<const T *>(a.u) + (size_t)bh * a.L * D + col;
     const float *dr = a.dr + (size_t)bh * a.N * a.L;
+    // sub-chunk s into buffer s % 2: the rows of the segments its tokens scored
+    auto stage = [&](int s) {
+        const int t0 = t_lo + s * kDkSub;
+        const int ns = min(t0 / a.C, kTab);
+        float *dst = sdr + (s & 1) * kTab * kDkSub;
+        for (int e = threadIdx.x; e < ns * (kDkSub / 4); e += kThreads) {
+            const int i = e / (kDkSub / 4), q = e % (kDkSub / 4);
+            cp_async16(dst + i * kDkSub + 4 * q, dr + (size_t)i * a.L + t0 + 4 * q);
+        }
+        cp_async_commit();
+    };
     float acc[kTab];
 #pragma unroll
     for (int i = 0; i < kTab; ++i) acc[i] = 0.f;
-    for (int t0 = t_lo; t0 < t_hi; t0 += kDkSub) {
-        const int cnt = min(kDkSub, t_hi - t0);
+    stage(0);
+    if (nsub > 1) stage(1);
+    else cp_async_commit();
+    for (int s = 0; s < nsub; ++s) {
+        cp_async_wait_one();  // every group but the newest: sub-chunk s is in
         __syncthreads();
-        for (int e = threadIdx.x; e < nstage * kDkSub; e += kThreads) {
-            const int i = e / kDkSub, t = e % kDkSub;
-            sdr[i][t] = t < cnt && i < (t0 + t) / a.C ? dr[(size_t)i * a.L + t0 + t] : 0.f;
-        }
-        __syncthreads();
-        for (int t = part * TG; t < cnt; t += parts * TG) {
+        const int t0 = t_lo + s * kDkSub;
+        const int ns = min(t0 / a.C, kTab);
+        const float *buf = sdr + (s & 1) * kTab * kDkSub;
+        float un[TG];
+#pragma unroll
+        for (int j = 0; j < TG; ++j) un[j] = to_f(u[(size_t)(t0 + part * TG + j) * D]);
+        for (int t = part * TG; t < kDkSub; t += parts * TG) {
             float uv[TG];
 #pragma unroll
-            for (int j = 0; j < TG; ++j) uv[j] = t + j < cnt ? to_f(u[(size_t)(t0 + t + j) * D]) : 0.f;
-            // segments the group's last token scored (the others' rows are zero there)
-            const int n_t = min((t0 + min(t + TG, cnt) - 1) / a.C, kTab);
+            for (int j = 0; j < TG; ++j) uv[j] = un[j];
+            if (t + parts * TG < kDkSub)
+#pragma unroll
+                for (int j = 0; j < TG; ++j) un[j] = to_f(u[(size_t)(t0 + t + parts * TG + j) * D]);
 #pragma unroll
             for (int ib = 0; ib < kTab / 8; ++ib) {
-                if (8 * ib >= n_t) break;
+                if (8 * ib >= ns) break;
 #pragma unroll
                 for (int ii = 0; ii < 8; ++ii) {
                     const int i = 8 * ib + ii;
-                    const float4 r = *reinterpret_cast<const float4 *>(&sdr[i][t]);
-                    acc[i] = fmaf(r.x, uv[0], fmaf(r.y, uv[1], fmaf(r.z, uv[2], fmaf(r.w, uv[3], acc[i]))));
+                    if (i < ns) {
+                        const float4 r = *reinterpret_cast<const float4 *>(buf + i * kDkSub + t);
+                        acc[i] = fmaf(r.x, uv[0], fmaf(r.y, uv[1], fmaf(r.z, uv[2], fmaf(r.w, uv[3], acc[i]))));
+                    }
                 }
             }
         }
+        __syncthreads();  // buffer s % 2 is free again
+        if (s + 2 < nsub) stage(s + 2);
+        else cp_async_commit();
     }
     float *dk = a.dkbar + (size_t)bh * a.N * D + col;
 #pragma unroll
@@ -1014,7 +1050,8 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     profile_after_kernel(s, "bwd_route_simt");
     if (a.dr && p.N > 1) {
         const int chunks = (p.L + kDkChunk - 1) / kDkChunk;
-        bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * chunks), kThreads, 0, s>>>(a, chunks);
+        if ((e = set_smem(bwd_dkbar_simt<T, D>, kDkSmem)) != cudaSuccess) return e;
+        bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * chunks), kThreads, kDkSmem, s>>>(a, chunks);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_dkbar_simt");
     }
