@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) bwd_gates_simt(BwdArgs a)
 // dg_on and dq, and computes per token
 //   delta_t = sum_i g dg + g_on dg_on,  dr_{t,i} = g (dg - delta) -> dr,
 //   du_t = sum_i dr_{t,i} kbar_i + dr_on p_t   (p_t = mean of the segment's keys up to t),
-//   dq_t in the output type, and token words 2-4 (online gate, delta, w = dr_on / cnt_t).
+//   dq_t in the output type, and for dk / dv the online gate and w = dr_on / cnt_t.
 // The gate and dr tables sit in shared memory as [i][t]; for du a warp owns kTB / 8
 // tokens and a lane D / 32 dimensions (a register tile over every cached segment).
 // ---------------------------------------------------------------------------
@@ -603,14 +603,10 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
             }
         }
     }
-    if (tid < cnt) {
+    if (tid < cnt) {  // for dk and dv: the online gate and the pooled-key weight
         const int t = tid;
-        float *w = a.tok + (tok0 + t) * kBwdTokWords;
-        w[0] = 0.f;  // (the softmax data are not kept on this path)
-        w[1] = 1.f;
-        w[2] = gon[t];
-        w[3] = dl[t];
-        w[4] = gated ? gon[t] * (dgo[t] - dl[t]) / (float)(tb + t - t0 + 1) : 0.f;
+        a.kv_gw[tok0 + t] = gon[t];
+        a.kv_gw[(size_t)a.BH * a.L + tok0 + t] = gated ? gon[t] * (dgo[t] - dl[t]) / (float)(tb + t - t0 + 1) : 0.f;
     }
 }
 
@@ -1069,7 +1065,7 @@ cudaError_t backward_tc_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
         if ((e = launch_bwd_G_tc(p, a.dy, a.q, a.gam, Gimg, s)) != cudaSuccess) return e;
         profile_after_kernel(s, "bwd_G_tc");
     }
-    if ((e = launch_bwd_kv_tc(p, a.q, a.k, a.v, a.u, a.dy, Gimg, a.tok, a.dkbar, a.dk, a.dv, s)) != cudaSuccess) return e;
+    if ((e = launch_bwd_kv_tc(p, a.q, a.k, a.v, a.u, a.dy, Gimg, a.kv_gw, a.dkbar, a.dk, a.dv, s)) != cudaSuccess) return e;
     profile_after_kernel(s, "bwd_kv_tc");
     return cudaSuccess;
 }
@@ -1081,14 +1077,13 @@ size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-// Scratch of one backward call, in this order: states, G (N d^2 floats per head
-// each), kbar, dkbar (N d), r_on (L), O_on, X_on (L d), per-token words (L x 5),
-// SSC selection indices and gates (L x topk each).
 // Scratch of one backward call.  FFMA path, in this order: states, G (N d^2 floats
 // per head each), kbar, dkbar (N d), r_on (L), O_on, X_on (L d), per-token words
 // (L x 5), SSC selection indices and gates (L x topk each).  Tensor-core path: states,
 // G, kbar, dkbar, per-token words, the gates of the cached segments (routed: L x N),
-// the forward state kernel's images and r_on, and the cached pass's outputs.
+// the keys before each 64-token tile (routed), the online gates and pooled-key
+// weights (2 L), the forward state kernel's images and r_on, and the cached pass's
+// outputs.
 size_t backward_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
@@ -1098,8 +1093,8 @@ size_t backward_scratch_bytes(const Problem &p)
     if (bwd_tc_supported(p)) {
         const size_t gam = mode_uses_u(p.mode) ? N : 0;
         const size_t kpre = mode_uses_u(p.mode) ? N * ((p.C + kTB - 1) / kTB) * d : 0;
-        return common + pad256(4 * BH * L * gam) + pad256(4 * BH * kpre) + pad256(tc_state_scratch_bytes(p)) +
-               pad256(bwd_cached_scratch_bytes(p));
+        return common + pad256(4 * BH * L * gam) + pad256(4 * BH * kpre) + pad256(8 * BH * L) +
+               pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p));
     }
     const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
     return common + pad256(4 * BH * L) + 2 * pad256(4 * BH * L * d) + 2 * pad256(4 * BH * L * sel);
@@ -1144,6 +1139,7 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         // and dk / dv on the tensor cores.
         float *gam = gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
         a.kpre_tiles = gated ? reinterpret_cast<float *>(take(4 * BH * N * ((p.C + kTB - 1) / kTB) * d)) : nullptr;
+        a.kv_gw = reinterpret_cast<float *>(take(8 * BH * L));
         void *state_scratch = take(tc_state_scratch_bytes(p));
         void *cached_scratch = take(bwd_cached_scratch_bytes(p));
         TcImages img{};

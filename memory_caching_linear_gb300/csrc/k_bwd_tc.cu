@@ -55,11 +55,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // One CTA per (b,h, pair of cached segments i0 = 2p, i1 = 2p + 1): every tile after
 // segment i0 is loaded once and feeds both accumulators (the tiles of segment i1
 // only the first).
@@ -573,22 +568,61 @@ __global__ void __launch_bounds__(kCThreads, 1)
 //   dv_j = G_n k_j + sum_{t >= j in n} g_on(t) (k_j . q_t) dy_t
 //   dk_j = G_n^T v_j + sum_{t >= j in n} g_on(t) (v_j . dy_t) q_t
 //          + sum_{t >= j in n} w_t u_t + dkbar_n / |n|      (w_t = dr_on(t) / cnt_t)
-// On the tensor cores: D_v = K G^T, D_k = V G (the G image); then for every chunk c'
-// >= c of the segment X = K Q'^T, Y = V dY'^T (SS); the workers turn them into
-// P3 = g_on mask(X), P4 = g_on mask(Y), P5 = w mask (mask: t >= j inside chunk c)
-// and D_v += P3 dY', D_k += P4 Q' + P5 U' (TS, the chunk tiles read MN-major).
-// Persistent, one CTA per SM, chunks with the most later chunks first.
-// TMEM: D_v [0,128) | D_k [128,256) | X [256,384) | Y [384,512).
+// On the tensor cores: D_v = K G^T, D_k = V G (the G image); then for every 64-token
+// sub-chunk s from chunk c to the segment's end X = K Q'^T, Y = V dY'^T (SS, N = 64);
+// the workers turn them into P3 = g_on mask(X), P4 = g_on mask(Y), P5 = w mask
+// (mask: t >= j) and D_v += P3 dY', D_k += P4 Q' + P5 U' (TS, the sub-chunk tiles
+// read MN-major).  X and Y are double-buffered, so the tensor cores compute the
+// next sub-chunk's products while the workers mask the current one; the sub-chunk
+// tiles come through a three-slot ring with the tokens' online gates and weights w, after
+// the G image of the segment (the first item of a chunk, in a slot of its own).
+// Eight worker warps, two per TMEM lane quadrant: warp half h takes the tokens
+// [32h, 32h+32) of a sub-chunk, i.e. the 32 columns [32h, 32h+32) of X and of Y, and
+// writes its P blocks into them (P3 / P4 into the first 16, P5 into the next 16 of Y).
+// Persistent, one CTA per SM.  A unit of work is a pair of chunks (c, CPS-1-c) of one
+// segment, so every unit streams the same number of sub-chunks, and the units of a
+// segment run side by side (its q, dy, u come from HBM about once).
+// TMEM: D_v [0,128) | D_k [128,256) | X0 Y0 [256,384) | X1 Y1 [384,512) (64 columns each).
 // ============================================================================
-constexpr int kVThreads = 192;
-constexpr size_t kVSmem = 6 * kGTile + 1024;  // K, V, G image; Q', dY', U' of the current chunk pair
+constexpr int kVWorkers = 256;
+constexpr int kVThreads = 64 + kVWorkers;                     // warp 0 TMA, warp 1 MMA issuer, 8 workers
+constexpr uint32_t kVStage = 3 * kG2Tile + 1024;              // Q', dY', U' of a 64-token sub-chunk; gates, w
+constexpr int kVRing = 3;
+constexpr size_t kVSmem = 2 * kGTile + kVRing * kVStage + 1024;  // K, V; the ring
 
 struct VArgs {
     const uint8_t *G;      // [BH][N] x 32 KB G images (segments < N-1)
-    const float *tok;      // [BH][L][kBwdTokWords]: word 2 the online gate, word 4 the pooled-key weight w
+    const float *gw;       // [2][BH][L]: the online gate, then the pooled-key weight w, per token
     const float *dkbar;    // [BH][N][d]
     void *dk, *dv;         // bf16 [BH][L][d] out
-    int BH, L, C, N, CPS, d, routed, num_tiles;
+    int BH, L, C, N, CPS, d, routed;
+    int UP;                // units per segment: ceil(CPS / 2)
+    int num_units;         // BH * N * UP
+};
+
+// The CTA's k-th tile: unit blockIdx + (k / 2) * grid, its first (heavier) or second chunk.
+// Returns false past the last unit; skips the repeated middle chunk of an odd CPS.
+struct VTiles {
+    int k = 0, h = 0;
+    __device__ bool next(const VArgs &a, int &bh, int &n, int &c)
+    {
+        for (;;) {
+            const int u = (int)blockIdx.x + k * (int)gridDim.x;
+            if (u >= a.num_units) return false;
+            const int p = u % a.UP, seg = u / a.UP;
+            bh = seg % a.BH;
+            n = seg / a.BH;
+            c = h ? a.CPS - 1 - p : p;
+            const bool valid = !(h && c == p);
+            if (h) {
+                ++k;
+                h = 0;
+            } else {
+                h = 1;
+            }
+            if (valid) return true;
+        }
+    }
 };
 
 __global__ void __launch_bounds__(kVThreads, 1)
@@ -598,22 +632,14 @@ __global__ void __launch_bounds__(kVThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sK = sm, *sV = sm + kGTile, *sG = sm + 2 * kGTile;
-    uint8_t *sQ = sm + 3 * kGTile, *sY = sm + 4 * kGTile, *sU = sm + 5 * kGTile;
-    __shared__ uint64_t kv_full, kv_empty, pr_full, pr_empty, xy_full, p_full, d_full, d_empty, fin;
-    __shared__ float gs[2][128], ws[2][128];
+    // K, V of the chunk; a ring of kVRing slots, each the G image of a chunk's segment
+    // (the first item of a chunk that has one) or a sub-chunk's Q', dY', U', gates and w
+    uint8_t *sK = sm, *sV = sm + kGTile, *sR = sm + 2 * kGTile;
+    __shared__ uint64_t kv_full, kv_empty, r_full[kVRing], r_empty[kVRing], xy_full[2], p_full[2], d_full, d_empty, fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int my_tiles = blockIdx.x < (unsigned)a.num_tiles ? (a.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    auto tile = [&](int j, int &bh, int &n, int &c) {  // chunk 0 (the most later chunks) first
-        const int id = (int)blockIdx.x + j * (int)gridDim.x;
-        const int per = a.BH * a.N;
-        c = id / per;
-        n = (id % per) / a.BH;
-        bh = (id % per) % a.BH;
-    };
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -623,12 +649,16 @@ __global__ void __launch_bounds__(kVThreads, 1)
         abort_flag = 0;
         mbar_init(&kv_full, 1);
         mbar_init(&kv_empty, 1);
-        mbar_init(&pr_full, 1);
-        mbar_init(&pr_empty, 1);
-        mbar_init(&xy_full, 1);
-        mbar_init(&p_full, 128);
+        for (int r = 0; r < kVRing; ++r) {
+            mbar_init(&r_full[r], 1);
+            mbar_init(&r_empty[r], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&xy_full[b], 1);
+            mbar_init(&p_full[b], kVWorkers);
+        }
         mbar_init(&d_full, 1);
-        mbar_init(&d_empty, 128);
+        mbar_init(&d_empty, kVWorkers);
         mbar_init(&fin, 1);
         fence_mbar_init();
     }
@@ -636,67 +666,105 @@ __global__ void __launch_bounds__(kVThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t tDv = tb, tDk = tb + 128, tX = tb + 256, tY = tb + 384;
+    const uint32_t tDv = tb, tDk = tb + 128, tXY = tb + 256;  // X_b = tXY + 128 b, Y_b = X_b + 64
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        if (lane == 0 && my_tiles > 0) {
+        if (lane == 0) {
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
             prefetch_tensormap(&mQ);
             prefetch_tensormap(&mY);
             if (a.routed) prefetch_tensormap(&mU);
-            uint32_t pc = 0;
+            uint32_t rc = 0, jt = 0;  // ring items, chunks
             bool ok = true;
-            for (int j = 0; j < my_tiles && ok; ++j) {
-                int bh, n, c;
-                tile(j, bh, n, c);
+            VTiles it;
+            int bh, n, c;
+            while (ok && it.next(a, bh, n, c)) {
                 const bool hasG = n < a.N - 1;
-                if (!(ok = mbar_wait(&kv_empty, (j & 1) ^ 1, &abort_flag))) break;
+                if (!(ok = mbar_wait(&kv_empty, (jt & 1) ^ 1, &abort_flag))) break;
                 const int row = bh * a.L + n * a.C + c * kGT;
-                mbar_arrive_expect_tx(&kv_full, (hasG ? 3 : 2) * kGTile);
+                mbar_arrive_expect_tx(&kv_full, 2 * kGTile);
                 tma_load_2d(sK, &mK, 0, row, &kv_full);
                 tma_load_2d(sK + 16384, &mK, 64, row, &kv_full);
                 tma_load_2d(sV, &mV, 0, row, &kv_full);
                 tma_load_2d(sV + 16384, &mV, 64, row, &kv_full);
-                if (hasG) bulk_load(sG, a.G + ((size_t)bh * a.N + n) * kGTile, kGTile, &kv_full);
-                for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
-                    if (!(ok = mbar_wait(&pr_empty, (pc & 1) ^ 1, &abort_flag))) break;
-                    const int r2 = bh * a.L + n * a.C + c2 * kGT;
-                    mbar_arrive_expect_tx(&pr_full, (a.routed ? 3 : 2) * kGTile);
-                    tma_load_2d(sQ, &mQ, 0, r2, &pr_full);
-                    tma_load_2d(sQ + 16384, &mQ, 64, r2, &pr_full);
-                    tma_load_2d(sY, &mY, 0, r2, &pr_full);
-                    tma_load_2d(sY + 16384, &mY, 64, r2, &pr_full);
+                const int S = 2 * (a.CPS - c);
+                for (int s = hasG ? -1 : 0; s < S; ++s, ++rc) {
+                    const uint32_t r = rc % kVRing;
+                    if (!(ok = mbar_wait(&r_empty[r], ((rc / kVRing) & 1) ^ 1, &abort_flag))) break;
+                    uint8_t *st = sR + r * kVStage;
+                    if (s < 0) {
+                        mbar_arrive_expect_tx(&r_full[r], kGTile);
+                        bulk_load(st, a.G + ((size_t)bh * a.N + n) * kGTile, kGTile, &r_full[r]);
+                        continue;
+                    }
+                    const int r2 = row + kG2 * s;
+                    mbar_arrive_expect_tx(&r_full[r], (a.routed ? 3 : 2) * kG2Tile + (a.routed ? 512 : 256));
+                    const float *gw = a.gw + (size_t)r2;  // the sub-chunk's online gates; w BH * L further
+                    bulk_load(st + 3 * kG2Tile, gw, 256, &r_full[r]);
+                    if (a.routed) bulk_load(st + 3 * kG2Tile + 256, gw + (size_t)a.BH * a.L, 256, &r_full[r]);
+                    tma_load_2d(st, &mQ, 0, r2, &r_full[r]);
+                    tma_load_2d(st + kG2Tile / 2, &mQ, 64, r2, &r_full[r]);
+                    tma_load_2d(st + kG2Tile, &mY, 0, r2, &r_full[r]);
+                    tma_load_2d(st + kG2Tile + kG2Tile / 2, &mY, 64, r2, &r_full[r]);
                     if (a.routed) {
-                        tma_load_2d(sU, &mU, 0, r2, &pr_full);
-                        tma_load_2d(sU + 16384, &mU, 64, r2, &pr_full);
+                        tma_load_2d(st + 2 * kG2Tile, &mU, 0, r2, &r_full[r]);
+                        tma_load_2d(st + 2 * kG2Tile + kG2Tile / 2, &mU, 64, r2, &r_full[r]);
                     }
                 }
+                ++jt;
             }
             // leave no copy in flight
             int give_up = 0;
-            if (pc > 0) mbar_wait_limit(&pr_full, (pc - 1) & 1, &give_up, kWaitLimitNs);
-            mbar_wait_limit(&kv_full, (my_tiles - 1) & 1, &give_up, kWaitLimitNs);
+            for (uint32_t q = rc > kVRing ? rc - kVRing : 0; q < rc; ++q)
+                mbar_wait_limit(&r_full[q % kVRing], (q / kVRing) & 1, &give_up, kWaitLimitNs);
+            if (jt > 0) mbar_wait_limit(&kv_full, (jt - 1) & 1, &give_up, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0 && my_tiles > 0) {
+        if (lane == 0) {
             constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);
-            auto kmaj = [](int kk) { return (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32); };
-            const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV), g0 = smem_u32(sG);
-            const uint32_t q0 = smem_u32(sQ), y0 = smem_u32(sY), u0 = smem_u32(sU);
-            uint32_t pc = 0;
+            constexpr uint32_t idXY = idesc_bf16(128, kG2, false, false);
+            auto kmaj = [](int kk) { return (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32); };      // 128-row tile
+            auto kmaj64 = [](int kk) { return (uint32_t)((kk >> 2) * 8192 + (kk & 3) * 32); };     // 64-row tile
+            const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV), r0 = smem_u32(sR);
+            auto slot = [&](uint32_t q) { return r0 + (q % kVRing) * kVStage; };
+            // X_x = K Q'^T, Y_x = V dY'^T of the sub-chunk in ring item q, into TMEM buffer x % 2
+            auto issue_xy = [&](uint32_t q, uint32_t x) {
+                const uint32_t b = x & 1, st = slot(q);
+                const uint32_t tX = tXY + 128 * b, tY = tX + 64;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tX, make_desc_sw128(k0 + kmaj(kk), 0, 1024), make_desc_sw128(st + kmaj64(kk), 0, 1024),
+                           idXY, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tY, make_desc_sw128(v0 + kmaj(kk), 0, 1024),
+                           make_desc_sw128(st + kG2Tile + kmaj64(kk), 0, 1024), idXY, kk > 0);
+                mma_commit(&xy_full[b]);
+            };
+            uint32_t rc = 0, pc = 0, jt = 0;  // ring items, sub-chunks, chunks
             bool ok = true;
-            for (int j = 0; j < my_tiles && ok; ++j) {
-                int bh, n, c;
-                tile(j, bh, n, c);
+            VTiles it;
+            int bh, n, c;
+            while (ok && it.next(a, bh, n, c)) {
                 const bool hasG = n < a.N - 1;
-                if (!(ok = mbar_wait(&kv_full, j & 1, &abort_flag) && mbar_wait(&d_empty, (j & 1) ^ 1, &abort_flag)))
+                const int S = 2 * (a.CPS - c);
+                const uint32_t q0 = rc + (hasG ? 1 : 0);  // ring item of the first sub-chunk
+                if (!(ok = mbar_wait(&kv_full, jt & 1, &abort_flag) &&
+                           mbar_wait(&r_full[q0 % kVRing], (q0 / kVRing) & 1, &abort_flag)))
                     break;
                 tc_fence_after();
+                issue_xy(q0, pc);
+                // the previous chunk's drain has read D
+                if (!(ok = mbar_wait(&d_empty, (jt & 1) ^ 1, &abort_flag))) break;
+                tc_fence_after();
                 if (hasG) {
+                    if (!(ok = mbar_wait(&r_full[rc % kVRing], (rc / kVRing) & 1, &abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t g0 = slot(rc);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // D_v = K G^T: B = G image K-major (rows = value dim)
                         mma_ss(tDv, make_desc_sw128(k0 + kmaj(kk), 0, 1024), make_desc_sw128(g0 + kmaj(kk), 0, 1024),
@@ -705,38 +773,42 @@ __global__ void __launch_bounds__(kVThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)  // D_k = V G: B = G image MN-major
                         mma_ss(tDk, make_desc_sw128(v0 + kmaj(kk), 0, 1024), make_desc_sw128(g0 + kk * 2048u, 16384, 1024),
                                idKM, kk > 0);
+                    mma_commit(&r_empty[rc % kVRing]);
                 }
-                for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
-                    if (!(ok = mbar_wait(&pr_full, pc & 1, &abort_flag))) break;
+                for (int s = 0; s < S && ok; ++s) {
+                    const uint32_t q = q0 + s, x = pc + s, b = x & 1;
+                    if (s + 1 < S) {  // the next sub-chunk's products while the workers mask this one
+                        if (!(ok = mbar_wait(&r_full[(q + 1) % kVRing], ((q + 1) / kVRing) & 1, &abort_flag))) break;
+                        tc_fence_after();
+                        issue_xy(q + 1, x + 1);
+                        if (s + 2 == S) mma_commit(&kv_empty);  // K and V are read for the last time
+                    }
+                    if (!(ok = mbar_wait(&p_full[b], (x >> 1) & 1, &abort_flag))) break;
                     tc_fence_after();
+                    const uint32_t st = slot(q);
+                    const uint32_t tX = tXY + 128 * b, tY = tX + 64;
+                    const bool first = !hasG && s == 0;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // X = K Q'^T
-                        mma_ss(tX, make_desc_sw128(k0 + kmaj(kk), 0, 1024), make_desc_sw128(q0 + kmaj(kk), 0, 1024), idKK,
-                               kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)  // D_v += P3 dY' (tokens 16 kk.. of P at 32 (kk/2) + 8 (kk%2))
+                        mma_ts(tDv, tX + 32 * (kk >> 1) + 8 * (kk & 1),
+                               make_desc_sw128(st + kG2Tile + kk * 2048u, kG2Tile / 2, 1024), idKM, !first || kk > 0);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // Y = V dY'^T
-                        mma_ss(tY, make_desc_sw128(v0 + kmaj(kk), 0, 1024), make_desc_sw128(y0 + kmaj(kk), 0, 1024), idKK,
-                               kk > 0);
-                    mma_commit(&xy_full);
-                    if (!(ok = mbar_wait(&p_full, pc & 1, &abort_flag))) break;
-                    tc_fence_after();
-                    const bool first = !hasG && c2 == c;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // D_v += P3 dY'
-                        mma_ts(tDv, tX + kk * 8, make_desc_sw128(y0 + kk * 2048u, 16384, 1024), idKM, !first || kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // D_k += P4 Q'
-                        mma_ts(tDk, tY + kk * 8, make_desc_sw128(q0 + kk * 2048u, 16384, 1024), idKM, !first || kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)  // D_k += P4 Q'
+                        mma_ts(tDk, tY + 32 * (kk >> 1) + 8 * (kk & 1), make_desc_sw128(st + kk * 2048u, kG2Tile / 2, 1024),
+                               idKM, !first || kk > 0);
                     if (a.routed) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)  // D_k += P5 U'
-                            mma_ts(tDk, tY + 64 + kk * 8, make_desc_sw128(u0 + kk * 2048u, 16384, 1024), idKM, 1);
+                        for (int kk = 0; kk < 4; ++kk)  // D_k += P5 U' (P5 16 columns after P4)
+                            mma_ts(tDk, tY + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                                   make_desc_sw128(st + 2 * kG2Tile + kk * 2048u, kG2Tile / 2, 1024), idKM, 1);
                     }
-                    mma_commit(&pr_empty);
+                    mma_commit(&r_empty[q % kVRing]);
                 }
                 if (!ok) break;
-                mma_commit(&kv_empty);
                 mma_commit(&d_full);
+                rc = q0 + S;
+                pc += S;
+                ++jt;
             }
             // leave no MMA in flight
             mma_commit(&fin);
@@ -745,69 +817,88 @@ __global__ void __launch_bounds__(kVThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- workers (thread = row j of chunk c)
-        const int q4 = warp & 3;
-        const uint32_t row = 32 * q4 + lane;
+        const int q4 = warp & 3, half = (warp - 2) >> 2;  // lane quadrant; tokens [32 half, 32 half + 32)
+        const int row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        uint32_t pc = 0;
+        uint32_t rc = 0, pc = 0, jt = 0;  // ring items, sub-chunks, chunks
         bool ok = true;
-        for (int j = 0; j < my_tiles && ok; ++j) {
-            int bh, n, c;
-            tile(j, bh, n, c);
-            for (int c2 = c; c2 < a.CPS && ok; ++c2, ++pc) {
-                // the gates and pooled-key weights of chunk c2's tokens (each worker brings its own)
-                const int b = pc & 1;
-                const float *tw = a.tok + ((size_t)bh * a.L + n * a.C + c2 * kGT + row) * kBwdTokWords;
-                gs[b][row] = tw[2];
-                ws[b][row] = a.routed ? tw[4] : 0.f;
-                named_bar_sync(1, 128);
-                if (!(ok = mbar_wait(&xy_full, pc & 1, &abort_flag))) break;
+        VTiles it;
+        int bh, n, c;
+        while (ok && it.next(a, bh, n, c)) {
+            const int S = 2 * (a.CPS - c);
+            const uint32_t q0 = rc + (n < a.N - 1 ? 1 : 0);
+            const size_t tok_c = (size_t)bh * a.L + n * a.C + c * kGT;  // the chunk's first token
+            for (int s = 0; s < S && ok; ++s) {
+                const uint32_t q = q0 + s, x = pc + s, b = x & 1;
+                // the item's gates came by TMA (this thread waits for them itself), X and Y from the MMA
+                if (!(ok = mbar_wait(&r_full[q % kVRing], (q / kVRing) & 1, &abort_flag) &&
+                           mbar_wait(&xy_full[b], (x >> 1) & 1, &abort_flag)))
+                    break;
                 tc_fence_after();
-                const bool diag = c2 == c;  // the same chunk: only t >= j
+                const float *gsm = reinterpret_cast<const float *>(sR + (q % kVRing) * kVStage + 3 * kG2Tile) + 32 * half;
+                const float *wsm = gsm + 64;
+                const uint32_t tX = tXY + 128 * b + lane_base + 32 * half, tY = tX + 64;
+                const int t_off = kG2 * s + 32 * half - row;  // token t of the half is kept when t + t_off >= 0
+                const bool diag = t_off < 0;                  // some token of the half lies before row j
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {  // 16 key columns t at a time
+                for (int m = 0; m < 2; ++m) {  // 16 token columns at a time
                     uint32_t x[16], y[16], o3[8], o4[8];
-                    tmem_ld16(tX + lane_base + 16 * m, x);
-                    tmem_ld16(tY + lane_base + 16 * m, y);
+                    tmem_ld16(tX + 16 * m, x);
+                    tmem_ld16(tY + 16 * m, y);
+                    float g[16];
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(gsm + 16 * m + 4 * k4);
+                        g[4 * k4] = v.x; g[4 * k4 + 1] = v.y; g[4 * k4 + 2] = v.z; g[4 * k4 + 3] = v.w;
+                    }
+                    if (diag)
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (16 * m + k + t_off < 0) g[k] = 0.f;
                     tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 16; k += 2) {
-                        const int t = 16 * m + k;
-                        const float g0 = (!diag || t >= (int)row) ? gs[b][t] : 0.f;
-                        const float g1 = (!diag || t + 1 >= (int)row) ? gs[b][t + 1] : 0.f;
-                        o3[k / 2] = pack_bf16x2(g0 * __uint_as_float(x[k]), g1 * __uint_as_float(x[k + 1]));
-                        o4[k / 2] = pack_bf16x2(g0 * __uint_as_float(y[k]), g1 * __uint_as_float(y[k + 1]));
+                        o3[k / 2] = pack_bf16x2(g[k] * __uint_as_float(x[k]), g[k + 1] * __uint_as_float(x[k + 1]));
+                        o4[k / 2] = pack_bf16x2(g[k] * __uint_as_float(y[k]), g[k + 1] * __uint_as_float(y[k + 1]));
                     }
-                    tmem_st8(tX + lane_base + 8 * m, o3);
-                    tmem_st8(tY + lane_base + 8 * m, o4);
+                    tmem_st8(tX + 8 * m, o3);
+                    tmem_st8(tY + 8 * m, o4);
                 }
-                if (a.routed) {  // P5 = w mask, written after every read of Y
+                if (a.routed) {  // P5 = w mask, written after every read of the half's Y columns
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
+                    for (int m = 0; m < 2; ++m) {
+                        float w[16];
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(wsm + 16 * m + 4 * k4);
+                            w[4 * k4] = v.x; w[4 * k4 + 1] = v.y; w[4 * k4 + 2] = v.z; w[4 * k4 + 3] = v.w;
+                        }
                         uint32_t o5[8];
 #pragma unroll
                         for (int k = 0; k < 16; k += 2) {
-                            const int t = 16 * m + k;
-                            o5[k / 2] = pack_bf16x2((!diag || t >= (int)row) ? ws[b][t] : 0.f,
-                                                    (!diag || t + 1 >= (int)row) ? ws[b][t + 1] : 0.f);
+                            const float w0 = 16 * m + k + t_off >= 0 ? w[k] : 0.f;
+                            const float w1 = 16 * m + k + 1 + t_off >= 0 ? w[k + 1] : 0.f;
+                            o5[k / 2] = pack_bf16x2(w0, w1);
                         }
-                        tmem_st8(tY + 64 + lane_base + 8 * m, o5);
+                        tmem_st8(tY + 16 + 8 * m, o5);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&p_full);
+                mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
-            // drain: dv = D_v, dk = D_k + dkbar_n / |n|
-            if (!(ok = mbar_wait(&d_full, j & 1, &abort_flag))) break;
+            // drain: dv = D_v, dk = D_k + dkbar_n / |n|; the half's 64 columns
+            if (!(ok = mbar_wait(&d_full, jt & 1, &abort_flag))) break;
             tc_fence_after();
-            const size_t tok = (size_t)bh * a.L + n * a.C + c * kGT + row;
+            const size_t tok = tok_c + row;
             __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(a.dv) + tok * a.d;
             __nv_bfloat16 *dko = static_cast<__nv_bfloat16 *>(a.dk) + tok * a.d;
             const float *rho = a.dkbar + ((size_t)bh * a.N + n) * a.d;
             const float inv_len = 1.f / (float)a.C;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int mm = 0; mm < 2; ++mm) {
+                const int m = 2 * half + mm;
                 uint32_t xv[32], xk[32];
                 tmem_ld32(tDv + lane_base + 32 * m, xv);
                 tmem_ld32(tDk + lane_base + 32 * m, xk);
@@ -832,6 +923,9 @@ __global__ void __launch_bounds__(kVThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&d_empty);
+            rc = q0 + S;
+            pc += S;
+            ++jt;
         }
     }
     tc_fence_before();
@@ -936,34 +1030,36 @@ cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k,
 namespace mc {
 
 cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
-                             const uint8_t *G, const float *tok, const float *dkbar, void *dk, void *dv, cudaStream_t s)
+                             const uint8_t *G, const float *gw, const float *dkbar, void *dk, void *dv, cudaStream_t s)
 {
     const bool routed = p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_SSC;
     CUtensorMap mK, mV, mQ, mY, mU;
     const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    // K, V: 128-token chunks; q, dy, u: 64-token sub-chunks
     if (!make_tmap_bf16_sw128(&mK, k, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mV, v, rows, p.d, kGT) ||
-        !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mY, dy, rows, p.d, kGT))
+        !make_tmap_bf16_sw128(&mQ, q, rows, p.d, kG2) || !make_tmap_bf16_sw128(&mY, dy, rows, p.d, kG2))
         return cudaErrorInvalidValue;
     if (routed) {
-        if (!make_tmap_bf16_sw128(&mU, u, rows, p.d, kGT)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16_sw128(&mU, u, rows, p.d, kG2)) return cudaErrorInvalidValue;
     } else {
-        mU = mK;
+        mU = mQ;
     }
     VArgs a{};
     a.G = G;
-    a.tok = tok;
+    a.gw = gw;
     a.dkbar = dkbar;
     a.dk = dk;
     a.dv = dv;
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kGT; a.d = p.d; a.routed = routed ? 1 : 0;
-    a.num_tiles = p.BH * p.N * a.CPS;
+    a.UP = (a.CPS + 1) / 2;
+    a.num_units = p.BH * p.N * a.UP;
     cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kVSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
-    const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+    const int grid = a.num_units < sms ? a.num_units : sms;
     bwd_kv_tc<<<grid, kVThreads, kVSmem, s>>>(mK, mV, mQ, mY, mU, a);
     return cudaGetLastError();
 }

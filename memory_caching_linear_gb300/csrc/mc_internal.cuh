@@ -161,6 +161,7 @@ struct BwdArgs {
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
     float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
+    float *kv_gw;         // [2][BH][L] the online gate and the pooled-key weight w per token (tensor-core path)
     int BH, L, C, N, mode, topk;
 };
 size_t backward_scratch_bytes(const Problem &p);
@@ -168,8 +169,9 @@ size_t backward_scratch_bytes(const Problem &p);
 // L % seg_len == 0, N <= 64.
 bool bwd_tc_supported(const Problem &p);
 cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, const float *gam, uint8_t *G, cudaStream_t s);
+// gw: [2][BH][L], the online gate of every token, then its pooled-key weight w (routed aggregations).
 cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
-                             const uint8_t *G, const float *tok, const float *dkbar, void *dk, void *dv, cudaStream_t s);
+                             const uint8_t *G, const float *gw, const float *dkbar, void *dk, void *dv, cudaStream_t s);
 size_t bwd_cached_scratch_bytes(const Problem &p);
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
                                  const TcImages &img, const float *gam, const float *tok, void *scratch,
