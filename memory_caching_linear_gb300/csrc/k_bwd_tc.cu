@@ -229,14 +229,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // (TS); then for the prefix state and each cached state X: W = dY X (SS, the image
 // read MN-major) for the dot with q, and D_q += (g o dY) X^T (TS, the same image).
 // Persistent, one CTA per SM, tiles with the most cached segments first.  Warp 0
-// streams Q, K, V, dY of the tile (TMA) and one 32 KB image per state through a
-// two-slot ring; warp 1 issues; warps 2-5 own a token row each.
+// loads Q and dY of the tile (TMA, resident while the tile runs) and streams K, V
+// and one 32 KB image per state through a four-slot ring (K and V are read by the
+// tile's first three products only); warp 1 issues; warps 2-5 own a token row each.
 // TMEM: D_q [0,128) | W0 [128,256) | W1 [256,384) (G1 / G2 at a tile's start) |
 //       A0 [384,448) | A1 [448,512).
 // ============================================================================
-constexpr int kCRing = 2;
+constexpr int kCRing = 4;
 constexpr int kCThreads = 192;
-constexpr size_t kCSmem = 4 * kGTile + kCRing * kGTile + 1024;
+constexpr size_t kCSmem = 2 * kGTile + kCRing * kGTile + 1024;
 
 struct CArgs {
     const uint8_t *images;  // [BH][N] x 32 KB state images
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sQ = sm, *sK = sm + kGTile, *sV = sm + 2 * kGTile, *sY = sm + 3 * kGTile, *ring = sm + 4 * kGTile;
+    uint8_t *sQ = sm, *sY = sm + kGTile, *ring = sm + 2 * kGTile;
     __shared__ uint64_t tile_full, tile_empty, ring_full[kCRing], ring_empty[kCRing];
     __shared__ uint64_t w_full[2], w_empty[2], a_full[2], a_empty[2], dq_full, dq_empty, fin;
     __shared__ uint32_t tmem_base;
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (threadIdx.x == 32) {
         abort_flag = 0;
         mbar_init(&tile_full, 1);
-        mbar_init(&tile_empty, 1 + 128);  // the tile's last MMA reading Q, K, V, dY + every worker has its rows
+        mbar_init(&tile_empty, 1 + 128);  // the tile's last MMA reading Q, dY + every worker has its rows
         for (int s = 0; s < kCRing; ++s) {
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
@@ -307,29 +308,35 @@ __global__ void __launch_bounds__(kCThreads, 1)
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
             prefetch_tensormap(&mY);
-            uint32_t gr = 0;
+            uint32_t gr = 0;  // ring items
             bool ok = true;
             for (int j = 0; j < my_tiles && ok; ++j) {
                 int bh, n, c;
                 tile(j, bh, n, c);
                 if (!(ok = mbar_wait(&tile_empty, (j & 1) ^ 1, &abort_flag))) break;
                 const int row = bh * a.L + n * a.C + c * kGT;
-                mbar_arrive_expect_tx(&tile_full, 4 * kGTile);
-                const CUtensorMap *maps[4] = {&mQ, &mK, &mV, &mY};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    tma_load_2d(sm + m * kGTile, maps[m], 0, row, &tile_full);
-                    tma_load_2d(sm + m * kGTile + 16384, maps[m], 64, row, &tile_full);
-                }
+                mbar_arrive_expect_tx(&tile_full, 2 * kGTile);
+                tma_load_2d(sQ, &mQ, 0, row, &tile_full);
+                tma_load_2d(sQ + 16384, &mQ, 64, row, &tile_full);
+                tma_load_2d(sY, &mY, 0, row, &tile_full);
+                tma_load_2d(sY + 16384, &mY, 64, row, &tile_full);
+                // ring items: K, V, then the prefix state (chunk c > 0) and the cached states
                 const int nimg = (c > 0 ? 1 : 0) + n;
-                for (int m = 0; m < nimg && ok; ++m, ++gr) {
+                for (int m = -2; m < nimg && ok; ++m, ++gr) {
                     const int s = gr % kCRing;
+                    if (!(ok = mbar_wait(&ring_empty[s], ((gr / kCRing) & 1) ^ 1, &abort_flag))) break;
+                    mbar_arrive_expect_tx(&ring_full[s], kGTile);
+                    uint8_t *dst = ring + s * kGTile;
+                    if (m < 0) {
+                        const CUtensorMap *map = m == -2 ? &mK : &mV;
+                        tma_load_2d(dst, map, 0, row, &ring_full[s]);
+                        tma_load_2d(dst + 16384, map, 64, row, &ring_full[s]);
+                        continue;
+                    }
                     const uint8_t *src = (c > 0 && m == 0)
                                              ? a.spre + (((size_t)bh * a.N + n) * a.CPS + c) * kGTile
                                              : a.images + ((size_t)bh * a.N + (m - (c > 0 ? 1 : 0))) * kGTile;
-                    if (!(ok = mbar_wait(&ring_empty[s], ((gr / kCRing) & 1) ^ 1, &abort_flag))) break;
-                    mbar_arrive_expect_tx(&ring_full[s], kGTile);
-                    bulk_load(ring + s * kGTile, src, kGTile, &ring_full[s]);
+                    bulk_load(dst, src, kGTile, &ring_full[s]);
                 }
             }
             // leave no copy in flight: the last use of every slot has landed
@@ -346,14 +353,21 @@ __global__ void __launch_bounds__(kCThreads, 1)
             constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);   // B MN-major
             uint32_t gw = 0, ga = 0, gr = 0;
             bool ok = true;
-            const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), y0 = smem_u32(sY);
+            const uint32_t q0 = smem_u32(sQ), y0 = smem_u32(sY);
             const uint32_t r0 = smem_u32(ring);
             auto kmaj = [](int kk) { return (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32); };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 int bh, n, c;
                 tile(j, bh, n, c);
                 const int nimg = (c > 0 ? 1 : 0) + n;
-                if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
+                // K and V: the tile's first two ring items
+                const uint32_t sk = gr % kCRing, sv = (gr + 1) % kCRing;
+                const uint32_t k0 = r0 + sk * kGTile, v0 = r0 + sv * kGTile;
+                if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag) &&
+                           mbar_wait(&ring_full[sk], (gr / kCRing) & 1, &abort_flag) &&
+                           mbar_wait(&ring_full[sv], ((gr + 1) / kCRing) & 1, &abort_flag)))
+                    break;
+                gr += 2;
                 // G1 = Q K^T, G2 = dY V^T into the two W buffers
                 const uint32_t w1 = gw % 2, w2 = (gw + 1) % 2;
                 if (!(ok = mbar_wait(&w_empty[w1], ((gw / 2) & 1) ^ 1, &abort_flag) &&
@@ -370,6 +384,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     mma_ss(tW0 + w2 * 128, make_desc_sw128(y0 + kmaj(kk), 0, 1024), make_desc_sw128(v0 + kmaj(kk), 0, 1024),
                            idKK, kk > 0);
                 mma_commit(&w_full[w2]);
+                mma_commit(&ring_empty[sv]);  // V is spent
                 gw += 2;
                 // D_q = P2 K once the workers have written P2
                 if (!(ok = mbar_wait(&a_full[ga % 2], (ga / 2) & 1, &abort_flag) &&
@@ -380,6 +395,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tDq, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(k0 + kk * 2048u, 16384, 1024), idKM, kk > 0);
                 mma_commit(&a_empty[ga % 2]);
+                mma_commit(&ring_empty[sk]);  // K is spent
                 ++ga;
                 if (nimg == 0) mma_commit(&tile_empty);
                 for (int m = 0; m < nimg && ok; ++m, ++gw, ++ga, ++gr) {
@@ -498,27 +514,37 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     yp[32 * h + 4 * cc + 2] = xy.z; yp[32 * h + 4 * cc + 3] = xy.w;
                 }
             mbar_arrive(&tile_empty);
-            // the prefix state (gate g_on) and the cached states (gate g_{t,i})
+            // the prefix state (gate g_on) and the cached states (gate g_{t,i}): A(m + 1) = g o dy is
+            // written before the dot with W(m), so the tensor cores never wait for the dot; the gates
+            // are fetched two states ahead
             const float *grow = routed ? a.gam + (size_t)bh * a.N * a.L + t : nullptr;
             float *dgrow = a.dg + (size_t)bh * a.N * a.L + t;
             const float gconst = a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
+            const int i0 = c > 0 ? -1 : 0;  // state index of item m is i0 + m (-1: the prefix state)
+            auto gate = [&](int m) {
+                const int i = i0 + m;
+                return i < 0 ? gon : (routed ? __ldg(grow + (size_t)i * a.L) : gconst);
+            };
+            float g_next = nimg > 1 ? gate(1) : 0.f;
+            if (nimg > 0 && !(ok = put_a(yp, gate(0)))) break;
             for (int m = 0; m < nimg && ok; ++m) {
-                const bool prefix = c > 0 && m == 0;
-                const int i = m - (c > 0 ? 1 : 0);
-                const float g = prefix ? gon : (routed ? __ldg(grow + (size_t)i * a.L) : gconst);
-                if (!(ok = put_a(yp, g))) break;
+                if (m + 1 < nimg) {
+                    const float g = g_next;
+                    if (m + 2 < nimg) g_next = gate(m + 2);
+                    if (!(ok = put_a(yp, g))) break;
+                }
                 const uint32_t w = gw % 2;
                 if (!(ok = mbar_wait(&w_full[w], (gw / 2) & 1, &abort_flag))) break;
                 tc_fence_after();
                 float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                for (int mm = 0; mm < 8; ++mm) {
-                    uint32_t x[16];
-                    tmem_ld16(tW0 + w * 128 + lane_base + 16 * mm, x);
+                for (int h = 0; h < 4; ++h) {  // 32 columns per wait
+                    uint32_t x[32];
+                    tmem_ld32(tW0 + w * 128 + lane_base + 32 * h, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t qq = qp[8 * mm + k];
+                    for (int k = 0; k < 16; ++k) {
+                        const uint32_t qq = qp[16 * h + k];
                         d0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), d0);
                         d1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), d1);
                     }
@@ -526,8 +552,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&w_empty[w]);
                 ++gw;
-                if (prefix) dgon += d0 + d1;
-                else dgrow[(size_t)i * a.L] = d0 + d1;
+                if (i0 + m < 0) dgon += d0 + d1;
+                else dgrow[(size_t)(i0 + m) * a.L] = d0 + d1;
             }
             if (!ok) break;
             a.dgon[(size_t)bh * a.L + t] = dgon;
