@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
     }
     __syncthreads();
 
-    if (lane_on) {
+    if (lane_on && a.dq_in) {
         T *dqo = static_cast<T *>(a.dq) + base;
 #pragma unroll
         for (int j = 0; j < TPW; ++j) {
@@ -607,36 +607,6 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
         const int t = tid;
         a.kv_gw[tok0 + t] = gon[t];
         a.kv_gw[(size_t)a.BH * a.L + tok0 + t] = gated ? gon[t] * (dgo[t] - dl[t]) / (float)(tb + t - t0 + 1) : 0.f;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// bwd_kpre_simt: for every segment, the sum of its keys before each 64-token tile
-// (the pooled key of the online memory needs it); one CTA of D threads per (bh,
-// segment), a thread per dimension walking the segment, four tokens in flight.
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(D) bwd_kpre_simt(BwdArgs a)
-{
-    const int n = (int)blockIdx.x % a.N, bh = (int)blockIdx.x / a.N;
-    const int t0 = n * a.C, t1 = min(t0 + a.C, a.L);
-    const int tps = (a.C + kTB - 1) / kTB;
-    const T *k = static_cast<const T *>(a.k) + (size_t)bh * a.L * D + threadIdx.x;
-    float *out = a.kpre_tiles + ((size_t)bh * a.N + n) * tps * D + threadIdx.x;
-    float s = 0.f;
-    for (int tile = 0; tile < tps; ++tile) {
-        out[(size_t)tile * D] = s;
-        const int tb = t0 + tile * kTB, te = min(tb + kTB, t1);
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        int t = tb;
-        for (; t + 3 < te; t += 4) {
-            s0 += to_f(k[(size_t)t * D]);
-            s1 += to_f(k[(size_t)(t + 1) * D]);
-            s2 += to_f(k[(size_t)(t + 2) * D]);
-            s3 += to_f(k[(size_t)(t + 3) * D]);
-        }
-        for (; t < te; ++t) s0 += to_f(k[(size_t)t * D]);
-        s += (s0 + s1) + (s2 + s3);
     }
 }
 
@@ -1035,11 +1005,6 @@ template <typename T, int D>
 cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
 {
     cudaError_t e;
-    if (a.kpre_tiles) {
-        bwd_kpre_simt<T, D><<<(unsigned)((long long)p.BH * p.N), D, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        profile_after_kernel(s, "bwd_kpre_simt");
-    }
     const long long tps = (p.C + kTB - 1) / kTB;
     bwd_route_simt<T, D><<<(unsigned)((long long)p.BH * p.N * tps), kThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1140,15 +1105,12 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         float *gam = gated ? reinterpret_cast<float *>(take(4 * BH * L * N)) : nullptr;
         a.kpre_tiles = gated ? reinterpret_cast<float *>(take(4 * BH * N * ((p.C + kTB - 1) / kTB) * d)) : nullptr;
         a.kv_gw = reinterpret_cast<float *>(take(8 * BH * L));
+        f.kpre_tiles = a.kpre_tiles;  // the state kernel writes the key means and the tile key prefixes
         void *state_scratch = take(tc_state_scratch_bytes(p));
         void *cached_scratch = take(bwd_cached_scratch_bytes(p));
         TcImages img{};
         if ((e = launch_state_tc(p, f, state_scratch, &img, s)) != cudaSuccess) return e;
         profile_after_kernel(s, "seg_state_tc");
-        if (gated) {
-            if ((e = launch_kbar_simt(p, f, s)) != cudaSuccess) return e;
-            profile_after_kernel(s, "kbar_simt");
-        }
         if ((e = cudaMemsetAsync(dkbar, 0, 4 * BH * N * d, s)) != cudaSuccess) return e;
         a.r_on = img.r_on;
         a.gam = gam;
@@ -1156,13 +1118,13 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
             if ((e = launch_bwd_gates_tc(p, u, img, gam, tok, s)) != cudaSuccess) return e;
             profile_after_kernel(s, "gate_tiles_tc");
         }
-        float *dg = nullptr, *dgon = nullptr, *dqf = nullptr;
-        if ((e = launch_bwd_cached_tc(p, q, k, v, dy, img, gam, tok, cached_scratch, &dg, &dgon, &dqf, s)) != cudaSuccess)
+        float *dg = nullptr, *dgon = nullptr;
+        if ((e = launch_bwd_cached_tc(p, q, k, v, dy, img, gam, tok, dq, cached_scratch, &dg, &dgon, s)) != cudaSuccess)
             return e;
         profile_after_kernel(s, "bwd_cached_tc");
         a.dg_in = dg;
         a.dgon_in = dgon;
-        a.dq_in = dqf;
+        a.dq_in = nullptr;  // dq is written whole by the cached pass
         a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
         return launch_bwd_tc_rest(p, a, s);
     }

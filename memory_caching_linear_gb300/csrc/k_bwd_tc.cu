@@ -246,7 +246,7 @@ struct CArgs {
     const float *tok;       // [BH][L][kBwdTokWords]: word 2 is the online gate (routed aggregations)
     float *dg;              // [BH][N][L] out: dy_t . M^(i) q_t
     float *dgon;            // [BH][L] out: dy_t . M_t q_t
-    float *dq;              // [BH][L][d] out: dq (fp32)
+    __nv_bfloat16 *dq;      // [BH][L][d] out: dq
     int BH, L, C, N, CPS, d, mode, num_tiles;
 };
 
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
             // drain D_q
             if (!(ok = mbar_wait(&dq_full, j & 1, &abort_flag))) break;
             tc_fence_after();
-            float *dqrow = a.dq + ((size_t)bh * a.L + t) * a.d;
+            __nv_bfloat16 *dqrow = a.dq + ((size_t)bh * a.L + t) * a.d;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 uint32_t x[32];
@@ -568,10 +568,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
                 tmem_wait_ld();
                 if (32 * m < a.d) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4 *>(dqrow + 32 * m + k) =
-                            make_float4(__uint_as_float(x[k]), __uint_as_float(x[k + 1]), __uint_as_float(x[k + 2]),
-                                        __uint_as_float(x[k + 3]));
+                    for (int k = 0; k < 32; k += 8)
+                        *reinterpret_cast<uint4 *>(dqrow + 32 * m + k) = make_uint4(
+                            pack_bf16x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])),
+                            pack_bf16x2(__uint_as_float(x[k + 2]), __uint_as_float(x[k + 3])),
+                            pack_bf16x2(__uint_as_float(x[k + 4]), __uint_as_float(x[k + 5])),
+                            pack_bf16x2(__uint_as_float(x[k + 6]), __uint_as_float(x[k + 7])));
                 }
             }
             tc_fence_before();
@@ -1010,21 +1012,19 @@ size_t bwd_cached_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    return pad(4 * BH * N * L) + pad(4 * BH * L) + pad(4 * BH * L * d);
+    return pad(4 * BH * N * L) + pad(4 * BH * L);
 }
 
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
-                                 const TcImages &img, const float *gam, const float *tok, void *scratch,
-                                 float **dg_out, float **dgon_out, float **dq_out, cudaStream_t s)
+                                 const TcImages &img, const float *gam, const float *tok, void *dq, void *scratch,
+                                 float **dg_out, float **dgon_out, cudaStream_t s)
 {
     const size_t BH = p.BH, N = p.N, L = p.L;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
     float *dg = static_cast<float *>(scratch);
     float *dgon = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(4 * BH * N * L));
-    float *dq = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dgon) + pad(4 * BH * L));
     *dg_out = dg;
     *dgon_out = dgon;
-    *dq_out = dq;
     CUtensorMap mQ, mK, mV, mY;
     const unsigned long long rows = (unsigned long long)BH * L;
     if (!make_tmap_bf16_sw128(&mQ, q, rows, p.d, kGT) || !make_tmap_bf16_sw128(&mK, k, rows, p.d, kGT) ||
@@ -1037,7 +1037,7 @@ cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k,
     a.tok = tok;
     a.dg = dg;
     a.dgon = dgon;
-    a.dq = dq;
+    a.dq = static_cast<__nv_bfloat16 *>(dq);
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kGT; a.d = p.d; a.mode = p.mode;
     a.num_tiles = p.BH * p.N * a.CPS;
     cudaError_t e = cudaFuncSetAttribute(bwd_cached_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCSmem);

@@ -70,6 +70,8 @@ struct TcArgs {
     float *r_on;          // [BH][L]
     float *gam_out;       // backward gates: [BH][N][L] g_{t,i}, or null
     float *tok_out;       // backward gates: [BH][L][kBwdTokWords], word 2 = the online gate
+    float *kbar_out;      // backward: fp32 key means [BH][N][d], or null
+    float *kpre_out;      // backward: keys of the segment before each 64-token tile [BH][N][2 CPS][d], or null
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
     int topk;             // SSC: cached segments selected per token
     int mean;             // Mean aggregation: the Residual path with every weight 1 / (n + 1)
@@ -388,9 +390,17 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             }
             named_bar_sync(1, 128);  // every worker has read ksum_s and written its partials
             if (ok) {
-                float cs = 0.f;
+                float cs = 0.f, ch = 0.f;
 #pragma unroll
-                for (int g8 = 0; g8 < 8; ++g8) cs += red_s[g8][row];
+                for (int g8 = 0; g8 < 8; ++g8) {
+                    cs += red_s[g8][row];
+                    if (g8 == 3) ch = cs;  // the chunk's first 64 rows
+                }
+                if (GATED && a.kpre_out && (int)row < a.d) {  // keys before the chunk's two 64-token halves
+                    float *kp = a.kpre_out + (((size_t)bh * a.N + seg) * (2 * nch) + 2 * c) * a.d + row;
+                    kp[0] = ks;
+                    kp[a.d] = ks + ch;
+                }
                 ks += cs;
                 ksum_s[row] = ks;
             }
@@ -457,6 +467,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     }
                     if (GATED) {
                         const float kbv = ks / (float)a.C;
+                        if (a.kbar_out && (int)row < a.d) a.kbar_out[sidx * a.d + row] = kbv;
                         const __nv_bfloat16 hi = __float2bfloat16_rn(kbv);
                         const __nv_bfloat16 lo = __float2bfloat16_rn(kbv - __bfloat162float(hi));
                         uint8_t *kimg = a.kbar_img + (size_t)bh * kTile;
@@ -1349,6 +1360,8 @@ cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, 
     a.kbar_img = base;
     base += pad256(BH * kTile);
     a.r_on = reinterpret_cast<float *>(base);
+    a.kbar_out = gated ? fa.kbar : nullptr;
+    a.kpre_out = gated ? fa.kpre_tiles : nullptr;
     a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = (int)CPS; a.d = p.d;
     a.num_tiles = (int)(BH * N * CPS);
     CUtensorMap mK, mV, mU;

@@ -43,6 +43,7 @@ struct FwdArgs {
     int32_t *sel_out;           // [BH][L][topk] (ssc_select only)
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L]; all null = plain update
     const int32_t *seg_off;     // optional [N+1] segment boundaries (device); then C is the longest segment
+    float *kpre_tiles;          // backward state kernel only: keys before each 64-token tile [BH][N][C/64][d]
     int BH, L, C, N, mode, topk;
 };
 
@@ -119,7 +120,9 @@ size_t tc_select_scratch_bytes(const Problem &p);
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 // The forward's state kernel alone, for the tensor-core backward: images of the cached
 // states [BH][N] and of the chunks' prefix states [BH][N][C/128] (32 KB each, 128x128
-// bf16, two 64-column 128-byte-swizzled panels, row = value dim), and r_on [BH][L].
+// bf16, two 64-column 128-byte-swizzled panels, row = value dim), and r_on [BH][L];
+// routed aggregations also get the fp32 key means (fa.kbar) and the keys before each
+// 64-token tile (fa.kpre_tiles).
 struct TcImages {
     const uint8_t *states_img, *spre_img, *kbar_img;
     const float *r_on;
@@ -157,7 +160,7 @@ struct BwdArgs {
     float *sel_g;         // SSC: [BH][L][topk] their gates
     float *gam;           // [BH][N][L] gates of the cached segments, for the tensor-core G (routed modes), or null
     const float *dg_in;   // [BH][N][L] dy_t . M^(i) q_t from the tensor cores, or null (computed here)
-    const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null
+    const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null (written already)
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
     float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
@@ -173,9 +176,10 @@ cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, con
 cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
                              const uint8_t *G, const float *gw, const float *dkbar, void *dk, void *dv, cudaStream_t s);
 size_t bwd_cached_scratch_bytes(const Problem &p);
+// dq (bf16 [BH][L][d]) is written whole; dg and dg_on go to scratch.
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
-                                 const TcImages &img, const float *gam, const float *tok, void *scratch,
-                                 float **dg_out, float **dgon_out, float **dq_out, cudaStream_t s);
+                                 const TcImages &img, const float *gam, const float *tok, void *dq, void *scratch,
+                                 float **dg_out, float **dgon_out, cudaStream_t s);
 cudaError_t take_bwd_abort(int *was_set);
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
                                  const void *dy, void *dq, void *dk, void *dv, void *du, void *scratch,
