@@ -27,6 +27,10 @@ constexpr int kThreads = 256;
 //                                                                [MC-ja §3.1 eq. 10]
 //   S += sum_j v_j k_j^T,  ksum += sum_j k_j
 // At the end S is the segment's cached state and ksum / len its key mean.
+// With a piece table (FwdArgs::seg_pieces) one CTA takes one piece of piece_len
+// tokens: it starts from zero, so for the second and later pieces of a segment
+// O_on and r_on miss the part of the state and key sum before the piece, which
+// seg_fix_simt adds after seg_prefix_simt has formed those prefixes.
 // Thread layout: tx = tid % 16, ty = tid / 16; a thread owns state entries
 // (ty + 16 i, tx + 16 j) and output entries (token ty + 16 p, dim tx + 16 r).
 // ---------------------------------------------------------------------------
@@ -47,10 +51,16 @@ __global__ void __launch_bounds__(kThreads) seg_scan_simt(FwdArgs a)
     float *Bs = As + TC * TP; // TC x TP, masked u.k
     float *ksum = Bs + TC * TP;
 
-    const int seg = blockIdx.x % a.N;
-    const int bh = blockIdx.x / a.N;
-    const int t0 = seg_begin(a, seg);
-    const int t1 = seg_end(a, seg);
+    const bool split = a.seg_pieces != nullptr;
+    const int unit = split ? a.npieces : a.N;
+    const int bh = blockIdx.x / unit;
+    const int pi = blockIdx.x % unit;  // the piece (split) or the segment
+    const int seg = split ? a.piece_seg[pi] : pi;
+    const int ts = seg_begin(a, seg), te = seg_end(a, seg);  // the segment
+    const int pidx = split ? pi - a.seg_pieces[seg] : 0;
+    const int t0 = split ? ts + pidx * a.piece_len : ts;    // this CTA's tokens [t0, t1)
+    const int t1 = split ? min(t0 + a.piece_len, te) : te;
+    const bool whole = !split || a.seg_pieces[seg + 1] - a.seg_pieces[seg] == 1;
     const size_t base = (size_t)bh * a.L * D;
     const T *q = static_cast<const T *>(a.q) + base;
     const T *k = static_cast<const T *>(a.k) + base;
@@ -136,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) seg_scan_simt(FwdArgs a)
             float acc = 0.f;
             for (int c = 0; c < D; ++c) acc = fmaf(Us[t * P + c], ksum[c], acc);
             for (int j = 0; j <= t; ++j) acc += Bs[t * TP + j];
-            r_on[c0 + t] = acc / (float)(c0 + t - t0 + 1);
+            r_on[c0 + t] = acc / (float)(c0 + t - ts + 1);
         }
         __syncthreads();  // Ss and ksum are read above and rewritten below
         for (int j = 0; j < cnt; ++j) {
@@ -161,12 +171,115 @@ __global__ void __launch_bounds__(kThreads) seg_scan_simt(FwdArgs a)
         }
     }
     __syncthreads();
-    float *st = a.states + ((size_t)bh * a.N + seg) * D * D;
+    float *st = whole ? a.states + ((size_t)bh * a.N + seg) * D * D : a.piece_state + ((size_t)bh * a.npieces + pi) * D * D;
 #pragma unroll
     for (int i = 0; i < RB; ++i)
 #pragma unroll
         for (int jj = 0; jj < RB; ++jj) st[(size_t)(ty + 16 * i) * D + tx + 16 * jj] = S[i][jj];
-    if (tid < D) a.kbar[((size_t)bh * a.N + seg) * D + tid] = ksum[tid] / (float)(t1 - t0);
+    if (tid < D) {
+        if (whole) a.kbar[((size_t)bh * a.N + seg) * D + tid] = ksum[tid] / (float)(t1 - t0);
+        else a.piece_ksum[((size_t)bh * a.npieces + pi) * D + tid] = ksum[tid];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// seg_prefix_simt: for every segment of more than one piece, a thread per state
+// entry (and per key column) walks the pieces in order, replacing each piece's own
+// sum by the sum of the pieces before it, and writes the total as the segment's
+// cached state (and key mean).  Grid: (bh, segment) x ceil((D*D + D) / 256).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads) seg_prefix_simt(FwdArgs a)
+{
+    const int bh = blockIdx.x / a.N, seg = blockIdx.x % a.N;
+    const int p0 = a.seg_pieces[seg], p1 = a.seg_pieces[seg + 1];
+    if (p1 - p0 < 2) return;
+    const int e = blockIdx.y * kThreads + threadIdx.x;
+    if (e >= D * D + D) return;
+    const bool key = e >= D * D;
+    float *x = key ? a.piece_ksum + ((size_t)bh * a.npieces + p0) * D + (e - D * D)
+                   : a.piece_state + ((size_t)bh * a.npieces + p0) * D * D + e;
+    const size_t stride = key ? D : (size_t)D * D;
+    float s = 0.f;
+    for (int p = p0; p < p1; ++p, x += stride) {
+        const float own = *x;
+        *x = s;
+        s += own;
+    }
+    if (key) a.kbar[((size_t)bh * a.N + seg) * D + (e - D * D)] = s / (float)(seg_end(a, seg) - seg_begin(a, seg));
+    else a.states[((size_t)bh * a.N + seg) * D * D + e] = s;
+}
+
+// ---------------------------------------------------------------------------
+// seg_fix_simt: one CTA per (bh, piece) after the first of its segment: adds the
+// state before the piece to the online reads, O_on[t] += S_pre q_t, and the keys
+// before it to the online scores, r_on[t] += <u_t, ksum_pre> / (t - ts + 1).
+// S_pre sits in shared memory; tokens go in tiles of 64 (the scan's thread layout).
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) seg_fix_simt(FwdArgs a)
+{
+    constexpr int P = D + 1;
+    constexpr int RB = D / 16;
+    constexpr int TF = 64;
+    constexpr int TPT = TF / 16;
+    extern __shared__ float sm[];
+    float *Ss = sm;           // D x P
+    float *Qs = Ss + D * P;   // TF x P
+    float *kp = Qs + TF * P;  // D
+    const int bh = blockIdx.x / a.npieces, pi = blockIdx.x % a.npieces;
+    const int seg = a.piece_seg[pi];
+    const int pidx = pi - a.seg_pieces[seg];
+    if (pidx == 0) return;
+    const int ts = seg_begin(a, seg);
+    const int t0 = ts + pidx * a.piece_len, t1 = min(t0 + a.piece_len, seg_end(a, seg));
+    const size_t base = (size_t)bh * a.L * D;
+    const T *q = static_cast<const T *>(a.q) + base;
+    const T *u = a.u ? static_cast<const T *>(a.u) + base : nullptr;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const float *sp = a.piece_state + ((size_t)bh * a.npieces + pi) * D * D;
+    for (int e = tid; e < D * D; e += kThreads) Ss[(e / D) * P + e % D] = sp[e];
+    for (int e = tid; e < D; e += kThreads) kp[e] = a.piece_ksum[((size_t)bh * a.npieces + pi) * D + e];
+    for (int c0 = t0; c0 < t1; c0 += TF) {
+        const int cnt = min(TF, t1 - c0);
+        __syncthreads();
+        for (int e = tid; e < TF * D; e += kThreads) {
+            const int r = e / D, c = e % D;
+            Qs[r * P + c] = r < cnt ? to_f(q[(size_t)(c0 + r) * D + c]) : 0.f;
+        }
+        __syncthreads();
+        float o[TPT][RB];
+#pragma unroll
+        for (int p = 0; p < TPT; ++p)
+#pragma unroll
+            for (int r = 0; r < RB; ++r) o[p][r] = 0.f;
+        for (int c = 0; c < D; ++c) {
+            float qv[TPT];
+#pragma unroll
+            for (int p = 0; p < TPT; ++p) qv[p] = Qs[(ty + 16 * p) * P + c];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const float s = Ss[(tx + 16 * r) * P + c];
+#pragma unroll
+                for (int p = 0; p < TPT; ++p) o[p][r] = fmaf(qv[p], s, o[p][r]);
+            }
+        }
+        float *O_on = a.O_on + base;
+#pragma unroll
+        for (int p = 0; p < TPT; ++p) {
+            const int t = ty + 16 * p;
+            if (t < cnt) {
+#pragma unroll
+                for (int r = 0; r < RB; ++r) O_on[(size_t)(c0 + t) * D + tx + 16 * r] += o[p][r];
+            }
+        }
+        if (u != nullptr && tid < cnt) {
+            const int t = tid;
+            float acc = 0.f;
+            for (int c = 0; c < D; ++c) acc = fmaf(to_f(u[(size_t)(c0 + t) * D + c]), kp[c], acc);
+            a.r_on[(size_t)bh * a.L + c0 + t] += acc / (float)(c0 + t - ts + 1);
+        }
+    }
 }
 
 // Key means alone (for the stand-alone router): the same sequential fp32 sum
@@ -434,8 +547,20 @@ cudaError_t seg_scan_impl(const Problem &p, const FwdArgs &a, cudaStream_t s)
     auto kern = seg_scan_simt<T, D, TC>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    const long long blocks = (long long)p.BH * p.N;
-    kern<<<(unsigned)blocks, kThreads, smem, s>>>(a);
+    if (!a.seg_pieces) {
+        kern<<<(unsigned)((long long)p.BH * p.N), kThreads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+    // long segments in pieces: every piece at once, then the prefixes over each segment's pieces
+    kern<<<(unsigned)((long long)p.BH * a.npieces), kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    seg_prefix_simt<D><<<dim3((unsigned)((long long)p.BH * p.N), (unsigned)((D * D + D + kThreads - 1) / kThreads)),
+                         kThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    constexpr size_t fsmem = sizeof(float) * (D * P + 64 * P + D);
+    auto fix = seg_fix_simt<T, D>;
+    if ((e = set_smem(fix, fsmem)) != cudaSuccess) return e;
+    fix<<<(unsigned)((long long)p.BH * a.npieces), kThreads, fsmem, s>>>(a);
     return cudaGetLastError();
 }
 

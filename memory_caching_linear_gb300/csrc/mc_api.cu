@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "mc_internal.cuh"
 
@@ -254,16 +255,42 @@ int forward_segments(const void *q, const void *k, const void *v, const void *u,
     }
     st = check_device();
     if (st != MC_OK) return st;
+    // Segments longer than kPieceLen tokens are scanned in pieces (all at once, then a
+    // prefix over each segment's pieces): boundaries, then the first piece of every
+    // segment, then the segment of every piece, in one host table.
+    std::vector<int32_t> table(seg_off, seg_off + nseg + 1);
+    int npieces = 0;
+    if (maxlen > kPieceLen) {
+        table.resize((size_t)2 * (nseg + 1));
+        for (int n = 0; n < nseg; ++n) {
+            table[(size_t)nseg + 1 + n] = npieces;
+            npieces += (seg_off[n + 1] - seg_off[n] + kPieceLen - 1) / kPieceLen;
+        }
+        table[(size_t)2 * nseg + 1] = npieces;
+        for (int n = 0; n < nseg; ++n)
+            for (int i = table[(size_t)nseg + 1 + n]; i < table[(size_t)nseg + 2 + n]; ++i) table.push_back(n);
+    }
     const ScratchPlan plan = plan_scratch(p, states == nullptr);
-    const size_t off_bytes = round_up(sizeof(int32_t) * (size_t)(nseg + 1));
+    const size_t off_bytes = round_up(sizeof(int32_t) * table.size());
+    const size_t piece_bytes = round_up(sizeof(float) * (size_t)p.BH * npieces * d * d) +
+                               round_up(sizeof(float) * (size_t)p.BH * npieces * d);
     void *scratch = nullptr;
-    if (scratch_alloc(&scratch, plan.total + off_bytes, stream) != cudaSuccess) {
+    if (scratch_alloc(&scratch, plan.total + off_bytes + piece_bytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_ALLOC;
     }
     char *base = static_cast<char *>(scratch);
     int32_t *doff = reinterpret_cast<int32_t *>(base + plan.total);
     FwdArgs a{};
+    if (npieces > 0) {
+        a.seg_pieces = doff + nseg + 1;
+        a.piece_seg = doff + 2 * (nseg + 1);
+        a.npieces = npieces;
+        a.piece_len = kPieceLen;
+        a.piece_state = reinterpret_cast<float *>(base + plan.total + off_bytes);
+        a.piece_ksum = reinterpret_cast<float *>(base + plan.total + off_bytes +
+                                                 round_up(sizeof(float) * (size_t)p.BH * npieces * d * d));
+    }
     a.q = q; a.k = k; a.v = v;
     a.u = mode_uses_u(p.mode) ? u : nullptr;
     a.y = y;
@@ -273,7 +300,7 @@ int forward_segments(const void *q, const void *k, const void *v, const void *u,
     a.kbar = reinterpret_cast<float *>(base + plan.off_kbar);
     a.seg_off = doff;
     a.BH = p.BH; a.L = L; a.C = maxlen; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
-    cudaError_t e = cudaMemcpyAsync(doff, seg_off, sizeof(int32_t) * (size_t)(nseg + 1), cudaMemcpyHostToDevice, stream);
+    cudaError_t e = cudaMemcpyAsync(doff, table.data(), sizeof(int32_t) * table.size(), cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) {
         profile_call_start(stream);
         e = launch_seg_scan_simt(p, a, stream);

@@ -21,6 +21,7 @@
 namespace mc {
 
 constexpr int kMaxTopk = 64;  // SSC selections kept per token on the device
+constexpr int kPieceLen = 512;  // tokens per piece when the FFMA scan splits a long segment
 
 // Aggregations whose gates come from the router <u_t, pooled keys>; Residual and
 // Mean weigh every memory the same and never read u.
@@ -44,6 +45,13 @@ struct FwdArgs {
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L]; all null = plain update
     const int32_t *seg_off;     // optional [N+1] segment boundaries (device); then C is the longest segment
     float *kpre_tiles;          // backward state kernel only: keys before each 64-token tile [BH][N][C/64][d]
+    // Optional split of long segments for the FFMA scan (null: one CTA walks a whole segment).
+    // Segment n is pieces [seg_pieces[n], seg_pieces[n+1]) of piece_len tokens (the last ragged).
+    const int32_t *seg_pieces;  // [N+1] first piece of each segment (device)
+    const int32_t *piece_seg;   // [npieces] segment of each piece (device)
+    int npieces, piece_len;
+    float *piece_state;         // [BH][npieces][d][d] scratch: a piece's own state, then the state before it
+    float *piece_ksum;          // [BH][npieces][d] scratch: the same for the key sums
     int BH, L, C, N, mode, topk;
 };
 

@@ -37,6 +37,9 @@ CASES = [
     ("log-4095-d64", 1, 1, 4095, 64, "bf16", None),
     ("custom-f32", 2, 1, 300, 16, "f32", [0, 7, 8, 100, 260, 300]),
     ("one-seg", 1, 1, 256, 64, "f32", [0, 256]),
+    # segments longer than the scan's 512-token pieces: ragged last pieces, a one-token segment between
+    ("pieces-ragged-f32", 1, 2, 2600, 32, "f32", [0, 1300, 1301, 2600]),
+    ("pieces-d128-bf16", 1, 1, 2048, 128, "bf16", [0, 1536, 2048]),
 ]
 
 
