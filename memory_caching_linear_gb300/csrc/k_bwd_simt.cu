@@ -493,16 +493,17 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
     const bool lane_on = c0 < D;
     const int tw = warp * TPW;  // the warp's first token of the tile
 
-    for (int e = tid; e < kTB * n; e += kThreads) {
+#pragma unroll 4
+    for (int e = tid; e < kTB * n; e += kThreads) {  // unrolled: several rows' loads in flight per thread
         const int i = e / kTB, t = e % kTB;
         const size_t gi = seg_base + (size_t)i * a.L + t;
         gt[e] = t < cnt ? (gated ? a.gam[gi] : gconst) : 0.f;
-        dt[e] = t < cnt ? a.dg_in[gi] : 0.f;
+        dt[e] = t < cnt ? a.dg_in[gi] + (a.dg_in2 ? a.dg_in2[gi] : 0.f) : 0.f;
     }
     if (tid < kTB) {
         const int t = tid;
         gon[t] = t < cnt ? (gated ? a.tok[(tok0 + t) * kBwdTokWords + 2] : gconst) : 0.f;
-        dgo[t] = t < cnt ? a.dgon_in[tok0 + t] : 0.f;
+        dgo[t] = t < cnt ? a.dgon_in[tok0 + t] + (a.dgon_in2 ? a.dgon_in2[tok0 + t] : 0.f) : 0.f;
     }
     // the key sums of each warp's tokens (the pooled key of the online memory)
     if (gated) {
@@ -540,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
     }
     __syncthreads();
     // dr = g (dg - delta), in place, and out for the key-mean gradient
+#pragma unroll 4
     for (int e = tid; e < kTB * n; e += kThreads) {
         const int t = e % kTB;
         const float dr = gt[e] * (dt[e] - dl[t]);
@@ -1124,6 +1126,8 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         profile_after_kernel(s, "bwd_cached_tc");
         a.dg_in = dg;
         a.dgon_in = dgon;
+        a.dg_in2 = dg + BH * N * L;  // the cached pass's second column half
+        a.dgon_in2 = dgon + BH * L;
         a.dq_in = nullptr;  // dq is written whole by the cached pass
         a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
         return launch_bwd_tc_rest(p, a, s);

@@ -225,18 +225,24 @@ __global__ void __launch_bounds__(kGThreads, 1)
 //     dq_t    += g_on (S_pre^T dy_t + sum_{j<=t} k_j (v_j . dy_t))
 //   every cached M^(i), i < n (gate g_{t,i}):
 //     dg_{t,i} = q_t . (M^(i)^T dy_t),   dq_t += g_{t,i} M^(i)^T dy_t
-// On the tensor cores: G1 = Q K^T and G2 = dY V^T (SS); P2 = g_on mask(G2) -> D_q = P2 K
-// (TS); then for the prefix state and each cached state X: W = dY X (SS, the image
-// read MN-major) for the dot with q, and D_q += (g o dY) X^T (TS, the same image).
+// On the tensor cores: G1 = Q K^T and G2 = dY V^T (SS); P2 = g_on mask(G2) -> P2 K
+// (TS), which starts the workers' dq; then for the prefix state and each cached state
+// X: W = dY X (SS, the image read MN-major), whose row t is M^T dy_t: the workers take
+// dg = q . W and, since the gate is a per-row scalar, dq += g W in fp32 registers
+// (one product per state).  Every product lands in one of kCW rotating TMEM buffers.
 // Persistent, one CTA per SM, tiles with the most cached segments first.  Warp 0
 // loads Q and dY of the tile (TMA, resident while the tile runs) and streams K, V
 // and one 32 KB image per state through a four-slot ring (K and V are read by the
-// tile's first three products only); warp 1 issues; warps 2-5 own a token row each.
-// TMEM: D_q [0,128) | W0 [128,256) | W1 [256,384) (G1 / G2 at a tile's start) |
-//       A0 [384,448) | A1 [448,512).
+// tile's first three products only); warp 1 issues; eight worker warps, two per TMEM
+// lane quadrant: warp half h owns the token rows of its quadrant and the columns
+// [64h, 64h+64) (q, dy, W, D_q) and the TMEM A columns [32h, 32h+32); the two halves'
+// partial dots go to two dg buffers, which the route kernel adds.
+// TMEM: W0 [0,128) | W1 [128,256) | W2 [256,384) | A0 [384,448) | A1 [448,512).
 // ============================================================================
-constexpr int kCRing = 4;
-constexpr int kCThreads = 192;
+constexpr int kCRing = 5;
+constexpr int kCW = 3;  // TMEM product buffers
+constexpr int kCWorkers = 256;
+constexpr int kCThreads = 64 + kCWorkers;
 constexpr size_t kCSmem = 2 * kGTile + kCRing * kGTile + 1024;
 
 struct CArgs {
@@ -244,8 +250,8 @@ struct CArgs {
     const uint8_t *spre;    // [BH][N][CPS] x 32 KB prefix-state images (chunk c > 0)
     const float *gam;       // [BH][N][L] gates of the cached segments (routed aggregations)
     const float *tok;       // [BH][L][kBwdTokWords]: word 2 is the online gate (routed aggregations)
-    float *dg;              // [BH][N][L] out: dy_t . M^(i) q_t
-    float *dgon;            // [BH][L] out: dy_t . M_t q_t
+    float *dg;              // 2 x [BH][N][L] out: dy_t . M^(i) q_t, summed over each column half
+    float *dgon;            // 2 x [BH][L] out: dy_t . M_t q_t, the same
     __nv_bfloat16 *dq;      // [BH][L][d] out: dq
     int BH, L, C, N, CPS, d, mode, num_tiles;
 };
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sQ = sm, *sY = sm + kGTile, *ring = sm + 2 * kGTile;
     __shared__ uint64_t tile_full, tile_empty, ring_full[kCRing], ring_empty[kCRing];
-    __shared__ uint64_t w_full[2], w_empty[2], a_full[2], a_empty[2], dq_full, dq_empty, fin;
+    __shared__ uint64_t w_full[kCW], w_empty[kCW], a_full[2], a_empty[2], fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -279,19 +285,19 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (threadIdx.x == 32) {
         abort_flag = 0;
         mbar_init(&tile_full, 1);
-        mbar_init(&tile_empty, 1 + 128);  // the tile's last MMA reading Q, dY + every worker has its rows
+        mbar_init(&tile_empty, 1 + kCWorkers);  // the tile's last MMA reading Q, dY + every worker has its rows
         for (int s = 0; s < kCRing; ++s) {
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kCW; ++s) {
             mbar_init(&w_full[s], 1);
-            mbar_init(&w_empty[s], 128);
-            mbar_init(&a_full[s], 128);
+            mbar_init(&w_empty[s], kCWorkers);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&a_full[s], kCWorkers);
             mbar_init(&a_empty[s], 1);
         }
-        mbar_init(&dq_full, 1);
-        mbar_init(&dq_empty, 128);
         mbar_init(&fin, 1);
         fence_mbar_init();
     }
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t tDq = tb, tW0 = tb + 128, tA0 = tb + 384;
+    const uint32_t tW0 = tb, tA0 = tb + 128 * kCW;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -369,9 +375,9 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     break;
                 gr += 2;
                 // G1 = Q K^T, G2 = dY V^T into the two W buffers
-                const uint32_t w1 = gw % 2, w2 = (gw + 1) % 2;
-                if (!(ok = mbar_wait(&w_empty[w1], ((gw / 2) & 1) ^ 1, &abort_flag) &&
-                           mbar_wait(&w_empty[w2], (((gw + 1) / 2) & 1) ^ 1, &abort_flag)))
+                const uint32_t w1 = gw % kCW, w2 = (gw + 1) % kCW;
+                if (!(ok = mbar_wait(&w_empty[w1], ((gw / kCW) & 1) ^ 1, &abort_flag) &&
+                           mbar_wait(&w_empty[w2], (((gw + 1) / kCW) & 1) ^ 1, &abort_flag)))
                     break;
                 tc_fence_after();
 #pragma unroll
@@ -386,22 +392,26 @@ __global__ void __launch_bounds__(kCThreads, 1)
                 mma_commit(&w_full[w2]);
                 mma_commit(&ring_empty[sv]);  // V is spent
                 gw += 2;
-                // D_q = P2 K once the workers have written P2
+                // P2 K once the workers have written P2: the start of their dq
+                const uint32_t w3 = gw % kCW;
                 if (!(ok = mbar_wait(&a_full[ga % 2], (ga / 2) & 1, &abort_flag) &&
-                           mbar_wait(&dq_empty, (j & 1) ^ 1, &abort_flag)))
+                           mbar_wait(&w_empty[w3], ((gw / kCW) & 1) ^ 1, &abort_flag)))
                     break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tDq, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(k0 + kk * 2048u, 16384, 1024), idKM, kk > 0);
+                    mma_ts(tW0 + w3 * 128, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(k0 + kk * 2048u, 16384, 1024), idKM,
+                           kk > 0);
+                mma_commit(&w_full[w3]);
                 mma_commit(&a_empty[ga % 2]);
                 mma_commit(&ring_empty[sk]);  // K is spent
+                ++gw;
                 ++ga;
                 if (nimg == 0) mma_commit(&tile_empty);
-                for (int m = 0; m < nimg && ok; ++m, ++gw, ++ga, ++gr) {
-                    const uint32_t s = gr % kCRing, w = gw % 2;
+                for (int m = 0; m < nimg && ok; ++m, ++gw, ++gr) {
+                    const uint32_t s = gr % kCRing, w = gw % kCW;
                     if (!(ok = mbar_wait(&ring_full[s], (gr / kCRing) & 1, &abort_flag) &&
-                               mbar_wait(&w_empty[w], ((gw / 2) & 1) ^ 1, &abort_flag)))
+                               mbar_wait(&w_empty[w], ((gw / kCW) & 1) ^ 1, &abort_flag)))
                         break;
                     tc_fence_after();
                     const uint32_t img = r0 + s * kGTile;
@@ -410,17 +420,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
                         mma_ss(tW0 + w * 128, make_desc_sw128(y0 + kmaj(kk), 0, 1024),
                                make_desc_sw128(img + kk * 2048u, 16384, 1024), idKM, kk > 0);
                     mma_commit(&w_full[w]);
+                    mma_commit(&ring_empty[s]);  // the image is spent
                     if (m == nimg - 1) mma_commit(&tile_empty);  // Q, K, V, dY are no longer read
-                    if (!(ok = mbar_wait(&a_full[ga % 2], (ga / 2) & 1, &abort_flag))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tDq, tA0 + (ga % 2) * 64 + kk * 8, make_desc_sw128(img + kk * 2048u, 16384, 1024), idKM, 1);
-                    mma_commit(&a_empty[ga % 2]);
-                    mma_commit(&ring_empty[s]);
                 }
                 if (!ok) break;
-                mma_commit(&dq_full);
             }
             // leave no MMA in flight
             mma_commit(&fin);
@@ -428,35 +431,14 @@ __global__ void __launch_bounds__(kCThreads, 1)
             mbar_wait_limit(&fin, 0, &give_up, kWaitLimitNs);
         }
     } else {
-        // ---------------------------------------------------------- workers (thread = token row)
-        const int q4 = warp & 3;
+        // ---------------------------------------------------------- workers (thread = token row, column half)
+        const int q4 = warp & 3, half = (warp - 2) >> 2;
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const bool routed = a.mode == MC_GRM || a.mode == MC_SOUP || a.mode == MC_SSC;
+        const size_t hoff = (size_t)half * a.BH * a.L;  // this half's dg / dg_on buffer (dg: times N)
         uint32_t gw = 0, ga = 0;
         bool ok = true;
-        // write g o dy into A slot ga % 2
-        auto put_a = [&](const uint32_t (&yp)[64], float g) -> bool {
-            if (!mbar_wait(&a_empty[ga % 2], ((ga / 2) & 1) ^ 1, &abort_flag)) return false;
-            tc_fence_after();
-            const __nv_bfloat162 g2 = __float2bfloat162_rn(g);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                uint32_t r[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&yp[16 * m + k]);
-                    __nv_bfloat162 pr = __hmul2(x, g2);
-                    r[k] = *reinterpret_cast<uint32_t *>(&pr);
-                }
-                tmem_st16(tA0 + (ga % 2) * 64 + lane_base + 16 * m, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&a_full[ga % 2]);
-            ++ga;
-            return true;
-        };
         for (int j = 0; j < my_tiles && ok; ++j) {
             int bh, n, c;
             tile(j, bh, n, c);
@@ -465,17 +447,18 @@ __global__ void __launch_bounds__(kCThreads, 1)
             if (!(ok = mbar_wait(&tile_full, j & 1, &abort_flag))) break;
             const float gon = routed ? __ldg(a.tok + ((size_t)bh * a.L + t) * kBwdTokWords + 2)
                                      : (a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f);
-            // in-chunk online part: dg_on += sum_{j<=t} G1 G2, P2 = g_on mask(G2)
+            // in-chunk online part over the half's key columns: dg_on += sum_{j<=t} G1 G2, P2 = g_on mask(G2)
             float dgon = 0.f;
             {
-                const uint32_t w1 = gw % 2, w2 = (gw + 1) % 2;
-                if (!(ok = mbar_wait(&w_full[w1], (gw / 2) & 1, &abort_flag) &&
-                           mbar_wait(&w_full[w2], ((gw + 1) / 2) & 1, &abort_flag) &&
+                const uint32_t w1 = gw % kCW, w2 = (gw + 1) % kCW;
+                if (!(ok = mbar_wait(&w_full[w1], (gw / kCW) & 1, &abort_flag) &&
+                           mbar_wait(&w_full[w2], ((gw + 1) / kCW) & 1, &abort_flag) &&
                            mbar_wait(&a_empty[ga % 2], ((ga / 2) & 1) ^ 1, &abort_flag)))
                     break;
                 tc_fence_after();
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {  // 16 key columns at a time
+                for (int mm = 0; mm < 4; ++mm) {  // 16 key columns at a time
+                    const int m = 4 * half + mm;
                     uint32_t x1[16], x2[16], o[8];
                     tmem_ld16(tW0 + w1 * 128 + lane_base + 16 * m, x1);
                     tmem_ld16(tW0 + w2 * 128 + lane_base + 16 * m, x2);
@@ -499,85 +482,90 @@ __global__ void __launch_bounds__(kCThreads, 1)
                 gw += 2;
                 ++ga;
             }
-            // the token's q and dy rows (128-byte swizzle: chunk c of row r at chunk c ^ (r % 8))
-            uint32_t qp[64], yp[64];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = h * 16384 + row * 128 + ((cc ^ (row & 7)) << 4);
-                    const uint4 xq = *reinterpret_cast<const uint4 *>(sQ + off);
-                    const uint4 xy = *reinterpret_cast<const uint4 *>(sY + off);
-                    qp[32 * h + 4 * cc] = xq.x; qp[32 * h + 4 * cc + 1] = xq.y;
-                    qp[32 * h + 4 * cc + 2] = xq.z; qp[32 * h + 4 * cc + 3] = xq.w;
-                    yp[32 * h + 4 * cc] = xy.x; yp[32 * h + 4 * cc + 1] = xy.y;
-                    yp[32 * h + 4 * cc + 2] = xy.z; yp[32 * h + 4 * cc + 3] = xy.w;
-                }
-            mbar_arrive(&tile_empty);
-            // the prefix state (gate g_on) and the cached states (gate g_{t,i}): A(m + 1) = g o dy is
-            // written before the dot with W(m), so the tensor cores never wait for the dot; the gates
-            // are fetched two states ahead
+            // the half's q columns come from the resident tile for every state (128-byte swizzle: chunk
+            // c of row r at chunk c ^ (r % 8); 64 columns per 16 KB panel, the half's is panel `half`);
+            // the tile is released after the last dot
+            const uint8_t *qrow = sQ + half * 16384 + row * 128;
+            if (nimg == 0) mbar_arrive(&tile_empty);
+            // the prefix state (gate g_on) and the cached states (gate g_{t,i}): dg = q . W and
+            // dq += g W over the half's 64 columns; the gates are fetched two states ahead
             const float *grow = routed ? a.gam + (size_t)bh * a.N * a.L + t : nullptr;
-            float *dgrow = a.dg + (size_t)bh * a.N * a.L + t;
+            float *dgrow = a.dg + hoff * a.N + (size_t)bh * a.N * a.L + t;
             const float gconst = a.mode == MC_MEAN ? 1.f / (float)(n + 1) : 1.f;
             const int i0 = c > 0 ? -1 : 0;  // state index of item m is i0 + m (-1: the prefix state)
             auto gate = [&](int m) {
                 const int i = i0 + m;
                 return i < 0 ? gon : (routed ? __ldg(grow + (size_t)i * a.L) : gconst);
             };
-            float g_next = nimg > 1 ? gate(1) : 0.f;
-            if (nimg > 0 && !(ok = put_a(yp, gate(0)))) break;
-            for (int m = 0; m < nimg && ok; ++m) {
-                if (m + 1 < nimg) {
-                    const float g = g_next;
-                    if (m + 2 < nimg) g_next = gate(m + 2);
-                    if (!(ok = put_a(yp, g))) break;
-                }
-                const uint32_t w = gw % 2;
-                if (!(ok = mbar_wait(&w_full[w], (gw / 2) & 1, &abort_flag))) break;
+            float g_cur = nimg > 0 ? gate(0) : 0.f, g_nxt = nimg > 1 ? gate(1) : 0.f;
+            // dq starts from the in-chunk product P2 K (the half's 64 columns)
+            float dqa[64];
+            {
+                const uint32_t w = gw % kCW;
+                if (!(ok = mbar_wait(&w_full[w], (gw / kCW) & 1, &abort_flag))) break;
                 tc_fence_after();
-                float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {  // 32 columns per wait
+                for (int h = 0; h < 2; ++h) {
                     uint32_t x[32];
-                    tmem_ld32(tW0 + w * 128 + lane_base + 32 * h, x);
+                    tmem_ld32(tW0 + w * 128 + lane_base + 64 * half + 32 * h, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const uint32_t qq = qp[16 * h + k];
-                        d0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), d0);
-                        d1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), d1);
-                    }
+                    for (int k = 0; k < 32; ++k) dqa[32 * h + k] = __uint_as_float(x[k]);
                 }
                 tc_fence_before();
                 mbar_arrive(&w_empty[w]);
+                ++gw;
+            }
+            for (int m = 0; m < nimg && ok; ++m) {
+                const float g = g_cur;
+                g_cur = g_nxt;
+                g_nxt = m + 2 < nimg ? gate(m + 2) : 0.f;
+                const uint32_t w = gw % kCW;
+                if (!(ok = mbar_wait(&w_full[w], (gw / kCW) & 1, &abort_flag))) break;
+                tc_fence_after();
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // the half's 64 columns, 32 per wait
+                    uint32_t x[32], qp[16];
+                    tmem_ld32(tW0 + w * 128 + lane_base + 64 * half + 32 * h, x);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int cc = 4 * h + c4;
+                        const uint4 xq = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ (row & 7)) << 4));
+                        qp[4 * c4] = xq.x; qp[4 * c4 + 1] = xq.y; qp[4 * c4 + 2] = xq.z; qp[4 * c4 + 3] = xq.w;
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const uint32_t qq = qp[k];
+                        d0 = fmaf(__uint_as_float(qq << 16), __uint_as_float(x[2 * k]), d0);
+                        d1 = fmaf(__uint_as_float(qq & 0xffff0000u), __uint_as_float(x[2 * k + 1]), d1);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) dqa[32 * h + k] = fmaf(g, __uint_as_float(x[k]), dqa[32 * h + k]);
+                }
+                tc_fence_before();
+                mbar_arrive(&w_empty[w]);
+                if (m == nimg - 1) mbar_arrive(&tile_empty);  // q is read for the last time
                 ++gw;
                 if (i0 + m < 0) dgon += d0 + d1;
                 else dgrow[(size_t)(i0 + m) * a.L] = d0 + d1;
             }
             if (!ok) break;
-            a.dgon[(size_t)bh * a.L + t] = dgon;
-            // drain D_q
-            if (!(ok = mbar_wait(&dq_full, j & 1, &abort_flag))) break;
-            tc_fence_after();
+            a.dgon[hoff + (size_t)bh * a.L + t] = dgon;
+            // the half's 64 columns of dq
             __nv_bfloat16 *dqrow = a.dq + ((size_t)bh * a.L + t) * a.d;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                uint32_t x[32];
-                tmem_ld32(tDq + lane_base + 32 * m, x);
-                tmem_wait_ld();
+            for (int mm = 0; mm < 2; ++mm) {
+                const int m = 2 * half + mm;
                 if (32 * m < a.d) {
 #pragma unroll
                     for (int k = 0; k < 32; k += 8)
                         *reinterpret_cast<uint4 *>(dqrow + 32 * m + k) = make_uint4(
-                            pack_bf16x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])),
-                            pack_bf16x2(__uint_as_float(x[k + 2]), __uint_as_float(x[k + 3])),
-                            pack_bf16x2(__uint_as_float(x[k + 4]), __uint_as_float(x[k + 5])),
-                            pack_bf16x2(__uint_as_float(x[k + 6]), __uint_as_float(x[k + 7])));
+                            pack_bf16x2(dqa[32 * mm + k], dqa[32 * mm + k + 1]), pack_bf16x2(dqa[32 * mm + k + 2], dqa[32 * mm + k + 3]),
+                            pack_bf16x2(dqa[32 * mm + k + 4], dqa[32 * mm + k + 5]), pack_bf16x2(dqa[32 * mm + k + 6], dqa[32 * mm + k + 7]));
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&dq_empty);
         }
     }
     tc_fence_before();
@@ -1010,9 +998,9 @@ namespace mc {
 
 size_t bwd_cached_scratch_bytes(const Problem &p)
 {
-    const size_t BH = p.BH, N = p.N, L = p.L, d = p.d;
+    const size_t BH = p.BH, N = p.N, L = p.L;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    return pad(4 * BH * N * L) + pad(4 * BH * L);
+    return pad(8 * BH * N * L) + pad(8 * BH * L);  // dg and dg_on, one buffer per column half
 }
 
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
@@ -1022,7 +1010,7 @@ cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k,
     const size_t BH = p.BH, N = p.N, L = p.L;
     auto pad = [](size_t x) { return (x + 255) & ~(size_t)255; };
     float *dg = static_cast<float *>(scratch);
-    float *dgon = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(4 * BH * N * L));
+    float *dgon = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dg) + pad(8 * BH * N * L));
     *dg_out = dg;
     *dgon_out = dgon;
     CUtensorMap mQ, mK, mV, mY;

@@ -170,6 +170,7 @@ struct BwdArgs {
     const float *dg_in;   // [BH][N][L] dy_t . M^(i) q_t from the tensor cores, or null (computed here)
     const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null (written already)
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
+    const float *dg_in2, *dgon_in2;  // second partial sums of dg_in and dgon_in (added to them), or null
     float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
     float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
     float *kv_gw;         // [2][BH][L] the online gate and the pooled-key weight w per token (tensor-core path)
@@ -184,7 +185,8 @@ cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, con
 cudaError_t launch_bwd_kv_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u, const void *dy,
                              const uint8_t *G, const float *gw, const float *dkbar, void *dk, void *dv, cudaStream_t s);
 size_t bwd_cached_scratch_bytes(const Problem &p);
-// dq (bf16 [BH][L][d]) is written whole; dg and dg_on go to scratch.
+// dq (bf16 [BH][L][d]) is written whole; dg ([BH][N][L]) and dg_on ([BH][L]) go to scratch as two
+// partial sums each (one per column half), the second BH*N*L (BH*L) floats after the first.
 cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k, const void *v, const void *dy,
                                  const TcImages &img, const float *gam, const float *tok, void *dq, void *scratch,
                                  float **dg_out, float **dgon_out, cudaStream_t s);
