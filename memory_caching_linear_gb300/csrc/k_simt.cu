@@ -541,7 +541,7 @@ cudaError_t set_smem(F *kern, size_t bytes)
 template <typename T, int D>
 cudaError_t seg_scan_impl(const Problem &p, const FwdArgs &a, cudaStream_t s)
 {
-    constexpr int TC = D >= 128 ? 32 : 64;
+    constexpr int TC = D >= 128 ? 16 : 64;  // d = 128: two CTAs per SM (102 KB of shared memory each)
     constexpr int P = D + 1, TP = TC + 1;
     const size_t smem = sizeof(float) * (4 * TC * P + D * P + 2 * TC * TP + D);
     auto kern = seg_scan_simt<T, D, TC>;
