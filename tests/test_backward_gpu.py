@@ -15,7 +15,7 @@ import torch
 
 import memory_caching_linear_gb300 as mcl
 import oracle
-from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
+from mc_inputs import GRM, LONG_GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -106,3 +106,39 @@ def test_autograd_wrapper_matches_the_entry_point():
     direct = mcl.mc_backward(q, k, v, u, dy, 64, GRM)
     for a, b in zip(grads, direct):
         torch.testing.assert_close(a, b, rtol=0, atol=0)
+
+
+# ------------------------------------------------------------------ full size: homogeneity identities
+# y_t = sum_i g_{t,i} M_i q_t, where the gates depend on neither q nor v and every memory M_i is
+# linear in v ("メモリキャッシング：メモリ容量が増大する RNN", §3 eq. 4b-5 and §3.1 eq. 7-10), so y is
+# homogeneous of degree one in q and in v, and Euler's theorem gives <dq, q> = <dv, v> = <dy, y>
+# for every (b, h) problem; with constant gates (Residual, Mean) also <dk, k> = <dy, y>.  These hold
+# at any size: they check the whole tensor-core gradient path at the long workload's full size,
+# where the oracle cannot run.  Tolerance: 1e-2 of the sum of the terms' magnitudes (bf16 outputs).
+
+def _identities(w, mode, topk=0):
+    dev = torch.device("cuda")
+    q, k, v, u = (t.to(dev) for t in workload_inputs(w))
+    g = torch.Generator().manual_seed(w.seed + 7)
+    dy = torch.randn(w.B, w.H, w.L, w.d, generator=g).to(q.dtype).to(dev)
+    y, _ = mcl.mc_forward(q, k, v, u, w.seg_len, mode, topk, want_states=False)
+    dq, dk, dv, du = mcl.mc_backward(q, k, v, u, dy, w.seg_len, mode, topk)
+    assert mcl.mc_check_device() == mcl.MC_OK
+
+    def dot(a, b):  # per (b, h): the sum of a * b and the sum of |a * b|, in fp64
+        p = a.double() * b.double()
+        return p.sum(dim=(2, 3)), p.abs().sum(dim=(2, 3))
+
+    ref, ref_abs = dot(dy, y)
+    pairs = [("dq", dq, q), ("dv", dv, v)] + ([("dk", dk, k)] if mode in (RESIDUAL, MEAN) else [])
+    for name, grad, x in pairs:
+        assert torch.isfinite(grad).all(), name
+        got, got_abs = dot(grad, x)
+        err = ((got - ref).abs() / (0.5 * (got_abs + ref_abs))).max().item()
+        assert err <= 1e-2, (w.name, mode, name, err)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [GRM, RESIDUAL, MEAN])
+def test_full_size_backward_identities(mode):
+    _identities(LONG_GRM, mode)

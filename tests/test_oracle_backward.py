@@ -98,6 +98,21 @@ def test_mean_backward_is_scaled_causal_la_backward(C):
         np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-10)
 
 
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
+def test_backward_euler_identities(mode, topk):
+    # y is homogeneous of degree one in q and in v (the gates depend on neither, every memory is
+    # linear in v: [MC-ja §3 eq. 4b-5, §3.1 eq. 7-10]), so <dq, q> = <dv, v> = <dy, y> per (b, h);
+    # with constant gates (Residual, Mean) y is also linear in k and <dk, k> = <dy, y>.
+    q, k, v, u, dy = _inputs(1, 2, 300, 16, 5)
+    y = oracle.forward(q, k, v, u, 64, mode, topk)["y"]
+    g = oracle.backward(q, k, v, u, dy, 64, mode, topk)
+    ref = (dy * y).sum(axis=(2, 3))
+    pairs = [("dq", q), ("dv", v)] + ([("dk", k)] if mode in (RESIDUAL, MEAN) else [])
+    for name, x in pairs:
+        got = (g[name] * x).sum(axis=(2, 3))
+        assert np.abs(got - ref).max() <= 1e-10 * np.abs(ref).max(), (mode, name)
+
+
 def test_backward_is_linear_in_dy():
     q, k, v, u, dy = _inputs(1, 2, 40, 6, 7)
     dy2 = np.random.default_rng(1).standard_normal(dy.shape)
