@@ -616,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
 // bwd_dkbar_simt: the key-mean gradients from the score gradients,
 // dkbar_i = sum_{t : n(t) > i} dr_{t,i} u_t, on the shapes of the tensor-core path
 // (N <= 64, seg_len and L multiples of kDkSub, so each kDkSub-token sub-chunk lies in
-// one segment).  One CTA per (bh, kDkChunk tokens): every token's u is read once and
+// one segment).  One CTA per (bh, kDkChunk tokens), the last chunks (the most cached
+// segments scored) first: every token's u is read once and
 // feeds every cached segment it scored; a thread keeps one dimension's sums for all
 // segments over a strided share of each sub-chunk, four tokens per step.  The
 // sub-chunks' dr rows are staged in shared memory by asynchronous copies, two
@@ -640,7 +641,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkbar_simt(BwdArgs a, int chunks
     constexpr int parts = kThreads / D;
     constexpr int TG = 4;  // tokens per step: one 16-byte row of dr per segment
     extern __shared__ __align__(16) float sdr[];  // [2][kTab][kDkSub]
-    const int ch = (int)blockIdx.x % chunks, bh = (int)blockIdx.x / chunks;
+    const int ch = chunks - 1 - (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;  // the most scores first
     const int t_lo = ch * kDkChunk, t_hi = min(t_lo + kDkChunk, a.L);
     const int nsub = (t_hi - t_lo) / kDkSub;
     const int col = threadIdx.x % D, part = threadIdx.x / D;
