@@ -57,7 +57,8 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 
 // One CTA per (b,h, pair of cached segments i0 = 2p, i1 = 2p + 1): every tile after
 // segment i0 is loaded once and feeds both accumulators (the tiles of segment i1
-// only the first).
+// only the first).  Every CTA walks its tiles from the sequence's end backwards, so
+// the pairs of a head that run at the same time read the same tiles (from L2).
 __global__ void __launch_bounds__(kGThreads, 1)
     bwd_G_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, GArgs a)
 {
@@ -105,14 +106,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int s = j % kGStages;
                 if (!mbar_wait(&empty[s], ((j / kGStages) & 1) ^ 1, &abort_flag)) break;
                 uint8_t *st = sm + s * kGStage;
-                const int row = bh * a.L + t_begin + j * kG2;
-                const bool g0 = routed, g1 = routed && two && j >= split;  // gates to bring along
+                const int jt = ntiles - 1 - j;  // the tile, from the end
+                const int row = bh * a.L + t_begin + jt * kG2;
+                const bool g0 = routed, g1 = routed && two && jt >= split;  // gates to bring along
                 mbar_arrive_expect_tx(&full[s], 2 * kG2Tile + (g0 ? 256 : 0) + (g1 ? 256 : 0));
                 tma_load_2d(st, &mY, 0, row, &full[s]);
                 tma_load_2d(st + kG2Tile / 2, &mY, 64, row, &full[s]);
                 tma_load_2d(st + kG2Tile, &mQ, 0, row, &full[s]);
                 tma_load_2d(st + kG2Tile + kG2Tile / 2, &mQ, 64, row, &full[s]);
-                const size_t goff = (size_t)t_begin + (size_t)j * kG2;
+                const size_t goff = (size_t)t_begin + (size_t)jt * kG2;
                 if (g0) bulk_load(st + 3 * kG2Tile, a.gam + ((size_t)bh * a.N + i0) * a.L + goff, 256, &full[s]);
                 if (g1) bulk_load(st + 3 * kG2Tile + 512, a.gam + ((size_t)bh * a.N + i1) * a.L + goff, 256, &full[s]);
                 issued = j + 1;
@@ -132,14 +134,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (!(ok = mbar_wait(&scaled[s], (j / kGStages) & 1, &abort_flag))) break;
                 tc_fence_after();
                 const uint32_t y0 = smem_u32(sm + s * kGStage), q0 = y0 + kG2Tile, y1 = y0 + 2 * kG2Tile;
-                const bool second = two && j >= split;
+                const bool second = two && ntiles - 1 - j >= split;  // segment i1's tiles come last
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {  // 16 tokens per step: 16 rows of 128 bytes; the 64-column halves 8 KB apart
                     const uint64_t bq = make_desc_sw128(q0 + kk * 2048u, kG2Tile / 2, 1024);
                     mma_ss(tD, make_desc_sw128(y0 + kk * 2048u, kG2Tile / 2, 1024), bq, idG, (j | kk) != 0);
                     if (second)
-                        mma_ss(tD + 128, make_desc_sw128(y1 + kk * 2048u, kG2Tile / 2, 1024), bq, idG,
-                               (j > split) || kk != 0);
+                        mma_ss(tD + 128, make_desc_sw128(y1 + kk * 2048u, kG2Tile / 2, 1024), bq, idG, (j | kk) != 0);
                 }
                 mma_commit(&empty[s]);
             }
@@ -153,11 +154,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int trow = r & 63, h = r >> 6;  // token row of the tile, 64-column panel
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kGStages;
-            const bool second = two && j >= split;
+            const int jt = ntiles - 1 - j;  // the tile, from the end
+            const bool second = two && jt >= split;
             if (!mbar_wait(&full[s], (j / kGStages) & 1, &abort_flag)) break;
             // the gates came with the tile (routed); Residual 1, Mean 1 / (n(t) + 1)
             const float *gsm = reinterpret_cast<const float *>(sm + s * kGStage + 3 * kG2Tile);
-            const float gc = a.mode == MC_MEAN ? 1.f / (float)((t_begin + j * kG2) / a.C + 1) : 1.f;
+            const float gc = a.mode == MC_MEAN ? 1.f / (float)((t_begin + jt * kG2) / a.C + 1) : 1.f;
             const float g0 = routed ? gsm[trow] : gc;
             const float g1 = routed ? (second ? gsm[128 + trow] : 0.f) : gc;
             const __nv_bfloat162 g02 = __float2bfloat162_rn(g0), g12 = __float2bfloat162_rn(g1);
