@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(kThreads) readout_simt(FwdArgs a)
     float *m_t = g + 2 * kTR;   // softmax max
     float *z_t = m_t + kTR;     // softmax sum
     float *gon = z_t + kTR;     // online gate
-    float *selv = gon + kTR;    // kTR x kMaxTopk (SSC: gate of each selected segment)
+    float *selv = gon + kTR;    // kTR x kMaxTopk (SSC: gate of each selected segment); this and the
+                                // rest exist for SSC only (the launch sizes shared memory by mode)
     int *seli = reinterpret_cast<int *>(selv + kTR * kMaxTopk);  // kTR x kMaxTopk
     int *cur = seli + kTR * kMaxTopk;
     int *nsel = cur + kTR;
@@ -569,8 +570,10 @@ cudaError_t readout_impl(const Problem &p, const FwdArgs &a, cudaStream_t s)
 {
     constexpr int P = D + 1;
     constexpr int KC = D < 32 ? D : 32;
-    const size_t smem = sizeof(float) * (2 * kTR * P + D * (KC + 1) + 5 * kTR + kTR * kMaxTopk) +
-                        sizeof(int) * (kTR * kMaxTopk + 2 * kTR);
+    // the SSC tables come last and only SSC gets them (two CTAs per SM at d = 128 otherwise)
+    const bool ssc = p.mode == MC_SSC;
+    const size_t smem = sizeof(float) * (2 * kTR * P + D * (KC + 1) + 5 * kTR) +
+                        (ssc ? sizeof(float) * kTR * kMaxTopk + sizeof(int) * (kTR * kMaxTopk + 2 * kTR) : 0);
     auto kern = readout_simt<T, D>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
