@@ -234,11 +234,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // (one product per state).  Every product lands in one of kCW rotating TMEM buffers.
 // Persistent, one CTA per SM, tiles with the most cached segments first.  Warp 0
 // loads Q and dY of the tile (TMA, resident while the tile runs) and streams K, V
-// and one 32 KB image per state through a four-slot ring (K and V are read by the
+// and one 32 KB image per state through a five-slot ring (K and V are read by the
 // tile's first three products only); warp 1 issues; eight worker warps, two per TMEM
-// lane quadrant: warp half h owns the token rows of its quadrant and the columns
-// [64h, 64h+64) (q, dy, W, D_q) and the TMEM A columns [32h, 32h+32); the two halves'
-// partial dots go to two dg buffers, which the route kernel adds.
+// lane quadrant: warp half h owns the token rows of its quadrant, the columns
+// [64h, 64h+64) of q, W and dq, and the TMEM A columns [32h, 32h+32) of P2; the two
+// halves' partial dots go to two dg buffers, which the route kernel adds.
 // TMEM: W0 [0,128) | W1 [128,256) | W2 [256,384) | A0 [384,448) | A1 [448,512).
 // ============================================================================
 constexpr int kCRing = 5;
