@@ -27,10 +27,11 @@
 //                   state, dq, du, dkbar (atomics) and the per-token softmax data;
 //   bwd_G_simt      per (b,h, cached segment i): G_i over every later token;
 //   bwd_scan_simt   per (b,h, segment): walks the segment backwards with E, writes dk, dv.
-// On the shapes of the tensor-core path the cached states' O(N L d^2) part runs on
-// the tensor cores (k_bwd_tc.cu: dg and the cached dq, and G), and the gate work on
-// whole shared-memory tables: bwd_route_simt (before the cached pass: the gates;
-// after it: delta, dr, du, dq) and bwd_dkbar_simt (the key-mean gradient from dr).
+// On the shapes of the tensor-core path the gates, the memories' reads (dg and all of
+// dq), G and dk / dv run on the tensor cores (k_bwd_tc.cu, and the gates mode of the
+// router kernel in k_tc.cu), and the gate work on whole shared-memory tables:
+// bwd_route_simt (delta, dr, du, the online gates and pooled-key weights for dk / dv)
+// and bwd_dkbar_simt (the key-mean gradient from dr).
 #include <type_traits>
 
 #include "mc_internal.cuh"
