@@ -494,12 +494,32 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
     const bool lane_on = c0 < D;
     const int tw = warp * TPW;  // the warp's first token of the tile
 
+    constexpr int kV = kTB / 4;  // 16-byte groups of 4 tokens per table row (rows start 64-token aligned)
 #pragma unroll 4
-    for (int e = tid; e < kTB * n; e += kThreads) {  // unrolled: several rows' loads in flight per thread
-        const int i = e / kTB, t = e % kTB;
+    for (int e = tid; e < kV * n; e += kThreads) {  // unrolled: several rows' loads in flight per thread
+        const int i = e / kV, t = 4 * (e % kV);
         const size_t gi = seg_base + (size_t)i * a.L + t;
-        gt[e] = t < cnt ? (gated ? a.gam[gi] : gconst) : 0.f;
-        dt[e] = t < cnt ? a.dg_in[gi] + (a.dg_in2 ? a.dg_in2[gi] : 0.f) : 0.f;
+        float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = g4;
+        if (t + 3 < cnt) {
+            g4 = gated ? *reinterpret_cast<const float4 *>(a.gam + gi) : make_float4(gconst, gconst, gconst, gconst);
+            d4 = *reinterpret_cast<const float4 *>(a.dg_in + gi);
+            if (a.dg_in2) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(a.dg_in2 + gi);
+                d4.x += e4.x; d4.y += e4.y; d4.z += e4.z; d4.w += e4.w;
+            }
+        } else {
+            float gs[4], ds[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const bool in = t + k < cnt;
+                gs[k] = in ? (gated ? a.gam[gi + k] : gconst) : 0.f;
+                ds[k] = in ? a.dg_in[gi + k] + (a.dg_in2 ? a.dg_in2[gi + k] : 0.f) : 0.f;
+            }
+            g4 = make_float4(gs[0], gs[1], gs[2], gs[3]);
+            d4 = make_float4(ds[0], ds[1], ds[2], ds[3]);
+        }
+        *reinterpret_cast<float4 *>(gt + i * kTB + t) = g4;
+        *reinterpret_cast<float4 *>(dt + i * kTB + t) = d4;
     }
     if (tid < kTB) {
         const int t = tid;
@@ -541,13 +561,24 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
         dl[t] = s;
     }
     __syncthreads();
-    // dr = g (dg - delta), in place, and out for the key-mean gradient
+    // dr = g (dg - delta), in place, and out for the key-mean gradient (4 tokens per thread and step)
 #pragma unroll 4
-    for (int e = tid; e < kTB * n; e += kThreads) {
-        const int t = e % kTB;
-        const float dr = gt[e] * (dt[e] - dl[t]);
-        dt[e] = dr;
-        if (gated && t < cnt) a.dr[seg_base + (size_t)(e / kTB) * a.L + t] = dr;
+    for (int e = tid; e < kV * n; e += kThreads) {
+        const int i = e / kV, t = 4 * (e % kV);
+        const float4 g4 = *reinterpret_cast<const float4 *>(gt + i * kTB + t);
+        const float4 d4 = *reinterpret_cast<const float4 *>(dt + i * kTB + t);
+        const float4 r4 = make_float4(g4.x * (d4.x - dl[t]), g4.y * (d4.y - dl[t + 1]), g4.z * (d4.z - dl[t + 2]),
+                                      g4.w * (d4.w - dl[t + 3]));
+        *reinterpret_cast<float4 *>(dt + i * kTB + t) = r4;
+        if (gated) {
+            float *out = a.dr + seg_base + (size_t)i * a.L + t;
+            if (t + 3 < cnt) {
+                *reinterpret_cast<float4 *>(out) = r4;
+            } else {
+                const float rs[4] = {r4.x, r4.y, r4.z, r4.w};
+                for (int k = 0; k < 4 && t + k < cnt; ++k) out[k] = rs[k];
+            }
+        }
     }
     __syncthreads();
 
