@@ -463,11 +463,13 @@ def backward_flops(w):
     the forward), dq (2 d^2) and the state gradient dy q^T (2 d^2); per token, twice the
     online write + read (8 d^2); per token and score, the score gradients du and the
     key-mean gradient (4 d).  Per kernel: the tensor-core cached pass does M q and dq of
-    the cached reads, the G kernels the state gradients, the gate kernel the score
-    gradients (and, without the tensor-core pass, the cached M q and dq too), the segment
+    the cached reads, the G kernels the state gradients, the FFMA gate kernel the score
+    gradients (and, without the tensor-core pass, the cached M q and dq too), the route
+    kernel du and the key-mean kernel dkbar (half the score gradients each), the segment
     scan the online write and read (4 d^2 per token and run), the reverse scan / the
     tensor-core dk, dv kernel the online gradients (6 d^2 per token), the state kernel the
-    online write (2 d^2 per token)."""
+    online write (2 d^2 per token); the tensor-core gates kernel recomputes the router's
+    scores (2 d per token and cached segment: forward work, outside the total)."""
     s, n = segment_counts(w)
     bh = w.B * w.H
     d = w.d
@@ -479,7 +481,8 @@ def backward_flops(w):
             "bwd_route_simt": bh * score // 2, "bwd_dkbar_simt": bh * score // 2,
             "bwd_G_tc": bh * 2 * d * d * sum(n), "bwd_G_simt": bh * 2 * d * d * sum(n),
             "seg_scan_simt": bh * 4 * d * d * w.L, "bwd_scan_simt": bh * 6 * d * d * w.L,
-            "bwd_kv_tc": bh * 6 * d * d * w.L, "seg_state_tc": bh * 2 * d * d * w.L, "kbar_simt": bh * d * w.L}
+            "bwd_kv_tc": bh * 6 * d * d * w.L, "seg_state_tc": bh * 2 * d * d * w.L,
+            "gate_tiles_tc": bh * 2 * d * sum(st - 1 for st in s) if routed else 0}
 
 
 def run_backward(args, w, wname):

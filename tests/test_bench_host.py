@@ -52,6 +52,19 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
+def test_backward_flops_tensor_core_split():
+    # the tensor-core backward's kernels share the stated work exactly (the gates kernel
+    # recomputes forward work, outside the total)
+    w = mc_inputs.LONG_GRM
+    f = bench.backward_flops(w)
+    tc = ("seg_state_tc", "bwd_cached_tc", "bwd_route_simt", "bwd_dkbar_simt", "bwd_G_tc", "bwd_kv_tc")
+    assert sum(f[k] for k in tc) == f["total"]
+    assert f["gate_tiles_tc"] == w.B * w.H * 2 * w.d * sum(t // w.seg_len for t in range(w.L))
+    assert abs(f["total"] / 1e12 - 3.4019) < 1e-3
+    r = bench.backward_flops(w.with_(mode=mc_inputs.RESIDUAL))
+    assert r["gate_tiles_tc"] == 0 and r["bwd_route_simt"] == 0
+
+
 def test_reduce_max_two_gloo_ranks():
     port = _free_port()
     mgr = mp.Manager()
