@@ -68,8 +68,8 @@ def test_argument_errors_never_reach_the_device(lib):
     assert _fwd(lib, q=None) == mcl.MC_ERR_NULL
     assert _fwd(lib, y=None) == mcl.MC_ERR_NULL
     assert _fwd(lib, u=None, mode=mcl.MC_GRM) == mcl.MC_ERR_NULL
-    for mode in (mcl.MC_RESIDUAL, mcl.MC_MEAN):  # no router input needed: the call gets past the checks
-        assert _fwd(lib, u=None, mode=mode) not in (mcl.MC_ERR_NULL, mcl.MC_ERR_MODE)
+    for mode in (mcl.MC_RESIDUAL, mcl.MC_MEAN):  # no router input needed: the null check passes (and the
+        assert _fwd(lib, u=None, mode=mode, q=FAKE + 8) == mcl.MC_ERR_ALIGN  # alignment check stops the call)
     assert _fwd(lib, mode=7) == mcl.MC_ERR_MODE
     assert _fwd(lib, mode=-1) == mcl.MC_ERR_MODE
     for bad in (dict(d=17), dict(d=256), dict(L=0), dict(B=0), dict(H=-1), dict(seg=0)):
@@ -94,8 +94,28 @@ def test_argument_errors_never_reach_the_device(lib):
     assert dec(mode=9) == mcl.MC_ERR_MODE
     assert dec(q=None) == mcl.MC_ERR_NULL
     assert dec(u=None) == mcl.MC_ERR_NULL
-    assert dec(u=None, mode=mcl.MC_MEAN) not in (mcl.MC_ERR_NULL, mcl.MC_ERR_MODE)
+    assert dec(u=None, mode=mcl.MC_MEAN, q=FAKE + 4) == mcl.MC_ERR_ALIGN  # past the null check, stopped after
     assert dec(q=FAKE + 4) == mcl.MC_ERR_ALIGN
+
+
+def test_backward_argument_errors_never_reach_the_device(lib):
+    def bwd(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, u=FAKE, dy=FAKE, B=1, H=1, L=64, d=16, seg=16, mode=mcl.MC_GRM, topk=0,
+                 dq=FAKE, dk=FAKE, dv=FAKE, du=FAKE)
+        a.update(kw)
+        return lib.mc_backward(a["q"], a["k"], a["v"], a["u"], a["dy"], a["B"], a["H"], a["L"], a["d"], a["seg"],
+                               a["mode"], a["topk"], a["dq"], a["dk"], a["dv"], a["du"], None)
+    for name in ("q", "k", "v", "dy", "dq", "dk", "dv"):
+        assert bwd(**{name: None}) == mcl.MC_ERR_NULL, name
+    assert bwd(u=None) == mcl.MC_ERR_NULL and bwd(du=None) == mcl.MC_ERR_NULL  # the router's input and gradient
+    for mode in (mcl.MC_RESIDUAL, mcl.MC_MEAN):  # no router: u and du may be absent (past the null check,
+        assert bwd(u=None, du=None, mode=mode, dq=FAKE + 8) == mcl.MC_ERR_ALIGN  # stopped by the alignment one)
+    assert bwd(mode=7) == mcl.MC_ERR_MODE
+    for bad in (dict(d=17), dict(L=0), dict(seg=0), dict(B=0)):
+        assert bwd(**bad) == mcl.MC_ERR_SHAPE, bad
+    assert bwd(mode=mcl.MC_SSC, topk=-1) == mcl.MC_ERR_TOPK
+    assert bwd(dq=FAKE + 8) == mcl.MC_ERR_ALIGN
+    assert bwd(du=FAKE + 4) == mcl.MC_ERR_ALIGN
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
