@@ -244,8 +244,10 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u,
  *   (B*H*N*d fp32) and, when states is NULL, the states (B*H*N*d*d fp32), each
  *   rounded up to 256 bytes; larger problems return MC_ERR_SCRATCH and enqueue
  *   nothing.  The call allocates and frees nothing.
- *   The first call on each device looks up the array's device address (once,
- *   with that device current); make that first call before any stream capture.
+ *   Every call looks up the array's device address on the current device (no
+ *   allocation), so a device reset between calls is harmless.  The first call on
+ *   a device may load the library's device code there: make that first call
+ *   before any stream capture.
  *   All calls share the one array: calls whose work overlaps on the GPU (other
  *   streams, other host threads) race on it and must be serialised by the
  *   caller.  Every scratch element is rewritten before it is read, so nothing

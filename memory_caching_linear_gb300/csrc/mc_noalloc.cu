@@ -12,8 +12,6 @@
 // array of kNoAllocScratchBytes (64 MiB) that every GPU which loads this
 // library holds until the process exits.  The caller still provides q, k, v, u,
 // y and (optionally) states.
-#include <mutex>
-
 #include "mc_internal.cuh"
 
 namespace {
@@ -21,33 +19,23 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 64ull << 20;
 
 // Host code must not use this name as an address: on the host it is only a
-// stand-in for the symbol.  The device address is looked up per device below.
+// stand-in for the symbol.  Its device address is looked up, with the device
+// current, on each call below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device ordinal
-
-// Set-up, once per device, with that device current: resolve the array's device address.
+// The array's device address for the current device.  Looked up on every call
+// (a symbol lookup, no allocation) rather than cached, so that a device reset or
+// a rebuilt primary context between calls never leaves a stale address behind.
+// The first lookup on a device may load the library's device code there.
 int scratch_for_current_device(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return MC_ERR_DEVICE;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return MC_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return MC_OK;
 }
 

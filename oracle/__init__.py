@@ -76,7 +76,7 @@ def _load():
             lib.mc_oracle_forward_swla.restype = i
             lib.mc_oracle_bruteforce_swla.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, i]
             lib.mc_oracle_bruteforce_swla.restype = i
-            lib.mc_oracle_backward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
+            lib.mc_oracle_backward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ip, dp, dp, dp, dp, i]
             lib.mc_oracle_backward.restype = i
             lib.mc_oracle_forward_segments.argtypes = [dp, dp, dp, dp, i, i, i, ip, i, i, i, ip, dp, dp, ip, dp, i]
             lib.mc_oracle_forward_segments.restype = i
@@ -215,10 +215,12 @@ def bruteforce(q, k, v, u, seg_len: int, mode: int, topk: int = 0, *, nthreads: 
     return y
 
 
-def backward(q, k, v, u, dy, seg_len: int, mode: int, topk: int = 0, *, nthreads: int = 0) -> dict:
+def backward(q, k, v, u, dy, seg_len: int, mode: int, topk: int = 0, *, given_sel=None,
+             nthreads: int = 0) -> dict:
     """Gradients of the forward for the upstream gradient ``dy`` of y (plain linear
     memory): a dict with ``dq``, ``dk``, ``dv``, ``du`` [B,H,L,d] float64 (``du`` is
-    zero for Residual and Mean, which read no u)."""
+    zero for Residual and Mean, which read no u).  ``given_sel`` [B,H,L,topk] replaces
+    the SSC router's choice, as in :func:`forward`."""
     lib = _load()
     q, k, v, u, dy = (_as_f64(a) for a in (q, k, v, u, dy))
     if u.size == 0 and mode in (RESIDUAL, MEAN):
@@ -228,9 +230,14 @@ def backward(q, k, v, u, dy, seg_len: int, mode: int, topk: int = 0, *, nthreads
         if a.shape != q.shape:
             raise ValueError("q, k, v, u, dy must share the shape [B, H, L, d]")
     out = {n: np.zeros((B, H, L, d), np.float64) for n in ("dq", "dk", "dv", "du")}
+    gs = None
+    if given_sel is not None:
+        gs = np.ascontiguousarray(np.asarray(given_sel, dtype=np.int32))
+        if gs.shape != (B, H, L, max(topk, 0)):
+            raise ValueError("given_sel must be [B,H,L,topk]")
     st = lib.mc_oracle_backward(*[_ptr(a, ctypes.c_double) for a in (q, k, v, u, dy)], B * H, L, d, seg_len,
-                                mode, max(topk, 0), *[_ptr(out[n], ctypes.c_double) for n in ("dq", "dk", "dv", "du")],
-                                nthreads)
+                                mode, max(topk, 0), _ptr(gs, ctypes.c_int32),
+                                *[_ptr(out[n], ctypes.c_double) for n in ("dq", "dk", "dv", "du")], nthreads)
     if st != 0:
         raise RuntimeError(f"mc_oracle_backward failed with status {st}")
     return out

@@ -479,7 +479,11 @@ static int head_backward(const head_job *J)
                 for (int i = 0; i < s; ++i) r[i] = dot(ut, kbar + (size_t)i * d, d);
                 r[s] = dot(ut, ksum, d) / cnt;
             }
-            if (J->mode == OR_SSC) {
+            if (J->mode == OR_SSC && J->given_sel) { /* the forward evaluated on a given selection */
+                const int32_t *gs = J->given_sel + (size_t)t * J->topk;
+                for (int c = 0; c < J->topk; ++c)
+                    if (gs[c] >= 0) idx[nsel++] = gs[c];
+            } else if (J->mode == OR_SSC) {
                 double gp;
                 nsel = ssc_rank(r, s, J->topk, idx, taken, &gp);
             } else {
@@ -725,9 +729,12 @@ int mc_oracle_bruteforce_swla(const double *q, const double *k, const double *v,
 /*
  * Gradients of the forward (plain linear memory) for the upstream gradient dy:
  * dq, dk, dv, du [BH][L][d] are written (du is zero for Residual and Mean).
+ * given_sel ([BH][L][topk], -1 padded; may be NULL) replaces the SSC router's
+ * choice, as in mc_oracle_forward: the gradient is then that of the forward
+ * evaluated on the given selection (the selection itself passes no gradient).
  */
 int mc_oracle_backward(const double *q, const double *k, const double *v, const double *u, const double *dy,
-                       int BH, int L, int d, int C, int mode, int topk,
+                       int BH, int L, int d, int C, int mode, int topk, const int32_t *given_sel,
                        double *dq, double *dk, double *dv, double *du, int nthreads)
 {
     int st = check_args(BH, L, d, C, mode, topk);
@@ -736,7 +743,8 @@ int mc_oracle_backward(const double *q, const double *k, const double *v, const 
     pool_ctx P;
     memset(&P, 0, sizeof(P));
     P.base = (head_job){q, k, v, u, L, d, C, mode, mode == OR_SSC ? topk : 0,
-                        NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, dy, dq, dk, dv, du, NULL, 0};
+                        NULL, mode == OR_SSC ? given_sel : NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                        dy, dq, dk, dv, du, NULL, 0};
     P.BH = BH;
     P.brute = 2;
     return run_pool(&P, nthreads);

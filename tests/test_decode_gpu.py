@@ -14,11 +14,11 @@ import torch
 import memory_caching_linear_gb300 as mcl
 import oracle
 from mc_inputs import GRM, MEAN, RESIDUAL, SOUP, SSC, make_inputs
+from ssc_valid import check_y_over_valid_sets, seg_starts
 
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 1e-2}
-GAP = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,20 +41,28 @@ def decode_all(q, k, v, u, C, mode, topk, n_max):
     return torch.stack(ys, 2).numpy(), cache
 
 
-@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
-@pytest.mark.parametrize("d,C,L,dtype", [(64, 128, 512, "bf16"), (32, 48, 200, "f32"), (128, 256, 768, "bf16")])
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2), (SSC, 4), (MEAN, 0)])
+@pytest.mark.parametrize("d,C,L,dtype", [(64, 128, 512, "bf16"), (32, 48, 200, "f32"), (128, 256, 768, "bf16"),
+                                         # 64 segments: the last token fills the 64th and last cache slot,
+                                         # so reads near the end go over 63 cached states
+                                         (128, 16, 1024, "bf16")])
 def test_decode_reproduces_the_forward(mode, topk, d, C, L, dtype):
-    q, k, v, u = make_inputs(1, 2, L, d, 17 + d, dtype)
+    q, k, v, u = make_inputs(1, 2, L, d, 17 + d + C, dtype)
     N = (L + C - 1) // C
     ref = oracle.forward(q, k, v, u, C, mode, topk)
     # the post-training average needs no router input
-    y, cache = decode_all(q, k, v, None if mode == MEAN else u, C, mode, topk, n_max=N + 1)
-    keep = np.ones(y.shape[:3], bool)
-    if mode == SSC:  # fp32 near-ties may rank either way
-        keep = ref["gap"] >= GAP
+    y, cache = decode_all(q, k, v, None if mode == MEAN else u, C, mode, topk, n_max=min(N + 1, 64))
     yref = ref["y"]
-    err = np.abs(y - yref)[keep].max() / np.abs(yref).max()
-    assert err <= TOL[dtype], err
+    if mode == SSC and 0 < topk < N - 1:
+        # near-ties in fp32 may rank either way: each such token must match the oracle
+        # on one of its valid top-k selections
+        ntie = check_y_over_valid_sets(
+            y, q, k, v, u, seg_starts(L, C), topk, ref,
+            lambda sel: oracle.forward(q, k, v, u, C, SSC, topk, given_sel=sel)["y"], TOL[dtype])
+        print(f"near-tie tokens checked against their valid selections: {ntie}")
+    else:
+        err = np.abs(y - yref).max() / np.abs(yref).max()
+        assert err <= TOL[dtype], err
     done = L // C  # segments completed by the last token
     st = cache.states[:, :, :done].cpu().numpy()
     serr = np.abs(st - ref["states"][:, :, :done]).max() / np.abs(ref["states"]).max()

@@ -31,7 +31,7 @@ def _inputs(B, H, L, d, seed):
     return q, k, v, u, dy
 
 
-def _finite_differences(args, dy, C, mode, topk, eps=1e-6):
+def _finite_differences(args, dy, C, mode, topk, eps=1e-6, given_sel=None):
     """d<y, dy>/dX for X in q, k, v, u, element by element (central differences)."""
     out = {}
     for j, name in enumerate(NAMES):
@@ -43,7 +43,7 @@ def _finite_differences(args, dy, C, mode, topk, eps=1e-6):
                 a = list(args)
                 a[j] = X.copy()
                 a[j][idx] += sgn * eps
-                val.append(np.sum(oracle.forward(*a, C, mode, topk)["y"] * dy))
+                val.append(np.sum(oracle.forward(*a, C, mode, topk, given_sel=given_sel)["y"] * dy))
             fd[idx] = (val[0] - val[1]) / (2 * eps)
         out[name] = fd
     return out
@@ -60,6 +60,36 @@ def test_backward_matches_finite_differences(mode, topk, L, C):
     for n in NAMES:
         scale = max(np.abs(fd[n]).max(), 1e-12)
         assert np.abs(g[n] - fd[n]).max() <= 1e-7 * scale + 1e-12, (n, mode, topk)
+
+
+def test_backward_on_a_given_selection():
+    """With the SSC selection given (as the forward takes it), the backward is the
+    derivative of the forward evaluated on that selection: central differences of the
+    forward with the same given selection agree.  The selection here is the router's
+    choice reversed (the lowest-scoring cached segment instead of the highest), so it is
+    not the one the router would make; and giving the router's own choice reproduces
+    the ungiven backward exactly."""
+    L, C, topk = 10, 3, 1
+    q, k, v, u, dy = _inputs(1, 1, L, 3, 41)
+    fwd = oracle.forward(q, k, v, u, C, SSC, topk)
+    base = oracle.backward(q, k, v, u, dy, C, SSC, topk)
+    same = oracle.backward(q, k, v, u, dy, C, SSC, topk, given_sel=fwd["sel"])
+    for n in NAMES:
+        np.testing.assert_array_equal(same[n], base[n])
+    # the lowest-scoring cached segment of every token (-1 where there is none)
+    kbar = np.stack([k[0, 0, n * C:min(L, n * C + C)].mean(0) for n in range((L + C - 1) // C)])
+    other = np.full((1, 1, L, topk), -1, np.int32)
+    for t in range(L):
+        s = t // C
+        if s > 0:
+            other[0, 0, t, 0] = int(np.argmin(kbar[:s] @ u[0, 0, t]))
+    assert np.any(other != fwd["sel"])
+    g = oracle.backward(q, k, v, u, dy, C, SSC, topk, given_sel=other)
+    fd = _finite_differences([q, k, v, u], dy, C, SSC, topk, given_sel=other)
+    for n in NAMES:
+        scale = max(np.abs(fd[n]).max(), 1e-12)
+        assert np.abs(g[n] - fd[n]).max() <= 1e-7 * scale + 1e-12, n
+        assert np.abs(g[n] - base[n]).max() > 1e-6 * scale, n  # a different function of the inputs
 
 
 def _causal_la_grads(q, k, v, dy):

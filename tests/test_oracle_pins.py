@@ -278,6 +278,48 @@ def test_ssc_ties_go_to_lower_index():
         assert sel[j] == (0 if r0 >= r2 else 2)
 
 
+def _router_case(a):
+    """d = 2, one token per segment (so each cached pooled key is that token's key),
+    k_i = (a_i, 0) and u_t = (1, 0): the router score of token t against cached segment
+    i < t is exactly a_i."""
+    L = len(a) + 1
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((1, 1, L, 2))
+    v = rng.standard_normal((1, 1, L, 2))
+    k = np.zeros((1, 1, L, 2))
+    k[0, 0, :len(a), 0] = a
+    k[0, 0, len(a), 0] = 0.375
+    u = np.zeros((1, 1, L, 2))
+    u[..., 0] = 1.0
+    return q, k, v, u
+
+
+def test_ssc_gap_hand_case():
+    """The router's near-tie record, worked by hand ([MC-sum §3.4]: the k largest cached
+    scores).  Scores a_i of the cached segments, exact binary fractions:
+      a = [1/2, 1/4, 1/2 + 2^-10, 1/4 + 2^-10, 1/8, 1/2 + 2^-11, 1/2 + 2^-30].
+    Ranking is in fp32, where 1/2 + 2^-30 rounds to 1/2 and ties with segment 0 (the lower
+    index wins); the gap is the fp64 distance between the last chosen score and the best
+    left out, infinite when nothing is left out.  Token t sees segments 0..t-1.
+      topk 2: t=3 [2,0] gap 1/4; t=4,5 [2,0] gap 1/4 - 2^-10; t=6,7 [2,5] gap 2^-11.
+      topk 3: t=3 [2,0,1] inf; t=4,5 [2,0,3] gap 2^-10; t=6 [2,5,0] gap 1/4 - 2^-10;
+              t=7 [2,5,0] gap 2^-30 (fp64 would have ranked segment 6 third)."""
+    a = [0.5, 0.25, 0.5 + 2**-10, 0.25 + 2**-10, 0.125, 0.5 + 2**-11, 0.5 + 2**-30]
+    q, k, v, u = _router_case(a)
+    inf = np.inf
+    want = {2: {3: ([2, 0], 0.25), 4: ([2, 0], 0.25 - 2**-10), 5: ([2, 0], 0.25 - 2**-10),
+                6: ([2, 5], 2**-11), 7: ([2, 5], 2**-11)},
+            3: {3: ([2, 0, 1], inf), 4: ([2, 0, 3], 2**-10), 5: ([2, 0, 3], 2**-10),
+                6: ([2, 5, 0], 0.25 - 2**-10), 7: ([2, 5, 0], 2**-30)}}
+    for topk, rows in want.items():
+        out = oracle.forward(q, k, v, u, 1, SSC, topk)
+        for t, (sel, gap) in rows.items():
+            assert [int(x) for x in out["sel"][0, 0, t]] == sel, (topk, t)
+            assert out["gap"][0, 0, t] == gap, (topk, t, out["gap"][0, 0, t], gap)
+        # fewer cached segments than topk: all of them, nothing left out
+        assert np.isinf(out["gap"][0, 0, :3]).all()
+
+
 # ---------------------------------------------------------------- invariants
 
 @pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 2)])
@@ -452,6 +494,9 @@ _MUTATIONS = [
      "for (int i = 1; i < s; ++i) add_matvec(yt, 1.0,"),
     ("ssc ties to higher index", r"if \(best < 0 \|\| fi > bv\) \{ /\* strict",
      "if (best < 0 || fi >= bv) { /* strict"),
+    ("gap from the first chosen score", r"\*gap = fabs\(r\[idx\[want - 1\]\] - r\[best\]\);",
+     "*gap = fabs(r[idx[0]] - r[best]);"),
+    ("router ranks in fp64", r"float fi = \(float\)r\[i\];", "double fi = r[i];"),
     ("soup uses online twice", r"Mstar\[e\] \+= g\[i\] \* Mi\[e\];", "Mstar[e] += g[s] * Mi[e];"),
     ("segment end one token early", r"if \(J->seg_off\) return J->seg_off\[n \+ 1\];",
      "if (J->seg_off) return J->seg_off[n + 1] - (n + 2 < J->nseg ? 1 : 0);"),
@@ -486,6 +531,7 @@ def _run_pins_against(libpath):
             lambda: test_soup_equals_grm_for_linear_memory(7),
             lambda: test_ssc_limits(),
             lambda: test_ssc_ties_go_to_lower_index(),
+            test_ssc_gap_hand_case,
             lambda: test_causality(GRM, 0),
             lambda: test_single_segment_is_plain_recurrent_model(GRM, 0),
             lambda: test_mean_is_linear_attention_over_the_memory_count(5),
