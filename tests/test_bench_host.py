@@ -97,3 +97,21 @@ def test_roofline_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     (tmp_path / bench.KERNEL_SOURCES[0]).write_text("changed")
     assert bench.ncu_traffic("readout_tc", "long-grm") is None
     assert bench.ncu_traffic("gates_tc", "long-grm") is None
+
+
+def test_workload_bounds_and_kernel_bytes():
+    """The long workload is bound by the tensor cores, the sweep's short-N rows, the d = 64
+    workload and SSC by HBM; each kernel's algorithmic bytes add up to the step's bytes
+    plus the inputs both kernels must read (k, v and u twice) and the bf16 state reads."""
+    peaks = {"bf16_tflops": 1946.8, "hbm_gbs": 6775.6}
+    assert bench.workload_bound(mc_inputs.LONG_GRM, peaks) == "tensor"
+    assert bench.workload_bound(mc_inputs.SSC_D128, peaks) == "hbm"
+    assert bench.workload_bound(mc_inputs.GRM_D64, peaks) == "hbm"
+    assert [bench.workload_bound(w, peaks) for w in mc_inputs.SWEEP] == ["hbm", "hbm", "hbm", "tensor"]
+    w = mc_inputs.LONG_GRM
+    kb = bench.kernel_bytes(w)
+    row = w.B * w.H * w.L * w.d * 2
+    assert kb["seg_state_tc"] + kb["readout_tc"] == bench.algorithmic_bytes(w) + 3 * row + \
+        w.B * w.H * w.N * w.d * w.d * 2
+    assert bench.metric_name(w) == bench.METRIC
+    assert "SSC" in bench.metric_name(mc_inputs.SSC_D128)
