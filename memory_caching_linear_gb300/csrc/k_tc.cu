@@ -18,8 +18,9 @@
 //   operand image (the "prefix state" of the chunk); at the end S is the
 //   segment's cached state M^(n) ([MC-ja §3, after eq. 4b]), written as fp32
 //   (the states output) and as a bf16 image.  It also forms the key mean
-//   kbar_n ([MC-ja §3.1 eq. 10], pooled keys) as hi + lo bf16 rows of a
-//   per-head operand image, and the online gate score
+//   kbar_n ([MC-ja §3.1 eq. 10], pooled keys) as hi + mid + lo bf16 rows of a
+//   per-head operand image (the three terms sum to the fp32 mean exactly), and
+//   the online gate score
 //     r_on[t] = <u_t, sum_{j=t0..t} k_j> / (t - t0 + 1)
 //   from R = U_c K_c^T (tensor core) masked to j <= t plus <u_t, keys before the chunk>.
 //
@@ -31,7 +32,8 @@
 //   prefix state; Mean: the same with g = 1 / (n + 1)) as MMAs into one fp32 accumulator D per CTA:
 //     G = Q K_c^T;  D = (g_n * mask(G)) V_c;  D += (g_i o Q) X_i^T
 //   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.  The gates come from the
-//   scores <u_t, kbar_i> (two MMAs per tile: kbar as hi and lo rows) and r_on[t]:
+//   scores <u_t, kbar_i> (three MMA sets per tile, kbar as hi, mid and lo rows:
+//   every product is exact and only the fp32 accumulation rounds) and r_on[t]:
 //   g = softmax over {scores_i}_{i<n} and r_on[t] (GRM; Soup is the same sum for
 //   a linear memory, [MC-sum §3.3]); SSC keeps the topk largest cached scores
 //   ([MC-sum §3.4]) and gives the others gate 0.
@@ -42,6 +44,7 @@
 
 #include "mc_internal.cuh"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 #include "tensormap.cuh"
 
 namespace mc {
@@ -54,10 +57,6 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 128;            // tile width: the head dimension (64 or 128), zero-padded to it
-constexpr int kTcMaxTopk = 16;     // SSC selections per token handled by the tensor-core path
-constexpr int kCT = 128;           // tokens per chunk / tile
-constexpr uint32_t kTile = 32768;  // one 128 x 128 bf16 operand tile
 
 struct TcArgs {
     const __nv_bfloat16 *q, *u;
@@ -65,7 +64,7 @@ struct TcArgs {
     float *states;        // [BH][N][128][128] fp32 (output)
     uint8_t *states_img;  // [BH][N] x 32 KB  bf16 operand images of M^(n)
     uint8_t *spre_img;    // [BH][N][CPS] x 32 KB  prefix state before chunk c (c >= 1)
-    uint8_t *kbar_img;    // [BH] x 32 KB: hi rows (16 KB) then lo rows (16 KB), row = segment
+    uint8_t *kbar_img;    // [BH][NB] x 48 KB: hi, mid, lo rows (16 KB each), row = segment % 64
     uint8_t *prefix_img;  // [BH][N] x 32 KB  sum_{i<n} M^(i) (Residual)
     float *r_on;          // [BH][L]
     float *gam_out;       // backward gates: [BH][N][L] g_{t,i}, or null
@@ -78,18 +77,9 @@ struct TcArgs {
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
     int BH, L, C, N, CPS;
     int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
+    int NB;               // blocks of 64 segments in a head's key-mean image (1 when N <= 64)
     int num_tiles;
 };
-
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
-{
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 // SWLA (sliding-window linear attention, c = 2, [MC-ja §3.1 eq. 28]) within one
 // 128-token chunk whose first token is t_c:
@@ -139,8 +129,6 @@ __device__ __forceinline__ float chunk_pick(const float (&v)[4], int j)
     return e == 0 ? v0 : e == 1 ? v1 : e == 2 ? v2 : v3;
 }
 
-// K-major SW128 descriptor start for the 16-wide K step kk of a tile with `rows` rows.
-__device__ __forceinline__ uint32_t kmaj_off(int kk, uint32_t rows) { return (kk >> 2) * rows * 128u + (kk & 3) * 32u; }
 
 // ============================================================================
 // seg_state_tc
@@ -468,11 +456,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     if (GATED) {
                         const float kbv = ks / (float)a.C;
                         if (a.kbar_out && (int)row < a.d) a.kbar_out[sidx * a.d + row] = kbv;
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(kbv);
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(kbv - __bfloat162float(hi));
-                        uint8_t *kimg = a.kbar_img + (size_t)bh * kTile;
-                        *reinterpret_cast<__nv_bfloat16 *>(kimg + sw128_offset(seg, row, 64)) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(kimg + 16384 + sw128_offset(seg, row, 64)) = lo;
+                        store_kbar_terms(a.kbar_img + (size_t)bh * a.NB * kKbImg, seg, row, kbv);
                     }
                 }
             }
@@ -506,12 +490,7 @@ __global__ void __launch_bounds__(kD) kbar_images_tc(const __nv_bfloat16 *__rest
         }
         s += cs;
     }
-    const float kb = s / (float)a.C;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(kb);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(kb - __bfloat162float(hi));
-    uint8_t *img = a.kbar_img + (size_t)bh * kTile;
-    *reinterpret_cast<__nv_bfloat16 *>(img + sw128_offset(seg, col, 64)) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(img + 16384 + sw128_offset(seg, col, 64)) = lo;
+    store_kbar_terms(a.kbar_img + (size_t)bh * a.NB * kKbImg, seg, col, s / (float)a.C);
 }
 
 // Residual: prefix sums of the cached states, P_n = sum_{i<n} M^(i) (fp32
@@ -601,11 +580,11 @@ __device__ __forceinline__ float token_gates(float (&sc)[64], int n, float ron, 
 // gate_tiles_tc -- the SSC router ([MC-sum §3.4]): for every token the topk
 // cached segments with the largest scores r_{t,i} = <u_t, kbar_i> (i < n), in rank
 // order, equal scores to the lower index, -1 padded; or the backward's gates.  Per 128-token chunk;
-// the scores come from two MMAs (kbar as hi + lo bf16 rows, so the score carries
-// ~16 bits of kbar; u is exact in bf16).
+// the scores come from three MMA sets (kbar as hi + mid + lo bf16 rows, which sum to the
+// fp32 kbar exactly; u is exact in bf16), so each score is an fp32 sum of exact products.
 // ============================================================================
 constexpr int kRouterThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 selection
-constexpr size_t kRouterSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
+constexpr size_t kRouterSmem = 2 * kTile + kKbImg + 1024;  // two U tiles, one key-mean image (one CTA per SM)
 
 // Persistent: CTA b handles the contiguous tile range [b*per, (b+1)*per) of the
 // (bh, chunk) tiles, so consecutive tiles share a head and its kbar image.
@@ -613,7 +592,7 @@ constexpr size_t kRouterSmem = 3 * kTile + 1024;  // two U tiles, one kbar image
 // GRM / Soup softmax, or SSC -- with the online score r_on, written as g_{t,i}
 // ([N][L] per head, 0 where not taken) and the online gate.
 template <int MODE>
-__global__ void __launch_bounds__(kRouterThreads, 2) gate_tiles_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
+__global__ void __launch_bounds__(kRouterThreads, 1) gate_tiles_tc(const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -656,8 +635,8 @@ __global__ void __launch_bounds__(kRouterThreads, 2) gate_tiles_tc(const __grid_
                 const int bh = it / chunks, t0 = (it % chunks) * kCT;
                 if (bh != prev_bh) {
                     if (!mbar_wait(&kb_empty, (kb_round & 1) ^ 1, &abort_flag)) break;
-                    mbar_arrive_expect_tx(&kb_full, kTile);
-                    bulk_load(sKb, a.kbar_img + (size_t)bh * kTile, kTile, &kb_full);
+                    mbar_arrive_expect_tx(&kb_full, kKbImg);
+                    bulk_load(sKb, a.kbar_img + (size_t)bh * kKbImg, kKbImg, &kb_full);
                     ++kb_round;
                     prev_bh = bh;
                 }
@@ -687,10 +666,11 @@ __global__ void __launch_bounds__(kRouterThreads, 2) gate_tiles_tc(const __grid_
                 const uint64_t dU = make_desc_sw128(smem_u32(sU + b * kTile), 0, 1024);
                 const uint32_t td = tb + b * 64;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) mma_ss(td, dU + (kmaj_off(kk, 128) >> 4), dKb + (kmaj_off(kk, 64) >> 4), idS, kk > 0);
+                for (int term = 0; term < 3; ++term)  // hi, mid, lo
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(td, dU + (kmaj_off(kk, 128) >> 4), dKb + ((16384 + kmaj_off(kk, 64)) >> 4), idS, 1);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(td, dU + (kmaj_off(kk, 128) >> 4), dKb + ((term * kKbPanel + kmaj_off(kk, 64)) >> 4), idS,
+                               (term | kk) != 0);
                 mma_commit(&s_full[b]);
                 mma_commit(&u_empty[b]);
                 if (it + 1 == last || (it + 1) / chunks != bh) mma_commit(&kb_empty);  // last tile of this head
@@ -748,7 +728,6 @@ __global__ void __launch_bounds__(kRouterThreads, 2) gate_tiles_tc(const __grid_
 // ============================================================================
 constexpr int kT2Threads = 192;    // warp 0 TMA, warp 1 MMA issuer, warps 2-5 token-row workers
 constexpr int kT2CtasPerSm = 2;    // two CTAs share each SM's tensor pipe
-constexpr uint32_t kPanel = 16384; // one 128 x 64 bf16 operand panel (SWIZZLE_128B)
 constexpr int kRing = 6;           // operand panels in flight per CTA
 constexpr uint32_t kT2Cols = 256;  // tensor memory per CTA: D (128 columns) | A slot 0 | A slot 1 (64 each)
 constexpr uint32_t kT2Decay = 4 * 5 * kCT * 4;   // SWLA: per worker warp, ell | lambda | beta_next | E | F of a chunk
@@ -850,7 +829,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // Panel sequence of a tile: (gated) U0 U1 KBhi KBlo (gate scores), Q0 K0 Q1 K1
+        // Panel sequence of a tile: (gated) U0 U1 KBhi KBmid KBlo (gate scores), Q0 K0 Q1 K1
         // (G), V0 V1 (P V), then both K panels of every cached operand.  The workers
         // release the Q panels.
         if (lane == 0 && my_tiles > 0) {
@@ -880,15 +859,15 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     }
                 }
                 uint8_t *dst = nullptr;
-                if (GATED) {  // U (two K panels) and the head's key-mean image (hi rows, lo rows)
+                if (GATED) {  // U (two K panels) and the head's key-mean image (hi, mid, lo rows)
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!(ok = (dst = slot()) != nullptr)) break;
                         tma_load_2d(dst, &mU, 64 * h, rr, &ring_full[g % kRing]);
                         ++g;
                     }
-                    for (int h = 0; h < 2 && ok; ++h) {
+                    for (int h = 0; h < 3 && ok; ++h) {
                         if (!(ok = (dst = slot()) != nullptr)) break;
-                        bulk_load(dst, a.kbar_img + (size_t)t.bh * kTile + h * kPanel, kPanel, &ring_full[g % kRing]);
+                        bulk_load(dst, a.kbar_img + (size_t)t.bh * kKbImg + h * kKbPanel, kPanel, &ring_full[g % kRing]);
                         ++g;
                     }
                 }
@@ -936,15 +915,17 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
                 if (GATED) {
-                    // gate scores S = U (kbar_hi + kbar_lo)^T into the tile's first A slot (the
-                    // workers read S there, then write P over it); the slot's last readers were
-                    // issued before this
+                    // gate scores S = U (kbar_hi + kbar_mid + kbar_lo)^T into the tile's first A slot
+                    // (the workers read S there, then write P over it); the slot's last readers
+                    // were issued before this
                     constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
                     const uint32_t ts = tA0 + (ac % 2) * 64;
-                    if (!(ok = ring_ready(g) && ring_ready(g + 1) && ring_ready(g + 2) && ring_ready(g + 3))) break;
+                    if (!(ok = ring_ready(g) && ring_ready(g + 1) && ring_ready(g + 2) && ring_ready(g + 3) &&
+                               ring_ready(g + 4)))
+                        break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {  // hi rows, then lo rows
+                    for (int kb = 0; kb < 3; ++kb) {  // hi rows, mid rows, lo rows
                         const uint64_t dkb = make_desc_sw128(s_base + ((g + 2 + kb) % kRing) * kPanel, 0, 1024);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -954,9 +935,9 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                                 mma_ss(ts, du + 2 * kk, dkb + ((8192u * h) >> 4) + 2 * kk, idS, (kb | h | kk) != 0);
                         }
                     }
-                    for (int i = 0; i < 4; ++i) mma_commit(&ring_empty[(g + i) % kRing]);
+                    for (int i = 0; i < 5; ++i) mma_commit(&ring_empty[(g + i) % kRing]);
                     mma_commit(&s_full);
-                    g += 4;
+                    g += 5;
                 }
                 if (!(ok = mbar_wait(&y_empty, (j & 1) ^ 1, &abort_flag))) break;  // D of tile j-1 drained
                 // G = Q K^T
@@ -1044,7 +1025,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             float gn = a.mean ? 1.f / (float)(t.n + 1) : 1.f;  // Residual: 1
             if (GATED) {
                 // the token's gates from the scores S in this tile's first A slot
-                g += 4;  // the U and key-mean panels, released by the issuer
+                g += 5;  // the U and key-mean panels, released by the issuer
                 const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
                 const float ron = __ldg(a.r_on + tok);
                 if (!(ok = mbar_wait(&s_full, j & 1, &abort_flag))) break;
@@ -1264,8 +1245,6 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_device_abort, 1);
 }
 
-size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
-
 int g_num_sms = 0;
 
 }  // namespace
@@ -1293,7 +1272,7 @@ bool tc_supported(const Problem &p)
 size_t tc_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
-    size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) +
+    size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kKbImg) +
                pad256(sizeof(float) * BH * p.L);
     if (!mode_uses_u(p.mode)) b += pad256(BH * N * kTile);  // prefix sums of the states
     return b;
@@ -1301,7 +1280,7 @@ size_t tc_scratch_bytes(const Problem &p)
 
 // SSC router alone (mc_ssc_select) on the tensor-core path's shapes: key-mean
 // images, then the router kernel.
-size_t tc_select_scratch_bytes(const Problem &p) { return pad256((size_t)p.BH * kTile); }
+size_t tc_select_scratch_bytes(const Problem &p) { return pad256((size_t)p.BH * kKbImg); }
 
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
 {
@@ -1314,7 +1293,7 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
     a.C = p.C;
     a.N = p.N;
     a.CPS = p.C / kCT;
-    a.d = p.d;
+    a.d = p.d; a.NB = (p.N + 63) / 64;
     CUtensorMap mU;
     if (!make_tmap_bf16_sw128(&mU, fa.u, (unsigned long long)p.BH * p.L, p.d, 128)) return cudaErrorInvalidValue;
     if (g_num_sms == 0) {
@@ -1323,14 +1302,14 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
         cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (g_num_sms <= 0) g_num_sms = 148;
     }
-    cudaError_t e = cudaMemsetAsync(a.kbar_img, 0, (size_t)p.BH * kTile, s);
+    cudaError_t e = cudaMemsetAsync(a.kbar_img, 0, (size_t)p.BH * kKbImg, s);
     if (e != cudaSuccess) return e;
     kbar_images_tc<<<(unsigned)(p.BH * p.N), kD, 0, s>>>(static_cast<const __nv_bfloat16 *>(fa.k), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(gate_tiles_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
     if (e != cudaSuccess) return e;
     const int gtiles = p.BH * (p.L / kCT);
-    const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
+    const int ggrid = gtiles < g_num_sms ? gtiles : g_num_sms;
     gate_tiles_tc<0><<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
     return cudaGetLastError();
 }
@@ -1338,7 +1317,7 @@ cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &fa, void *scra
 size_t tc_state_scratch_bytes(const Problem &p)
 {
     const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
-    return pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kTile) + pad256(sizeof(float) * BH * p.L);
+    return pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kKbImg) + pad256(sizeof(float) * BH * p.L);
 }
 
 // The forward's segment-state kernel alone (plain update): the fp32 states, their and
@@ -1358,11 +1337,11 @@ cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, 
     a.spre_img = base;
     base += pad256(BH * N * CPS * kTile);
     a.kbar_img = base;
-    base += pad256(BH * kTile);
+    base += pad256(BH * kKbImg);
     a.r_on = reinterpret_cast<float *>(base);
     a.kbar_out = gated ? fa.kbar : nullptr;
     a.kpre_out = gated ? fa.kpre_tiles : nullptr;
-    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = (int)CPS; a.d = p.d;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = (int)CPS; a.d = p.d; a.NB = (p.N + 63) / 64;
     a.num_tiles = (int)(BH * N * CPS);
     CUtensorMap mK, mV, mU;
     const unsigned long long rows = (unsigned long long)BH * p.L;
@@ -1380,7 +1359,7 @@ cudaError_t launch_state_tc(const Problem &p, const FwdArgs &fa, void *scratch, 
         if (g_num_sms <= 0) g_num_sms = 148;
     }
     cudaError_t e;
-    if (gated && (e = cudaMemsetAsync(a.kbar_img, 0, BH * kTile, s)) != cudaSuccess) return e;
+    if (gated && (e = cudaMemsetAsync(a.kbar_img, 0, BH * kKbImg, s)) != cudaSuccess) return e;
     auto k1 = gated ? seg_state_tc<true, false> : seg_state_tc<false, false>;
     const size_t smem1 = t1_smem_bytes<false>();
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
@@ -1403,14 +1382,14 @@ cudaError_t launch_bwd_gates_tc(const Problem &p, const void *u, const TcImages 
     a.gam_out = gam;
     a.tok_out = tok;
     a.topk = p.topk;
-    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kCT; a.d = p.d;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = p.C / kCT; a.d = p.d; a.NB = (p.N + 63) / 64;
     CUtensorMap mU;
     if (!make_tmap_bf16_sw128(&mU, u, (unsigned long long)p.BH * p.L, p.d, 128)) return cudaErrorInvalidValue;
     auto k = p.mode == MC_SSC ? gate_tiles_tc<2> : gate_tiles_tc<1>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterSmem);
     if (e != cudaSuccess) return e;
     const int gtiles = p.BH * (p.L / kCT);
-    const int ggrid = gtiles < 2 * g_num_sms ? gtiles : 2 * g_num_sms;
+    const int ggrid = gtiles < g_num_sms ? gtiles : g_num_sms;
     k<<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
     return cudaGetLastError();
 }
@@ -1430,7 +1409,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.spre_img = base;
     base += pad256(BH * N * CPS * kTile);
     a.kbar_img = base;
-    base += pad256(BH * kTile);
+    base += pad256(BH * kKbImg);
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
@@ -1442,7 +1421,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.C = p.C;
     a.N = p.N;
     a.CPS = (int)CPS;
-    a.d = p.d;
+    a.d = p.d; a.NB = (p.N + 63) / 64;
     a.num_tiles = (int)(BH * N * CPS);
 
     CUtensorMap mQ, mK, mV, mV64, mU;
@@ -1465,7 +1444,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     }
     cudaError_t e;
     if (gated) {
-        e = cudaMemsetAsync(a.kbar_img, 0, BH * kTile, s);
+        e = cudaMemsetAsync(a.kbar_img, 0, BH * kKbImg, s);
         if (e != cudaSuccess) return e;
     }
 
