@@ -55,21 +55,48 @@ def segment_counts(w):
     return s, n
 
 
+def factorised_reads(w):
+    """Per head, sum over tokens of the earlier tokens the factorised readout must read:
+    y_t = sum_j g_{t,seg(j)} v_j (k_j . q_t) over j <= t in the memories token t reads
+    (every earlier token for GRM / Soup / Mean and for Residual's plain causal sum; for
+    SSC its own segment's tokens up to t and the topk selected segments)."""
+    C, L = w.seg_len, w.L
+    if w.mode != SSC:
+        return L * (L + 1) // 2
+    tot = 0
+    for t in range(L):
+        s = t // C
+        tot += min(w.topk, s) * C + (t - s * C + 1)
+    return tot
+
+
 def algorithmic_flops(w):
-    """Per step, all heads: online write + read (4 d^2 per token), cached reads
-    (2 d^2 per token and cached segment read), gate scores (2 d per token and score).
-    Split by kernel: "state" is the online write (2 d^2 per token, the segment-state
-    kernel); "readout" the online read, the cached reads and the gate scores."""
+    """Per step, all heads.  State form (the segment-state and readout kernels): online
+    write + read (4 d^2 per token), cached reads (2 d^2 per token and cached segment read),
+    gate scores (2 d per token and score).  Factorised form (the piece-state, gate and
+    factorised readout kernels): the cached states written (2 d^2 per token), 4 d per token
+    and earlier token read (k_j . q_t, then v_j times it), the same gate scores.  The
+    method's work ("total") is the smaller of the two; each kernel is credited with its
+    own form's share."""
     s, n = segment_counts(w)
     d = w.d
+    bh = w.B * w.H
     per_head_online = w.L * 4 * d * d
     per_head_cached = 2 * d * d * sum(n)
-    per_head_gate = 0 if w.mode == RESIDUAL else 2 * d * sum(s)
-    bh = w.B * w.H
-    return {"total": bh * (per_head_online + per_head_cached + per_head_gate),
+    per_head_gate = 0 if w.mode in (RESIDUAL, mc_inputs.MEAN) else 2 * d * sum(s)
+    state_form = per_head_online + per_head_cached + per_head_gate
+    fact_read = 4 * d * factorised_reads(w)
+    fact_form = w.L * 2 * d * d + fact_read + per_head_gate
+    return {"total": bh * min(state_form, fact_form),
+            "state_form": bh * state_form, "factorised_form": bh * fact_form,
             "online": bh * per_head_online,
             "state": bh * per_head_online // 2,
-            "readout": bh * (per_head_online // 2 + per_head_cached + per_head_gate)}
+            "readout": bh * (per_head_online // 2 + per_head_cached + per_head_gate),
+            "seg_state_tc": bh * per_head_online // 2,
+            "readout_tc": bh * (per_head_online // 2 + per_head_cached + per_head_gate),
+            "seg_piece_tc": bh * w.L * 2 * d * d,
+            "gates_tc": bh * per_head_gate,
+            "readout_fact_tc": bh * fact_read}
 
 
 def algorithmic_bytes(w):
@@ -82,16 +109,23 @@ def algorithmic_bytes(w):
 def kernel_bytes(w):
     """Algorithmic bytes per launch of each tensor-core kernel, given the split of the
     step between them: what each must read and write at least.  The segment-state
-    kernel reads k, v (and u for the routed aggregations) and writes the fp32 states;
-    the readout reads q, k, v (u), every cached state once as a bf16 operand, and
-    writes y.  Scratch images that only pass between the kernels are not counted."""
+    kernels read k, v (and u for the routed aggregations) and write the fp32 states;
+    the state-form readout reads q, k, v (u), every cached state once as a bf16 operand,
+    and writes y; the gate kernel reads u and writes the bf16 gates; the factorised
+    readout reads q, k, v and the gates and writes y.  Scratch images that only pass
+    between the kernels are not counted."""
     elt = 2 if w.dtype == "bf16" else 4
     bh = w.B * w.H
     row = w.L * w.d * elt
     routed = w.mode not in (RESIDUAL, mc_inputs.MEAN)
     st32 = w.N * w.d * w.d * 4
+    s, _ = segment_counts(w)
+    gate_bytes = 2 * (sum(s)) if routed else 0  # bf16 gates, one per token and memory it reads
     return {"seg_state_tc": bh * ((3 if routed else 2) * row + st32),
-            "readout_tc": bh * ((5 if routed else 4) * row + st32 // 2)}
+            "readout_tc": bh * ((5 if routed else 4) * row + st32 // 2),
+            "seg_piece_tc": bh * ((3 if routed else 2) * row + st32),
+            "gates_tc": bh * (row + gate_bytes),
+            "readout_fact_tc": bh * (4 * row + gate_bytes)}
 
 
 def workload_bound(w, peaks):
@@ -369,7 +403,7 @@ def run_ours(args, w, wname="long-grm"):
         avg_ms = sum(dom_ms) / len(dom_ms)
         tensor = "tc" in dom_name
         dtype_path = "bf16" if tensor else "f32"
-        work = flops["readout"] if "readout" in dom_name else flops["state"]
+        work = flops.get(dom_name, flops["readout"] if "readout" in dom_name else flops["state"])
         achieved = work / (avg_ms / 1e3) / 1e12
         if tensor:
             sustained = max_ms > 1000.0
@@ -695,7 +729,7 @@ def run_reference(args, w):
 
 
 WORKLOADS = {"long-grm": mc_inputs.LONG_GRM, "grm-d64": mc_inputs.GRM_D64, "ssc": mc_inputs.SSC_D128,
-             "swla-grm": mc_inputs.SWLA_LONG,
+             "swla-grm": mc_inputs.SWLA_LONG, "fact-c32": mc_inputs.FACT_C32, "long-c512": mc_inputs.LONG_C512,
              "tiny": mc_inputs.TINY, **{f"sweep-c{w.seg_len}": w for w in mc_inputs.SWEEP}}
 
 

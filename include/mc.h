@@ -43,6 +43,15 @@
  *     on the same stream; the pool keeps freed blocks for later calls until
  *     mc_trim_scratch().  Calls on different streams are independent.
  *   - d must be 16, 32, 64 or 128.  B, H, L, seg_len >= 1.
+ *   - The kernels are chosen per shape.  bf16 inputs with d = 64 or 128 run on the
+ *     tensor cores: the cached readout in the state form (every cached state read
+ *     once per 128-token tile, a C x d by d x (N d) product) when seg_len is a
+ *     multiple of 128, L a multiple of seg_len and N <= 64; otherwise, when seg_len
+ *     is a multiple of 16 (N <= 512 for the routed aggregations), in the factorised
+ *     form y_t = sum_{j <= t} g_{t, seg(j)} v_j (k_j . q_t), which costs 4 d t per
+ *     token instead of 2 d^2 (N - 1) and so wins for segments shorter than d / 2
+ *     ([MC-sum §2.2]: the read is O(N) per token).  Everything else (fp32 inputs,
+ *     d = 16 or 32, other segment lengths) runs on CUDA-core kernels.
  *   - Return value: MC_OK (0) or a negative MC_ERR_* code (shape is checked
  *     first, then the mode, then pointers).  On an argument
  *     error nothing is enqueued.  On MC_ERR_CUDA the contents of y and states
@@ -256,6 +265,20 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u,
 int mc_forward_noalloc(const void *q, const void *k, const void *v, const void *u,
                        int B, int H, int L, int d, int seg_len, int agg_mode, int topk,
                        void *y, float *states, mc_stream_t stream);
+
+/*
+ * mc_set_readout_form -- how later forward calls in this process choose the form
+ *   of the cached readout on the tensor cores (a switch for measurement; the
+ *   library does not need it):
+ *     MC_READOUT_AUTO        (0) per shape, as described at the top (the default);
+ *     MC_READOUT_FACTORISED  (1) the factorised form wherever it applies, also on
+ *                                shapes the state form would take.
+ *   Both give the same y up to rounding.  Returns the previous setting (>= 0), or
+ *   MC_ERR_MODE for an unknown form.  The setting is process-wide; change it only
+ *   while no forward call is being made on another thread.
+ */
+enum { MC_READOUT_AUTO = 0, MC_READOUT_FACTORISED = 1 };
+int mc_set_readout_form(int form);
 
 /*
  * mc_trim_scratch -- return the scratch memory cached by the library's pool on

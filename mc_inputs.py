@@ -53,7 +53,7 @@ class Workload:
         return Workload(**d)
 
 
-# The synthetic workloads.  seed = the workload's index in this list (tiny = 0).
+# The synthetic workloads, each with its own seed (tiny = 0).
 TINY = Workload("tiny-grm B1 H1 L256 d16 C64 fp32", 1, 1, 256, 16, 64, GRM, "f32", seed=0)
 GRM_D64 = Workload("grm B4 H8 L4096 d64 C256 bf16", 4, 8, 4096, 64, 256, GRM, "bf16", seed=1)
 SWEEP = tuple(
@@ -67,7 +67,13 @@ LONG_GRM = Workload("long-grm B1 H16 L65536 d128 C1024 bf16", 1, 16, 65536, 128,
 SWLA_LONG = Workload("swla-grm B1 H16 L65536 d128 C1024 bf16", 1, 16, 65536, 128, 1024, GRM, "bf16",
                      seed=5, swla=True)
 
-ALL = (TINY, GRM_D64) + SWEEP + (SSC_D128, LONG_GRM, SWLA_LONG)
+# Short segments (seg_len < d / 2), where the cached readout runs in the factorised form:
+# the sweep's batch, heads, length and head dimension at seg_len 32 (N = 256).
+FACT_C32 = Workload("fact-grm B8 H16 L8192 d128 C32 bf16", 8, 16, 8192, 128, 32, GRM, "bf16", seed=8)
+# The long-context workload with twice as many, shorter segments (N = 128).
+LONG_C512 = Workload("long-grm B1 H16 L65536 d128 C512 bf16", 1, 16, 65536, 128, 512, GRM, "bf16", seed=9)
+
+ALL = (TINY, GRM_D64) + SWEEP + (SSC_D128, LONG_GRM, SWLA_LONG, FACT_C32, LONG_C512)
 
 
 def _np_inputs(B: int, H: int, L: int, d: int, seed: int):

@@ -25,8 +25,9 @@ MC_ERR_ALLOC, MC_ERR_CUDA, MC_ERR_DEVICE_TIMEOUT, MC_ERR_ALIGN, MC_ERR_DEVICE = 
 MC_ERR_SCRATCH = -10
 
 EXPORTED = ("mc_forward", "mc_forward_f32", "mc_forward_swla", "mc_forward_segments", "mc_log_segments", "mc_backward", "mc_backward_f32", "mc_decode_step", "mc_ssc_select", "mc_forward_host", "mc_forward_noalloc",
-            "mc_check_device", "mc_trim_scratch", "mc_profile_begin", "mc_profile_end", "mc_profile_stage",
-            "mc_status_string")
+            "mc_check_device", "mc_trim_scratch", "mc_set_readout_form", "mc_profile_begin", "mc_profile_end",
+            "mc_profile_stage", "mc_status_string")
+MC_READOUT_AUTO, MC_READOUT_FACTORISED = 0, 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmc.so")
@@ -72,6 +73,8 @@ def load_library():
     lib.mc_forward_noalloc.restype = i
     lib.mc_trim_scratch.argtypes = []
     lib.mc_trim_scratch.restype = i
+    lib.mc_set_readout_form.argtypes = [i]
+    lib.mc_set_readout_form.restype = i
     lib.mc_check_device.argtypes = [vp]
     lib.mc_check_device.restype = i
     lib.mc_profile_begin.argtypes = [vp, i]
@@ -328,6 +331,15 @@ def mc_check_device(stream=None) -> int:
     """Synchronise the stream and return MC_OK or MC_ERR_DEVICE_TIMEOUT (a kernel gave up
     on a bounded wait since the last check)."""
     return load_library().mc_check_device(_stream_handle(stream, torch.device("cuda")))
+
+
+def mc_set_readout_form(form: int) -> int:
+    """MC_READOUT_AUTO (the default) or MC_READOUT_FACTORISED for later forward calls;
+    returns the previous setting."""
+    st = load_library().mc_set_readout_form(int(form))
+    if st < 0:
+        raise MCError(st, "mc_set_readout_form")
+    return st
 
 
 def mc_trim_scratch() -> int:

@@ -2,6 +2,7 @@
 // scratch, and the choice of kernels for a shape.
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -77,6 +78,8 @@ void profile_after_kernel(cudaStream_t s, const char *name)
 }
 
 namespace {
+
+std::atomic<int> g_readout_form{MC_READOUT_AUTO};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -162,7 +165,8 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     st = check_device();
     if (st != MC_OK) return st;
 
-    if (tc_supported(p)) {
+    const bool factorised = g_readout_form.load() == MC_READOUT_FACTORISED && !swla && gen_supported(p);
+    if (tc_supported(p) && !factorised) {
         const size_t b_states = states ? 0 : round_up(sizeof(float) * (size_t)p.BH * p.N * d * d);
         void *scratch = nullptr;
         if (scratch_alloc(&scratch, b_states + tc_scratch_bytes(p), stream) != cudaSuccess) {
@@ -180,6 +184,28 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
         cudaError_t e = launch_forward_tc(p, a, static_cast<char *>(scratch) + b_states, stream);
         cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e != cudaSuccess || ef != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_CUDA;
+        }
+        return MC_OK;
+    }
+
+    if (gen_supported(p)) {  // any seg_len a multiple of 16: the factorised readout on the tensor cores
+        void *scratch = nullptr;
+        const size_t bytes = gen_scratch_bytes(p);
+        if (bytes && scratch_alloc(&scratch, bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_ALLOC;
+        }
+        FwdArgs a{};
+        a.q = q; a.k = k; a.v = v;
+        a.u = mode_uses_u(p.mode) ? u : nullptr;
+        a.y = y;
+        a.states = states;  // NULL: the states are not needed by this path and not formed
+        a.BH = p.BH; a.L = L; a.C = seg_len; a.N = p.N; a.mode = p.mode; a.topk = p.topk;
+        cudaError_t e = launch_forward_gen(p, a, scratch, stream);
+        cudaError_t ef = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
         if (e != cudaSuccess || ef != cudaSuccess) {
             cudaGetLastError();
             return MC_ERR_CUDA;
@@ -503,6 +529,22 @@ int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int 
         }
         return MC_OK;
     }
+    if (mc::gen_supported(p)) {  // the general path's own router, bit for bit
+        void *scratch = nullptr;
+        if (mc::scratch_alloc(&scratch, mc::gen_select_scratch_bytes(p), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_ALLOC;
+        }
+        mc::FwdArgs a{};
+        a.k = k; a.u = u; a.sel_out = idx;
+        cudaError_t e = mc::launch_ssc_select_gen(p, a, scratch, stream);
+        cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e != cudaSuccess || ef != cudaSuccess) {
+            cudaGetLastError();
+            return MC_ERR_CUDA;
+        }
+        return MC_OK;
+    }
     float *kbar = nullptr;
     if (mc::scratch_alloc(reinterpret_cast<void **>(&kbar), sizeof(float) * (size_t)p.BH * p.N * d, stream) !=
         cudaSuccess) {
@@ -621,6 +663,12 @@ int mc_forward_host(const void *q, const void *k, const void *v, const void *u, 
     return MC_OK;
 }
 
+int mc_set_readout_form(int form)
+{
+    if (form != MC_READOUT_AUTO && form != MC_READOUT_FACTORISED) return MC_ERR_MODE;
+    return mc::g_readout_form.exchange(form);
+}
+
 int mc_trim_scratch(void)
 {
     std::lock_guard<std::mutex> lock(mc::g_pool_mu);
@@ -642,12 +690,13 @@ int mc_check_device(mc_stream_t stream)
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    int was = 0, was_bwd = 0;
-    if (mc::take_device_abort(&was) != cudaSuccess || mc::take_bwd_abort(&was_bwd) != cudaSuccess) {
+    int was = 0, was_bwd = 0, was_gen = 0;
+    if (mc::take_device_abort(&was) != cudaSuccess || mc::take_bwd_abort(&was_bwd) != cudaSuccess ||
+        mc::take_gen_abort(&was_gen) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    return was || was_bwd ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
+    return was || was_bwd || was_gen ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
 }
 
 int mc_profile_begin(void *const *events, int capacity)

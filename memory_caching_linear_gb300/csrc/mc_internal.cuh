@@ -143,6 +143,16 @@ cudaError_t launch_bwd_gates_tc(const Problem &p, const void *u, const TcImages 
 // Reads and clears the device-side record of an abandoned bounded wait.
 cudaError_t take_device_abort(int *was_set);
 
+// General tensor-core path (k_gen.cu): bf16, d in {64, 128}, seg_len a multiple of 16,
+// any L (a ragged last segment), N <= 512 for the routed aggregations, SSC topk <= 16.
+// The cached readout runs in the factorised form sum_j g_{t,seg(j)} v_j (k_j . q_t).
+bool gen_supported(const Problem &p);
+size_t gen_scratch_bytes(const Problem &p);
+cudaError_t launch_forward_gen(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+size_t gen_select_scratch_bytes(const Problem &p);
+cudaError_t launch_ssc_select_gen(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+cudaError_t take_gen_abort(int *was_set);
+
 // SIMT kernels (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_seg_scan_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_readout_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);

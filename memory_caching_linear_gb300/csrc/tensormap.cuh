@@ -1,4 +1,4 @@
-// tensormap.cuh -- host helper: 2-D bf16 TMA descriptors with 128-byte swizzle,
+// tensormap.cuh -- host helpers: 2-D and 3-D bf16 TMA descriptors with 128-byte swizzle,
 // encoded through the driver entry point (no link-time dependency on libcuda).
 #pragma once
 
@@ -48,6 +48,25 @@ inline bool make_tmap_bf16_sw128(CUtensorMap *map, const void *base, unsigned lo
                                  unsigned long long cols, unsigned box_rows)
 {
     return make_tmap_bf16(map, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// A [heads][rows][cols] bf16 tensor (row-major, contiguous) moved in boxes of
+// box_rows x 64 elements of one head, 128-byte swizzled.  Coordinates are (column,
+// row, head); rows at or past `rows` read as zeros (the TMA's out-of-bounds fill), so
+// a box that runs past a head's last row never touches the next head.
+inline bool make_tmap_bf16_3d_sw128(CUtensorMap *map, const void *base, unsigned long long heads,
+                                    unsigned long long rows, unsigned long long cols, unsigned box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {cols, rows, heads};
+    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace mc

@@ -138,6 +138,59 @@ def test_parity_tensor_core_ssc(name, B, H, L, d, C, topk):
     assert rel_err(st, ref["states"]) <= TOL["bf16"]
 
 
+# Shapes of the general tensor-core path, where the cached readout runs in the factorised
+# form sum_j g_{t,seg(j)} v_j (k_j . q_t): segments shorter than a 128-token tile (several
+# per tile), longer but not a multiple of it (segments straddle tiles), a ragged last
+# segment, more than 64 segments up to the path's 512, d = 64 and 128.
+GEN_CASES = [
+    ("gen-C16-N128", 1, 2, 2048, 128, 16),
+    ("gen-C32-N64", 1, 2, 2048, 128, 32),
+    ("gen-C64-N16", 2, 1, 1024, 128, 64),
+    ("gen-C96-ragged", 1, 2, 1000, 128, 96),
+    ("gen-d64-C48-ragged", 1, 2, 1500, 64, 48),
+    ("gen-C384-ragged", 1, 1, 2000, 128, 384),
+    ("gen-d64-C16-N512", 1, 1, 8192, 64, 16),
+]
+
+
+@pytest.mark.parametrize("mode,topk", [(RESIDUAL, 0), (GRM, 0), (SOUP, 0), (SSC, 0), (SSC, 3), (SSC, 16), (MEAN, 0)])
+@pytest.mark.parametrize("name,B,H,L,d,C", GEN_CASES, ids=[c[0] for c in GEN_CASES])
+def test_parity_general_path(name, B, H, L, d, C, mode, topk):
+    """The general tensor-core path (segment pieces, gates in HBM, factorised readout)
+    against the oracle, element by element: y and the cached states."""
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype="bf16")
+    ref = oracle.forward(q, k, v, u, C, mode, topk)
+    y, st = run_gpu(q, k, v, u, C, mode, topk)
+    yref = ref["y"]
+    N = (L + C - 1) // C
+    if mode == SSC and 0 < topk < N - 1:
+        yref = check_ssc_selection(q, k, v, u, C, topk, ref, TOL["bf16"])
+    assert rel_err(y, yref) <= TOL["bf16"], (name, mode, topk, rel_err(y, yref))
+    assert rel_err(st, ref["states"]) <= TOL["bf16"], (name, mode, rel_err(st, ref["states"]))
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (RESIDUAL, 0), (SSC, 4), (MEAN, 0)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_readout_forms_agree(d, mode, topk):
+    """On a shape both forms take (seg_len 128, N = 16), the factorised readout and the
+    state form give the same y within the bf16 bound, and the same states bit for bit
+    up to the fp32 order of the sums."""
+    q, k, v, u = (t.cuda() for t in make_inputs(1, 2, 2048, d, 90 + d, "bf16"))
+    y_state, st_state = mcl.mc_forward(q, k, v, u, 128, mode, topk)
+    prev = mcl.mc_set_readout_form(mcl.MC_READOUT_FACTORISED)
+    try:
+        y_fact, st_fact = mcl.mc_forward(q, k, v, u, 128, mode, topk)
+    finally:
+        mcl.mc_set_readout_form(prev)
+    torch.cuda.synchronize()
+    assert mcl.mc_check_device() == mcl.MC_OK
+    a, b = y_fact.float().cpu().numpy(), y_state.float().cpu().numpy()
+    assert rel_err(a, b) <= TOL["bf16"]
+    assert rel_err(st_fact.cpu().numpy(), st_state.cpu().numpy()) <= 1e-5
+    assert mcl.mc_set_readout_form(mcl.MC_READOUT_AUTO) == mcl.MC_READOUT_AUTO
+
+
 @pytest.mark.parametrize("name,B,H,L,d,C,dtype", [("mean-tc", 1, 2, 2048, 128, 256, "bf16"),
                                                   ("mean-ffma", 1, 2, 300, 32, 64, "f32")])
 def test_mean_needs_no_u(name, B, H, L, d, C, dtype):
