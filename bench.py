@@ -749,6 +749,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run a slice of the workload: B = 1 and this many heads (for profiler captures)")
+    ap.add_argument("--readout", choices=["auto", "factorised"], default="auto",
+                    help="form of the cached readout (mc_set_readout_form)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -766,6 +770,14 @@ def main(argv=None):
             print(json.dumps(run_backward(args, WORKLOADS[name], name)), flush=True)
         return
     w = WORKLOADS[args.workload]
+    if args.heads:
+        w = w.with_(B=1, H=args.heads, name=f"{w.name} (slice: B1 H{args.heads})")
+    if args.readout == "factorised" and args.impl == "ours":
+        import memory_caching_linear_gb300 as mcl
+        from memory_caching_linear_gb300 import build as mcbuild
+        mcbuild.build()
+        mcl.mc_set_readout_form(mcl.MC_READOUT_FACTORISED)
+        w = w.with_(name=f"{w.name} (factorised readout)")
     if args.mode:
         w = w.with_(mode={"residual": RESIDUAL, "grm": GRM, "soup": 2, "ssc": SSC}[args.mode])
     res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w, args.workload)

@@ -382,14 +382,16 @@ constexpr int kGMaxN = 512;                                  // cached segments 
 
 // Persistent, one CTA per SM over contiguous ranges of (bh, 128-token tile).  Per tile the
 // scores against every cached segment its last token sees go to tensor memory (blocks of
-// 64 segments, 64 columns each); each worker thread then forms its token's gates.
+// 64 segments, 64 columns each); each worker thread then forms its token's gates.  With
+// at most 256 segments two tiles' scores fit, so the next tile's MMAs run while the
+// workers read this one's.
 template <bool SSC>
 __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__ CUtensorMap mU, GenArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sU = sm, *sKb = sm + 2 * kTile;
-    __shared__ uint64_t u_full[2], u_empty[2], kb_full[2], kb_empty[2], s_full, t_free, fin;
+    __shared__ uint64_t u_full[2], u_empty[2], kb_full[2], kb_empty[2], s_full[2], t_free[2], fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -416,8 +418,10 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
             mbar_init(&kb_full[i], 1);
             mbar_init(&kb_empty[i], 1);
         }
-        mbar_init(&s_full, 1);
-        mbar_init(&t_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&t_free[i], 128);
+        }
         mbar_init(&fin, 1);
         fence_mbar_init();
     }
@@ -425,6 +429,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
+    const int nbuf = (a.N - 1 + 63) / 64 <= 4 ? 2 : 1;  // score buffers of 256 columns, or one of 512
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tensormap(&mU);
@@ -454,10 +459,12 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
             bool ok = true, issued = false;
             for (int it = first; it < last && ok; ++it) {
                 const int i = it - first, ub = i & 1;
-                if (!(ok = mbar_wait(&t_free, (i & 1) ^ 1, &abort_flag))) break;  // the previous tile's scores are read
+                const int sb = i % nbuf, use = i / nbuf;  // score buffer, and its use count
+                if (!(ok = mbar_wait(&t_free[sb], (use & 1) ^ 1, &abort_flag))) break;  // its last scores are read
                 if (!(ok = mbar_wait(&u_full[ub], (i >> 1) & 1, &abort_flag))) break;
                 tc_fence_after();
                 const int nblk = tile_blocks(it);
+                const uint32_t ts = tb + 256 * sb;
                 const uint64_t dU = make_desc_sw128(smem_u32(sU + ub * kTile), 0, 1024);
                 for (int blk = 0; blk < nblk; ++blk, ++kbc) {
                     const int slot = kbc & 1;
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
                     for (int term = 0; term < 3; ++term)  // hi, mid, lo
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tb + 64 * blk, dU + (kmaj_off(kk, 128) >> 4),
+                            mma_ss(ts + 64 * blk, dU + (kmaj_off(kk, 128) >> 4),
                                    dKb + ((term * kKbPanel + kmaj_off(kk, 64)) >> 4), idS, (term | kk) != 0);
                     mma_commit(&kb_empty[slot]);
                     issued = true;
@@ -476,10 +483,10 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
                 if (!ok) break;
                 if (nblk > 0) {
                     mma_commit(&u_empty[ub]);
-                    mma_commit(&s_full);
+                    mma_commit(&s_full[sb]);
                 } else {  // no cached segment yet: nothing was issued
                     mbar_arrive(&u_empty[ub]);
-                    mbar_arrive(&s_full);
+                    mbar_arrive(&s_full[sb]);
                 }
             }
             if (issued) {  // leave no MMA in flight
@@ -501,42 +508,44 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
             const int st = min(t, a.L - 1) / a.C;  // cached segments of this token
             const int nblk = tile_blocks(it);
             const float ron = valid ? a.r_on[(size_t)bh * a.Lp + t] : 0.f;
-            if (!(ok = mbar_wait(&s_full, i & 1, &abort_flag))) break;
+            const int sb = i % nbuf, use = i / nbuf;
+            const uint32_t ts = tb + 256 * sb + lane_base;
+            if (!(ok = mbar_wait(&s_full[sb], use & 1, &abort_flag))) break;
             tc_fence_after();
             __nv_bfloat16 *gcol = a.gates + (size_t)bh * a.N * a.Lp + t;  // gate of segment n at gcol[n Lp]
-            float m = ron, z;
+            const int n32 = 2 * nblk;  // 32-column groups of scores
             if (!SSC) {
-                // softmax over the cached scores i < st and the online score
-                for (int c16 = 0; c16 < 4 * nblk; ++c16) {
-                    float v[16];
-                    tmem_ld16f(tb + lane_base + 16 * c16, v);
+                // softmax over the cached scores i < st and the online score: a running maximum
+                // and sum over 32 scores at a time, then the gates
+                float m = ron, z = 1.f;
+                for (int c = 0; c < n32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(ts + 32 * c, v);
                     tmem_wait_ld();
+                    float mc = m;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (16 * c16 + e < st) m = fmaxf(m, v[e]);
-                }
-                z = __expf(ron - m);
-                for (int c16 = 0; c16 < 4 * nblk; ++c16) {
-                    float v[16];
-                    tmem_ld16f(tb + lane_base + 16 * c16, v);
-                    tmem_wait_ld();
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * c + e < st) mc = fmaxf(mc, __uint_as_float(v[e]));
+                    z *= __expf(m - mc);
+                    m = mc;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (16 * c16 + e < st) z += __expf(v[e] - m);
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * c + e < st) z += __expf(__uint_as_float(v[e]) - m);
                 }
                 const float inv = 1.f / z;
-                for (int c16 = 0; c16 < 4 * nblk; ++c16) {
-                    float v[16];
-                    tmem_ld16f(tb + lane_base + 16 * c16, v);
+                for (int c = 0; c < n32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(ts + 32 * c, v);
                     tmem_wait_ld();
                     if (valid) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (16 * c16 + e < st) gcol[(size_t)(16 * c16 + e) * a.Lp] = __float2bfloat16_rn(__expf(v[e] - m) * inv);
+                        for (int e = 0; e < 32; ++e)
+                            if (32 * c + e < st)
+                                gcol[(size_t)(32 * c + e) * a.Lp] = __float2bfloat16_rn(__expf(__uint_as_float(v[e]) - m) * inv);
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&t_free);
+                mbar_arrive(&t_free[sb]);
                 if (valid) gcol[(size_t)st * a.Lp] = __float2bfloat16_rn(__expf(ron - m) * inv);
             } else {
                 // the topk largest cached scores (equal scores: lower index first), then a softmax
@@ -545,19 +554,20 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
                 int idxs[kTcMaxTopk];
                 int cnt = 0;
                 const int k = min(a.topk, st);
-                for (int c16 = 0; c16 < 4 * nblk; ++c16) {
-                    float v[16];
-                    tmem_ld16f(tb + lane_base + 16 * c16, v);
+                for (int c = 0; c < n32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(ts + 32 * c, v);
                     tmem_wait_ld();
                     if (k > 0) {
-                        for (int e = 0; e < 16; ++e)
-                            if (16 * c16 + e < st) topk_insert(vals, idxs, cnt, k, v[e], 16 * c16 + e);
+                        for (int e = 0; e < 32; ++e)
+                            if (32 * c + e < st) topk_insert(vals, idxs, cnt, k, __uint_as_float(v[e]), 32 * c + e);
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&t_free);
+                mbar_arrive(&t_free[sb]);
+                float m = ron;
                 for (int c = 0; c < cnt; ++c) m = fmaxf(m, vals[c]);
-                z = __expf(ron - m);
+                float z = __expf(ron - m);
                 for (int c = 0; c < cnt; ++c) z += __expf(vals[c] - m);
                 const float inv = 1.f / z;
                 if (valid) {
@@ -584,17 +594,44 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
 // ============================================================================
 // readout_fact_tc
 // ============================================================================
-constexpr int kFThreads = 192;     // warp 0 TMA, warp 1 MMA issuer, warps 2-5 token rows
+constexpr int kFThreads = 320;     // warp 0 TMA, warp 1 MMA issuer, warps 2-9 token rows (two per lane quarter)
 constexpr int kFRing = 4;          // 16 KB operand panels in flight (one key tile's K and V)
 constexpr uint32_t kFCols = 256;   // tensor memory per CTA: D (d columns) | G (128 columns, P written over it)
-constexpr size_t kFSmem = 2 * kPanel + kFRing * kPanel + 1024;  // Q tile + ring; two CTAs per SM
+constexpr int kFGRing = 4;         // key tiles whose gate rows are staged ahead
+constexpr int kFGRows = 9;         // gate rows (segments) one key tile can touch: 128 / 16 + 1
+constexpr uint32_t kFGStage = kFGRows * 256;  // 128 bf16 gates of the query tile per row
+constexpr size_t kFSmem = 2 * kPanel + kFRing * kPanel + kFGRing * kFGStage + 1024;  // two CTAs per SM
 
 enum { kWRouted = 0, kWOne = 1, kWMean = 2 };
 
+// (w0 x0, w1 x1) rounded to a bf16 pair (x0 in the low half): one packed fp32 multiply and
+// one conversion.
+__device__ __forceinline__ uint32_t scale_pack(uint32_t x0, uint32_t x1, uint64_t w01)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b64 xx, pp;\n\t.reg .b32 lo, hi;\n\tmov.b64 xx, {%1, %2};\n\tmul.rn.f32x2 pp, xx, %3;\n\t"
+        "mov.b64 {lo, hi}, pp;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "r"(x0), "r"(x1), "l"(w01));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t pair_of(float lo, float hi)
+{
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+
 // One tile = 128 query tokens of one head; for every key tile kt up to it:
 //   G = Q K_kt^T;  P = w o mask(G) (written over G);  D += P V_kt.
-// Tiles are ordered head by head, the longest first within a head, and taken round
-// robin, so the CTAs running together share a few heads' keys and values in L2.
+// The producer also stages, per key tile, the query tile's gates of the segments the key
+// tile touches (rows of 128 bf16) in shared memory.
+// Two worker warps share each quarter of the tensor-memory lanes (token rows): warp half h
+// turns columns 64h .. 64h + 63 of G into P and writes it over the first 32 of those
+// columns (each warp overwrites only what it has read), so keys 64h + 16 kk' .. sit at
+// column 64h + 8 kk'.
+// Tiles are ordered head by head, the longest first within a head, so the CTAs running
+// together share a few heads' keys and values in L2; CTA j takes positions j, 2P - 1 - j,
+// 2P + j, ... of that order (P CTAs), which evens out the sums of the tiles' lengths.
 template <int DP, int WMODE>
 __global__ void __launch_bounds__(kFThreads, 2)
     readout_fact_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -604,17 +641,27 @@ __global__ void __launch_bounds__(kFThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sQ = sm, *sR = sm + 2 * kPanel;
-    __shared__ uint64_t ring_full[kFRing], ring_empty[kFRing];
+    __shared__ uint64_t ring_full[kFRing], ring_empty[kFRing], gr_full[kFGRing], gr_empty[kFGRing];
     __shared__ uint64_t q_full, q_empty, g_full, p_full, g_free, y_full, y_empty, fin;
+    uint8_t *sGr = sm + 2 * kPanel + kFRing * kPanel;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int QT = (a.L + kCT - 1) / kCT;
     const int ntiles = a.BH * QT;
+    const int P = gridDim.x, j0 = blockIdx.x;
+    // position of this CTA's n-th tile in the order (snake over rounds of P)
+    auto pos_of = [&](int n) { return n * P + ((n & 1) ? P - 1 - j0 : j0); };
     auto tile_of = [&](int id, int &bh, int &qt) {
         bh = id / QT;
         qt = QT - 1 - id % QT;
+    };
+    // the query tile's last segment, and the gate rows [i0, i1] key tile kt needs
+    auto gate_rows = [&](int qt, int kt, int &i0, int &i1) {
+        const int smax = (min(qt * kCT + kCT, a.L) - 1) / a.C;
+        i0 = kt * kCT / a.C;
+        i1 = min((kt * kCT + kCT - 1) / a.C, smax);
     };
     if (warp == 0) {
         tmem_alloc(&tmem_base, kFCols);
@@ -626,13 +673,17 @@ __global__ void __launch_bounds__(kFThreads, 2)
             mbar_init(&ring_full[s], 1);
             mbar_init(&ring_empty[s], 1);
         }
+        for (int s = 0; s < kFGRing; ++s) {
+            mbar_init(&gr_full[s], 1);
+            mbar_init(&gr_empty[s], 8);  // one arrive per worker warp
+        }
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
         mbar_init(&g_full, 1);
-        mbar_init(&p_full, 128);
+        mbar_init(&p_full, 256);
         mbar_init(&g_free, 1);
         mbar_init(&y_full, 1);
-        mbar_init(&y_empty, 128);
+        mbar_init(&y_empty, 256);
         mbar_init(&fin, 1);
         fence_mbar_init();
     }
@@ -647,7 +698,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
             prefetch_tensormap(&mQ);
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
-            uint32_t g = 0, qc = 0;
+            uint32_t g = 0, qc = 0, kc = 0;
             bool ok = true;
             auto slot = [&]() -> uint8_t * {
                 const int s = g % kFRing;
@@ -655,14 +706,24 @@ __global__ void __launch_bounds__(kFThreads, 2)
                 mbar_arrive_expect_tx(&ring_full[s], kPanel);
                 return sR + s * kPanel;
             };
-            for (int id = blockIdx.x; id < ntiles && ok; id += gridDim.x, ++qc) {
+            for (int n = 0; pos_of(n) < ntiles && ok; ++n, ++qc) {
                 int bh, qt;
-                tile_of(id, bh, qt);
+                tile_of(pos_of(n), bh, qt);
                 if (!(ok = mbar_wait(&q_empty, (qc & 1) ^ 1, &abort_flag))) break;
                 mbar_arrive_expect_tx(&q_full, NP * kPanel);
                 for (int h = 0; h < NP; ++h) tma_load_3d(sQ + h * kPanel, &mQ, 64 * h, qt * kCT, bh, &q_full);
-                for (int kt = 0; kt <= qt && ok; ++kt) {
+                for (int kt = 0; kt <= qt && ok; ++kt, ++kc) {
                     uint8_t *dst;
+                    if (WMODE == kWRouted) {  // the gate rows of this key tile
+                        const int gs = kc % kFGRing;
+                        if (!(ok = mbar_wait(&gr_empty[gs], ((kc / kFGRing) & 1) ^ 1, &abort_flag))) break;
+                        int i0, i1;
+                        gate_rows(qt, kt, i0, i1);
+                        mbar_arrive_expect_tx(&gr_full[gs], (uint32_t)(i1 - i0 + 1) * 256u);
+                        for (int i = i0; i <= i1; ++i)
+                            bulk_load(sGr + gs * kFGStage + (i - i0) * 256,
+                                      a.gates + ((size_t)bh * a.N + i) * a.Lp + (size_t)qt * kCT, 256u, &gr_full[gs]);
+                    }
                     for (int h = 0; h < NP && ok; ++h) {  // K panels
                         if (!(ok = (dst = slot()) != nullptr)) break;
                         tma_load_3d(dst, &mK, 64 * h, kt * kCT, bh, &ring_full[g % kFRing]);
@@ -688,6 +749,11 @@ __global__ void __launch_bounds__(kFThreads, 2)
                 const uint32_t u = g - 1 - i;
                 mbar_wait_limit(&ring_full[u % kFRing], (u / kFRing) & 1, &give_up, kWaitLimitNs);
             }
+            if (WMODE == kWRouted)
+                for (uint32_t i = 0; i < (uint32_t)kFGRing && i < kc; ++i) {
+                    const uint32_t u = kc - 1 - i;
+                    mbar_wait_limit(&gr_full[u % kFGRing], (u / kFGRing) & 1, &give_up, kWaitLimitNs);
+                }
             if (qc > 0) mbar_wait_limit(&q_full, (qc - 1) & 1, &give_up, kWaitLimitNs);
         }
     } else if (warp == 1) {
@@ -698,9 +764,9 @@ __global__ void __launch_bounds__(kFThreads, 2)
             bool ok = true;
             auto ring_ready = [&](uint32_t u) { return mbar_wait(&ring_full[u % kFRing], (u / kFRing) & 1, &abort_flag); };
             const uint32_t sQb = smem_u32(sQ), sRb = smem_u32(sR);
-            for (int id = blockIdx.x; id < ntiles && ok; id += gridDim.x, ++qc, ++yc) {
+            for (int n = 0; pos_of(n) < ntiles && ok; ++n, ++qc, ++yc) {
                 int bh, qt;
-                tile_of(id, bh, qt);
+                tile_of(pos_of(n), bh, qt);
                 if (!(ok = mbar_wait(&q_full, qc & 1, &abort_flag))) break;
                 for (int kt = 0; kt <= qt && ok; ++kt, ++gc) {
                     if (!(ok = mbar_wait(&g_free, (gc & 1) ^ 1, &abort_flag))) break;  // P of the previous key tile read
@@ -728,7 +794,7 @@ __global__ void __launch_bounds__(kFThreads, 2)
                             const uint64_t dv = make_desc_sw128(sRb + (g % kFRing) * kPanel, kPanel / 2, 1024);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ts(tD, tG + (4 * h + kk) * 8, dv + kk * (2048u >> 4), idPV, (kt | h | kk) != 0);
+                                mma_ts(tD, tG + 64 * h + 8 * kk, dv + kk * (2048u >> 4), idPV, (kt | h | kk) != 0);
                             mma_commit(&ring_empty[g % kFRing]);
                             ++g;
                         }
@@ -737,7 +803,8 @@ __global__ void __launch_bounds__(kFThreads, 2)
                         tc_fence_after();
                         const uint64_t dv = make_desc_sw128(sRb + (g % kFRing) * kPanel, 0, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) mma_ts(tD, tG + kk * 8, dv + kk * (2048u >> 4), idPV, (kt | kk) != 0);
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tD, tG + 64 * (kk >> 2) + 8 * (kk & 3), dv + kk * (2048u >> 4), idPV, (kt | kk) != 0);
                         mma_commit(&ring_empty[g % kFRing]);
                         ++g;
                     }
@@ -753,103 +820,129 @@ __global__ void __launch_bounds__(kFThreads, 2)
         }
     } else {
         const int q4 = warp & 3;
+        const int half = (warp - 2) >> 2;  // columns 64 half .. 64 half + 63 of G; column half of D
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         uint32_t gc = 0, yc = 0;
         bool ok = true;
-        for (int id = blockIdx.x; id < ntiles && ok; id += gridDim.x, ++yc) {
+        for (int n = 0; pos_of(n) < ntiles && ok; ++n, ++yc) {
             int bh, qt;
-            tile_of(id, bh, qt);
+            tile_of(pos_of(n), bh, qt);
             const int t = qt * kCT + (int)row;
             const bool valid = t < a.L;
             const int st = min(t, a.L - 1) / a.C;  // the token's segment
             const float wmean = valid ? (WMODE == kWMean ? 1.f / (float)(st + 1) : 1.f) : 0.f;
-            const __nv_bfloat16 *gcol = a.gates + (size_t)bh * a.N * a.Lp + t;
             for (int kt = 0; kt <= qt && ok; ++kt, ++gc) {
-                // weights of the key tile's columns, per 32-column block: segment sa up to
+                // weights of this warp's 64 columns, per 32-column block: segment sa up to
                 // column bnd, then segment sa + 1 (segments are whole 16-token steps)
-                float ga[4], gb[4];
-                int bnd[4];
+                float ga[2], gb[2];
+                int bnd[2];
+                int i0 = 0, i1 = 0;
+                const __nv_bfloat16 *grow = nullptr;
+                if (WMODE == kWRouted) {
+                    const int gs = gc % kFGRing;
+                    gate_rows(qt, kt, i0, i1);
+                    if (!(ok = mbar_wait(&gr_full[gs], (gc / kFGRing) & 1, &abort_flag))) break;
+                    grow = reinterpret_cast<const __nv_bfloat16 *>(sGr + gs * kFGStage) + row;
+                }
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int j0 = kt * kCT + 32 * h;
+                for (int h = 0; h < 2; ++h) {
+                    const int j0 = kt * kCT + 64 * half + 32 * h;
                     const int sa = j0 / a.C;
                     bnd[h] = min(32, (sa + 1) * a.C - j0);
                     if (WMODE == kWRouted) {
-                        ga[h] = valid ? __bfloat162float(gcol[(size_t)min(sa, st) * a.Lp]) : 0.f;
-                        gb[h] = valid && bnd[h] < 32 ? __bfloat162float(gcol[(size_t)min(sa + 1, st) * a.Lp]) : ga[h];
+                        ga[h] = valid ? __bfloat162float(grow[(min(sa, st) - i0) * kCT]) : 0.f;
+                        gb[h] = valid && bnd[h] < 32 ? __bfloat162float(grow[(min(sa + 1, st) - i0) * kCT]) : ga[h];
                     } else {
                         ga[h] = gb[h] = wmean;
                     }
                 }
+                if (WMODE == kWRouted) {  // the gate rows are in registers: hand the stage back
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&gr_empty[gc % kFGRing]);
+                }
                 if (!(ok = mbar_wait(&g_full, gc & 1, &abort_flag))) break;
                 tc_fence_after();
-                const bool diag = kt == qt;
+                uint32_t x[64];
+                tmem_ld32(tG + lane_base + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32(tG + lane_base + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+                tmem_wait_ld();
+                const int rel = (int)row - 64 * half;  // columns c <= rel are at or before the token
+                if (kt < qt) {  // every key precedes the token
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t x[32], o[16];
-                    tmem_ld32(tG + lane_base + 32 * h, x);
-                    tmem_wait_ld();
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t o[16];
+                        const uint64_t wa = pair_of(ga[h], ga[h]), wb = pair_of(gb[h], gb[h]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c0 = 32 * h + 2 * i;
-                        const float w0 = 2 * i < bnd[h] ? ga[h] : gb[h];
-                        const float w1 = 2 * i + 1 < bnd[h] ? ga[h] : gb[h];
-                        const float p0 = diag && c0 > (int)row ? 0.f : w0 * __uint_as_float(x[2 * i]);
-                        const float p1 = diag && c0 + 1 > (int)row ? 0.f : w1 * __uint_as_float(x[2 * i + 1]);
-                        o[i] = pack_bf16x2(p0, p1);
+                        for (int i = 0; i < 16; ++i)  // bnd is a multiple of 16: a pair never straddles it
+                            o[i] = scale_pack(x[32 * h + 2 * i], x[32 * h + 2 * i + 1], 2 * i < bnd[h] ? wa : wb);
+                        tmem_st16(tG + lane_base + 64 * half + 16 * h, o);  // P over G columns this warp has read
                     }
-                    tmem_st16(tG + lane_base + 16 * h, o);  // P over the G columns already read
+                } else {  // the diagonal tile: keys after the token are masked
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t o[16];
+                        const uint64_t wa = pair_of(ga[h], ga[h]), wb = pair_of(gb[h], gb[h]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int c0 = 32 * h + 2 * i;
+                            const uint32_t pk = scale_pack(x[c0], x[c0 + 1], 2 * i < bnd[h] ? wa : wb);
+                            o[i] = c0 + 1 <= rel ? pk : (c0 <= rel ? (pk & 0xffffu) : 0u);
+                        }
+                        tmem_st16(tG + lane_base + 64 * half + 16 * h, o);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full);
             }
             if (!ok) break;
-            // drain: D in the 16x256b layout (a quad of threads holds 8 consecutive columns
-            // of a row), then a 4 x 4 transpose within the quad so that every thread stores
-            // 16 contiguous bytes
+            // drain this warp's column half of D: the 16x256b layout (a quad of threads holds
+            // 8 consecutive columns of a row), then a 4 x 4 transpose within the quad so that
+            // every thread stores 16 contiguous bytes
             if (!(ok = mbar_wait(&y_full, yc & 1, &abort_flag))) break;
             tc_fence_after();
-            uint32_t yb[64];
+            const bool drains = half < NP;
+            uint32_t yb[32];
+            if (drains) {
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-                for (int ch = 0; ch < NP; ++ch) {
+                for (int hl = 0; hl < 2; ++hl) {
                     uint32_t x[32];
-                    tmem_ld_16x256b_x8(tD + ((uint32_t)(32 * q4 + 16 * hl) << 16) + 64 * ch, x);
+                    tmem_ld_16x256b_x8(tD + ((uint32_t)(32 * q4 + 16 * hl) << 16) + 64 * half, x);
                     tmem_wait_ld();
 #pragma unroll
                     for (int b = 0; b < 8; ++b) {
-                        yb[16 * (2 * hl + ch) + b] = pack_bf16x2(__uint_as_float(x[4 * b]), __uint_as_float(x[4 * b + 1]));
-                        yb[16 * (2 * hl + ch) + 8 + b] = pack_bf16x2(__uint_as_float(x[4 * b + 2]), __uint_as_float(x[4 * b + 3]));
+                        yb[16 * hl + b] = pack_bf16x2(__uint_as_float(x[4 * b]), __uint_as_float(x[4 * b + 1]));
+                        yb[16 * hl + 8 + b] = pack_bf16x2(__uint_as_float(x[4 * b + 2]), __uint_as_float(x[4 * b + 3]));
                     }
                 }
+            }
             tc_fence_before();
             mbar_arrive(&y_empty);
-            const int c = lane & 3;
-            __nv_bfloat16 *ytile = a.y + ((size_t)bh * a.L + (size_t)qt * kCT) * DP;
+            if (drains) {
+                const int c = lane & 3;
+                __nv_bfloat16 *ytile = a.y + ((size_t)bh * a.L + (size_t)qt * kCT) * DP;
 #pragma unroll
-            for (int g4 = 0; g4 < 16; ++g4) {  // (lane half, column half, row A/B, block group) groups of 4 pairs
-                const int hl = g4 >> 3, ch = (g4 >> 2) & 1, rb = (g4 >> 1) & 1, bg = g4 & 1;
-                if (ch >= NP) continue;
-                uint32_t *xv = yb + 4 * g4;
+                for (int g4 = 0; g4 < 8; ++g4) {  // (lane half, row A/B, block group) groups of 4 pairs
+                    const int hl = g4 >> 2, rb = (g4 >> 1) & 1, bg = g4 & 1;
+                    uint32_t *xv = yb + 4 * g4;
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const uint32_t send = (c & 2) ? xv[k2] : xv[k2 + 2];
-                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
-                    if (c & 2) xv[k2] = recv; else xv[k2 + 2] = recv;
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const uint32_t send = (c & 2) ? xv[k2] : xv[k2 + 2];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+                        if (c & 2) xv[k2] = recv; else xv[k2 + 2] = recv;
+                    }
+#pragma unroll
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        const uint32_t send = (c & 1) ? xv[2 * b2] : xv[2 * b2 + 1];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        if (c & 1) xv[2 * b2] = recv; else xv[2 * b2 + 1] = recv;
+                    }
+                    const int r = 32 * q4 + 16 * hl + 8 * rb + (lane >> 2);
+                    if (qt * kCT + r < a.L)
+                        *reinterpret_cast<uint4 *>(ytile + (size_t)r * DP + 64 * half + 8 * (4 * bg + c)) =
+                            make_uint4(xv[0], xv[1], xv[2], xv[3]);
                 }
-#pragma unroll
-                for (int b2 = 0; b2 < 2; ++b2) {
-                    const uint32_t send = (c & 1) ? xv[2 * b2] : xv[2 * b2 + 1];
-                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                    if (c & 1) xv[2 * b2] = recv; else xv[2 * b2 + 1] = recv;
-                }
-                const int r = 32 * q4 + 16 * hl + 8 * rb + (lane >> 2);
-                if (qt * kCT + r < a.L)
-                    *reinterpret_cast<uint4 *>(ytile + (size_t)r * DP + 64 * ch + 8 * (4 * bg + c)) =
-                        make_uint4(xv[0], xv[1], xv[2], xv[3]);
             }
         }
     }
