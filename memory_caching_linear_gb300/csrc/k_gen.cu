@@ -1059,6 +1059,28 @@ cudaError_t launch_gen_front(const Problem &p, const FwdArgs &fa, GenArgs &a, ui
 
 size_t gen_scratch_bytes(const Problem &p) { return gen_plan(p).total; }
 
+// The gate kernel alone, on the state-form path's key-mean images ([BH][ceil(N/64)] blocks)
+// and online scores ([BH][L], L a multiple of 128): gates [BH][N][L] bf16.
+cudaError_t launch_gates_gen(const Problem &p, const void *u, uint8_t *kbar_img, float *r_on, __nv_bfloat16 *gates,
+                             cudaStream_t s)
+{
+    if (p.L % kCT != 0 || p.N > kGMaxN) return cudaErrorInvalidValue;
+    GenArgs a{};
+    a.kbar_img = kbar_img;
+    a.r_on = r_on;
+    a.gates = gates;
+    a.BH = p.BH; a.L = p.L; a.Lp = p.L; a.d = p.d; a.C = p.C; a.N = p.N; a.NB = (p.N + 63) / 64;
+    a.topk = p.topk;
+    CUtensorMap mU;
+    if (!make_tmap_bf16_3d_sw128(&mU, u, p.BH, p.L, p.d, 128)) return cudaErrorInvalidValue;
+    auto k2 = p.mode == MC_SSC ? gates_tc<true> : gates_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+    if (e != cudaSuccess) return e;
+    const int tiles = p.BH * (p.L / kCT), sms = sm_count();
+    k2<<<tiles < sms ? tiles : sms, kGThreads, kGSmem, s>>>(mU, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_forward_gen(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)
 {
     GenArgs a{};

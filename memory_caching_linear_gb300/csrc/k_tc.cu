@@ -72,6 +72,7 @@ struct TcArgs {
     float *kbar_out;      // backward: fp32 key means [BH][N][d], or null
     float *kpre_out;      // backward: keys of the segment before each 64-token tile [BH][N][2 CPS][d], or null
     int32_t *sel_out;     // SSC: optional [BH][L][topk] router output (rank order, -1 padded)
+    const __nv_bfloat16 *gates;  // gates from HBM (more than 64 segments): [BH][N][L] bf16, or null
     int topk;             // SSC: cached segments selected per token
     int mean;             // Mean aggregation: the Residual path with every weight 1 / (n + 1)
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
@@ -779,7 +780,10 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 // release those panels once G is done), read the gate rows in the tile-transposed
 // layout (coalesced), and write y from a quad-transposed register layout.  Two CTAs run on each SM, so while one waits on its G -> P step or its
 // drain the other keeps the tensor pipe busy.
-template <bool GATED, bool DECAY, bool SSC>
+// GG: the gates come from HBM (gates[bh][i][t], the online gate at i = n), written by
+// the gate kernel, instead of being formed here from scores in tensor memory; the tile then
+// reads no U or key-mean panels, and any number of cached segments works.
+template <bool GATED, bool DECAY, bool SSC, bool GG = false>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mU, TcArgs a)
@@ -836,7 +840,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             prefetch_tensormap(&mQ);
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
-            if (GATED) prefetch_tensormap(&mU);
+            if (GATED && !GG) prefetch_tensormap(&mU);
             uint32_t g = 0;
             bool ok = true;
             auto slot = [&]() -> uint8_t * {
@@ -848,10 +852,10 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
                 const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
-                if ((GATED || DECAY) && j + 1 < my_tiles) {  // rows the workers read directly
+                if (((GATED && !GG) || DECAY) && j + 1 < my_tiles) {  // rows the workers read directly
                     const TileInfo tn = decode_tile(a, tile_id(j + 1));
                     const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT) / kCT;
-                    if (GATED) prefetch_l2(a.r_on + tn_id * kCT, kCT * 4);
+                    if (GATED && !GG) prefetch_l2(a.r_on + tn_id * kCT, kCT * 4);
                     if (DECAY) {
                         prefetch_l2(a.alpha + tn_id * kCT, kCT * 4);
                         prefetch_l2(a.beta + tn_id * kCT, kCT * 4);
@@ -859,7 +863,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     }
                 }
                 uint8_t *dst = nullptr;
-                if (GATED) {  // U (two K panels) and the head's key-mean image (hi, mid, lo rows)
+                if (GATED && !GG) {  // U (two K panels) and the head's key-mean image (hi, mid, lo rows)
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!(ok = (dst = slot()) != nullptr)) break;
                         tma_load_2d(dst, &mU, 64 * h, rr, &ring_full[g % kRing]);
@@ -914,7 +918,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
-                if (GATED) {
+                if (GATED && !GG) {
                     // gate scores S = U (kbar_hi + kbar_mid + kbar_lo)^T into the tile's first A slot
                     // (the workers read S there, then write P over it); the slot's last readers
                     // were issued before this
@@ -1023,7 +1027,11 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             const TileInfo t = decode_tile(a, tile_id(j));
             const int items = tile_items<GATED>(t);
             float gn = a.mean ? 1.f / (float)(t.n + 1) : 1.f;  // Residual: 1
-            if (GATED) {
+            // GG: this token's gates in HBM, gcol[i L] for memory i (the online one at i = n)
+            const __nv_bfloat16 *gcol =
+                a.gates + (size_t)t.bh * a.N * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
+            if (GG) gn = __bfloat162float(gcol[(size_t)t.n * a.L]);
+            if (GATED && !GG) {
                 // the token's gates from the scores S in this tile's first A slot
                 g += 5;  // the U and key-mean panels, released by the issuer
                 const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
@@ -1155,11 +1163,20 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             publish();
             // cached operands: g_i o Q
             const __nv_bfloat16 *gl = reinterpret_cast<const __nv_bfloat16 *>(gm2);
+            // GG: item k's gate from HBM, loaded one item ahead
+            auto item_gate = [&](int k) -> __nv_bfloat16 {
+                const int i = t.c > 0 ? k - 1 : k;
+                return gcol[(size_t)(i < 0 ? t.n : i) * a.L];
+            };
+            __nv_bfloat16 gnext = GG && items > 0 ? item_gate(0) : __float2bfloat16_rn(0.f);
 #pragma unroll 1
             for (int k = 0; k < items; ++k) {
                 __nv_bfloat162 gam2 = __float2bfloat162_rn(gn);  // Residual: 1, Mean: 1 / (n + 1)
                 const bool prefix = t.c > 0 && k == 0;  // item 0 of a chunk c > 0 is its prefix state (gate g_n)
-                if (GATED) {
+                if (GG) {
+                    gam2 = __bfloat162bfloat162(gnext);
+                    if (k + 1 < items) gnext = item_gate(k + 1);
+                } else if (GATED) {
                     const int i = t.c > 0 ? k - 1 : k;
                     gam2 = __bfloat162bfloat162(i < 0 ? gl[63] : gl[i]);
                 }
@@ -1262,19 +1279,28 @@ cudaError_t take_device_abort(int *was_set)
     return e;
 }
 
+constexpr int kTcMaxN = 512;  // cached segments the gate kernel handles (gates through HBM beyond 64)
+
 bool tc_supported(const Problem &p)
 {
-    return p.bf16 && (p.d == kD || p.d == 64) && p.C % kCT == 0 && p.L % p.C == 0 && p.N <= 64 &&
+    return p.bf16 && (p.d == kD || p.d == 64) && p.C % kCT == 0 && p.L % p.C == 0 &&
+           (!mode_uses_u(p.mode) || p.N <= kTcMaxN) &&
            (p.mode == MC_GRM || p.mode == MC_SOUP || p.mode == MC_RESIDUAL ||
             p.mode == MC_MEAN || (p.mode == MC_SSC && p.topk >= 0 && p.topk <= kTcMaxTopk));
 }
 
+bool tc_fused_gates(const Problem &p) { return tc_supported(p) && p.N <= 64; }
+
+// Gates through HBM: the routed aggregations with more than 64 segments.
+static bool tc_hbm_gates(const Problem &p) { return mode_uses_u(p.mode) && p.N > 64; }
+
 size_t tc_scratch_bytes(const Problem &p)
 {
-    const size_t BH = p.BH, N = p.N, CPS = p.C / kCT;
-    size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * kKbImg) +
+    const size_t BH = p.BH, N = p.N, CPS = p.C / kCT, NB = (N + 63) / 64;
+    size_t b = pad256(BH * N * kTile) + pad256(BH * N * CPS * kTile) + pad256(BH * NB * kKbImg) +
                pad256(sizeof(float) * BH * p.L);
     if (!mode_uses_u(p.mode)) b += pad256(BH * N * kTile);  // prefix sums of the states
+    if (tc_hbm_gates(p)) b += pad256(sizeof(__nv_bfloat16) * BH * N * p.L);
     return b;
 }
 
@@ -1409,10 +1435,13 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     a.spre_img = base;
     base += pad256(BH * N * CPS * kTile);
     a.kbar_img = base;
-    base += pad256(BH * kKbImg);
+    base += pad256(BH * ((N + 63) / 64) * kKbImg);
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = gated ? nullptr : base;
+    const bool gg = tc_hbm_gates(p);  // routed, so there are no prefix-sum images
+    __nv_bfloat16 *gates = gg ? reinterpret_cast<__nv_bfloat16 *>(base) : nullptr;
+    a.gates = gates;
     a.sel_out = fa.sel_out;
     a.topk = p.topk;
     a.mean = p.mode == MC_MEAN;
@@ -1444,7 +1473,7 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
     }
     cudaError_t e;
     if (gated) {
-        e = cudaMemsetAsync(a.kbar_img, 0, BH * kKbImg, s);
+        e = cudaMemsetAsync(a.kbar_img, 0, BH * ((N + 63) / 64) * kKbImg, s);
         if (e != cudaSuccess) return e;
     }
 
@@ -1470,9 +1499,15 @@ cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "prefix_images");
     }
+    if (gg) {  // more than 64 segments: every token's gates through HBM
+        if (decay) return cudaErrorInvalidValue;
+        if ((e = launch_gates_gen(p, fa.u, a.kbar_img, a.r_on, gates, s)) != cudaSuccess) return e;
+        profile_after_kernel(s, "gates_tc");
+    }
     {
         const bool ssc = p.mode == MC_SSC;
         auto k2 = !gated ? (decay ? readout_tc<false, true, false> : readout_tc<false, false, false>)
+                  : gg   ? (ssc ? readout_tc<true, false, true, true> : readout_tc<true, false, false, true>)
                   : ssc  ? (decay ? readout_tc<true, true, true> : readout_tc<true, false, true>)
                          : (decay ? readout_tc<true, true, false> : readout_tc<true, false, false>);
         e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);

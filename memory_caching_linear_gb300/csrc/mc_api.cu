@@ -161,7 +161,7 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
         if (topk >= p.N - 1) p.mode = MC_GRM;
         else if (topk > kMaxTopk) return MC_ERR_TOPK;
     }
-    if (swla && !tc_supported(p)) return MC_ERR_SHAPE;  // the SWLA update runs on the tensor-core path only
+    if (swla && !tc_fused_gates(p)) return MC_ERR_SHAPE;  // the SWLA update runs on the tensor-core path only
     st = check_device();
     if (st != MC_OK) return st;
 
@@ -513,7 +513,7 @@ int mc_ssc_select(const void *k, const void *u, int B, int H, int L, int d, int 
     p.bf16 = is_bf16 != 0;
     p.mode = MC_SSC;
     p.topk = topk;
-    if (mc::tc_supported(p)) {  // the tensor-core forward's own router, bit for bit
+    if (mc::tc_fused_gates(p)) {  // the tensor-core forward's own router, bit for bit
         void *scratch = nullptr;
         if (mc::scratch_alloc(&scratch, mc::tc_select_scratch_bytes(p), stream) != cudaSuccess) {
             cudaGetLastError();

@@ -119,9 +119,12 @@ cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t s);
 void profile_call_start(cudaStream_t s);
 void profile_after_kernel(cudaStream_t s, const char *name);
 
-// Tensor-core path (k_tc.cu): bf16, d = 128, seg_len % 128 == 0, L % seg_len == 0,
-// N <= 64, Residual / GRM / Soup.
+// Tensor-core state-form path (k_tc.cu): bf16, d = 64 or 128, seg_len % 128 == 0,
+// L % seg_len == 0; the routed aggregations up to 512 segments (beyond 64 the gates go
+// through HBM), SSC topk <= 16.  tc_fused_gates: N <= 64, the gates formed in the readout
+// (the SWLA update, the stand-alone router and the backward need this).
 bool tc_supported(const Problem &p);
+bool tc_fused_gates(const Problem &p);
 size_t tc_scratch_bytes(const Problem &p);
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 size_t tc_select_scratch_bytes(const Problem &p);
@@ -152,6 +155,9 @@ cudaError_t launch_forward_gen(const Problem &p, const FwdArgs &a, void *scratch
 size_t gen_select_scratch_bytes(const Problem &p);
 cudaError_t launch_ssc_select_gen(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 cudaError_t take_gen_abort(int *was_set);
+// The general path's gate kernel for the state form with more than 64 segments.
+cudaError_t launch_gates_gen(const Problem &p, const void *u, uint8_t *kbar_img, float *r_on, __nv_bfloat16 *gates,
+                             cudaStream_t s);
 
 // SIMT kernels (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_seg_scan_simt(const Problem &p, const FwdArgs &a, cudaStream_t s);

@@ -15,7 +15,7 @@ import torch
 
 import memory_caching_linear_gb300 as mcl
 import oracle
-from mc_inputs import GRM, GRM_D64, LONG_GRM, MEAN, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, SWLA_LONG, TINY, make_inputs, \
+from mc_inputs import FACT_C32, GRM, GRM_D64, LONG_C512, LONG_GRM, MEAN, RESIDUAL, SOUP, SSC, SSC_D128, SWEEP, SWLA_LONG, TINY, make_inputs, \
     make_swla_scalars, workload_swla_scalars, \
     workload_inputs
 
@@ -105,8 +105,11 @@ TC_CASES = [
     ("tc-C2048-N1", 2, 1, 2048, 128, 2048),
     ("tc-C256-N4-BH160", 10, 16, 1024, 128, 256),
     ("tc-d64-C128-N32", 1, 2, 4096, 64, 128),  # d = 64: tiles zero-padded to 128 by the TMA
+    # more than 64 segments: the gates go through HBM (three key-mean blocks at N = 130)
+    ("tc-C128-N96", 1, 1, 12288, 128, 128),
+    ("tc-d64-C128-N130", 1, 1, 16640, 64, 128),
 ]
-TC_SSC_CASES = TC_CASES[:2] + TC_CASES[-1:]
+TC_SSC_CASES = TC_CASES[:2] + TC_CASES[-3:]
 
 
 @pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP, MEAN])
@@ -419,6 +422,18 @@ def test_full_size_ssc():
 @pytest.mark.slow
 def test_full_size_long_grm():
     _sampled_check(LONG_GRM, heads=[(0, 0), (0, 15)], segs=[0, 1, 40, 63])
+
+
+@pytest.mark.slow
+def test_full_size_long_c512():
+    """The long workload at seg_len 512: 128 segments, the state form with its gates in HBM."""
+    _sampled_check(LONG_C512, heads=[(0, 0), (0, 15)], segs=[0, 1, 64, 127])
+
+
+@pytest.mark.slow
+def test_full_size_fact_c32():
+    """Segments of 32 tokens (N = 256): the factorised readout at the bench's full size."""
+    _sampled_check(FACT_C32, heads=[(0, 0), (7, 15)], segs=[0, 100, 255])
 
 
 @pytest.mark.slow
