@@ -376,13 +376,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // ============================================================================
 // gates_tc
 // ============================================================================
-constexpr int kGThreads = 192;                               // warp 0 TMA, warp 1 MMA, warps 2-5 token rows
+constexpr int kGThreads = 576;                               // warp 0 TMA, warp 1 MMA, warps 2-17 token rows
+constexpr int kGParts = 4;                                   // worker warps per quarter of the token rows
 constexpr size_t kGSmem = 2 * kTile + 2 * kKbImg + 1024;     // U x 2, key-mean blocks x 2
 constexpr int kGMaxN = 512;                                  // cached segments the score columns hold
 
 // Persistent, one CTA per SM over contiguous ranges of (bh, 128-token tile).  Per tile the
 // scores against every cached segment its last token sees go to tensor memory (blocks of
-// 64 segments, 64 columns each); each worker thread then forms its token's gates.  With
+// 64 segments, 64 columns each); four worker warps per quarter of the token rows then form
+// the gates, each over every fourth 32-column group of scores (GRM: partial maxima and
+// sums combined through shared memory; SSC: the first of the four ranks alone).  With
 // at most 256 segments two tiles' scores fit, so the next tile's MMAs run while the
 // workers read this one's.
 template <bool SSC>
@@ -394,6 +397,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
     __shared__ uint64_t u_full[2], u_empty[2], kb_full[2], kb_empty[2], s_full[2], t_free[2], fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    __shared__ float red_m[2][kGParts][kCT], red_z[2][kGParts][kCT];  // per tile parity: partial maxima and sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int QT = a.Lp / kCT;
     const int total = a.BH * QT;
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&t_free[i], 128);
+            mbar_init(&t_free[i], 32 * 4 * kGParts);
         }
         mbar_init(&fin, 1);
         fence_mbar_init();
@@ -497,10 +501,13 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
         }
     } else {
         const int q4 = warp & 3;
+        const int part = (warp - 2) >> 2;  // every fourth 32-column group of scores, from group `part`
         const uint32_t row = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        // A worker that gives up (a bounded wait ran out) keeps walking the tiles without
+        // work so that every worker reaches the same named barriers.
         bool ok = true;
-        for (int it = first; it < last && ok; ++it) {
+        for (int it = first; it < last; ++it) {
             const int i = it - first;
             const int bh = it / QT, T0 = (it % QT) * kCT;
             const int t = T0 + (int)row;
@@ -510,15 +517,19 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
             const float ron = valid ? a.r_on[(size_t)bh * a.Lp + t] : 0.f;
             const int sb = i % nbuf, use = i / nbuf;
             const uint32_t ts = tb + 256 * sb + lane_base;
-            if (!(ok = mbar_wait(&s_full[sb], use & 1, &abort_flag))) break;
+            if (ok) ok = mbar_wait(&s_full[sb], use & 1, &abort_flag);
+            if (!ok) {
+                if (!SSC) named_bar_sync(1, 32 * 4 * kGParts);
+                continue;
+            }
             tc_fence_after();
             __nv_bfloat16 *gcol = a.gates + (size_t)bh * a.N * a.Lp + t;  // gate of segment n at gcol[n Lp]
             const int n32 = 2 * nblk;  // 32-column groups of scores
             if (!SSC) {
-                // softmax over the cached scores i < st and the online score: a running maximum
-                // and sum over 32 scores at a time, then the gates
-                float m = ron, z = 1.f;
-                for (int c = 0; c < n32; ++c) {
+                // softmax over the cached scores i < st and the online score: this part's running
+                // maximum and sum over its groups, combined with the other parts', then the gates
+                float m = -3.402823466e38f, z = 0.f;
+                for (int c = part; c < n32; c += kGParts) {
                     uint32_t v[32];
                     tmem_ld32(ts + 32 * c, v);
                     tmem_wait_ld();
@@ -532,8 +543,17 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
                     for (int e = 0; e < 32; ++e)
                         if (32 * c + e < st) z += __expf(__uint_as_float(v[e]) - m);
                 }
-                const float inv = 1.f / z;
-                for (int c = 0; c < n32; ++c) {
+                red_m[i & 1][part][row] = m;
+                red_z[i & 1][part][row] = z;
+                named_bar_sync(1, 32 * 4 * kGParts);
+                float M = ron;
+#pragma unroll
+                for (int q = 0; q < kGParts; ++q) M = fmaxf(M, red_m[i & 1][q][row]);
+                float Z = __expf(ron - M);
+#pragma unroll
+                for (int q = 0; q < kGParts; ++q) Z += red_z[i & 1][q][row] * __expf(red_m[i & 1][q][row] - M);
+                const float inv = 1.f / Z;
+                for (int c = part; c < n32; c += kGParts) {
                     uint32_t v[32];
                     tmem_ld32(ts + 32 * c, v);
                     tmem_wait_ld();
@@ -541,12 +561,15 @@ __global__ void __launch_bounds__(kGThreads, 1) gates_tc(const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             if (32 * c + e < st)
-                                gcol[(size_t)(32 * c + e) * a.Lp] = __float2bfloat16_rn(__expf(__uint_as_float(v[e]) - m) * inv);
+                                gcol[(size_t)(32 * c + e) * a.Lp] = __float2bfloat16_rn(__expf(__uint_as_float(v[e]) - M) * inv);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&t_free[sb]);
-                if (valid) gcol[(size_t)st * a.Lp] = __float2bfloat16_rn(__expf(ron - m) * inv);
+                if (valid && part == 0) gcol[(size_t)st * a.Lp] = __float2bfloat16_rn(__expf(ron - M) * inv);
+            } else if (part != 0) {  // SSC ranks in the first part alone
+                tc_fence_before();
+                mbar_arrive(&t_free[sb]);
             } else {
                 // the topk largest cached scores (equal scores: lower index first), then a softmax
                 // over them and the online score; every other cached segment gets gate 0
