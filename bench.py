@@ -118,11 +118,14 @@ def kernel_bytes(w):
     bh = w.B * w.H
     row = w.L * w.d * elt
     routed = w.mode not in (RESIDUAL, mc_inputs.MEAN)
+    # u is read for the tokens after the first segment only: those before have one memory,
+    # whose gate is 1 whatever the score
+    urow = (w.L - min(w.seg_len, w.L)) * w.d * elt if routed else 0
     st32 = w.N * w.d * w.d * 4
     s, _ = segment_counts(w)
     gate_bytes = 2 * (sum(s)) if routed else 0  # bf16 gates, one per token and memory it reads
-    return {"seg_state_tc": bh * ((3 if routed else 2) * row + st32),
-            "readout_tc": bh * ((5 if routed else 4) * row + st32 // 2),
+    return {"seg_state_tc": bh * (2 * row + urow + st32),
+            "readout_tc": bh * (4 * row + urow + st32 // 2),
             "seg_piece_tc": bh * ((3 if routed else 2) * row + st32),
             "gates_tc": bh * (row + gate_bytes),
             "readout_fact_tc": bh * (4 * row + gate_bytes)}

@@ -208,7 +208,10 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 uint8_t *st = sm + s * t1_stage_bytes<DECAY>();
                 // SWLA: alpha and beta reach one token into the next chunk when it is in the same segment
                 const uint32_t dec_ab = (c + 1 < nch ? 132u : 128u) * 4u;
-                mbar_arrive_expect_tx(&full[s], (GATED ? 3 * kTile : 2 * kTile) + (DECAY ? 2 * dec_ab + 512u : 0u));
+                // the first segment's tokens have no cached memory: their single gate is 1 and
+                // their online score is not needed, so u is not read there
+                const bool scored = GATED && sid % a.N != 0;
+                mbar_arrive_expect_tx(&full[s], (scored ? 3 * kTile : 2 * kTile) + (DECAY ? 2 * dec_ab + 512u : 0u));
                 if (DECAY) {
                     float *dec = reinterpret_cast<float *>(st + kT1DecOff);
                     bulk_load(dec, a.alpha + rr, dec_ab, &full[s]);
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 tma_load_2d(st + 16384, &mK, 64, rr, &full[s]);
                 tma_load_2d(st + kTile, &mV, 0, rr, &full[s]);
                 tma_load_2d(st + kTile + 16384, &mV, 64, rr, &full[s]);
-                if (GATED) {
+                if (scored) {
                     tma_load_2d(st + 2 * kTile, &mU, 0, rr, &full[s]);
                     tma_load_2d(st + 2 * kTile + 16384, &mU, 64, rr, &full[s]);
                 }
@@ -229,20 +232,23 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         if (lane == 0) {
             constexpr uint32_t idR = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idS = idesc_bf16(128, 128, true, true);
+            uint32_t rc = 0;  // chunks with online scores (not in a head's first segment)
             for (int gch = 0; gch < my_chunks; ++gch) {
                 const int s = gch & 1, b = gch & 1;
                 const uint32_t r = gch >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sm + s * t1_stage_bytes<DECAY>()), vb = kb + kTile, ub = kb + 2 * kTile;
-                if (GATED) {  // R = U K^T (online gate score of the chunk's tokens)
-                    if (!mbar_wait(&r_empty[b], (r & 1) ^ 1, &abort_flag)) break;
+                if (GATED && seg_of(gch) % a.N != 0) {  // R = U K^T (online gate score of the chunk's tokens)
+                    const int rb = rc & 1;
+                    if (!mbar_wait(&r_empty[rb], ((rc >> 1) & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tR0 + b * 128, make_desc_sw128(ub + kmaj_off(kk, 128), 0, 1024),
+                        mma_ss(tR0 + rb * 128, make_desc_sw128(ub + kmaj_off(kk, 128), 0, 1024),
                                make_desc_sw128(kb + kmaj_off(kk, 128), 0, 1024), idR, kk > 0);
-                    mma_commit(&r_full[b]);
+                    mma_commit(&r_full[rb]);
+                    ++rc;
                 }
                 // Z = V^T K, the chunk's own state (fresh accumulator); SWLA: V^T diag(w) K
                 if (!mbar_wait(&z_empty[b], (r & 1) ^ 1, &abort_flag)) break;
@@ -266,6 +272,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
         bool ok = true;
+        uint32_t rc = 0;  // chunks with online scores, in step with the MMA issuer
         for (int gch = 0; gch < my_chunks; ++gch) {
             const int sid = seg_of(gch), c = gch % nch;
             const int bh = sid / a.N, seg = sid % a.N;
@@ -319,7 +326,9 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 }
                 mbar_arrive(&v_scaled);
             }
-            if (GATED && ok) {
+            if (GATED && seg == 0 && ok) a.r_on[(size_t)row0 + c * kCT + row] = 0.f;  // single gate: the score is unused
+            if (GATED && seg != 0 && ok) {
+                const int rb = rc & 1;
                 float d4[4] = {0.f, 0.f, 0.f, 0.f};  // <u_t, keys of the segment before this chunk>
 #pragma unroll
                 for (int cc = 0; cc < 16; ++cc) {
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     dd = fmaf(u67.x, k1.z, dd); dd = fmaf(u67.y, k1.w, dd);
                 }
                 const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-                ok = mbar_wait(&r_full[b], r & 1, &abort_flag);
+                ok = mbar_wait(&r_full[rb], (rc >> 1) & 1, &abort_flag);
                 if (ok) {
                     tc_fence_after();
                     float w4[4] = {0.f, 0.f, 0.f, 0.f};  // sum_{j <= t} <u_t, k_j> within the chunk
@@ -345,7 +354,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     for (int j16 = 0; j16 < 8; ++j16) {
                         if (16 * j16 > 32 * q4 + 31) break;  // columns past the warp's last row are masked
                         uint32_t v[16];
-                        tmem_ld16(tR0 + b * 128 + lane_base + 16 * j16, v);
+                        tmem_ld16(tR0 + rb * 128 + lane_base + 16 * j16, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -353,11 +362,12 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     }
                     const float w = (w4[0] + w4[1]) + (w4[2] + w4[3]);
                     tc_fence_before();
-                    mbar_arrive(&r_empty[b]);
+                    mbar_arrive(&r_empty[rb]);
                     const int t_in_seg = c * kCT + (int)row;
                     a.r_on[(size_t)row0 + t_in_seg] = (dot + w) / (float)(t_in_seg + 1);
                 }
             }
+            if (GATED && seg != 0) ++rc;
             // Key column sums of the chunk, in a fixed order: thread (rg, cc) sums
             // columns 8cc..8cc+7 over rows 16rg..16rg+15 in row order; then column
             // `row` adds the eight group sums in rg order to the running sum.
@@ -863,7 +873,9 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     }
                 }
                 uint8_t *dst = nullptr;
-                if (GATED && !GG) {  // U (two K panels) and the head's key-mean image (hi, mid, lo rows)
+                // U (two K panels) and the head's key-mean image (hi, mid, lo rows); tiles of a
+                // head's first segment have one memory, gate 1, and need neither
+                if (GATED && !GG && t.n > 0) {
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!(ok = (dst = slot()) != nullptr)) break;
                         tma_load_2d(dst, &mU, 64 * h, rr, &ring_full[g % kRing]);
@@ -918,7 +930,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
                 const TileInfo t = decode_tile(a, tile_id(j));
-                if (GATED && !GG) {
+                if (GATED && !GG && t.n > 0) {
                     // gate scores S = U (kbar_hi + kbar_mid + kbar_lo)^T into the tile's first A slot
                     // (the workers read S there, then write P over it); the slot's last readers
                     // were issued before this
@@ -1009,6 +1021,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const bool leader = warp == 2 && lane == 0;  // releases the Q panels
         uint32_t ac = 0, g = 0;  // A-slot / ring counters, in step with the MMA issuer
+        uint32_t scn = 0;        // tiles whose gate scores the issuer computed
         bool ok = true;
         uint32_t gm2[32];  // gate pairs of the token: (g_{2p}, g_{2p+1}); g_n is element 63
         auto claim = [&]() -> bool {  // the next A slot is free
@@ -1031,12 +1044,13 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             const __nv_bfloat16 *gcol =
                 a.gates + (size_t)t.bh * a.N * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
             if (GG) gn = __bfloat162float(gcol[(size_t)t.n * a.L]);
-            if (GATED && !GG) {
+            if (GATED && !GG && t.n > 0) {
                 // the token's gates from the scores S in this tile's first A slot
                 g += 5;  // the U and key-mean panels, released by the issuer
                 const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
                 const float ron = __ldg(a.r_on + tok);
-                if (!(ok = mbar_wait(&s_full, j & 1, &abort_flag))) break;
+                if (!(ok = mbar_wait(&s_full, scn & 1, &abort_flag))) break;
+                ++scn;
                 tc_fence_after();
                 float sc[64];
 #pragma unroll
@@ -1178,7 +1192,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                     if (k + 1 < items) gnext = item_gate(k + 1);
                 } else if (GATED) {
                     const int i = t.c > 0 ? k - 1 : k;
-                    gam2 = __bfloat162bfloat162(i < 0 ? gl[63] : gl[i]);
+                    gam2 = __bfloat162bfloat162(i < 0 ? __float2bfloat16_rn(gn) : gl[i]);
                 }
                 if (DECAY && prefix) gam2 = __float2bfloat162_rn(gn * __expf(ellt));  // A(t_c, t) S^_c q_t
                 const bool scale = GATED || (DECAY && prefix) || a.mean;

@@ -111,7 +111,8 @@ def test_workload_bounds_and_kernel_bytes():
     w = mc_inputs.LONG_GRM
     kb = bench.kernel_bytes(w)
     row = w.B * w.H * w.L * w.d * 2
-    assert kb["seg_state_tc"] + kb["readout_tc"] == bench.algorithmic_bytes(w) + 3 * row + \
+    urow0 = w.B * w.H * w.seg_len * w.d * 2  # u of the first segment is not read
+    assert kb["seg_state_tc"] + kb["readout_tc"] == bench.algorithmic_bytes(w) + 3 * row - 2 * urow0 + \
         w.B * w.H * w.N * w.d * w.d * 2
     assert bench.metric_name(w) == bench.METRIC
     assert "SSC" in bench.metric_name(mc_inputs.SSC_D128)
