@@ -147,14 +147,18 @@ def metric_name(w):
 
 # ----------------------------------------------------------------------------- peaks and clocks
 
-KERNEL_SOURCES = ("memory_caching_linear_gb300/csrc/k_tc.cu", "memory_caching_linear_gb300/csrc/sm100.cuh",
-                  "memory_caching_linear_gb300/csrc/mc_internal.cuh")
+_CSRC = "memory_caching_linear_gb300/csrc/"
+# the sources each tensor-core kernel is built from: the state-form path, and the general path
+KERNEL_SOURCES = tuple(_CSRC + f for f in ("k_tc.cu", "sm100.cuh", "tc_common.cuh", "mc_internal.cuh"))
+GEN_KERNEL_SOURCES = tuple(_CSRC + f for f in ("k_gen.cu", "sm100.cuh", "tc_common.cuh", "tensormap.cuh",
+                                               "mc_internal.cuh"))
+GEN_KERNELS = ("seg_piece_tc", "gates_tc", "readout_fact_tc")
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the tensor-core kernel sources, in a fixed order."""
+def kernel_source_hash(kernel: str = "readout_tc") -> str:
+    """sha256 over the sources `kernel` is built from, in a fixed order."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (GEN_KERNEL_SOURCES if kernel in GEN_KERNELS else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -162,7 +166,7 @@ def kernel_source_hash() -> str:
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary
-    profiles/<kernel>_<workload>.md, or None when there is none or the kernel sources
+    profiles/<kernel>_<workload>.md, or None when there is none or the kernel's sources
     changed after the counters were taken (the summary records their hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
@@ -176,7 +180,7 @@ def ncu_traffic(kernel: str, workload: str):
             key, _, val = line.partition(":")
             fields[key.strip().strip("`")] = val.strip().strip("`")
     try:
-        if fields.get("kernel_source_sha256") != kernel_source_hash():
+        if fields.get("kernel_source_sha256") != kernel_source_hash(kernel):
             return None
         return int(fields["traffic_bytes_per_launch"])
     except (KeyError, ValueError, OSError):

@@ -83,7 +83,7 @@ def test_single_rank_reduce_is_identity():
 def test_roofline_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     """`traffic` comes from a committed ncu summary only while the kernel sources it
     was taken on are unchanged (the summary records their sha256)."""
-    for rel in bench.KERNEL_SOURCES:
+    for rel in set(bench.KERNEL_SOURCES + bench.GEN_KERNEL_SOURCES):
         dst = tmp_path / rel
         dst.parent.mkdir(parents=True, exist_ok=True)
         dst.write_text("kernel source " + rel)
@@ -97,6 +97,10 @@ def test_roofline_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     (tmp_path / bench.KERNEL_SOURCES[0]).write_text("changed")
     assert bench.ncu_traffic("readout_tc", "long-grm") is None
     assert bench.ncu_traffic("gates_tc", "long-grm") is None
+    fact = tmp_path / "profiles" / "readout_fact_tc_fact-c32.md"
+    fact.write_text(f"- kernel_source_sha256: `{bench.kernel_source_hash('readout_fact_tc')}`\n"
+                    "- traffic_bytes_per_launch: 123\n")
+    assert bench.ncu_traffic("readout_fact_tc", "fact-c32") == 123  # the state-form sources do not matter to it
 
 
 def test_workload_bounds_and_kernel_bytes():
