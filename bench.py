@@ -545,7 +545,8 @@ def backward_flops(w):
     key-mean gradient (4 d).  Per kernel: the tensor-core cached pass does M q and dq of
     the cached reads, the G kernels the state gradients, the FFMA gate kernel the score
     gradients (and, without the tensor-core pass, the cached M q and dq too), the route
-    kernel du and the key-mean kernel dkbar (half the score gradients each), the segment
+    kernel du and the key-mean kernel dkbar (half the score gradients each; the key-mean
+    kernel runs on the tensor cores on the tensor-core path), the segment
     scan the online write and read (4 d^2 per token and run), the reverse scan / the
     tensor-core dk, dv kernel the online gradients (6 d^2 per token), the state kernel the
     online write (2 d^2 per token); the tensor-core gates kernel recomputes the router's
@@ -558,7 +559,7 @@ def backward_flops(w):
     cached = 4 * d * d * sum(n)
     return {"total": bh * (6 * d * d * sum(n) + 8 * d * d * w.L + score),
             "bwd_cached_tc": bh * cached, "bwd_gates_simt": bh * (cached + score),
-            "bwd_route_simt": bh * score // 2, "bwd_dkbar_simt": bh * score // 2,
+            "bwd_route_simt": bh * score // 2, "bwd_dkbar_simt": bh * score // 2, "bwd_dkbar_tc": bh * score // 2,
             "bwd_G_tc": bh * 2 * d * d * sum(n), "bwd_G_simt": bh * 2 * d * d * sum(n),
             "seg_scan_simt": bh * 4 * d * d * w.L, "bwd_scan_simt": bh * 6 * d * d * w.L,
             "bwd_kv_tc": bh * 6 * d * d * w.L, "seg_state_tc": bh * 2 * d * d * w.L,

@@ -570,13 +570,42 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_route_simt(BwdArgs a)
         const float4 r4 = make_float4(g4.x * (d4.x - dl[t]), g4.y * (d4.y - dl[t + 1]), g4.z * (d4.z - dl[t + 2]),
                                       g4.w * (d4.w - dl[t + 3]));
         *reinterpret_cast<float4 *>(dt + i * kTB + t) = r4;
-        if (gated) {
+        if (gated && a.dr_hi) {  // hi = RN(dr), lo = RN(dr - hi): two bf16 terms, 16 bits of dr
+            const size_t o = ((size_t)bh * a.Np + i) * a.L + tb + t;
+            const float rs[4] = {r4.x, r4.y, r4.z, r4.w};
+            __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hi[k] = __float2bfloat16_rn(rs[k]);
+                lo[k] = __float2bfloat16_rn(rs[k] - __bfloat162float(hi[k]));
+            }
+            if (t + 3 < cnt) {
+                *reinterpret_cast<uint2 *>(a.dr_hi + o) = *reinterpret_cast<const uint2 *>(hi);
+                *reinterpret_cast<uint2 *>(a.dr_lo + o) = *reinterpret_cast<const uint2 *>(lo);
+            } else {
+                for (int k = 0; k < 4 && t + k < cnt; ++k) {
+                    a.dr_hi[o + k] = hi[k];
+                    a.dr_lo[o + k] = lo[k];
+                }
+            }
+        } else if (gated && a.dr) {
             float *out = a.dr + seg_base + (size_t)i * a.L + t;
             if (t + 3 < cnt) {
                 *reinterpret_cast<float4 *>(out) = r4;
             } else {
                 const float rs[4] = {r4.x, r4.y, r4.z, r4.w};
                 for (int k = 0; k < 4 && t + k < cnt; ++k) out[k] = rs[k];
+            }
+        }
+    }
+    if (gated && a.dr_hi) {  // zero rows n .. up to the next multiple of 16 (the key-mean MMA reads them)
+        const int nz = min((n + 15) & ~15, a.Np) - n;
+        for (int e = tid; e < nz * kTB; e += kThreads) {
+            const int i = n + e / kTB, t = e % kTB;
+            if (t < cnt) {
+                const size_t o = ((size_t)bh * a.Np + i) * a.L + tb + t;
+                a.dr_hi[o] = __float2bfloat16_rn(0.f);
+                a.dr_lo[o] = __float2bfloat16_rn(0.f);
             }
         }
     }
@@ -1044,7 +1073,10 @@ cudaError_t route_impl(const Problem &p, const BwdArgs &a, cudaStream_t s)
     bwd_route_simt<T, D><<<(unsigned)((long long)p.BH * p.N * tps), kThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_after_kernel(s, "bwd_route_simt");
-    if (a.dr && p.N > 1) {
+    if (a.dr_hi && p.N > 1) {  // the key-mean gradient on the tensor cores
+        if ((e = launch_bwd_dkbar_tc(p, a.u, a.dr_hi, a.dr_lo, a.Np, a.dkbar, s)) != cudaSuccess) return e;
+        profile_after_kernel(s, "bwd_dkbar_tc");
+    } else if (a.dr && p.N > 1) {
         const int chunks = (p.L + kDkChunk - 1) / kDkChunk;
         if ((e = set_smem(bwd_dkbar_simt<T, D>, kDkSmem)) != cudaSuccess) return e;
         bwd_dkbar_simt<T, D><<<(unsigned)((long long)p.BH * chunks), kThreads, kDkSmem, s>>>(a, chunks);
@@ -1093,8 +1125,9 @@ size_t backward_scratch_bytes(const Problem &p)
     if (bwd_tc_supported(p)) {
         const size_t gam = mode_uses_u(p.mode) ? N : 0;
         const size_t kpre = mode_uses_u(p.mode) ? N * ((p.C + kTB - 1) / kTB) * d : 0;
+        const size_t drp = mode_uses_u(p.mode) ? 2 * pad256(2 * BH * ((N + 15) & ~(size_t)15) * L) : 0;
         return common + pad256(4 * BH * L * gam) + pad256(4 * BH * kpre) + pad256(8 * BH * L) +
-               pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p));
+               pad256(tc_state_scratch_bytes(p)) + pad256(bwd_cached_scratch_bytes(p)) + drp;
     }
     const size_t sel = p.mode == MC_SSC ? (size_t)p.topk : 0;
     return common + pad256(4 * BH * L) + 2 * pad256(4 * BH * L * d) + 2 * pad256(4 * BH * L * sel);
@@ -1162,7 +1195,12 @@ cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k,
         a.dg_in2 = dg + BH * N * L;  // the cached pass's second column half
         a.dgon_in2 = dgon + BH * L;
         a.dq_in = nullptr;  // dq is written whole by the cached pass
-        a.dr = gated ? dg : nullptr;  // the score gradients replace dg in place
+        a.dr = nullptr;
+        if (gated) {  // the score gradients as the key-mean MMA's bf16 hi / lo planes
+            a.Np = (int)((N + 15) & ~(size_t)15);
+            a.dr_hi = reinterpret_cast<__nv_bfloat16 *>(take(2 * BH * a.Np * L));
+            a.dr_lo = reinterpret_cast<__nv_bfloat16 *>(take(2 * BH * a.Np * L));
+        }
         return launch_bwd_tc_rest(p, a, s);
     }
 

@@ -981,6 +981,203 @@ cudaError_t launch_bwd_G_tc(const Problem &p, const void *dy, const void *q, con
     return cudaGetLastError();
 }
 
+// ============================================================================
+// bwd_dkbar_tc -- the key-mean gradients ([MC-ja §3.1 eq. 10]: kbar_i enters the score
+//   <u_t, kbar_i> of every later token):  dkbar_i = sum_t dr_{t,i} u_t, as
+//     D[c][i] += sum_{t in tile} u_t[c] dr_{t,i}        (fp32 in tensor memory)
+//   with A = the tile's u (MN-major: M = the head dimension, K = 128 tokens) and B = the
+//   tile's dr rows (K-major: N = the tile's cached segments rounded up to 16, K = tokens),
+//   dr as two bf16 terms hi + lo (16 bits; u is exact in bf16).  Persistent, one CTA per SM
+//   over contiguous ranges of 128-token tiles (those of a head's first segment have no
+//   cached segment and are skipped); the accumulator starts from zero for each head and is
+//   added to dkbar with fp32 atomics when the CTA leaves the head.
+// ============================================================================
+constexpr int kDThreads = 192;                       // warp 0 TMA, warp 1 MMA issuer, warps 2-5 drain
+constexpr int kDStages = 3;
+constexpr uint32_t kDPlane = 16384;                  // 64 segment rows x 128 tokens of dr: two 8 KB panels
+constexpr uint32_t kDStage = kGTile + 2 * kDPlane;   // u tile, dr hi, dr lo
+constexpr size_t kDSmem = kDStages * kDStage + 1024;
+
+struct DkArgs {
+    float *dkbar;  // [BH][N][d], accumulated
+    int BH, L, C, N, Np, d;
+};
+
+__global__ void __launch_bounds__(kDThreads, 1)
+    bwd_dkbar_tc(const __grid_constant__ CUtensorMap mU, const __grid_constant__ CUtensorMap mHi,
+                 const __grid_constant__ CUtensorMap mLo, DkArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    __shared__ uint64_t full[kDStages], empty[kDStages], acc_full, acc_ready, fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int TPH = a.L / kGT;  // tiles per head
+    const int total = a.BH * TPH;
+    const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int first = (int)blockIdx.x * per, last = min(total, first + per);
+    auto seg_of = [&](int it) { return (it % TPH) * kGT / a.C; };  // cached segments of the tile's tokens
+    // a head's first tiles (segment 0) do nothing: the working tiles of a head are contiguous,
+    // so a run of one head ends at the range's end or where the head changes
+    auto run_ends = [&](int it) { return it + 1 >= last || (it + 1) / TPH != it / TPH; };
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 64);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        abort_flag = 0;
+        for (int i = 0; i < kDStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&acc_ready, 128);
+        mbar_init(&fin, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_base;
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&mU);
+            prefetch_tensormap(&mHi);
+            prefetch_tensormap(&mLo);
+            uint32_t q = 0;
+            for (int it = first; it < last; ++it) {
+                if (seg_of(it) == 0) continue;
+                const int bh = it / TPH, t0 = (it % TPH) * kGT;
+                const int s = q % kDStages;
+                if (!mbar_wait(&empty[s], ((q / kDStages) & 1) ^ 1, &abort_flag)) break;
+                uint8_t *st = sm + s * kDStage;
+                mbar_arrive_expect_tx(&full[s], kDStage);
+                tma_load_2d(st, &mU, 0, bh * a.L + t0, &full[s]);
+                tma_load_2d(st + 16384, &mU, 64, bh * a.L + t0, &full[s]);
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_2d(st + kGTile + 8192 * h, &mHi, t0 + 64 * h, bh * a.Np, &full[s]);
+                    tma_load_2d(st + kGTile + kDPlane + 8192 * h, &mLo, t0 + 64 * h, bh * a.Np, &full[s]);
+                }
+                ++q;
+            }
+            int give_up = 0;  // leave no copy in flight
+            for (uint32_t i = 0; i < (uint32_t)kDStages && i < q; ++i) {
+                const uint32_t u = q - 1 - i;
+                mbar_wait_limit(&full[u % kDStages], (u / kDStages) & 1, &give_up, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t q = 0, runs = 0;
+            bool ok = true, fresh = true, issued = false;
+            for (int it = first; it < last && ok; ++it) {
+                const int n = seg_of(it);
+                if (n == 0) continue;
+                if (fresh) {  // the workers have zeroed the accumulator for this head
+                    if (!(ok = mbar_wait(&acc_ready, runs & 1, &abort_flag))) break;
+                    fresh = false;
+                }
+                const int s = q % kDStages;
+                if (!(ok = mbar_wait(&full[s], (q / kDStages) & 1, &abort_flag))) break;
+                tc_fence_after();
+                const uint32_t sb = smem_u32(sm + s * kDStage);
+                const int nt = (n + 15) & ~15;  // the MMA's N: the tile's cached segments, whole 16s
+                const uint32_t id = idesc_bf16(128, nt, true, false);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t du = make_desc_sw128(sb + kk * 2048u, 16384, 1024);  // MN-major u
+#pragma unroll
+                    for (int pl = 0; pl < 2; ++pl) {
+                        const uint64_t dr = make_desc_sw128(sb + kGTile + pl * kDPlane + (kk >> 2) * 8192u + (kk & 3) * 32u, 0, 1024);  // K-major, 64 rows
+                        mma_ss(tD, du, dr, id, 1);
+                    }
+                }
+                issued = true;
+                mma_commit(&empty[s]);
+                ++q;
+                if (run_ends(it)) {
+                    mma_commit(&acc_full);
+                    ++runs;
+                    fresh = true;
+                }
+            }
+            if (issued) {
+                mma_commit(&fin);
+                int give_up = 0;
+                mbar_wait_limit(&fin, 0, &give_up, kWaitLimitNs);
+            }
+        }
+    } else {
+        const int q4 = warp & 3;
+        const uint32_t row = 32 * q4 + lane;  // TMEM lane = the head dimension c
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        uint32_t runs = 0;
+        bool ok = true, fresh = true;
+        for (int it = first; it < last && ok; ++it) {
+            const int n = seg_of(it);
+            if (n == 0) continue;
+            if (fresh) {  // a new head: the accumulator starts from zero
+                uint32_t z[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+                for (int c16 = 0; c16 < 4; ++c16) tmem_st16(tD + lane_base + 16 * c16, z);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&acc_ready);
+                fresh = false;
+            }
+            if (!run_ends(it)) continue;
+            if (!(ok = mbar_wait(&acc_full, runs & 1, &abort_flag))) break;
+            tc_fence_after();
+            float v[64];
+#pragma unroll
+            for (int c16 = 0; c16 < 4; ++c16) tmem_ld16f(tD + lane_base + 16 * c16, v + 16 * c16);
+            tmem_wait_ld();
+            tc_fence_before();
+            const int bh = it / TPH;
+            if ((int)row < a.d) {
+                float *dk = a.dkbar + (size_t)bh * a.N * a.d + row;
+                for (int i = 0; i < a.N && i < 64; ++i)
+                    if (v[i] != 0.f) atomicAdd(dk + (size_t)i * a.d, v[i]);
+            }
+            ++runs;
+            fresh = true;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tD, 64);
+    }
+    if (threadIdx.x == 0 && abort_flag) atomicExch(&g_bwd_abort, 1);
+}
+
+cudaError_t launch_bwd_dkbar_tc(const Problem &p, const void *u, const __nv_bfloat16 *dr_hi,
+                                const __nv_bfloat16 *dr_lo, int Np, float *dkbar, cudaStream_t s)
+{
+    if (p.N < 2 || Np > 64 || p.L % kGT != 0) return p.N < 2 ? cudaSuccess : cudaErrorInvalidValue;
+    CUtensorMap mU, mHi, mLo;
+    const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    if (!make_tmap_bf16_sw128(&mU, u, rows, p.d, 128) ||
+        !make_tmap_bf16(&mHi, dr_hi, (unsigned long long)p.BH * Np, p.L, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&mLo, dr_lo, (unsigned long long)p.BH * Np, p.L, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    DkArgs a{};
+    a.dkbar = dkbar;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.Np = Np; a.d = p.d;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkbar_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+    const int total = p.BH * (p.L / kGT);
+    bwd_dkbar_tc<<<total < sms ? total : sms, kDThreads, kDSmem, s>>>(mU, mHi, mLo, a);
+    return cudaGetLastError();
+}
+
 cudaError_t take_bwd_abort(int *was_set)
 {
     int v = 0;

@@ -187,7 +187,10 @@ struct BwdArgs {
     const float *dq_in;   // [BH][L][d] dq from the tensor cores (all of it when X_on is null), or null (written already)
     const float *dgon_in; // [BH][L] dy_t . M_t q_t from the tensor cores, or null (from O_on)
     const float *dg_in2, *dgon_in2;  // second partial sums of dg_in and dgon_in (added to them), or null
-    float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in)
+    float *dr;            // [BH][N][L] the score gradients g (dg - delta) (may alias dg_in), or null
+    __nv_bfloat16 *dr_hi, *dr_lo;  // tensor-core path: dr as two exact bf16 terms [BH][Np][L] (rows n .. Np of a
+                                   // segment-n token zero up to the next multiple of 16), or null
+    int Np;               // N rounded up to a multiple of 16
     float *kpre_tiles;    // [BH][N][ceil(C/64)][d] keys of each segment before each 64-token tile, or null
     float *kv_gw;         // [2][BH][L] the online gate and the pooled-key weight w per token (tensor-core path)
     int BH, L, C, N, mode, topk;
@@ -207,6 +210,10 @@ cudaError_t launch_bwd_cached_tc(const Problem &p, const void *q, const void *k,
                                  const TcImages &img, const float *gam, const float *tok, void *dq, void *scratch,
                                  float **dg_out, float **dgon_out, cudaStream_t s);
 cudaError_t take_bwd_abort(int *was_set);
+// The key-mean gradients on the tensor cores: dkbar [BH][N][d] += sum_t dr_{t,i} u_t from the
+// route kernel's hi / lo planes of dr.
+cudaError_t launch_bwd_dkbar_tc(const Problem &p, const void *u, const __nv_bfloat16 *dr_hi,
+                                const __nv_bfloat16 *dr_lo, int Np, float *dkbar, cudaStream_t s);
 cudaError_t launch_backward_simt(const Problem &p, const void *q, const void *k, const void *v, const void *u,
                                  const void *dy, void *dq, void *dk, void *dv, void *du, void *scratch,
                                  cudaStream_t s);

@@ -57,7 +57,7 @@ def test_backward_flops_tensor_core_split():
     # recomputes forward work, outside the total)
     w = mc_inputs.LONG_GRM
     f = bench.backward_flops(w)
-    tc = ("seg_state_tc", "bwd_cached_tc", "bwd_route_simt", "bwd_dkbar_simt", "bwd_G_tc", "bwd_kv_tc")
+    tc = ("seg_state_tc", "bwd_cached_tc", "bwd_route_simt", "bwd_dkbar_tc", "bwd_G_tc", "bwd_kv_tc")
     assert sum(f[k] for k in tc) == f["total"]
     assert f["gate_tiles_tc"] == w.B * w.H * 2 * w.d * sum(t // w.seg_len for t in range(w.L))
     assert abs(f["total"] / 1e12 - 3.4019) < 1e-3
