@@ -80,7 +80,41 @@ struct TcArgs {
     int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
     int NB;               // blocks of 64 segments in a head's key-mean image (1 when N <= 64)
     int num_tiles;
+    // Given segment boundaries (the VAR kernels): segments 0 .. Nseg-1 of every head start at
+    // sg_off[n] (a multiple of 128) and are whole 128-token chunks; sg_cbase[n] is the segment's
+    // first chunk among the head's NC chunks (prefix-state images [BH][NC]); the readout's tiles
+    // are vtiles[id / BH] = (segment, chunk), heaviest first.
+    const int32_t *sg_off, *sg_cbase;
+    const int2 *vtiles;
+    int Nseg, NC;
 };
+
+// A head's segment as the kernels see it: constant length C, or from the tables.
+struct SegInfo {
+    int bh, seg, nch, off, len, cbase;
+};
+
+template <bool VAR>
+__device__ __forceinline__ SegInfo seg_info(const TcArgs &a, int uid)
+{
+    SegInfo u;
+    if (!VAR) {  // units head by head
+        u.bh = uid / a.N;
+        u.seg = uid % a.N;
+        u.nch = a.CPS;
+        u.off = u.seg * a.C;
+        u.len = a.C;
+        u.cbase = u.seg * a.CPS;
+    } else {  // units segment by segment (the longest first), every head of a segment together
+        u.seg = uid / a.BH;
+        u.bh = uid % a.BH;
+        u.off = a.sg_off[u.seg];
+        u.len = a.sg_off[u.seg + 1] - u.off;
+        u.nch = u.len / kCT;
+        u.cbase = a.sg_cbase[u.seg];
+    }
+    return u;
+}
 
 // SWLA (sliding-window linear attention, c = 2, [MC-ja §3.1 eq. 28]) within one
 // 128-token chunk whose first token is t_c:
@@ -146,7 +180,7 @@ static_assert(kT1DecBytes <= 2048, "the SWLA scalars fit the stage's tail");
 template <bool DECAY>
 __host__ __device__ constexpr size_t t1_smem_bytes() { return 2 * t1_stage_bytes<DECAY>() + 4 * kT1Stage2 + 1024; }
 
-template <bool GATED, bool DECAY>
+template <bool GATED, bool DECAY, bool VAR = false>
 __global__ void __launch_bounds__(kT1Threads, 1)
     seg_state_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                  const __grid_constant__ CUtensorMap mU, TcArgs a)
@@ -161,14 +195,33 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     __shared__ __align__(16) float red_s[8][kD];  // column-sum partials of 16-row groups
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nch = a.CPS;
-    // Persistent: this CTA walks segments blockIdx.x, blockIdx.x + gridDim.x, ...;
+    // Persistent: this CTA walks segments (units) blockIdx.x, blockIdx.x + gridDim.x, ...;
     // its chunks form one stream (global chunk counter g) so loads run ahead
     // across segment boundaries.
-    const int nseg_total = a.BH * a.N;
+    const int nseg_total = a.BH * (VAR ? a.Nseg : a.N);
     const int my_segs = (int)blockIdx.x < nseg_total ? (nseg_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int my_chunks = my_segs * nch;
-    auto seg_of = [&](int gch) { return (int)blockIdx.x + (gch / nch) * (int)gridDim.x; };
+    int my_chunks = 0;
+    for (int k = 0; k < my_segs; ++k) my_chunks += seg_info<VAR>(a, (int)blockIdx.x + k * (int)gridDim.x).nch;
+    const int NCH = VAR ? a.NC : a.N * a.CPS;  // prefix-state images per head
+    // each role walks the chunk stream with a cursor: the unit, and the chunk within it
+    struct Cursor {
+        int k, c;
+        SegInfo u;
+    };
+    auto start = [&]() {
+        Cursor q;
+        q.k = 0;
+        q.c = 0;
+        q.u = seg_info<VAR>(a, (int)blockIdx.x);
+        return q;
+    };
+    auto advance = [&](Cursor &q) {
+        if (++q.c == q.u.nch) {
+            q.c = 0;
+            ++q.k;
+            if (q.k < my_segs) q.u = seg_info<VAR>(a, (int)blockIdx.x + q.k * (int)gridDim.x);
+        }
+    };
 
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -199,9 +252,10 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             prefetch_tensormap(&mK);
             prefetch_tensormap(&mV);
             if (GATED) prefetch_tensormap(&mU);
-            for (int gch = 0; gch < my_chunks; ++gch) {
-                const int sid = seg_of(gch), c = gch % nch;
-                const int rr = (sid / a.N) * a.L + (sid % a.N) * a.C + c * kCT;
+            Cursor cu = start();
+            for (int gch = 0; gch < my_chunks; ++gch, advance(cu)) {
+                const int c = cu.c, nch = cu.u.nch;
+                const int rr = cu.u.bh * a.L + cu.u.off + c * kCT;
                 const int s = gch & 1;
                 const uint32_t r = gch >> 1;
                 if (!mbar_wait(&empty[s], (r & 1) ^ 1, &abort_flag)) break;
@@ -210,7 +264,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 const uint32_t dec_ab = (c + 1 < nch ? 132u : 128u) * 4u;
                 // the first segment's tokens have no cached memory: their single gate is 1 and
                 // their online score is not needed, so u is not read there
-                const bool scored = GATED && sid % a.N != 0;
+                const bool scored = GATED && cu.u.seg != 0;
                 mbar_arrive_expect_tx(&full[s], (scored ? 3 * kTile : 2 * kTile) + (DECAY ? 2 * dec_ab + 512u : 0u));
                 if (DECAY) {
                     float *dec = reinterpret_cast<float *>(st + kT1DecOff);
@@ -233,13 +287,14 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             constexpr uint32_t idR = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idS = idesc_bf16(128, 128, true, true);
             uint32_t rc = 0;  // chunks with online scores (not in a head's first segment)
-            for (int gch = 0; gch < my_chunks; ++gch) {
+            Cursor cu = start();
+            for (int gch = 0; gch < my_chunks; ++gch, advance(cu)) {
                 const int s = gch & 1, b = gch & 1;
                 const uint32_t r = gch >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sm + s * t1_stage_bytes<DECAY>()), vb = kb + kTile, ub = kb + 2 * kTile;
-                if (GATED && seg_of(gch) % a.N != 0) {  // R = U K^T (online gate score of the chunk's tokens)
+                if (GATED && cu.u.seg != 0) {  // R = U K^T (online gate score of the chunk's tokens)
                     const int rb = rc & 1;
                     if (!mbar_wait(&r_empty[rb], ((rc >> 1) & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
@@ -273,10 +328,11 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         // without work so that every warp reaches the same named barriers.
         bool ok = true;
         uint32_t rc = 0;  // chunks with online scores, in step with the MMA issuer
-        for (int gch = 0; gch < my_chunks; ++gch) {
-            const int sid = seg_of(gch), c = gch % nch;
-            const int bh = sid / a.N, seg = sid % a.N;
-            const int row0 = bh * a.L + seg * a.C;
+        Cursor cu = start();
+        for (int gch = 0; gch < my_chunks; ++gch, advance(cu)) {
+            const int c = cu.c, nch = cu.u.nch;
+            const int bh = cu.u.bh, seg = cu.u.seg;
+            const int row0 = bh * a.L + cu.u.off;
             const int s = gch & 1, b = gch & 1;
             const uint32_t r = gch >> 1;
             if (c == 0) {  // a new segment: memory restarts at zero
@@ -395,7 +451,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     cs += red_s[g8][row];
                     if (g8 == 3) ch = cs;  // the chunk's first 64 rows
                 }
-                if (GATED && a.kpre_out && (int)row < a.d) {  // keys before the chunk's two 64-token halves
+                if (!VAR && GATED && a.kpre_out && (int)row < a.d) {  // keys before the chunk's two 64-token halves
                     float *kp = a.kpre_out + (((size_t)bh * a.N + seg) * (2 * nch) + 2 * c) * a.d + row;
                     kp[0] = ks;
                     kp[a.d] = ks + ch;
@@ -421,7 +477,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 tc_fence_before();
                 mbar_arrive(&z_empty[b]);
                 const size_t sidx = (size_t)bh * a.N + seg;
-                uint8_t *img = c + 1 < nch ? a.spre_img + (sidx * a.CPS + c + 1) * kTile : a.states_img + sidx * kTile;
+                uint8_t *img = c + 1 < nch ? a.spre_img + ((size_t)bh * NCH + cu.u.cbase + c + 1) * kTile
+                                           : a.states_img + sidx * kTile;
                 // Through the warp's 4 KB staging area, one 64-column panel at a time: the
                 // warp's 32 rows of a panel are 4 KB contiguous in the image, stored 512
                 // contiguous bytes per instruction.
@@ -465,7 +522,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                         __syncwarp();
                     }
                     if (GATED) {
-                        const float kbv = ks / (float)a.C;
+                        const float kbv = ks / (float)cu.u.len;
                         if (a.kbar_out && (int)row < a.d) a.kbar_out[sidx * a.d + row] = kbv;
                         store_kbar_terms(a.kbar_img + (size_t)bh * a.NB * kKbImg, seg, row, kbv);
                     }
@@ -746,16 +803,30 @@ constexpr size_t kT2Smem = kRing * kPanel + kT2Decay + 1024;  // two CTAs fit in
 
 struct TileInfo {
     int n, c, bh;
+    int off;    // the segment's first token within the head
+    int cbase;  // the segment's first chunk among the head's chunks
 };
 
+template <bool VAR>
 __device__ __forceinline__ TileInfo decode_tile(const TcArgs &a, int id)
 {
-    const int per_seg = a.BH * a.CPS;
     TileInfo t;
-    t.n = a.N - 1 - id / per_seg;
-    const int rem = id % per_seg;
-    t.c = rem / a.BH;
-    t.bh = rem % a.BH;
+    if (!VAR) {
+        const int per_seg = a.BH * a.CPS;
+        t.n = a.N - 1 - id / per_seg;
+        const int rem = id % per_seg;
+        t.c = rem / a.BH;
+        t.bh = rem % a.BH;
+        t.off = t.n * a.C;
+        t.cbase = t.n * a.CPS;
+    } else {
+        const int2 nc = a.vtiles[id / a.BH];
+        t.n = nc.x;
+        t.c = nc.y;
+        t.bh = id % a.BH;
+        t.off = a.sg_off[t.n];
+        t.cbase = a.sg_cbase[t.n];
+    }
     return t;
 }
 
@@ -767,12 +838,13 @@ __device__ __forceinline__ int tile_items(const TileInfo &t)
     return GATED ? t.n + (t.c > 0 ? 1 : 0) : (t.n > 0 ? 1 : 0) + (t.c > 0 ? 1 : 0);
 }
 
-template <bool GATED>
+template <bool GATED, bool VAR>
 __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const TileInfo &t, int k)
 {
     const size_t sb = (size_t)t.bh * a.N;
     if (t.c > 0) {
-        if (k == 0) return a.spre_img + ((sb + t.n) * a.CPS + t.c) * kTile;
+        const size_t nch_head = VAR ? (size_t)a.NC : (size_t)a.N * a.CPS;
+        if (k == 0) return a.spre_img + ((size_t)t.bh * nch_head + t.cbase + t.c) * kTile;
         --k;
     }
     return GATED ? a.states_img + (sb + k) * kTile : a.prefix_img + (sb + t.n) * kTile;
@@ -793,7 +865,7 @@ __device__ __forceinline__ const uint8_t *item_image(const TcArgs &a, const Tile
 // GG: the gates come from HBM (gates[bh][i][t], the online gate at i = n), written by
 // the gate kernel, instead of being formed here from scores in tensor memory; the tile then
 // reads no U or key-mean panels, and any number of cached segments works.
-template <bool GATED, bool DECAY, bool SSC, bool GG = false>
+template <bool GATED, bool DECAY, bool SSC, bool GG = false, bool VAR = false>
 __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
     readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mU, TcArgs a)
@@ -860,11 +932,11 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 return sm + s * kPanel;
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
-                const TileInfo t = decode_tile(a, tile_id(j));
-                const int rr = t.bh * a.L + t.n * a.C + t.c * kCT;
+                const TileInfo t = decode_tile<VAR>(a, tile_id(j));
+                const int rr = t.bh * a.L + t.off + t.c * kCT;
                 if (((GATED && !GG) || DECAY) && j + 1 < my_tiles) {  // rows the workers read directly
-                    const TileInfo tn = decode_tile(a, tile_id(j + 1));
-                    const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.n * a.C + (size_t)tn.c * kCT) / kCT;
+                    const TileInfo tn = decode_tile<VAR>(a, tile_id(j + 1));
+                    const size_t tn_id = ((size_t)tn.bh * a.L + (size_t)tn.off + (size_t)tn.c * kCT) / kCT;
                     if (GATED && !GG) prefetch_l2(a.r_on + tn_id * kCT, kCT * 4);
                     if (DECAY) {
                         prefetch_l2(a.alpha + tn_id * kCT, kCT * 4);
@@ -903,7 +975,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 }
                 const int items = tile_items<GATED>(t);
                 for (int k = 0; k < items && ok; ++k) {
-                    const uint8_t *src = item_image<GATED>(a, t, k);
+                    const uint8_t *src = item_image<GATED, VAR>(a, t, k);
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!(ok = (dst = slot()) != nullptr)) break;
                         bulk_load(dst, src + h * kPanel, kPanel, &ring_full[g % kRing]);
@@ -929,7 +1001,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 return mbar_wait(&ring_full[u % kRing], (u / kRing) & 1, &abort_flag);
             };
             for (int j = 0; j < my_tiles && ok; ++j) {
-                const TileInfo t = decode_tile(a, tile_id(j));
+                const TileInfo t = decode_tile<VAR>(a, tile_id(j));
                 if (GATED && !GG && t.n > 0) {
                     // gate scores S = U (kbar_hi + kbar_mid + kbar_lo)^T into the tile's first A slot
                     // (the workers read S there, then write P over it); the slot's last readers
@@ -1037,17 +1109,17 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
         };
         float *dsm = reinterpret_cast<float *>(sm + kRing * kPanel) + q4 * 5 * kCT;  // SWLA: ell | lambda | beta_{j+1} | E | F
         for (int j = 0; j < my_tiles && ok; ++j) {
-            const TileInfo t = decode_tile(a, tile_id(j));
+            const TileInfo t = decode_tile<VAR>(a, tile_id(j));
             const int items = tile_items<GATED>(t);
             float gn = a.mean ? 1.f / (float)(t.n + 1) : 1.f;  // Residual: 1
             // GG: this token's gates in HBM, gcol[i L] for memory i (the online one at i = n)
             const __nv_bfloat16 *gcol =
-                a.gates + (size_t)t.bh * a.N * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
+                a.gates + (size_t)t.bh * a.N * a.L + (size_t)t.off + (size_t)t.c * kCT + row;
             if (GG) gn = __bfloat162float(gcol[(size_t)t.n * a.L]);
             if (GATED && !GG && t.n > 0) {
                 // the token's gates from the scores S in this tile's first A slot
                 g += 5;  // the U and key-mean panels, released by the issuer
-                const size_t tok = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT + row;
+                const size_t tok = (size_t)t.bh * a.L + (size_t)t.off + (size_t)t.c * kCT + row;
                 const float ron = __ldg(a.r_on + tok);
                 if (!(ok = mbar_wait(&s_full, scn & 1, &abort_flag))) break;
                 ++scn;
@@ -1070,7 +1142,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             }
             float ellt = 0.f;  // SWLA: log of A(t_c, t) for this token row
             if (DECAY) {
-                const size_t tok0 = (size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT;
+                const size_t tok0 = (size_t)t.bh * a.L + (size_t)t.off + (size_t)t.c * kCT;
                 const ChunkDecay cd = load_chunk_decay(a.alpha, a.beta, a.lam, tok0, lane);
                 const float b_up = __shfl_down_sync(0xffffffffu, cd.bet[0], 1);  // beta of token 4 (lane + 1)
 #pragma unroll
@@ -1240,7 +1312,7 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
             mbar_arrive(&y_empty);
             {
                 const int c = lane & 3;
-                __nv_bfloat16 *ytile = a.y + ((size_t)t.bh * a.L + (size_t)t.n * a.C + (size_t)t.c * kCT) * a.d;
+                __nv_bfloat16 *ytile = a.y + ((size_t)t.bh * a.L + (size_t)t.off + (size_t)t.c * kCT) * a.d;
 #pragma unroll
                 for (int g4 = 0; g4 < 16; ++g4) {  // (lane half, column half, row A/B, block group) groups of 4 pairs
                     if (64 * ((g4 >> 2) & 1) >= a.d) continue;  // d = 64: the padded columns are not stored
@@ -1432,6 +1504,114 @@ cudaError_t launch_bwd_gates_tc(const Problem &p, const void *u, const TcImages 
     const int ggrid = gtiles < g_num_sms ? gtiles : g_num_sms;
     k<<<ggrid, kRouterThreads, kRouterSmem, s>>>(mU, a);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// The state form over given segment boundaries: segments 0 .. Nseg-1 of every head
+// are whole 128-token chunks (start and length multiples of 128).  Scratch layout:
+// state images [BH][N], prefix-state images [BH][NC], key-mean image [BH], the online
+// scores [BH][L], and for Residual / Mean the prefix sums of the states [BH][N].
+// ---------------------------------------------------------------------------
+size_t tc_segments_scratch_bytes(const Problem &p, int NC)
+{
+    const size_t BH = p.BH, N = p.N;
+    size_t b = pad256(BH * N * kTile) + pad256(BH * (size_t)NC * kTile) + pad256(BH * kKbImg) +
+               pad256(sizeof(float) * BH * p.L);
+    if (!mode_uses_u(p.mode)) b += pad256(BH * N * kTile);
+    return b;
+}
+
+namespace {
+TcArgs segments_args(const Problem &p, const FwdArgs &fa, const TcSegTables &tb, void *scratch)
+{
+    const size_t BH = p.BH, N = p.N;
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    TcArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(fa.q);
+    a.u = static_cast<const __nv_bfloat16 *>(fa.u);
+    a.y = static_cast<__nv_bfloat16 *>(fa.y);
+    a.states = fa.states;
+    a.states_img = base;
+    base += pad256(BH * N * kTile);
+    a.spre_img = base;
+    base += pad256(BH * (size_t)tb.NC * kTile);
+    a.kbar_img = base;
+    base += pad256(BH * kKbImg);
+    a.r_on = reinterpret_cast<float *>(base);
+    base += pad256(sizeof(float) * BH * p.L);
+    a.prefix_img = mode_uses_u(p.mode) ? nullptr : base;
+    a.kbar_out = mode_uses_u(p.mode) ? fa.kbar : nullptr;  // fp32 key means, for the segments after
+    a.topk = p.topk;
+    a.mean = p.mode == MC_MEAN;
+    a.BH = p.BH; a.L = p.L; a.C = p.C; a.N = p.N; a.CPS = 0; a.d = p.d; a.NB = 1;
+    a.sg_off = tb.off;
+    a.sg_cbase = tb.cbase;
+    a.vtiles = tb.tiles;
+    a.Nseg = tb.Nseg;
+    a.NC = tb.NC;
+    a.num_tiles = p.BH * tb.NC;
+    return a;
+}
+}  // namespace
+
+cudaError_t launch_state_tc_segments(const Problem &p, const FwdArgs &fa, const TcSegTables &tb, void *scratch,
+                                     cudaStream_t s)
+{
+    const bool gated = mode_uses_u(p.mode);
+    TcArgs a = segments_args(p, fa, tb, scratch);
+    CUtensorMap mK, mV, mU;
+    const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    if (!make_tmap_bf16_sw128(&mK, fa.k, rows, p.d, 128) || !make_tmap_bf16_sw128(&mV, fa.v, rows, p.d, 128))
+        return cudaErrorInvalidValue;
+    if (gated) {
+        if (!make_tmap_bf16_sw128(&mU, fa.u, rows, p.d, 128)) return cudaErrorInvalidValue;
+    } else {
+        mU = mK;
+    }
+    cudaError_t e;
+    if (gated && (e = cudaMemsetAsync(a.kbar_img, 0, (size_t)p.BH * kKbImg, s)) != cudaSuccess) return e;
+    auto k1 = gated ? seg_state_tc<true, false, true> : seg_state_tc<false, false, true>;
+    const size_t smem1 = t1_smem_bytes<false>();
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
+    const int units = p.BH * tb.Nseg, sms = sm_count();
+    k1<<<units < sms ? units : sms, kT1Threads, smem1, s>>>(mK, mV, mU, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_after_kernel(s, "seg_state_tc");
+    return cudaSuccess;
+}
+
+// After every segment's state exists (fp32, fa.states): the Residual prefix sums and the
+// readout of the tokens of segments 0 .. Nseg-1.
+cudaError_t launch_readout_tc_segments(const Problem &p, const FwdArgs &fa, const TcSegTables &tb, void *scratch,
+                                       cudaStream_t s)
+{
+    const bool gated = mode_uses_u(p.mode);
+    TcArgs a = segments_args(p, fa, tb, scratch);
+    CUtensorMap mQ, mK, mV64, mU;
+    const unsigned long long rows = (unsigned long long)p.BH * p.L;
+    if (!make_tmap_bf16_sw128(&mQ, fa.q, rows, p.d, 128) || !make_tmap_bf16_sw128(&mK, fa.k, rows, p.d, 128) ||
+        !make_tmap_bf16_sw128(&mV64, fa.v, rows, p.d, 64))
+        return cudaErrorInvalidValue;
+    if (gated) {
+        if (!make_tmap_bf16_sw128(&mU, fa.u, rows, p.d, 128)) return cudaErrorInvalidValue;
+    } else {
+        mU = mK;
+    }
+    cudaError_t e;
+    if (!gated) {
+        dim3 grid((kD * kD + 255) / 256, (unsigned)p.BH);
+        prefix_images<<<grid, 256, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        profile_after_kernel(s, "prefix_images");
+    }
+    auto k2 = !gated ? readout_tc<false, false, false, false, true>
+              : p.mode == MC_SSC ? readout_tc<true, false, true, false, true> : readout_tc<true, false, false, false, true>;
+    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem)) != cudaSuccess) return e;
+    const int slots = kT2CtasPerSm * sm_count();
+    k2<<<a.num_tiles < slots ? a.num_tiles : slots, kT2Threads, kT2Smem, s>>>(mQ, mK, mV64, mU, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_after_kernel(s, "readout_tc");
+    return cudaSuccess;
 }
 
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)

@@ -2,6 +2,7 @@
 // scratch, and the choice of kernels for a shape.
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -245,6 +246,101 @@ int forward_common(const void *q, const void *k, const void *v, const void *u, i
     return MC_OK;
 }
 
+// The forward over given boundaries (host seg_off) whose first nbig segments are whole
+// 128-token chunks and whose remaining segments lie in the last L % 128 tokens: the
+// state-form tensor-core kernels for the first, the CUDA-core scan and readout for the tail.
+int forward_segments_tc(const Problem &p, const void *q, const void *k, const void *v, const void *u,
+                        const int32_t *seg_off, int nbig, void *y, float *states, cudaStream_t stream)
+{
+    const int N = p.N, L = p.L, d = p.d;
+    const int ntail = N - nbig;
+    const int NC = seg_off[nbig] / 128;  // 128-token chunks of the tensor-core segments
+    int tail_max = 0;
+    for (int n = nbig; n < N; ++n) tail_max = std::max(tail_max, seg_off[n + 1] - seg_off[n]);
+    // one int32 table: boundaries [N + 1], first chunks [nbig], readout tiles [2 NC] (segment,
+    // chunk, the segments with more cached states first), then for the tail scan the first
+    // piece of every segment [N + 1] and the segment of every piece [ntail]
+    std::vector<int32_t> tab(seg_off, seg_off + N + 1);
+    const size_t o_cbase = tab.size();
+    for (int n = 0; n < nbig; ++n) tab.push_back(seg_off[n] / 128);
+    if (tab.size() % 2) tab.push_back(0);  // int2 alignment
+    const size_t o_tiles = tab.size();
+    for (int n = nbig - 1; n >= 0; --n)
+        for (int c = 0; c < (seg_off[n + 1] - seg_off[n]) / 128; ++c) {
+            tab.push_back(n);
+            tab.push_back(c);
+        }
+    const size_t o_pieces = tab.size();
+    for (int n = 0; n <= N; ++n) tab.push_back(n <= nbig ? 0 : n - nbig);
+    const size_t o_pseg = tab.size();
+    for (int j = 0; j < ntail; ++j) tab.push_back(nbig + j);
+
+    const size_t BH = p.BH;
+    const size_t b_tab = round_up(sizeof(int32_t) * tab.size());
+    const size_t b_states = states ? 0 : round_up(sizeof(float) * BH * N * d * d);
+    const size_t b_kbar = round_up(sizeof(float) * BH * N * d);
+    const size_t b_O = ntail ? round_up(sizeof(float) * BH * L * d) : 0;
+    const size_t b_r = ntail ? round_up(sizeof(float) * BH * L) : 0;
+    const size_t b_tc = tc_segments_scratch_bytes(p, NC);
+    void *scratch = nullptr;
+    if (scratch_alloc(&scratch, b_tab + b_states + b_kbar + b_O + b_r + b_tc, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_ALLOC;
+    }
+    char *base = static_cast<char *>(scratch);
+    int32_t *dtab = reinterpret_cast<int32_t *>(base);
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.u = mode_uses_u(p.mode) ? u : nullptr;
+    a.y = y;
+    a.states = states ? states : reinterpret_cast<float *>(base + b_tab);
+    a.kbar = reinterpret_cast<float *>(base + b_tab + b_states);
+    a.O_on = ntail ? reinterpret_cast<float *>(base + b_tab + b_states + b_kbar) : nullptr;
+    a.r_on = ntail ? reinterpret_cast<float *>(base + b_tab + b_states + b_kbar + b_O) : nullptr;
+    void *tc_scratch = base + b_tab + b_states + b_kbar + b_O + b_r;
+    TcSegTables tb{};
+    tb.off = dtab;
+    tb.cbase = dtab + o_cbase;
+    tb.tiles = reinterpret_cast<const int2 *>(dtab + o_tiles);
+    tb.Nseg = nbig;
+    tb.NC = NC;
+    cudaError_t e = cudaMemcpyAsync(dtab, tab.data(), sizeof(int32_t) * tab.size(), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) {
+        profile_call_start(stream);
+        e = launch_state_tc_segments(p, a, tb, tc_scratch, stream);
+    }
+    if (e == cudaSuccess && ntail) {  // the tail's segments on the CUDA cores, one piece each
+        FwdArgs t = a;
+        t.seg_off = dtab;
+        t.seg_pieces = dtab + o_pieces;
+        t.piece_seg = dtab + o_pseg;
+        t.npieces = ntail;
+        t.piece_len = 128;
+        t.BH = p.BH; t.L = L; t.C = tail_max; t.N = N; t.mode = p.mode; t.topk = p.topk;
+        Problem pt = p;
+        pt.C = tail_max;
+        e = launch_seg_scan_simt(pt, t, stream);
+        profile_after_kernel(stream, "seg_scan_simt");
+    }
+    if (e == cudaSuccess) e = launch_readout_tc_segments(p, a, tb, tc_scratch, stream);
+    if (e == cudaSuccess && ntail) {
+        FwdArgs t = a;
+        t.seg_off = dtab;
+        t.readout_last = ntail;
+        t.BH = p.BH; t.L = L; t.C = tail_max; t.N = N; t.mode = p.mode; t.topk = p.topk;
+        Problem pt = p;
+        pt.C = tail_max;
+        e = launch_readout_simt(pt, t, stream);
+        profile_after_kernel(stream, "readout_simt");
+    }
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess || ef != cudaSuccess) {
+        cudaGetLastError();
+        return MC_ERR_CUDA;
+    }
+    return MC_OK;
+}
+
 // The forward over given segment boundaries (FFMA kernels; seg_off is host memory).
 int forward_segments(const void *q, const void *k, const void *v, const void *u, int B, int H, int L, int d,
                      const int32_t *seg_off, int nseg, int agg_mode, int topk, void *y, float *states, bool bf16,
@@ -281,6 +377,14 @@ int forward_segments(const void *q, const void *k, const void *v, const void *u,
     }
     st = check_device();
     if (st != MC_OK) return st;
+    // Tensor cores for the leading segments that are whole 128-token chunks (start and
+    // length multiples of 128) when the rest -- a tail of shorter segments -- fits in the
+    // last L % 128 tokens (the logarithmic segmentation of Log-Linear++ is of this kind).
+    int nbig = 0;
+    while (nbig < nseg && seg_off[nbig] % 128 == 0 && (seg_off[nbig + 1] - seg_off[nbig]) % 128 == 0) ++nbig;
+    if (bf16 && (d == 64 || d == 128) && p.N <= 64 && nbig >= 1 && L - seg_off[nbig] < 128 &&
+        (p.mode != MC_SSC || p.topk <= 16))
+        return forward_segments_tc(p, q, k, v, u, seg_off, nbig, y, states, stream);
     // Segments longer than kPieceLen tokens are scanned in pieces (all at once, then a
     // prefix over each segment's pieces): boundaries, then the first piece of every
     // segment, then the segment of every piece, in one host table.

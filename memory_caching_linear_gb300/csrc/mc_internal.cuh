@@ -52,6 +52,7 @@ struct FwdArgs {
     int npieces, piece_len;
     float *piece_state;         // [BH][npieces][d][d] scratch: a piece's own state, then the state before it
     float *piece_ksum;          // [BH][npieces][d] scratch: the same for the key sums
+    int readout_last;           // readout_simt: launch only for the last this many segments (0: all)
     int BH, L, C, N, mode, topk;
 };
 
@@ -125,6 +126,19 @@ void profile_after_kernel(cudaStream_t s, const char *name);
 // (the SWLA update, the stand-alone router and the backward need this).
 bool tc_supported(const Problem &p);
 bool tc_fused_gates(const Problem &p);
+// The state form over given segment boundaries (mc_forward_segments): segments 0 .. Nseg-1
+// are whole 128-token chunks; off [Nseg + 1] their first tokens (device), cbase [Nseg] their
+// first chunks (off / 128), tiles [NC] the readout's (segment, chunk) slots heaviest first.
+struct TcSegTables {
+    const int32_t *off, *cbase;
+    const int2 *tiles;
+    int Nseg, NC;
+};
+size_t tc_segments_scratch_bytes(const Problem &p, int NC);
+cudaError_t launch_state_tc_segments(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
+                                     cudaStream_t s);
+cudaError_t launch_readout_tc_segments(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
+                                       cudaStream_t s);
 size_t tc_scratch_bytes(const Problem &p);
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 size_t tc_select_scratch_bytes(const Problem &p);

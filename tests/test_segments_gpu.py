@@ -74,3 +74,51 @@ def test_constant_boundaries_match_mc_forward():
     y1, s1 = mcl.mc_forward_segments(q, k, v, u, list(range(0, 641, 128)), GRM)
     torch.testing.assert_close(y1, y0, rtol=0, atol=0)
     torch.testing.assert_close(s1, s0, rtol=0, atol=0)
+
+
+# Given boundaries whose leading segments are whole 128-token chunks and whose other
+# segments lie in the last L % 128 tokens run the tensor-core kernels for the former
+# and the CUDA-core scan and readout for the tail.
+TC_CASES = [
+    # (name, B, H, L, d, boundaries or None for the logarithmic segmentation)
+    ("tc-log-777", 1, 2, 777, 128, None),         # 512, 256 | 8, 1
+    ("tc-log-4095-d64", 1, 1, 4095, 64, None),     # 2048 .. 128 | 64 .. 1
+    ("tc-no-tail", 2, 1, 2048, 128, [0, 1536, 2048]),
+    ("tc-mixed", 1, 2, 1380, 128, [0, 384, 1152, 1280, 1300, 1301, 1380]),  # 384, 768, 128 | 20, 1, 79
+]
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (RESIDUAL, 0), (SOUP, 0), (SSC, 2), (MEAN, 0)])
+@pytest.mark.parametrize("name,B,H,L,d,off", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_segments_tensor_core_parity(name, B, H, L, d, off, mode, topk):
+    off_gpu = mcl.log_segments(L) if off is None else off
+    off = oracle.log_segments(L) if off is None else off
+    q, k, v, u = make_inputs(B, H, L, d, seed=zlib.crc32(name.encode()) % 1000, dtype="bf16")
+    ref = oracle.forward(q, k, v, u, None, mode, topk, seg_off=off)
+    dev = torch.device("cuda")
+    args = [t.to(dev) for t in (q, k, v, u)]
+    with mcl.KernelProfile() as prof:
+        y, st = mcl.mc_forward_segments(*args, off_gpu, mode, topk)
+    torch.cuda.synchronize()
+    assert mcl.mc_check_device() == mcl.MC_OK
+    assert "seg_state_tc" in prof.stages and "readout_tc" in prof.stages, prof.stages
+    tail = L % 128 != 0
+    assert ("readout_simt" in prof.stages) == tail, prof.stages
+    y, st = y.float().cpu().numpy(), st.cpu().numpy()
+    if mode == SSC and 0 < topk < len(off) - 2:
+        check_y_over_valid_sets(
+            y, q, k, v, u, off, topk, ref,
+            lambda sel: oracle.forward(q, k, v, u, None, SSC, topk, seg_off=off, given_sel=sel)["y"], TOL["bf16"])
+    else:
+        assert rel_err(y, ref["y"]) <= TOL["bf16"], (name, mode, rel_err(y, ref["y"]))
+    assert rel_err(st, ref["states"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode,topk", [(GRM, 0), (RESIDUAL, 0), (SSC, 2)])
+def test_constant_boundaries_match_mc_forward_tensor_cores(mode, topk):
+    # the same segments through both tensor-core paths: the same arithmetic per tile
+    q, k, v, u = (t.cuda() for t in make_inputs(1, 2, 2048, 128, 4, "bf16"))
+    y0, s0 = mcl.forward(q, k, v, u, 256, mode, topk)
+    y1, s1 = mcl.mc_forward_segments(q, k, v, u, list(range(0, 2049, 256)), mode, topk)
+    torch.testing.assert_close(s1, s0, rtol=0, atol=0)
+    torch.testing.assert_close(y1, y0, rtol=0, atol=0)
