@@ -149,7 +149,8 @@ def metric_name(w):
 
 _CSRC = "memory_caching_linear_gb300/csrc/"
 # the sources each tensor-core kernel is built from: the state-form path, and the general path
-KERNEL_SOURCES = tuple(_CSRC + f for f in ("k_tc.cu", "sm100.cuh", "tc_common.cuh", "mc_internal.cuh"))
+KERNEL_SOURCES = tuple(_CSRC + f for f in ("k_tc.cu", "k_tc64.cu", "tc_state_form.cuh", "sm100.cuh",
+                                           "tc_common.cuh", "tensormap.cuh", "mc_internal.cuh"))
 GEN_KERNEL_SOURCES = tuple(_CSRC + f for f in ("k_gen.cu", "sm100.cuh", "tc_common.cuh", "tensormap.cuh",
                                                "mc_internal.cuh"))
 GEN_KERNELS = ("seg_piece_tc", "gates_tc", "readout_fact_tc")

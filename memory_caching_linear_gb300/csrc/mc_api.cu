@@ -794,13 +794,13 @@ int mc_check_device(mc_stream_t stream)
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    int was = 0, was_bwd = 0, was_gen = 0;
+    int was = 0, was_bwd = 0, was_gen = 0, was64 = 0;
     if (mc::take_device_abort(&was) != cudaSuccess || mc::take_bwd_abort(&was_bwd) != cudaSuccess ||
-        mc::take_gen_abort(&was_gen) != cudaSuccess) {
+        mc::take_gen_abort(&was_gen) != cudaSuccess || mc::take_tc64_abort(&was64) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_CUDA;
     }
-    return was || was_bwd || was_gen ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
+    return was || was_bwd || was_gen || was64 ? MC_ERR_DEVICE_TIMEOUT : MC_OK;
 }
 
 int mc_profile_begin(void *const *events, int capacity)

@@ -141,6 +141,13 @@ cudaError_t launch_readout_tc_segments(const Problem &p, const FwdArgs &a, const
                                        cudaStream_t s);
 size_t tc_scratch_bytes(const Problem &p);
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+// The d = 64 instantiations of the forward and segment launchers (k_tc64.cu).
+cudaError_t launch_forward_tc64(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
+cudaError_t launch_state_tc_segments64(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
+                                       cudaStream_t s);
+cudaError_t launch_readout_tc_segments64(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
+                                         cudaStream_t s);
+cudaError_t take_tc64_abort(int *was_set);
 size_t tc_select_scratch_bytes(const Problem &p);
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 // The forward's state kernel alone, for the tensor-core backward: images of the cached

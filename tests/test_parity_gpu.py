@@ -104,12 +104,13 @@ TC_CASES = [
     ("tc-C512-N8", 1, 2, 4096, 128, 512),
     ("tc-C2048-N1", 2, 1, 2048, 128, 2048),
     ("tc-C256-N4-BH160", 10, 16, 1024, 128, 256),
-    ("tc-d64-C128-N32", 1, 2, 4096, 64, 128),  # d = 64: tiles zero-padded to 128 by the TMA
+    ("tc-d64-C128-N32", 1, 2, 4096, 64, 128),  # d = 64: 64-wide tiles
+    ("tc-d64-C512-N8", 1, 2, 4096, 64, 512),   # d = 64, four chunks per segment (prefix-state images)
     # more than 64 segments: the gates go through HBM (three key-mean blocks at N = 130)
     ("tc-C128-N96", 1, 1, 12288, 128, 128),
     ("tc-d64-C128-N130", 1, 1, 16640, 64, 128),
 ]
-TC_SSC_CASES = TC_CASES[:2] + TC_CASES[-3:]
+TC_SSC_CASES = TC_CASES[:2] + TC_CASES[4:]
 
 
 @pytest.mark.parametrize("mode", [RESIDUAL, GRM, SOUP, MEAN])
