@@ -720,7 +720,8 @@ def run_segments(args):
     big, tail = range(nbig), range(nbig, len(lens))
     f_state = bh * w.L * 2 * d * d
     work_of = {"seg_state_tc": bh * l_big * 2 * d * d, "readout_tc": read_flops(big),
-               "seg_scan_simt": bh * (w.L - l_big) * 2 * d * d, "readout_simt": read_flops(tail)}
+               "seg_scan_simt": bh * (w.L - l_big) * 2 * d * d, "readout_simt": read_flops(tail),
+               "tail_readout_simt": read_flops(tail)}
     dom = max(kernels_ms, key=kernels_ms.get)
     work = work_of.get(dom, 0)
     if dom.endswith("_tc"):
@@ -743,9 +744,10 @@ def run_segments(args):
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom, "launch_ms": kernels_ms[dom],
                      "algorithmic_tflop_per_launch": round(work / 1e12, 4), "peak_source": psrc},
-        # the piece-split scan records one stage for its three launches (scan, piece prefix, fix-up)
-        "kernels_ms": kernels_ms, "gpu_launches": prof.kernel_count() + (
-            2 * prof.stages.count("seg_scan_simt") if (nbig or max(lens) > 512) else 0),
+        # stages of several launches: the tail readout (gates, partials, finish) and, on the CUDA-core
+        # path with segments longer than 512 tokens, the piece-split scan (scan, piece prefix, fix-up)
+        "kernels_ms": kernels_ms, "gpu_launches": prof.kernel_count() + 2 * prof.stages.count("tail_readout_simt") + (
+            2 * prof.stages.count("seg_scan_simt") if (not nbig and max(lens) > 512) else 0),
         "clocks": sampler.summary(),
     }
 

@@ -555,6 +555,7 @@ cudaError_t seg_scan_impl(const Problem &p, const FwdArgs &a, cudaStream_t s)
     // long segments in pieces: every piece at once, then the prefixes over each segment's pieces
     kern<<<(unsigned)((long long)p.BH * a.npieces), kThreads, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!a.piece_state) return cudaSuccess;  // one piece per segment: nothing to carry between pieces
     seg_prefix_simt<D><<<dim3((unsigned)((long long)p.BH * p.N), (unsigned)((D * D + D + kThreads - 1) / kThreads)),
                          kThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -281,9 +281,11 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
     const size_t b_kbar = round_up(sizeof(float) * BH * N * d);
     const size_t b_O = ntail ? round_up(sizeof(float) * BH * L * d) : 0;
     const size_t b_r = ntail ? round_up(sizeof(float) * BH * L) : 0;
+    const int t_tail = seg_off[nbig];  // the tail's first token
+    const size_t b_acc = ntail ? round_up(tail_scratch_bytes(p, t_tail)) : 0;
     const size_t b_tc = tc_segments_scratch_bytes(p, NC);
     void *scratch = nullptr;
-    if (scratch_alloc(&scratch, b_tab + b_states + b_kbar + b_O + b_r + b_tc, stream) != cudaSuccess) {
+    if (scratch_alloc(&scratch, b_tab + b_states + b_kbar + b_O + b_r + b_acc + b_tc, stream) != cudaSuccess) {
         cudaGetLastError();
         return MC_ERR_ALLOC;
     }
@@ -297,7 +299,8 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
     a.kbar = reinterpret_cast<float *>(base + b_tab + b_states);
     a.O_on = ntail ? reinterpret_cast<float *>(base + b_tab + b_states + b_kbar) : nullptr;
     a.r_on = ntail ? reinterpret_cast<float *>(base + b_tab + b_states + b_kbar + b_O) : nullptr;
-    void *tc_scratch = base + b_tab + b_states + b_kbar + b_O + b_r;
+    void *tail_scratch = base + b_tab + b_states + b_kbar + b_O + b_r;
+    void *tc_scratch = base + b_tab + b_states + b_kbar + b_O + b_r + b_acc;
     TcSegTables tb{};
     tb.off = dtab;
     tb.cbase = dtab + o_cbase;
@@ -323,15 +326,12 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
         profile_after_kernel(stream, "seg_scan_simt");
     }
     if (e == cudaSuccess) e = launch_readout_tc_segments(p, a, tb, tc_scratch, stream);
-    if (e == cudaSuccess && ntail) {
+    if (e == cudaSuccess && ntail) {  // the tail's tokens read every earlier state
         FwdArgs t = a;
         t.seg_off = dtab;
-        t.readout_last = ntail;
         t.BH = p.BH; t.L = L; t.C = tail_max; t.N = N; t.mode = p.mode; t.topk = p.topk;
-        Problem pt = p;
-        pt.C = tail_max;
-        e = launch_readout_simt(pt, t, stream);
-        profile_after_kernel(stream, "readout_simt");
+        e = launch_tail_readout(p, t, t_tail, tail_scratch, stream);
+        profile_after_kernel(stream, "tail_readout_simt");
     }
     cudaError_t ef = cudaFreeAsync(scratch, stream);
     if (e != cudaSuccess || ef != cudaSuccess) {

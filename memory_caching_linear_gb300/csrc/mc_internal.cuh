@@ -69,15 +69,23 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// Gate score <u_t, kbar_i> in fp32, summed in key order.  Every kernel that
+// Gate score <u_t, kbar_i> in fp32 on the CUDA cores: four interleaved partial sums
+// (columns 4j + r into p_r, j ascending) added as (p0 + p1) + (p2 + p3), i.e. four
+// independent dependency chains; d is a multiple of 4.  Every CUDA-core kernel that
 // needs a router score calls this one function, so the SSC ranking seen by
-// mc_ssc_select is bit-identical to the one the forward uses.
-// kb must be GLOBAL memory (it is read with __ldg); u_row may be shared or global.
+// mc_ssc_select is bit-identical to the one the forward uses.  u_row and kb may each be
+// in shared or global memory.
 __device__ __forceinline__ float gate_score(const float *__restrict__ u_row, const float *__restrict__ kb, int d)
 {
-    float acc = 0.f;
-    for (int c = 0; c < d; ++c) acc = fmaf(u_row[c], __ldg(kb + c), acc);
-    return acc;
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < d; c += 4) {
+        p0 = fmaf(u_row[c], kb[c], p0);
+        p1 = fmaf(u_row[c + 1], kb[c + 1], p1);
+        p2 = fmaf(u_row[c + 2], kb[c + 2], p2);
+        p3 = fmaf(u_row[c + 3], kb[c + 3], p3);
+    }
+    return (p0 + p1) + (p2 + p3);
 }
 
 // Insert (val, idx) into a top-k list kept sorted by value descending, index
@@ -148,6 +156,11 @@ cudaError_t launch_state_tc_segments64(const Problem &p, const FwdArgs &a, const
 cudaError_t launch_readout_tc_segments64(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
                                          cudaStream_t s);
 cudaError_t take_tc64_abort(int *was_set);
+// The readout of the tokens [t_tail, L) (fewer than 128, the segments after the tensor-core
+// ones of a given segmentation; k_tail.cu): needs O_on, r_on of those tokens and the fp32
+// states and key means of every segment; bf16 inputs, d = 64 or 128, N <= 64.
+size_t tail_scratch_bytes(const Problem &p, int t_tail);
+cudaError_t launch_tail_readout(const Problem &p, const FwdArgs &a, int t_tail, void *scratch, cudaStream_t s);
 size_t tc_select_scratch_bytes(const Problem &p);
 cudaError_t launch_ssc_select_tc(const Problem &p, const FwdArgs &a, void *scratch, cudaStream_t s);
 // The forward's state kernel alone, for the tensor-core backward: images of the cached

@@ -103,7 +103,7 @@ def test_segments_tensor_core_parity(name, B, H, L, d, off, mode, topk):
     assert mcl.mc_check_device() == mcl.MC_OK
     assert "seg_state_tc" in prof.stages and "readout_tc" in prof.stages, prof.stages
     tail = L % 128 != 0
-    assert ("readout_simt" in prof.stages) == tail, prof.stages
+    assert ("tail_readout_simt" in prof.stages) == tail, prof.stages
     y, st = y.float().cpu().numpy(), st.cpu().numpy()
     if mode == SSC and 0 < topk < len(off) - 2:
         check_y_over_valid_sets(
