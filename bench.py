@@ -820,7 +820,10 @@ def main(argv=None):
     if args.workload.startswith("bwd-"):
         if args.impl == "ours":
             name = args.workload[4:]
-            print(json.dumps(run_backward(args, WORKLOADS[name], name)), flush=True)
+            wb = WORKLOADS[name]
+            if args.heads:
+                wb = wb.with_(B=1, H=args.heads, name=f"{wb.name} (slice: B1 H{args.heads})")
+            print(json.dumps(run_backward(args, wb, name)), flush=True)
         return
     w = WORKLOADS[args.workload]
     if args.heads:
