@@ -370,7 +370,7 @@ cudaError_t launch_readout_tc_segments(const Problem &p, const FwdArgs &fa, cons
                      : readout_segments_impl<128>(p, fa, tb, scratch, s);
 }
 
-size_t tc_segments_scratch_bytes(const Problem &p, int NC) { return segments_scratch_bytes(p, NC); }
+size_t tc_segments_scratch_bytes(const Problem &p, int NC, int nslots) { return segments_scratch_bytes(p, NC, nslots); }
 
 // d = 64 runs the 64-wide instantiations, compiled in their own translation unit.
 cudaError_t launch_forward_tc(const Problem &p, const FwdArgs &fa, void *scratch, cudaStream_t s)

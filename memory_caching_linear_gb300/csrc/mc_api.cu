@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cstring>
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -274,6 +275,30 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
     for (int n = 0; n <= N; ++n) tab.push_back(n <= nbig ? 0 : n - nbig);
     const size_t o_pseg = tab.size();
     for (int j = 0; j < ntail; ++j) tab.push_back(nbig + j);
+    // The state walk's units: pieces of kStatePiece chunks (a segment's last piece shorter), so that no
+    // CTA walks a long segment alone; the pieces before a segment's last get their own states from a
+    // first pass (slots), and every piece starts from the sum of the ones before it.  Int4 rows
+    // (segment, first chunk, chunks, aux), the longest first.
+    constexpr int kStatePiece = 16;
+    std::vector<std::array<int32_t, 4>> u1, u2;
+    int nslots = 0;
+    for (int n = 0; n < nbig; ++n) {
+        const int nch = (seg_off[n + 1] - seg_off[n]) / 128;
+        const int pl = std::max(kStatePiece, (nch + 255) / 256);  // at most 256 pieces (8-bit count)
+        const int np = (nch + pl - 1) / pl;
+        for (int q = 0; q < np; ++q) {
+            const int len = std::min(pl, nch - q * pl);
+            if (q + 1 < np) u1.push_back({n, q * pl, len, nslots + q});
+            u2.push_back({n, q * pl, len, (nslots << 8) | q});
+        }
+        nslots += np - 1;
+    }
+    std::stable_sort(u2.begin(), u2.end(), [](const auto &x, const auto &y) { return x[2] > y[2]; });
+    while (tab.size() % 4) tab.push_back(0);  // int4 alignment
+    const size_t o_u1 = tab.size();
+    for (const auto &x : u1) tab.insert(tab.end(), x.begin(), x.end());
+    const size_t o_u2 = tab.size();
+    for (const auto &x : u2) tab.insert(tab.end(), x.begin(), x.end());
 
     const size_t BH = p.BH;
     const size_t b_tab = round_up(sizeof(int32_t) * tab.size());
@@ -283,7 +308,7 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
     const size_t b_r = ntail ? round_up(sizeof(float) * BH * L) : 0;
     const int t_tail = seg_off[nbig];  // the tail's first token
     const size_t b_acc = ntail ? round_up(tail_scratch_bytes(p, t_tail)) : 0;
-    const size_t b_tc = tc_segments_scratch_bytes(p, NC);
+    const size_t b_tc = tc_segments_scratch_bytes(p, NC, nslots);
     void *scratch = nullptr;
     if (scratch_alloc(&scratch, b_tab + b_states + b_kbar + b_O + b_r + b_acc + b_tc, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -307,6 +332,11 @@ int forward_segments_tc(const Problem &p, const void *q, const void *k, const vo
     tb.tiles = reinterpret_cast<const int2 *>(dtab + o_tiles);
     tb.Nseg = nbig;
     tb.NC = NC;
+    tb.units1 = reinterpret_cast<const int4 *>(dtab + o_u1);
+    tb.units2 = reinterpret_cast<const int4 *>(dtab + o_u2);
+    tb.n1 = (int)u1.size();
+    tb.n2 = (int)u2.size();
+    tb.nslots = nslots;
     cudaError_t e = cudaMemcpyAsync(dtab, tab.data(), sizeof(int32_t) * tab.size(), cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) {
         profile_call_start(stream);

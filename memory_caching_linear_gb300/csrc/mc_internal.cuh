@@ -137,12 +137,16 @@ bool tc_fused_gates(const Problem &p);
 // The state form over given segment boundaries (mc_forward_segments): segments 0 .. Nseg-1
 // are whole 128-token chunks; off [Nseg + 1] their first tokens (device), cbase [Nseg] their
 // first chunks (off / 128), tiles [NC] the readout's (segment, chunk) slots heaviest first.
+// units1 [n1] are the pieces whose own state and key sums the first pass forms (slots 0 .. nslots-1),
+// units2 [n2] every piece, each starting from the totals of the pieces before it (state form walk).
 struct TcSegTables {
     const int32_t *off, *cbase;
     const int2 *tiles;
     int Nseg, NC;
+    const int4 *units1, *units2;
+    int n1, n2, nslots;
 };
-size_t tc_segments_scratch_bytes(const Problem &p, int NC);
+size_t tc_segments_scratch_bytes(const Problem &p, int NC, int nslots);
 cudaError_t launch_state_tc_segments(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,
                                      cudaStream_t s);
 cudaError_t launch_readout_tc_segments(const Problem &p, const FwdArgs &a, const TcSegTables &tb, void *scratch,

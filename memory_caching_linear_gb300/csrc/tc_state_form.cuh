@@ -54,11 +54,21 @@ struct TcArgs {
     const int32_t *sg_off, *sg_cbase;
     const int2 *vtiles;
     int Nseg, NC;
+    // The state kernel's units over given boundaries: pieces (segment, first chunk within it, chunks,
+    // aux) of the whole-chunk segments, the longest first.  With `totals` set the kernel only forms
+    // each unit's own state and key sum (aux = its slot in ptot / pks); otherwise a unit starts
+    // from the sum of the totals of the pieces before it (aux = first slot << 8 | their count).
+    const int4 *units;
+    int NU, totals, nslots;
+    float *ptot;  // [BH][nslots][d][d] fp32
+    float *pks;   // [BH][nslots][d] fp32
 };
 
 // A head's segment as the kernels see it: constant length C, or from the tables.
 struct SegInfo {
     int bh, seg, nch, off, len, cbase;
+    int pc0, aux;  // VAR: the unit's first chunk within its segment, and its table word
+    bool last;     // the unit ends its segment
 };
 
 template <bool VAR>
@@ -72,13 +82,20 @@ __device__ __forceinline__ SegInfo seg_info(const TcArgs &a, int uid)
         u.off = u.seg * a.C;
         u.len = a.C;
         u.cbase = u.seg * a.CPS;
-    } else {  // units segment by segment (the longest first), every head of a segment together
-        u.seg = uid / a.BH;
+        u.pc0 = 0;
+        u.aux = 0;
+        u.last = true;
+    } else {  // units from the table (the longest first), every head of a unit together
+        const int4 t = a.units[uid / a.BH];
+        u.seg = t.x;
         u.bh = uid % a.BH;
-        u.off = a.sg_off[u.seg];
-        u.len = a.sg_off[u.seg + 1] - u.off;
-        u.nch = u.len / kCT;
-        u.cbase = a.sg_cbase[u.seg];
+        u.pc0 = t.y;
+        u.nch = t.z;
+        u.aux = t.w;
+        u.len = a.sg_off[u.seg + 1] - a.sg_off[u.seg];
+        u.off = a.sg_off[u.seg] + t.y * kCT;
+        u.cbase = a.sg_cbase[u.seg] + t.y;
+        u.last = t.y + t.z == u.len / kCT;
     }
     return u;
 }
@@ -176,7 +193,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     // Persistent: this CTA walks segments (units) blockIdx.x, blockIdx.x + gridDim.x, ...;
     // its chunks form one stream (global chunk counter g) so loads run ahead
     // across segment boundaries.
-    const int nseg_total = a.BH * (VAR ? a.Nseg : a.N);
+    const int nseg_total = a.BH * (VAR ? a.NU : a.N);
+    const bool totals = VAR && a.totals;  // units form their own state only (no images, no scores)
     const int my_segs = (int)blockIdx.x < nseg_total ? (nseg_total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     int my_chunks = 0;
     for (int k = 0; k < my_segs; ++k) my_chunks += seg_info<VAR>(a, (int)blockIdx.x + k * (int)gridDim.x).nch;
@@ -248,7 +266,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 const uint32_t dec_ab = (c + 1 < nch ? 132u : 128u) * 4u;
                 // the first segment's tokens have no cached memory: their single gate is 1 and
                 // their online score is not needed, so u is not read there
-                const bool scored = GATED && cu.u.seg != 0;
+                const bool scored = GATED && cu.u.seg != 0 && !totals;
                 mbar_arrive_expect_tx(&full[s], (scored ? 3 * kOp : 2 * kOp) + (DECAY ? 2 * dec_ab + 512u : 0u));
                 if (DECAY) {
                     float *dec = reinterpret_cast<float *>(st + t1_dec_off<D>());
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 const uint32_t kb = smem_u32(sm + s * kStage), vb = kb + kOp, ub = kb + 2 * kOp;
                 // V^T is M = 128 rows: the two 64-row halves of V (D = 128), or V and the zero panel
                 const uint32_t v_lbo = D == 128 ? kPanel : smem_u32(zero_panel) - vb;
-                if (GATED && cu.u.seg != 0) {  // R = U K^T (online gate score of the chunk's tokens)
+                if (GATED && cu.u.seg != 0 && !totals) {  // R = U K^T (online gate score of the chunk's tokens)
                     const int rb = rc & 1;
                     if (!mbar_wait(&r_empty[rb], ((rc >> 1) & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
@@ -319,11 +337,24 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             const int row0 = bh * a.L + cu.u.off;
             const int s = gch & 1, b = gch & 1;
             const uint32_t r = gch >> 1;
-            if (c == 0) {  // a new segment: memory restarts at zero
+            if (c == 0) {  // a new unit: memory restarts at zero, or at the sum of the earlier pieces' totals
 #pragma unroll
                 for (int k = 0; k < D; ++k) S[k] = 0.f;
                 ks = 0.f;
-                ksum_s[row] = 0.f;
+                if (VAR && !totals && (int)row < D) {
+                    const int slot0 = cu.u.aux >> 8, npre = cu.u.aux & 255;
+                    for (int pp = 0; pp < npre; ++pp) {
+                        const size_t sl = (size_t)bh * a.nslots + slot0 + pp;
+                        const float4 *tp = reinterpret_cast<const float4 *>(a.ptot + (sl * D + row) * D);
+#pragma unroll
+                        for (int k4 = 0; k4 < D / 4; ++k4) {
+                            const float4 x = tp[k4];
+                            S[4 * k4] += x.x; S[4 * k4 + 1] += x.y; S[4 * k4 + 2] += x.z; S[4 * k4 + 3] += x.w;
+                        }
+                        ks += a.pks[sl * D + row];
+                    }
+                }
+                ksum_s[row] = ks;
                 named_bar_sync(1, 128);
             }
             if (ok) ok = mbar_wait(&full[s], r & 1, &abort_flag);
@@ -366,8 +397,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 }
                 mbar_arrive(&v_scaled);
             }
-            if (GATED && seg == 0 && ok) a.r_on[(size_t)row0 + c * kCT + row] = 0.f;  // single gate: the score is unused
-            if (GATED && seg != 0 && ok) {
+            if (GATED && seg == 0 && ok && !totals) a.r_on[(size_t)row0 + c * kCT + row] = 0.f;  // single gate: the score is unused
+            if (GATED && seg != 0 && ok && !totals) {
                 const int rb = rc & 1;
                 float d4[4] = {0.f, 0.f, 0.f, 0.f};  // <u_t, keys of the segment before this chunk>
 #pragma unroll
@@ -403,11 +434,11 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     const float w = (w4[0] + w4[1]) + (w4[2] + w4[3]);
                     tc_fence_before();
                     mbar_arrive(&r_empty[rb]);
-                    const int t_in_seg = c * kCT + (int)row;
-                    a.r_on[(size_t)row0 + t_in_seg] = (dot + w) / (float)(t_in_seg + 1);
+                    const int t_in_seg = (cu.u.pc0 + c) * kCT + (int)row;
+                    a.r_on[(size_t)row0 + c * kCT + row] = (dot + w) / (float)(t_in_seg + 1);
                 }
             }
-            if (GATED && seg != 0) ++rc;
+            if (GATED && seg != 0 && !totals) ++rc;
             // Key column sums of the chunk, in a fixed order: thread (rg, cc) sums
             // columns 8cc..8cc+7 over rows 16rg..16rg+15 in row order; then column
             // `row` adds the eight group sums in rg order to the running sum.
@@ -462,14 +493,22 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                 tc_fence_before();
                 mbar_arrive(&z_empty[b]);
                 const size_t sidx = (size_t)bh * a.N + seg;
-                uint8_t *img = c + 1 < nch ? a.spre_img + ((size_t)bh * NCH + cu.u.cbase + c + 1) * kImg
-                                           : a.states_img + sidx * kImg;
+                const bool seg_end = c + 1 == nch && cu.u.last;
+                if (totals && c + 1 == nch && (int)row < D) {  // the piece's own state and key sums
+                    const size_t sl = (size_t)bh * a.nslots + cu.u.aux;
+                    float4 *tp = reinterpret_cast<float4 *>(a.ptot + (sl * D + row) * D);
+#pragma unroll
+                    for (int k4 = 0; k4 < D / 4; ++k4) tp[k4] = make_float4(S[4 * k4], S[4 * k4 + 1], S[4 * k4 + 2], S[4 * k4 + 3]);
+                    a.pks[sl * D + row] = ks;
+                }
+                uint8_t *img = !seg_end ? a.spre_img + ((size_t)bh * NCH + cu.u.cbase + c + 1) * kImg
+                                        : a.states_img + sidx * kImg;
                 // Through the warp's 4 KB staging area, one 64-column panel at a time: the
                 // warp's 32 rows of a panel are 4 KB contiguous in the image, stored 512
                 // contiguous bytes per instruction.  (D = 64: rows 64.. are zero and not stored.)
 #pragma unroll
                 for (int p = 0; p < NP; ++p) {
-                    if (32 * q4 >= D) break;  // warp-uniform
+                    if (32 * q4 >= D || totals) break;  // warp-uniform
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {  // 16-byte chunk c8 of the row's panel p
                         const int cc = 8 * p + c8;
@@ -483,7 +522,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     for (int i = 0; i < 8; ++i) dst[32 * i + lane] = reinterpret_cast<const uint4 *>(wst)[32 * i + lane];
                     __syncwarp();
                 }
-                if (c + 1 == nch) {  // the segment's cached state (fp32) and key mean
+                if (seg_end && !totals) {  // the segment's cached state (fp32) and key mean
                     // fp32 rows (d values), 32 columns (128 bytes) at a time through the staging
                     // area (16-byte chunk c of row r at chunk c ^ (r % 8)), 4 rows per instruction;
                     // with d < 128 the padded rows and columns are not stored
@@ -1309,14 +1348,16 @@ cudaError_t forward_impl(const Problem &p, const FwdArgs &fa, void *scratch, cud
 // The state form over given segment boundaries: segments 0 .. Nseg-1 of every head
 // are whole 128-token chunks (start and length multiples of 128).  Scratch layout:
 // state images [BH][N], prefix-state images [BH][NC], key-mean image [BH], the online
-// scores [BH][L], and for Residual / Mean the prefix sums of the states [BH][N].
+// scores [BH][L], for Residual / Mean the prefix sums of the states [BH][N], then the pieces'
+// own states [BH][nslots][d][d] and key sums [BH][nslots][d] (fp32).
 // ---------------------------------------------------------------------------
-inline size_t segments_scratch_bytes(const Problem &p, int NC)
+inline size_t segments_scratch_bytes(const Problem &p, int NC, int nslots)
 {
     const size_t BH = p.BH, N = p.N, im = img_bytes(p);
     size_t b = pad256(BH * N * im) + pad256(BH * (size_t)NC * im) + pad256(BH * kKbImg) +
                pad256(sizeof(float) * BH * p.L);
     if (!mode_uses_u(p.mode)) b += pad256(BH * N * im);
+    b += pad256(sizeof(float) * BH * nslots * p.d * p.d) + pad256(sizeof(float) * BH * nslots * p.d);
     return b;
 }
 
@@ -1338,6 +1379,11 @@ inline TcArgs segments_args(const Problem &p, const FwdArgs &fa, const TcSegTabl
     a.r_on = reinterpret_cast<float *>(base);
     base += pad256(sizeof(float) * BH * p.L);
     a.prefix_img = mode_uses_u(p.mode) ? nullptr : base;
+    if (!mode_uses_u(p.mode)) base += pad256(BH * N * im);
+    a.ptot = reinterpret_cast<float *>(base);
+    base += pad256(sizeof(float) * BH * tb.nslots * p.d * p.d);
+    a.pks = reinterpret_cast<float *>(base);
+    a.nslots = tb.nslots;
     a.kbar_out = mode_uses_u(p.mode) ? fa.kbar : nullptr;  // fp32 key means, for the segments after
     a.topk = p.topk;
     a.mean = p.mode == MC_MEAN;
@@ -1364,7 +1410,21 @@ cudaError_t state_segments_impl(const Problem &p, const FwdArgs &fa, const TcSeg
     auto k1 = gated ? seg_state_tc<true, false, true, D> : seg_state_tc<false, false, true, D>;
     const size_t smem1 = t1_smem_bytes<false, D>();
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
-    const int units = p.BH * tb.Nseg, sms = sm_count();
+    const int sms = sm_count();
+    if (tb.n1 > 0) {  // the pieces' own states first: every later piece starts from their sums
+        TcArgs a1 = a;
+        a1.units = tb.units1;
+        a1.NU = tb.n1;
+        a1.totals = 1;
+        const int units = p.BH * tb.n1;
+        k1<<<units < sms ? units : sms, kT1Threads, smem1, s>>>(m.k, m.v, m.u, a1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        profile_after_kernel(s, "seg_piece_sums_tc");
+    }
+    a.units = tb.units2;
+    a.NU = tb.n2;
+    a.totals = 0;
+    const int units = p.BH * tb.n2;
     k1<<<units < sms ? units : sms, kT1Threads, smem1, s>>>(m.k, m.v, m.u, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_after_kernel(s, "seg_state_tc");

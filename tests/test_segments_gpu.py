@@ -85,6 +85,9 @@ TC_CASES = [
     ("tc-log-4095-d64", 1, 1, 4095, 64, None),     # 2048 .. 128 | 64 .. 1
     ("tc-no-tail", 2, 1, 2048, 128, [0, 1536, 2048]),
     ("tc-mixed", 1, 2, 1380, 128, [0, 384, 1152, 1280, 1300, 1301, 1380]),  # 384, 768, 128 | 20, 1, 79
+    # segments longer than the state walk's 16-chunk pieces: 32 chunks (two pieces), 48 chunks (three)
+    ("tc-log-5000", 1, 1, 5000, 128, None),  # 4096, 512, 256, 128 | 8
+    ("tc-pieces-d64", 1, 2, 6500, 64, [0, 6144, 6400, 6500]),  # 6144 (three pieces), 256 | 100
 ]
 
 
@@ -122,3 +125,13 @@ def test_constant_boundaries_match_mc_forward_tensor_cores(mode, topk):
     y1, s1 = mcl.mc_forward_segments(q, k, v, u, list(range(0, 2049, 256)), mode, topk)
     torch.testing.assert_close(s1, s0, rtol=0, atol=0)
     torch.testing.assert_close(y1, y0, rtol=0, atol=0)
+
+
+def test_piece_split_state_walk_matches_mc_forward():
+    # 4096-token segments are two 16-chunk pieces for mc_forward_segments and one walk for mc_forward:
+    # the same states up to the order of the fp32 sums
+    q, k, v, u = (t.cuda() for t in make_inputs(1, 2, 8192, 128, 6, "bf16"))
+    y0, s0 = mcl.forward(q, k, v, u, 4096, GRM)
+    y1, s1 = mcl.mc_forward_segments(q, k, v, u, [0, 4096, 8192], GRM)
+    torch.testing.assert_close(s1, s0, rtol=1e-5, atol=1e-5)
+    torch.testing.assert_close(y1.float(), y0.float(), rtol=2e-2, atol=2e-2)
