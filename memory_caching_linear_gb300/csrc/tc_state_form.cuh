@@ -877,8 +877,8 @@ __global__ void __launch_bounds__(kT2Threads, kT2CtasPerSm)
                 if (GATED && !GG && t.n > 0) {
                     // gate scores S = U (kbar_hi + kbar_mid + kbar_lo)^T into the tile's first A slot
                     // (the workers read S there, then write P over it); the slot's last readers
-                    // were issued before this
-                    constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+                    // were issued before this.  Only the first n columns are read: N = n rounded up to 16.
+                    const uint32_t idS = idesc_bf16(128, 16 * ((t.n + 15) / 16), false, false);
                     const uint32_t ts = tA0 + (ac % 2) * 64;
                     bool ready = true;
                     for (int i = 0; i < NP + 3 && ready; ++i) ready = ring_ready(g + i);
