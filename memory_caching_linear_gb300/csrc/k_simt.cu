@@ -579,8 +579,7 @@ cudaError_t readout_impl(const Problem &p, const FwdArgs &a, cudaStream_t s)
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const long long tps = (p.C + kTR - 1) / kTR;
-    // the grid takes the segments from the last: a prefix of it covers the last few
-    const long long blocks = (long long)p.BH * (a.readout_last > 0 ? a.readout_last : p.N) * tps;
+    const long long blocks = (long long)p.BH * p.N * tps;
     kern<<<(unsigned)blocks, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

@@ -52,7 +52,6 @@ struct FwdArgs {
     int npieces, piece_len;
     float *piece_state;         // [BH][npieces][d][d] scratch: a piece's own state, then the state before it
     float *piece_ksum;          // [BH][npieces][d] scratch: the same for the key sums
-    int readout_last;           // readout_simt: launch only for the last this many segments (0: all)
     int BH, L, C, N, mode, topk;
 };
 
