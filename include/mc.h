@@ -143,8 +143,16 @@ int mc_forward_swla(const void *q, const void *k, const void *v, const void *u,
  *             read during the call only.
  *   states  : fp32 [B][H][nseg][d][d] or NULL.
  *   is_bf16 : q, k, v, u, y are bf16 if non-zero, fp32 otherwise.
- *   Other arguments as mc_forward.  Runs on the FFMA kernels.  MC_ERR_SHAPE for
- *   boundaries that do not rise strictly from 0 to L.
+ *   Other arguments as mc_forward.  MC_ERR_SHAPE for boundaries that do not rise
+ *   strictly from 0 to L.
+ *   Kernels: with bf16 inputs, d in {64, 128}, nseg <= 64 (SSC: topk <= 16), when the
+ *   leading segments start and end on multiples of 128 tokens and the remaining
+ *   segments lie in the last L mod 128 tokens (the logarithmic segmentation is of this
+ *   kind), the leading segments run on the tensor cores (the state form over tables
+ *   of offsets; segments longer than 2048 tokens in pieces whose own states are
+ *   formed first) and the short tail on the CUDA cores; every other case runs on the
+ *   CUDA-core kernels.  The tensor-core path reads bf16 operand images of the states,
+ *   as mc_forward does.
  */
 int mc_forward_segments(const void *q, const void *k, const void *v, const void *u,
                         int B, int H, int L, int d, const int32_t *seg_off, int nseg,
