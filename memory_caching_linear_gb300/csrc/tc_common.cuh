@@ -14,7 +14,7 @@
 
 namespace mc {
 
-constexpr int kD = 128;            // tile width: the head dimension (64 or 128), zero-padded to it where needed
+constexpr int kD = 128;            // the widest head dimension (tiles of the router and the backward are 128 wide)
 constexpr int kTcMaxTopk = 16;     // SSC selections per token handled by the tensor-core paths
 constexpr int kCT = 128;           // tokens per chunk / tile
 constexpr uint32_t kTile = 32768;  // one 128 x 128 bf16 operand tile

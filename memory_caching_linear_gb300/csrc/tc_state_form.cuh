@@ -4,6 +4,39 @@
 // units that launch them (k_tc.cu for D = 128, k_tc64.cu for D = 64); each has its own
 // copy of the kernels and of the abort flag.
 //
+// seg_state_tc -- persistent; each CTA walks its segments in chunks of 128 tokens
+//   with the running state S = sum v_j k_j^T (fp32, one row per worker thread):
+//     S += V_c^T K_c                        (update rule, [MC-ja §3 eq. 4b])
+//   Before each chunk's update it writes S (the state before the chunk) as a bf16
+//   operand image (the "prefix state" of the chunk); at the end S is the
+//   segment's cached state M^(n) ([MC-ja §3, after eq. 4b]), written as fp32
+//   (the states output) and as a bf16 image.  It also forms the key mean
+//   kbar_n ([MC-ja §3.1 eq. 10], pooled keys) as hi + mid + lo bf16 rows of a
+//   per-head operand image (the three terms sum to the fp32 mean exactly), and
+//   the online gate score
+//     r_on[t] = <u_t, sum_{j=t0..t} k_j> / (t - t0 + 1)
+//   from R = U_c K_c^T (tensor core) masked to j <= t plus <u_t, keys before the chunk>.
+//
+// readout_tc -- persistent, two CTAs per SM; a tile is (bh, segment n, chunk c)
+//   of 128 tokens, heaviest tiles first.  For the tile's tokens it computes
+//     y_t = g_{t,n} [ S_pre(c) q_t + sum_{j in chunk, j<=t} v_j (k_j . q_t) ]
+//         + sum_{i<n} g_{t,i} M^(i) q_t                      ([MC-ja §3.1 eq. 9])
+//   (Residual: g = 1, [MC-ja §3.1 eq. 7], where the cached sum collapses to one
+//   prefix state; Mean: the same with g = 1 / (n + 1)) as MMAs into one fp32 accumulator D per CTA:
+//     G = Q K_c^T;  D = (g_n * mask(G)) V_c;  D += (g_i o Q) X_i^T
+//   for X_i in {S_pre(c) (weight g_n), M^(0..n-1)}.  The gates come from the
+//   scores <u_t, kbar_i> (three MMA sets per tile, kbar as hi, mid and lo rows:
+//   every product is exact and only the fp32 accumulation rounds) and r_on[t]:
+//   g = softmax over {scores_i}_{i<n} and r_on[t] (GRM; Soup is the same sum for
+//   a linear memory, [MC-sum §3.3]); SSC keeps the topk largest cached scores
+//   ([MC-sum §3.4]) and gives the others gate 0.  With more than 64 segments (GG) the
+//   gates come from HBM instead, written by the general path's gate kernel.
+//
+// Over given segment boundaries (VAR) the state kernel's units are pieces of whole-chunk
+// segments from a host table (a first launch in `totals` mode forms the pieces' own states,
+// the second starts each piece from their sums) and the readout's tiles come from a
+// (segment, chunk) table.
+//
 // Pages cited:
 //   [MC-ja]  "メモリキャッシング：メモリ容量が増大する RNN" (news.neo-ai.one/ja/article/2519)
 //   [MC-sum] "给 RNN 装上“会增长的记忆”：解读 Google 的 Memory Caching"
@@ -44,7 +77,7 @@ struct TcArgs {
     int mean;             // Mean aggregation: the Residual path with every weight 1 / (n + 1)
     const float *alpha, *beta, *lam;  // SWLA per-token scalars [BH][L] (SWLA kernels only)
     int BH, L, C, N, CPS;
-    int d;                // head dimension of q, k, v, u, y and the states (64 or 128; tiles are 128 wide)
+    int d;                // head dimension of q, k, v, u, y and the states (64 or 128: the tiles' width D)
     int NB;               // blocks of 64 segments in a head's key-mean image (1 when N <= 64)
     int num_tiles;
     // Given segment boundaries (the VAR kernels): segments 0 .. Nseg-1 of every head start at
