@@ -39,7 +39,7 @@ constexpr uint32_t kGTile = 32768;   // one 128 x 128 bf16 operand tile (two 16 
 // g o dy for the second segment, and both segments' gates.
 constexpr int kG2 = 64;                    // tokens per G tile
 constexpr uint32_t kG2Tile = 16384;        // one 64 x 128 bf16 operand tile (two 8 KB panels)
-constexpr int kGStages = 4;
+constexpr int kGStages = 2;   // per CTA; two CTAs share an SM
 constexpr int kGThreads = 192;             // warp 0 TMA, warp 1 MMA issuer, warps 2-5 scale and drain
 constexpr uint32_t kGStage = 3 * kG2Tile + 1024;
 constexpr size_t kGSmem = kGStages * kGStage + 1024;
@@ -59,7 +59,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 // segment i0 is loaded once and feeds both accumulators (the tiles of segment i1
 // only the first).  Every CTA walks its tiles from the sequence's end backwards, so
 // the pairs of a head that run at the same time read the same tiles (from L2).
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(kGThreads, 2)
     bwd_G_tc(const __grid_constant__ CUtensorMap mY, const __grid_constant__ CUtensorMap mQ, GArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
