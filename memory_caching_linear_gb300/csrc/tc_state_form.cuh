@@ -80,6 +80,7 @@ struct TcArgs {
     int d;                // head dimension of q, k, v, u, y and the states (64 or 128: the tiles' width D)
     int NB;               // blocks of 64 segments in a head's key-mean image (1 when N <= 64)
     int num_tiles;
+    int hg;               // readout: heads per group (tiles go group by group, the heaviest first within one)
     // Given segment boundaries (the VAR kernels): segments 0 .. Nseg-1 of every head start at
     // sg_off[n] (a multiple of 128) and are whole 128-token chunks; sg_cbase[n] is the segment's
     // first chunk among the head's NC chunks (prefix-state images [BH][NC]); the readout's tiles
@@ -702,11 +703,18 @@ __device__ __forceinline__ TileInfo decode_tile(const TcArgs &a, int id)
 {
     TileInfo t;
     if (!VAR) {
-        const int per_seg = a.BH * a.CPS;
-        t.n = a.N - 1 - id / per_seg;
-        const int rem = id % per_seg;
-        t.c = rem / a.BH;
-        t.bh = rem % a.BH;
+        // groups of hg heads (the last one smaller), so that the cached images the tiles in flight
+        // read stay within the L2; inside a group the segments with the most cached states first
+        const int per_group = a.hg * a.N * a.CPS;
+        const int grp = id / per_group;
+        const int first = grp * a.hg;
+        const int heads = min(a.hg, a.BH - first);
+        const int rem0 = id - grp * per_group;
+        const int per_seg = heads * a.CPS;
+        t.n = a.N - 1 - rem0 / per_seg;
+        const int rem = rem0 % per_seg;
+        t.c = rem / heads;
+        t.bh = first + rem % heads;
         t.off = t.n * a.C;
         t.cbase = t.n * a.CPS;
     } else {
@@ -1324,6 +1332,17 @@ cudaError_t forward_impl(const Problem &p, const FwdArgs &fa, void *scratch, cud
     a.CPS = (int)CPS;
     a.d = p.d; a.NB = (p.N + 63) / 64;
     a.num_tiles = (int)(BH * N * CPS);
+    // heads per readout group: when every head's state images (read by every later tile of their head;
+    // the prefix images are read once) exceed 48 MB, groups whose images take about 32 MB of the L2,
+    // as equal as possible
+    {
+        const size_t per_head = N * im;
+        int hg = (int)((size_t)32 * 1024 * 1024 / (per_head > 0 ? per_head : 1));
+        hg = hg < 8 ? 8 : hg > p.BH ? p.BH : hg;
+        if (BH * per_head <= (size_t)48 * 1024 * 1024) hg = p.BH;
+        const int groups = (p.BH + hg - 1) / hg;
+        a.hg = (p.BH + groups - 1) / groups;
+    }
     FwdMaps m;
     if (!make_fwd_maps(p, fa, &m)) return cudaErrorInvalidValue;
     const int sms = sm_count();
