@@ -197,15 +197,18 @@ constexpr uint32_t kT1DecBytes = 2 * 132 * 4 + 128 * 4;
 template <bool DECAY, int D = 128>
 __host__ __device__ constexpr uint32_t t1_stage_bytes() { return t1_dec_off<D>() + (DECAY ? 2048u : 0u); }  // tiles stay 1024-aligned
 static_assert(kT1DecBytes <= 2048, "the SWLA scalars fit the stage's tail");
-// D = 64 adds a 16 KB zero panel: the upper 64 rows of the M = 128 operand V^T.
+// D = 128: two stages, one CTA per SM.  D = 64: one stage and a 16 KB zero panel (the upper 64 rows of
+// the M = 128 operand V^T), two CTAs per SM.
+template <int D>
+__host__ __device__ constexpr int t1_stages() { return D == 64 ? 1 : 2; }
 template <bool DECAY, int D = 128>
 __host__ __device__ constexpr size_t t1_smem_bytes()
 {
-    return 2 * t1_stage_bytes<DECAY, D>() + 4 * kT1Stage2 + (D == 64 ? kPanel : 0) + 1024;
+    return t1_stages<D>() * t1_stage_bytes<DECAY, D>() + 4 * kT1Stage2 + (D == 64 ? kPanel : 0) + 1024;
 }
 
 template <bool GATED, bool DECAY, bool VAR = false, int D = 128>
-__global__ void __launch_bounds__(kT1Threads, 1)
+__global__ void __launch_bounds__(kT1Threads, D == 64 ? 2 : 1)
     seg_state_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                  const __grid_constant__ CUtensorMap mU, TcArgs a)
 {
@@ -214,6 +217,9 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     constexpr uint32_t kOp = NP * kPanel;   // one chunk's K, V or U tile
     constexpr uint32_t kImg = D * D * 2;    // a D x D bf16 operand image
     constexpr uint32_t kStage = t1_stage_bytes<DECAY, D>();
+    constexpr int NS = t1_stages<D>();       // operand stages
+    constexpr int NR = D == 64 ? 1 : 2;      // U K^T buffers in tensor memory
+    constexpr uint32_t kCols = D == 64 ? 256 : 512;  // R x NR | Z x 2 (D columns each, 128 apart at D = 128)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     __shared__ uint64_t full[2], empty[2], r_full[2], r_empty[2], z_full[2], z_empty[2];
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     };
 
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 512);
+        tmem_alloc(&tmem_base, kCols);
         tmem_relinquish();
     }
     if (threadIdx.x == 32) {
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         mbar_init(&v_scaled, 128);
         fence_mbar_init();
     }
-    uint8_t *const zero_panel = sm + 2 * kStage + 4 * kT1Stage2;  // D = 64 only
+    uint8_t *const zero_panel = sm + NS * kStage + 4 * kT1Stage2;  // D = 64 only
     if (D == 64) {
         for (int i = threadIdx.x; i < (int)(kPanel / 16); i += kT1Threads)
             reinterpret_cast<uint4 *>(zero_panel)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -280,8 +286,9 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    // tensor memory: R (U K^T) x 2 | Z (chunk state V^T K) x 2, 128 columns each
-    const uint32_t tR0 = tb, tZ0 = tb + 256;
+    // tensor memory: R (U K^T) x NR, 128 columns each | Z (chunk state V^T K) x 2
+    const uint32_t tR0 = tb, tZ0 = tb + 128 * NR;
+    constexpr uint32_t kZStride = D == 64 ? 64 : 128;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -292,8 +299,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             for (int gch = 0; gch < my_chunks; ++gch, advance(cu)) {
                 const int c = cu.c, nch = cu.u.nch;
                 const int rr = cu.u.bh * a.L + cu.u.off + c * kCT;
-                const int s = gch & 1;
-                const uint32_t r = gch >> 1;
+                const int s = gch % NS;
+                const uint32_t r = gch / NS;
                 if (!mbar_wait(&empty[s], (r & 1) ^ 1, &abort_flag)) break;
                 uint8_t *st = sm + s * kStage;
                 // SWLA: alpha and beta reach one token into the next chunk when it is in the same segment
@@ -323,16 +330,16 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             uint32_t rc = 0;  // chunks with online scores (not in a head's first segment)
             Cursor cu = start();
             for (int gch = 0; gch < my_chunks; ++gch, advance(cu)) {
-                const int s = gch & 1, b = gch & 1;
-                const uint32_t r = gch >> 1;
+                const int s = gch % NS, b = gch & 1;
+                const uint32_t r = gch / NS, rz = gch >> 1;
                 if (!mbar_wait(&full[s], r & 1, &abort_flag)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sm + s * kStage), vb = kb + kOp, ub = kb + 2 * kOp;
                 // V^T is M = 128 rows: the two 64-row halves of V (D = 128), or V and the zero panel
                 const uint32_t v_lbo = D == 128 ? kPanel : smem_u32(zero_panel) - vb;
                 if (GATED && cu.u.seg != 0 && !totals) {  // R = U K^T (online gate score of the chunk's tokens)
-                    const int rb = rc & 1;
-                    if (!mbar_wait(&r_empty[rb], ((rc >> 1) & 1) ^ 1, &abort_flag)) break;
+                    const int rb = rc % NR;
+                    if (!mbar_wait(&r_empty[rb], ((rc / NR) & 1) ^ 1, &abort_flag)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4 * NP; ++kk)
@@ -342,12 +349,12 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     ++rc;
                 }
                 // Z = V^T K, the chunk's own state (fresh accumulator); SWLA: V^T diag(w) K
-                if (!mbar_wait(&z_empty[b], (r & 1) ^ 1, &abort_flag)) break;
+                if (!mbar_wait(&z_empty[b], (rz & 1) ^ 1, &abort_flag)) break;
                 if (DECAY && !mbar_wait(&v_scaled, gch & 1, &abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tZ0 + b * 128, make_desc_sw128(vb + kk * 2048u, v_lbo, 1024),
+                    mma_ss(tZ0 + b * kZStride, make_desc_sw128(vb + kk * 2048u, v_lbo, 1024),
                            make_desc_sw128(kb + kk * 2048u, 16384, 1024), idS, kk > 0);
                 mma_commit(&z_full[b]);
                 mma_commit(&empty[s]);
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
         const uint32_t row = 32 * q4 + lane;  // TMEM lane = token row (R) = value row (Z, S) = key column (sums)
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         float S[D];  // running state row: S[row][k] = sum_{j before the chunk} v_j[row] k_j[k]
-        uint8_t *wst = sm + 2 * kStage + q4 * kT1Stage2;  // this warp's staging area for global stores
+        uint8_t *wst = sm + NS * kStage + q4 * kT1Stage2;  // this warp's staging area for global stores
         float ks = 0.f;  // running sum of key column `row` over the segment, in token order
         // A worker that gives up (bounded wait ran out) keeps walking the loop
         // without work so that every warp reaches the same named barriers.
@@ -369,8 +376,8 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             const int c = cu.c, nch = cu.u.nch;
             const int bh = cu.u.bh, seg = cu.u.seg;
             const int row0 = bh * a.L + cu.u.off;
-            const int s = gch & 1, b = gch & 1;
-            const uint32_t r = gch >> 1;
+            const int s = gch % NS, b = gch & 1;
+            const uint32_t r = gch / NS, rz = gch >> 1;
             if (c == 0) {  // a new unit: memory restarts at zero, or at the sum of the earlier pieces' totals
 #pragma unroll
                 for (int k = 0; k < D; ++k) S[k] = 0.f;
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             }
             if (GATED && seg == 0 && ok && !totals) a.r_on[(size_t)row0 + c * kCT + row] = 0.f;  // single gate: the score is unused
             if (GATED && seg != 0 && ok && !totals) {
-                const int rb = rc & 1;
+                const int rb = rc % NR;
                 float d4[4] = {0.f, 0.f, 0.f, 0.f};  // <u_t, keys of the segment before this chunk>
 #pragma unroll
                 for (int cc = 0; cc < D / 8; ++cc) {
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
                     dd = fmaf(u67.x, k1.z, dd); dd = fmaf(u67.y, k1.w, dd);
                 }
                 const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-                ok = mbar_wait(&r_full[rb], (rc >> 1) & 1, &abort_flag);
+                ok = mbar_wait(&r_full[rb], (rc / NR) & 1, &abort_flag);
                 if (ok) {
                     tc_fence_after();
                     float w4[4] = {0.f, 0.f, 0.f, 0.f};  // sum_{j <= t} <u_t, k_j> within the chunk
@@ -513,13 +520,13 @@ __global__ void __launch_bounds__(kT1Threads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             // S += Z_c; then S is the prefix state of chunk c + 1
-            if (ok) ok = mbar_wait(&z_full[b], r & 1, &abort_flag);
+            if (ok) ok = mbar_wait(&z_full[b], rz & 1, &abort_flag);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int j16 = 0; j16 < D / 16; ++j16) {
                     uint32_t v[16];
-                    tmem_ld16(tZ0 + b * 128 + lane_base + 16 * j16, v);
+                    tmem_ld16(tZ0 + b * kZStride + lane_base + 16 * j16, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) S[16 * j16 + i] = fmaf(zdecay, S[16 * j16 + i], __uint_as_float(v[i]));
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(kT1Threads, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tb, 512);
+        tmem_dealloc(tb, kCols);
     }
     if (threadIdx.x == 0 && abort_flag) atomicExch(&g_tc_abort, 1);
 }
@@ -1363,8 +1370,8 @@ cudaError_t forward_impl(const Problem &p, const FwdArgs &fa, void *scratch, cud
         const size_t smem1 = decay ? t1_smem_bytes<true, D>() : t1_smem_bytes<false, D>();
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
         if (e != cudaSuccess) return e;
-        const int nseg = (int)(BH * N);
-        k1<<<nseg < sms ? nseg : sms, kT1Threads, smem1, s>>>(m.k, m.v, m.u, a);
+        const int nseg = (int)(BH * N), slots1 = (D == 64 ? 2 : 1) * sms;  // D = 64: two CTAs per SM
+        k1<<<nseg < slots1 ? nseg : slots1, kT1Threads, smem1, s>>>(m.k, m.v, m.u, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         profile_after_kernel(s, "seg_state_tc");
     }
@@ -1462,7 +1469,7 @@ cudaError_t state_segments_impl(const Problem &p, const FwdArgs &fa, const TcSeg
     auto k1 = gated ? seg_state_tc<true, false, true, D> : seg_state_tc<false, false, true, D>;
     const size_t smem1 = t1_smem_bytes<false, D>();
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
-    const int sms = sm_count();
+    const int sms = (D == 64 ? 2 : 1) * sm_count();  // state CTAs at once (D = 64: two per SM)
     if (tb.n1 > 0) {  // the pieces' own states first: every later piece starts from their sums
         TcArgs a1 = a;
         a1.units = tb.units1;
