@@ -192,6 +192,26 @@ L2_BYTES = 129 * 10**6
 FLUSH_BYTES = 256 * 2**20  # written between timed steps when the inputs would stay in L2
 
 
+def l2_note(inputs_bytes):
+    """How the timed steps treat the L2 for inputs of this size (see timed_steps)."""
+    gib = inputs_bytes / 2**30
+    if inputs_bytes > 2 * L2_BYTES:
+        return f"inputs {gib:.2f} GiB > L2 129 MB, not flushed"
+    return f"inputs {gib:.3f} GiB fit in L2: 256 MiB written before every timed step (not timed)"
+
+
+def forward_inputs_bytes(w):
+    """Bytes of q, k, v, u of a forward workload."""
+    return 4 * w.B * w.H * w.L * w.d * (2 if w.dtype == "bf16" else 4)
+
+
+def forward_config(w, world, note):
+    """The `config` object of a forward workload's JSON line (both arms)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
+            "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype, "l2": note,
+            "parallelism": f"replicas x{world} (independent (batch, head) problems)"}
+
+
 def timed_steps(step, steps, inputs_bytes):
     """Run `steps` calls of step() and return (ms, l2 note).  Inputs larger than twice the
     L2 run back to back between two events on the current stream; smaller ones get a
@@ -199,7 +219,6 @@ def timed_steps(step, steps, inputs_bytes):
     and events around each call, whose times are summed."""
     import torch
     stream = torch.cuda.current_stream()
-    gib = inputs_bytes / 2**30
     if inputs_bytes > 2 * L2_BYTES:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -208,7 +227,7 @@ def timed_steps(step, steps, inputs_bytes):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
-        return ev0.elapsed_time(ev1), f"inputs {gib:.2f} GiB > L2 129 MB, not flushed"
+        return ev0.elapsed_time(ev1), l2_note(inputs_bytes)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
@@ -218,8 +237,7 @@ def timed_steps(step, steps, inputs_bytes):
         step()
         b.record(stream)
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in evs), \
-        f"inputs {gib:.3f} GiB fit in L2: 256 MiB written before every timed step (not timed)"
+    return sum(a.elapsed_time(b) for a, b in evs), l2_note(inputs_bytes)
 
 
 def measured_peaks():
@@ -396,8 +414,8 @@ def run_ours(args, w, wname="long-grm"):
 
     if world > 1:
         dist.barrier()
-    in_bytes = 4 * w.B * w.H * w.L * w.d * (2 if w.dtype == "bf16" else 4)
-    ms, l2_note = timed_steps(step, args.steps, in_bytes)
+    in_bytes = forward_inputs_bytes(w)
+    ms, note = timed_steps(step, args.steps, in_bytes)
     if world > 1:
         dist.barrier()
     # Per-kernel times come from a second pass of the same K steps with events
@@ -461,10 +479,7 @@ def run_ours(args, w, wname="long-grm"):
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_path,
         "data": "synthetic (seeded numpy normals: q,k unit rows, v ~ N(0,1), u ~ N(0,1)/sqrt(d)"
                 + ("; SWLA alpha = 1 - 0.1 sigmoid(z), beta, lambda = sigmoid(z))" if w.swla else ")"),
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
-                   "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype,
-                   "l2": l2_note,
-                   "parallelism": f"replicas x{world} (independent (batch, head) problems)"},
+        "config": forward_config(w, world, note),
         "tc_fraction_of_bf16_peak": round(flops["total"] / step_s / 1e12 / peaks["bf16_tflops"], 4),
         "algorithmic_tflop_per_step": round(flops["total"] / 1e12, 4),
         "hbm_fraction": round(algorithmic_bytes(w) / step_s / 1e9 / peaks["hbm_gbs"], 4),
@@ -615,7 +630,7 @@ def run_backward(args, w, wname):
     for _ in range(nwarm):
         step()
     torch.cuda.synchronize()
-    tot_ms, l2_note = timed_steps(step, args.steps, 5 * q.numel() * q.element_size())
+    tot_ms, note = timed_steps(step, args.steps, 5 * q.numel() * q.element_size())
     prof = mcl.KernelProfile(capacity=args.steps * 8 + 8)
     with prof:
         for _ in range(args.steps):
@@ -647,7 +662,7 @@ def run_backward(args, w, wname):
         "data": "synthetic (the forward workload's seeded inputs; dy ~ N(0, 1))",
         "config": {"workload": f"bwd-{wname} {w.name}", "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len,
                    "N": w.N, "agg": mc_inputs.MODE_NAMES[w.mode], "input_dtype": w.dtype,
-                   "l2": l2_note},
+                   "l2": note},
         "algorithmic_tflop_per_step": round(flops["total"] / 1e12, 4),
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "kernel": dom, "launch_ms": dom_ms,
@@ -774,8 +789,7 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same generator as the GPU arm)",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "seg_len": w.seg_len, "N": w.N,
-                       "agg": mc_inputs.MODE_NAMES[w.mode], "topk": w.topk, "input_dtype": w.dtype},
+            "config": forward_config(w, world, l2_note(forward_inputs_bytes(w))),
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
