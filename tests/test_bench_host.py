@@ -120,3 +120,23 @@ def test_workload_bounds_and_kernel_bytes():
         w.B * w.H * w.N * w.d * w.d * 2
     assert bench.metric_name(w) == bench.METRIC
     assert "SSC" in bench.metric_name(mc_inputs.SSC_D128)
+
+
+def test_reference_arm_reports_the_gpu_arms_config(monkeypatch):
+    """Both arms print one config object for a workload: the same keys and values, including
+    how the timed steps treat the L2 and the replica layout."""
+    w = mc_inputs.TINY
+    monkeypatch.setattr(bench, "oracle_sample", lambda w, budget_s: (1.0, 1, "stub sample", None))
+    monkeypatch.setattr(bench, "dist_env", lambda: (1, 0, 0))
+
+    class Args:
+        steps, warmup = 1, 0
+
+    line = bench.run_reference(Args, w)
+    note = bench.l2_note(bench.forward_inputs_bytes(w))
+    assert line["config"] == bench.forward_config(w, 1, note)
+    assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert "fit in L2" in note
+    assert "not flushed" in bench.l2_note(bench.forward_inputs_bytes(mc_inputs.LONG_GRM))
+    assert set(line["config"]) >= {"workload", "B", "H", "L", "d", "seg_len", "N", "agg", "topk", "input_dtype",
+                                   "l2", "parallelism"}
