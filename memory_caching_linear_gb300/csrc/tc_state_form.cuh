@@ -239,6 +239,29 @@ __global__ void __launch_bounds__(kT1Threads, D == 64 ? 2 : 1)
     int my_chunks = 0;
     for (int k = 0; k < my_segs; ++k) my_chunks += seg_info<VAR>(a, (int)blockIdx.x + k * (int)gridDim.x).nch;
     const int NCH = VAR ? a.NC : a.N * a.CPS;  // prefix-state images per head
+    if (GATED && !totals) {
+        // The key-mean image's rows past the last segment (segments N .. 64 NB - 1, which no unit writes)
+        // are zero when the readout's score MMAs read them: every thread clears a strided share of them.
+        const int nrow = VAR ? a.Nseg : a.N;
+        const int tail = a.NB * 64 - nrow;
+        if (tail > 0) {
+            const long long per_head = 3LL * NP * tail * 8;  // terms x panels x rows x 16-byte chunks
+            const long long total = per_head * a.BH;
+            for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+                 i += (long long)gridDim.x * blockDim.x) {
+                const int bh = (int)(i / per_head);
+                long long r = i % per_head;
+                const int ch = (int)(r & 7);
+                r >>= 3;
+                const int row = nrow + (int)(r % tail);
+                r /= tail;
+                const int panel = (int)(r % NP), term = (int)(r / NP);
+                uint8_t *p = a.kbar_img + ((size_t)bh * a.NB + (row >> 6)) * kKbImg + (size_t)term * kKbPanel +
+                             panel * (64 * 128) + (row & 63) * 128 + ch * 16;
+                *reinterpret_cast<uint4 *>(p) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
     // each role walks the chunk stream with a cursor: the unit, and the chunk within it
     struct Cursor {
         int k, c;
@@ -1354,10 +1377,6 @@ cudaError_t forward_impl(const Problem &p, const FwdArgs &fa, void *scratch, cud
     if (!make_fwd_maps(p, fa, &m)) return cudaErrorInvalidValue;
     const int sms = sm_count();
     cudaError_t e;
-    if (gated) {
-        e = cudaMemsetAsync(a.kbar_img, 0, BH * ((N + 63) / 64) * kKbImg, s);
-        if (e != cudaSuccess) return e;
-    }
 
     profile_call_start(s);
     const bool decay = fa.alpha != nullptr;
@@ -1465,7 +1484,6 @@ cudaError_t state_segments_impl(const Problem &p, const FwdArgs &fa, const TcSeg
     FwdMaps m;
     if (!make_fwd_maps(p, fa, &m)) return cudaErrorInvalidValue;
     cudaError_t e;
-    if (gated && (e = cudaMemsetAsync(a.kbar_img, 0, (size_t)p.BH * kKbImg, s)) != cudaSuccess) return e;
     auto k1 = gated ? seg_state_tc<true, false, true, D> : seg_state_tc<false, false, true, D>;
     const size_t smem1 = t1_smem_bytes<false, D>();
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) != cudaSuccess) return e;
